@@ -1,0 +1,464 @@
+"""Benchmark: allreduce of P logical rank buffers on one GB300.
+
+Default workload (one step = one fused allreduce through the C ABI):
+  P = 4 ranks, bf16 sum, 32 Mi elements (64 MiB) per rank, out of place,
+  values N(0, 1) from seed 1. Footprint 512 MiB > 129 MB of L2, so timed
+  iterations stream from HBM without an explicit L2 flush.
+
+Reported (one JSON line on rank 0):
+  value      algbw = P * count * bytes / time (GB/s), device-resident inputs
+  roofline   HBM bound: algorithmic bytes 2 * P * S per launch (read every
+             rank's shard once, write every rank's result once) / mean
+             launch time from CUDA events on the launching stream, against
+             the measured copy bandwidth
+  e2e        same metric through the C ABI with the inputs copied from pinned
+             host memory and every result copied back, inside the timed region
+  cpu_baseline  the CPU oracle (threaded, same per-element order) on the
+             host cores, on the same workload
+
+`--impl reference` times the CPU oracle as the reference arm. Under torchrun
+(N > 1) every rank runs an independent replica on its own GPU (the path has
+no data exchange between GPUs); value = all ranks' bytes / slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+from datetime import datetime
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "allreduce algbw GB/s & HBM-peak fraction vs P, msg size, CTA cap (1 GB300)"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "c1": dict(name="C1: P=2 fp32 sum allreduce, out of place, 1,048,576 elems (4 MiB)/rank, "
+                    "uniform[-1,1) seed 0", p=2, count=1_048_576, dtype="f32", op="sum",
+               kind="uniform_f32", seed=0, kw={}, in_place=False, cap=0),
+    "c2": dict(name="C2: P=4 bf16 sum allreduce, out of place, 32 Mi elems (64 MiB)/rank, "
+                    "N(0,1) seed 1", p=4, count=32 * 1024 * 1024, dtype="bf16", op="sum",
+               kind="normal_bf16", seed=1, kw=dict(mu=0.0, sigma=1.0), in_place=False, cap=0),
+    "c4": dict(name="C4: P=8 bf16 sum allreduce, 64 Mi elems (128 MiB)/rank, N(0,0.02) seed 3",
+               p=8, count=64 * 1024 * 1024, dtype="bf16", op="sum", kind="normal_bf16", seed=3,
+               kw=dict(mu=0.0, sigma=0.02), in_place=False, cap=0),
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    try:
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 copy measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = ROOT / "collective_communication_planner_gb300" / "csrc"
+    for f in sorted(list(csrc.glob("*.cu")) + list(csrc.glob("*.cuh")) + [csrc / "internal.h"]):
+        h.update(f.name.encode())
+        h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_key: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    p = ROOT / "profiles" / "dram_traffic.json"
+    try:
+        d = json.loads(p.read_text())
+    except Exception:
+        return None
+    e = d.get(workload_key)
+    if not e or e.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return int(e["dram_bytes_read"]) + int(e["dram_bytes_write"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.t:
+                self.t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for ts, ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                stamp = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except Exception:
+                stamp = ts
+            rows.append((stamp, parts))
+        sel = [r for s, r in rows if t0 - 0.15 <= s <= t1 + 0.15]
+        window = "soak + timed region"
+        if not sel:
+            sel = [r for _, r in rows]
+            window = "whole run (no sample fell inside the timed region)"
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except Exception:
+                return None
+
+        sm = sorted(v for v in (num(r[2]) for r in sel) if v is not None)
+        mx = [v for v in (num(r[3]) for r in sel) if v is not None]
+        pw = [v for v in (num(r[4]) for r in sel) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in sel for i in range(4)
+                          if r[6 + i].lower() in ("active", "0x1", "1")})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(sel), "window": window}
+
+
+# ------------------------------------------------------------------ workload data
+def make_inputs(w):
+    import datagen
+    return datagen.rank_buffers(w["kind"], w["seed"], w["p"], w["count"], **w["kw"])
+
+
+def host_to_torch(x):
+    import numpy as np
+    import torch
+    if x.dtype == np.uint16:
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(x)
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def time_oracle(w, xs, min_seconds: float, max_reps: int = 1000, elems: int | None = None):
+    """Times the threaded oracle allreduce over the first `elems` elements of
+    each rank; returns (seconds per call, threads used, reps)."""
+    import numpy as np
+    import oracle
+    n = elems or w["count"]
+    sub = [x[:n] for x in xs]
+    out = np.empty(n, dtype=xs[0].dtype)
+    recvs = [out] * len(sub)
+    nthreads = os.cpu_count() or 1
+    oracle.allreduce(sub, w["dtype"], w["op"], recvs=recvs, nthreads=nthreads)  # warm
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.allreduce(sub, w["dtype"], w["op"], recvs=recvs, nthreads=nthreads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return el / reps, min(nthreads, n // 4096 + 1), reps
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, w, rank, world, dist):
+    import numpy as np
+    import torch
+    import collective_communication_planner_gb300 as tccl
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    p, n, es = w["p"], w["count"], (2 if w["dtype"] == "bf16" else 4)
+    S = n * es
+    alg_bytes = p * S                      # algbw numerator
+    hbm_bytes = 2 * p * S                  # read P shards, write P results
+    xs = make_inputs(w)
+    host = [host_to_torch(x) for x in xs]
+    sends = [h.to(dev) for h in host]
+    recvs = sends if w["in_place"] else [torch.empty_like(s) for s in sends]
+    stream = torch.cuda.Stream(device=dev)
+    st = stream.cuda_stream
+    g = tccl.Group(p)
+    dt = tccl.DTYPES[w["dtype"]]
+    op = tccl.OPS[w["op"]]
+    cap = args.cap if args.cap is not None else w["cap"]
+
+    def step():
+        r = tccl.tcclAllReduce(g.handle, sends, recvs, n, dt, op, st, cap)
+        if r != tccl.tcclSuccess:
+            raise tccl.TcclError(r, "tcclAllReduce")
+
+    # parity spot check of this exact launch configuration before timing
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    import oracle
+    k = min(n, 1 << 16)
+    idx = np.random.default_rng(0).choice(n, size=k, replace=False)
+    idx.sort()
+    exp = oracle.allreduce([x[idx].copy() for x in xs], w["dtype"], w["op"])[0]
+    got = recvs[p - 1].view(torch.int16 if w["dtype"] == "bf16" else recvs[0].dtype)
+    got = got.cpu().numpy()[idx].view(exp.dtype)
+    if not np.array_equal(got.view(np.uint8), exp.view(np.uint8)):
+        raise SystemExit("bench: result differs from the oracle on sampled elements")
+    info = g.last_launch()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            step()
+    # soak: keep the GPU under this load for ~1 s so clocks settle and the
+    # sampler sees the loaded state
+    t_soak = time.time()
+    stream.synchronize()
+    while time.time() - t_soak < args.soak:
+        for _ in range(50):
+            step()
+        stream.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    t_start = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            ev[2 * i].record(stream)
+            step()
+            ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    if dist is not None:
+        dist.barrier()
+    sampler.stop()
+    total_ms = ev[0].elapsed_time(ev[-1])
+    launch_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)) / args.steps
+    clocks = sampler.summary(t_soak, t_end)
+
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * alg_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    achieved = hbm_bytes / (launch_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+
+    # reduce-scatter then all-gather on the same workload (two launches)
+    rc = n // p
+    parts = [torch.empty(rc, dtype=sends[0].dtype, device=dev) for _ in range(p)]
+    outs = [torch.empty(n, dtype=sends[0].dtype, device=dev) for _ in range(p)]
+    rs_steps = max(10, min(args.steps, 200))
+
+    def rs_ag():
+        r1 = tccl.tcclReduceScatter(g.handle, sends, parts, rc, dt, op, st, cap)
+        r2 = tccl.tcclAllGather(g.handle, parts, outs, rc, dt, st, cap)
+        if r1 or r2:
+            raise tccl.TcclError(r1 or r2, "reduce-scatter / all-gather")
+
+    for _ in range(3):
+        rs_ag()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(rs_steps):
+        rs_ag()
+    e1.record(stream)
+    e1.synchronize()
+    rs_ms = e0.elapsed_time(e1) / rs_steps
+
+    # end to end through the C ABI: pinned host inputs in, every result out
+    h_in = [h.pin_memory() for h in host]
+    h_out = [torch.empty_like(h).pin_memory() for h in host]
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for d, h in zip(sends, h_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            for h, d in zip(h_out, recvs):
+                h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    stream.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    out = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            sec, cores, reps = time_oracle(w, xs, args.cpu_seconds)
+            cpu = {"value": alg_bytes / sec / 1e9, "unit": "GB/s", "cores": cores,
+                   "kind": "oracle",
+                   "sample": f"whole workload ({p} x {n} elements), {reps} repetitions, "
+                             f"threaded oracle (same per-element order as the plain one)"}
+        out = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if w["dtype"] != "i32" else "int32",
+            "data": "synthetic (seeded SplitMix64 streams per rank)",
+            "config": {"workload": w["name"], "P": p, "count": n, "bytes_per_rank": S,
+                       "elem_dtype": w["dtype"], "op": w["op"], "in_place": w["in_place"],
+                       "cta_cap": cap, "engine": info["engine"], "ctas": info["ctas"],
+                       "stages": info["stages"], "chunk_bytes": info["chunk_bytes"],
+                       "l2": f"inputs larger than L2 ({2 * p * S >> 20} MiB footprint), no flush",
+                       "parallelism": f"replicas{world}" if world > 1 else "single"},
+            "hbm_fraction": round(achieved / peak, 4),
+            "busbw": round(S / (ms_per_step * 1e-3) * 2 * (p - 1) / p / 1e9, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic, "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": hbm_bytes,
+                         "mean_launch_ms": round(launch_ms, 5)},
+            "rs_then_ag": {"ms_per_step": round(rs_ms, 5),
+                           "algbw": round(alg_bytes / (rs_ms * 1e-3) / 1e9, 2),
+                           "hbm_bytes_per_step": 2 * (p + 1) * S},
+            "e2e": {"value": round(world * alg_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": p * S, "d2h_bytes_per_step": p * S,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "cpu_baseline": cpu,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+        }
+    g.close()
+    return out
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, w):
+    """The CPU oracle as the reference arm: each step is the threaded oracle
+    on a bounded prefix of the same workload."""
+    xs = make_inputs(w)
+    p, n, es = w["p"], w["count"], (2 if w["dtype"] == "bf16" else 4)
+    full_sec, _, _ = time_oracle(w, xs, 0.0, max_reps=1)
+    budget = 60.0  # seconds for warm-up + timed steps
+    per_step = budget / max(1, args.steps + args.warmup)
+    elems = n
+    while elems > 4096 and full_sec * elems / n > per_step:
+        elems //= 2
+    import numpy as np
+    import oracle
+    sub = [x[:elems] for x in xs]
+    out = np.empty(elems, dtype=xs[0].dtype)
+    nthreads = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.allreduce(sub, w["dtype"], w["op"], recvs=[out] * p, nthreads=nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.allreduce(sub, w["dtype"], w["op"], recvs=[out] * p, nthreads=nthreads)
+    sec = (time.perf_counter() - t0) / args.steps
+    value = p * elems * es / sec / 1e9
+    cores = min(nthreads, elems // 4096 + 1)
+    sample = f"first {elems} of {n} elements per rank ({p} ranks) per step"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w["name"], "P": p, "count": n, "bytes_per_rank": n * es},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2")
+    ap.add_argument("--cap", type=int, default=None, help="CTA cap (default: the workload's)")
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load first")
+    ap.add_argument("--cpu-seconds", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("gloo")
+        dist = dist_mod
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+    out = run_ours(args, w, rank, world, dist)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

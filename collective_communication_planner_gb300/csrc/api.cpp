@@ -1,0 +1,548 @@
+// C ABI of the library (include/tccl.h): argument validation, the plan
+// cache, device tables and launches. Host code only; kernels live in the .cu
+// translation units.
+#include "tccl.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "plan.h"
+
+using namespace tccl;
+
+namespace {
+
+int log_level() {
+  static int lvl = [] {
+    const char* e = std::getenv("TCCL_LOG");
+    return e ? std::atoi(e) : 0;
+  }();
+  return lvl;
+}
+
+int elem_size_of(int dtype) { return dtype == kBF16 ? 2 : 4; }
+
+struct PlanKey {
+  int coll;
+  int elem_size;
+  uint64_t count;
+  int cap;
+  std::string mod16;  // address mod 16 of every send then recv buffer
+  bool operator<(const PlanKey& o) const {
+    if (coll != o.coll) return coll < o.coll;
+    if (elem_size != o.elem_size) return elem_size < o.elem_size;
+    if (count != o.count) return count < o.count;
+    if (cap != o.cap) return cap < o.cap;
+    return mod16 < o.mod16;
+  }
+};
+
+struct CachedPlan {
+  Lowered low;
+  // bulk engine: device copies of the window table and per-CTA offsets
+  Window* d_win = nullptr;
+  uint32_t* d_cta_first = nullptr;
+  // small engines: the launch argument block without its pointers
+  std::vector<unsigned char> small_args;
+  ~CachedPlan() {
+    if (d_win) cudaFree(d_win);
+    if (d_cta_first) cudaFree(d_cta_first);
+  }
+};
+
+template <int MAXR, int MAXW>
+void build_small_args(const Lowered& low, int nranks, int elem_size,
+                      std::vector<unsigned char>* out) {
+  out->assign(sizeof(SmallArgs<MAXR, MAXW>), 0);
+  auto* a = reinterpret_cast<SmallArgs<MAXR, MAXW>*>(out->data());
+  a->nwin = (int)low.win.size();
+  a->nranks = nranks;
+  a->elem_size = elem_size;
+  for (size_t i = 0; i < low.win.size(); ++i) a->win[i] = low.win[i];
+  for (size_t i = 0; i < low.vec_prefix.size(); ++i) {
+    a->vec_prefix[i] = low.vec_prefix[i];
+    a->elem_prefix[i] = low.elem_prefix[i];
+  }
+}
+
+template <int MAXR, int MAXW>
+void fill_small_ptrs(std::vector<unsigned char>* buf, int nranks, const void* const* send,
+                     void* const* recv, uint32_t* sm_mask) {
+  auto* a = reinterpret_cast<SmallArgs<MAXR, MAXW>*>(buf->data());
+  for (int r = 0; r < nranks; ++r) {
+    a->p.src[r] = send[r];
+    a->p.dst[r] = recv[r];
+  }
+  a->sm_mask = sm_mask;
+}
+
+bool ranges_overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb) {
+  if (na == 0 || nb == 0) return false;
+  return a < b + nb && b < a + na;
+}
+
+// Argument rules shared by the collectives and tcclPlanInspect.
+tcclResult_t validate(int coll, int nranks, const void* const* send, void* const* recv,
+                      size_t count, int dtype, int op) {
+  if (coll < kAllReduce || coll > kAllGather) return tcclInvalidArgument;
+  if (nranks < 1 || nranks > TCCL_MAX_RANKS) return tcclInvalidArgument;
+  if (dtype < kF32 || dtype > kI32) return tcclInvalidArgument;
+  if (coll != kAllGather && (op < kSum || op > kMax)) return tcclInvalidArgument;
+  if (!send || !recv) return tcclInvalidArgument;
+  if (count == 0) return tcclSuccess;
+  const int es = elem_size_of(dtype);
+  const uint64_t big = (uint64_t)nranks * (uint64_t)es;
+  if (count > (SIZE_MAX / 4) / big) return tcclInvalidArgument;
+  const size_t sbytes = (coll == kReduceScatter ? nranks * count : count) * es;
+  const size_t rbytes = (coll == kAllGather ? nranks * count : count) * es;
+  const size_t shard_bytes = count * es;
+  for (int r = 0; r < nranks; ++r) {
+    if (!send[r] || !recv[r]) return tcclInvalidArgument;
+    if (((uintptr_t)send[r] % es) || ((uintptr_t)recv[r] % es)) return tcclInvalidArgument;
+  }
+  for (int r = 0; r < nranks; ++r) {
+    const uintptr_t rr = (uintptr_t)recv[r];
+    const uintptr_t sr = (uintptr_t)send[r];
+    // the recv buffer against its own rank's send buffer: in place the NCCL
+    // way, or disjoint
+    bool in_place = false;
+    if (coll == kAllReduce) in_place = (rr == sr);
+    if (coll == kReduceScatter) in_place = (rr == sr + r * shard_bytes);
+    if (coll == kAllGather) in_place = (sr == rr + r * shard_bytes);
+    if (!in_place && ranges_overlap(rr, rbytes, sr, sbytes)) return tcclInvalidArgument;
+    for (int k = 0; k < nranks; ++k) {
+      if (k == r) continue;
+      if (ranges_overlap(rr, rbytes, (uintptr_t)recv[k], rbytes)) return tcclInvalidArgument;
+      if (ranges_overlap(rr, rbytes, (uintptr_t)send[k], sbytes)) return tcclInvalidArgument;
+    }
+  }
+  return tcclSuccess;
+}
+
+// Nothing to move: one rank, in place.
+bool is_noop(int coll, int nranks, const void* const* send, void* const* recv) {
+  if (nranks != 1) return false;
+  (void)coll;
+  return send[0] == recv[0];
+}
+
+Config config_from_env() {
+  Config c;
+  auto geti = [](const char* n, int d) {
+    const char* e = std::getenv(n);
+    return e ? std::atoi(e) : d;
+  };
+  if (const char* e = std::getenv("TCCL_ENGINE")) {
+    std::string v(e);
+    if (v == "bulk") c.engine = kEngineBulk;
+    else if (v == "warp") c.engine = kEngineWarp;
+    else if (v == "vec") c.engine = kEngineVec;
+  }
+  if (const char* e = std::getenv("TCCL_SMALL_MAX_BYTES")) c.small_max_bytes = std::strtoull(e, 0, 10);
+  c.stage_bytes = geti("TCCL_STAGE_BYTES", 0);
+  c.stages = geti("TCCL_STAGES", 0);
+  if (const char* e = std::getenv("TCCL_STORE_MODE")) {
+    std::string v(e);
+    if (v == "bulk") c.store_mode = kStoreBulk;
+    else if (v == "vec") c.store_mode = kStoreVec;
+  }
+  c.consumer_warps = geti("TCCL_CONSUMER_WARPS", 0);
+  c.ctas_per_sm = geti("TCCL_CTAS_PER_SM", 0);
+  if (const char* e = std::getenv("TCCL_WAIT_TIMEOUT_MS")) c.wait_timeout_ms = std::atof(e);
+  return resolve_config(c);
+}
+
+Config from_public(const tcclConfig_t& p) {
+  Config c;
+  c.engine = p.engine;
+  c.small_max_bytes = p.small_max_bytes;
+  c.stage_bytes = p.stage_bytes;
+  c.stages = p.stages;
+  c.store_mode = p.store_mode;
+  c.consumer_warps = p.consumer_warps;
+  c.ctas_per_sm = p.ctas_per_sm;
+  c.wait_timeout_ms = p.wait_timeout_ms;
+  return resolve_config(c);
+}
+
+tcclConfig_t to_public(const Config& c) {
+  tcclConfig_t p;
+  std::memset(&p, 0, sizeof(p));
+  p.engine = c.engine;
+  p.small_max_bytes = c.small_max_bytes;
+  p.stage_bytes = c.stage_bytes;
+  p.stages = c.stages;
+  p.store_mode = c.store_mode;
+  p.consumer_warps = c.consumer_warps;
+  p.ctas_per_sm = c.ctas_per_sm;
+  p.wait_timeout_ms = c.wait_timeout_ms;
+  return p;
+}
+
+bool config_ok(const tcclConfig_t& p) {
+  return p.engine >= 0 && p.engine <= 3 && p.store_mode >= 0 && p.store_mode <= 2 &&
+         p.stage_bytes >= 0 && p.stages >= 0 && p.consumer_warps >= 0 && p.ctas_per_sm >= 0 &&
+         p.wait_timeout_ms >= 0;
+}
+
+void fill_info(const Lowered& low, tcclLaunchInfo_t* info) {
+  std::memset(info, 0, sizeof(*info));
+  info->engine = low.shape.engine;
+  info->store_mode = low.shape.store_mode;
+  info->ctas = low.shape.grid;
+  info->threads = low.shape.threads;
+  info->stages = low.shape.stages;
+  info->chunk_bytes = low.shape.chunk_bytes;
+  info->windows = (int)low.win.size();
+  info->tasks = low.ntasks;
+  info->smem_bytes = low.shape.smem;
+}
+
+void dump_plan(const Plan& pl, const Lowered& low) {
+  std::fprintf(stderr, "[tccl] plan coll=%d P=%d count=%llu shard=%llu tasks=%zu engine=%d grid=%d "
+               "threads=%d stages=%d chunk=%d smem=%zu windows=%zu\n",
+               pl.coll, pl.nranks, (unsigned long long)pl.count,
+               (unsigned long long)pl.shard_elems, pl.tasks.size(), low.shape.engine,
+               low.shape.grid, low.shape.threads, low.shape.stages, low.shape.chunk_bytes,
+               low.shape.smem, low.win.size());
+  if (log_level() < 2) return;
+  for (size_t i = 0; i < pl.tasks.size(); ++i) {
+    const LogicalTask& t = pl.tasks[i];
+    std::fprintf(stderr, "[tccl]  task %zu %s owner=%d src=%zu intervals dst=%zu intervals deps=%zu\n",
+                 i, t.kind == kShardIn ? "shard-in" : "shard-out", t.exec_rank, t.src.size(),
+                 t.dst.size(), t.deps.size());
+  }
+  for (const Window& w : low.win)
+    std::fprintf(stderr, "[tccl]  win cta=%d src=%d+%llu dst=%d+%llu bytes=%u scalar=%u task=%u\n",
+                 w.cta, w.src_sel, (unsigned long long)w.src_off, w.dst_sel,
+                 (unsigned long long)w.dst_off, w.bytes, w.scalar, w.task);
+}
+
+}  // namespace
+
+struct tcclGroup {
+  int nranks = 0;
+  int device = 0;
+  DeviceDesc dev;
+  Config cfg;
+  int* d_status = nullptr;     // [0] status code
+  uint32_t* d_sm_mask = nullptr;  // 256-bit SM bitmap
+  bool record_sms = false;
+  uint64_t inject_ns = 0;
+  std::map<PlanKey, std::unique_ptr<CachedPlan>> plans;
+  tcclLaunchInfo_t last;
+};
+
+namespace {
+
+tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* const* recv,
+                      size_t count, int es, int cap, CachedPlan** out) {
+  PlanKey key{coll, es, (uint64_t)count, cap > 0 ? cap : 0, std::string()};
+  key.mod16.resize(2 * g->nranks);
+  for (int r = 0; r < g->nranks; ++r) {
+    key.mod16[r] = (char)((uintptr_t)send[r] & 15);
+    key.mod16[g->nranks + r] = (char)((uintptr_t)recv[r] & 15);
+  }
+  auto it = g->plans.find(key);
+  if (it != g->plans.end()) {
+    *out = it->second.get();
+    return tcclSuccess;
+  }
+  Plan pl = plan_collective(coll, g->nranks, count, es, 0);
+  auto cp = std::make_unique<CachedPlan>();
+  std::string why;
+  std::vector<uint8_t> sm(g->nranks), rm(g->nranks);
+  for (int r = 0; r < g->nranks; ++r) {
+    sm[r] = (uint8_t)key.mod16[r];
+    rm[r] = (uint8_t)key.mod16[g->nranks + r];
+  }
+  if (!lower_plan(pl, sm.data(), rm.data(), g->cfg, g->dev, cap, &cp->low, &why)) {
+    if (log_level()) std::fprintf(stderr, "[tccl] cannot lower: %s\n", why.c_str());
+    return tcclInvalidUsage;
+  }
+  if (log_level()) dump_plan(pl, cp->low);
+  const Lowered& low = cp->low;
+  if (low.shape.engine == kEngineBulk) {
+    const size_t wbytes = low.win.size() * sizeof(Window);
+    const size_t cbytes = low.cta_first.size() * sizeof(uint32_t);
+    // one synchronous upload per plan: a new shape's first call must not be
+    // made inside a CUDA graph capture
+    if (cudaMalloc(&cp->d_win, std::max<size_t>(wbytes, 32)) != cudaSuccess ||
+        cudaMalloc(&cp->d_cta_first, cbytes) != cudaSuccess)
+      return tcclCudaError;
+    if ((wbytes && cudaMemcpy(cp->d_win, low.win.data(), wbytes, cudaMemcpyHostToDevice) != cudaSuccess) ||
+        cudaMemcpy(cp->d_cta_first, low.cta_first.data(), cbytes, cudaMemcpyHostToDevice) != cudaSuccess)
+      return tcclCudaError;
+  } else if (low.size_class == 0) {
+    build_small_args<kSmallRanks, kSmallWindows>(low, g->nranks, es, &cp->small_args);
+  } else {
+    build_small_args<kMaxRanks, kLargeWindows>(low, g->nranks, es, &cp->small_args);
+  }
+  *out = cp.get();
+  g->plans.emplace(key, std::move(cp));
+  return tcclSuccess;
+}
+
+tcclResult_t run_collective(tcclGroup* g, int coll, const void* const* send, void* const* recv,
+                            size_t count, int dtype, int op, cudaStream_t stream, int cap) {
+  if (!g) return tcclInvalidArgument;
+  tcclResult_t v = validate(coll, g->nranks, send, recv, count, dtype, op);
+  if (v != tcclSuccess) return v;
+  if (count == 0 || is_noop(coll, g->nranks, send, recv)) {
+    std::memset(&g->last, 0, sizeof(g->last));
+    return tcclSuccess;
+  }
+  if (coll == kAllGather) op = kSum;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return tcclCudaError;
+  if (cur != g->device && cudaSetDevice(g->device) != cudaSuccess) return tcclCudaError;
+  const int es = elem_size_of(dtype);
+  CachedPlan* cp = nullptr;
+  tcclResult_t r = get_plan(g, coll, send, recv, count, es, cap, &cp);
+  int err = 0;
+  if (r == tcclSuccess) {
+    const Lowered& low = cp->low;
+    uint32_t* mask = g->record_sms ? g->d_sm_mask : nullptr;
+    if (low.shape.engine == kEngineBulk) {
+      BulkArgs a;
+      std::memset(&a, 0, sizeof(a));
+      for (int k = 0; k < g->nranks; ++k) {
+        a.p.src[k] = send[k];
+        a.p.dst[k] = recv[k];
+      }
+      a.win = cp->d_win;
+      a.cta_first = cp->d_cta_first;
+      a.status = g->d_status;
+      a.sm_mask = mask;
+      a.timeout_ns = (uint64_t)(g->cfg.wait_timeout_ms * 1e6);
+      a.inject_timeout_ns = g->inject_ns;
+      a.nranks = g->nranks;
+      a.chunk_bytes = low.shape.chunk_bytes;
+      a.stages = low.shape.stages;
+      a.store_mode = low.shape.store_mode;
+      a.consumer_warps = low.shape.consumer_warps;
+      a.release_lag = low.shape.release_lag;
+      a.elem_size = es;
+      err = launch_bulk(coll, dtype, op, a, low.shape, stream);
+    } else {
+      std::vector<unsigned char>& buf = cp->small_args;
+      if (low.size_class == 0)
+        fill_small_ptrs<kSmallRanks, kSmallWindows>(&buf, g->nranks, send, recv, mask);
+      else
+        fill_small_ptrs<kMaxRanks, kLargeWindows>(&buf, g->nranks, send, recv, mask);
+      if (coll == kAllReduce)
+        err = launch_small_ar(dtype, op, low.shape.engine, low.size_class, buf.data(), low.shape, stream);
+      else if (coll == kReduceScatter)
+        err = launch_small_rs(dtype, op, low.shape.engine, low.size_class, buf.data(), low.shape, stream);
+      else
+        err = launch_small_ag(dtype, op, low.shape.engine, low.size_class, buf.data(), low.shape, stream);
+    }
+    fill_info(low, &g->last);
+  }
+  if (cur != g->device) cudaSetDevice(cur);
+  if (r != tcclSuccess) return r;
+  if (err != 0) {
+    if (log_level()) std::fprintf(stderr, "[tccl] launch failed: %s\n", cudaGetErrorString((cudaError_t)err));
+    return tcclCudaError;
+  }
+  return tcclSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tcclGetErrorString(tcclResult_t r) {
+  switch (r) {
+    case tcclSuccess: return "success";
+    case tcclInvalidArgument: return "invalid argument";
+    case tcclInvalidUsage: return "invalid usage";
+    case tcclCudaError: return "CUDA error";
+    case tcclDeviceTimeout: return "device-side wait timed out";
+    case tcclInternalError: return "internal error";
+  }
+  return "unknown result code";
+}
+
+tcclResult_t tcclGetVersion(int* version) {
+  if (!version) return tcclInvalidArgument;
+  *version = TCCL_VERSION;
+  return tcclSuccess;
+}
+
+tcclResult_t tcclGroupCreate(int nranks, tcclGroup_t* out) {
+  if (!out || nranks < 1 || nranks > TCCL_MAX_RANKS) return tcclInvalidArgument;
+  *out = nullptr;
+  auto g = std::make_unique<tcclGroup>();
+  g->nranks = nranks;
+  if (cudaGetDevice(&g->device) != cudaSuccess) return tcclCudaError;
+  if (cudaDeviceGetAttribute(&g->dev.sm_count, cudaDevAttrMultiProcessorCount, g->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&g->dev.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, g->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&g->dev.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, g->device) != cudaSuccess)
+    return tcclCudaError;
+  g->cfg = config_from_env();
+  if (prepare_bulk_kernels((size_t)g->dev.smem_optin) != 0) return tcclCudaError;
+  if (cudaMalloc(&g->d_status, 64) != cudaSuccess) return tcclCudaError;
+  if (cudaMalloc(&g->d_sm_mask, 64) != cudaSuccess) {
+    cudaFree(g->d_status);
+    return tcclCudaError;
+  }
+  if (cudaMemset(g->d_status, 0, 64) != cudaSuccess || cudaMemset(g->d_sm_mask, 0, 64) != cudaSuccess) {
+    cudaFree(g->d_status);
+    cudaFree(g->d_sm_mask);
+    return tcclCudaError;
+  }
+  std::memset(&g->last, 0, sizeof(g->last));
+  *out = g.release();
+  return tcclSuccess;
+}
+
+tcclResult_t tcclGroupDestroy(tcclGroup_t g) {
+  if (!g) return tcclInvalidArgument;
+  cudaDeviceSynchronize();
+  g->plans.clear();
+  cudaFree(g->d_status);
+  cudaFree(g->d_sm_mask);
+  delete g;
+  return tcclSuccess;
+}
+
+tcclResult_t tcclGroupGetConfig(tcclGroup_t g, tcclConfig_t* cfg) {
+  if (!g || !cfg) return tcclInvalidArgument;
+  *cfg = to_public(g->cfg);
+  return tcclSuccess;
+}
+
+tcclResult_t tcclGroupSetConfig(tcclGroup_t g, const tcclConfig_t* cfg) {
+  if (!g || !cfg || !config_ok(*cfg)) return tcclInvalidArgument;
+  cudaDeviceSynchronize();  // plans in flight keep their device tables until done
+  g->cfg = from_public(*cfg);
+  g->plans.clear();
+  return tcclSuccess;
+}
+
+tcclResult_t tcclAllReduce(tcclGroup_t g, const void* const sendbufs[], void* const recvbufs[],
+                           size_t count, tcclDataType_t datatype, tcclRedOp_t op,
+                           cudaStream_t stream, int cta_cap) {
+  return run_collective(g, kAllReduce, sendbufs, recvbufs, count, datatype, op, stream, cta_cap);
+}
+
+tcclResult_t tcclReduceScatter(tcclGroup_t g, const void* const sendbufs[],
+                               void* const recvbufs[], size_t recvcount,
+                               tcclDataType_t datatype, tcclRedOp_t op, cudaStream_t stream,
+                               int cta_cap) {
+  return run_collective(g, kReduceScatter, sendbufs, recvbufs, recvcount, datatype, op, stream,
+                        cta_cap);
+}
+
+tcclResult_t tcclAllGather(tcclGroup_t g, const void* const sendbufs[], void* const recvbufs[],
+                           size_t sendcount, tcclDataType_t datatype, cudaStream_t stream,
+                           int cta_cap) {
+  return run_collective(g, kAllGather, sendbufs, recvbufs, sendcount, datatype, kSum, stream,
+                        cta_cap);
+}
+
+tcclResult_t tcclGroupQueryError(tcclGroup_t g, tcclResult_t* async_status) {
+  if (!g || !async_status) return tcclInvalidArgument;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return tcclCudaError;
+  if (cur != g->device) cudaSetDevice(g->device);
+  int st = 0;
+  bool ok = cudaDeviceSynchronize() == cudaSuccess &&
+            cudaMemcpy(&st, g->d_status, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess &&
+            cudaMemset(g->d_status, 0, sizeof(int)) == cudaSuccess;
+  if (cur != g->device) cudaSetDevice(cur);
+  if (!ok) return tcclCudaError;
+  *async_status = (tcclResult_t)st;
+  return tcclSuccess;
+}
+
+tcclResult_t tcclGetLastLaunchInfo(tcclGroup_t g, tcclLaunchInfo_t* info) {
+  if (!g || !info) return tcclInvalidArgument;
+  *info = g->last;
+  return tcclSuccess;
+}
+
+tcclResult_t tcclGroupRecordSms(tcclGroup_t g, int enable) {
+  if (!g) return tcclInvalidArgument;
+  g->record_sms = enable != 0;
+  return tcclSuccess;
+}
+
+tcclResult_t tcclGroupReadSmRecord(tcclGroup_t g, int* distinct_sms) {
+  if (!g || !distinct_sms) return tcclInvalidArgument;
+  uint32_t m[8];
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(m, g->d_sm_mask, sizeof(m), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(g->d_sm_mask, 0, sizeof(m)) != cudaSuccess)
+    return tcclCudaError;
+  int n = 0;
+  for (uint32_t w : m) n += __builtin_popcount(w);
+  *distinct_sms = n;
+  return tcclSuccess;
+}
+
+tcclResult_t tcclGroupInjectWaitTimeout(tcclGroup_t g, int enable, double timeout_ms) {
+  if (!g || (enable && timeout_ms <= 0)) return tcclInvalidArgument;
+  g->inject_ns = enable ? (uint64_t)(timeout_ms * 1e6) : 0;
+  return tcclSuccess;
+}
+
+tcclResult_t tcclPlanInspect(int coll, int nranks, const void* const sendbufs[],
+                             void* const recvbufs[], size_t count, tcclDataType_t datatype,
+                             int cta_cap, int sm_count, int smem_per_block,
+                             const tcclConfig_t* cfg, int64_t* windows, int max_windows,
+                             int* n_windows, int* n_tasks, tcclLaunchInfo_t* info) {
+  if (!n_windows || !n_tasks || !info || sm_count < 1 || smem_per_block < 1) return tcclInvalidArgument;
+  if (cfg && !config_ok(*cfg)) return tcclInvalidArgument;
+  tcclResult_t v = validate(coll, nranks, sendbufs, recvbufs, count, datatype, 0);
+  if (v != tcclSuccess) return v;
+  *n_windows = 0;
+  *n_tasks = 0;
+  std::memset(info, 0, sizeof(*info));
+  if (count == 0) return tcclSuccess;
+  const int es = elem_size_of(datatype);
+  Plan pl = plan_collective(coll, nranks, count, es, 0);
+  std::vector<uint8_t> sm(nranks), rm(nranks);
+  for (int r = 0; r < nranks; ++r) {
+    sm[r] = (uint8_t)((uintptr_t)sendbufs[r] & 15);
+    rm[r] = (uint8_t)((uintptr_t)recvbufs[r] & 15);
+  }
+  DeviceDesc dev;
+  dev.sm_count = sm_count;
+  dev.smem_optin = smem_per_block;
+  dev.smem_per_sm = smem_per_block + 1024;
+  Config c = cfg ? from_public(*cfg) : resolve_config(Config());
+  Lowered low;
+  std::string why;
+  if (!lower_plan(pl, sm.data(), rm.data(), c, dev, cta_cap, &low, &why)) return tcclInvalidUsage;
+  *n_tasks = (int)pl.tasks.size();
+  *n_windows = (int)low.win.size();
+  fill_info(low, info);
+  if (windows) {
+    for (int i = 0; i < std::min(max_windows, (int)low.win.size()); ++i) {
+      const Window& w = low.win[i];
+      int64_t* o = windows + 8 * (size_t)i;
+      o[0] = w.cta;
+      o[1] = w.src_sel;
+      o[2] = (int64_t)w.src_off;
+      o[3] = w.dst_sel;
+      o[4] = (int64_t)w.dst_off;
+      o[5] = w.bytes;
+      o[6] = w.scalar;
+      o[7] = w.task;
+    }
+  }
+  return tcclSuccess;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Launch helpers: map runtime (dtype, op, engine, size class) onto kernel
+// template instances.
+#pragma once
+
+#include "kernels_common.cuh"
+
+namespace tccl {
+namespace dev {
+
+template <int C, int D, int O>
+int launch_bulk_t(const BulkArgs& a, const LaunchShape& s, cudaStream_t st) {
+  bulk_kernel<C, D, O><<<s.grid, s.threads, s.smem, st>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+
+template <int C, int D, int O>
+int set_bulk_smem(size_t bytes) {
+  cudaError_t e = cudaFuncSetAttribute(bulk_kernel<C, D, O>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bulk_kernel<C, D, O>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  return static_cast<int>(e);
+}
+
+template <int C, int D, int O, int MAXR, int MAXW>
+int launch_small_t(int engine, const void* args, const LaunchShape& s, cudaStream_t st) {
+  const auto& a = *static_cast<const SmallArgs<MAXR, MAXW>*>(args);
+  if (engine == kEngineWarp)
+    small_kernel<C, D, O, MAXR, MAXW, true><<<s.grid, s.threads, 0, st>>>(a);
+  else
+    small_kernel<C, D, O, MAXR, MAXW, false><<<s.grid, s.threads, 0, st>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+
+template <int C, int D, int O>
+int launch_small_sc(int engine, int size_class, const void* args, const LaunchShape& s,
+                    cudaStream_t st) {
+  if (size_class == 0) return launch_small_t<C, D, O, kSmallRanks, kSmallWindows>(engine, args, s, st);
+  return launch_small_t<C, D, O, kMaxRanks, kLargeWindows>(engine, args, s, st);
+}
+
+// (dtype, op) -> F<C, D, O>(args...) for reducing collectives
+#define TCCL_REDUCE_SWITCH(COLL, FN, ...)                                   \
+  switch (dtype * 3 + op) {                                                 \
+    case kF32 * 3 + kSum: return FN<COLL, kF32, kSum>(__VA_ARGS__);         \
+    case kF32 * 3 + kMin: return FN<COLL, kF32, kMin>(__VA_ARGS__);         \
+    case kF32 * 3 + kMax: return FN<COLL, kF32, kMax>(__VA_ARGS__);         \
+    case kBF16 * 3 + kSum: return FN<COLL, kBF16, kSum>(__VA_ARGS__);       \
+    case kBF16 * 3 + kMin: return FN<COLL, kBF16, kMin>(__VA_ARGS__);       \
+    case kBF16 * 3 + kMax: return FN<COLL, kBF16, kMax>(__VA_ARGS__);       \
+    case kI32 * 3 + kSum: return FN<COLL, kI32, kSum>(__VA_ARGS__);         \
+    case kI32 * 3 + kMin: return FN<COLL, kI32, kMin>(__VA_ARGS__);         \
+    case kI32 * 3 + kMax: return FN<COLL, kI32, kMax>(__VA_ARGS__);         \
+    default: return static_cast<int>(cudaErrorInvalidValue);                \
+  }
+
+// all-gather only needs the element size
+#define TCCL_COPY_SWITCH(FN, ...)                                                   \
+  return (dtype == kBF16) ? FN<kAllGather, kBF16, kSum>(__VA_ARGS__)                \
+                          : FN<kAllGather, kF32, kSum>(__VA_ARGS__);
+
+}  // namespace dev
+}  // namespace tccl

@@ -1,0 +1,102 @@
+// Internal types shared by the host planner/lowering (plan.cpp, api.cpp) and
+// the device kernels (kernels.cu). Nothing here is part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace tccl {
+
+constexpr int kMaxRanks = 64;
+constexpr int kSmallRanks = 8;    // small-argument class of the warp/vec engines
+constexpr int kSmallWindows = 8;
+constexpr int kLargeWindows = 3 * kMaxRanks + 2;
+
+enum Coll : int { kAllReduce = 0, kReduceScatter = 1, kAllGather = 2 };
+enum DType : int { kF32 = 0, kBF16 = 1, kI32 = 2 };
+enum RedOp : int { kSum = 0, kMin = 1, kMax = 2 };
+enum Engine : int { kEngineAuto = 0, kEngineBulk = 1, kEngineWarp = 2, kEngineVec = 3 };
+enum StoreMode : int { kStoreAuto = 0, kStoreBulk = 1, kStoreVec = 2 };
+
+// Status codes a kernel may leave in the group's status word (same values
+// as tcclResult_t).
+constexpr int kStatusTimeout = 4;
+
+// One physical window: a contiguous byte range of a lowered task, resolved
+// against the per-rank base pointers of the call. The "selected" source set
+// is every rank's send buffer (src_sel < 0, a reduction) or one rank's
+// (src_sel = r); likewise for destinations.
+struct Window {
+  uint64_t src_off;  // byte offset into each selected send buffer
+  uint64_t dst_off;  // byte offset into each selected recv buffer
+  uint32_t bytes;    // window length in bytes (multiple of the element size)
+  int16_t src_sel;
+  int16_t dst_sel;
+  uint16_t scalar;   // 1: element-wise path (edge or not 16-byte co-aligned)
+  uint16_t task;     // logical task (shard) the window came from
+  int32_t cta;       // bulk engine: owning CTA; warp/vec engines: -1
+};
+static_assert(sizeof(Window) == 32, "Window layout");
+
+template <int MAXR>
+struct BasePtrs {
+  const void* src[MAXR];
+  void* dst[MAXR];
+};
+
+// Bulk (TMA pipeline) engine: windows live in a device table, grouped by CTA.
+struct BulkArgs {
+  BasePtrs<kMaxRanks> p;
+  const Window* win;          // device table
+  const uint32_t* cta_first;  // device table, grid + 1 entries
+  int* status;                // group status word (device)
+  uint32_t* sm_mask;          // SM recorder bitmap (device) or null
+  uint64_t timeout_ns;        // bound on every wait
+  uint64_t inject_timeout_ns; // test hook: > 0 makes CTA 0 wait on a barrier nothing signals
+  int nranks;
+  int chunk_bytes;            // bytes per source per chunk (multiple of 16)
+  int stages;
+  int store_mode;             // kStoreBulk or kStoreVec
+  int consumer_warps;
+  int release_lag;            // all-gather bulk stores: store groups kept in flight
+  int elem_size;
+};
+
+// Warp / vec (small-message) engines: the whole lowered plan rides in the
+// kernel parameters, so a launch reads no table from memory.
+template <int MAXR, int MAXW>
+struct SmallArgs {
+  BasePtrs<MAXR> p;
+  Window win[MAXW];
+  uint64_t vec_prefix[MAXW + 1];   // 16-byte units before window w (vector windows only)
+  uint64_t elem_prefix[MAXW + 1];  // elements before window w (scalar windows only)
+  uint32_t* sm_mask;
+  int nwin;
+  int nranks;
+  int elem_size;
+};
+
+struct LaunchShape {
+  int engine = 0;
+  int store_mode = 0;
+  int grid = 0;
+  int threads = 0;
+  int stages = 0;
+  int chunk_bytes = 0;
+  int consumer_warps = 0;
+  int release_lag = 0;
+  size_t smem = 0;
+};
+
+// Kernel launchers (kernels.cu). Each returns a cudaError_t as int.
+int launch_bulk(int coll, int dtype, int op, const BulkArgs& a, const LaunchShape& s,
+                void* stream);
+int launch_small_ar(int dtype, int op, int engine, int size_class, const void* args,
+                    const LaunchShape& s, void* stream);
+int launch_small_rs(int dtype, int op, int engine, int size_class, const void* args,
+                    const LaunchShape& s, void* stream);
+int launch_small_ag(int dtype, int op, int engine, int size_class, const void* args,
+                    const LaunchShape& s, void* stream);
+int prepare_bulk_kernels(size_t smem_bytes);  // opt-in shared memory for the bulk kernels
+
+}  // namespace tccl

@@ -1,0 +1,600 @@
+// Device code for the three engines (sm_103a).
+//
+// Bulk engine: the T-CCL "TMA engine" ("NCCL M2N vs T-CCL" article, section
+// 2.3 and the kernel sketches of section 2.5), rebuilt for one GPU. Each CTA
+// is persistent over its windows. One producer thread issues, per chunk, one
+// `cp.async.bulk` load per source rank into a shared-memory stage and arms
+// the stage's mbarrier with the expected byte count (shard-in load,
+// section 2.2 "reduction localisation"). Consumer warps wait on the stage,
+// fold the P contributions in ascending rank order in fp32 / int32 registers
+// and emit the reduced chunk, which exists once on chip, to every destination
+// (section 2.2 "shard-out: load once, reuse for all peer stores"): either as
+// P `cp.async.bulk` stores from a shared-memory result slot, or as P 128-bit
+// stores from registers. Every wait is bounded; on expiry the kernel records
+// a timeout in the group's status word, skips its remaining work and exits.
+//
+// Warp / vec engines (small messages): no shared memory, no barriers. The
+// warp engine gives each (16-byte vector, rank) pair its own lane: lanes load
+// one vector each, and every lane of a group of P folds the group's values in
+// rank order through warp shuffles, then stores its rank's copy. The vec
+// engine gives each vector to one lane, which loads all P contributions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace tccl {
+namespace dev {
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// global -> shared bulk copy, completion counted in bytes on `bar`
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// shared -> global bulk copy, tracked by bulk async-groups
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_addr(smem_src)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_read_dyn(int n) {
+  switch (n) {
+    case 0: bulk_wait_read<0>(); break;
+    case 1: bulk_wait_read<1>(); break;
+    case 2: bulk_wait_read<2>(); break;
+    case 3: bulk_wait_read<3>(); break;
+    case 4: bulk_wait_read<4>(); break;
+    case 5: bulk_wait_read<5>(); break;
+    case 6: bulk_wait_read<6>(); break;
+    default: bulk_wait_read<7>(); break;
+  }
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// order this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy) reads of them
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t s;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
+  return s;
+}
+
+__device__ __forceinline__ void record_sm(uint32_t* mask) {
+  if (mask) {
+    uint32_t s = sm_id();
+    atomicOr(&mask[(s >> 5) & 7], 1u << (s & 31));
+  }
+}
+
+// 128-bit global accesses with the streaming (evict-first) cache policy:
+// every byte of this path is read or written exactly once.
+__device__ __forceinline__ uint4 ld_global_v4(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
+  __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
+// Bounded wait on an mbarrier phase. Gives up when another thread of the CTA
+// has flagged an abort, or after `timeout_ns` of %globaltimer time, in which
+// case it flags the abort and records a timeout in the status word.
+static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort_flag, uint64_t timeout_ns,
+                                          int* status, bool honour_abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && *abort_flag) return false;
+    if ((i & 31) == 0 && global_ns() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      atomicCAS(status, 0, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ folds
+// R = left fold in ascending rank order. fp32 adds round to nearest (no
+// contraction: there is no multiply); min/max keep the earlier rank on ties;
+// bf16 widens exactly to fp32 and is rounded once, to nearest even, at the end;
+// int32 sums wrap.
+template <int OP>
+__device__ __forceinline__ float step_f32(float acc, float x) {
+  if (OP == kSum) return __fadd_rn(acc, x);
+  if (OP == kMin) return (x < acc) ? x : acc;
+  return (x > acc) ? x : acc;
+}
+
+template <int OP>
+__device__ __forceinline__ int32_t step_i32(int32_t acc, int32_t x) {
+  if (OP == kSum) return static_cast<int32_t>(static_cast<uint32_t>(acc) + static_cast<uint32_t>(x));
+  if (OP == kMin) return (x < acc) ? x : acc;
+  return (x > acc) ? x : acc;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int DT, int OP>
+struct Fold;
+
+template <int OP>
+struct Fold<kF32, OP> {
+  float a[4];
+  __device__ __forceinline__ void init(uint4 u) {
+    a[0] = __uint_as_float(u.x);
+    a[1] = __uint_as_float(u.y);
+    a[2] = __uint_as_float(u.z);
+    a[3] = __uint_as_float(u.w);
+  }
+  __device__ __forceinline__ void add(uint4 u) {
+    a[0] = step_f32<OP>(a[0], __uint_as_float(u.x));
+    a[1] = step_f32<OP>(a[1], __uint_as_float(u.y));
+    a[2] = step_f32<OP>(a[2], __uint_as_float(u.z));
+    a[3] = step_f32<OP>(a[3], __uint_as_float(u.w));
+  }
+  __device__ __forceinline__ uint4 out() const {
+    return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                      __float_as_uint(a[3]));
+  }
+};
+
+template <int OP>
+struct Fold<kBF16, OP> {
+  float a[8];
+  __device__ __forceinline__ void init(uint4 u) {
+    a[0] = bf16_lo(u.x); a[1] = bf16_hi(u.x);
+    a[2] = bf16_lo(u.y); a[3] = bf16_hi(u.y);
+    a[4] = bf16_lo(u.z); a[5] = bf16_hi(u.z);
+    a[6] = bf16_lo(u.w); a[7] = bf16_hi(u.w);
+  }
+  __device__ __forceinline__ void add(uint4 u) {
+    a[0] = step_f32<OP>(a[0], bf16_lo(u.x)); a[1] = step_f32<OP>(a[1], bf16_hi(u.x));
+    a[2] = step_f32<OP>(a[2], bf16_lo(u.y)); a[3] = step_f32<OP>(a[3], bf16_hi(u.y));
+    a[4] = step_f32<OP>(a[4], bf16_lo(u.z)); a[5] = step_f32<OP>(a[5], bf16_hi(u.z));
+    a[6] = step_f32<OP>(a[6], bf16_lo(u.w)); a[7] = step_f32<OP>(a[7], bf16_hi(u.w));
+  }
+  __device__ __forceinline__ uint4 out() const {
+    return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                      pack_bf16x2(a[6], a[7]));
+  }
+};
+
+template <int OP>
+struct Fold<kI32, OP> {
+  int32_t a[4];
+  __device__ __forceinline__ void init(uint4 u) {
+    a[0] = static_cast<int32_t>(u.x);
+    a[1] = static_cast<int32_t>(u.y);
+    a[2] = static_cast<int32_t>(u.z);
+    a[3] = static_cast<int32_t>(u.w);
+  }
+  __device__ __forceinline__ void add(uint4 u) {
+    a[0] = step_i32<OP>(a[0], static_cast<int32_t>(u.x));
+    a[1] = step_i32<OP>(a[1], static_cast<int32_t>(u.y));
+    a[2] = step_i32<OP>(a[2], static_cast<int32_t>(u.z));
+    a[3] = step_i32<OP>(a[3], static_cast<int32_t>(u.w));
+  }
+  __device__ __forceinline__ uint4 out() const {
+    return make_uint4(static_cast<uint32_t>(a[0]), static_cast<uint32_t>(a[1]),
+                      static_cast<uint32_t>(a[2]), static_cast<uint32_t>(a[3]));
+  }
+};
+
+// One element of every selected source, folded, stored to every selected
+// destination: the element-wise path for window edges and buffers that are
+// not 16-byte co-aligned.
+template <int COLL, int DT, int OP, int MAXR>
+__device__ __forceinline__ void scalar_element(const BasePtrs<MAXR>& p, int nranks,
+                                               const Window& w, uint64_t e) {
+  constexpr int es = (DT == kBF16) ? 2 : 4;
+  const uint64_t so = w.src_off + e * es;
+  const uint64_t dso = w.dst_off + e * es;
+  const int d0 = w.dst_sel < 0 ? 0 : w.dst_sel;
+  const int d1 = w.dst_sel < 0 ? nranks : w.dst_sel + 1;
+  if (COLL == kAllGather) {
+    const char* s = static_cast<const char*>(p.src[w.src_sel < 0 ? 0 : w.src_sel]) + so;
+    if (es == 2) {
+      uint16_t v = *reinterpret_cast<const uint16_t*>(s);
+      for (int d = d0; d < d1; ++d) *reinterpret_cast<uint16_t*>(static_cast<char*>(p.dst[d]) + dso) = v;
+    } else {
+      uint32_t v = *reinterpret_cast<const uint32_t*>(s);
+      for (int d = d0; d < d1; ++d) *reinterpret_cast<uint32_t*>(static_cast<char*>(p.dst[d]) + dso) = v;
+    }
+    return;
+  }
+  if (DT == kF32) {
+    float acc = *reinterpret_cast<const float*>(static_cast<const char*>(p.src[0]) + so);
+    for (int r = 1; r < nranks; ++r)
+      acc = step_f32<OP>(acc, *reinterpret_cast<const float*>(static_cast<const char*>(p.src[r]) + so));
+    for (int d = d0; d < d1; ++d) *reinterpret_cast<float*>(static_cast<char*>(p.dst[d]) + dso) = acc;
+  } else if (DT == kBF16) {
+    float acc = bf16_lo(*reinterpret_cast<const uint16_t*>(static_cast<const char*>(p.src[0]) + so));
+    for (int r = 1; r < nranks; ++r)
+      acc = step_f32<OP>(acc, bf16_lo(*reinterpret_cast<const uint16_t*>(static_cast<const char*>(p.src[r]) + so)));
+    uint16_t h = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+    for (int d = d0; d < d1; ++d) *reinterpret_cast<uint16_t*>(static_cast<char*>(p.dst[d]) + dso) = h;
+  } else {
+    int32_t acc = *reinterpret_cast<const int32_t*>(static_cast<const char*>(p.src[0]) + so);
+    for (int r = 1; r < nranks; ++r)
+      acc = step_i32<OP>(acc, *reinterpret_cast<const int32_t*>(static_cast<const char*>(p.src[r]) + so));
+    for (int d = d0; d < d1; ++d) *reinterpret_cast<int32_t*>(static_cast<char*>(p.dst[d]) + dso) = acc;
+  }
+}
+
+// ------------------------------------------------------------------ bulk engine
+constexpr int kBarrierRegion = 1024;  // mbarriers + abort flag, ahead of the stages
+constexpr int kMaxStages = 32;
+
+template <int COLL, int DT, int OP>
+__global__ void __launch_bounds__(1024, 1) bulk_kernel(const __grid_constant__ BulkArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int S = a.stages;
+  const int P = a.nranks;
+  const int nsrc = (COLL == kAllGather) ? 1 : P;
+  const uint32_t chunk = static_cast<uint32_t>(a.chunk_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* never = empty + kMaxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(never + 1);
+  unsigned char* stage_base = smem + kBarrierRegion;
+  unsigned char* result_base = stage_base + static_cast<size_t>(S) * nsrc * chunk;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ncw = a.consumer_warps;
+  const bool ag_bulk = (COLL == kAllGather) && a.store_mode == kStoreBulk;
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < S; ++k) {
+      mbar_init(&full[k], 1);
+      mbar_init(&empty[k], ag_bulk ? 1 : ncw);
+    }
+    mbar_init(never, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    record_sm(a.sm_mask);
+  }
+  __syncthreads();
+
+  const uint32_t wbeg = a.cta_first[blockIdx.x];
+  const uint32_t wend = a.cta_first[blockIdx.x + 1];
+
+  // ---------------- producer: one thread issues every bulk load
+  if (warp == 0) {
+    if (lane != 0) return;
+    uint32_t it = 0;
+    bool ok = true;
+    for (uint32_t wi = wbeg; wi < wend && ok; ++wi) {
+      const Window w = a.win[wi];
+      if (w.scalar) continue;
+      const char* src_one = static_cast<const char*>(a.p.src[w.src_sel < 0 ? 0 : w.src_sel]);
+      for (uint32_t off = 0; off < w.bytes; off += chunk) {
+        const uint32_t n = min(chunk, w.bytes - off);
+        const uint32_t k = it % S;
+        if (it >= static_cast<uint32_t>(S)) {
+          ok = wait_bounded(&empty[k], ((it / S) & 1) ^ 1, abort_flag, a.timeout_ns, a.status, true);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(&full[k], n * nsrc);
+        unsigned char* st = stage_base + static_cast<size_t>(k) * nsrc * chunk;
+        if (COLL == kAllGather) {
+          bulk_load(st, src_one + w.src_off + off, n, &full[k]);
+        } else {
+          for (int r = 0; r < nsrc; ++r)
+            bulk_load(st + static_cast<size_t>(r) * chunk,
+                      static_cast<const char*>(a.p.src[r]) + w.src_off + off, n, &full[k]);
+        }
+        ++it;
+      }
+    }
+    if (!ok) {
+      // an abort: let every load this thread issued land before the CTA's
+      // shared memory goes away (the last S iterations are the only ones
+      // that can still be in flight)
+      const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
+      for (uint32_t j = first; j < it; ++j)
+        wait_bounded(&full[j % S], (j / S) & 1, abort_flag, a.timeout_ns, a.status, false);
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const int ctid = threadIdx.x - 32;
+  const int nct = ncw * 32;
+  uint32_t it = 0;
+  bool ok = true;
+
+  if (ag_bulk) {
+    // all-gather with bulk stores: the stage itself is the shard, read once
+    // from memory and stored from shared memory to all P destinations
+    for (uint32_t wi = wbeg; wi < wend; ++wi) {
+      const Window w = a.win[wi];
+      if (w.scalar) {
+        if (!*abort_flag)
+          for (uint64_t e = ctid; e < w.bytes / (DT == kBF16 ? 2 : 4); e += nct)
+            scalar_element<COLL, DT, OP, kMaxRanks>(a.p, P, w, e);
+        continue;
+      }
+      if (ctid != 0) continue;
+      const int d0 = w.dst_sel < 0 ? 0 : w.dst_sel;
+      const int d1 = w.dst_sel < 0 ? P : w.dst_sel + 1;
+      for (uint32_t off = 0; off < w.bytes && ok; off += chunk) {
+        const uint32_t n = min(chunk, w.bytes - off);
+        const uint32_t k = it % S;
+        ok = wait_bounded(&full[k], (it / S) & 1, abort_flag, a.timeout_ns, a.status, true);
+        if (ok && a.inject_timeout_ns && blockIdx.x == 0 && it == 0)
+          ok = wait_bounded(never, 0, abort_flag, a.inject_timeout_ns, a.status, true);
+        if (!ok) break;
+        const unsigned char* st = stage_base + static_cast<size_t>(k) * chunk;
+        fence_proxy_async_smem();
+        for (int d = d0; d < d1; ++d)
+          bulk_store(static_cast<char*>(a.p.dst[d]) + w.dst_off + off, st, n);
+        bulk_commit();
+        bulk_wait_read_dyn(a.release_lag);
+        if (it >= static_cast<uint32_t>(a.release_lag)) mbar_arrive(&empty[(it - a.release_lag) % S]);
+        ++it;
+      }
+    }
+    if (ctid == 0) bulk_wait_all();
+    return;
+  }
+
+  const bool bulk_out = (a.store_mode == kStoreBulk);
+  for (uint32_t wi = wbeg; wi < wend; ++wi) {
+    const Window w = a.win[wi];
+    if (w.scalar) {
+      if (!*abort_flag)
+        for (uint64_t e = ctid; e < w.bytes / (DT == kBF16 ? 2 : 4); e += nct)
+          scalar_element<COLL, DT, OP, kMaxRanks>(a.p, P, w, e);
+      continue;
+    }
+    const int d0 = w.dst_sel < 0 ? 0 : w.dst_sel;
+    const int d1 = w.dst_sel < 0 ? P : w.dst_sel + 1;
+    for (uint32_t off = 0; off < w.bytes; off += chunk) {
+      const uint32_t n = min(chunk, w.bytes - off);
+      const uint32_t nv = n >> 4;
+      const uint32_t k = it % S;
+      if (ok) ok = wait_bounded(&full[k], (it / S) & 1, abort_flag, a.timeout_ns, a.status, true);
+      if (ok && a.inject_timeout_ns && blockIdx.x == 0 && it == 0)
+        ok = wait_bounded(never, 0, abort_flag, a.inject_timeout_ns, a.status, true);
+      const unsigned char* st = stage_base + static_cast<size_t>(k) * nsrc * chunk;
+      if (!bulk_out) {
+        if (ok) {
+          for (uint32_t v = ctid; v < nv; v += nct) {
+            uint4 res;
+            if (COLL == kAllGather) {
+              res = reinterpret_cast<const uint4*>(st)[v];
+            } else {
+              Fold<DT, OP> f;
+              f.init(reinterpret_cast<const uint4*>(st)[v]);
+#pragma unroll 4
+              for (int r = 1; r < P; ++r)
+                f.add(reinterpret_cast<const uint4*>(st + static_cast<size_t>(r) * chunk)[v]);
+              res = f.out();
+            }
+            const uint64_t o = w.dst_off + off + static_cast<uint64_t>(v) * 16;
+            for (int d = d0; d < d1; ++d) st_global_v4(static_cast<char*>(a.p.dst[d]) + o, res);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[k]);
+      } else {
+        unsigned char* res_slot = result_base + static_cast<size_t>(it & 1) * chunk;
+        if (ctid == 0) bulk_wait_read<1>();  // the slot's previous stores have read it
+        named_bar_sync(1, nct);
+        if (ok) {
+          for (uint32_t v = ctid; v < nv; v += nct) {
+            Fold<DT, OP> f;
+            f.init(reinterpret_cast<const uint4*>(st)[v]);
+#pragma unroll 4
+            for (int r = 1; r < P; ++r)
+              f.add(reinterpret_cast<const uint4*>(st + static_cast<size_t>(r) * chunk)[v]);
+            reinterpret_cast<uint4*>(res_slot)[v] = f.out();
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[k]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, nct);
+        if (ctid == 0 && ok && !*abort_flag) {
+          for (int d = d0; d < d1; ++d)
+            bulk_store(static_cast<char*>(a.p.dst[d]) + w.dst_off + off, res_slot, n);
+          bulk_commit();
+        }
+      }
+      ++it;
+    }
+  }
+  if (ctid == 0) bulk_wait_all();
+}
+
+// ------------------------------------------------------------------ small engines
+template <int MAXW>
+__device__ __forceinline__ int find_window(const uint64_t* prefix, int nwin, uint64_t u) {
+  int lo = 0, hi = nwin - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int COLL, int DT, int OP, int MAXR, int MAXW, bool SHFL>
+__global__ void __launch_bounds__(256) small_kernel(const __grid_constant__ SmallArgs<MAXR, MAXW> a) {
+  if (threadIdx.x == 0) record_sm(a.sm_mask);
+  const int P = a.nranks;
+  const uint64_t nvec = a.vec_prefix[a.nwin];
+  const uint64_t nelem = a.elem_prefix[a.nwin];
+  const uint64_t gtid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const uint64_t nthr = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+
+  if (SHFL) {
+    // one lane per (vector, rank): groups of P lanes, 32 / P groups per warp
+    const int lane = threadIdx.x & 31;
+    const int vpw = 32 / P;
+    const int g = lane / P;
+    const int r = lane - g * P;
+    const bool lane_used = g < vpw;
+    const int base_lane = lane_used ? g * P : 0;
+    const uint64_t gwarp = gtid >> 5;
+    const uint64_t nwarps = nthr >> 5;
+    for (uint64_t base = gwarp * vpw; base < nvec; base += nwarps * vpw) {
+      const uint64_t u = base + g;
+      const bool valid = lane_used && u < nvec;
+      uint4 x = make_uint4(0, 0, 0, 0);
+      int wi = 0;
+      uint64_t off = 0;
+      if (valid) {
+        wi = find_window<MAXW>(a.vec_prefix, a.nwin, u);
+        off = (u - a.vec_prefix[wi]) * 16;
+        const Window& w = a.win[wi];
+        if (COLL == kAllGather) {
+          if (r == 0)
+            x = ld_global_v4(static_cast<const char*>(a.p.src[w.src_sel < 0 ? 0 : w.src_sel]) + w.src_off + off);
+        } else {
+          x = ld_global_v4(static_cast<const char*>(a.p.src[r]) + w.src_off + off);
+        }
+      }
+      uint4 res;
+      if (COLL == kAllGather) {
+        res.x = __shfl_sync(0xFFFFFFFFu, x.x, base_lane);
+        res.y = __shfl_sync(0xFFFFFFFFu, x.y, base_lane);
+        res.z = __shfl_sync(0xFFFFFFFFu, x.z, base_lane);
+        res.w = __shfl_sync(0xFFFFFFFFu, x.w, base_lane);
+      } else {
+        Fold<DT, OP> f;
+        for (int rr = 0; rr < P; ++rr) {
+          uint4 y;
+          y.x = __shfl_sync(0xFFFFFFFFu, x.x, base_lane + rr);
+          y.y = __shfl_sync(0xFFFFFFFFu, x.y, base_lane + rr);
+          y.z = __shfl_sync(0xFFFFFFFFu, x.z, base_lane + rr);
+          y.w = __shfl_sync(0xFFFFFFFFu, x.w, base_lane + rr);
+          if (rr == 0) f.init(y);
+          else f.add(y);
+        }
+        res = f.out();
+      }
+      if (valid) {
+        const Window& w = a.win[wi];
+        if (w.dst_sel < 0) {
+          st_global_v4(static_cast<char*>(a.p.dst[r]) + w.dst_off + off, res);
+        } else if (r == 0) {
+          st_global_v4(static_cast<char*>(a.p.dst[w.dst_sel]) + w.dst_off + off, res);
+        }
+      }
+    }
+  } else {
+    for (uint64_t u = gtid; u < nvec; u += nthr) {
+      const int wi = find_window<MAXW>(a.vec_prefix, a.nwin, u);
+      const Window& w = a.win[wi];
+      const uint64_t off = (u - a.vec_prefix[wi]) * 16;
+      uint4 res;
+      if (COLL == kAllGather) {
+        res = ld_global_v4(static_cast<const char*>(a.p.src[w.src_sel < 0 ? 0 : w.src_sel]) + w.src_off + off);
+      } else {
+        Fold<DT, OP> f;
+        f.init(ld_global_v4(static_cast<const char*>(a.p.src[0]) + w.src_off + off));
+#pragma unroll 8
+        for (int r = 1; r < P; ++r)
+          f.add(ld_global_v4(static_cast<const char*>(a.p.src[r]) + w.src_off + off));
+        res = f.out();
+      }
+      const int d0 = w.dst_sel < 0 ? 0 : w.dst_sel;
+      const int d1 = w.dst_sel < 0 ? P : w.dst_sel + 1;
+      for (int d = d0; d < d1; ++d) st_global_v4(static_cast<char*>(a.p.dst[d]) + w.dst_off + off, res);
+    }
+  }
+
+  for (uint64_t e = gtid; e < nelem; e += nthr) {
+    const int wi = find_window<MAXW>(a.elem_prefix, a.nwin, e);
+    scalar_element<COLL, DT, OP, MAXR>(a.p, P, a.win[wi], e - a.elem_prefix[wi]);
+  }
+}
+
+}  // namespace dev
+}  // namespace tccl

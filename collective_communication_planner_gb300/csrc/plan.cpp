@@ -1,0 +1,395 @@
+// Task planner and lowering pass. See plan.h.
+#include "plan.h"
+
+#include <algorithm>
+#include <cstdio>
+
+namespace tccl {
+
+namespace {
+
+uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+uint64_t round_up(uint64_t a, uint64_t m) { return ceil_div(a, m) * m; }
+
+constexpr uint32_t kMaxWindowBytes = 1u << 30;
+
+struct PhysTask {
+  int src_sel;
+  int dst_sel;
+  uint64_t src_off;
+  uint64_t dst_off;
+  uint64_t bytes;
+  int task;
+};
+
+std::vector<Interval> all_ranks(int p, uint64_t b, uint64_t e) {
+  std::vector<Interval> v;
+  v.reserve(p);
+  for (int r = 0; r < p; ++r) v.push_back({r, b, e});
+  return v;
+}
+
+// A task's interval list selects either every rank at one common interval
+// (sel = -1) or a single rank (sel = that rank).
+bool selection(const std::vector<Interval>& iv, int p, int es, int* sel, uint64_t* off,
+               uint64_t* bytes) {
+  if (iv.empty()) return false;
+  for (const Interval& x : iv)
+    if (x.begin != iv[0].begin || x.end != iv[0].end) return false;
+  if ((int)iv.size() == p && p > 1) {
+    for (int r = 0; r < p; ++r)
+      if (iv[r].rank != r) return false;
+    *sel = -1;
+  } else if (iv.size() == 1) {
+    *sel = (p == 1) ? -1 : iv[0].rank;
+  } else {
+    return false;
+  }
+  *off = iv[0].begin * (uint64_t)es;
+  *bytes = (iv[0].end - iv[0].begin) * (uint64_t)es;
+  return true;
+}
+
+void push_split(std::vector<Window>& out, Window w, uint64_t bytes, uint32_t limit) {
+  while (bytes > 0) {
+    uint64_t n = std::min<uint64_t>(bytes, limit);
+    w.bytes = (uint32_t)n;
+    out.push_back(w);
+    w.src_off += n;
+    w.dst_off += n;
+    bytes -= n;
+  }
+}
+
+}  // namespace
+
+uint64_t message_bytes(int coll, int nranks, uint64_t count, int elem_size) {
+  if (coll == kAllReduce) return count * (uint64_t)elem_size;
+  return (uint64_t)nranks * count * (uint64_t)elem_size;
+}
+
+Plan plan_collective(int coll, int nranks, uint64_t count, int elem_size, int op) {
+  Plan pl;
+  pl.coll = coll;
+  pl.nranks = nranks;
+  pl.elem_size = elem_size;
+  pl.op = op;
+  pl.count = count;
+  const int p = nranks;
+  if (coll == kAllReduce) {
+    // shard length: ceil(count / P), rounded up so every shard starts 16-byte
+    // aligned relative to the buffer base; trailing shards may be short or empty
+    uint64_t q = round_up(ceil_div(count, (uint64_t)p), 16 / (uint64_t)elem_size);
+    pl.shard_elems = q;
+    for (int s = 0; s < p; ++s) {
+      uint64_t b = std::min<uint64_t>((uint64_t)s * q, count);
+      uint64_t e = std::min<uint64_t>((uint64_t)(s + 1) * q, count);
+      if (b == e) continue;
+      LogicalTask in{kShardIn, op, s, s, kSendBuf, kOwnerShard, all_ranks(p, b, e), {{s, b, e}},
+                     {}};
+      int in_idx = (int)pl.tasks.size();
+      pl.tasks.push_back(in);
+      LogicalTask out{kShardOut, -1, s, s, kOwnerShard, kRecvBuf, {{s, b, e}}, all_ranks(p, b, e),
+                      {in_idx}};
+      pl.tasks.push_back(out);
+    }
+  } else if (coll == kReduceScatter) {
+    pl.shard_elems = count;
+    if (count == 0) return pl;
+    for (int s = 0; s < p; ++s) {
+      uint64_t b = (uint64_t)s * count, e = b + count;
+      pl.tasks.push_back({kShardIn, op, s, s, kSendBuf, kRecvBuf, all_ranks(p, b, e),
+                          {{s, 0, count}}, {}});
+    }
+  } else {
+    pl.shard_elems = count;
+    if (count == 0) return pl;
+    for (int s = 0; s < p; ++s) {
+      uint64_t b = (uint64_t)s * count, e = b + count;
+      pl.tasks.push_back({kShardOut, -1, s, s, kSendBuf, kRecvBuf, {{s, 0, count}},
+                          all_ranks(p, b, e), {}});
+    }
+  }
+  return pl;
+}
+
+Config resolve_config(const Config& in) {
+  Config c = in;
+  if (c.small_max_bytes == 0) c.small_max_bytes = 256 * 1024;
+  if (c.stage_bytes <= 0) c.stage_bytes = 32 * 1024;
+  if (c.stages <= 0) c.stages = 8;
+  if (c.consumer_warps <= 0) c.consumer_warps = 8;
+  if (c.consumer_warps > 31) c.consumer_warps = 31;
+  if (c.ctas_per_sm <= 0) c.ctas_per_sm = 1;
+  if (c.ctas_per_sm > 4) c.ctas_per_sm = 4;
+  if (c.wait_timeout_ms <= 0) c.wait_timeout_ms = 2000.0;
+  return c;
+}
+
+bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv_mod16,
+                const Config& cfg_in, const DeviceDesc& dev, int cta_cap, Lowered* out,
+                std::string* why) {
+  const Config cfg = resolve_config(cfg_in);
+  const int p = plan.nranks;
+  const int es = plan.elem_size;
+  *out = Lowered();
+  out->ntasks = (int)plan.tasks.size();
+
+  // ---- 1. logical -> physical tasks. A shard-out whose only dependency is
+  // the shard-in that produced its source interval is fused with it: the
+  // reduced shard then never leaves the chip (loaded once, stored P times).
+  std::vector<PhysTask> phys;
+  std::vector<char> consumed(plan.tasks.size(), 0);
+  for (size_t i = 0; i < plan.tasks.size(); ++i) {
+    const LogicalTask& t = plan.tasks[i];
+    if (t.kind == kShardOut && t.src_buf == kOwnerShard) {
+      if (t.deps.size() != 1) {
+        *why = "shard-out with an unexpected dependency list";
+        return false;
+      }
+      const LogicalTask& in = plan.tasks[t.deps[0]];
+      if (in.kind != kShardIn || in.dst.size() != 1 || t.src.size() != 1 ||
+          in.dst[0].begin != t.src[0].begin || in.dst[0].end != t.src[0].end ||
+          in.dst[0].rank != t.src[0].rank) {
+        *why = "shard-out does not consume its shard-in's result";
+        return false;
+      }
+      PhysTask pt{};
+      uint64_t b1, b2;
+      if (!selection(in.src, p, es, &pt.src_sel, &pt.src_off, &b1) ||
+          !selection(t.dst, p, es, &pt.dst_sel, &pt.dst_off, &b2) || b1 != b2) {
+        *why = "fused shard task has irregular intervals";
+        return false;
+      }
+      pt.bytes = b1;
+      pt.task = t.shard;
+      consumed[t.deps[0]] = 1;
+      phys.push_back(pt);
+    }
+  }
+  for (size_t i = 0; i < plan.tasks.size(); ++i) {
+    const LogicalTask& t = plan.tasks[i];
+    if (consumed[i] || (t.kind == kShardOut && t.src_buf == kOwnerShard)) continue;
+    PhysTask pt{};
+    uint64_t b1, b2;
+    if (!selection(t.src, p, es, &pt.src_sel, &pt.src_off, &b1) ||
+        !selection(t.dst, p, es, &pt.dst_sel, &pt.dst_off, &b2) || b1 != b2) {
+      *why = "task has irregular intervals";
+      return false;
+    }
+    pt.bytes = b1;
+    pt.task = t.shard;
+    phys.push_back(pt);
+  }
+
+  // ---- 2. alignment split: a task whose selected source and destination
+  // addresses agree mod 16 gets a scalar head, a 16-byte body and a scalar
+  // tail; any other task runs element-wise.
+  std::vector<Window> wins;
+  for (const PhysTask& pt : phys) {
+    if (pt.bytes == 0) continue;
+    int a = -1;
+    bool co = true;
+    auto check = [&](int m) {
+      if (a < 0) a = m;
+      else if (a != m) co = false;
+    };
+    for (int r = 0; r < p; ++r) {
+      if (pt.src_sel < 0 || pt.src_sel == r) check((int)((send_mod16[r] + pt.src_off) & 15));
+      if (pt.dst_sel < 0 || pt.dst_sel == r) check((int)((recv_mod16[r] + pt.dst_off) & 15));
+    }
+    Window w{};
+    w.src_sel = (int16_t)pt.src_sel;
+    w.dst_sel = (int16_t)pt.dst_sel;
+    w.task = (uint16_t)pt.task;
+    w.cta = -1;
+    w.src_off = pt.src_off;
+    w.dst_off = pt.dst_off;
+    if (!co) {
+      w.scalar = 1;
+      push_split(wins, w, pt.bytes, kMaxWindowBytes);
+      continue;
+    }
+    uint64_t head = std::min<uint64_t>(pt.bytes, (uint64_t)((16 - a) & 15));
+    uint64_t body = (pt.bytes - head) & ~(uint64_t)15;
+    uint64_t tail = pt.bytes - head - body;
+    if (head) {
+      w.scalar = 1;
+      push_split(wins, w, head, kMaxWindowBytes);
+      w.src_off += head;
+      w.dst_off += head;
+    }
+    if (body) {
+      w.scalar = 0;
+      push_split(wins, w, body, kMaxWindowBytes);
+      w.src_off += body;
+      w.dst_off += body;
+    }
+    if (tail) {
+      w.scalar = 1;
+      push_split(wins, w, tail, kMaxWindowBytes);
+    }
+  }
+
+  // ---- 3. engine choice
+  int engine = cfg.engine;
+  if (engine == kEngineAuto) {
+    bool small = message_bytes(plan.coll, p, plan.count, es) <= cfg.small_max_bytes;
+    engine = small ? kEngineWarp : kEngineBulk;
+  }
+  if (engine == kEngineWarp && p > 32) engine = kEngineVec;
+  LaunchShape& sh = out->shape;
+  sh.engine = engine;
+  const int max_ctas_total = std::max(1, dev.sm_count) * std::max(1, cfg.ctas_per_sm);
+
+  if (engine == kEngineWarp || engine == kEngineVec) {
+    // merge neighbours that continue each other (same selections, adjacent
+    // offsets): for allreduce this folds the P shard bodies into one window
+    std::vector<Window> m;
+    for (const Window& w : wins) {
+      if (!m.empty()) {
+        Window& b = m.back();
+        if (!b.scalar && !w.scalar && b.src_sel == w.src_sel && b.dst_sel == w.dst_sel &&
+            b.src_off + b.bytes == w.src_off && b.dst_off + b.bytes == w.dst_off &&
+            (uint64_t)b.bytes + w.bytes <= 0xFFFFFFF0ull) {
+          b.bytes += w.bytes;
+          continue;
+        }
+      }
+      m.push_back(w);
+    }
+    out->win = m;
+    out->size_class = (p <= kSmallRanks && (int)m.size() <= kSmallWindows) ? 0 : 1;
+    if ((int)m.size() > kLargeWindows) {
+      *why = "too many windows for the small-message engines";
+      return false;
+    }
+    out->vec_prefix.assign(m.size() + 1, 0);
+    out->elem_prefix.assign(m.size() + 1, 0);
+    for (size_t i = 0; i < m.size(); ++i) {
+      out->vec_prefix[i + 1] = out->vec_prefix[i] + (m[i].scalar ? 0 : m[i].bytes / 16);
+      out->elem_prefix[i + 1] = out->elem_prefix[i] + (m[i].scalar ? m[i].bytes / es : 0);
+    }
+    uint64_t nvec = out->vec_prefix.back();
+    uint64_t nelem = out->elem_prefix.back();
+    const int threads = 256;
+    uint64_t lanes;
+    if (engine == kEngineWarp) {
+      int vpw = 32 / p;  // vectors per warp: one group of P lanes per vector
+      lanes = ceil_div(nvec, (uint64_t)vpw) * 32;
+    } else {
+      lanes = nvec;
+    }
+    lanes = std::max<uint64_t>(lanes, nelem);
+    uint64_t blocks = std::max<uint64_t>(1, ceil_div(lanes, threads));
+    uint64_t cap = (uint64_t)dev.sm_count * 8;
+    if (cta_cap > 0) cap = std::min<uint64_t>(cap, (uint64_t)cta_cap);
+    sh.grid = (int)std::max<uint64_t>(1, std::min(blocks, cap));
+    sh.threads = threads;
+    sh.smem = 0;
+    return true;
+  }
+
+  // ---- 4. bulk engine: chunks, stages, CTAs
+  const int nsrc = (plan.coll == kAllGather) ? 1 : p;
+  int store = cfg.store_mode;
+  if (store == kStoreAuto) store = (plan.coll == kAllGather) ? kStoreBulk : kStoreVec;
+  sh.store_mode = store;
+  uint64_t chunk = ((uint64_t)cfg.stage_bytes / nsrc) & ~(uint64_t)15;
+  chunk = std::min<uint64_t>(chunk, 16384);
+  chunk = std::max<uint64_t>(chunk, 256);
+  const int result_slots = (store == kStoreBulk && plan.coll != kAllGather) ? 2 : 0;
+  int budget = dev.smem_optin;
+  if (dev.smem_per_sm > 0)
+    budget = std::min(budget, dev.smem_per_sm / std::max(1, cfg.ctas_per_sm) - 1024);
+  int stages = 0;
+  for (;;) {
+    int64_t room = (int64_t)budget - 1024 - (int64_t)result_slots * (int64_t)chunk;
+    stages = room > 0 ? (int)std::min<int64_t>(cfg.stages, room / (int64_t)(nsrc * chunk)) : 0;
+    if (stages >= 2 || chunk <= 16) break;
+    chunk = std::max<uint64_t>(16, (chunk / 2) & ~(uint64_t)15);
+  }
+  if (stages < 2) {
+    *why = "shared memory too small for a two-stage pipeline";
+    return false;
+  }
+  stages = std::min(stages, 32);
+  sh.stages = stages;
+  sh.chunk_bytes = (int)chunk;
+  sh.consumer_warps = cfg.consumer_warps;
+  sh.threads = 32 * (1 + cfg.consumer_warps);
+  sh.release_lag = std::max(1, std::min(7, stages / 2));
+  sh.smem = 1024 + (size_t)stages * nsrc * chunk + (size_t)result_slots * chunk;
+
+  std::vector<Window> vecw, scal;
+  uint64_t body = 0, sbytes = 0;
+  for (const Window& w : wins) {
+    if (w.scalar) {
+      scal.push_back(w);
+      sbytes += w.bytes;
+    } else {
+      vecw.push_back(w);
+      body += w.bytes;
+    }
+  }
+  int max_g = max_ctas_total;
+  if (cta_cap > 0) max_g = std::min(max_g, cta_cap);
+  int grid;
+  std::vector<Window> assigned;
+  if (body > 0) {
+    grid = (int)std::min<uint64_t>(max_g, ceil_div(body, chunk));
+    uint64_t per = round_up(ceil_div(body, grid), 16);
+    grid = (int)ceil_div(body, per);
+    // cut the concatenated vector windows into `grid` contiguous pieces
+    uint64_t pos = 0;
+    for (const Window& w : vecw) {
+      uint64_t wb = 0;
+      while (wb < w.bytes) {
+        uint64_t cta = (pos + wb) / per;
+        uint64_t cta_end = (cta + 1) * per;
+        uint64_t n = std::min<uint64_t>(w.bytes - wb, cta_end - (pos + wb));
+        Window piece = w;
+        piece.src_off += wb;
+        piece.dst_off += wb;
+        piece.bytes = (uint32_t)n;
+        piece.cta = (int32_t)cta;
+        assigned.push_back(piece);
+        wb += n;
+      }
+      pos += w.bytes;
+    }
+  } else {
+    grid = 1;
+  }
+  if (!scal.empty()) {
+    uint64_t limit = std::max<uint64_t>(4096, round_up(ceil_div(sbytes, (uint64_t)max_g), es));
+    std::vector<Window> pieces;
+    for (const Window& w : scal) {
+      Window x = w;
+      uint64_t left = w.bytes;
+      while (left > 0) {
+        uint64_t n = std::min<uint64_t>(left, limit);
+        x.bytes = (uint32_t)n;
+        pieces.push_back(x);
+        x.src_off += n;
+        x.dst_off += n;
+        left -= n;
+      }
+    }
+    if (body == 0) grid = (int)std::min<uint64_t>(max_g, pieces.size());
+    for (size_t i = 0; i < pieces.size(); ++i) {
+      pieces[i].cta = (int32_t)(i % (size_t)grid);
+      assigned.push_back(pieces[i]);
+    }
+  }
+  std::stable_sort(assigned.begin(), assigned.end(),
+                   [](const Window& x, const Window& y) { return x.cta < y.cta; });
+  out->win = assigned;
+  out->cta_first.assign(grid + 1, 0);
+  for (const Window& w : assigned) out->cta_first[w.cta + 1]++;
+  for (int i = 0; i < grid; ++i) out->cta_first[i + 1] += out->cta_first[i];
+  sh.grid = grid;
+  return true;
+}
+
+}  // namespace tccl

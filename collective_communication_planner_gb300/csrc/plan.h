@@ -1,0 +1,99 @@
+// Task planner and lowering pass (host only).
+//
+// The planner follows T-CCL's task-based planning ("NCCL M2N vs T-CCL"
+// article, section 2.3): the logical tensor is split into P shards, shard s
+// is owned by rank s, and the planner emits logical tasks {op, executing
+// rank, source intervals, destination intervals, dependencies}. The lowering
+// pass resolves each logical task into physical ones (addresses relative to
+// the call's base pointers, and the transfer mechanism), then cuts them into
+// windows and chunks for one engine (same section, "lower" and "TMA engine").
+#pragma once
+
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace tccl {
+
+// Element interval [begin, end) of one rank's buffer.
+struct Interval {
+  int rank;
+  uint64_t begin;
+  uint64_t end;
+};
+
+enum TaskKind : int {
+  kShardIn = 0,   // load every rank's part of the shard and reduce it at the owner
+  kShardOut = 1,  // take the owner's final shard once and store it to every rank
+};
+
+// Where a task's intervals live.
+enum BufKind : int { kSendBuf = 0, kRecvBuf = 1, kOwnerShard = 2 };
+
+struct LogicalTask {
+  TaskKind kind;
+  int op;           // reduction (shard-in) or -1 (shard-out copies)
+  int exec_rank;    // the shard's owner
+  int shard;
+  BufKind src_buf;
+  BufKind dst_buf;
+  std::vector<Interval> src;
+  std::vector<Interval> dst;
+  std::vector<int> deps;  // indices of tasks that must finish first
+};
+
+struct Plan {
+  int coll = 0;
+  int nranks = 0;
+  int elem_size = 0;
+  int op = 0;
+  uint64_t count = 0;        // the call's count argument
+  uint64_t shard_elems = 0;  // shard length q
+  std::vector<LogicalTask> tasks;
+};
+
+// Splits the collective into logical tasks.
+Plan plan_collective(int coll, int nranks, uint64_t count, int elem_size, int op);
+
+struct DeviceDesc {
+  int sm_count = 0;
+  int smem_optin = 0;   // max dynamic shared memory per block (opt-in)
+  int smem_per_sm = 0;  // shared memory per SM
+};
+
+struct Config {
+  int engine = kEngineAuto;
+  size_t small_max_bytes = 0;
+  int stage_bytes = 0;
+  int stages = 0;
+  int store_mode = kStoreAuto;
+  int consumer_warps = 0;
+  int ctas_per_sm = 0;
+  double wait_timeout_ms = 0;
+};
+
+// Fills zero fields with the library defaults.
+Config resolve_config(const Config& in);
+
+struct Lowered {
+  LaunchShape shape;
+  std::vector<Window> win;           // bulk: sorted by CTA; small engines: in plan order
+  std::vector<uint32_t> cta_first;   // bulk: grid + 1 entries
+  std::vector<uint64_t> vec_prefix;  // small engines: nwin + 1 entries
+  std::vector<uint64_t> elem_prefix; // small engines: nwin + 1 entries
+  int ntasks = 0;
+  int size_class = 0;  // small engines: 0 = (8 ranks, 8 windows), 1 = (64, 194)
+};
+
+// Lowers a plan for the given buffer alignments (address mod 16 of each
+// rank's send and recv buffer). Returns false with a reason when the
+// configuration cannot be lowered (which the API reports as invalid usage).
+bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv_mod16,
+                const Config& cfg, const DeviceDesc& dev, int cta_cap, Lowered* out,
+                std::string* why);
+
+// Per-rank message size the Auto engine choice looks at.
+uint64_t message_bytes(int coll, int nranks, uint64_t count, int elem_size);
+
+}  // namespace tccl

@@ -1,0 +1,221 @@
+/*
+ * tccl — NCCL-semantics collectives over P logical ranks held in one GPU.
+ *
+ * Each of the P ranks is a separate buffer in the same GPU's memory. The
+ * library plans, lowers and runs allreduce, reduce-scatter and all-gather over
+ * those buffers with hand-written sm_103a kernels: a shard-in phase bulk-loads
+ * each rank's chunk into a multi-stage shared-memory pipeline and reduces it
+ * locally in ascending rank order; a shard-out phase stores the reduced shard,
+ * held once on chip, to every destination.
+ *
+ * Source of the semantics: the T-CCL design as described in the "NCCL M2N vs
+ * T-CCL" article (section 2.3 "programming model", 2.4 API table: Group,
+ * allreduce / reducescatter / allgather with NCCL semantics, in-place and
+ * out-of-place, on a stream), and NCCL's own host API (`ncclAllReduce`), as
+ * summarised in the "NCCL Roadmap" post, section "NCCL の API の全体像".
+ *
+ * Conventions for every call below
+ *  - All calls are asynchronous and stream ordered, like NCCL: they enqueue
+ *    work on `stream` and return. Buffers must stay valid until that work
+ *    completes. A null stream is the legacy default stream.
+ *  - The caller owns every buffer. Plain cudaMalloc / framework allocations
+ *    are accepted; nothing is registered (the article's section 2.2, "user
+ *    buffer compatible").
+ *  - The pointer arrays themselves (`sendbufs`, `recvbufs`) are host arrays of
+ *    device pointers, read during the call only; the caller may reuse them on
+ *    return.
+ *  - Every device pointer must be aligned to its element size. Any other
+ *    alignment is accepted; 16-byte co-aligned buffers take the fast path.
+ *  - The library never aborts, traps or prints (unless the environment
+ *    variable TCCL_LOG is set to 1 or 2, which dumps plans to stderr).
+ *  - A group is not thread safe: serialise calls on one group.
+ */
+#ifndef TCCL_H
+#define TCCL_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TCCL_VERSION 1000
+#define TCCL_MAX_RANKS 64
+
+typedef struct tcclGroup* tcclGroup_t;
+
+typedef enum {
+  tcclSuccess = 0,
+  tcclInvalidArgument = 1, /* null/misaligned pointer, bad enum, bad overlap, overflow */
+  tcclInvalidUsage = 2,    /* call not valid in the group's state */
+  tcclCudaError = 3,       /* a CUDA runtime call or kernel launch failed */
+  tcclDeviceTimeout = 4,   /* a device-side wait gave up (reported asynchronously) */
+  tcclInternalError = 5
+} tcclResult_t;
+
+typedef enum { tcclFloat32 = 0, tcclBfloat16 = 1, tcclInt32 = 2 } tcclDataType_t;
+
+/* Element-wise reductions: the add / min / max the article's section 2.1
+ * lists for bulk reductions. Reduction order is always ascending rank. */
+typedef enum { tcclSum = 0, tcclMin = 1, tcclMax = 2 } tcclRedOp_t;
+
+/* Which kernel family runs a call (see tcclConfig_t). */
+typedef enum {
+  tcclEngineAuto = 0,
+  tcclEngineBulk = 1, /* TMA cp.async.bulk pipeline: mbarrier stages, reduce, bulk stores */
+  tcclEngineWarp = 2, /* small-message path: one lane per (vector, rank), shuffle fold */
+  tcclEngineVec = 3   /* plain 128-bit loads/stores, each lane folds all ranks */
+} tcclEngine_t;
+
+typedef enum {
+  tcclStoreAuto = 0,
+  tcclStoreBulk = 1, /* reduced chunk staged once in shared memory, P bulk stores */
+  tcclStoreVec = 2   /* reduced vector held once in registers, P 128-bit stores */
+} tcclStoreMode_t;
+
+/*
+ * Tuning knobs of a group. Defaults come from tcclGroupCreate (which also
+ * reads TCCL_ENGINE, TCCL_SMALL_MAX_BYTES, TCCL_STAGE_BYTES, TCCL_STAGES,
+ * TCCL_STORE_MODE, TCCL_CONSUMER_WARPS, TCCL_CTAS_PER_SM and
+ * TCCL_WAIT_TIMEOUT_MS once). Zero in a field means "library default".
+ */
+typedef struct {
+  int engine;              /* tcclEngine_t */
+  size_t small_max_bytes;  /* Auto picks the small-message path at or below this many bytes per rank buffer */
+  int stage_bytes;         /* bulk engine: shared-memory bytes of one pipeline stage (all sources of one chunk) */
+  int stages;              /* bulk engine: pipeline depth (reduced to what shared memory holds) */
+  int store_mode;          /* tcclStoreMode_t */
+  int consumer_warps;      /* bulk engine: reducing warps per CTA (one more warp issues loads) */
+  int ctas_per_sm;         /* bulk engine: resident CTAs per SM the grid is sized for (1 or 2) */
+  double wait_timeout_ms;  /* device-side bound on every wait before it reports tcclDeviceTimeout */
+} tcclConfig_t;
+
+/* What the last launch on a group looked like. */
+typedef struct {
+  int engine;          /* tcclEngine_t actually used (never Auto); 0 if nothing was launched */
+  int store_mode;      /* tcclStoreMode_t actually used */
+  int ctas;            /* grid size */
+  int threads;         /* threads per CTA */
+  int stages;          /* bulk engine pipeline depth (0 otherwise) */
+  int chunk_bytes;     /* bulk engine bytes per source per chunk (0 otherwise) */
+  int windows;         /* physical windows in the lowered plan */
+  int tasks;           /* logical tasks in the plan */
+  size_t smem_bytes;   /* dynamic shared memory per CTA */
+} tcclLaunchInfo_t;
+
+const char* tcclGetErrorString(tcclResult_t r);
+tcclResult_t tcclGetVersion(int* version);
+
+/*
+ * Create a group of `nranks` logical ranks (1 .. TCCL_MAX_RANKS) on the
+ * current CUDA device (the article's `tcl::Group::create`, single-process
+ * mode). Allocates a few hundred bytes of device memory for the group's
+ * status word and plan tables. Returns tcclInvalidArgument for a bad
+ * `nranks` or null `out`, tcclCudaError if the device cannot be queried.
+ */
+tcclResult_t tcclGroupCreate(int nranks, tcclGroup_t* out);
+
+/* Frees the group and its device memory. Synchronises the device first. */
+tcclResult_t tcclGroupDestroy(tcclGroup_t g);
+
+tcclResult_t tcclGroupGetConfig(tcclGroup_t g, tcclConfig_t* cfg);
+/* Replaces the group's tuning; cached plans are dropped. */
+tcclResult_t tcclGroupSetConfig(tcclGroup_t g, const tcclConfig_t* cfg);
+
+/*
+ * Allreduce (the article's `tcl::allreduce(sendbuf, recvbuf, count, op,
+ * stream)`, one buffer per logical rank):
+ *   recvbufs[r][i] = op-fold over k = 0..P-1 (ascending) of sendbufs[k][i],
+ *   for every rank r and every i < count.
+ * `count` is elements per rank. fp32 and bf16 accumulate in fp32; bf16 is
+ * rounded once at the end, to nearest even. int32 sums wrap.
+ * In-place: recvbufs[r] == sendbufs[r] (per rank; mixing is allowed).
+ * Any other overlap between a recv buffer and another buffer is
+ * tcclInvalidArgument; send buffers may overlap each other.
+ * `cta_cap` > 0 bounds the number of CTAs (and so SMs) the call occupies;
+ * <= 0 means uncapped. count == 0 returns tcclSuccess without a launch.
+ */
+tcclResult_t tcclAllReduce(tcclGroup_t g, const void* const sendbufs[], void* const recvbufs[],
+                           size_t count, tcclDataType_t datatype, tcclRedOp_t op,
+                           cudaStream_t stream, int cta_cap);
+
+/*
+ * Reduce-scatter (the shard-in phase alone):
+ *   recvbufs[r][j] = op-fold over k of sendbufs[k][r*recvcount + j].
+ * Each send buffer holds P*recvcount elements, each recv buffer recvcount.
+ * In-place: recvbufs[r] == sendbufs[r] + r*recvcount elements.
+ */
+tcclResult_t tcclReduceScatter(tcclGroup_t g, const void* const sendbufs[],
+                               void* const recvbufs[], size_t recvcount,
+                               tcclDataType_t datatype, tcclRedOp_t op, cudaStream_t stream,
+                               int cta_cap);
+
+/*
+ * All-gather (the shard-out phase alone: each shard read once, stored to all
+ * P destinations):
+ *   recvbufs[r][k*sendcount + j] = sendbufs[k][j] for every r.
+ * Each send buffer holds sendcount elements, each recv buffer P*sendcount.
+ * In-place: sendbufs[r] == recvbufs[r] + r*sendcount elements.
+ * The datatype only sets the element size.
+ */
+tcclResult_t tcclAllGather(tcclGroup_t g, const void* const sendbufs[], void* const recvbufs[],
+                           size_t sendcount, tcclDataType_t datatype, cudaStream_t stream,
+                           int cta_cap);
+
+/*
+ * Waits for all work on the device, then returns (and clears) the group's
+ * asynchronous status in *async_status: tcclSuccess, or tcclDeviceTimeout if
+ * a kernel gave up on a wait since the last query. Such a kernel skipped the
+ * rest of its work, so its outputs are undefined.
+ */
+tcclResult_t tcclGroupQueryError(tcclGroup_t g, tcclResult_t* async_status);
+
+tcclResult_t tcclGetLastLaunchInfo(tcclGroup_t g, tcclLaunchInfo_t* info);
+
+/*
+ * SM-footprint recorder. While enabled, every CTA of every launch sets the
+ * bit of the SM it ran on; tcclGroupReadSmRecord synchronises the device,
+ * returns the number of distinct SMs seen since the last read and clears the
+ * record. Off by default (it adds one atomic per CTA).
+ */
+tcclResult_t tcclGroupRecordSms(tcclGroup_t g, int enable);
+tcclResult_t tcclGroupReadSmRecord(tcclGroup_t g, int* distinct_sms);
+
+/*
+ * Host-only view of the planner and lowering (no GPU needed). Plans and
+ * lowers one collective for a device with `sm_count` SMs and
+ * `smem_per_block` bytes of opt-in shared memory, as a call with these
+ * pointers would be, without launching anything. `coll` is 0 allreduce,
+ * 1 reduce-scatter, 2 all-gather; `count` is the per-call count argument.
+ * The buffer addresses are only used for their alignment and overlap.
+ * Writes up to `max_windows` windows, eight int64 values each:
+ *   {cta, src_sel, src_off, dst_sel, dst_off, bytes, scalar, task}:
+ * owning CTA (-1 when the engine does not bind
+ * windows to CTAs), source rank or -1 for all ranks, byte offset into the
+ * source buffer(s), destination rank or -1, byte offset into the
+ * destination buffer(s), window bytes, 1 if the window needs the
+ * element-wise (unaligned) path, and the logical task it came from.
+ * *n_windows receives the total count, *info the launch shape.
+ * Argument errors are reported exactly as the collective call would.
+ */
+tcclResult_t tcclPlanInspect(int coll, int nranks, const void* const sendbufs[],
+                             void* const recvbufs[], size_t count, tcclDataType_t datatype,
+                             int cta_cap, int sm_count, int smem_per_block,
+                             const tcclConfig_t* cfg, int64_t* windows, int max_windows,
+                             int* n_windows, int* n_tasks, tcclLaunchInfo_t* info);
+
+/*
+ * Test hook for the bounded-wait error path: while enabled, each bulk-engine
+ * launch makes its first CTA wait on a barrier that nothing signals, with a
+ * `timeout_ms` bound; the CTA then records tcclDeviceTimeout, skips its
+ * remaining work and exits normally (no trap, no fault). Other CTAs finish.
+ */
+tcclResult_t tcclGroupInjectWaitTimeout(tcclGroup_t g, int enable, double timeout_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCCL_H */

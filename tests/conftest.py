@@ -16,3 +16,12 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return ROOT / "tests" / "golden"
+
+
+def _build_everything():
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+_build_everything()

@@ -1,0 +1,321 @@
+"""GPU parity: every engine, collective, dtype and op against the CPU oracle,
+bit for bit, through the C ABI.
+
+Sizes span several chunks per CTA and end in ragged tails; edge cases cover
+P = 1, counts smaller than P, misaligned and mutually misaligned buffers,
+in-place forms, CTA caps, guard zones around every destination, the
+bounded-wait timeout path and CUDA graph replay.
+"""
+import numpy as np
+import pytest
+import torch
+
+import collective_communication_planner_gb300 as tccl
+import datagen
+import oracle
+from gpu_util import DT_CODE, NP_OF, TORCH_OF, Guarded, first_mismatch, same_bits, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+ENGINES = {"bulk": tccl.tcclEngineBulk, "warp": tccl.tcclEngineWarp, "vec": tccl.tcclEngineVec}
+KIND = {"f32": "uniform_f32", "bf16": "normal_bf16", "i32": "int32"}
+
+
+def inputs(dtype, p, n, seed=11):
+    return datagen.rank_buffers(KIND[dtype], seed, p, n)
+
+
+@pytest.fixture(scope="module")
+def groups():
+    made = {}
+
+    def get(p):
+        if p not in made:
+            made[p] = tccl.Group(p)
+        return made[p]
+
+    yield get
+    for g in made.values():
+        g.close()
+
+
+def configure(g, engine, store=tccl.tcclStoreAuto, stage_bytes=0, stages=0):
+    g.set_config(engine=ENGINES[engine] if isinstance(engine, str) else engine,
+                 store_mode=store, stage_bytes=stage_bytes, stages=stages)
+
+
+def run_allreduce(g, xs, dtype, op, cap=0, send_off=0, recv_off=0, in_place=False):
+    p, n = len(xs), xs[0].size
+    sends = [Guarded(n, dtype, send_off) for _ in range(p)]
+    for s, x in zip(sends, xs):
+        s.tensor.copy_(to_device(x))
+    recvs = sends if in_place else [Guarded(n, dtype, recv_off) for _ in range(p)]
+    r = tccl.tcclAllReduce(g.handle, [s.tensor for s in sends], [t.tensor for t in recvs], n,
+                           DT_CODE[dtype], tccl.OPS[op], torch.cuda.current_stream().cuda_stream,
+                           cap)
+    assert r == tccl.tcclSuccess, tccl.tcclGetErrorString(r)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    for t in recvs:
+        assert t.guards_intact()
+    return [t.host() for t in recvs]
+
+
+def assert_ranks_equal(got, exp, what):
+    for r in range(len(exp)):
+        mm = first_mismatch(got[r], exp[r])
+        assert mm is None, f"{what}: rank {r} first mismatch at {mm[0]} ({mm[1]} elements)"
+
+
+# ------------------------------------------------------------------ allreduce
+@pytest.mark.parametrize("engine", ["bulk", "warp", "vec"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("op", ["sum", "min", "max"])
+def test_allreduce_engines_dtypes_ops(groups, engine, dtype, op):
+    for p, n in ((2, 70_001), (3, 1000), (8, 300_007), (5, 17)):
+        g = groups(p)
+        configure(g, engine)
+        xs = inputs(dtype, p, n)
+        exp = oracle.allreduce(xs, dtype, op, nthreads=0)
+        got = run_allreduce(g, xs, dtype, op)
+        assert_ranks_equal(got, exp, f"AR {engine} {dtype} {op} P={p} n={n}")
+
+
+@pytest.mark.parametrize("engine", ["bulk", "warp", "vec"])
+@pytest.mark.parametrize("n", [1, 2, 3, 7, 8, 9, 15, 16, 17, 63, 64, 65, 4095, 4096, 4097])
+def test_allreduce_small_and_ragged_counts(groups, engine, n):
+    for p in (1, 2, 8):
+        g = groups(p)
+        configure(g, engine)
+        xs = inputs("bf16", p, n, seed=n)
+        exp = oracle.allreduce(xs, "bf16", "sum")
+        assert_ranks_equal(run_allreduce(g, xs, "bf16", "sum"), exp, f"{engine} P={p} n={n}")
+
+
+@pytest.mark.parametrize("engine", ["bulk", "vec", "warp"])
+@pytest.mark.parametrize("offs", [(4, 4), (8, 8), (12, 12), (4, 8), (0, 4), (2, 2)])
+def test_allreduce_misaligned_buffers(groups, engine, offs):
+    p, n = 4, 50_001
+    dtype = "bf16" if offs[0] % 4 or offs[1] % 4 else "f32"
+    g = groups(p)
+    configure(g, engine)
+    xs = inputs(dtype, p, n)
+    exp = oracle.allreduce(xs, dtype, "sum")
+    got = run_allreduce(g, xs, dtype, "sum", send_off=offs[0], recv_off=offs[1])
+    assert_ranks_equal(got, exp, f"misaligned {offs}")
+
+
+@pytest.mark.parametrize("engine", ["bulk", "warp"])
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+def test_allreduce_in_place(groups, engine, dtype):
+    p, n = 8, 123_457
+    g = groups(p)
+    configure(g, engine)
+    xs = inputs(dtype, p, n)
+    exp = oracle.allreduce(xs, dtype, "sum")
+    got = run_allreduce(g, xs, dtype, "sum", in_place=True)
+    assert_ranks_equal(got, exp, "in place")
+
+
+@pytest.mark.parametrize("store", [tccl.tcclStoreBulk, tccl.tcclStoreVec])
+@pytest.mark.parametrize("stage_bytes,stages", [(0, 0), (4096, 2), (65536, 3), (16384, 12)])
+def test_bulk_store_modes_and_pipeline_shapes(groups, store, stage_bytes, stages):
+    p, n = 4, 1_000_003
+    g = groups(p)
+    configure(g, "bulk", store=store, stage_bytes=stage_bytes, stages=stages)
+    xs = inputs("bf16", p, n)
+    exp = oracle.allreduce(xs, "bf16", "sum", nthreads=0)
+    got = run_allreduce(g, xs, "bf16", "sum")
+    info = g.last_launch()
+    assert info["engine"] == tccl.tcclEngineBulk and info["store_mode"] == store
+    assert_ranks_equal(got, exp, f"store {store} stage {stage_bytes}x{stages}")
+
+
+@pytest.mark.parametrize("cap", [1, 3, 8, 16, 32])
+def test_cta_cap_results_and_sm_footprint(groups, cap):
+    p, n = 8, 2_000_001
+    g = groups(p)
+    configure(g, "bulk")
+    xs = inputs("bf16", p, n)
+    exp = oracle.allreduce(xs, "bf16", "sum", nthreads=0)
+    g.read_sm_record()
+    g.record_sms(True)
+    got = run_allreduce(g, xs, "bf16", "sum", cap=cap)
+    sms = g.read_sm_record()
+    g.record_sms(False)
+    assert g.last_launch()["ctas"] == cap
+    assert 1 <= sms <= cap
+    assert_ranks_equal(got, exp, f"cap {cap}")
+
+
+def test_one_rank_copy_and_count_zero(groups):
+    g = groups(1)
+    configure(g, tccl.tcclEngineAuto)
+    x = inputs("f32", 1, 1000)
+    assert_ranks_equal(run_allreduce(g, x, "f32", "sum"), x, "P=1 copy")
+    t = torch.zeros(4, device="cuda")
+    assert tccl.tcclAllReduce(g.handle, [t], [t], 0, 0, 0, 0, 0) == tccl.tcclSuccess
+
+
+def test_same_send_buffer_for_every_rank(groups):
+    p, n = 8, 100_000
+    g = groups(p)
+    configure(g, "bulk")
+    small = (np.arange(n) % 61 - 30).astype(np.float32)
+    src = to_device(small)
+    recvs = [torch.empty_like(src) for _ in range(p)]
+    g.all_reduce([src] * p, recvs)
+    torch.cuda.synchronize()
+    for r in recvs:
+        assert np.array_equal(to_host(r), (p * small).astype(np.float32))
+
+
+# ------------------------------------------------------------------ reduce-scatter / all-gather
+@pytest.mark.parametrize("engine", ["bulk", "warp", "vec"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+def test_reduce_scatter_then_allgather(groups, engine, dtype):
+    for p, rc in ((4, 100_003), (2, 9), (8, 4096), (3, 77_777)):
+        g = groups(p)
+        configure(g, engine)
+        xs = inputs(dtype, p, p * rc)
+        exp_rs = oracle.reduce_scatter(xs, dtype, "sum", nthreads=0)
+        exp_ar = oracle.allreduce(xs, dtype, "sum", nthreads=0)
+        sends = [to_device(x) for x in xs]
+        parts = [Guarded(rc, dtype) for _ in range(p)]
+        g.reduce_scatter(sends, [t.tensor for t in parts], op="sum")
+        gathered = [Guarded(p * rc, dtype) for _ in range(p)]
+        g.all_gather([t.tensor for t in parts], [t.tensor for t in gathered])
+        torch.cuda.synchronize()
+        assert g.query_error() == tccl.tcclSuccess
+        assert all(t.guards_intact() for t in parts + gathered)
+        assert_ranks_equal([t.host() for t in parts], exp_rs, f"RS {engine} {dtype} P={p}")
+        assert_ranks_equal([t.host() for t in gathered], exp_ar, f"RS+AG {engine} {dtype} P={p}")
+
+
+@pytest.mark.parametrize("engine", ["bulk", "warp", "vec"])
+@pytest.mark.parametrize("op", ["min", "max"])
+def test_reduce_scatter_min_max(groups, engine, op):
+    p, rc = 8, 33_333
+    g = groups(p)
+    configure(g, engine)
+    xs = inputs("f32", p, p * rc)
+    exp = oracle.reduce_scatter(xs, "f32", op)
+    sends = [to_device(x) for x in xs]
+    parts = [torch.empty(rc, dtype=torch.float32, device="cuda") for _ in range(p)]
+    g.reduce_scatter(sends, parts, op=op)
+    torch.cuda.synchronize()
+    assert_ranks_equal([to_host(t) for t in parts], exp, f"RS {op}")
+
+
+@pytest.mark.parametrize("engine", ["bulk", "warp", "vec"])
+@pytest.mark.parametrize("store", [tccl.tcclStoreBulk, tccl.tcclStoreVec])
+def test_allgather_store_modes(groups, engine, store):
+    p, sc = 8, 250_001
+    g = groups(p)
+    configure(g, engine, store=store)
+    xs = inputs("bf16", p, sc)
+    exp = oracle.allgather(xs)
+    recvs = [Guarded(p * sc, "bf16") for _ in range(p)]
+    g.all_gather([to_device(x) for x in xs], [t.tensor for t in recvs])
+    torch.cuda.synchronize()
+    assert all(t.guards_intact() for t in recvs)
+    assert_ranks_equal([t.host() for t in recvs], exp, f"AG {engine} store {store}")
+
+
+@pytest.mark.parametrize("engine", ["bulk", "warp", "vec"])
+def test_reduce_scatter_and_allgather_in_place(groups, engine):
+    p, n = 4, 10_007
+    g = groups(p)
+    configure(g, engine)
+    xs = inputs("f32", p, p * n)
+    exp_rs = oracle.reduce_scatter(xs, "f32", "sum")
+    bufs = [to_device(x) for x in xs]
+    # reduce-scatter in place: rank r's result lands in block r of its send buffer
+    tccl_r = tccl.tcclReduceScatter(g.handle, bufs, [b[r * n:] for r, b in enumerate(bufs)], n,
+                                    0, 0, torch.cuda.current_stream().cuda_stream, 0)
+    assert tccl_r == tccl.tcclSuccess
+    torch.cuda.synchronize()
+    for r in range(p):
+        assert same_bits(to_host(bufs[r][r * n:(r + 1) * n]), exp_rs[r])
+    # all-gather in place: rank r's input is block r of its recv buffer
+    exp_ag = oracle.allgather(exp_rs)
+    r2 = tccl.tcclAllGather(g.handle, [b[r * n:] for r, b in enumerate(bufs)], bufs, n, 0,
+                            torch.cuda.current_stream().cuda_stream, 0)
+    assert r2 == tccl.tcclSuccess
+    torch.cuda.synchronize()
+    assert_ranks_equal([to_host(b) for b in bufs], exp_ag, "AG in place")
+
+
+# ------------------------------------------------------------------ runtime behaviour
+def test_bounded_wait_timeout_is_reported_and_context_survives(groups):
+    p, n = 4, 1 << 20
+    g = groups(p)
+    configure(g, "bulk")
+    xs = inputs("f32", p, n)
+    sends = [to_device(x) for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    assert tccl.tcclGroupInjectWaitTimeout(g.handle, True, 50.0) == tccl.tcclSuccess
+    g.all_reduce(sends, recvs)
+    assert g.query_error() == tccl.tcclDeviceTimeout
+    assert g.query_error() == tccl.tcclSuccess  # cleared by the read
+    assert tccl.tcclGroupInjectWaitTimeout(g.handle, False, 0.0) == tccl.tcclSuccess
+    g.all_reduce(sends, recvs)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    exp = oracle.allreduce(xs, "f32", "sum", nthreads=0)
+    assert_ranks_equal([to_host(r) for r in recvs], exp, "after timeout")
+
+
+def test_graph_capture_replay(groups):
+    p, n = 8, 8192 * 8
+    g = groups(p)
+    configure(g, tccl.tcclEngineAuto)
+    xs = inputs("bf16", p, n)
+    sends = [to_device(x) for x in xs]
+    recvs = [torch.zeros_like(s) for s in sends]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g.all_reduce(sends, recvs)  # plans the shape outside the capture
+    torch.cuda.synchronize()
+    for r in recvs:
+        r.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        g.all_reduce(sends, recvs, stream=s.cuda_stream)
+    for r in recvs:
+        r.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    exp = oracle.allreduce(xs, "bf16", "sum")
+    assert_ranks_equal([to_host(r) for r in recvs], exp, "graph replay")
+
+
+def test_runs_on_a_side_stream(groups):
+    p, n = 4, 500_000
+    g = groups(p)
+    configure(g, "bulk")
+    xs = inputs("bf16", p, n)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        sends = [to_device(x) for x in xs]
+        recvs = [torch.empty_like(t) for t in sends]
+        g.all_reduce(sends, recvs)
+    s.synchronize()
+    exp = oracle.allreduce(xs, "bf16", "sum")
+    assert_ranks_equal([to_host(r) for r in recvs], exp, "side stream")
+
+
+def test_invalid_arguments_on_device(groups):
+    g = groups(2)
+    a = torch.zeros(64, device="cuda")
+    b = torch.zeros(64, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    # overlapping recv buffers
+    assert tccl.tcclAllReduce(g.handle, [a, b], [a[:32], a[16:48]], 32, 0, 0, st, 0) == \
+        tccl.tcclInvalidArgument
+    # bad op / dtype
+    assert tccl.tcclAllReduce(g.handle, [a, b], [a, b], 64, 0, 5, st, 0) == tccl.tcclInvalidArgument
+    assert tccl.tcclAllReduce(g.handle, [a, b], [a, b], 64, 9, 0, st, 0) == tccl.tcclInvalidArgument
+    # misaligned for the element size
+    assert tccl.tcclAllReduce(g.handle, [a.data_ptr() + 2, b], [a, b], 8, 0, 0, st, 0) == \
+        tccl.tcclInvalidArgument

@@ -1,0 +1,279 @@
+"""Planner and lowering, checked on the host through tcclPlanInspect.
+
+Invariants (no GPU needed):
+  * every destination byte is written by exactly one window, and from the
+    right source bytes (AR: same offset; RS: shard s of every send buffer;
+    AG: rank k's send buffer into block k);
+  * body windows are 16-byte co-aligned in every buffer they touch and a
+    multiple of 16 bytes; edges and non co-aligned tasks run element-wise;
+  * the bulk engine never uses more CTAs than the cap, windows are grouped by
+    CTA, and the pipeline fits in shared memory;
+  * logical tasks: AR = P shard-ins + P shard-outs (each after its shard-in),
+    RS = P shard-ins, AG = P shard-outs;
+  * argument validation matches the header.
+"""
+import itertools
+
+import pytest
+
+import collective_communication_planner_gb300 as tccl
+
+AR, RS, AG = tccl.COLL_ALLREDUCE, tccl.COLL_REDUCE_SCATTER, tccl.COLL_ALLGATHER
+ES = {tccl.tcclFloat32: 4, tccl.tcclBfloat16: 2, tccl.tcclInt32: 4}
+BASE = 1 << 40  # fake device addresses, far apart
+
+
+def bufs(p, nbytes_send, nbytes_recv, send_mis=0, recv_mis=0, in_place=None, coll=AR,
+         shard_bytes=0):
+    stride = 1 << 34
+    send = [BASE + 2 * r * stride + (send_mis if isinstance(send_mis, int) else send_mis[r])
+            for r in range(p)]
+    recv = [BASE + (2 * r + 1) * stride + (recv_mis if isinstance(recv_mis, int) else recv_mis[r])
+            for r in range(p)]
+    if in_place:
+        if coll == AR:
+            recv = list(send)
+        elif coll == RS:
+            recv = [send[r] + r * shard_bytes for r in range(p)]
+        else:
+            send = [recv[r] + r * shard_bytes for r in range(p)]
+    return send, recv
+
+
+def cfg(engine=0, store=0, stage_bytes=0, stages=0):
+    c = tccl.tcclConfig_t()
+    c.engine = engine
+    c.store_mode = store
+    c.stage_bytes = stage_bytes
+    c.stages = stages
+    return c
+
+
+def inspect(coll, p, count, dt, send, recv, cap=0, engine=0, sm=152, smem=232448,
+            max_windows=8192, **kw):
+    r, wins, ntasks, info = tccl.tcclPlanInspect(coll, p, send, recv, count, dt, cap, sm, smem,
+                                                 cfg(engine, **kw), max_windows=max_windows)
+    return r, wins, ntasks, info
+
+
+def check_cover(coll, p, count, es, send, recv, wins, info):
+    """Exactly-once coverage of every destination byte with the right source."""
+    if coll == AR:
+        dst_len = count * es
+    elif coll == RS:
+        dst_len = count * es
+    else:
+        dst_len = p * count * es
+    covered = {r: [] for r in range(p)}
+    for w in wins:
+        assert w["bytes"] > 0 and w["bytes"] % es == 0
+        dranks = range(p) if w["dst_sel"] < 0 else [w["dst_sel"]]
+        sranks = range(p) if w["src_sel"] < 0 else [w["src_sel"]]
+        for d in dranks:
+            covered[d].append((w["dst_off"], w["dst_off"] + w["bytes"]))
+        if coll == AR:
+            assert w["src_sel"] == -1 and w["dst_sel"] == -1 or p == 1
+            assert w["src_off"] == w["dst_off"]
+        elif coll == RS:
+            s = w["dst_sel"] if p > 1 else 0
+            assert w["src_sel"] == -1 or p == 1
+            assert w["src_off"] == s * count * es + w["dst_off"]
+        else:
+            k = w["src_sel"] if p > 1 else 0
+            assert w["dst_sel"] == -1 or p == 1
+            assert w["dst_off"] == k * count * es + w["src_off"]
+        if not w["scalar"]:
+            assert w["bytes"] % 16 == 0
+            for s in sranks:
+                assert (send[s] + w["src_off"]) % 16 == 0
+            for d in dranks:
+                assert (recv[d] + w["dst_off"]) % 16 == 0
+    for r in range(p):
+        iv = sorted(covered[r])
+        pos = 0
+        for b, e in iv:
+            assert b == pos, (r, b, pos)
+            pos = e
+        assert pos == dst_len
+    if info.engine == tccl.tcclEngineBulk:
+        ctas = [w["cta"] for w in wins]
+        assert ctas == sorted(ctas)
+        assert min(ctas) >= 0 and max(ctas) < info.ctas
+        assert info.smem_bytes <= 232448
+        assert info.stages >= 2 and info.chunk_bytes % 16 == 0
+
+
+CASES = list(itertools.product([AR, RS, AG], [1, 2, 3, 4, 8, 64],
+                               [0, 1, 7, 8, 1000, 4096 + 3, 1 << 20],
+                               [tccl.tcclFloat32, tccl.tcclBfloat16]))
+
+
+@pytest.mark.parametrize("coll,p,count,dt", CASES)
+@pytest.mark.parametrize("engine", [tccl.tcclEngineBulk, tccl.tcclEngineWarp, tccl.tcclEngineVec])
+def test_exact_cover_aligned(coll, p, count, dt, engine):
+    es = ES[dt]
+    send, recv = bufs(p, 0, 0)
+    r, wins, ntasks, info = inspect(coll, p, count, dt, send, recv, engine=engine)
+    assert r == tccl.tcclSuccess
+    if count == 0:
+        assert wins == [] and ntasks == 0
+        return
+    check_cover(coll, p, count, es, send, recv, wins, info)
+
+
+@pytest.mark.parametrize("coll", [AR, RS, AG])
+@pytest.mark.parametrize("mis", [(4, 4), (8, 8), (4, 12), (2, 2), (6, 6), "mixed"])
+@pytest.mark.parametrize("engine", [tccl.tcclEngineBulk, tccl.tcclEngineVec])
+def test_exact_cover_misaligned(coll, mis, engine):
+    p, count, dt = 4, 10_001, tccl.tcclBfloat16
+    if mis == "mixed":
+        send, recv = bufs(p, 0, 0, send_mis=[0, 2, 4, 6], recv_mis=[2, 2, 2, 2])
+    else:
+        send, recv = bufs(p, 0, 0, send_mis=mis[0], recv_mis=mis[1])
+    r, wins, _, info = inspect(coll, p, count, dt, send, recv, engine=engine)
+    assert r == tccl.tcclSuccess
+    check_cover(coll, p, count, 2, send, recv, wins, info)
+    if mis != "mixed" and mis[0] == mis[1] and coll == AR:
+        # co-aligned: at most a scalar head and tail per shard
+        assert sum(w["bytes"] for w in wins if w["scalar"]) <= 2 * 16 * p
+    if mis == (4, 12) and coll == AR:
+        assert all(w["scalar"] for w in wins)
+
+
+@pytest.mark.parametrize("coll", [AR, RS, AG])
+def test_exact_cover_in_place(coll):
+    p, count, dt = 8, 33_333, tccl.tcclFloat32
+    send, recv = bufs(p, 0, 0, in_place=True, coll=coll, shard_bytes=count * 4)
+    r, wins, _, info = inspect(coll, p, count, dt, send, recv, engine=tccl.tcclEngineBulk)
+    assert r == tccl.tcclSuccess
+    check_cover(coll, p, count, 4, send, recv, wins, info)
+
+
+@pytest.mark.parametrize("cap", [1, 2, 8, 9, 16, 32, 151, 152, 1000])
+def test_cta_cap_bounds_the_grid(cap):
+    p, count = 8, 64 << 20
+    send, recv = bufs(p, 0, 0)
+    for engine in (tccl.tcclEngineBulk, tccl.tcclEngineVec, tccl.tcclEngineWarp):
+        r, wins, _, info = inspect(AR, p, count, tccl.tcclBfloat16, send, recv, cap=cap,
+                                   engine=engine, max_windows=4096)
+        assert r == tccl.tcclSuccess
+        assert 1 <= info.ctas <= min(cap, 152 * 8)
+        if engine == tccl.tcclEngineBulk:
+            assert info.ctas == min(cap, 152)
+            check_cover(AR, p, count, 2, send, recv, wins, info)
+
+
+def test_bulk_pieces_are_balanced():
+    p, count = 8, 64 << 20
+    send, recv = bufs(p, 0, 0)
+    r, wins, _, info = inspect(AR, p, count, tccl.tcclBfloat16, send, recv,
+                               engine=tccl.tcclEngineBulk)
+    per = {}
+    for w in wins:
+        per[w["cta"]] = per.get(w["cta"], 0) + w["bytes"]
+    sizes = sorted(per.values())
+    assert info.ctas == 152 and len(per) == 152
+    assert sizes[-1] - sizes[0] <= sizes[-1] // 100 + 16
+
+
+def test_task_structure():
+    p = 4
+    send, recv = bufs(p, 0, 0)
+    for coll, exp in ((AR, 2 * p), (RS, p), (AG, p)):
+        r, _, ntasks, info = inspect(coll, p, 1000, tccl.tcclFloat32, send, recv)
+        assert r == 0 and ntasks == exp and info.tasks == exp
+    # allreduce with fewer elements than ranks: empty shards get no tasks
+    r, wins, ntasks, _ = inspect(AR, 8, 3, tccl.tcclFloat32, *bufs(8, 0, 0))
+    assert r == 0 and ntasks == 2
+
+
+def test_auto_engine_choice():
+    p = 8
+    send, recv = bufs(p, 0, 0)
+    r, _, _, info = inspect(AR, p, 8192, tccl.tcclBfloat16, send, recv)  # 16 KiB per rank
+    assert info.engine == tccl.tcclEngineWarp
+    r, _, _, info = inspect(AR, p, 64 << 20, tccl.tcclBfloat16, send, recv)
+    assert info.engine == tccl.tcclEngineBulk
+    r, _, _, info = inspect(AR, 40, 1024, tccl.tcclFloat32, *bufs(40, 0, 0),
+                            engine=tccl.tcclEngineWarp)
+    assert info.engine == tccl.tcclEngineVec  # more ranks than lanes
+
+
+def test_pipeline_shape_follows_shared_memory():
+    send, recv = bufs(8, 0, 0)
+    r, _, _, info = inspect(AR, 8, 1 << 24, tccl.tcclBfloat16, send, recv,
+                            engine=tccl.tcclEngineBulk, stage_bytes=32768, stages=32)
+    assert info.chunk_bytes == 4096 and info.stages == (232448 - 1024) // 32768
+    r, _, _, small = inspect(AR, 8, 1 << 24, tccl.tcclBfloat16, send, recv,
+                             engine=tccl.tcclEngineBulk, smem=48 * 1024)
+    assert small.smem_bytes <= 48 * 1024 and small.stages >= 2
+
+
+# ------------------------------------------------------------------ validation
+def test_rejects_null_and_misaligned_pointers():
+    p = 2
+    send, recv = bufs(p, 0, 0)
+    for coll in (AR, RS, AG):
+        r, *_ = inspect(coll, p, 16, tccl.tcclFloat32, [send[0], 0], recv)
+        assert r == tccl.tcclInvalidArgument
+        r, *_ = inspect(coll, p, 16, tccl.tcclFloat32, send, [recv[0] + 2, recv[1]])
+        assert r == tccl.tcclInvalidArgument
+        r, *_ = inspect(coll, p, 16, tccl.tcclBfloat16, send, [recv[0] + 2, recv[1]])
+        assert r == tccl.tcclSuccess
+
+
+def test_rejects_bad_enums_and_rank_counts():
+    send, recv = bufs(2, 0, 0)
+    r, *_ = inspect(AR, 2, 16, 7, send, recv)
+    assert r == tccl.tcclInvalidArgument
+    r, *_ = tccl.tcclPlanInspect(3, 2, send, recv, 16, 0)
+    assert r == tccl.tcclInvalidArgument
+    r, *_ = tccl.tcclPlanInspect(AR, 0, [], [], 16, 0)
+    assert r == tccl.tcclInvalidArgument
+    r, *_ = tccl.tcclPlanInspect(AR, 65, [BASE] * 65, [BASE] * 65, 16, 0)
+    assert r == tccl.tcclInvalidArgument
+
+
+def test_overlap_rules():
+    p, count, es = 4, 1000, 4
+    send, recv = bufs(p, 0, 0)
+    # recv overlapping another rank's recv
+    bad = list(recv)
+    bad[1] = recv[0] + 64
+    assert inspect(AR, p, count, 0, send, bad)[0] == tccl.tcclInvalidArgument
+    # recv partially overlapping its own send (not the in-place form)
+    bad = list(recv)
+    bad[2] = send[2] + 16
+    assert inspect(AR, p, count, 0, send, bad)[0] == tccl.tcclInvalidArgument
+    # recv overlapping another rank's send
+    bad = list(recv)
+    bad[0] = send[1]
+    assert inspect(AR, p, count, 0, send, bad)[0] == tccl.tcclInvalidArgument
+    # send buffers may alias each other (read only)
+    assert inspect(AR, p, count, 0, [send[0]] * p, recv)[0] == tccl.tcclSuccess
+    # in-place forms are accepted; mixing in-place and out-of-place too
+    mixed = list(recv)
+    mixed[1] = send[1]
+    assert inspect(AR, p, count, 0, send, mixed)[0] == tccl.tcclSuccess
+    s, r_ = bufs(p, 0, 0, in_place=True, coll=RS, shard_bytes=count * es)
+    assert inspect(RS, p, count, 0, s, r_)[0] == tccl.tcclSuccess
+    r_bad = list(r_)
+    r_bad[1] = s[1]  # shard 0 of rank 1's send, not shard 1
+    assert inspect(RS, p, count, 0, s, r_bad)[0] == tccl.tcclInvalidArgument
+    s, r_ = bufs(p, 0, 0, in_place=True, coll=AG, shard_bytes=count * es)
+    assert inspect(AG, p, count, 0, s, r_)[0] == tccl.tcclSuccess
+    s_bad = list(s)
+    s_bad[0] = r_[0] + 4
+    assert inspect(AG, p, count, 0, s_bad, r_)[0] == tccl.tcclInvalidArgument
+
+
+def test_count_zero_is_success_without_work():
+    send, recv = bufs(4, 0, 0)
+    r, wins, nt, info = inspect(AR, 4, 0, 0, send, recv)
+    assert r == tccl.tcclSuccess and wins == [] and nt == 0 and info.ctas == 0
+
+
+def test_count_overflow_rejected():
+    send, recv = bufs(8, 0, 0)
+    r, *_ = inspect(RS, 8, (1 << 62), 0, send, recv)
+    assert r == tccl.tcclInvalidArgument
