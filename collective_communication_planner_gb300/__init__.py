@@ -74,6 +74,7 @@ def _open():
                                 ctypes.POINTER(ctypes.c_int64), i, ctypes.POINTER(i),
                                 ctypes.POINTER(i), ctypes.POINTER(tcclLaunchInfo_t)]),
         "tcclGroupInjectWaitTimeout": (i, [vp, i, ctypes.c_double]),
+        "tcclAllReduceNoAlloc": (i, [i, pvp, pvp, sz, i, i, vp, i]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -88,7 +89,7 @@ EXPORTED = ("tcclGetErrorString", "tcclGetVersion", "tcclGroupCreate", "tcclGrou
             "tcclGroupGetConfig", "tcclGroupSetConfig", "tcclAllReduce", "tcclReduceScatter",
             "tcclAllGather", "tcclGroupQueryError", "tcclGetLastLaunchInfo",
             "tcclGroupRecordSms", "tcclGroupReadSmRecord", "tcclPlanInspect",
-            "tcclGroupInjectWaitTimeout")
+            "tcclGroupInjectWaitTimeout", "tcclAllReduceNoAlloc")
 
 
 def _ptr(x) -> int:
@@ -176,6 +177,15 @@ def tcclGetLastLaunchInfo(group):
     info = tcclLaunchInfo_t()
     r = _lib.tcclGetLastLaunchInfo(group, ctypes.byref(info))
     return r, info
+
+
+def tcclAllReduceNoAlloc(nranks, sendbufs, recvbufs, count, datatype, op, stream=None,
+                         cta_cap=0) -> int:
+    """Allreduce without a group, for callers that cannot allocate GPU memory
+    (its scratch is a static device array; see include/tccl.h)."""
+    sp, _k1 = _ptr_array(sendbufs)
+    rp, _k2 = _ptr_array(recvbufs)
+    return _lib.tcclAllReduceNoAlloc(nranks, sp, rp, count, datatype, op, _stream(stream), cta_cap)
 
 
 def tcclGroupRecordSms(group, enable: bool) -> int:

@@ -20,7 +20,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 HOST_SOURCES = ["api.cpp", "plan.cpp"]
 CUDA_SOURCES = ["kernels_bulk.cu", "kernels_small_ar.cu", "kernels_small_rs.cu",
-                "kernels_small_ag.cu"]
+                "kernels_small_ag.cu", "no_alloc.cu"]
 
 
 def _cuda_home() -> Path:

@@ -19,6 +19,56 @@
 
 using namespace tccl;
 
+namespace tccl {
+
+namespace {
+bool ranges_overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb) {
+  if (na == 0 || nb == 0) return false;
+  return a < b + nb && b < a + na;
+}
+int elem_size_of_dtype(int dtype) { return dtype == kBF16 ? 2 : 4; }
+}  // namespace
+
+// Argument rules shared by every collective entry point (see plan.h).
+int validate_collective_args(int coll, int nranks, const void* const* send, void* const* recv,
+                             size_t count, int dtype, int op) {
+  if (coll < kAllReduce || coll > kAllGather) return tcclInvalidArgument;
+  if (nranks < 1 || nranks > TCCL_MAX_RANKS) return tcclInvalidArgument;
+  if (dtype < kF32 || dtype > kI32) return tcclInvalidArgument;
+  if (coll != kAllGather && (op < kSum || op > kMax)) return tcclInvalidArgument;
+  if (!send || !recv) return tcclInvalidArgument;
+  if (count == 0) return tcclSuccess;
+  const int es = elem_size_of_dtype(dtype);
+  const uint64_t big = (uint64_t)nranks * (uint64_t)es;
+  if (count > (SIZE_MAX / 4) / big) return tcclInvalidArgument;
+  const size_t sbytes = (coll == kReduceScatter ? nranks * count : count) * es;
+  const size_t rbytes = (coll == kAllGather ? nranks * count : count) * es;
+  const size_t shard_bytes = count * es;
+  for (int r = 0; r < nranks; ++r) {
+    if (!send[r] || !recv[r]) return tcclInvalidArgument;
+    if (((uintptr_t)send[r] % es) || ((uintptr_t)recv[r] % es)) return tcclInvalidArgument;
+  }
+  for (int r = 0; r < nranks; ++r) {
+    const uintptr_t rr = (uintptr_t)recv[r];
+    const uintptr_t sr = (uintptr_t)send[r];
+    // the recv buffer against its own rank's send buffer: in place the NCCL
+    // way, or disjoint
+    bool in_place = false;
+    if (coll == kAllReduce) in_place = (rr == sr);
+    if (coll == kReduceScatter) in_place = (rr == sr + r * shard_bytes);
+    if (coll == kAllGather) in_place = (sr == rr + r * shard_bytes);
+    if (!in_place && ranges_overlap(rr, rbytes, sr, sbytes)) return tcclInvalidArgument;
+    for (int k = 0; k < nranks; ++k) {
+      if (k == r) continue;
+      if (ranges_overlap(rr, rbytes, (uintptr_t)recv[k], rbytes)) return tcclInvalidArgument;
+      if (ranges_overlap(rr, rbytes, (uintptr_t)send[k], sbytes)) return tcclInvalidArgument;
+    }
+  }
+  return tcclSuccess;
+}
+
+}  // namespace tccl
+
 namespace {
 
 int log_level() {
@@ -83,49 +133,6 @@ void fill_small_ptrs(std::vector<unsigned char>* buf, int nranks, const void* co
     a->p.dst[r] = recv[r];
   }
   a->sm_mask = sm_mask;
-}
-
-bool ranges_overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb) {
-  if (na == 0 || nb == 0) return false;
-  return a < b + nb && b < a + na;
-}
-
-// Argument rules shared by the collectives and tcclPlanInspect.
-tcclResult_t validate(int coll, int nranks, const void* const* send, void* const* recv,
-                      size_t count, int dtype, int op) {
-  if (coll < kAllReduce || coll > kAllGather) return tcclInvalidArgument;
-  if (nranks < 1 || nranks > TCCL_MAX_RANKS) return tcclInvalidArgument;
-  if (dtype < kF32 || dtype > kI32) return tcclInvalidArgument;
-  if (coll != kAllGather && (op < kSum || op > kMax)) return tcclInvalidArgument;
-  if (!send || !recv) return tcclInvalidArgument;
-  if (count == 0) return tcclSuccess;
-  const int es = elem_size_of(dtype);
-  const uint64_t big = (uint64_t)nranks * (uint64_t)es;
-  if (count > (SIZE_MAX / 4) / big) return tcclInvalidArgument;
-  const size_t sbytes = (coll == kReduceScatter ? nranks * count : count) * es;
-  const size_t rbytes = (coll == kAllGather ? nranks * count : count) * es;
-  const size_t shard_bytes = count * es;
-  for (int r = 0; r < nranks; ++r) {
-    if (!send[r] || !recv[r]) return tcclInvalidArgument;
-    if (((uintptr_t)send[r] % es) || ((uintptr_t)recv[r] % es)) return tcclInvalidArgument;
-  }
-  for (int r = 0; r < nranks; ++r) {
-    const uintptr_t rr = (uintptr_t)recv[r];
-    const uintptr_t sr = (uintptr_t)send[r];
-    // the recv buffer against its own rank's send buffer: in place the NCCL
-    // way, or disjoint
-    bool in_place = false;
-    if (coll == kAllReduce) in_place = (rr == sr);
-    if (coll == kReduceScatter) in_place = (rr == sr + r * shard_bytes);
-    if (coll == kAllGather) in_place = (sr == rr + r * shard_bytes);
-    if (!in_place && ranges_overlap(rr, rbytes, sr, sbytes)) return tcclInvalidArgument;
-    for (int k = 0; k < nranks; ++k) {
-      if (k == r) continue;
-      if (ranges_overlap(rr, rbytes, (uintptr_t)recv[k], rbytes)) return tcclInvalidArgument;
-      if (ranges_overlap(rr, rbytes, (uintptr_t)send[k], sbytes)) return tcclInvalidArgument;
-    }
-  }
-  return tcclSuccess;
 }
 
 // Nothing to move: one rank, in place.
@@ -295,7 +302,7 @@ tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* con
 tcclResult_t run_collective(tcclGroup* g, int coll, const void* const* send, void* const* recv,
                             size_t count, int dtype, int op, cudaStream_t stream, int cap) {
   if (!g) return tcclInvalidArgument;
-  tcclResult_t v = validate(coll, g->nranks, send, recv, count, dtype, op);
+  tcclResult_t v = (tcclResult_t)validate_collective_args(coll, g->nranks, send, recv, count, dtype, op);
   if (v != tcclSuccess) return v;
   if (count == 0 || is_noop(coll, g->nranks, send, recv)) {
     std::memset(&g->last, 0, sizeof(g->last));
@@ -504,7 +511,7 @@ tcclResult_t tcclPlanInspect(int coll, int nranks, const void* const sendbufs[],
                              int* n_windows, int* n_tasks, tcclLaunchInfo_t* info) {
   if (!n_windows || !n_tasks || !info || sm_count < 1 || smem_per_block < 1) return tcclInvalidArgument;
   if (cfg && !config_ok(*cfg)) return tcclInvalidArgument;
-  tcclResult_t v = validate(coll, nranks, sendbufs, recvbufs, count, datatype, 0);
+  tcclResult_t v = (tcclResult_t)validate_collective_args(coll, nranks, sendbufs, recvbufs, count, datatype, 0);
   if (v != tcclSuccess) return v;
   *n_windows = 0;
   *n_tasks = 0;

@@ -1,0 +1,151 @@
+// tcclAllReduceNoAlloc: the bulk-engine allreduce for callers that cannot
+// allocate GPU memory.
+//
+// Some callers cannot call cudaMalloc: code that runs inside another
+// framework's memory manager (which owns every device allocation and forbids
+// side allocations), allocator hooks and out-of-memory handlers, or processes
+// whose device memory is fully reserved up front. tcclGroupCreate allocates a
+// status word and per-plan window tables, so it is out of reach for them.
+// This entry point needs no group: the bulk kernel's scratch (status word,
+// per-CTA offsets and the window table) lives in one file-scope __device__
+// array below, which every GPU that loads this library holds until the
+// process exits. The caller passes only inputs and outputs.
+#include "tccl.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+#include "plan.h"
+
+namespace tccl {
+namespace {
+
+constexpr size_t kScratchBytes = TCCL_NO_ALLOC_SCRATCH_BYTES;
+constexpr size_t kStatusOff = 0;            // int status word (cleared every call)
+constexpr size_t kCtaOff = 256;             // uint32_t per-CTA window offsets
+constexpr size_t kWinOff = kCtaOff + 4 * (TCCL_NO_ALLOC_MAX_CTAS + 1 + 63);  // 256-aligned
+constexpr size_t kMaxWindows = (kScratchBytes - kWinOff) / sizeof(Window);
+static_assert(kWinOff % 256 == 0, "window table alignment");
+static_assert(kMaxWindows >= TCCL_NO_ALLOC_MAX_CTAS + 3 * kMaxRanks, "scratch too small");
+
+// The scratch. Host code must not use this name as an address: on the host
+// it is only a stand-in for the symbol. The device address comes from
+// cudaGetSymbolAddress, taken once per device below.
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[kScratchBytes];
+
+struct DeviceSetup {
+  bool ready = false;
+  unsigned char* scratch = nullptr;  // device address of g_no_alloc_scratch
+  DeviceDesc dev;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceSetup g_setup[kMaxDevices];
+std::mutex g_setup_mu;
+
+// Once per device, with that device current: resolve the scratch array's
+// device address and read the limits the lowering needs.
+int setup_device(int device, DeviceSetup** out) {
+  if (device < 0 || device >= kMaxDevices) return tcclInvalidUsage;
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  DeviceSetup& s = g_setup[device];
+  if (!s.ready) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_no_alloc_scratch) != cudaSuccess || ptr == nullptr)
+      return tcclCudaError;
+    if (cudaDeviceGetAttribute(&s.dev.sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&s.dev.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&s.dev.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess)
+      return tcclCudaError;
+    if (prepare_bulk_kernels((size_t)s.dev.smem_optin) != 0) return tcclCudaError;
+    s.scratch = static_cast<unsigned char*>(ptr);
+    s.ready = true;
+  }
+  *out = &s;
+  return tcclSuccess;
+}
+
+bool log_on() {
+  const char* e = std::getenv("TCCL_LOG");
+  return e && std::atoi(e) > 0;
+}
+
+}  // namespace
+}  // namespace tccl
+
+using namespace tccl;
+
+extern "C" tcclResult_t tcclAllReduceNoAlloc(int nranks, const void* const sendbufs[],
+                                             void* const recvbufs[], size_t count,
+                                             tcclDataType_t datatype, tcclRedOp_t op,
+                                             cudaStream_t stream, int cta_cap) {
+  int v = validate_collective_args(kAllReduce, nranks, sendbufs, recvbufs, count, datatype, op);
+  if (v != tcclSuccess) return (tcclResult_t)v;
+  if (count == 0 || (nranks == 1 && sendbufs[0] == recvbufs[0])) return tcclSuccess;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) return tcclCudaError;
+  DeviceSetup* ds = nullptr;
+  int st = setup_device(device, &ds);
+  if (st != tcclSuccess) return (tcclResult_t)st;
+
+  const int es = datatype == tcclBfloat16 ? 2 : 4;
+  Plan pl = plan_collective(kAllReduce, nranks, count, es, op);
+  uint8_t sm[kMaxRanks], rm[kMaxRanks];
+  for (int r = 0; r < nranks; ++r) {
+    sm[r] = (uint8_t)((uintptr_t)sendbufs[r] & 15);
+    rm[r] = (uint8_t)((uintptr_t)recvbufs[r] & 15);
+  }
+  Config cfg;
+  cfg.engine = kEngineBulk;
+  Lowered low;
+  std::string why;
+  if (!lower_plan(pl, sm, rm, cfg, ds->dev, cta_cap, &low, &why)) return tcclInvalidUsage;
+  if (low.shape.grid > TCCL_NO_ALLOC_MAX_CTAS || low.win.size() > kMaxWindows) {
+    if (log_on())
+      std::fprintf(stderr,
+                   "[tccl] tcclAllReduceNoAlloc: plan needs %d CTAs and %zu windows; the static "
+                   "scratch holds at most %d CTAs and %zu windows\n",
+                   low.shape.grid, low.win.size(), TCCL_NO_ALLOC_MAX_CTAS, kMaxWindows);
+    return tcclInvalidUsage;
+  }
+
+  // Stage this call's plan into the shared scratch, in stream order, and
+  // clear the status word the kernel reports timeouts in.
+  unsigned char* base = ds->scratch;
+  const size_t wbytes = low.win.size() * sizeof(Window);
+  const size_t cbytes = low.cta_first.size() * sizeof(uint32_t);
+  if (cudaMemsetAsync(base + kStatusOff, 0, sizeof(int), stream) != cudaSuccess ||
+      cudaMemcpyAsync(base + kCtaOff, low.cta_first.data(), cbytes, cudaMemcpyHostToDevice,
+                      stream) != cudaSuccess ||
+      (wbytes && cudaMemcpyAsync(base + kWinOff, low.win.data(), wbytes, cudaMemcpyHostToDevice,
+                                 stream) != cudaSuccess))
+    return tcclCudaError;
+
+  BulkArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < nranks; ++r) {
+    a.p.src[r] = sendbufs[r];
+    a.p.dst[r] = recvbufs[r];
+  }
+  a.win = reinterpret_cast<const Window*>(base + kWinOff);
+  a.cta_first = reinterpret_cast<const uint32_t*>(base + kCtaOff);
+  a.status = reinterpret_cast<int*>(base + kStatusOff);
+  a.sm_mask = nullptr;
+  a.timeout_ns = (uint64_t)(resolve_config(cfg).wait_timeout_ms * 1e6);
+  a.inject_timeout_ns = 0;
+  a.nranks = nranks;
+  a.chunk_bytes = low.shape.chunk_bytes;
+  a.stages = low.shape.stages;
+  a.store_mode = low.shape.store_mode;
+  a.consumer_warps = low.shape.consumer_warps;
+  a.release_lag = low.shape.release_lag;
+  a.elem_size = es;
+  int err = launch_bulk(kAllReduce, datatype, op, a, low.shape, stream);
+  return err == 0 ? tcclSuccess : tcclCudaError;
+}

@@ -93,6 +93,12 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
                 const Config& cfg, const DeviceDesc& dev, int cta_cap, Lowered* out,
                 std::string* why);
 
+// Checks a collective call's arguments: enums, rank count, null and
+// misaligned pointers, size overflow, and buffer overlap (only the NCCL
+// in-place forms may alias). Returns a tcclResult_t value.
+int validate_collective_args(int coll, int nranks, const void* const* send, void* const* recv,
+                             size_t count, int dtype, int op);
+
 // Per-rank message size the Auto engine choice looks at.
 uint64_t message_bytes(int coll, int nranks, uint64_t count, int elem_size);
 

@@ -214,6 +214,41 @@ tcclResult_t tcclPlanInspect(int coll, int nranks, const void* const sendbufs[],
  */
 tcclResult_t tcclGroupInjectWaitTimeout(tcclGroup_t g, int enable, double timeout_ms);
 
+/*
+ * Allreduce for callers that cannot allocate GPU memory (no counterpart in
+ * the paper: a convenience of this library).
+ *
+ * Who needs it: code that must not call cudaMalloc, such as a component
+ * running under another framework's memory manager that owns every device
+ * allocation, an allocator hook or out-of-memory handler, or a process whose
+ * device memory is reserved up front. tcclGroupCreate allocates device memory
+ * (a status word and plan tables), so this call takes no group.
+ *
+ * Computes exactly what tcclAllReduce computes, with the bulk engine, and
+ * allocates no device or pinned memory: it calls no cudaMalloc, cudaFree,
+ * cudaMallocHost, cudaMallocAsync or other allocating CUDA routine. Its
+ * scratch (status word, per-CTA offsets, window table) is one static device
+ * array of TCCL_NO_ALLOC_SCRATCH_BYTES that every GPU loading this library
+ * holds until the process exits; host-side planning uses ordinary C++ heap
+ * memory.
+ *  - The first call on a device (with that device current) resolves the
+ *    array's device address with cudaGetSymbolAddress; make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array and overwrites it, in stream order, with
+ *    its own plan, so calls whose work overlaps on the GPU (different streams,
+ *    or other threads) race and give undefined results. Serialise them.
+ *  - Plans needing more than TCCL_NO_ALLOC_MAX_CTAS CTAs, or more windows
+ *    than the array holds, are rejected with tcclInvalidUsage (TCCL_LOG=1
+ *    prints the sizes); every other argument rule is tcclAllReduce's.
+ *  - A device-side wait that gives up is not reported: the kernel records it
+ *    in the array's status word, which this call clears and nothing reads.
+ */
+#define TCCL_NO_ALLOC_SCRATCH_BYTES (256 * 1024)
+#define TCCL_NO_ALLOC_MAX_CTAS 1024
+tcclResult_t tcclAllReduceNoAlloc(int nranks, const void* const sendbufs[],
+                                  void* const recvbufs[], size_t count, tcclDataType_t datatype,
+                                  tcclRedOp_t op, cudaStream_t stream, int cta_cap);
+
 #ifdef __cplusplus
 }
 #endif
