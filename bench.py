@@ -167,6 +167,24 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(sel), "window": window}
 
 
+# ------------------------------------------------------------------ replicas
+def replica_time(dist, local_ms: float) -> float:
+    """Slowest replica's time (max over ranks); a host-side scalar exchange,
+    not a data-path collective. Without a process group, the local time."""
+    if dist is None:
+        return local_ms
+    import torch
+    t = torch.tensor([local_ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, bytes_per_replica: int, slowest_ms: float) -> float:
+    """GB/s of all replicas together: every replica moves the same bytes
+    (weak scaling), and the job takes as long as its slowest replica."""
+    return world * bytes_per_replica / (slowest_ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ workload data
 def make_inputs(w):
     import datagen
@@ -279,12 +297,9 @@ def run_ours(args, w, rank, world, dist):
     launch_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)) / args.steps
     clocks = sampler.summary(t_soak, t_end)
 
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = replica_time(dist, total_ms)
     ms_per_step = total_ms / args.steps
-    value = world * alg_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_rate(world, alg_bytes, ms_per_step)
     peak, peak_src = measured_peak()
     achieved = hbm_bytes / (launch_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
@@ -333,10 +348,7 @@ def run_ours(args, w, rank, world, dist):
     e1.record(stream)
     e1.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = replica_time(dist, e2e_ms)
 
     out = None
     if rank == 0:
@@ -369,7 +381,7 @@ def run_ours(args, w, rank, world, dist):
             "rs_then_ag": {"ms_per_step": round(rs_ms, 5),
                            "algbw": round(alg_bytes / (rs_ms * 1e-3) / 1e9, 2),
                            "hbm_bytes_per_step": 2 * (p + 1) * S},
-            "e2e": {"value": round(world * alg_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "e2e": {"value": round(whole_job_rate(world, alg_bytes, e2e_ms), 2), "unit": "GB/s",
                     "h2d_bytes_per_step": p * S, "d2h_bytes_per_step": p * S,
                     "ms_per_step": round(e2e_ms, 4)},
             "cpu_baseline": cpu,
@@ -417,6 +429,194 @@ def run_reference(args, w):
                     "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------------------------ sweep mode
+def sweep(args):
+    """One JSON line per configuration point of the five workloads (C1..C5):
+    device time per op (CUDA events, back-to-back launches; graph-captured
+    too for small messages), algbw, bus bandwidth, HBM fraction, SMs used, and
+    the CPU oracle on 1 core and on all cores for one point per workload."""
+    import numpy as np
+    import torch
+    import collective_communication_planner_gb300 as tccl
+    import datagen
+    import oracle
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    st = stream.cuda_stream
+    peak, _ = measured_peak()
+    ncores = os.cpu_count() or 1
+
+    def ev_time(fn, min_ms=60.0):
+        for _ in range(3):
+            fn()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        it = 1
+        while True:
+            e0.record(stream)
+            for _ in range(it):
+                fn()
+            e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            if ms >= min_ms or it >= 20000:
+                return ms / it
+            it = min(20000, max(it * 2, int(it * min_ms / max(ms, 1e-3)) + 1))
+
+    def graph_time(fn, reps=20):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                fn()
+        t = ev_time(g.replay, 30.0) / reps
+        del g
+        return t
+
+    def cpu_time(fn, min_s=0.5):
+        fn()
+        n, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= min_s:
+                return el / n
+
+    def emit(**kw):
+        print(json.dumps(kw), flush=True)
+
+    def to_dev(x):
+        return host_to_torch(x).to(dev)
+
+    def run_point(cfg, g, coll, p, n, dtype, op, sends, recvs, cap=0, graph=False, sms=False):
+        es = 2 if dtype == "bf16" else 4
+        dt, o = tccl.DTYPES[dtype], tccl.OPS[op]
+        if coll == "AR":
+            fn = lambda: tccl.tcclAllReduce(g.handle, sends, recvs, n, dt, o, st, cap)
+            S, hbm = n * es, 2 * p * n * es
+        elif coll == "RS":
+            fn = lambda: tccl.tcclReduceScatter(g.handle, sends, recvs, n, dt, o, st, cap)
+            S, hbm = p * n * es, (p + 1) * p * n * es   # S = per-rank send bytes
+        else:
+            fn = lambda: tccl.tcclAllGather(g.handle, sends, recvs, n, dt, st, cap)
+            S, hbm = p * n * es, (p + 1) * p * n * es   # S = per-rank recv bytes
+        assert fn() == 0
+        info = g.last_launch()
+        used = None
+        if sms:
+            g.read_sm_record()
+            g.record_sms(True)
+            fn()
+            used = g.read_sm_record()
+            g.record_sms(False)
+        ms = ev_time(fn)
+        row = dict(config=cfg, coll=coll, P=p, dtype=dtype, op=op, count=n,
+                   bytes_per_rank=(n * es if coll == "AR" else S), cap=cap,
+                   us=round(ms * 1e3, 3),
+                   algbw=round(p * (n * es if coll == "AR" else S) / (ms * 1e-3) / 1e9, 2),
+                   busbw=round(S / (ms * 1e-3) * (2 if coll == "AR" else 1) * (p - 1) / p / 1e9, 2),
+                   hbm_GBps=round(hbm / (ms * 1e-3) / 1e9, 1),
+                   hbm_fraction=round(hbm / (ms * 1e-3) / 1e9 / peak, 4),
+                   l2_resident=hbm < 129e6, engine=info["engine"], ctas=info["ctas"],
+                   sms_used=used)
+        if graph:
+            row["graph_us"] = round(graph_time(fn) * 1e3, 3)
+        assert g.query_error() == 0
+        return row
+
+    only = set(args.sweep_configs.split(",")) if args.sweep_configs else None
+
+    # C1
+    if not only or "c1" in only:
+        p, n = 2, 1_048_576
+        xs = datagen.rank_buffers("uniform_f32", 0, p, n)
+        g = tccl.Group(p)
+        sends = [to_dev(x) for x in xs]
+        recvs = [torch.empty_like(t) for t in sends]
+        row = run_point("C1", g, "AR", p, n, "f32", "sum", sends, recvs, graph=True)
+        row["cpu_1core_s"] = cpu_time(lambda: oracle.allreduce(xs, "f32", "sum", nthreads=1))
+        row["cpu_all_s"] = cpu_time(lambda: oracle.allreduce(xs, "f32", "sum", nthreads=0))
+        row["cpu_cores"] = ncores
+        emit(**row)
+        g.close()
+    # C2
+    if not only or "c2" in only:
+        p, n = 4, 32 << 20
+        rc = n // p
+        xs = datagen.rank_buffers("normal_bf16", 1, p, n, mu=0.0, sigma=1.0)
+        g = tccl.Group(p)
+        sends = [to_dev(x) for x in xs]
+        recvs = [torch.empty_like(t) for t in sends]
+        parts = [torch.empty(rc, dtype=torch.bfloat16, device=dev) for _ in range(p)]
+        row = run_point("C2", g, "AR", p, n, "bf16", "sum", sends, recvs)
+        row["cpu_1core_s"] = cpu_time(lambda: oracle.allreduce(xs, "bf16", "sum", nthreads=1), 1.0)
+        row["cpu_all_s"] = cpu_time(lambda: oracle.allreduce(xs, "bf16", "sum", nthreads=0))
+        row["cpu_cores"] = ncores
+        emit(**row)
+        emit(**run_point("C2", g, "RS", p, rc, "bf16", "sum", sends, parts))
+        emit(**run_point("C2", g, "AG", p, rc, "bf16", "sum", parts, recvs))
+        g.close()
+        del sends, recvs, parts
+    # C3
+    if not only or "c3" in only:
+        p = 8
+        g = tccl.Group(p)
+        for nbytes in [4096 << k for k in range(17)]:
+            n = nbytes // 4
+            for dtype, op in (("f32", "sum"), ("f32", "min"), ("f32", "max"), ("i32", "sum")):
+                xs = (datagen.rank_buffers("uniform_f32", 2, p, n) if dtype == "f32" else
+                      datagen.rank_buffers("int32", 2, p, n, lo=-1000, hi=1000))
+                bufs = [to_dev(x) for x in xs]
+                row = run_point("C3", g, "AR", p, n, dtype, op, bufs, bufs, graph=nbytes <= (1 << 20))
+                if nbytes == (256 << 20) and op == "sum" and dtype == "f32":
+                    row["cpu_1core_s"] = cpu_time(lambda: oracle.allreduce(xs, dtype, op, nthreads=1), 1.0)
+                    row["cpu_all_s"] = cpu_time(lambda: oracle.allreduce(xs, dtype, op, nthreads=0))
+                    row["cpu_cores"] = ncores
+                emit(**row)
+                del bufs
+            torch.cuda.empty_cache()
+        g.close()
+    # C4
+    if not only or "c4" in only:
+        p, n = 8, 64 << 20
+        xs = datagen.rank_buffers("normal_bf16", 3, p, n, mu=0.0, sigma=0.02)
+        g = tccl.Group(p)
+        sends = [to_dev(x) for x in xs]
+        recvs = [torch.empty_like(t) for t in sends]
+        for cap in (8, 16, 32, 0):
+            row = run_point("C4", g, "AR", p, n, "bf16", "sum", sends, recvs, cap=cap, sms=True)
+            if cap == 0:
+                row["cpu_1core_s"] = cpu_time(lambda: oracle.allreduce(xs, "bf16", "sum", nthreads=1), 1.0)
+                row["cpu_all_s"] = cpu_time(lambda: oracle.allreduce(xs, "bf16", "sum", nthreads=0))
+                row["cpu_cores"] = ncores
+            emit(**row)
+        g.close()
+        del sends, recvs
+        torch.cuda.empty_cache()
+    # C5
+    if not only or "c5" in only:
+        p = 8
+        g = tccl.Group(p)
+        for tokens in (1, 8, 64, 512, 4096):
+            n = tokens * 8192
+            xs = datagen.rank_buffers("normal_bf16", 4, p, n, mu=0.0, sigma=1.0)
+            sends = [to_dev(x) for x in xs]
+            recvs = [torch.empty_like(t) for t in sends]
+            row = run_point("C5", g, "AR", p, n, "bf16", "sum", sends, recvs, graph=tokens <= 64)
+            row["tokens"] = tokens
+            if tokens == 4096:
+                row["cpu_1core_s"] = cpu_time(lambda: oracle.allreduce(xs, "bf16", "sum", nthreads=1), 1.0)
+                row["cpu_all_s"] = cpu_time(lambda: oracle.allreduce(xs, "bf16", "sum", nthreads=0))
+                row["cpu_cores"] = ncores
+            emit(**row)
+        g.close()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -428,6 +628,9 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load first")
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="measure every configuration point of C1..C5 (one JSON line each)")
+    ap.add_argument("--sweep-configs", default="", help="comma list, e.g. c3,c5")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -451,6 +654,9 @@ def main():
     import __graft_entry__
     if rank == 0 or world == 1:
         __graft_entry__.build()
+    if args.sweep:
+        sweep(args)
+        return
     if dist is not None:
         dist.barrier()
     out = run_ours(args, w, rank, world, dist)

@@ -98,14 +98,17 @@ struct PlanKey {
 
 struct CachedPlan {
   Lowered low;
-  // bulk engine: device copies of the window table and per-CTA offsets
-  Window* d_win = nullptr;
-  uint32_t* d_cta_first = nullptr;
+  // bulk engine: one device allocation holding the window table, the chunk
+  // prefix and the per-CTA scalar-window offsets
+  unsigned char* d_table = nullptr;
+  const Window* d_win = nullptr;
+  const uint64_t* d_prefix = nullptr;
+  const uint32_t* d_cta_first = nullptr;
+  unsigned long long* d_sched = nullptr;
   // small engines: the launch argument block without its pointers
   std::vector<unsigned char> small_args;
   ~CachedPlan() {
-    if (d_win) cudaFree(d_win);
-    if (d_cta_first) cudaFree(d_cta_first);
+    if (d_table) cudaFree(d_table);
   }
 };
 
@@ -155,6 +158,7 @@ Config config_from_env() {
     else if (v == "vec") c.engine = kEngineVec;
   }
   if (const char* e = std::getenv("TCCL_SMALL_MAX_BYTES")) c.small_max_bytes = std::strtoull(e, 0, 10);
+  if (const char* e = std::getenv("TCCL_VEC_MAX_BYTES")) c.vec_max_bytes = std::strtoull(e, 0, 10);
   c.stage_bytes = geti("TCCL_STAGE_BYTES", 0);
   c.stages = geti("TCCL_STAGES", 0);
   if (const char* e = std::getenv("TCCL_STORE_MODE")) {
@@ -163,6 +167,15 @@ Config config_from_env() {
     else if (v == "vec") c.store_mode = kStoreVec;
   }
   c.consumer_warps = geti("TCCL_CONSUMER_WARPS", 0);
+  c.prefetch_chunks = geti("TCCL_PREFETCH_CHUNKS", -1);
+  c.load_policy = geti("TCCL_LOAD_POLICY", 0);
+  if (const char* e = std::getenv("TCCL_MAX_CHUNK_BYTES")) c.max_chunk_bytes = std::strtoull(e, 0, 10);
+  if (const char* e = std::getenv("TCCL_CHUNK_ORDER")) {
+    std::string v(e);
+    if (v == "blocked") c.chunk_order = kOrderBlocked;
+    else if (v == "cyclic") c.chunk_order = kOrderCyclic;
+    else if (v == "dynamic") c.chunk_order = kOrderDynamic;
+  }
   c.ctas_per_sm = geti("TCCL_CTAS_PER_SM", 0);
   if (const char* e = std::getenv("TCCL_WAIT_TIMEOUT_MS")) c.wait_timeout_ms = std::atof(e);
   return resolve_config(c);
@@ -172,12 +185,17 @@ Config from_public(const tcclConfig_t& p) {
   Config c;
   c.engine = p.engine;
   c.small_max_bytes = p.small_max_bytes;
+  c.vec_max_bytes = p.vec_max_bytes;
   c.stage_bytes = p.stage_bytes;
   c.stages = p.stages;
   c.store_mode = p.store_mode;
   c.consumer_warps = p.consumer_warps;
   c.ctas_per_sm = p.ctas_per_sm;
   c.wait_timeout_ms = p.wait_timeout_ms;
+  c.chunk_order = p.chunk_order;
+  c.prefetch_chunks = p.prefetch_chunks;
+  c.load_policy = p.load_policy;
+  c.max_chunk_bytes = p.max_chunk_bytes;
   return resolve_config(c);
 }
 
@@ -186,19 +204,25 @@ tcclConfig_t to_public(const Config& c) {
   std::memset(&p, 0, sizeof(p));
   p.engine = c.engine;
   p.small_max_bytes = c.small_max_bytes;
+  p.vec_max_bytes = c.vec_max_bytes;
   p.stage_bytes = c.stage_bytes;
   p.stages = c.stages;
   p.store_mode = c.store_mode;
   p.consumer_warps = c.consumer_warps;
   p.ctas_per_sm = c.ctas_per_sm;
   p.wait_timeout_ms = c.wait_timeout_ms;
+  p.chunk_order = c.chunk_order;
+  p.prefetch_chunks = c.prefetch_chunks;
+  p.load_policy = c.load_policy;
+  p.max_chunk_bytes = c.max_chunk_bytes;
   return p;
 }
 
 bool config_ok(const tcclConfig_t& p) {
   return p.engine >= 0 && p.engine <= 3 && p.store_mode >= 0 && p.store_mode <= 2 &&
          p.stage_bytes >= 0 && p.stages >= 0 && p.consumer_warps >= 0 && p.ctas_per_sm >= 0 &&
-         p.wait_timeout_ms >= 0;
+         p.wait_timeout_ms >= 0 && p.chunk_order >= 0 && p.chunk_order <= 3 &&
+         p.prefetch_chunks >= -1 && p.load_policy >= 0 && p.load_policy <= 2;
 }
 
 void fill_info(const Lowered& low, tcclLaunchInfo_t* info) {
@@ -212,6 +236,8 @@ void fill_info(const Lowered& low, tcclLaunchInfo_t* info) {
   info->windows = (int)low.win.size();
   info->tasks = low.ntasks;
   info->smem_bytes = low.shape.smem;
+  info->chunk_order = low.shape.engine == kEngineBulk ? low.shape.order : 0;
+  info->total_chunks = low.total_chunks;
 }
 
 void dump_plan(const Plan& pl, const Lowered& low) {
@@ -279,16 +305,18 @@ tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* con
   if (log_level()) dump_plan(pl, cp->low);
   const Lowered& low = cp->low;
   if (low.shape.engine == kEngineBulk) {
-    const size_t wbytes = low.win.size() * sizeof(Window);
-    const size_t cbytes = low.cta_first.size() * sizeof(uint32_t);
+    std::vector<unsigned char> host;
+    size_t off_prefix = 0, off_cta = 0, off_sched = 0;
+    pack_bulk_table(low, &host, &off_prefix, &off_cta, &off_sched);
     // one synchronous upload per plan: a new shape's first call must not be
     // made inside a CUDA graph capture
-    if (cudaMalloc(&cp->d_win, std::max<size_t>(wbytes, 32)) != cudaSuccess ||
-        cudaMalloc(&cp->d_cta_first, cbytes) != cudaSuccess)
+    if (cudaMalloc(&cp->d_table, host.size()) != cudaSuccess) return tcclCudaError;
+    if (cudaMemcpy(cp->d_table, host.data(), host.size(), cudaMemcpyHostToDevice) != cudaSuccess)
       return tcclCudaError;
-    if ((wbytes && cudaMemcpy(cp->d_win, low.win.data(), wbytes, cudaMemcpyHostToDevice) != cudaSuccess) ||
-        cudaMemcpy(cp->d_cta_first, low.cta_first.data(), cbytes, cudaMemcpyHostToDevice) != cudaSuccess)
-      return tcclCudaError;
+    cp->d_win = reinterpret_cast<const Window*>(cp->d_table);
+    cp->d_prefix = reinterpret_cast<const uint64_t*>(cp->d_table + off_prefix);
+    cp->d_cta_first = reinterpret_cast<const uint32_t*>(cp->d_table + off_cta);
+    cp->d_sched = reinterpret_cast<unsigned long long*>(cp->d_table + off_sched);
   } else if (low.size_class == 0) {
     build_small_args<kSmallRanks, kSmallWindows>(low, g->nranks, es, &cp->small_args);
   } else {
@@ -327,7 +355,15 @@ tcclResult_t run_collective(tcclGroup* g, int coll, const void* const* send, voi
         a.p.dst[k] = recv[k];
       }
       a.win = cp->d_win;
+      a.chunk_prefix = cp->d_prefix;
       a.cta_first = cp->d_cta_first;
+      a.total_chunks = low.total_chunks;
+      a.chunks_per_cta = low.chunks_per_cta;
+      a.nbody = low.nbody;
+      a.sched = cp->d_sched;
+      a.order = low.shape.order;
+      a.prefetch_chunks = low.shape.prefetch_chunks;
+      a.load_evict_first = low.shape.load_evict_first;
       a.status = g->d_status;
       a.sm_mask = mask;
       a.timeout_ns = (uint64_t)(g->cfg.wait_timeout_ms * 1e6);

@@ -17,6 +17,7 @@ enum DType : int { kF32 = 0, kBF16 = 1, kI32 = 2 };
 enum RedOp : int { kSum = 0, kMin = 1, kMax = 2 };
 enum Engine : int { kEngineAuto = 0, kEngineBulk = 1, kEngineWarp = 2, kEngineVec = 3 };
 enum StoreMode : int { kStoreAuto = 0, kStoreBulk = 1, kStoreVec = 2 };
+enum ChunkOrder : int { kOrderAuto = 0, kOrderBlocked = 1, kOrderCyclic = 2, kOrderDynamic = 3 };
 
 // Status codes a kernel may leave in the group's status word (same values
 // as tcclResult_t).
@@ -34,7 +35,7 @@ struct Window {
   int16_t dst_sel;
   uint16_t scalar;   // 1: element-wise path (edge or not 16-byte co-aligned)
   uint16_t task;     // logical task (shard) the window came from
-  int32_t cta;       // bulk engine: owning CTA; warp/vec engines: -1
+  int32_t cta;       // bulk engine scalar windows: owning CTA; otherwise -1
 };
 static_assert(sizeof(Window) == 32, "Window layout");
 
@@ -44,22 +45,36 @@ struct BasePtrs {
   void* dst[MAXR];
 };
 
-// Bulk (TMA pipeline) engine: windows live in a device table, grouped by CTA.
+// Bulk (TMA pipeline) engine. The plan's body windows (16-byte co-aligned)
+// form one sequence of equal chunks (each window's last chunk may be short).
+// CTA j takes the range [j*k, (j+1)*k) (blocked order), chunks j, j+G, j+2G,
+// ... (cyclic order: all CTAs sweep the buffers together), or claims chunks
+// one at a time from a device counter (dynamic order: faster SMs take more).
+// Element-wise windows are bound to CTAs.
 struct BulkArgs {
   BasePtrs<kMaxRanks> p;
-  const Window* win;          // device table
-  const uint32_t* cta_first;  // device table, grid + 1 entries
-  int* status;                // group status word (device)
-  uint32_t* sm_mask;          // SM recorder bitmap (device) or null
-  uint64_t timeout_ns;        // bound on every wait
-  uint64_t inject_timeout_ns; // test hook: > 0 makes CTA 0 wait on a barrier nothing signals
+  const Window* win;             // device table: nbody body windows, then scalar windows
+  const uint64_t* chunk_prefix;  // device table, nbody + 1 entries: chunks before body window w
+  const uint32_t* cta_first;     // device table, grid + 1 entries: CTA j's scalar windows are
+                                 // win[nbody + cta_first[j] .. nbody + cta_first[j + 1])
+  int* status;                   // status word (device)
+  uint32_t* sm_mask;             // SM recorder bitmap (device) or null
+  uint64_t timeout_ns;           // bound on every wait
+  uint64_t inject_timeout_ns;    // test hook: > 0 makes CTA 0 wait on a barrier nothing signals
+  uint64_t total_chunks;
+  uint64_t chunks_per_cta;       // blocked order
+  unsigned long long* sched;     // dynamic order: {next chunk, CTAs finished}, zero between launches
+  int nbody;
+  int order;                     // kOrderBlocked, kOrderCyclic or kOrderDynamic
   int nranks;
-  int chunk_bytes;            // bytes per source per chunk (multiple of 16)
+  int chunk_bytes;               // bytes per source per chunk (multiple of 16)
   int stages;
-  int store_mode;             // kStoreBulk or kStoreVec
+  int store_mode;                // kStoreBulk or kStoreVec
   int consumer_warps;
-  int release_lag;            // all-gather bulk stores: store groups kept in flight
+  int release_lag;               // all-gather bulk stores: store groups kept in flight
   int elem_size;
+  int prefetch_chunks;           // L2 prefetch distance beyond the shared-memory ring (0: off)
+  int load_evict_first;          // bulk loads carry an L2 evict-first policy
 };
 
 // Warp / vec (small-message) engines: the whole lowered plan rides in the
@@ -85,6 +100,9 @@ struct LaunchShape {
   int chunk_bytes = 0;
   int consumer_warps = 0;
   int release_lag = 0;
+  int order = 0;
+  int prefetch_chunks = 0;
+  int load_evict_first = 0;
   size_t smem = 0;
 };
 

@@ -81,6 +81,29 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
       : "memory");
 }
 
+// the same, with an L2 cache-eviction policy for the read lines
+__device__ __forceinline__ void bulk_load_hint(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// evict-first L2 policy for data read exactly once
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// global -> L2 bulk prefetch (no completion tracking): lets the L2 act as a
+// deeper staging level in front of the shared-memory ring
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
 // shared -> global bulk copy, tracked by bulk async-groups
 __device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
@@ -122,6 +145,21 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads:
+// every thread gets the same answer.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -307,20 +345,87 @@ __device__ __forceinline__ void scalar_element(const BasePtrs<MAXR>& p, int nran
 }
 
 // ------------------------------------------------------------------ bulk engine
-constexpr int kBarrierRegion = 1024;  // mbarriers + abort flag, ahead of the stages
 constexpr int kMaxStages = 32;
+constexpr uint64_t kNoChunk = ~0ull;  // end-of-stream marker in a stage's chunk slot
+
+// Head of the dynamic shared memory, ahead of the stages.
+struct BulkSmemHead {
+  uint64_t full[kMaxStages];      // stage k holds its chunk (tx-count barrier, 1 arrival)
+  uint64_t empty[kMaxStages];     // stage k may be refilled
+  uint64_t never;                 // test hook: a barrier nothing signals
+  uint64_t chunk_of[kMaxStages];  // chunk index carried by stage k, or kNoChunk
+  int abort_flag;
+};
+constexpr int kBarrierRegion = 1024;
+static_assert(sizeof(BulkSmemHead) <= kBarrierRegion, "shared-memory head");
+
+// Chunk index -> (window, byte offset, length), for increasing indices.
+struct ChunkLocator {
+  uint64_t lo, hi;
+  int wi;
+  Window w;
+  __device__ __forceinline__ void init() {
+    wi = -1;
+    lo = hi = 0;
+  }
+  __device__ __forceinline__ void locate(const BulkArgs& a, uint64_t c, uint32_t& off,
+                                         uint32_t& n) {
+    if (c >= hi) {
+      do {
+        ++wi;
+        hi = a.chunk_prefix[wi + 1];
+      } while (c >= hi);
+      lo = a.chunk_prefix[wi];
+      w = a.win[wi];
+    }
+    off = static_cast<uint32_t>((c - lo) * static_cast<uint64_t>(a.chunk_bytes));
+    n = min(static_cast<uint32_t>(a.chunk_bytes), w.bytes - off);
+  }
+};
+
+// This CTA's chunks in the static orders: a contiguous range (blocked) or
+// every gridDim.x-th chunk (cyclic).
+struct StaticOrder {
+  uint64_t c, end, step;
+  __device__ __forceinline__ void init(const BulkArgs& a) {
+    if (a.order == kOrderBlocked) {
+      c = static_cast<uint64_t>(blockIdx.x) * a.chunks_per_cta;
+      end = min(c + a.chunks_per_cta, a.total_chunks);
+      step = 1;
+    } else {
+      c = blockIdx.x;
+      end = a.total_chunks;
+      step = gridDim.x;
+    }
+  }
+  __device__ __forceinline__ bool next(uint64_t& out) {
+    if (c >= end) return false;
+    out = c;
+    c += step;
+    return true;
+  }
+};
+
+template <int COLL, int DT, int OP>
+__device__ __forceinline__ void bulk_scalar_windows(const BulkArgs& a, int ctid, int nct) {
+  const uint32_t b = a.nbody + a.cta_first[blockIdx.x];
+  const uint32_t e = a.nbody + a.cta_first[blockIdx.x + 1];
+  for (uint32_t wi = b; wi < e; ++wi) {
+    const Window w = a.win[wi];
+    for (uint64_t x = ctid; x < w.bytes / (DT == kBF16 ? 2 : 4); x += nct)
+      scalar_element<COLL, DT, OP, kMaxRanks>(a.p, a.nranks, w, x);
+  }
+}
 
 template <int COLL, int DT, int OP>
 __global__ void __launch_bounds__(1024, 1) bulk_kernel(const __grid_constant__ BulkArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
+  BulkSmemHead& h = *reinterpret_cast<BulkSmemHead*>(smem);
+  volatile int* abort_flag = &h.abort_flag;
   const int S = a.stages;
   const int P = a.nranks;
   const int nsrc = (COLL == kAllGather) ? 1 : P;
   const uint32_t chunk = static_cast<uint32_t>(a.chunk_bytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kMaxStages;
-  uint64_t* never = empty + kMaxStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(never + 1);
   unsigned char* stage_base = smem + kBarrierRegion;
   unsigned char* result_base = stage_base + static_cast<size_t>(S) * nsrc * chunk;
   const int warp = threadIdx.x >> 5;
@@ -330,54 +435,109 @@ __global__ void __launch_bounds__(1024, 1) bulk_kernel(const __grid_constant__ B
 
   if (threadIdx.x == 0) {
     for (int k = 0; k < S; ++k) {
-      mbar_init(&full[k], 1);
-      mbar_init(&empty[k], ag_bulk ? 1 : ncw);
+      mbar_init(&h.full[k], 1);
+      mbar_init(&h.empty[k], ag_bulk ? 1 : ncw);
     }
-    mbar_init(never, 1);
-    *abort_flag = 0;
+    mbar_init(&h.never, 1);
+    h.abort_flag = 0;
     fence_mbar_init();
     record_sm(a.sm_mask);
   }
   __syncthreads();
 
-  const uint32_t wbeg = a.cta_first[blockIdx.x];
-  const uint32_t wend = a.cta_first[blockIdx.x + 1];
-
-  // ---------------- producer: one thread issues every bulk load
+  // ---------------- producer: one thread chooses the chunks and issues every
+  // bulk load; it tells the consumers which chunk each stage holds
   if (warp == 0) {
     if (lane != 0) return;
-    uint32_t it = 0;
+    const bool dynamic = a.order == kOrderDynamic;
+    ChunkLocator loc;
+    loc.init();
+    StaticOrder so;
+    so.init(a);
+    // L2 prefetch ahead of the ring (static orders only: the sequence is known)
+    ChunkLocator pf_loc;
+    pf_loc.init();
+    StaticOrder pf;
+    pf.init(a);
+    uint32_t pf_pos = 0;
+    const bool prefetch = !dynamic && a.prefetch_chunks > 0;
+    if (prefetch) {
+      uint64_t skip;
+      while (pf_pos < static_cast<uint32_t>(S) && pf.next(skip)) ++pf_pos;
+    }
+    const uint64_t policy = l2_evict_first_policy();
+    unsigned long long next_claim = dynamic ? atomicAdd(&a.sched[0], 1ull) : 0ull;
+    uint32_t it = 0, off, n;
     bool ok = true;
-    for (uint32_t wi = wbeg; wi < wend && ok; ++wi) {
-      const Window w = a.win[wi];
-      if (w.scalar) continue;
-      const char* src_one = static_cast<const char*>(a.p.src[w.src_sel < 0 ? 0 : w.src_sel]);
-      for (uint32_t off = 0; off < w.bytes; off += chunk) {
-        const uint32_t n = min(chunk, w.bytes - off);
-        const uint32_t k = it % S;
-        if (it >= static_cast<uint32_t>(S)) {
-          ok = wait_bounded(&empty[k], ((it / S) & 1) ^ 1, abort_flag, a.timeout_ns, a.status, true);
-          if (!ok) break;
-        }
-        mbar_arrive_expect_tx(&full[k], n * nsrc);
-        unsigned char* st = stage_base + static_cast<size_t>(k) * nsrc * chunk;
-        if (COLL == kAllGather) {
-          bulk_load(st, src_one + w.src_off + off, n, &full[k]);
-        } else {
-          for (int r = 0; r < nsrc; ++r)
-            bulk_load(st + static_cast<size_t>(r) * chunk,
-                      static_cast<const char*>(a.p.src[r]) + w.src_off + off, n, &full[k]);
-        }
-        ++it;
+    for (;;) {
+      uint64_t c;
+      bool more;
+      if (dynamic) {
+        c = next_claim;
+        more = c < a.total_chunks;
+        // claim the following chunk now; its latency hides behind this one
+        if (more) next_claim = atomicAdd(&a.sched[0], 1ull);
+      } else {
+        more = so.next(c);
       }
+      if (prefetch && more) {
+        const uint32_t want = it + S + a.prefetch_chunks;
+        uint64_t pc;
+        while (pf_pos < want && pf.next(pc)) {
+          uint32_t po, pn;
+          pf_loc.locate(a, pc, po, pn);
+          if (COLL == kAllGather) {
+            const char* src = static_cast<const char*>(a.p.src[pf_loc.w.src_sel < 0 ? 0 : pf_loc.w.src_sel]);
+            bulk_prefetch_l2(src + pf_loc.w.src_off + po, pn);
+          } else {
+            for (int r = 0; r < nsrc; ++r)
+              bulk_prefetch_l2(static_cast<const char*>(a.p.src[r]) + pf_loc.w.src_off + po, pn);
+          }
+          ++pf_pos;
+        }
+      }
+      const uint32_t k = it % S;
+      if (it >= static_cast<uint32_t>(S)) {
+        ok = wait_bounded(&h.empty[k], ((it / S) & 1) ^ 1, abort_flag, a.timeout_ns, a.status, true);
+        if (!ok) break;
+      }
+      if (!more) {
+        h.chunk_of[k] = kNoChunk;  // published by the arrive's release
+        mbar_arrive(&h.full[k]);
+        break;
+      }
+      loc.locate(a, c, off, n);
+      h.chunk_of[k] = c;
+      mbar_arrive_expect_tx(&h.full[k], n * nsrc);
+      unsigned char* st = stage_base + static_cast<size_t>(k) * nsrc * chunk;
+      if (COLL == kAllGather) {
+        const char* src = static_cast<const char*>(a.p.src[loc.w.src_sel < 0 ? 0 : loc.w.src_sel]);
+        if (a.load_evict_first) bulk_load_hint(st, src + loc.w.src_off + off, n, &h.full[k], policy);
+        else bulk_load(st, src + loc.w.src_off + off, n, &h.full[k]);
+      } else {
+        for (int r = 0; r < nsrc; ++r) {
+          const char* src = static_cast<const char*>(a.p.src[r]) + loc.w.src_off + off;
+          unsigned char* dst = st + static_cast<size_t>(r) * chunk;
+          if (a.load_evict_first) bulk_load_hint(dst, src, n, &h.full[k], policy);
+          else bulk_load(dst, src, n, &h.full[k]);
+        }
+      }
+      ++it;
     }
     if (!ok) {
       // an abort: let every load this thread issued land before the CTA's
-      // shared memory goes away (the last S iterations are the only ones
-      // that can still be in flight)
+      // shared memory goes away (only the last S iterations can be in flight)
       const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
       for (uint32_t j = first; j < it; ++j)
-        wait_bounded(&full[j % S], (j / S) & 1, abort_flag, a.timeout_ns, a.status, false);
+        wait_bounded(&h.full[j % S], (j / S) & 1, abort_flag, a.timeout_ns, a.status, false);
+    }
+    if (dynamic) {
+      // the last CTA to finish claiming resets the counter for the next launch
+      __threadfence();
+      if (atomicAdd(&a.sched[1], 1ull) == gridDim.x - 1) {
+        atomicExch(&a.sched[0], 0ull);
+        atomicExch(&a.sched[1], 0ull);
+      }
     }
     return;
   }
@@ -385,111 +545,106 @@ __global__ void __launch_bounds__(1024, 1) bulk_kernel(const __grid_constant__ B
   // ---------------- consumers
   const int ctid = threadIdx.x - 32;
   const int nct = ncw * 32;
-  uint32_t it = 0;
+  ChunkLocator loc;
+  loc.init();
+  uint32_t it = 0, off, n;
   bool ok = true;
 
   if (ag_bulk) {
     // all-gather with bulk stores: the stage itself is the shard, read once
     // from memory and stored from shared memory to all P destinations
-    for (uint32_t wi = wbeg; wi < wend; ++wi) {
-      const Window w = a.win[wi];
-      if (w.scalar) {
-        if (!*abort_flag)
-          for (uint64_t e = ctid; e < w.bytes / (DT == kBF16 ? 2 : 4); e += nct)
-            scalar_element<COLL, DT, OP, kMaxRanks>(a.p, P, w, e);
-        continue;
-      }
-      if (ctid != 0) continue;
-      const int d0 = w.dst_sel < 0 ? 0 : w.dst_sel;
-      const int d1 = w.dst_sel < 0 ? P : w.dst_sel + 1;
-      for (uint32_t off = 0; off < w.bytes && ok; off += chunk) {
-        const uint32_t n = min(chunk, w.bytes - off);
+    if (ctid == 0) {
+      for (;;) {
         const uint32_t k = it % S;
-        ok = wait_bounded(&full[k], (it / S) & 1, abort_flag, a.timeout_ns, a.status, true);
+        ok = wait_bounded(&h.full[k], (it / S) & 1, abort_flag, a.timeout_ns, a.status, true);
         if (ok && a.inject_timeout_ns && blockIdx.x == 0 && it == 0)
-          ok = wait_bounded(never, 0, abort_flag, a.inject_timeout_ns, a.status, true);
+          ok = wait_bounded(&h.never, 0, abort_flag, a.inject_timeout_ns, a.status, true);
         if (!ok) break;
+        const uint64_t c = h.chunk_of[k];
+        if (c == kNoChunk) break;
+        loc.locate(a, c, off, n);
         const unsigned char* st = stage_base + static_cast<size_t>(k) * chunk;
+        const int d0 = loc.w.dst_sel < 0 ? 0 : loc.w.dst_sel;
+        const int d1 = loc.w.dst_sel < 0 ? P : loc.w.dst_sel + 1;
         fence_proxy_async_smem();
         for (int d = d0; d < d1; ++d)
-          bulk_store(static_cast<char*>(a.p.dst[d]) + w.dst_off + off, st, n);
+          bulk_store(static_cast<char*>(a.p.dst[d]) + loc.w.dst_off + off, st, n);
         bulk_commit();
         bulk_wait_read_dyn(a.release_lag);
-        if (it >= static_cast<uint32_t>(a.release_lag)) mbar_arrive(&empty[(it - a.release_lag) % S]);
+        if (it >= static_cast<uint32_t>(a.release_lag))
+          mbar_arrive(&h.empty[(it - a.release_lag) % S]);
         ++it;
       }
+      bulk_wait_all();
     }
-    if (ctid == 0) bulk_wait_all();
+    if (!*abort_flag) bulk_scalar_windows<COLL, DT, OP>(a, ctid, nct);
     return;
   }
 
   const bool bulk_out = (a.store_mode == kStoreBulk);
-  for (uint32_t wi = wbeg; wi < wend; ++wi) {
-    const Window w = a.win[wi];
-    if (w.scalar) {
-      if (!*abort_flag)
-        for (uint64_t e = ctid; e < w.bytes / (DT == kBF16 ? 2 : 4); e += nct)
-          scalar_element<COLL, DT, OP, kMaxRanks>(a.p, P, w, e);
-      continue;
-    }
-    const int d0 = w.dst_sel < 0 ? 0 : w.dst_sel;
-    const int d1 = w.dst_sel < 0 ? P : w.dst_sel + 1;
-    for (uint32_t off = 0; off < w.bytes; off += chunk) {
-      const uint32_t n = min(chunk, w.bytes - off);
+  for (;;) {
+    const uint32_t k = it % S;
+    if (ok) ok = wait_bounded(&h.full[k], (it / S) & 1, abort_flag, a.timeout_ns, a.status, true);
+    if (ok && a.inject_timeout_ns && blockIdx.x == 0 && it == 0)
+      ok = wait_bounded(&h.never, 0, abort_flag, a.inject_timeout_ns, a.status, true);
+    const uint64_t c = ok ? h.chunk_of[k] : kNoChunk;
+    const unsigned char* st = stage_base + static_cast<size_t>(k) * nsrc * chunk;
+    if (!bulk_out) {
+      // each warp decides for itself (its lanes agree through the vote)
+      if (__any_sync(0xFFFFFFFFu, c == kNoChunk)) break;
+      loc.locate(a, c, off, n);
       const uint32_t nv = n >> 4;
-      const uint32_t k = it % S;
-      if (ok) ok = wait_bounded(&full[k], (it / S) & 1, abort_flag, a.timeout_ns, a.status, true);
-      if (ok && a.inject_timeout_ns && blockIdx.x == 0 && it == 0)
-        ok = wait_bounded(never, 0, abort_flag, a.inject_timeout_ns, a.status, true);
-      const unsigned char* st = stage_base + static_cast<size_t>(k) * nsrc * chunk;
-      if (!bulk_out) {
-        if (ok) {
-          for (uint32_t v = ctid; v < nv; v += nct) {
-            uint4 res;
-            if (COLL == kAllGather) {
-              res = reinterpret_cast<const uint4*>(st)[v];
-            } else {
-              Fold<DT, OP> f;
-              f.init(reinterpret_cast<const uint4*>(st)[v]);
+      const int d0 = loc.w.dst_sel < 0 ? 0 : loc.w.dst_sel;
+      const int d1 = loc.w.dst_sel < 0 ? P : loc.w.dst_sel + 1;
+      for (uint32_t v = ctid; v < nv; v += nct) {
+        uint4 res;
+        if (COLL == kAllGather) {
+          res = reinterpret_cast<const uint4*>(st)[v];
+        } else {
+          Fold<DT, OP> f;
+          f.init(reinterpret_cast<const uint4*>(st)[v]);
 #pragma unroll 4
-              for (int r = 1; r < P; ++r)
-                f.add(reinterpret_cast<const uint4*>(st + static_cast<size_t>(r) * chunk)[v]);
-              res = f.out();
-            }
-            const uint64_t o = w.dst_off + off + static_cast<uint64_t>(v) * 16;
-            for (int d = d0; d < d1; ++d) st_global_v4(static_cast<char*>(a.p.dst[d]) + o, res);
-          }
+          for (int r = 1; r < P; ++r)
+            f.add(reinterpret_cast<const uint4*>(st + static_cast<size_t>(r) * chunk)[v]);
+          res = f.out();
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[k]);
-      } else {
-        unsigned char* res_slot = result_base + static_cast<size_t>(it & 1) * chunk;
-        if (ctid == 0) bulk_wait_read<1>();  // the slot's previous stores have read it
-        named_bar_sync(1, nct);
-        if (ok) {
-          for (uint32_t v = ctid; v < nv; v += nct) {
-            Fold<DT, OP> f;
-            f.init(reinterpret_cast<const uint4*>(st)[v]);
-#pragma unroll 4
-            for (int r = 1; r < P; ++r)
-              f.add(reinterpret_cast<const uint4*>(st + static_cast<size_t>(r) * chunk)[v]);
-            reinterpret_cast<uint4*>(res_slot)[v] = f.out();
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[k]);
-        fence_proxy_async_smem();
-        named_bar_sync(1, nct);
-        if (ctid == 0 && ok && !*abort_flag) {
-          for (int d = d0; d < d1; ++d)
-            bulk_store(static_cast<char*>(a.p.dst[d]) + w.dst_off + off, res_slot, n);
-          bulk_commit();
-        }
+        const uint64_t o = loc.w.dst_off + off + static_cast<uint64_t>(v) * 16;
+        for (int d = d0; d < d1; ++d) st_global_v4(static_cast<char*>(a.p.dst[d]) + o, res);
       }
-      ++it;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&h.empty[k]);
+    } else {
+      unsigned char* res_slot = result_base + static_cast<size_t>(it & 1) * chunk;
+      if (ctid == 0) bulk_wait_read<1>();  // the slot's previous stores have read it
+      // all consumer threads agree whether to stop; this is also the barrier
+      // after which the result slot may be overwritten
+      if (named_bar_or(1, nct, c == kNoChunk)) break;
+      loc.locate(a, c, off, n);
+      const uint32_t nv = n >> 4;
+      for (uint32_t v = ctid; v < nv; v += nct) {
+        Fold<DT, OP> f;
+        f.init(reinterpret_cast<const uint4*>(st)[v]);
+#pragma unroll 4
+        for (int r = 1; r < P; ++r)
+          f.add(reinterpret_cast<const uint4*>(st + static_cast<size_t>(r) * chunk)[v]);
+        reinterpret_cast<uint4*>(res_slot)[v] = f.out();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&h.empty[k]);
+      fence_proxy_async_smem();
+      named_bar_sync(1, nct);
+      if (ctid == 0 && !*abort_flag) {
+        const int d0 = loc.w.dst_sel < 0 ? 0 : loc.w.dst_sel;
+        const int d1 = loc.w.dst_sel < 0 ? P : loc.w.dst_sel + 1;
+        for (int d = d0; d < d1; ++d)
+          bulk_store(static_cast<char*>(a.p.dst[d]) + loc.w.dst_off + off, res_slot, n);
+        bulk_commit();
+      }
     }
+    ++it;
   }
   if (ctid == 0) bulk_wait_all();
+  if (!*abort_flag) bulk_scalar_windows<COLL, DT, OP>(a, ctid, nct);
 }
 
 // ------------------------------------------------------------------ small engines

@@ -27,11 +27,15 @@ namespace tccl {
 namespace {
 
 constexpr size_t kScratchBytes = TCCL_NO_ALLOC_SCRATCH_BYTES;
-constexpr size_t kStatusOff = 0;            // int status word (cleared every call)
-constexpr size_t kCtaOff = 256;             // uint32_t per-CTA window offsets
-constexpr size_t kWinOff = kCtaOff + 4 * (TCCL_NO_ALLOC_MAX_CTAS + 1 + 63);  // 256-aligned
+// Layout of the scratch array (byte offsets).
+constexpr size_t kStatusOff = 0;                 // int status word (cleared every call)
+constexpr size_t kSchedOff = 64;                 // two 8-byte scheduler words (cleared every call)
+constexpr size_t kCtaOff = 256;                  // uint32_t per-CTA scalar-window offsets
+constexpr size_t kPrefixOff = kCtaOff + 4 * (TCCL_NO_ALLOC_MAX_CTAS + 1 + 63);
+constexpr size_t kMaxBody = 1023;                // body windows (chunk prefix entries - 1)
+constexpr size_t kWinOff = kPrefixOff + 8 * (kMaxBody + 1);
 constexpr size_t kMaxWindows = (kScratchBytes - kWinOff) / sizeof(Window);
-static_assert(kWinOff % 256 == 0, "window table alignment");
+static_assert(kPrefixOff % 256 == 0 && kWinOff % 256 == 0, "table alignment");
 static_assert(kMaxWindows >= TCCL_NO_ALLOC_MAX_CTAS + 3 * kMaxRanks, "scratch too small");
 
 // The scratch. Host code must not use this name as an address: on the host
@@ -106,23 +110,29 @@ extern "C" tcclResult_t tcclAllReduceNoAlloc(int nranks, const void* const sendb
   Lowered low;
   std::string why;
   if (!lower_plan(pl, sm, rm, cfg, ds->dev, cta_cap, &low, &why)) return tcclInvalidUsage;
-  if (low.shape.grid > TCCL_NO_ALLOC_MAX_CTAS || low.win.size() > kMaxWindows) {
+  if (low.shape.grid > TCCL_NO_ALLOC_MAX_CTAS || low.win.size() > kMaxWindows ||
+      (size_t)low.nbody > kMaxBody) {
     if (log_on())
       std::fprintf(stderr,
-                   "[tccl] tcclAllReduceNoAlloc: plan needs %d CTAs and %zu windows; the static "
-                   "scratch holds at most %d CTAs and %zu windows\n",
-                   low.shape.grid, low.win.size(), TCCL_NO_ALLOC_MAX_CTAS, kMaxWindows);
+                   "[tccl] tcclAllReduceNoAlloc: plan needs %d CTAs, %zu windows (%d bodies); "
+                   "the static scratch holds at most %d CTAs, %zu windows, %zu bodies\n",
+                   low.shape.grid, low.win.size(), low.nbody, TCCL_NO_ALLOC_MAX_CTAS,
+                   kMaxWindows, kMaxBody);
     return tcclInvalidUsage;
   }
 
   // Stage this call's plan into the shared scratch, in stream order, and
-  // clear the status word the kernel reports timeouts in.
+  // clear the status word the kernel reports timeouts in and the chunk
+  // scheduler's counters.
   unsigned char* base = ds->scratch;
   const size_t wbytes = low.win.size() * sizeof(Window);
+  const size_t pbytes = low.chunk_prefix.size() * sizeof(uint64_t);
   const size_t cbytes = low.cta_first.size() * sizeof(uint32_t);
-  if (cudaMemsetAsync(base + kStatusOff, 0, sizeof(int), stream) != cudaSuccess ||
+  if (cudaMemsetAsync(base + kStatusOff, 0, kCtaOff, stream) != cudaSuccess ||
       cudaMemcpyAsync(base + kCtaOff, low.cta_first.data(), cbytes, cudaMemcpyHostToDevice,
                       stream) != cudaSuccess ||
+      cudaMemcpyAsync(base + kPrefixOff, low.chunk_prefix.data(), pbytes,
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess ||
       (wbytes && cudaMemcpyAsync(base + kWinOff, low.win.data(), wbytes, cudaMemcpyHostToDevice,
                                  stream) != cudaSuccess))
     return tcclCudaError;
@@ -134,7 +144,15 @@ extern "C" tcclResult_t tcclAllReduceNoAlloc(int nranks, const void* const sendb
     a.p.dst[r] = recvbufs[r];
   }
   a.win = reinterpret_cast<const Window*>(base + kWinOff);
+  a.chunk_prefix = reinterpret_cast<const uint64_t*>(base + kPrefixOff);
   a.cta_first = reinterpret_cast<const uint32_t*>(base + kCtaOff);
+  a.total_chunks = low.total_chunks;
+  a.chunks_per_cta = low.chunks_per_cta;
+  a.nbody = low.nbody;
+  a.sched = reinterpret_cast<unsigned long long*>(base + kSchedOff);
+  a.order = low.shape.order;
+  a.prefetch_chunks = low.shape.prefetch_chunks;
+  a.load_evict_first = low.shape.load_evict_first;
   a.status = reinterpret_cast<int*>(base + kStatusOff);
   a.sm_mask = nullptr;
   a.timeout_ns = (uint64_t)(resolve_config(cfg).wait_timeout_ms * 1e6);

@@ -3,6 +3,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstring>
 
 namespace tccl {
 
@@ -48,6 +49,26 @@ bool selection(const std::vector<Interval>& iv, int p, int es, int* sel, uint64_
   *off = iv[0].begin * (uint64_t)es;
   *bytes = (iv[0].end - iv[0].begin) * (uint64_t)es;
   return true;
+}
+
+// Merges neighbours that continue each other (same selections, adjacent
+// offsets, both 16-byte bodies): for allreduce this folds the P shard bodies
+// into one window.
+std::vector<Window> merge_adjacent(const std::vector<Window>& wins) {
+  std::vector<Window> m;
+  for (const Window& w : wins) {
+    if (!m.empty()) {
+      Window& b = m.back();
+      if (!b.scalar && !w.scalar && b.src_sel == w.src_sel && b.dst_sel == w.dst_sel &&
+          b.src_off + b.bytes == w.src_off && b.dst_off + b.bytes == w.dst_off &&
+          (uint64_t)b.bytes + w.bytes <= 0xFFFFFFF0ull) {
+        b.bytes += w.bytes;
+        continue;
+      }
+    }
+    m.push_back(w);
+  }
+  return m;
 }
 
 void push_split(std::vector<Window>& out, Window w, uint64_t bytes, uint32_t limit) {
@@ -115,14 +136,22 @@ Plan plan_collective(int coll, int nranks, uint64_t count, int elem_size, int op
 
 Config resolve_config(const Config& in) {
   Config c = in;
-  if (c.small_max_bytes == 0) c.small_max_bytes = 256 * 1024;
-  if (c.stage_bytes <= 0) c.stage_bytes = 32 * 1024;
+  // defaults chosen by launch-shape sweeps on GB300 (P = 4 and 8, bf16)
+  if (c.small_max_bytes == 0) c.small_max_bytes = 128 * 1024;
+  if (c.vec_max_bytes == 0) c.vec_max_bytes = 4 * 1024 * 1024;
+  if (c.stage_bytes <= 0) c.stage_bytes = 64 * 1024;
   if (c.stages <= 0) c.stages = 8;
-  if (c.consumer_warps <= 0) c.consumer_warps = 8;
+  if (c.consumer_warps <= 0) c.consumer_warps = 16;
   if (c.consumer_warps > 31) c.consumer_warps = 31;
   if (c.ctas_per_sm <= 0) c.ctas_per_sm = 1;
   if (c.ctas_per_sm > 4) c.ctas_per_sm = 4;
   if (c.wait_timeout_ms <= 0) c.wait_timeout_ms = 2000.0;
+  if (c.chunk_order < kOrderAuto || c.chunk_order > kOrderDynamic) c.chunk_order = kOrderAuto;
+  if (c.prefetch_chunks < 0) c.prefetch_chunks = 0;
+  if (c.prefetch_chunks > 64) c.prefetch_chunks = 64;
+  if (c.load_policy < 0 || c.load_policy > 2) c.load_policy = 0;
+  if (c.max_chunk_bytes == 0) c.max_chunk_bytes = 16384;
+  c.max_chunk_bytes = std::min<size_t>(std::max<size_t>(c.max_chunk_bytes, 256), 65536) & ~(size_t)15;
   return c;
 }
 
@@ -231,33 +260,24 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
     }
   }
 
-  // ---- 3. engine choice
+  // ---- 3. engine choice: the warp engine for the smallest messages (one
+  // lane per vector and rank), the vec engine for mid sizes, the bulk (TMA)
+  // pipeline for large messages and for every capped large call
+  const int max_ctas_total = std::max(1, dev.sm_count) * std::max(1, cfg.ctas_per_sm);
+  const bool capped = cta_cap > 0 && cta_cap < max_ctas_total;
   int engine = cfg.engine;
   if (engine == kEngineAuto) {
-    bool small = message_bytes(plan.coll, p, plan.count, es) <= cfg.small_max_bytes;
-    engine = small ? kEngineWarp : kEngineBulk;
+    const uint64_t mb = message_bytes(plan.coll, p, plan.count, es);
+    if (mb <= cfg.small_max_bytes) engine = kEngineWarp;
+    else if (mb <= cfg.vec_max_bytes && !capped) engine = kEngineVec;
+    else engine = kEngineBulk;
   }
   if (engine == kEngineWarp && p > 32) engine = kEngineVec;
   LaunchShape& sh = out->shape;
   sh.engine = engine;
-  const int max_ctas_total = std::max(1, dev.sm_count) * std::max(1, cfg.ctas_per_sm);
 
   if (engine == kEngineWarp || engine == kEngineVec) {
-    // merge neighbours that continue each other (same selections, adjacent
-    // offsets): for allreduce this folds the P shard bodies into one window
-    std::vector<Window> m;
-    for (const Window& w : wins) {
-      if (!m.empty()) {
-        Window& b = m.back();
-        if (!b.scalar && !w.scalar && b.src_sel == w.src_sel && b.dst_sel == w.dst_sel &&
-            b.src_off + b.bytes == w.src_off && b.dst_off + b.bytes == w.dst_off &&
-            (uint64_t)b.bytes + w.bytes <= 0xFFFFFFF0ull) {
-          b.bytes += w.bytes;
-          continue;
-        }
-      }
-      m.push_back(w);
-    }
+    std::vector<Window> m = merge_adjacent(wins);
     out->win = m;
     out->size_class = (p <= kSmallRanks && (int)m.size() <= kSmallWindows) ? 0 : 1;
     if ((int)m.size() > kLargeWindows) {
@@ -292,11 +312,15 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
 
   // ---- 4. bulk engine: chunks, stages, CTAs
   const int nsrc = (plan.coll == kAllGather) ? 1 : p;
+  // all-gather stores straight from the stage; a reduced chunk goes out as
+  // bulk stores from a result slot when every SM streams, and as register
+  // stores (no extra shared-memory pass) when a cap concentrates the work
   int store = cfg.store_mode;
-  if (store == kStoreAuto) store = (plan.coll == kAllGather) ? kStoreBulk : kStoreVec;
+  if (store == kStoreAuto)
+    store = (plan.coll == kAllGather || !capped) ? kStoreBulk : kStoreVec;
   sh.store_mode = store;
   uint64_t chunk = ((uint64_t)cfg.stage_bytes / nsrc) & ~(uint64_t)15;
-  chunk = std::min<uint64_t>(chunk, 16384);
+  chunk = std::min<uint64_t>(chunk, cfg.max_chunk_bytes);
   chunk = std::max<uint64_t>(chunk, 256);
   const int result_slots = (store == kStoreBulk && plan.coll != kAllGather) ? 2 : 0;
   int budget = dev.smem_optin;
@@ -319,51 +343,43 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
   sh.consumer_warps = cfg.consumer_warps;
   sh.threads = 32 * (1 + cfg.consumer_warps);
   sh.release_lag = std::max(1, std::min(7, stages / 2));
+  sh.prefetch_chunks = cfg.prefetch_chunks;
+  sh.load_evict_first = cfg.load_policy == 1 ? 1 : 0;
   sh.smem = 1024 + (size_t)stages * nsrc * chunk + (size_t)result_slots * chunk;
 
-  std::vector<Window> vecw, scal;
-  uint64_t body = 0, sbytes = 0;
-  for (const Window& w : wins) {
+  std::vector<Window> body, scal;
+  uint64_t sbytes = 0;
+  for (const Window& w : merge_adjacent(wins)) {
     if (w.scalar) {
       scal.push_back(w);
       sbytes += w.bytes;
     } else {
-      vecw.push_back(w);
-      body += w.bytes;
+      body.push_back(w);
     }
   }
   int max_g = max_ctas_total;
   if (cta_cap > 0) max_g = std::min(max_g, cta_cap);
-  int grid;
-  std::vector<Window> assigned;
-  if (body > 0) {
-    grid = (int)std::min<uint64_t>(max_g, ceil_div(body, chunk));
-    uint64_t per = round_up(ceil_div(body, grid), 16);
-    grid = (int)ceil_div(body, per);
-    // cut the concatenated vector windows into `grid` contiguous pieces
-    uint64_t pos = 0;
-    for (const Window& w : vecw) {
-      uint64_t wb = 0;
-      while (wb < w.bytes) {
-        uint64_t cta = (pos + wb) / per;
-        uint64_t cta_end = (cta + 1) * per;
-        uint64_t n = std::min<uint64_t>(w.bytes - wb, cta_end - (pos + wb));
-        Window piece = w;
-        piece.src_off += wb;
-        piece.dst_off += wb;
-        piece.bytes = (uint32_t)n;
-        piece.cta = (int32_t)cta;
-        assigned.push_back(piece);
-        wb += n;
-      }
-      pos += w.bytes;
-    }
-  } else {
-    grid = 1;
+  // body windows -> one sequence of chunks
+  out->nbody = (int)body.size();
+  out->chunk_prefix.assign(body.size() + 1, 0);
+  for (size_t i = 0; i < body.size(); ++i)
+    out->chunk_prefix[i + 1] = out->chunk_prefix[i] + ceil_div(body[i].bytes, chunk);
+  const uint64_t total = out->chunk_prefix.back();
+  out->total_chunks = total;
+  int grid = total > 0 ? (int)std::min<uint64_t>(max_g, total) : 1;
+  // uncapped: claim chunks dynamically (SMs stream at different rates);
+  // capped: a fixed cyclic share per CTA
+  int order = cfg.chunk_order != kOrderAuto ? cfg.chunk_order
+                                            : (capped ? kOrderCyclic : kOrderDynamic);
+  sh.order = order;
+  if (total > 0 && order == kOrderBlocked) {
+    out->chunks_per_cta = ceil_div(total, (uint64_t)grid);
+    grid = (int)ceil_div(total, out->chunks_per_cta);
   }
+  // element-wise windows: cut into pieces and bound to CTAs round robin
+  std::vector<Window> pieces;
   if (!scal.empty()) {
     uint64_t limit = std::max<uint64_t>(4096, round_up(ceil_div(sbytes, (uint64_t)max_g), es));
-    std::vector<Window> pieces;
     for (const Window& w : scal) {
       Window x = w;
       uint64_t left = w.bytes;
@@ -376,20 +392,32 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
         left -= n;
       }
     }
-    if (body == 0) grid = (int)std::min<uint64_t>(max_g, pieces.size());
-    for (size_t i = 0; i < pieces.size(); ++i) {
-      pieces[i].cta = (int32_t)(i % (size_t)grid);
-      assigned.push_back(pieces[i]);
-    }
+    if (total == 0) grid = (int)std::min<uint64_t>(max_g, pieces.size());
+    for (size_t i = 0; i < pieces.size(); ++i) pieces[i].cta = (int32_t)(i % (size_t)grid);
+    std::stable_sort(pieces.begin(), pieces.end(),
+                     [](const Window& x, const Window& y) { return x.cta < y.cta; });
   }
-  std::stable_sort(assigned.begin(), assigned.end(),
-                   [](const Window& x, const Window& y) { return x.cta < y.cta; });
-  out->win = assigned;
+  out->win = body;
+  out->win.insert(out->win.end(), pieces.begin(), pieces.end());
   out->cta_first.assign(grid + 1, 0);
-  for (const Window& w : assigned) out->cta_first[w.cta + 1]++;
+  for (const Window& w : pieces) out->cta_first[w.cta + 1]++;
   for (int i = 0; i < grid; ++i) out->cta_first[i + 1] += out->cta_first[i];
   sh.grid = grid;
   return true;
+}
+
+void pack_bulk_table(const Lowered& low, std::vector<unsigned char>* out, size_t* off_prefix,
+                     size_t* off_cta, size_t* off_sched) {
+  const size_t wbytes = low.win.size() * sizeof(Window);
+  const size_t pbytes = low.chunk_prefix.size() * sizeof(uint64_t);
+  const size_t cbytes = low.cta_first.size() * sizeof(uint32_t);
+  *off_prefix = wbytes;
+  *off_cta = wbytes + pbytes;
+  *off_sched = (wbytes + pbytes + cbytes + 15) & ~(size_t)15;  // two zeroed 8-byte words
+  out->assign(*off_sched + 16, 0);
+  if (wbytes) std::memcpy(out->data(), low.win.data(), wbytes);
+  if (pbytes) std::memcpy(out->data() + *off_prefix, low.chunk_prefix.data(), pbytes);
+  if (cbytes) std::memcpy(out->data() + *off_cta, low.cta_first.data(), cbytes);
 }
 
 }  // namespace tccl

@@ -65,12 +65,17 @@ struct DeviceDesc {
 struct Config {
   int engine = kEngineAuto;
   size_t small_max_bytes = 0;
+  size_t vec_max_bytes = 0;
   int stage_bytes = 0;
   int stages = 0;
   int store_mode = kStoreAuto;
   int consumer_warps = 0;
   int ctas_per_sm = 0;
   double wait_timeout_ms = 0;
+  int chunk_order = kOrderAuto;
+  int prefetch_chunks = -1;   // -1: library default
+  int load_policy = 0;        // 0 default (evict-normal), 1 evict-first, 2 evict-normal
+  size_t max_chunk_bytes = 0;
 };
 
 // Fills zero fields with the library defaults.
@@ -78,8 +83,13 @@ Config resolve_config(const Config& in);
 
 struct Lowered {
   LaunchShape shape;
-  std::vector<Window> win;           // bulk: sorted by CTA; small engines: in plan order
-  std::vector<uint32_t> cta_first;   // bulk: grid + 1 entries
+  std::vector<Window> win;           // bulk: body windows, then scalar windows by CTA;
+                                     // small engines: in plan order
+  int nbody = 0;                     // bulk: body windows at the front of `win`
+  std::vector<uint64_t> chunk_prefix;  // bulk: nbody + 1 entries
+  uint64_t total_chunks = 0;         // bulk
+  uint64_t chunks_per_cta = 0;       // bulk, blocked order
+  std::vector<uint32_t> cta_first;   // bulk: grid + 1 entries into the scalar windows
   std::vector<uint64_t> vec_prefix;  // small engines: nwin + 1 entries
   std::vector<uint64_t> elem_prefix; // small engines: nwin + 1 entries
   int ntasks = 0;
@@ -92,6 +102,12 @@ struct Lowered {
 bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv_mod16,
                 const Config& cfg, const DeviceDesc& dev, int cta_cap, Lowered* out,
                 std::string* why);
+
+// Serialises a bulk plan's device table: windows, then the chunk prefix
+// (8-byte aligned), then the per-CTA scalar-window offsets, then the two
+// zeroed scheduler words of the dynamic chunk order.
+void pack_bulk_table(const Lowered& low, std::vector<unsigned char>* out, size_t* off_prefix,
+                     size_t* off_cta, size_t* off_sched);
 
 // Checks a collective call's arguments: enums, rank count, null and
 // misaligned pointers, size overflow, and buffer overlap (only the NCCL

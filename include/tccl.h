@@ -28,7 +28,9 @@
  *    alignment is accepted; 16-byte co-aligned buffers take the fast path.
  *  - The library never aborts, traps or prints (unless the environment
  *    variable TCCL_LOG is set to 1 or 2, which dumps plans to stderr).
- *  - A group is not thread safe: serialise calls on one group.
+ *  - A group is not thread safe: serialise calls on one group. The GPU work of
+ *    two calls on one group must not overlap either (as with one NCCL
+ *    communicator): calls on different streams need an ordering between them.
  */
 #ifndef TCCL_H
 #define TCCL_H
@@ -75,21 +77,36 @@ typedef enum {
   tcclStoreVec = 2   /* reduced vector held once in registers, P 128-bit stores */
 } tcclStoreMode_t;
 
+/* How the bulk engine's persistent CTAs share the chunks of a call. */
+typedef enum {
+  tcclOrderAuto = 0,
+  tcclOrderBlocked = 1, /* CTA j takes one contiguous run of chunks */
+  tcclOrderCyclic = 2,  /* CTA j takes chunks j, j+G, j+2G, ...: all CTAs sweep the buffers together */
+  tcclOrderDynamic = 3  /* CTAs claim chunks from a device counter: faster SMs take more (default) */
+} tcclChunkOrder_t;
+
 /*
  * Tuning knobs of a group. Defaults come from tcclGroupCreate (which also
- * reads TCCL_ENGINE, TCCL_SMALL_MAX_BYTES, TCCL_STAGE_BYTES, TCCL_STAGES,
- * TCCL_STORE_MODE, TCCL_CONSUMER_WARPS, TCCL_CTAS_PER_SM and
- * TCCL_WAIT_TIMEOUT_MS once). Zero in a field means "library default".
+ * reads TCCL_ENGINE, TCCL_SMALL_MAX_BYTES, TCCL_VEC_MAX_BYTES, TCCL_STAGE_BYTES, TCCL_STAGES,
+ * TCCL_STORE_MODE, TCCL_CONSUMER_WARPS, TCCL_CTAS_PER_SM,
+ * TCCL_WAIT_TIMEOUT_MS, TCCL_CHUNK_ORDER, TCCL_PREFETCH_CHUNKS,
+ * TCCL_LOAD_POLICY and TCCL_MAX_CHUNK_BYTES once). Zero in a field means "library default".
  */
 typedef struct {
   int engine;              /* tcclEngine_t */
-  size_t small_max_bytes;  /* Auto picks the small-message path at or below this many bytes per rank buffer */
+  size_t small_max_bytes;  /* Auto picks the warp engine at or below this many bytes per rank buffer */
+  size_t vec_max_bytes;    /* ... and the vec engine up to this many (uncapped calls only) */
   int stage_bytes;         /* bulk engine: shared-memory bytes of one pipeline stage (all sources of one chunk) */
   int stages;              /* bulk engine: pipeline depth (reduced to what shared memory holds) */
   int store_mode;          /* tcclStoreMode_t */
   int consumer_warps;      /* bulk engine: reducing warps per CTA (one more warp issues loads) */
   int ctas_per_sm;         /* bulk engine: resident CTAs per SM the grid is sized for (1 or 2) */
   double wait_timeout_ms;  /* device-side bound on every wait before it reports tcclDeviceTimeout */
+  int chunk_order;         /* bulk engine: tcclChunkOrder_t */
+  int prefetch_chunks;     /* bulk engine: chunks prefetched into L2 beyond the shared-memory ring
+                              (-1 in SetConfig keeps the library default, 0 turns it off) */
+  int load_policy;         /* bulk engine: L2 policy of bulk loads: 0 default, 1 evict-first, 2 evict-normal */
+  size_t max_chunk_bytes;  /* bulk engine: upper bound on bytes per source per chunk */
 } tcclConfig_t;
 
 /* What the last launch on a group looked like. */
@@ -103,6 +120,8 @@ typedef struct {
   int windows;         /* physical windows in the lowered plan */
   int tasks;           /* logical tasks in the plan */
   size_t smem_bytes;   /* dynamic shared memory per CTA */
+  int chunk_order;     /* bulk engine: tcclChunkOrder_t used (0 otherwise) */
+  uint64_t total_chunks; /* bulk engine: chunks per source in the call */
 } tcclLaunchInfo_t;
 
 const char* tcclGetErrorString(tcclResult_t r);
@@ -192,10 +211,10 @@ tcclResult_t tcclGroupReadSmRecord(tcclGroup_t g, int* distinct_sms);
  * The buffer addresses are only used for their alignment and overlap.
  * Writes up to `max_windows` windows, eight int64 values each:
  *   {cta, src_sel, src_off, dst_sel, dst_off, bytes, scalar, task}:
- * owning CTA (-1 when the engine does not bind
- * windows to CTAs), source rank or -1 for all ranks, byte offset into the
- * source buffer(s), destination rank or -1, byte offset into the
- * destination buffer(s), window bytes, 1 if the window needs the
+ * owning CTA (-1 unless the window is element-wise and run by the bulk
+ * engine, which binds those to CTAs), source rank or -1 for all ranks, byte
+ * offset into the source buffer(s), destination rank or -1, byte offset into
+ * the destination buffer(s), window bytes, 1 if the window needs the
  * element-wise (unaligned) path, and the logical task it came from.
  * *n_windows receives the total count, *info the launch shape.
  * Argument errors are reported exactly as the collective call would.

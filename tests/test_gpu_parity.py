@@ -131,6 +131,35 @@ def test_bulk_store_modes_and_pipeline_shapes(groups, store, stage_bytes, stages
     assert_ranks_equal(got, exp, f"store {store} stage {stage_bytes}x{stages}")
 
 
+ORDERS = {"blocked": tccl.tcclOrderBlocked, "cyclic": tccl.tcclOrderCyclic,
+          "dynamic": tccl.tcclOrderDynamic}
+
+
+@pytest.mark.parametrize("order", ["blocked", "cyclic", "dynamic"])
+@pytest.mark.parametrize("store", [tccl.tcclStoreBulk, tccl.tcclStoreVec])
+def test_bulk_chunk_orders_all_collectives(groups, order, store):
+    p, n = 4, 2_000_003
+    g = groups(p)
+    g.set_config(engine=tccl.tcclEngineBulk, store_mode=store, chunk_order=ORDERS[order],
+                 stage_bytes=0, stages=0)
+    xs = inputs("bf16", p, n)
+    for rep in range(2):  # the dynamic order's counter must be reset between launches
+        got = run_allreduce(g, xs, "bf16", "sum", cap=17 if rep else 0)
+        assert g.last_launch()["chunk_order"] == ORDERS[order]
+        assert_ranks_equal(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), f"AR {order}")
+    rc = n // p
+    sends = [to_device(x[:p * rc]) for x in xs]
+    parts = [torch.empty(rc, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    outs = [torch.empty(p * rc, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    g.reduce_scatter(sends, parts)
+    g.all_gather(parts, outs)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    exp_rs = oracle.reduce_scatter([x[:p * rc] for x in xs], "bf16", "sum", nthreads=0)
+    assert_ranks_equal([to_host(t) for t in parts], exp_rs, f"RS {order}")
+    assert_ranks_equal([to_host(t) for t in outs], oracle.allgather(exp_rs), f"AG {order}")
+
+
 @pytest.mark.parametrize("cap", [1, 3, 8, 16, 32])
 def test_cta_cap_results_and_sm_footprint(groups, cap):
     p, n = 8, 2_000_001
@@ -247,23 +276,34 @@ def test_reduce_scatter_and_allgather_in_place(groups, engine):
 
 
 # ------------------------------------------------------------------ runtime behaviour
-def test_bounded_wait_timeout_is_reported_and_context_survives(groups):
+@pytest.mark.parametrize("order", ["blocked", "dynamic"])
+@pytest.mark.parametrize("store", [tccl.tcclStoreBulk, tccl.tcclStoreVec])
+@pytest.mark.parametrize("coll", ["allreduce", "allgather"])
+def test_bounded_wait_timeout_is_reported_and_context_survives(groups, order, store, coll):
     p, n = 4, 1 << 20
     g = groups(p)
-    configure(g, "bulk")
+    g.set_config(engine=tccl.tcclEngineBulk, store_mode=store, chunk_order=ORDERS[order],
+                 stage_bytes=0, stages=0)
     xs = inputs("f32", p, n)
     sends = [to_device(x) for x in xs]
-    recvs = [torch.empty_like(s) for s in sends]
+    if coll == "allreduce":
+        recvs = [torch.empty_like(s) for s in sends]
+        run = lambda: g.all_reduce(sends, recvs)
+        exp = oracle.allreduce(xs, "f32", "sum", nthreads=0)
+    else:
+        recvs = [torch.empty(p * n, dtype=torch.float32, device="cuda") for _ in range(p)]
+        run = lambda: g.all_gather(sends, recvs)
+        exp = oracle.allgather(xs)
     assert tccl.tcclGroupInjectWaitTimeout(g.handle, True, 50.0) == tccl.tcclSuccess
-    g.all_reduce(sends, recvs)
+    run()
     assert g.query_error() == tccl.tcclDeviceTimeout
     assert g.query_error() == tccl.tcclSuccess  # cleared by the read
     assert tccl.tcclGroupInjectWaitTimeout(g.handle, False, 0.0) == tccl.tcclSuccess
-    g.all_reduce(sends, recvs)
-    torch.cuda.synchronize()
-    assert g.query_error() == tccl.tcclSuccess
-    exp = oracle.allreduce(xs, "f32", "sum", nthreads=0)
-    assert_ranks_equal([to_host(r) for r in recvs], exp, "after timeout")
+    for _ in range(2):  # later launches (and the dynamic order's counter) are sound
+        run()
+        torch.cuda.synchronize()
+        assert g.query_error() == tccl.tcclSuccess
+        assert_ranks_equal([to_host(r) for r in recvs], exp, "after timeout")
 
 
 def test_graph_capture_replay(groups):

@@ -96,11 +96,17 @@ def check_cover(coll, p, count, es, send, recv, wins, info):
             pos = e
         assert pos == dst_len
     if info.engine == tccl.tcclEngineBulk:
-        ctas = [w["cta"] for w in wins]
+        # body windows first (shared chunk sequence), then element-wise
+        # windows grouped by the CTA that runs them
+        body = [w for w in wins if not w["scalar"]]
+        assert wins[:len(body)] == body and all(w["cta"] == -1 for w in body)
+        ctas = [w["cta"] for w in wins[len(body):]]
         assert ctas == sorted(ctas)
-        assert min(ctas) >= 0 and max(ctas) < info.ctas
+        assert all(0 <= c < info.ctas for c in ctas)
+        assert info.total_chunks == sum(-(-w["bytes"] // info.chunk_bytes) for w in body)
         assert info.smem_bytes <= 232448
         assert info.stages >= 2 and info.chunk_bytes % 16 == 0
+        assert info.ctas >= 1
 
 
 CASES = list(itertools.product([AR, RS, AG], [1, 2, 3, 4, 8, 64],
@@ -163,17 +169,37 @@ def test_cta_cap_bounds_the_grid(cap):
             check_cover(AR, p, count, 2, send, recv, wins, info)
 
 
-def test_bulk_pieces_are_balanced():
-    p, count = 8, 64 << 20
+def chunk_owners(total, grid, order):
+    """Which CTA runs each chunk, as the kernel's chunk cursor walks them."""
+    owner = [None] * total
+    per = -(-total // grid)
+    for j in range(grid):
+        seq = range(j, total, grid) if order == tccl.tcclOrderCyclic else \
+            range(j * per, min((j + 1) * per, total))
+        for c in seq:
+            assert owner[c] is None
+            owner[c] = j
+    return owner
+
+
+@pytest.mark.parametrize("order", [tccl.tcclOrderCyclic, tccl.tcclOrderBlocked])
+@pytest.mark.parametrize("count", [1000, 1 << 20, 64 << 20, (64 << 20) + 7])
+@pytest.mark.parametrize("cap", [0, 16])
+def test_bulk_chunk_sequence_is_covered_once_and_balanced(order, count, cap):
+    p = 8
     send, recv = bufs(p, 0, 0)
-    r, wins, _, info = inspect(AR, p, count, tccl.tcclBfloat16, send, recv,
-                               engine=tccl.tcclEngineBulk)
-    per = {}
-    for w in wins:
-        per[w["cta"]] = per.get(w["cta"], 0) + w["bytes"]
-    sizes = sorted(per.values())
-    assert info.ctas == 152 and len(per) == 152
-    assert sizes[-1] - sizes[0] <= sizes[-1] // 100 + 16
+    c = cfg(tccl.tcclEngineBulk)
+    c.chunk_order = order
+    r, wins, _, info = tccl.tcclPlanInspect(AR, p, send, recv, count, tccl.tcclBfloat16, cap, 152,
+                                            232448, c)
+    assert r == 0 and info.chunk_order == order
+    body = [w for w in wins if not w["scalar"]]
+    assert len(body) == 1  # co-aligned allreduce: the shard bodies merge into one window
+    owner = chunk_owners(info.total_chunks, info.ctas, order)
+    assert None not in owner
+    loads = [owner.count(j) for j in range(info.ctas)]
+    assert max(loads) - min(loads) <= (1 if order == tccl.tcclOrderCyclic else max(loads))
+    assert info.ctas <= (cap or 152)
 
 
 def test_task_structure():
@@ -192,8 +218,15 @@ def test_auto_engine_choice():
     send, recv = bufs(p, 0, 0)
     r, _, _, info = inspect(AR, p, 8192, tccl.tcclBfloat16, send, recv)  # 16 KiB per rank
     assert info.engine == tccl.tcclEngineWarp
+    r, _, _, info = inspect(AR, p, 1 << 20, tccl.tcclBfloat16, send, recv)  # 2 MiB per rank
+    assert info.engine == tccl.tcclEngineVec
+    r, _, _, info = inspect(AR, p, 1 << 20, tccl.tcclBfloat16, send, recv, cap=16)
+    assert info.engine == tccl.tcclEngineBulk  # capped mid-size calls keep the TMA pipeline
     r, _, _, info = inspect(AR, p, 64 << 20, tccl.tcclBfloat16, send, recv)
     assert info.engine == tccl.tcclEngineBulk
+    assert info.chunk_order == tccl.tcclOrderDynamic and info.store_mode == tccl.tcclStoreBulk
+    r, _, _, info = inspect(AR, p, 64 << 20, tccl.tcclBfloat16, send, recv, cap=16)
+    assert info.chunk_order == tccl.tcclOrderCyclic and info.store_mode == tccl.tcclStoreVec
     r, _, _, info = inspect(AR, 40, 1024, tccl.tcclFloat32, *bufs(40, 0, 0),
                             engine=tccl.tcclEngineWarp)
     assert info.engine == tccl.tcclEngineVec  # more ranks than lanes
@@ -203,7 +236,8 @@ def test_pipeline_shape_follows_shared_memory():
     send, recv = bufs(8, 0, 0)
     r, _, _, info = inspect(AR, 8, 1 << 24, tccl.tcclBfloat16, send, recv,
                             engine=tccl.tcclEngineBulk, stage_bytes=32768, stages=32)
-    assert info.chunk_bytes == 4096 and info.stages == (232448 - 1024) // 32768
+    # uncapped allreduce: bulk stores, so two 4 KiB result slots share the budget
+    assert info.chunk_bytes == 4096 and info.stages == (232448 - 1024 - 2 * 4096) // 32768
     r, _, _, small = inspect(AR, 8, 1 << 24, tccl.tcclBfloat16, send, recv,
                              engine=tccl.tcclEngineBulk, smem=48 * 1024)
     assert small.smem_bytes <= 48 * 1024 and small.stages >= 2
