@@ -617,6 +617,24 @@ def sweep(args):
         g.close()
 
 
+# ------------------------------------------------------------------ probe mode
+def probe():
+    """Builds and runs the per-SM bandwidth probe
+    (collective_communication_planner_gb300/probes/sm_bandwidth.cu): what one
+    SM can read, write and copy with each mechanism, which bounds what a CTA
+    cap can deliver. Prints the probe's JSON lines."""
+    src = ROOT / "collective_communication_planner_gb300" / "probes" / "sm_bandwidth.cu"
+    out_dir = ROOT / "collective_communication_planner_gb300" / "_build"
+    out_dir.mkdir(exist_ok=True)
+    exe = out_dir / "sm_bandwidth_probe"
+    subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
+                           "-std=c++17", "-lineinfo", "-o", str(exe), str(src)])
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    sys.stdout.write(r.stdout)
+    if r.returncode != 0:
+        raise SystemExit(f"probe failed ({r.returncode}): {r.stderr.strip()}")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -631,7 +649,12 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="measure every configuration point of C1..C5 (one JSON line each)")
     ap.add_argument("--sweep-configs", default="", help="comma list, e.g. c3,c5")
+    ap.add_argument("--probe", action="store_true",
+                    help="run the per-SM bandwidth probe (bounds for CTA-capped runs)")
     args = ap.parse_args()
+    if args.probe:
+        probe()
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = WORKLOADS[args.workload]

@@ -25,6 +25,7 @@ tcclSum, tcclMin, tcclMax = 0, 1, 2
 tcclEngineAuto, tcclEngineBulk, tcclEngineWarp, tcclEngineVec = 0, 1, 2, 3
 tcclStoreAuto, tcclStoreBulk, tcclStoreVec = 0, 1, 2
 tcclOrderAuto, tcclOrderBlocked, tcclOrderCyclic, tcclOrderDynamic = 0, 1, 2, 3
+tcclLayoutAuto, tcclLayoutShared, tcclLayoutPerRank = 0, 1, 2
 TCCL_MAX_RANKS = 64
 
 COLL_ALLREDUCE, COLL_REDUCE_SCATTER, COLL_ALLGATHER = 0, 1, 2
@@ -40,7 +41,8 @@ class tcclConfig_t(ctypes.Structure):
                 ("store_mode", ctypes.c_int), ("consumer_warps", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("wait_timeout_ms", ctypes.c_double),
                 ("chunk_order", ctypes.c_int), ("prefetch_chunks", ctypes.c_int),
-                ("load_policy", ctypes.c_int), ("max_chunk_bytes", ctypes.c_size_t)]
+                ("load_policy", ctypes.c_int), ("max_chunk_bytes", ctypes.c_size_t),
+                ("stage_layout", ctypes.c_int)]
 
 
 class tcclLaunchInfo_t(ctypes.Structure):
@@ -48,7 +50,8 @@ class tcclLaunchInfo_t(ctypes.Structure):
                 ("threads", ctypes.c_int), ("stages", ctypes.c_int),
                 ("chunk_bytes", ctypes.c_int), ("windows", ctypes.c_int),
                 ("tasks", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
-                ("chunk_order", ctypes.c_int), ("total_chunks", ctypes.c_uint64)]
+                ("chunk_order", ctypes.c_int), ("total_chunks", ctypes.c_uint64),
+                ("stage_layout", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -170,6 +170,11 @@ Config config_from_env() {
   c.prefetch_chunks = geti("TCCL_PREFETCH_CHUNKS", -1);
   c.load_policy = geti("TCCL_LOAD_POLICY", 0);
   if (const char* e = std::getenv("TCCL_MAX_CHUNK_BYTES")) c.max_chunk_bytes = std::strtoull(e, 0, 10);
+  if (const char* e = std::getenv("TCCL_STAGE_LAYOUT")) {
+    std::string v(e);
+    if (v == "shared") c.stage_layout = kLayoutShared;
+    else if (v == "per_rank") c.stage_layout = kLayoutPerRank;
+  }
   if (const char* e = std::getenv("TCCL_CHUNK_ORDER")) {
     std::string v(e);
     if (v == "blocked") c.chunk_order = kOrderBlocked;
@@ -193,6 +198,7 @@ Config from_public(const tcclConfig_t& p) {
   c.ctas_per_sm = p.ctas_per_sm;
   c.wait_timeout_ms = p.wait_timeout_ms;
   c.chunk_order = p.chunk_order;
+  c.stage_layout = p.stage_layout;
   c.prefetch_chunks = p.prefetch_chunks;
   c.load_policy = p.load_policy;
   c.max_chunk_bytes = p.max_chunk_bytes;
@@ -212,6 +218,7 @@ tcclConfig_t to_public(const Config& c) {
   p.ctas_per_sm = c.ctas_per_sm;
   p.wait_timeout_ms = c.wait_timeout_ms;
   p.chunk_order = c.chunk_order;
+  p.stage_layout = c.stage_layout;
   p.prefetch_chunks = c.prefetch_chunks;
   p.load_policy = c.load_policy;
   p.max_chunk_bytes = c.max_chunk_bytes;
@@ -222,7 +229,8 @@ bool config_ok(const tcclConfig_t& p) {
   return p.engine >= 0 && p.engine <= 3 && p.store_mode >= 0 && p.store_mode <= 2 &&
          p.stage_bytes >= 0 && p.stages >= 0 && p.consumer_warps >= 0 && p.ctas_per_sm >= 0 &&
          p.wait_timeout_ms >= 0 && p.chunk_order >= 0 && p.chunk_order <= 3 &&
-         p.prefetch_chunks >= -1 && p.load_policy >= 0 && p.load_policy <= 2;
+         p.prefetch_chunks >= -1 && p.load_policy >= 0 && p.load_policy <= 2 &&
+         p.stage_layout >= 0 && p.stage_layout <= 2;
 }
 
 void fill_info(const Lowered& low, tcclLaunchInfo_t* info) {
@@ -238,6 +246,7 @@ void fill_info(const Lowered& low, tcclLaunchInfo_t* info) {
   info->smem_bytes = low.shape.smem;
   info->chunk_order = low.shape.engine == kEngineBulk ? low.shape.order : 0;
   info->total_chunks = low.total_chunks;
+  info->stage_layout = low.shape.engine == kEngineBulk ? (low.shape.rank_streamed ? 2 : 1) : 0;
 }
 
 void dump_plan(const Plan& pl, const Lowered& low) {
@@ -363,6 +372,7 @@ tcclResult_t run_collective(tcclGroup* g, int coll, const void* const* send, voi
       a.sched = cp->d_sched;
       a.order = low.shape.order;
       a.prefetch_chunks = low.shape.prefetch_chunks;
+      a.rank_streamed = low.shape.rank_streamed;
       a.load_evict_first = low.shape.load_evict_first;
       a.status = g->d_status;
       a.sm_mask = mask;

@@ -18,6 +18,13 @@ enum RedOp : int { kSum = 0, kMin = 1, kMax = 2 };
 enum Engine : int { kEngineAuto = 0, kEngineBulk = 1, kEngineWarp = 2, kEngineVec = 3 };
 enum StoreMode : int { kStoreAuto = 0, kStoreBulk = 1, kStoreVec = 2 };
 enum ChunkOrder : int { kOrderAuto = 0, kOrderBlocked = 1, kOrderCyclic = 2, kOrderDynamic = 3 };
+// Bulk engine stage layout: a stage holds one chunk of every source rank
+// (kLayoutShared), or one rank's chunk (kLayoutPerRank: P stages per chunk,
+// partial sums kept in registers, TMA copies as large as a whole stage).
+enum StageLayout : int { kLayoutAuto = 0, kLayoutShared = 1, kLayoutPerRank = 2 };
+
+constexpr int kMaxConsumerWarps = 16;  // bulk kernel: 1 + 16 warps = 544 threads
+constexpr int kPerRankVectors = 4;     // per-rank layout: 16-byte vectors per consumer thread
 
 // Status codes a kernel may leave in the group's status word (same values
 // as tcclResult_t).
@@ -73,6 +80,7 @@ struct BulkArgs {
   int consumer_warps;
   int release_lag;               // all-gather bulk stores: store groups kept in flight
   int elem_size;
+  int rank_streamed;             // kLayoutPerRank (1) or kLayoutShared (0)
   int prefetch_chunks;           // L2 prefetch distance beyond the shared-memory ring (0: off)
   int load_evict_first;          // bulk loads carry an L2 evict-first policy
 };
@@ -101,6 +109,7 @@ struct LaunchShape {
   int consumer_warps = 0;
   int release_lag = 0;
   int order = 0;
+  int rank_streamed = 0;
   int prefetch_chunks = 0;
   int load_evict_first = 0;
   size_t smem = 0;

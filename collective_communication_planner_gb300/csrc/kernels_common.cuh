@@ -417,8 +417,70 @@ __device__ __forceinline__ void bulk_scalar_windows(const BulkArgs& a, int ctid,
   }
 }
 
+// Consumers of the per-rank stage layout: a chunk arrives as P consecutive
+// stages (rank 0 first); each consumer thread folds its kPerRankVectors
+// vectors of every stage into fp32 / int32 registers and, after rank P-1,
+// stores the result to every destination. Only 128-bit register stores.
 template <int COLL, int DT, int OP>
-__global__ void __launch_bounds__(1024, 1) bulk_kernel(const __grid_constant__ BulkArgs a) {
+__device__ __forceinline__ void per_rank_consumers(const BulkArgs& a, BulkSmemHead& h,
+                                                   const unsigned char* stage_base, int ctid,
+                                                   int nct, int lane) {
+  constexpr int V = kPerRankVectors;
+  const int S = a.stages;
+  const int P = a.nranks;
+  const uint32_t chunk = static_cast<uint32_t>(a.chunk_bytes);
+  volatile int* abort_flag = &h.abort_flag;
+  ChunkLocator loc;
+  loc.init();
+  uint32_t it = 0, off = 0, n = 0;
+  bool ok = true;
+  for (;;) {
+    Fold<DT, OP> acc[V];
+    bool stop = false;
+    for (int r = 0; r < P; ++r) {
+      const uint32_t k = it % S;
+      if (ok) ok = wait_bounded(&h.full[k], (it / S) & 1, abort_flag, a.timeout_ns, a.status, true);
+      if (ok && a.inject_timeout_ns && blockIdx.x == 0 && it == 0)
+        ok = wait_bounded(&h.never, 0, abort_flag, a.inject_timeout_ns, a.status, true);
+      const uint64_t c = (ok && r == 0) ? h.chunk_of[k] : 0;
+      if (__any_sync(0xFFFFFFFFu, !ok || c == kNoChunk)) {
+        stop = true;
+        break;
+      }
+      if (r == 0) loc.locate(a, c, off, n);
+      const uint4* st = reinterpret_cast<const uint4*>(stage_base + static_cast<size_t>(k) * chunk);
+      const uint32_t nv = n >> 4;
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const uint32_t v = ctid + j * nct;
+        if (v < nv) {
+          if (r == 0) acc[j].init(st[v]);
+          else acc[j].add(st[v]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&h.empty[k]);
+      ++it;
+    }
+    if (stop) break;
+    const uint32_t nv = n >> 4;
+    const int d0 = loc.w.dst_sel < 0 ? 0 : loc.w.dst_sel;
+    const int d1 = loc.w.dst_sel < 0 ? P : loc.w.dst_sel + 1;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const uint32_t v = ctid + j * nct;
+      if (v < nv) {
+        const uint4 res = acc[j].out();
+        const uint64_t o = loc.w.dst_off + off + static_cast<uint64_t>(v) * 16;
+        for (int d = d0; d < d1; ++d) st_global_v4(static_cast<char*>(a.p.dst[d]) + o, res);
+      }
+    }
+  }
+}
+
+template <int COLL, int DT, int OP>
+__global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
+    bulk_kernel(const __grid_constant__ BulkArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   BulkSmemHead& h = *reinterpret_cast<BulkSmemHead*>(smem);
   volatile int* abort_flag = &h.abort_flag;
@@ -507,6 +569,30 @@ __global__ void __launch_bounds__(1024, 1) bulk_kernel(const __grid_constant__ B
         break;
       }
       loc.locate(a, c, off, n);
+      if (COLL != kAllGather && a.rank_streamed) {
+        // P stages for this chunk, rank 0 first; rank 0's slot carries the index
+        h.chunk_of[k] = c;
+        bool stream_ok = true;
+        for (int r = 0; r < P; ++r) {
+          const uint32_t kr = it % S;
+          if (r > 0 && it >= static_cast<uint32_t>(S)) {
+            stream_ok = wait_bounded(&h.empty[kr], ((it / S) & 1) ^ 1, abort_flag, a.timeout_ns,
+                                     a.status, true);
+            if (!stream_ok) break;
+          }
+          mbar_arrive_expect_tx(&h.full[kr], n);
+          const char* src = static_cast<const char*>(a.p.src[r]) + loc.w.src_off + off;
+          unsigned char* dst = stage_base + static_cast<size_t>(kr) * chunk;
+          if (a.load_evict_first) bulk_load_hint(dst, src, n, &h.full[kr], policy);
+          else bulk_load(dst, src, n, &h.full[kr]);
+          ++it;
+        }
+        if (!stream_ok) {
+          ok = false;
+          break;
+        }
+        continue;
+      }
       h.chunk_of[k] = c;
       mbar_arrive_expect_tx(&h.full[k], n * nsrc);
       unsigned char* st = stage_base + static_cast<size_t>(k) * nsrc * chunk;
@@ -577,6 +663,13 @@ __global__ void __launch_bounds__(1024, 1) bulk_kernel(const __grid_constant__ B
       }
       bulk_wait_all();
     }
+    if (!*abort_flag) bulk_scalar_windows<COLL, DT, OP>(a, ctid, nct);
+    return;
+  }
+
+  if (COLL != kAllGather && a.rank_streamed) {
+    per_rank_consumers<COLL, DT, OP>(a, h, stage_base, ctid, nct, lane);
+    if (ctid == 0) bulk_wait_all();
     if (!*abort_flag) bulk_scalar_windows<COLL, DT, OP>(a, ctid, nct);
     return;
   }

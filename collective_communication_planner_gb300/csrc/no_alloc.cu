@@ -152,6 +152,7 @@ extern "C" tcclResult_t tcclAllReduceNoAlloc(int nranks, const void* const sendb
   a.sched = reinterpret_cast<unsigned long long*>(base + kSchedOff);
   a.order = low.shape.order;
   a.prefetch_chunks = low.shape.prefetch_chunks;
+  a.rank_streamed = low.shape.rank_streamed;
   a.load_evict_first = low.shape.load_evict_first;
   a.status = reinterpret_cast<int*>(base + kStatusOff);
   a.sm_mask = nullptr;

@@ -142,7 +142,8 @@ Config resolve_config(const Config& in) {
   if (c.stage_bytes <= 0) c.stage_bytes = 64 * 1024;
   if (c.stages <= 0) c.stages = 8;
   if (c.consumer_warps <= 0) c.consumer_warps = 16;
-  if (c.consumer_warps > 31) c.consumer_warps = 31;
+  if (c.consumer_warps > kMaxConsumerWarps) c.consumer_warps = kMaxConsumerWarps;
+  if (c.stage_layout < kLayoutAuto || c.stage_layout > kLayoutPerRank) c.stage_layout = kLayoutAuto;
   if (c.ctas_per_sm <= 0) c.ctas_per_sm = 1;
   if (c.ctas_per_sm > 4) c.ctas_per_sm = 4;
   if (c.wait_timeout_ms <= 0) c.wait_timeout_ms = 2000.0;
@@ -311,17 +312,27 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
   }
 
   // ---- 4. bulk engine: chunks, stages, CTAs
-  const int nsrc = (plan.coll == kAllGather) ? 1 : p;
+  int layout = cfg.stage_layout;
+  if (plan.coll == kAllGather) layout = kLayoutShared;  // one source: nothing to stream
+  // many ranks make the shared layout's per-rank copies tiny (64 KiB / P);
+  // below 2 KiB per copy the per-rank layout, with whole-stage copies, wins
+  if (layout == kLayoutAuto)
+    layout = ((uint64_t)cfg.stage_bytes / (uint64_t)p < 2048) ? kLayoutPerRank : kLayoutShared;
+  sh.rank_streamed = layout == kLayoutPerRank ? 1 : 0;
+  const int nsrc = (plan.coll == kAllGather || sh.rank_streamed) ? 1 : p;
   // all-gather stores straight from the stage; a reduced chunk goes out as
   // bulk stores from a result slot when every SM streams, and as register
   // stores (no extra shared-memory pass) when a cap concentrates the work
   int store = cfg.store_mode;
   if (store == kStoreAuto)
     store = (plan.coll == kAllGather || !capped) ? kStoreBulk : kStoreVec;
+  if (sh.rank_streamed) store = kStoreVec;  // the sums leave from registers
   sh.store_mode = store;
   uint64_t chunk = ((uint64_t)cfg.stage_bytes / nsrc) & ~(uint64_t)15;
   chunk = std::min<uint64_t>(chunk, cfg.max_chunk_bytes);
   chunk = std::max<uint64_t>(chunk, 256);
+  if (sh.rank_streamed)  // every consumer thread owns kPerRankVectors vectors of a chunk
+    chunk = (uint64_t)16 * kPerRankVectors * 32 * cfg.consumer_warps;
   const int result_slots = (store == kStoreBulk && plan.coll != kAllGather) ? 2 : 0;
   int budget = dev.smem_optin;
   if (dev.smem_per_sm > 0)
@@ -330,7 +341,7 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
   for (;;) {
     int64_t room = (int64_t)budget - 1024 - (int64_t)result_slots * (int64_t)chunk;
     stages = room > 0 ? (int)std::min<int64_t>(cfg.stages, room / (int64_t)(nsrc * chunk)) : 0;
-    if (stages >= 2 || chunk <= 16) break;
+    if (stages >= 2 || chunk <= 16 || sh.rank_streamed) break;
     chunk = std::max<uint64_t>(16, (chunk / 2) & ~(uint64_t)15);
   }
   if (stages < 2) {

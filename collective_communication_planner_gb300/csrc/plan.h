@@ -73,6 +73,7 @@ struct Config {
   int ctas_per_sm = 0;
   double wait_timeout_ms = 0;
   int chunk_order = kOrderAuto;
+  int stage_layout = kLayoutAuto;
   int prefetch_chunks = -1;   // -1: library default
   int load_policy = 0;        // 0 default (evict-normal), 1 evict-first, 2 evict-normal
   size_t max_chunk_bytes = 0;

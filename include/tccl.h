@@ -77,6 +77,14 @@ typedef enum {
   tcclStoreVec = 2   /* reduced vector held once in registers, P 128-bit stores */
 } tcclStoreMode_t;
 
+/* What one bulk-engine pipeline stage holds. */
+typedef enum {
+  tcclLayoutAuto = 0,
+  tcclLayoutShared = 1,  /* one chunk of every source rank: the fold reads P rows of a stage */
+  tcclLayoutPerRank = 2  /* one rank's chunk: P consecutive stages per chunk, partial sums in
+                            registers; each bulk copy is a whole stage whatever P is */
+} tcclStageLayout_t;
+
 /* How the bulk engine's persistent CTAs share the chunks of a call. */
 typedef enum {
   tcclOrderAuto = 0,
@@ -90,7 +98,7 @@ typedef enum {
  * reads TCCL_ENGINE, TCCL_SMALL_MAX_BYTES, TCCL_VEC_MAX_BYTES, TCCL_STAGE_BYTES, TCCL_STAGES,
  * TCCL_STORE_MODE, TCCL_CONSUMER_WARPS, TCCL_CTAS_PER_SM,
  * TCCL_WAIT_TIMEOUT_MS, TCCL_CHUNK_ORDER, TCCL_PREFETCH_CHUNKS,
- * TCCL_LOAD_POLICY and TCCL_MAX_CHUNK_BYTES once). Zero in a field means "library default".
+ * TCCL_LOAD_POLICY, TCCL_MAX_CHUNK_BYTES and TCCL_STAGE_LAYOUT once). Zero in a field means "library default".
  */
 typedef struct {
   int engine;              /* tcclEngine_t */
@@ -99,7 +107,7 @@ typedef struct {
   int stage_bytes;         /* bulk engine: shared-memory bytes of one pipeline stage (all sources of one chunk) */
   int stages;              /* bulk engine: pipeline depth (reduced to what shared memory holds) */
   int store_mode;          /* tcclStoreMode_t */
-  int consumer_warps;      /* bulk engine: reducing warps per CTA (one more warp issues loads) */
+  int consumer_warps;      /* bulk engine: reducing warps per CTA, 1..16 (one more warp issues loads) */
   int ctas_per_sm;         /* bulk engine: resident CTAs per SM the grid is sized for (1 or 2) */
   double wait_timeout_ms;  /* device-side bound on every wait before it reports tcclDeviceTimeout */
   int chunk_order;         /* bulk engine: tcclChunkOrder_t */
@@ -107,6 +115,7 @@ typedef struct {
                               (-1 in SetConfig keeps the library default, 0 turns it off) */
   int load_policy;         /* bulk engine: L2 policy of bulk loads: 0 default, 1 evict-first, 2 evict-normal */
   size_t max_chunk_bytes;  /* bulk engine: upper bound on bytes per source per chunk */
+  int stage_layout;        /* bulk engine: tcclStageLayout_t */
 } tcclConfig_t;
 
 /* What the last launch on a group looked like. */
@@ -122,6 +131,7 @@ typedef struct {
   size_t smem_bytes;   /* dynamic shared memory per CTA */
   int chunk_order;     /* bulk engine: tcclChunkOrder_t used (0 otherwise) */
   uint64_t total_chunks; /* bulk engine: chunks per source in the call */
+  int stage_layout;    /* bulk engine: tcclStageLayout_t used (0 otherwise) */
 } tcclLaunchInfo_t;
 
 const char* tcclGetErrorString(tcclResult_t r);

@@ -39,8 +39,16 @@ def groups():
         g.close()
 
 
+def reset_config(g, **kw):
+    """Library defaults (a zeroed config) plus the given fields."""
+    c = tccl.tcclConfig_t()
+    for k, v in kw.items():
+        setattr(c, k, v)
+    assert tccl.tcclGroupSetConfig(g.handle, c) == tccl.tcclSuccess
+
+
 def configure(g, engine, store=tccl.tcclStoreAuto, stage_bytes=0, stages=0):
-    g.set_config(engine=ENGINES[engine] if isinstance(engine, str) else engine,
+    reset_config(g, engine=ENGINES[engine] if isinstance(engine, str) else engine,
                  store_mode=store, stage_bytes=stage_bytes, stages=stages)
 
 
@@ -140,7 +148,7 @@ ORDERS = {"blocked": tccl.tcclOrderBlocked, "cyclic": tccl.tcclOrderCyclic,
 def test_bulk_chunk_orders_all_collectives(groups, order, store):
     p, n = 4, 2_000_003
     g = groups(p)
-    g.set_config(engine=tccl.tcclEngineBulk, store_mode=store, chunk_order=ORDERS[order],
+    reset_config(g, engine=tccl.tcclEngineBulk, store_mode=store, chunk_order=ORDERS[order],
                  stage_bytes=0, stages=0)
     xs = inputs("bf16", p, n)
     for rep in range(2):  # the dynamic order's counter must be reset between launches
@@ -158,6 +166,44 @@ def test_bulk_chunk_orders_all_collectives(groups, order, store):
     exp_rs = oracle.reduce_scatter([x[:p * rc] for x in xs], "bf16", "sum", nthreads=0)
     assert_ranks_equal([to_host(t) for t in parts], exp_rs, f"RS {order}")
     assert_ranks_equal([to_host(t) for t in outs], oracle.allgather(exp_rs), f"AG {order}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("op", ["sum", "min", "max"])
+@pytest.mark.parametrize("cw", [8, 16])
+def test_per_rank_stage_layout(groups, dtype, op, cw):
+    for p, n, cap in ((2, 1_000_003, 0), (8, 700_001, 0), (5, 123_457, 7), (8, 1 << 20, 16)):
+        g = groups(p)
+        reset_config(g, engine=tccl.tcclEngineBulk, stage_layout=tccl.tcclLayoutPerRank,
+                     consumer_warps=cw, store_mode=0, stage_bytes=0, stages=0, chunk_order=0)
+        xs = inputs(dtype, p, n)
+        got = run_allreduce(g, xs, dtype, op, cap=cap)
+        info = g.last_launch()
+        assert info["stage_layout"] == tccl.tcclLayoutPerRank
+        assert_ranks_equal(got, oracle.allreduce(xs, dtype, op, nthreads=0),
+                           f"per-rank AR {dtype} {op} P={p} cap={cap}")
+    # reduce-scatter through the same layout
+    p, rc = 4, 250_007
+    g = groups(p)
+    xs = inputs(dtype, p, p * rc)
+    sends = [to_device(x) for x in xs]
+    parts = [torch.empty(rc, dtype=TORCH_OF[dtype], device="cuda") for _ in range(p)]
+    g.reduce_scatter(sends, parts, op=op)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    assert_ranks_equal([to_host(t) for t in parts],
+                       oracle.reduce_scatter(xs, dtype, op, nthreads=0), "per-rank RS")
+
+
+def test_per_rank_layout_many_ranks(groups):
+    p, n = 64, 200_003
+    g = groups(p)
+    xs = inputs("bf16", p, n)
+    exp = oracle.allreduce(xs, "bf16", "sum", nthreads=0)
+    for layout in (tccl.tcclLayoutShared, tccl.tcclLayoutPerRank):
+        reset_config(g, engine=tccl.tcclEngineBulk, stage_layout=layout, consumer_warps=16,
+                     store_mode=0, stage_bytes=0, stages=0, chunk_order=0)
+        assert_ranks_equal(run_allreduce(g, xs, "bf16", "sum"), exp, f"P=64 layout {layout}")
 
 
 @pytest.mark.parametrize("cap", [1, 3, 8, 16, 32])
@@ -277,13 +323,14 @@ def test_reduce_scatter_and_allgather_in_place(groups, engine):
 
 # ------------------------------------------------------------------ runtime behaviour
 @pytest.mark.parametrize("order", ["blocked", "dynamic"])
-@pytest.mark.parametrize("store", [tccl.tcclStoreBulk, tccl.tcclStoreVec])
+@pytest.mark.parametrize("store", [tccl.tcclStoreBulk, tccl.tcclStoreVec, "per_rank"])
 @pytest.mark.parametrize("coll", ["allreduce", "allgather"])
 def test_bounded_wait_timeout_is_reported_and_context_survives(groups, order, store, coll):
     p, n = 4, 1 << 20
     g = groups(p)
-    g.set_config(engine=tccl.tcclEngineBulk, store_mode=store, chunk_order=ORDERS[order],
-                 stage_bytes=0, stages=0)
+    layout = tccl.tcclLayoutPerRank if store == "per_rank" else tccl.tcclLayoutShared
+    reset_config(g, engine=tccl.tcclEngineBulk, store_mode=0 if store == "per_rank" else store,
+                 chunk_order=ORDERS[order], stage_bytes=0, stages=0, stage_layout=layout)
     xs = inputs("f32", p, n)
     sends = [to_device(x) for x in xs]
     if coll == "allreduce":

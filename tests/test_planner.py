@@ -243,6 +243,46 @@ def test_pipeline_shape_follows_shared_memory():
     assert small.smem_bytes <= 48 * 1024 and small.stages >= 2
 
 
+@pytest.mark.parametrize("p", [2, 8, 64])
+@pytest.mark.parametrize("cw", [8, 16])
+def test_per_rank_stage_layout_shape(p, cw):
+    send, recv = bufs(p, 0, 0)
+    c = cfg(tccl.tcclEngineBulk)
+    c.stage_layout = tccl.tcclLayoutPerRank
+    c.consumer_warps = cw
+    r, wins, _, info = tccl.tcclPlanInspect(AR, p, send, recv, 1 << 22, tccl.tcclBfloat16, 0,
+                                            152, 232448, c)
+    assert r == 0 and info.stage_layout == tccl.tcclLayoutPerRank
+    # a stage is one rank's chunk: 4 vectors per consumer thread, whatever P is
+    assert info.chunk_bytes == 16 * 4 * 32 * cw
+    assert info.store_mode == tccl.tcclStoreVec
+    assert info.smem_bytes == 1024 + info.stages * info.chunk_bytes <= 232448
+    check_cover(AR, p, 1 << 22, 2, send, recv, wins, info)
+    # all-gather keeps the shared layout (a single source)
+    r, _, _, info = tccl.tcclPlanInspect(AG, p, send, recv, 1 << 16, tccl.tcclBfloat16, 0, 152,
+                                         232448, c)
+    assert info.stage_layout == tccl.tcclLayoutShared
+
+
+def test_auto_layout_switches_to_per_rank_for_many_ranks():
+    for p, exp in ((8, tccl.tcclLayoutShared), (16, tccl.tcclLayoutShared),
+                   (32, tccl.tcclLayoutShared), (33, tccl.tcclLayoutPerRank),
+                   (64, tccl.tcclLayoutPerRank)):
+        send, recv = bufs(p, 0, 0)
+        r, _, _, info = tccl.tcclPlanInspect(AR, p, send, recv, 1 << 22, tccl.tcclBfloat16, 0,
+                                             152, 232448, cfg(tccl.tcclEngineBulk))
+        assert r == 0 and info.stage_layout == exp, p
+
+
+def test_consumer_warps_are_capped_at_sixteen():
+    send, recv = bufs(4, 0, 0)
+    c = cfg(tccl.tcclEngineBulk)
+    c.consumer_warps = 31
+    r, _, _, info = tccl.tcclPlanInspect(AR, 4, send, recv, 1 << 22, tccl.tcclBfloat16, 0, 152,
+                                         232448, c)
+    assert info.threads == 32 * 17
+
+
 # ------------------------------------------------------------------ validation
 def test_rejects_null_and_misaligned_pointers():
     p = 2
