@@ -671,6 +671,101 @@ def sweep(args):
         g.close()
 
 
+# ------------------------------------------------------------------ overlap mode
+def overlap(args):
+    """Allreduce beside a concurrent GEMM (the T-CCL GEMM-overlap study, on one
+    GPU): a cuBLAS bf16 GEMM loop on one stream, the C4 allreduce (P=8, bf16,
+    128 MiB per rank) on another, for several CTA caps. Reports each alone,
+    both together, the GEMM slowdown and the overlapped / serial speedup. The
+    allreduce result under contention is checked against the oracle."""
+    import numpy as np
+    import torch
+    import collective_communication_planner_gb300 as tccl
+    import datagen
+    import oracle
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS["c4"]
+    p, n = w["p"], w["count"]
+    xs = make_inputs(w)
+    if args.overlap_engine == tccl.tcclEngineTmaReduce:
+        # bf16 sums round at every step in the copy hardware: use the fp32 form
+        # of the same values (half the elements, same bytes per rank)
+        n //= 2
+        xs = [((x[:n].astype(np.uint32) << 16).view(np.float32)).copy() for x in xs]
+    sends = [host_to_torch(x).to(dev) for x in xs]
+    recvs = [torch.empty_like(t) for t in sends]
+    dt_code = tccl.tcclFloat32 if xs[0].dtype == np.float32 else tccl.tcclBfloat16
+    m = args.gemm_n
+    A = torch.randn(m, m, device=dev, dtype=torch.bfloat16)
+    B = torch.randn(m, m, device=dev, dtype=torch.bfloat16)
+    C = torch.empty(m, m, device=dev, dtype=torch.bfloat16)
+    s_g, s_c = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    g = tccl.Group(p)
+    if args.overlap_engine:
+        g.set_config(engine=args.overlap_engine)
+    reps = args.overlap_reps
+    flops = 2.0 * m ** 3
+    hbm = 2 * p * n * xs[0].dtype.itemsize
+
+    def gemm():
+        with torch.cuda.stream(s_g):
+            torch.matmul(A, B, out=C)
+
+    def ar(cap):
+        r = tccl.tcclAllReduce(g.handle, sends, recvs, n, dt_code, tccl.tcclSum,
+                               s_c.cuda_stream, cap)
+        if r != tccl.tcclSuccess:
+            raise tccl.TcclError(r, "tcclAllReduce")
+
+    def timed(fn_g, fn_c):
+        torch.cuda.synchronize()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        e[0].record(s_g)
+        s_c.wait_event(e[0])
+        for _ in range(reps):
+            if fn_g:
+                fn_g()
+            if fn_c:
+                fn_c()
+        e[1].record(s_g)
+        e[2].record(s_c)
+        torch.cuda.synchronize()
+        return e[0].elapsed_time(e[1]), e[0].elapsed_time(e[2])
+
+    for _ in range(3):
+        gemm()
+        ar(0)
+    torch.cuda.synchronize()
+    gemm_alone, _ = timed(gemm, None)
+    idx = np.random.default_rng(1).choice(n, size=1 << 15, replace=False)
+    otype = "f32" if xs[0].dtype == np.float32 else "bf16"
+    exp = oracle.allreduce([x[idx].copy() for x in xs], otype, "sum")[0]
+    for cap in args.overlap_caps:
+        _, ar_alone = timed(None, lambda: ar(cap))
+        for t in recvs:
+            t.zero_()
+        g_ms, c_ms = timed(gemm, lambda: ar(cap))
+        got = recvs[3].cpu().numpy()[idx] if otype == "f32" else \
+            recvs[3].view(torch.int16).cpu().numpy()[idx].view(np.uint16)
+        both = max(g_ms, c_ms)
+        print(json.dumps({
+            "mode": "overlap", "cap": cap, "engine": g.last_launch()["engine"], "gemm": f"bf16 {m}x{m}x{m}", "reps": reps,
+            "gemm_alone_ms": round(gemm_alone / reps, 4),
+            "gemm_tflops_alone": round(flops / (gemm_alone / reps * 1e-3) / 1e12, 1),
+            "allreduce_alone_ms": round(ar_alone / reps, 4),
+            "allreduce_alone_GBps": round(hbm / (ar_alone / reps * 1e-3) / 1e9, 1),
+            "gemm_with_allreduce_ms": round(g_ms / reps, 4),
+            "allreduce_with_gemm_ms": round(c_ms / reps, 4),
+            "allreduce_with_gemm_GBps": round(hbm / (c_ms / reps * 1e-3) / 1e9, 1),
+            "gemm_slowdown": round(g_ms / gemm_alone, 3),
+            "overlap_speedup_vs_serial": round((gemm_alone + ar_alone) / both, 3),
+            "allreduce_correct": bool(np.array_equal(got, exp))}), flush=True)
+    assert g.query_error() == tccl.tcclSuccess
+    g.close()
+
+
 # ------------------------------------------------------------------ probe mode
 def probe():
     """Builds and runs the per-SM bandwidth probe
@@ -705,6 +800,14 @@ def main():
     ap.add_argument("--sweep-configs", default="", help="comma list, e.g. c3,c5")
     ap.add_argument("--probe", action="store_true",
                     help="run the per-SM bandwidth probe (bounds for CTA-capped runs)")
+    ap.add_argument("--overlap", action="store_true",
+                    help="allreduce beside a concurrent cuBLAS GEMM, across CTA caps")
+    ap.add_argument("--gemm-n", type=int, default=8192)
+    ap.add_argument("--overlap-engine", type=int, default=0,
+                    help="engine for the overlap study (0 auto, 1 bulk, 4 TMA-reduce)")
+    ap.add_argument("--overlap-reps", type=int, default=20)
+    ap.add_argument("--overlap-caps", type=lambda v: [int(x) for x in v.split(",")],
+                    default=[8, 16, 32, 64, 0])
     args = ap.parse_args()
     if args.probe:
         probe()
@@ -733,6 +836,9 @@ def main():
         __graft_entry__.build()
     if args.sweep:
         sweep(args)
+        return
+    if args.overlap:
+        overlap(args)
         return
     if dist is not None:
         dist.barrier()

@@ -22,7 +22,7 @@ tcclSuccess, tcclInvalidArgument, tcclInvalidUsage = 0, 1, 2
 tcclCudaError, tcclDeviceTimeout, tcclInternalError = 3, 4, 5
 tcclFloat32, tcclBfloat16, tcclInt32 = 0, 1, 2
 tcclSum, tcclMin, tcclMax = 0, 1, 2
-tcclEngineAuto, tcclEngineBulk, tcclEngineWarp, tcclEngineVec = 0, 1, 2, 3
+tcclEngineAuto, tcclEngineBulk, tcclEngineWarp, tcclEngineVec, tcclEngineTmaReduce = 0, 1, 2, 3, 4
 tcclStoreAuto, tcclStoreBulk, tcclStoreVec = 0, 1, 2
 tcclOrderAuto, tcclOrderBlocked, tcclOrderCyclic, tcclOrderDynamic = 0, 1, 2, 3
 tcclLayoutAuto, tcclLayoutShared, tcclLayoutPerRank = 0, 1, 2

@@ -153,6 +153,7 @@ Config config_from_env() {
   };
   if (const char* e = std::getenv("TCCL_ENGINE")) {
     std::string v(e);
+    if (v == "tma_reduce") c.engine = kEngineTmaReduce;
     if (v == "bulk") c.engine = kEngineBulk;
     else if (v == "warp") c.engine = kEngineWarp;
     else if (v == "vec") c.engine = kEngineVec;
@@ -226,7 +227,7 @@ tcclConfig_t to_public(const Config& c) {
 }
 
 bool config_ok(const tcclConfig_t& p) {
-  return p.engine >= 0 && p.engine <= 3 && p.store_mode >= 0 && p.store_mode <= 2 &&
+  return p.engine >= 0 && p.engine <= 4 && p.store_mode >= 0 && p.store_mode <= 2 &&
          p.stage_bytes >= 0 && p.stages >= 0 && p.consumer_warps >= 0 && p.ctas_per_sm >= 0 &&
          p.wait_timeout_ms >= 0 && p.chunk_order >= 0 && p.chunk_order <= 3 &&
          p.prefetch_chunks >= -1 && p.load_policy >= 0 && p.load_policy <= 2 &&
@@ -244,7 +245,8 @@ void fill_info(const Lowered& low, tcclLaunchInfo_t* info) {
   info->windows = (int)low.win.size();
   info->tasks = low.ntasks;
   info->smem_bytes = low.shape.smem;
-  info->chunk_order = low.shape.engine == kEngineBulk ? low.shape.order : 0;
+  const bool bulkish = low.shape.engine == kEngineBulk || low.shape.engine == kEngineTmaReduce;
+  info->chunk_order = bulkish ? low.shape.order : 0;
   info->total_chunks = low.total_chunks;
   info->stage_layout = low.shape.engine == kEngineBulk ? (low.shape.rank_streamed ? 2 : 1) : 0;
 }
@@ -313,7 +315,7 @@ tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* con
   }
   if (log_level()) dump_plan(pl, cp->low);
   const Lowered& low = cp->low;
-  if (low.shape.engine == kEngineBulk) {
+  if (low.shape.engine == kEngineBulk || low.shape.engine == kEngineTmaReduce) {
     std::vector<unsigned char> host;
     size_t off_prefix = 0, off_cta = 0, off_sched = 0;
     pack_bulk_table(low, &host, &off_prefix, &off_cta, &off_sched);
@@ -352,11 +354,18 @@ tcclResult_t run_collective(tcclGroup* g, int coll, const void* const* send, voi
   const int es = elem_size_of(dtype);
   CachedPlan* cp = nullptr;
   tcclResult_t r = get_plan(g, coll, send, recv, count, es, cap, &cp);
+  if (r == tcclSuccess && cp->low.shape.engine == kEngineTmaReduce &&
+      !tma_reduce_supported(dtype, op)) {
+    if (log_level())
+      std::fprintf(stderr, "[tccl] the TMA-reduce engine cannot reduce dtype %d with op %d "
+                           "exactly in rank order\n", dtype, op);
+    r = tcclInvalidUsage;
+  }
   int err = 0;
   if (r == tcclSuccess) {
     const Lowered& low = cp->low;
     uint32_t* mask = g->record_sms ? g->d_sm_mask : nullptr;
-    if (low.shape.engine == kEngineBulk) {
+    if (low.shape.engine == kEngineBulk || low.shape.engine == kEngineTmaReduce) {
       BulkArgs a;
       std::memset(&a, 0, sizeof(a));
       for (int k = 0; k < g->nranks; ++k) {
@@ -385,7 +394,8 @@ tcclResult_t run_collective(tcclGroup* g, int coll, const void* const* send, voi
       a.consumer_warps = low.shape.consumer_warps;
       a.release_lag = low.shape.release_lag;
       a.elem_size = es;
-      err = launch_bulk(coll, dtype, op, a, low.shape, stream);
+      err = low.shape.engine == kEngineBulk ? launch_bulk(coll, dtype, op, a, low.shape, stream)
+                                            : launch_reduce(coll, dtype, op, a, low.shape, stream);
     } else {
       std::vector<unsigned char>& buf = cp->small_args;
       if (low.size_class == 0)

@@ -14,6 +14,31 @@ int launch_bulk_t(const BulkArgs& a, const LaunchShape& s, cudaStream_t st) {
 }
 
 template <int C, int D, int O>
+int launch_reduce_t(const BulkArgs& a, const LaunchShape& s, cudaStream_t st) {
+  reduce_kernel<C, D, O><<<s.grid, s.threads, s.smem, st>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+
+template <int C, int D, int O>
+int set_reduce_smem(size_t bytes) {
+  return static_cast<int>(cudaFuncSetAttribute(reduce_kernel<C, D, O>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(bytes)));
+}
+
+// (dtype, op) -> F<C, D, O> for the pairs the TMA-reduce engine supports
+#define TCCL_TMA_REDUCE_SWITCH(COLL, FN, ...)                               \
+  switch (dtype * 3 + op) {                                                 \
+    case kF32 * 3 + kSum: return FN<COLL, kF32, kSum>(__VA_ARGS__);         \
+    case kBF16 * 3 + kMin: return FN<COLL, kBF16, kMin>(__VA_ARGS__);       \
+    case kBF16 * 3 + kMax: return FN<COLL, kBF16, kMax>(__VA_ARGS__);       \
+    case kI32 * 3 + kSum: return FN<COLL, kI32, kSum>(__VA_ARGS__);         \
+    case kI32 * 3 + kMin: return FN<COLL, kI32, kMin>(__VA_ARGS__);         \
+    case kI32 * 3 + kMax: return FN<COLL, kI32, kMax>(__VA_ARGS__);         \
+    default: return static_cast<int>(cudaErrorInvalidValue);                \
+  }
+
+template <int C, int D, int O>
 int set_bulk_smem(size_t bytes) {
   cudaError_t e = cudaFuncSetAttribute(bulk_kernel<C, D, O>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,

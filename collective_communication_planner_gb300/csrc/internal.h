@@ -15,7 +15,13 @@ constexpr int kLargeWindows = 3 * kMaxRanks + 2;
 enum Coll : int { kAllReduce = 0, kReduceScatter = 1, kAllGather = 2 };
 enum DType : int { kF32 = 0, kBF16 = 1, kI32 = 2 };
 enum RedOp : int { kSum = 0, kMin = 1, kMax = 2 };
-enum Engine : int { kEngineAuto = 0, kEngineBulk = 1, kEngineWarp = 2, kEngineVec = 3 };
+enum Engine : int {
+  kEngineAuto = 0,
+  kEngineBulk = 1,
+  kEngineWarp = 2,
+  kEngineVec = 3,
+  kEngineTmaReduce = 4
+};
 enum StoreMode : int { kStoreAuto = 0, kStoreBulk = 1, kStoreVec = 2 };
 enum ChunkOrder : int { kOrderAuto = 0, kOrderBlocked = 1, kOrderCyclic = 2, kOrderDynamic = 3 };
 // Bulk engine stage layout: a stage holds one chunk of every source rank
@@ -124,6 +130,12 @@ int launch_small_rs(int dtype, int op, int engine, int size_class, const void* a
                     const LaunchShape& s, void* stream);
 int launch_small_ag(int dtype, int op, int engine, int size_class, const void* args,
                     const LaunchShape& s, void* stream);
+int launch_reduce(int coll, int dtype, int op, const BulkArgs& a, const LaunchShape& s,
+                  void* stream);
+// (dtype, op) pairs the copy hardware reduces exactly in a fixed order
+inline bool tma_reduce_supported(int dtype, int op) {
+  return (dtype == kF32 && op == kSum) || dtype == kI32 || (dtype == kBF16 && op != kSum);
+}
 int prepare_bulk_kernels(size_t smem_bytes);  // opt-in shared memory for the bulk kernels
 
 }  // namespace tccl

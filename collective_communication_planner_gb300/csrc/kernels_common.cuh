@@ -104,6 +104,37 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t byte
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
 }
 
+// shared -> global bulk reduction (element-wise op applied at the destination
+// by the memory system), tracked by bulk async-groups like a bulk store
+template <int DT, int OP>
+__device__ __forceinline__ void bulk_reduce(void* gdst, const void* smem_src, uint32_t bytes) {
+  if (DT == kF32) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                     gdst), "r"(smem_addr(smem_src)), "r"(bytes)
+                 : "memory");
+  } else if (DT == kI32 && OP == kSum) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.s32 [%0], [%1], %2;" ::"l"(
+                     gdst), "r"(smem_addr(smem_src)), "r"(bytes)
+                 : "memory");
+  } else if (DT == kI32 && OP == kMin) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.min.s32 [%0], [%1], %2;" ::"l"(
+                     gdst), "r"(smem_addr(smem_src)), "r"(bytes)
+                 : "memory");
+  } else if (DT == kI32) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.max.s32 [%0], [%1], %2;" ::"l"(
+                     gdst), "r"(smem_addr(smem_src)), "r"(bytes)
+                 : "memory");
+  } else if (OP == kMin) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.min.bf16 [%0], [%1], %2;" ::"l"(
+                     gdst), "r"(smem_addr(smem_src)), "r"(bytes)
+                 : "memory");
+  } else {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.max.bf16 [%0], [%1], %2;" ::"l"(
+                     gdst), "r"(smem_addr(smem_src)), "r"(bytes)
+                 : "memory");
+  }
+}
+
 // shared -> global bulk copy, tracked by bulk async-groups
 __device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
@@ -738,6 +769,109 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
   }
   if (ctid == 0) bulk_wait_all();
   if (!*abort_flag) bulk_scalar_windows<COLL, DT, OP>(a, ctid, nct);
+}
+
+// ------------------------------------------------------------------ TMA-reduce engine
+// The reduction itself offloaded to the copy hardware, as the shard-in of the
+// T-CCL description does: for each chunk, rank 0's data is bulk-stored into
+// the owner's buffer, then ranks 1 .. P-1 are bulk-reduced into it in
+// ascending order (each reduction complete before the next is issued, so the
+// order is fixed). For allreduce the final chunk is then loaded once and
+// bulk-stored to every other rank. No thread touches the data. Lane 0 of
+// every warp runs its own stream of chunks (every (grid x warps)-th chunk)
+// with two shared-memory buffers, so the load of rank r+1 overlaps the
+// reduction of rank r. Types the hardware reduces exactly in this order:
+// fp32 add (round to nearest), int32 add/min/max, bf16 min/max.
+template <int COLL, int DT, int OP>
+__global__ void __launch_bounds__(32 * kMaxConsumerWarps, 1)
+    reduce_kernel(const __grid_constant__ BulkArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // 2 per warp, then the test barrier
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 512);
+  unsigned char* buf_base = smem + 1024;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int lanes = blockDim.x >> 5;
+  const int P = a.nranks;
+  const uint32_t chunk = static_cast<uint32_t>(a.chunk_bytes);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2 * lanes + 1; ++i) mbar_init(&bars[i], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    record_sm(a.sm_mask);
+  }
+  __syncthreads();
+  if (lane == 0) {
+    uint64_t* bar = bars + 2 * warp;
+    unsigned char* xbase = buf_base + static_cast<size_t>(2 * warp) * chunk;
+    auto x = [&](int b) { return xbase + static_cast<size_t>(b) * chunk; };
+    uint32_t phase = 0;    // bit b: parity to wait for on bar[b]
+    uint32_t pending = 0;  // bit b: a load into buffer b not yet waited for
+    ChunkLocator loc;
+    loc.init();
+    bool ok = true;
+    const uint64_t first = static_cast<uint64_t>(blockIdx.x) * lanes + warp;
+    const uint64_t step = static_cast<uint64_t>(gridDim.x) * lanes;
+    auto issue = [&](int b, const char* src, uint32_t n) {
+      mbar_arrive_expect_tx(&bar[b], n);
+      bulk_load(x(b), src, n, &bar[b]);
+      pending |= 1u << b;
+    };
+    auto wait_buf = [&](int b) {
+      const bool done = wait_bounded(&bar[b], (phase >> b) & 1, abort_flag, a.timeout_ns,
+                                     a.status, true);
+      if (done) {
+        phase ^= 1u << b;
+        pending &= ~(1u << b);
+      }
+      return done;
+    };
+    for (uint64_t c = first; c < a.total_chunks && ok; c += step) {
+      uint32_t off, n;
+      loc.locate(a, c, off, n);
+      const Window& w = loc.w;
+      const int owner_rank = w.dst_sel < 0 ? 0 : w.dst_sel;
+      char* owner = static_cast<char*>(a.p.dst[owner_rank]) + w.dst_off + off;
+      bulk_wait_read<0>();  // both buffers free: earlier stores have read them
+      issue(0, static_cast<const char*>(a.p.src[0]) + w.src_off + off, n);
+      int b = 0;
+      for (int r = 0; r < P; ++r) {
+        if (r + 1 < P) {
+          bulk_wait_read<0>();  // rank r-1's reduction has read the other buffer
+          issue(b ^ 1, static_cast<const char*>(a.p.src[r + 1]) + w.src_off + off, n);
+        }
+        ok = wait_buf(b);
+        if (ok && a.inject_timeout_ns && blockIdx.x == 0 && warp == 0 && c == first && r == 0)
+          // test hook: a barrier nothing arrives on
+          ok = wait_bounded(&bars[2 * lanes], 0, abort_flag, a.inject_timeout_ns, a.status, true);
+        if (!ok) break;
+        bulk_wait_all();  // rank r-1's update of the owner chunk is complete
+        if (r == 0) bulk_store(owner, x(b), n);
+        else bulk_reduce<DT, OP>(owner, x(b), n);
+        bulk_commit();
+        b ^= 1;
+      }
+      if (!ok) break;
+      bulk_wait_all();  // the owner chunk holds the final result
+      if (COLL == kAllReduce && P > 1) {
+        // shard-out: the final chunk is loaded once and stored to every rank
+        issue(0, owner, n);
+        ok = wait_buf(0);
+        if (!ok) break;
+        for (int d = 0; d < P; ++d)
+          if (d != owner_rank)
+            bulk_store(static_cast<char*>(a.p.dst[d]) + w.dst_off + off, x(0), n);
+        bulk_commit();
+      }
+    }
+    bulk_wait_all();
+    // after an abort, let any load still in flight land before the CTA exits
+    for (int b = 0; b < 2; ++b)
+      if (pending & (1u << b))
+        wait_bounded(&bar[b], (phase >> b) & 1, abort_flag, a.timeout_ns, a.status, false);
+  }
+  __syncthreads();
+  if (!*abort_flag) bulk_scalar_windows<COLL, DT, OP>(a, threadIdx.x, blockDim.x);
 }
 
 // ------------------------------------------------------------------ small engines

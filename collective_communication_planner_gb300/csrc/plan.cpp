@@ -156,6 +156,71 @@ Config resolve_config(const Config& in) {
   return c;
 }
 
+// Body windows -> one chunk sequence (prefix table), element-wise windows cut
+// into pieces and bound to CTAs, and the grid size. Each CTA runs `lanes`
+// independent chunk streams (the TMA-reduce engine) or one (the bulk engine).
+void build_chunk_tables(const std::vector<Window>& wins, uint64_t chunk, int lanes,
+                        int max_ctas_total, int cta_cap, const Config& cfg, int es, bool capped,
+                        Lowered* out) {
+  LaunchShape& sh = out->shape;
+  std::vector<Window> body, scal;
+  uint64_t sbytes = 0;
+  for (const Window& w : merge_adjacent(wins)) {
+    if (w.scalar) {
+      scal.push_back(w);
+      sbytes += w.bytes;
+    } else {
+      body.push_back(w);
+    }
+  }
+  int max_g = max_ctas_total;
+  if (cta_cap > 0) max_g = std::min(max_g, cta_cap);
+  // body windows -> one sequence of chunks
+  out->nbody = (int)body.size();
+  out->chunk_prefix.assign(body.size() + 1, 0);
+  for (size_t i = 0; i < body.size(); ++i)
+    out->chunk_prefix[i + 1] = out->chunk_prefix[i] + ceil_div(body[i].bytes, chunk);
+  const uint64_t total = out->chunk_prefix.back();
+  out->total_chunks = total;
+  int grid = total > 0 ? (int)std::min<uint64_t>(max_g, ceil_div(total, (uint64_t)lanes)) : 1;
+  // uncapped: claim chunks dynamically (SMs stream at different rates);
+  // capped: a fixed cyclic share per CTA
+  int order = cfg.chunk_order != kOrderAuto ? cfg.chunk_order
+                                            : (capped ? kOrderCyclic : kOrderDynamic);
+  sh.order = order;
+  if (total > 0 && order == kOrderBlocked) {
+    out->chunks_per_cta = ceil_div(total, (uint64_t)grid);
+    grid = (int)ceil_div(total, out->chunks_per_cta);
+  }
+  // element-wise windows: cut into pieces and bound to CTAs round robin
+  std::vector<Window> pieces;
+  if (!scal.empty()) {
+    uint64_t limit = std::max<uint64_t>(4096, round_up(ceil_div(sbytes, (uint64_t)max_g), es));
+    for (const Window& w : scal) {
+      Window x = w;
+      uint64_t left = w.bytes;
+      while (left > 0) {
+        uint64_t n = std::min<uint64_t>(left, limit);
+        x.bytes = (uint32_t)n;
+        pieces.push_back(x);
+        x.src_off += n;
+        x.dst_off += n;
+        left -= n;
+      }
+    }
+    if (total == 0) grid = (int)std::min<uint64_t>(max_g, pieces.size());
+    for (size_t i = 0; i < pieces.size(); ++i) pieces[i].cta = (int32_t)(i % (size_t)grid);
+    std::stable_sort(pieces.begin(), pieces.end(),
+                     [](const Window& x, const Window& y) { return x.cta < y.cta; });
+  }
+  out->win = body;
+  out->win.insert(out->win.end(), pieces.begin(), pieces.end());
+  out->cta_first.assign(grid + 1, 0);
+  for (const Window& w : pieces) out->cta_first[w.cta + 1]++;
+  for (int i = 0; i < grid; ++i) out->cta_first[i + 1] += out->cta_first[i];
+  sh.grid = grid;
+}
+
 bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv_mod16,
                 const Config& cfg_in, const DeviceDesc& dev, int cta_cap, Lowered* out,
                 std::string* why) {
@@ -311,7 +376,34 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
     return true;
   }
 
-  // ---- 4. bulk engine: chunks, stages, CTAs
+  int smem_budget = dev.smem_optin;
+  if (dev.smem_per_sm > 0)
+    smem_budget = std::min(smem_budget, dev.smem_per_sm / std::max(1, cfg.ctas_per_sm) - 1024);
+
+  // ---- 4a. TMA-reduce engine: the copy hardware applies the reduction
+  if (engine == kEngineTmaReduce) {
+    if (plan.coll == kAllGather) {
+      *why = "an all-gather has nothing for the TMA-reduce engine to reduce";
+      return false;
+    }
+    const uint64_t chunk = 8192;
+    const int lanes = std::min<int>(cfg.consumer_warps, (smem_budget - 1024) / (int)(2 * chunk));
+    if (lanes < 1) {
+      *why = "shared memory too small for the TMA-reduce engine";
+      return false;
+    }
+    sh.chunk_bytes = (int)chunk;
+    sh.stages = 2;
+    sh.consumer_warps = lanes;
+    sh.threads = 32 * lanes;
+    sh.store_mode = kStoreBulk;
+    sh.smem = 1024 + (size_t)lanes * 2 * chunk;
+    build_chunk_tables(wins, chunk, lanes, max_ctas_total, cta_cap, cfg, es, capped, out);
+    sh.order = kOrderCyclic;  // every (grid x lanes)-th chunk per lane
+    return true;
+  }
+
+  // ---- 4b. bulk engine: chunks, stages, CTAs
   int layout = cfg.stage_layout;
   if (plan.coll == kAllGather) layout = kLayoutShared;  // one source: nothing to stream
   // many ranks make the shared layout's per-rank copies tiny (64 KiB / P);
@@ -334,9 +426,7 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
   if (sh.rank_streamed)  // every consumer thread owns kPerRankVectors vectors of a chunk
     chunk = (uint64_t)16 * kPerRankVectors * 32 * cfg.consumer_warps;
   const int result_slots = (store == kStoreBulk && plan.coll != kAllGather) ? 2 : 0;
-  int budget = dev.smem_optin;
-  if (dev.smem_per_sm > 0)
-    budget = std::min(budget, dev.smem_per_sm / std::max(1, cfg.ctas_per_sm) - 1024);
+  const int budget = smem_budget;
   int stages = 0;
   for (;;) {
     int64_t room = (int64_t)budget - 1024 - (int64_t)result_slots * (int64_t)chunk;
@@ -358,62 +448,7 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
   sh.load_evict_first = cfg.load_policy == 1 ? 1 : 0;
   sh.smem = 1024 + (size_t)stages * nsrc * chunk + (size_t)result_slots * chunk;
 
-  std::vector<Window> body, scal;
-  uint64_t sbytes = 0;
-  for (const Window& w : merge_adjacent(wins)) {
-    if (w.scalar) {
-      scal.push_back(w);
-      sbytes += w.bytes;
-    } else {
-      body.push_back(w);
-    }
-  }
-  int max_g = max_ctas_total;
-  if (cta_cap > 0) max_g = std::min(max_g, cta_cap);
-  // body windows -> one sequence of chunks
-  out->nbody = (int)body.size();
-  out->chunk_prefix.assign(body.size() + 1, 0);
-  for (size_t i = 0; i < body.size(); ++i)
-    out->chunk_prefix[i + 1] = out->chunk_prefix[i] + ceil_div(body[i].bytes, chunk);
-  const uint64_t total = out->chunk_prefix.back();
-  out->total_chunks = total;
-  int grid = total > 0 ? (int)std::min<uint64_t>(max_g, total) : 1;
-  // uncapped: claim chunks dynamically (SMs stream at different rates);
-  // capped: a fixed cyclic share per CTA
-  int order = cfg.chunk_order != kOrderAuto ? cfg.chunk_order
-                                            : (capped ? kOrderCyclic : kOrderDynamic);
-  sh.order = order;
-  if (total > 0 && order == kOrderBlocked) {
-    out->chunks_per_cta = ceil_div(total, (uint64_t)grid);
-    grid = (int)ceil_div(total, out->chunks_per_cta);
-  }
-  // element-wise windows: cut into pieces and bound to CTAs round robin
-  std::vector<Window> pieces;
-  if (!scal.empty()) {
-    uint64_t limit = std::max<uint64_t>(4096, round_up(ceil_div(sbytes, (uint64_t)max_g), es));
-    for (const Window& w : scal) {
-      Window x = w;
-      uint64_t left = w.bytes;
-      while (left > 0) {
-        uint64_t n = std::min<uint64_t>(left, limit);
-        x.bytes = (uint32_t)n;
-        pieces.push_back(x);
-        x.src_off += n;
-        x.dst_off += n;
-        left -= n;
-      }
-    }
-    if (total == 0) grid = (int)std::min<uint64_t>(max_g, pieces.size());
-    for (size_t i = 0; i < pieces.size(); ++i) pieces[i].cta = (int32_t)(i % (size_t)grid);
-    std::stable_sort(pieces.begin(), pieces.end(),
-                     [](const Window& x, const Window& y) { return x.cta < y.cta; });
-  }
-  out->win = body;
-  out->win.insert(out->win.end(), pieces.begin(), pieces.end());
-  out->cta_first.assign(grid + 1, 0);
-  for (const Window& w : pieces) out->cta_first[w.cta + 1]++;
-  for (int i = 0; i < grid; ++i) out->cta_first[i + 1] += out->cta_first[i];
-  sh.grid = grid;
+  build_chunk_tables(wins, chunk, 1, max_ctas_total, cta_cap, cfg, es, capped, out);
   return true;
 }
 

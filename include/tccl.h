@@ -68,7 +68,11 @@ typedef enum {
   tcclEngineAuto = 0,
   tcclEngineBulk = 1, /* TMA cp.async.bulk pipeline: mbarrier stages, reduce, bulk stores */
   tcclEngineWarp = 2, /* small-message path: one lane per (vector, rank), shuffle fold */
-  tcclEngineVec = 3   /* plain 128-bit loads/stores, each lane folds all ranks */
+  tcclEngineVec = 3,  /* plain 128-bit loads/stores, each lane folds all ranks */
+  tcclEngineTmaReduce = 4 /* the copy hardware reduces: rank 0 bulk-stored, ranks 1..P-1
+                             bulk-reduced in order, result loaded once and bulk-stored to all;
+                             fp32 sum, int32 sum/min/max, bf16 min/max only (other pairs:
+                             tcclInvalidUsage); never chosen by Auto */
 } tcclEngine_t;
 
 typedef enum {

@@ -130,12 +130,14 @@ def test_allreduce_in_place(groups, engine, dtype):
 def test_bulk_store_modes_and_pipeline_shapes(groups, store, stage_bytes, stages):
     p, n = 4, 1_000_003
     g = groups(p)
-    configure(g, "bulk", store=store, stage_bytes=stage_bytes, stages=stages)
+    reset_config(g, engine=tccl.tcclEngineBulk, store_mode=store, stage_bytes=stage_bytes,
+                 stages=stages, stage_layout=tccl.tcclLayoutShared)
     xs = inputs("bf16", p, n)
     exp = oracle.allreduce(xs, "bf16", "sum", nthreads=0)
     got = run_allreduce(g, xs, "bf16", "sum")
     info = g.last_launch()
     assert info["engine"] == tccl.tcclEngineBulk and info["store_mode"] == store
+    assert info["stage_layout"] == tccl.tcclLayoutShared
     assert_ranks_equal(got, exp, f"store {store} stage {stage_bytes}x{stages}")
 
 
@@ -204,6 +206,69 @@ def test_per_rank_layout_many_ranks(groups):
         reset_config(g, engine=tccl.tcclEngineBulk, stage_layout=layout, consumer_warps=16,
                      store_mode=0, stage_bytes=0, stages=0, chunk_order=0)
         assert_ranks_equal(run_allreduce(g, xs, "bf16", "sum"), exp, f"P=64 layout {layout}")
+
+
+TMA_REDUCE_PAIRS = [("f32", "sum"), ("i32", "sum"), ("i32", "min"), ("i32", "max"),
+                    ("bf16", "min"), ("bf16", "max")]
+
+
+@pytest.mark.parametrize("dtype,op", TMA_REDUCE_PAIRS)
+def test_tma_reduce_engine(groups, dtype, op):
+    for p, n, cap, offs in ((1, 10_000, 0, 0), (2, 1_000_003, 0, 0), (3, 77_777, 5, 4),
+                            (8, 500_001, 0, 0), (8, 300_000, 16, 8)):
+        g = groups(p)
+        reset_config(g, engine=tccl.tcclEngineTmaReduce)
+        xs = inputs(dtype, p, n)
+        got = run_allreduce(g, xs, dtype, op, cap=cap, send_off=offs, recv_off=offs)
+        assert p == 1 or g.last_launch()["engine"] == tccl.tcclEngineTmaReduce
+        assert_ranks_equal(got, oracle.allreduce(xs, dtype, op, nthreads=0),
+                           f"TMA-reduce AR {dtype} {op} P={p} cap={cap} off={offs}")
+    p, n = 4, 200_003
+    g = groups(p)
+    reset_config(g, engine=tccl.tcclEngineTmaReduce)
+    xs = inputs(dtype, p, n)
+    got = run_allreduce(g, xs, dtype, op, in_place=True)
+    assert_ranks_equal(got, oracle.allreduce(xs, dtype, op, nthreads=0), "TMA-reduce in place")
+    rc = 123_457
+    xs = inputs(dtype, p, p * rc)
+    sends = [to_device(x) for x in xs]
+    parts = [torch.empty(rc, dtype=TORCH_OF[dtype], device="cuda") for _ in range(p)]
+    g.reduce_scatter(sends, parts, op=op)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    assert_ranks_equal([to_host(t) for t in parts],
+                       oracle.reduce_scatter(xs, dtype, op, nthreads=0), "TMA-reduce RS")
+
+
+@pytest.mark.parametrize("dtype,op", [("bf16", "sum"), ("f32", "min"), ("f32", "max")])
+def test_tma_reduce_engine_rejects_inexact_pairs(groups, dtype, op):
+    g = groups(2)
+    reset_config(g, engine=tccl.tcclEngineTmaReduce)
+    a = torch.zeros(4096, dtype=TORCH_OF[dtype], device="cuda")
+    b = torch.zeros_like(a)
+    c = torch.zeros_like(a)
+    d = torch.zeros_like(a)
+    r = tccl.tcclAllReduce(g.handle, [a, b], [c, d], 4096, DT_CODE[dtype], tccl.OPS[op],
+                           torch.cuda.current_stream().cuda_stream, 0)
+    assert r == tccl.tcclInvalidUsage
+
+
+def test_tma_reduce_engine_timeout_path(groups):
+    p, n = 4, 1 << 20
+    g = groups(p)
+    reset_config(g, engine=tccl.tcclEngineTmaReduce)
+    xs = inputs("f32", p, n)
+    sends = [to_device(x) for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    assert tccl.tcclGroupInjectWaitTimeout(g.handle, True, 50.0) == tccl.tcclSuccess
+    g.all_reduce(sends, recvs)
+    assert g.query_error() == tccl.tcclDeviceTimeout
+    assert tccl.tcclGroupInjectWaitTimeout(g.handle, False, 0.0) == tccl.tcclSuccess
+    g.all_reduce(sends, recvs)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    assert_ranks_equal([to_host(r) for r in recvs], oracle.allreduce(xs, "f32", "sum", nthreads=0),
+                       "TMA-reduce after timeout")
 
 
 @pytest.mark.parametrize("cap", [1, 3, 8, 16, 32])

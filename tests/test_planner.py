@@ -274,6 +274,26 @@ def test_auto_layout_switches_to_per_rank_for_many_ranks():
         assert r == 0 and info.stage_layout == exp, p
 
 
+@pytest.mark.parametrize("coll", [AR, RS])
+@pytest.mark.parametrize("p", [1, 2, 8])
+def test_tma_reduce_engine_shape(coll, p):
+    send, recv = bufs(p, 0, 0)
+    r, wins, _, info = inspect(coll, p, 1_000_003, tccl.tcclFloat32, send, recv,
+                               engine=tccl.tcclEngineTmaReduce)
+    assert r == 0 and info.engine == tccl.tcclEngineTmaReduce
+    lanes = info.threads // 32
+    assert info.chunk_bytes == 8192 and info.stages == 2
+    assert info.smem_bytes == 1024 + lanes * 2 * 8192 <= 232448
+    assert info.ctas <= -(-info.total_chunks // lanes)
+    check_cover(coll, p, 1_000_003, 4, send, recv, wins, info)
+
+
+def test_tma_reduce_engine_rejects_allgather():
+    send, recv = bufs(4, 0, 0)
+    r, *_ = inspect(AG, 4, 1000, tccl.tcclFloat32, send, recv, engine=tccl.tcclEngineTmaReduce)
+    assert r == tccl.tcclInvalidUsage
+
+
 def test_consumer_warps_are_capped_at_sixteen():
     send, recv = bufs(4, 0, 0)
     c = cfg(tccl.tcclEngineBulk)
