@@ -766,6 +766,66 @@ def overlap(args):
     g.close()
 
 
+# ------------------------------------------------------------------ reshard mode
+def reshard_bench(args):
+    """M-to-N reshard throughput (the M2N workload on logical ranks): an
+    8192 x 8192 bf16 weight between several training and generation layouts.
+    Bytes moved = each source piece read once + every destination block
+    written once per replica. Results checked against the reshard oracle."""
+    import numpy as np
+    import torch
+    import collective_communication_planner_gb300 as tccl
+    import datagen
+    from oracle import reshard as rs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    R = tccl.TCCL_REPLICATE
+    shape = (8192, 8192)
+    glob = datagen.rank_buffers("normal_bf16", 7, 1, shape[0] * shape[1])[0].reshape(shape)
+    peak, _ = measured_peak()
+    g = tccl.Group(64)
+    cases = [("TP8 rows -> TP2xDP4 cols", ((8,), (0,)), ((4, 2), (R, 1))),
+             ("TP4 rows -> TP2xDP2 rows (article example A shape)", ((1, 4), (R, 0)), ((2, 2), (R, 0))),
+             ("TP8 cols -> TP8 rows", ((8,), (1,)), ((8,), (0,))),
+             ("TP2 rows -> DP8 replicas", ((2,), (0,)), ((8,), (R,)))]
+    stream = torch.cuda.current_stream()
+    for name, src, dst in cases:
+        sb = []
+        for m in range(rs.nranks(src[0])):
+            box = rs.local_box(shape, src[0], src[1], m)
+            sb.append(np.ascontiguousarray(glob[tuple(slice(lo, hi) for lo, hi in box)]).ravel())
+        exp = rs.reshard(sb, src[0], src[1], dst[0], dst[1], shape)
+        sends = [host_to_torch(b).to(dev) for b in sb]
+        recvs = [torch.empty(e.size, dtype=torch.bfloat16, device=dev) for e in exp]
+        sl = tccl.make_layout(src[0], src[1], 0)
+        dl = tccl.make_layout(dst[0], dst[1], rs.nranks(src[0]))
+        r, tr, br, bw, nw = tccl.tcclReshardInspect(sl, dl, list(shape), tccl.tcclBfloat16,
+                                                    sends, recvs)
+        fn = lambda: g.reshard(sends, sl, recvs, dl, shape)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        ok = all(np.array_equal(t.view(torch.int16).cpu().numpy().view(np.uint16), e)
+                 for t, e in zip(recvs, exp))
+        print(json.dumps({"mode": "reshard", "case": name, "tensor": "bf16 8192x8192",
+                          "transfers": len(tr), "windows": nw, "bytes_read": br,
+                          "bytes_written": bw, "us": round(ms * 1e3, 2),
+                          "GBps": round((br + bw) / (ms * 1e-3) / 1e9, 1),
+                          "hbm_fraction": round((br + bw) / (ms * 1e-3) / 1e9 / peak, 4),
+                          "correct": ok}), flush=True)
+        del sends, recvs
+    assert g.query_error() == tccl.tcclSuccess
+    g.close()
+
+
 # ------------------------------------------------------------------ probe mode
 def probe():
     """Builds and runs the per-SM bandwidth probe
@@ -802,6 +862,8 @@ def main():
                     help="run the per-SM bandwidth probe (bounds for CTA-capped runs)")
     ap.add_argument("--overlap", action="store_true",
                     help="allreduce beside a concurrent cuBLAS GEMM, across CTA caps")
+    ap.add_argument("--reshard", action="store_true",
+                    help="M-to-N reshard throughput on an 8192 x 8192 bf16 weight")
     ap.add_argument("--gemm-n", type=int, default=8192)
     ap.add_argument("--overlap-engine", type=int, default=0,
                     help="engine for the overlap study (0 auto, 1 bulk, 4 TMA-reduce)")
@@ -839,6 +901,9 @@ def main():
         return
     if args.overlap:
         overlap(args)
+        return
+    if args.reshard:
+        reshard_bench(args)
         return
     if dist is not None:
         dist.barrier()

@@ -57,6 +57,27 @@ class tcclLaunchInfo_t(ctypes.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
+TCCL_REPLICATE = -1
+
+
+class tcclLayout_t(ctypes.Structure):
+    _fields_ = [("ndims", ctypes.c_int), ("dims", ctypes.c_int * 4),
+                ("start_rank", ctypes.c_int), ("placements", ctypes.c_int * 4)]
+
+
+def make_layout(dims, placements, start_rank=0) -> tcclLayout_t:
+    """A mesh of `dims` (row-major rank order) from `start_rank`, one placement
+    per mesh axis: TCCL_REPLICATE or the tensor dimension that axis shards."""
+    lay = tcclLayout_t()
+    lay.ndims = len(dims)
+    for i, v in enumerate(dims):
+        lay.dims[i] = v
+    for i in range(4):
+        lay.placements[i] = placements[i] if i < len(placements) else TCCL_REPLICATE
+    lay.start_rank = start_rank
+    return lay
+
+
 def _open():
     if not LIB_PATH.exists():
         raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
@@ -83,6 +104,13 @@ def _open():
                                 ctypes.POINTER(i), ctypes.POINTER(tcclLaunchInfo_t)]),
         "tcclGroupInjectWaitTimeout": (i, [vp, i, ctypes.c_double]),
         "tcclAllReduceNoAlloc": (i, [i, pvp, pvp, sz, i, i, vp, i]),
+        "tcclReshard": (i, [vp, pvp, ctypes.POINTER(tcclLayout_t), pvp,
+                            ctypes.POINTER(tcclLayout_t), i, ctypes.POINTER(sz), i, vp, i]),
+        "tcclReshardInspect": (i, [ctypes.POINTER(tcclLayout_t), ctypes.POINTER(tcclLayout_t), i,
+                                   ctypes.POINTER(sz), i, pvp, pvp, i, i,
+                                   ctypes.POINTER(ctypes.c_int64), i, ctypes.POINTER(i),
+                                   ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                                   ctypes.POINTER(i)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -97,7 +125,8 @@ EXPORTED = ("tcclGetErrorString", "tcclGetVersion", "tcclGroupCreate", "tcclGrou
             "tcclGroupGetConfig", "tcclGroupSetConfig", "tcclAllReduce", "tcclReduceScatter",
             "tcclAllGather", "tcclGroupQueryError", "tcclGetLastLaunchInfo",
             "tcclGroupRecordSms", "tcclGroupReadSmRecord", "tcclPlanInspect",
-            "tcclGroupInjectWaitTimeout", "tcclAllReduceNoAlloc")
+            "tcclGroupInjectWaitTimeout", "tcclAllReduceNoAlloc", "tcclReshard",
+            "tcclReshardInspect")
 
 
 def _ptr(x) -> int:
@@ -194,6 +223,38 @@ def tcclAllReduceNoAlloc(nranks, sendbufs, recvbufs, count, datatype, op, stream
     sp, _k1 = _ptr_array(sendbufs)
     rp, _k2 = _ptr_array(recvbufs)
     return _lib.tcclAllReduceNoAlloc(nranks, sp, rp, count, datatype, op, _stream(stream), cta_cap)
+
+
+def _shape(shape):
+    return (ctypes.c_size_t * len(shape))(*shape)
+
+
+def tcclReshard(group, srcbufs, src_layout, dstbufs, dst_layout, shape, datatype, stream=None,
+                cta_cap=0) -> int:
+    sp, _k1 = _ptr_array(srcbufs)
+    dp, _k2 = _ptr_array(dstbufs)
+    return _lib.tcclReshard(group, sp, ctypes.byref(src_layout), dp, ctypes.byref(dst_layout),
+                            len(shape), _shape(shape), datatype, _stream(stream), cta_cap)
+
+
+def tcclReshardInspect(src_layout, dst_layout, shape, datatype, srcbufs, dstbufs, sm_count=152,
+                       cta_cap=0, max_transfers=4096):
+    """Host-only plan view: (result, transfers, bytes_read, bytes_written, windows) with
+    transfers a list of dicts (src, dst_mask, lo, hi)."""
+    sp, _k1 = _ptr_array(srcbufs)
+    dp, _k2 = _ptr_array(dstbufs)
+    buf = (ctypes.c_int64 * (10 * max_transfers))()
+    nt, nw = ctypes.c_int(), ctypes.c_int()
+    br, bw = ctypes.c_int64(), ctypes.c_int64()
+    r = _lib.tcclReshardInspect(ctypes.byref(src_layout), ctypes.byref(dst_layout), len(shape),
+                                _shape(shape), datatype, sp, dp, sm_count, cta_cap, buf,
+                                max_transfers, ctypes.byref(nt), ctypes.byref(br),
+                                ctypes.byref(bw), ctypes.byref(nw))
+    nd = len(shape)
+    tr = [dict(src=buf[10 * i], dst_mask=buf[10 * i + 1] & ((1 << 64) - 1),
+               lo=list(buf[10 * i + 2:10 * i + 2 + nd]), hi=list(buf[10 * i + 6:10 * i + 6 + nd]))
+          for i in range(min(nt.value, max_transfers))]
+    return r, tr, br.value, bw.value, nw.value
 
 
 def tcclGroupRecordSms(group, enable: bool) -> int:
@@ -324,6 +385,14 @@ class Group:
                              stream if stream is not None else _current_stream(), cta_cap),
                "tcclAllGather")
         return recvs
+
+    def reshard(self, srcs, src_layout, dsts, dst_layout, shape, cta_cap=0, stream=None):
+        """Every destination rank gets its block of the tensor (see tcclReshard)."""
+        dt = _dtype_code(srcs[0])
+        _check(tcclReshard(self.handle, srcs, src_layout, dsts, dst_layout, list(shape), dt,
+                           stream if stream is not None else _current_stream(), cta_cap),
+               "tcclReshard")
+        return dsts
 
     def query_error(self) -> int:
         r, s = tcclGroupQueryError(self.handle)

@@ -18,9 +18,9 @@ INCLUDE = ROOT / "include"
 LIB = PKG / "libtccl.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-HOST_SOURCES = ["api.cpp", "plan.cpp"]
+HOST_SOURCES = ["api.cpp", "plan.cpp", "reshard.cpp"]
 CUDA_SOURCES = ["kernels_bulk.cu", "kernels_small_ar.cu", "kernels_small_rs.cu",
-                "kernels_small_ag.cu", "no_alloc.cu"]
+                "kernels_small_ag.cu", "kernels_reshard.cu", "no_alloc.cu"]
 
 
 def _cuda_home() -> Path:

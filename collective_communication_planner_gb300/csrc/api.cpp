@@ -16,18 +16,20 @@
 
 #include "internal.h"
 #include "plan.h"
+#include "reshard.h"
 
 using namespace tccl;
 
 namespace tccl {
 
 namespace {
+int elem_size_of_dtype(int dtype) { return dtype == kBF16 ? 2 : 4; }
+}  // namespace
+
 bool ranges_overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb) {
   if (na == 0 || nb == 0) return false;
   return a < b + nb && b < a + na;
 }
-int elem_size_of_dtype(int dtype) { return dtype == kBF16 ? 2 : 4; }
-}  // namespace
 
 // Argument rules shared by every collective entry point (see plan.h).
 int validate_collective_args(int coll, int nranks, const void* const* send, void* const* recv,
@@ -273,6 +275,14 @@ void dump_plan(const Plan& pl, const Lowered& low) {
 
 }  // namespace
 
+struct CachedReshard {
+  ReshardPlan plan;
+  unsigned char* d_table = nullptr;
+  ~CachedReshard() {
+    if (d_table) cudaFree(d_table);
+  }
+};
+
 struct tcclGroup {
   int nranks = 0;
   int device = 0;
@@ -283,6 +293,7 @@ struct tcclGroup {
   bool record_sms = false;
   uint64_t inject_ns = 0;
   std::map<PlanKey, std::unique_ptr<CachedPlan>> plans;
+  std::map<std::string, std::unique_ptr<CachedReshard>> reshards;
   tcclLaunchInfo_t last;
 };
 
@@ -420,6 +431,44 @@ tcclResult_t run_collective(tcclGroup* g, int coll, const void* const* send, voi
   return tcclSuccess;
 }
 
+bool to_layout(const tcclLayout_t* p, MeshLayout* l) {
+  if (!p || p->ndims < 1 || p->ndims > TCCL_MAX_MESH_DIMS) return false;
+  l->ndims = p->ndims;
+  l->start = p->start_rank;
+  for (int a = 0; a < p->ndims; ++a) {
+    l->dims[a] = p->dims[a];
+    l->place[a] = p->placements[a];
+  }
+  return true;
+}
+
+// Validates a reshard call's buffers against the plan's block sizes.
+tcclResult_t check_reshard_buffers(const MeshLayout& src, const MeshLayout& dst, int nd,
+                                   const uint64_t* shape, int es, const void* const* sb,
+                                   void* const* dbuf) {
+  if (!sb || !dbuf) return tcclInvalidArgument;
+  auto block_bytes = [&](const MeshLayout& l, int m) {
+    Box b = layout_box(l, nd, shape, m);
+    uint64_t n = (uint64_t)es;
+    for (int d = 0; d < nd; ++d) n *= b.hi[d] - b.lo[d];
+    return n;
+  };
+  for (int m = 0; m < src.size(); ++m)
+    if (!sb[m] || (uintptr_t)sb[m] % es) return tcclInvalidArgument;
+  for (int m = 0; m < dst.size(); ++m)
+    if (!dbuf[m] || (uintptr_t)dbuf[m] % es) return tcclInvalidArgument;
+  for (int m = 0; m < dst.size(); ++m) {
+    const uintptr_t a = (uintptr_t)dbuf[m];
+    const uint64_t na = block_bytes(dst, m);
+    for (int k = 0; k < dst.size(); ++k)
+      if (k != m && ranges_overlap(a, na, (uintptr_t)dbuf[k], block_bytes(dst, k)))
+        return tcclInvalidArgument;
+    for (int k = 0; k < src.size(); ++k)
+      if (ranges_overlap(a, na, (uintptr_t)sb[k], block_bytes(src, k))) return tcclInvalidArgument;
+  }
+  return tcclSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -473,6 +522,7 @@ tcclResult_t tcclGroupDestroy(tcclGroup_t g) {
   if (!g) return tcclInvalidArgument;
   cudaDeviceSynchronize();
   g->plans.clear();
+  g->reshards.clear();
   cudaFree(g->d_status);
   cudaFree(g->d_sm_mask);
   delete g;
@@ -490,6 +540,7 @@ tcclResult_t tcclGroupSetConfig(tcclGroup_t g, const tcclConfig_t* cfg) {
   cudaDeviceSynchronize();  // plans in flight keep their device tables until done
   g->cfg = from_public(*cfg);
   g->plans.clear();
+  g->reshards.clear();
   return tcclSuccess;
 }
 
@@ -551,6 +602,136 @@ tcclResult_t tcclGroupReadSmRecord(tcclGroup_t g, int* distinct_sms) {
   int n = 0;
   for (uint32_t w : m) n += __builtin_popcount(w);
   *distinct_sms = n;
+  return tcclSuccess;
+}
+
+tcclResult_t tcclReshard(tcclGroup_t g, const void* const srcbufs[], const tcclLayout_t* src,
+                         void* const dstbufs[], const tcclLayout_t* dst, int tensor_ndims,
+                         const size_t* tensor_shape, tcclDataType_t datatype,
+                         cudaStream_t stream, int cta_cap) {
+  if (!g || !tensor_shape || tensor_ndims < 1 || tensor_ndims > TCCL_MAX_TENSOR_DIMS)
+    return tcclInvalidArgument;
+  if (datatype < tcclFloat32 || datatype > tcclInt32) return tcclInvalidArgument;
+  MeshLayout sl, dl;
+  if (!to_layout(src, &sl) || !to_layout(dst, &dl)) return tcclInvalidArgument;
+  uint64_t shape[TCCL_MAX_TENSOR_DIMS];
+  for (int d = 0; d < tensor_ndims; ++d) shape[d] = tensor_shape[d];
+  std::string why;
+  if (!check_layout(sl, tensor_ndims, shape, &why) || !check_layout(dl, tensor_ndims, shape, &why) ||
+      sl.start + sl.size() > g->nranks || dl.start + dl.size() > g->nranks) {
+    if (log_level()) std::fprintf(stderr, "[tccl] reshard: %s\n", why.empty() ? "mesh outside the group" : why.c_str());
+    return tcclInvalidArgument;
+  }
+  const int es = elem_size_of(datatype);
+  tcclResult_t v = check_reshard_buffers(sl, dl, tensor_ndims, shape, es, srcbufs, dstbufs);
+  if (v != tcclSuccess) return v;
+  // plan cache key: layouts, shape, element size, cap, buffer alignments
+  std::string key;
+  auto put = [&](const void* p, size_t n) { key.append(static_cast<const char*>(p), n); };
+  put(&sl, sizeof(sl));
+  put(&dl, sizeof(dl));
+  put(&tensor_ndims, sizeof(int));
+  put(shape, sizeof(uint64_t) * tensor_ndims);
+  put(&es, sizeof(int));
+  put(&cta_cap, sizeof(int));
+  std::vector<uint8_t> sm(sl.size()), dm(dl.size());
+  for (int m = 0; m < sl.size(); ++m) sm[m] = (uint8_t)((uintptr_t)srcbufs[m] & 15);
+  for (int m = 0; m < dl.size(); ++m) dm[m] = (uint8_t)((uintptr_t)dstbufs[m] & 15);
+  put(sm.data(), sm.size());
+  put(dm.data(), dm.size());
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return tcclCudaError;
+  if (cur != g->device && cudaSetDevice(g->device) != cudaSuccess) return tcclCudaError;
+  tcclResult_t result = tcclSuccess;
+  auto it = g->reshards.find(key);
+  CachedReshard* cr = nullptr;
+  if (it != g->reshards.end()) {
+    cr = it->second.get();
+  } else {
+    auto fresh = std::make_unique<CachedReshard>();
+    if (!plan_reshard(sl, dl, tensor_ndims, shape, es, sm.data(), dm.data(), g->dev.sm_count,
+                      cta_cap, &fresh->plan, &why)) {
+      if (log_level()) std::fprintf(stderr, "[tccl] reshard: %s\n", why.c_str());
+      result = tcclInvalidArgument;
+    } else {
+      const size_t wb = fresh->plan.win.size() * sizeof(ReshardWindow);
+      const size_t pb = fresh->plan.unit_prefix.size() * sizeof(uint64_t);
+      std::vector<unsigned char> host(wb + pb);
+      if (wb) std::memcpy(host.data(), fresh->plan.win.data(), wb);
+      std::memcpy(host.data() + wb, fresh->plan.unit_prefix.data(), pb);
+      if (cudaMalloc(&fresh->d_table, host.size()) != cudaSuccess ||
+          cudaMemcpy(fresh->d_table, host.data(), host.size(), cudaMemcpyHostToDevice) != cudaSuccess)
+        result = tcclCudaError;
+      else {
+        cr = fresh.get();
+        g->reshards.emplace(key, std::move(fresh));
+      }
+    }
+  }
+  if (result == tcclSuccess && !cr->plan.win.empty()) {
+    ReshardArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.win = reinterpret_cast<const ReshardWindow*>(cr->d_table);
+    a.unit_prefix = reinterpret_cast<const uint64_t*>(cr->d_table + cr->plan.win.size() * sizeof(ReshardWindow));
+    for (int m = 0; m < sl.size(); ++m) a.src[m] = srcbufs[m];
+    for (int m = 0; m < dl.size(); ++m) a.dst[m] = dstbufs[m];
+    a.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
+    a.nwin = (int)cr->plan.win.size();
+    a.elem_size = es;
+    if (launch_reshard(a, cr->plan.grid, stream) != 0) result = tcclCudaError;
+    std::memset(&g->last, 0, sizeof(g->last));
+    g->last.ctas = cr->plan.grid;
+    g->last.threads = 256;
+    g->last.windows = (int)cr->plan.win.size();
+    g->last.tasks = (int)cr->plan.transfers.size();
+  }
+  if (cur != g->device) cudaSetDevice(cur);
+  return result;
+}
+
+tcclResult_t tcclReshardInspect(const tcclLayout_t* src, const tcclLayout_t* dst,
+                                int tensor_ndims, const size_t* tensor_shape,
+                                tcclDataType_t datatype, const void* const srcbufs[],
+                                void* const dstbufs[], int sm_count, int cta_cap,
+                                int64_t* transfers, int max_transfers, int* n_transfers,
+                                int64_t* bytes_read, int64_t* bytes_written, int* n_windows) {
+  if (!tensor_shape || tensor_ndims < 1 || tensor_ndims > TCCL_MAX_TENSOR_DIMS || !n_transfers ||
+      !bytes_read || !bytes_written || !n_windows || sm_count < 1)
+    return tcclInvalidArgument;
+  if (datatype < tcclFloat32 || datatype > tcclInt32) return tcclInvalidArgument;
+  MeshLayout sl, dl;
+  if (!to_layout(src, &sl) || !to_layout(dst, &dl)) return tcclInvalidArgument;
+  uint64_t shape[TCCL_MAX_TENSOR_DIMS];
+  for (int d = 0; d < tensor_ndims; ++d) shape[d] = tensor_shape[d];
+  std::string why;
+  if (!check_layout(sl, tensor_ndims, shape, &why) || !check_layout(dl, tensor_ndims, shape, &why))
+    return tcclInvalidArgument;
+  const int es = elem_size_of(datatype);
+  tcclResult_t v = check_reshard_buffers(sl, dl, tensor_ndims, shape, es, srcbufs, dstbufs);
+  if (v != tcclSuccess) return v;
+  std::vector<uint8_t> sm(sl.size()), dm(dl.size());
+  for (int m = 0; m < sl.size(); ++m) sm[m] = (uint8_t)((uintptr_t)srcbufs[m] & 15);
+  for (int m = 0; m < dl.size(); ++m) dm[m] = (uint8_t)((uintptr_t)dstbufs[m] & 15);
+  ReshardPlan plan;
+  if (!plan_reshard(sl, dl, tensor_ndims, shape, es, sm.data(), dm.data(), sm_count, cta_cap,
+                    &plan, &why))
+    return tcclInvalidArgument;
+  *n_transfers = (int)plan.transfers.size();
+  *bytes_read = (int64_t)plan.bytes_read;
+  *bytes_written = (int64_t)plan.bytes_written;
+  *n_windows = (int)plan.win.size();
+  if (transfers) {
+    for (int i = 0; i < std::min(max_transfers, (int)plan.transfers.size()); ++i) {
+      const ReshardTransfer& t = plan.transfers[i];
+      int64_t* o = transfers + 10 * (size_t)i;
+      o[0] = t.src_rank;
+      o[1] = (int64_t)t.dst_mask;
+      for (int d = 0; d < 4; ++d) {
+        o[2 + d] = d < tensor_ndims ? (int64_t)t.box.lo[d] : 0;
+        o[6 + d] = d < tensor_ndims ? (int64_t)t.box.hi[d] : 0;
+      }
+    }
+  }
   return tcclSuccess;
 }
 

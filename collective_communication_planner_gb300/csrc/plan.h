@@ -116,6 +116,9 @@ void pack_bulk_table(const Lowered& low, std::vector<unsigned char>* out, size_t
 int validate_collective_args(int coll, int nranks, const void* const* send, void* const* recv,
                              size_t count, int dtype, int op);
 
+// [a, a + na) and [b, b + nb) share a byte.
+bool ranges_overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb);
+
 // Per-rank message size the Auto engine choice looks at.
 uint64_t message_bytes(int coll, int nranks, uint64_t count, int elem_size);
 

@@ -248,6 +248,57 @@ tcclResult_t tcclPlanInspect(int coll, int nranks, const void* const sendbufs[],
 tcclResult_t tcclGroupInjectWaitTimeout(tcclGroup_t g, int enable, double timeout_ms);
 
 /*
+ * M-to-N reshard between two layouts of one tensor (the M2N collective of the
+ * "NCCL M2N vs T-CCL" article, §1.2-§1.4, on logical ranks of one GPU).
+ *
+ * A layout is a mesh of ranks: `ndims` dimensions `dims` in row-major rank
+ * order, holding group ranks [start_rank, start_rank + prod(dims)), and one
+ * placement per mesh axis, TCCL_REPLICATE or the tensor dimension that axis
+ * shards into equal contiguous blocks. At most one axis may shard (the
+ * article's constraint), each sharded dimension must divide evenly, and the
+ * source and destination meshes must not share ranks.
+ *
+ * srcbufs[m] / dstbufs[m] is mesh rank m's local block, contiguous and
+ * row-major. Source replicas must hold identical data. Afterwards every
+ * destination rank holds exactly the block its layout names. The plan comes
+ * from the layouts alone by interval intersection: every piece a destination
+ * block needs is read once, from the least-loaded source replica, and written
+ * to every destination replica of that block.
+ *
+ * Errors: tcclInvalidArgument for a bad layout, shape, pointer or overlap
+ * (destination buffers may not overlap each other or any source), or meshes
+ * outside the group's ranks.
+ */
+#define TCCL_REPLICATE (-1)
+#define TCCL_MAX_MESH_DIMS 4
+#define TCCL_MAX_TENSOR_DIMS 4
+typedef struct {
+  int ndims;
+  int dims[TCCL_MAX_MESH_DIMS];
+  int start_rank;
+  int placements[TCCL_MAX_MESH_DIMS];
+} tcclLayout_t;
+
+tcclResult_t tcclReshard(tcclGroup_t g, const void* const srcbufs[], const tcclLayout_t* src,
+                         void* const dstbufs[], const tcclLayout_t* dst, int tensor_ndims,
+                         const size_t* tensor_shape, tcclDataType_t datatype,
+                         cudaStream_t stream, int cta_cap);
+
+/*
+ * Host-only view of a reshard plan (no GPU needed). Writes up to
+ * `max_transfers` transfers, ten int64 values each:
+ *   {source mesh rank, destination replica mask, lo[4], hi[4]} (global
+ *   coordinates of the piece; unused dimensions 0), and the totals.
+ * Buffer addresses are used only for their alignment.
+ */
+tcclResult_t tcclReshardInspect(const tcclLayout_t* src, const tcclLayout_t* dst,
+                                int tensor_ndims, const size_t* tensor_shape,
+                                tcclDataType_t datatype, const void* const srcbufs[],
+                                void* const dstbufs[], int sm_count, int cta_cap,
+                                int64_t* transfers, int max_transfers, int* n_transfers,
+                                int64_t* bytes_read, int64_t* bytes_written, int* n_windows);
+
+/*
  * Allreduce for callers that cannot allocate GPU memory (no counterpart in
  * the paper: a convenience of this library).
  *

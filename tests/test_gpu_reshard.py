@@ -1,0 +1,94 @@
+"""GPU parity for tcclReshard against the reshard oracle, bit for bit:
+the article's example A, many (mesh, placement) pairs, three dtypes, 2-D and
+3-D tensors, misaligned buffers (element-wise path), CTA caps, and a
+weight-sized reshard."""
+import numpy as np
+import pytest
+import torch
+
+import collective_communication_planner_gb300 as tccl
+import datagen
+from gpu_util import Guarded, first_mismatch, to_device, to_host
+from oracle import reshard as rs
+
+pytestmark = pytest.mark.gpu
+R = tccl.TCCL_REPLICATE
+KIND = {"f32": "uniform_f32", "bf16": "normal_bf16", "i32": "int32"}
+
+
+def global_tensor(dtype, shape, seed=5):
+    n = int(np.prod(shape))
+    return datagen.rank_buffers(KIND[dtype], seed, 1, n)[0].reshape(shape)
+
+
+def src_blocks(glob, dims, place):
+    out = []
+    for m in range(rs.nranks(dims)):
+        box = rs.local_box(glob.shape, dims, place, m)
+        out.append(np.ascontiguousarray(glob[tuple(slice(lo, hi) for lo, hi in box)]).ravel())
+    return out
+
+
+def run(g, glob, src, dst, dtype, cap=0, mis=0):
+    shape = glob.shape
+    sb = src_blocks(glob, *src)
+    exp = rs.reshard(sb, src[0], src[1], dst[0], dst[1], shape)
+    sends = []
+    for b in sb:
+        t = Guarded(b.size, dtype, mis)
+        t.tensor.copy_(to_device(b))
+        sends.append(t)
+    recvs = [Guarded(e.size, dtype, mis) for e in exp]
+    g.reshard([t.tensor for t in sends], tccl.make_layout(src[0], src[1], 0),
+              [t.tensor for t in recvs], tccl.make_layout(dst[0], dst[1], rs.nranks(src[0])),
+              shape, cta_cap=cap)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    for m, (t, e) in enumerate(zip(recvs, exp)):
+        assert t.guards_intact()
+        mm = first_mismatch(t.host(), e)
+        assert mm is None, f"{src} -> {dst} {dtype}: rank {m} first mismatch {mm}"
+
+
+@pytest.fixture(scope="module")
+def group():
+    g = tccl.Group(64)
+    yield g
+    g.close()
+
+
+def test_article_example_a(group, golden_dir):
+    glob = global_tensor("bf16", (4, 8))
+    run(group, glob, ((1, 4), (R, 0)), ((2, 2), (R, 0)), "bf16")
+
+
+LAYOUTS = [((4,), (0,)), ((4,), (R,)), ((2, 2), (R, 0)), ((2, 2), (0, R)), ((2, 2), (1, R)),
+           ((1, 4), (R, 1)), ((2, 4), (R, 0)), ((8,), (1,)), ((2, 1, 2), (R, R, 1))]
+
+
+@pytest.mark.parametrize("src", LAYOUTS)
+@pytest.mark.parametrize("dst", LAYOUTS[::2])
+def test_layout_pairs(group, src, dst):
+    glob = global_tensor("f32", (64, 96))
+    run(group, glob, src, dst, "f32")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("mis", [0, 4])
+@pytest.mark.parametrize("cap", [0, 3])
+def test_dtypes_alignment_caps(group, dtype, mis, cap):
+    glob = global_tensor(dtype, (256, 1000))
+    run(group, glob, ((8,), (1,)), ((2, 2), (R, 0)), dtype, cap=cap, mis=mis)
+    run(group, glob, ((4,), (0,)), ((2, 4), (R, 1)), dtype, cap=cap, mis=mis)
+
+
+def test_three_dimensional(group):
+    glob = global_tensor("bf16", (8, 16, 64))
+    run(group, glob, ((2, 2), (R, 2)), ((4,), (1,)), "bf16")
+    run(group, glob, ((4,), (0,)), ((2, 4), (R, 2)), "bf16")
+
+
+def test_weight_sized_reshard(group):
+    # an 8192 x 8192 bf16 weight: TP8 (row shards) -> TP2 x DP4 (column shards, replicated)
+    glob = global_tensor("bf16", (8192, 8192), seed=9)
+    run(group, glob, ((8,), (0,)), ((4, 2), (R, 1)), "bf16")
