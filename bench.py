@@ -826,6 +826,76 @@ def reshard_bench(args):
     g.close()
 
 
+# ------------------------------------------------------------------ rmsnorm mode
+def rmsnorm_bench(args):
+    """The allreduce fused with RMSNorm against the plain allreduce, on the
+    C5 shapes (P=8, bf16 [tokens, 8192]): device time per op (and per op in a
+    CUDA graph for small token counts), GB/s of 2*P*S + gamma bytes. Results
+    checked against the RMSNorm oracle (within one bf16 ulp)."""
+    import numpy as np
+    import torch
+    import collective_communication_planner_gb300 as tccl
+    import datagen
+    from oracle import rmsnorm as rn
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    p, hidden = 8, 8192
+    g = tccl.Group(p)
+    stream = torch.cuda.current_stream()
+    peak, _ = measured_peak()
+    gamma_h = datagen.rank_buffers("normal_bf16", 104, 1, hidden)[0]
+    gamma = host_to_torch(gamma_h).to(dev)
+
+    def ev(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def graph_us(fn):
+        s2 = torch.cuda.Stream()
+        with torch.cuda.stream(s2):
+            fn()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s2):
+            for _ in range(20):
+                fn()
+        return ev(gr.replay, 20) / 20 * 1e3
+
+    for tokens in (1, 8, 64, 512, 4096):
+        n = tokens * hidden
+        xs = datagen.rank_buffers("normal_bf16", 4, p, n)
+        exp, exp64 = rn.allreduce_rmsnorm(xs, gamma_h, tokens, hidden, 1e-6, "bf16")
+        sends = [host_to_torch(x).to(dev).view(tokens, hidden) for x in xs]
+        recvs = [torch.empty_like(t) for t in sends]
+        fused = lambda: g.all_reduce_rmsnorm(sends, recvs, gamma)
+        plain = lambda: g.all_reduce(sends, recvs)
+        reps = 200 if tokens <= 64 else 30
+        f_ms, p_ms = ev(fused, reps), ev(plain, reps)
+        fused()
+        torch.cuda.synchronize()
+        got = recvs[5].view(torch.int16).cpu().numpy().ravel().view(np.uint16)
+        d = np.abs(got.astype(np.int64) - exp.astype(np.int64))
+        row = {"mode": "rmsnorm", "P": p, "tokens": tokens, "hidden": hidden,
+               "fused_us": round(f_ms * 1e3, 2), "allreduce_us": round(p_ms * 1e3, 2),
+               "fused_hbm_fraction": round((2 * p * n * 2 + hidden * 2) / (f_ms * 1e-3) / 1e9 / peak, 4),
+               "max_ulp": int(d.max()), "ulp_mismatches": int(np.count_nonzero(d))}
+        if tokens <= 64:
+            row["fused_graph_us"] = round(graph_us(fused), 2)
+            row["allreduce_graph_us"] = round(graph_us(plain), 2)
+        print(json.dumps(row), flush=True)
+    assert g.query_error() == tccl.tcclSuccess
+    g.close()
+
+
 # ------------------------------------------------------------------ probe mode
 def probe():
     """Builds and runs the per-SM bandwidth probe
@@ -864,6 +934,8 @@ def main():
                     help="allreduce beside a concurrent cuBLAS GEMM, across CTA caps")
     ap.add_argument("--reshard", action="store_true",
                     help="M-to-N reshard throughput on an 8192 x 8192 bf16 weight")
+    ap.add_argument("--rmsnorm", action="store_true",
+                    help="allreduce fused with RMSNorm vs the plain allreduce (C5 shapes)")
     ap.add_argument("--gemm-n", type=int, default=8192)
     ap.add_argument("--overlap-engine", type=int, default=0,
                     help="engine for the overlap study (0 auto, 1 bulk, 4 TMA-reduce)")
@@ -904,6 +976,9 @@ def main():
         return
     if args.reshard:
         reshard_bench(args)
+        return
+    if args.rmsnorm:
+        rmsnorm_bench(args)
         return
     if dist is not None:
         dist.barrier()

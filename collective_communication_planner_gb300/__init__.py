@@ -104,6 +104,7 @@ def _open():
                                 ctypes.POINTER(i), ctypes.POINTER(tcclLaunchInfo_t)]),
         "tcclGroupInjectWaitTimeout": (i, [vp, i, ctypes.c_double]),
         "tcclAllReduceNoAlloc": (i, [i, pvp, pvp, sz, i, i, vp, i]),
+        "tcclAllReduceRMSNorm": (i, [vp, pvp, pvp, sz, sz, vp, ctypes.c_float, i, vp, i]),
         "tcclReshard": (i, [vp, pvp, ctypes.POINTER(tcclLayout_t), pvp,
                             ctypes.POINTER(tcclLayout_t), i, ctypes.POINTER(sz), i, vp, i]),
         "tcclReshardInspect": (i, [ctypes.POINTER(tcclLayout_t), ctypes.POINTER(tcclLayout_t), i,
@@ -126,7 +127,7 @@ EXPORTED = ("tcclGetErrorString", "tcclGetVersion", "tcclGroupCreate", "tcclGrou
             "tcclAllGather", "tcclGroupQueryError", "tcclGetLastLaunchInfo",
             "tcclGroupRecordSms", "tcclGroupReadSmRecord", "tcclPlanInspect",
             "tcclGroupInjectWaitTimeout", "tcclAllReduceNoAlloc", "tcclReshard",
-            "tcclReshardInspect")
+            "tcclReshardInspect", "tcclAllReduceRMSNorm")
 
 
 def _ptr(x) -> int:
@@ -223,6 +224,14 @@ def tcclAllReduceNoAlloc(nranks, sendbufs, recvbufs, count, datatype, op, stream
     sp, _k1 = _ptr_array(sendbufs)
     rp, _k2 = _ptr_array(recvbufs)
     return _lib.tcclAllReduceNoAlloc(nranks, sp, rp, count, datatype, op, _stream(stream), cta_cap)
+
+
+def tcclAllReduceRMSNorm(group, sendbufs, recvbufs, rows, hidden, gamma, eps, datatype,
+                         stream=None, cta_cap=0) -> int:
+    sp, _k1 = _ptr_array(sendbufs)
+    rp, _k2 = _ptr_array(recvbufs)
+    return _lib.tcclAllReduceRMSNorm(group, sp, rp, rows, hidden, _ptr(gamma), float(eps),
+                                     datatype, _stream(stream), cta_cap)
 
 
 def _shape(shape):
@@ -384,6 +393,16 @@ class Group:
         _check(tcclAllGather(self.handle, sends, recvs, sends[0].numel(), dt,
                              stream if stream is not None else _current_stream(), cta_cap),
                "tcclAllGather")
+        return recvs
+
+    def all_reduce_rmsnorm(self, sends, recvs, gamma, eps=1e-6, cta_cap=0, stream=None):
+        """recvs[r][t, :] = RMSNorm(sum over ranks of sends[.][t, :]) * gamma, with
+        every tensor [rows, hidden] (see tcclAllReduceRMSNorm)."""
+        rows, hidden = sends[0].shape
+        dt = _dtype_code(sends[0])
+        _check(tcclAllReduceRMSNorm(self.handle, sends, recvs, rows, hidden, gamma, eps, dt,
+                                    stream if stream is not None else _current_stream(), cta_cap),
+               "tcclAllReduceRMSNorm")
         return recvs
 
     def reshard(self, srcs, src_layout, dsts, dst_layout, shape, cta_cap=0, stream=None):

@@ -17,6 +17,7 @@
 #include "internal.h"
 #include "plan.h"
 #include "reshard.h"
+#include "rmsnorm.h"
 
 using namespace tccl;
 
@@ -687,6 +688,57 @@ tcclResult_t tcclReshard(tcclGroup_t g, const void* const srcbufs[], const tcclL
   }
   if (cur != g->device) cudaSetDevice(cur);
   return result;
+}
+
+tcclResult_t tcclAllReduceRMSNorm(tcclGroup_t g, const void* const sendbufs[],
+                                  void* const recvbufs[], size_t rows, size_t hidden,
+                                  const void* gamma, float eps, tcclDataType_t datatype,
+                                  cudaStream_t stream, int cta_cap) {
+  if (!g) return tcclInvalidArgument;
+  if (datatype != tcclFloat32 && datatype != tcclBfloat16) return tcclInvalidArgument;
+  const int es = elem_size_of(datatype);
+  const size_t vec_elems = 16 / es;
+  const size_t max_hidden = std::min<size_t>((size_t)kRmsMaxThreads * kRmsMaxVectors * vec_elems,
+                                             (size_t)16384);
+  if (hidden == 0 || hidden % vec_elems || hidden > max_hidden || !(eps >= 0.f)) return tcclInvalidArgument;
+  if (rows > (SIZE_MAX / 4) / hidden) return tcclInvalidArgument;
+  tcclResult_t v = (tcclResult_t)validate_collective_args(kAllReduce, g->nranks, sendbufs, recvbufs,
+                                                          rows * hidden, datatype, kSum);
+  if (v != tcclSuccess) return v;
+  if (rows == 0) return tcclSuccess;
+  if (!gamma || (uintptr_t)gamma % 16) return tcclInvalidArgument;
+  for (int r = 0; r < g->nranks; ++r) {
+    if ((uintptr_t)sendbufs[r] % 16 || (uintptr_t)recvbufs[r] % 16) return tcclInvalidArgument;
+    if (ranges_overlap((uintptr_t)gamma, hidden * es, (uintptr_t)recvbufs[r], rows * hidden * es))
+      return tcclInvalidArgument;
+  }
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return tcclCudaError;
+  if (cur != g->device && cudaSetDevice(g->device) != cudaSuccess) return tcclCudaError;
+  RmsArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int r = 0; r < g->nranks; ++r) {
+    a.p.src[r] = sendbufs[r];
+    a.p.dst[r] = recvbufs[r];
+  }
+  a.gamma = gamma;
+  a.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
+  a.rows = rows;
+  a.hidden = (uint32_t)hidden;
+  a.eps = eps;
+  a.nranks = g->nranks;
+  const size_t nvec = hidden / vec_elems;
+  const int vectors = nvec > (size_t)4 * kRmsMaxThreads ? 8 : 4;
+  int threads = (int)std::min<size_t>(kRmsMaxThreads, ((nvec + vectors - 1) / vectors + 31) / 32 * 32);
+  threads = std::max(threads, 32);
+  uint64_t grid = std::min<uint64_t>(rows, (uint64_t)g->dev.sm_count * 8);
+  if (cta_cap > 0) grid = std::min<uint64_t>(grid, (uint64_t)cta_cap);
+  const int err = launch_rmsnorm(datatype, a, (int)grid, threads, vectors, stream);
+  std::memset(&g->last, 0, sizeof(g->last));
+  g->last.ctas = (int)grid;
+  g->last.threads = threads;
+  if (cur != g->device) cudaSetDevice(cur);
+  return err == 0 ? tcclSuccess : tcclCudaError;
 }
 
 tcclResult_t tcclReshardInspect(const tcclLayout_t* src, const tcclLayout_t* dst,

@@ -1,0 +1,109 @@
+// Allreduce of [rows, hidden] activations fused with an RMSNorm of each
+// reduced row, before the row is stored to every rank (the Device API example
+// the "NCCL Roadmap" post describes: receive, sum, normalise, send out in one
+// kernel). The reduced row never leaves the chip unnormalised.
+#include "kernels_common.cuh"
+#include "rmsnorm.h"
+
+namespace tccl {
+namespace {
+
+// V: 16-byte vectors of a row per thread. Loads of RB ranks are issued
+// together before they are folded (ascending rank order is kept), so a row
+// costs a few memory round trips, not P of them.
+template <int DT, int V>
+__global__ void __launch_bounds__(kRmsMaxThreads) rmsnorm_kernel(const __grid_constant__ RmsArgs a) {
+  using dev::Fold;
+  constexpr int kVecElems = DT == kBF16 ? 8 : 4;
+  constexpr int RB = 16 / V;  // ranks per load batch: V * RB 16-byte registers in flight
+  extern __shared__ __align__(16) uint4 gamma_smem[];
+  __shared__ float partial[kRmsMaxThreads / 32];
+  __shared__ float row_scale;
+  if (threadIdx.x == 0) dev::record_sm(a.sm_mask);
+  const int P = a.nranks;
+  const uint32_t nvec = a.hidden / kVecElems;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (uint32_t v = threadIdx.x; v < nvec; v += blockDim.x)
+    gamma_smem[v] = dev::ld_global_v4(static_cast<const char*>(a.gamma) + v * 16ull);
+  __syncthreads();
+  for (uint64_t t = blockIdx.x; t < a.rows; t += gridDim.x) {
+    const uint64_t row_off = t * static_cast<uint64_t>(a.hidden) * (DT == kBF16 ? 2 : 4);
+    Fold<DT, kSum> acc[V];
+    for (int r0 = 0; r0 < P; r0 += RB) {
+      uint4 x[V][RB];
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const uint32_t v = threadIdx.x + j * blockDim.x;
+#pragma unroll
+        for (int k = 0; k < RB; ++k)
+          if (v < nvec && r0 + k < P)
+            x[j][k] = dev::ld_global_v4(static_cast<const char*>(a.p.src[r0 + k]) + row_off + v * 16ull);
+      }
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const uint32_t v = threadIdx.x + j * blockDim.x;
+        if (v < nvec) {
+#pragma unroll
+          for (int k = 0; k < RB; ++k) {
+            if (r0 + k >= P) break;
+            if (r0 + k == 0) acc[j].init(x[j][k]);
+            else acc[j].add(x[j][k]);
+          }
+        }
+      }
+    }
+    // sum of squares of the reduced row
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const uint32_t v = threadIdx.x + j * blockDim.x;
+      if (v < nvec)
+#pragma unroll
+        for (int e = 0; e < kVecElems; ++e) ss = __fadd_rn(ss, __fmul_rn(acc[j].a[e], acc[j].a[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, o));
+    if (lane == 0) partial[warp] = ss;
+    __syncthreads();
+    if (warp == 0) {
+      float w = lane < nwarps ? partial[lane] : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) w = __fadd_rn(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
+      if (lane == 0) row_scale = rsqrtf(__fadd_rn(__fdiv_rn(w, static_cast<float>(a.hidden)), a.eps));
+    }
+    __syncthreads();
+    const float scale = row_scale;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const uint32_t v = threadIdx.x + j * blockDim.x;
+      if (v < nvec) {
+        Fold<DT, kSum> g;
+        g.init(gamma_smem[v]);
+#pragma unroll
+        for (int e = 0; e < kVecElems; ++e)
+          acc[j].a[e] = __fmul_rn(__fmul_rn(acc[j].a[e], scale), g.a[e]);
+        const uint4 y = acc[j].out();
+        const uint64_t o = row_off + v * 16ull;
+        for (int d = 0; d < P; ++d) dev::st_global_v4(static_cast<char*>(a.p.dst[d]) + o, y);
+      }
+    }
+    __syncthreads();  // partial[] and row_scale are reused by the next row
+  }
+}
+
+}  // namespace
+
+int launch_rmsnorm(int dtype, const RmsArgs& a, int grid, int threads, int vectors, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t smem = static_cast<size_t>(a.hidden) * (dtype == kBF16 ? 2 : 4);
+  if (dtype == kBF16) {
+    if (vectors <= 4) rmsnorm_kernel<kBF16, 4><<<grid, threads, smem, st>>>(a);
+    else rmsnorm_kernel<kBF16, 8><<<grid, threads, smem, st>>>(a);
+  } else {
+    if (vectors <= 4) rmsnorm_kernel<kF32, 4><<<grid, threads, smem, st>>>(a);
+    else rmsnorm_kernel<kF32, 8><<<grid, threads, smem, st>>>(a);
+  }
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace tccl

@@ -248,6 +248,26 @@ tcclResult_t tcclPlanInspect(int coll, int nranks, const void* const sendbufs[],
 tcclResult_t tcclGroupInjectWaitTimeout(tcclGroup_t g, int enable, double timeout_ms);
 
 /*
+ * Allreduce fused with RMSNorm (the "NCCL Roadmap" post, section "GENK と
+ * Flow", mentions a Device API example that folds a Transformer RMSNorm into
+ * one kernel with the reduce-scatter and all-gather). Every rank buffer holds
+ * [rows, hidden] activations; afterwards every recv buffer holds
+ *   y[t, j] = s[t, j] * rsqrt(mean_k(s[t, k]^2) + eps) * gamma[j],
+ * s = the ascending-rank fp32 sum of the sends (never rounded), y rounded once
+ * to the datatype (fp32 or bf16). gamma: `hidden` elements of the datatype in
+ * device memory. The row's sum of squares is a parallel reduction, so results
+ * match a plain evaluation to within one unit in the last place of the output
+ * type, not bit for bit.
+ * Limits: hidden a multiple of 8 (bf16) or 4 (fp32), at most 16384 (bf16) or
+ * 8192 (fp32); every buffer 16-byte aligned; in place allowed as for
+ * tcclAllReduce; int32 is tcclInvalidArgument.
+ */
+tcclResult_t tcclAllReduceRMSNorm(tcclGroup_t g, const void* const sendbufs[],
+                                  void* const recvbufs[], size_t rows, size_t hidden,
+                                  const void* gamma, float eps, tcclDataType_t datatype,
+                                  cudaStream_t stream, int cta_cap);
+
+/*
  * M-to-N reshard between two layouts of one tensor (the M2N collective of the
  * "NCCL M2N vs T-CCL" article, §1.2-§1.4, on logical ranks of one GPU).
  *

@@ -1,0 +1,103 @@
+"""GPU parity for tcclAllReduceRMSNorm against the RMSNorm oracle.
+
+Tolerance (derived from the arithmetic, the pages give none): the rank sum is
+bit-exact (the same ascending fp32 fold as the allreduce); the row's sum of
+squares is a fp32 tree reduction (relative error below log2(hidden) * 2^-24 ~
+1e-6), rsqrtf adds at most 2 ulp, two fp32 products 2^-23. All of it is far
+below half a bf16 ulp (2^-9), so a bf16 output differs from the fp64-evaluated
+oracle by at most one ulp and only rarely; a fp32 output agrees to 2^-18
+relative."""
+import numpy as np
+import pytest
+import torch
+
+import collective_communication_planner_gb300 as tccl
+import datagen
+from gpu_util import to_device, to_host
+from oracle import rmsnorm as rn
+
+pytestmark = pytest.mark.gpu
+KIND = {"f32": "uniform_f32", "bf16": "normal_bf16"}
+TORCH = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module")
+def groups():
+    made = {}
+
+    def get(p):
+        if p not in made:
+            made[p] = tccl.Group(p)
+        return made[p]
+
+    yield get
+    for g in made.values():
+        g.close()
+
+
+def check(got, exp_rounded, exp64, dtype, what):
+    if dtype == "bf16":
+        d = np.abs(got.astype(np.int64) - exp_rounded.astype(np.int64))
+        sign_flip = (got >> 15) != (exp_rounded >> 15)
+        assert not np.any(sign_flip & (d > 1)), what
+        assert d.max() <= 1, f"{what}: max bf16 ulp distance {d.max()}"
+        assert np.count_nonzero(d) <= max(2, got.size // 1000), f"{what}: {np.count_nonzero(d)} differ"
+    else:
+        err = np.abs(got.astype(np.float64) - exp64)
+        assert np.all(err <= 2.0 ** -18 * np.abs(exp64) + 1e-30), f"{what}: max rel {np.max(err / (np.abs(exp64) + 1e-30))}"
+
+
+def run(g, dtype, p, rows, hidden, eps=1e-6, cap=0, in_place=False, seed=4):
+    xs = datagen.rank_buffers(KIND[dtype], seed, p, rows * hidden)
+    gamma = datagen.rank_buffers(KIND[dtype], seed + 100, 1, hidden)[0]
+    exp, exp64 = rn.allreduce_rmsnorm(xs, gamma, rows, hidden, eps, dtype)
+    sends = [to_device(x).view(rows, hidden) for x in xs]
+    recvs = sends if in_place else [torch.empty_like(s) for s in sends]
+    g.all_reduce_rmsnorm(sends, recvs, to_device(gamma), eps=eps, cta_cap=cap)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    for r in range(p):
+        check(to_host(recvs[r]).ravel(), exp, exp64, dtype, f"{dtype} P={p} rows={rows} hidden={hidden} rank {r}")
+
+
+@pytest.mark.parametrize("tokens", [1, 8, 64, 512, 4096])
+def test_tp_activations_bf16(groups, tokens):
+    run(groups(8), "bf16", 8, tokens, 8192)
+
+
+@pytest.mark.parametrize("dtype,hidden", [("bf16", 256), ("bf16", 1000), ("bf16", 16384),
+                                          ("f32", 4), ("f32", 4096), ("f32", 8192)])
+@pytest.mark.parametrize("p", [1, 3, 8])
+def test_shapes_and_types(groups, dtype, hidden, p):
+    run(groups(p), dtype, p, 37, hidden)
+
+
+def test_in_place_caps_and_eps(groups):
+    run(groups(4), "bf16", 4, 300, 4096, cap=3, in_place=True)
+    run(groups(4), "f32", 4, 64, 2048, eps=0.5)
+
+
+def test_rejects_unsupported_calls(groups):
+    g = groups(2)
+    st = torch.cuda.current_stream().cuda_stream
+
+    def bufs(rows, hidden, dtype=torch.bfloat16):
+        return [torch.zeros(rows, hidden, dtype=dtype, device="cuda") for _ in range(2)]
+
+    gam = torch.ones(32768, dtype=torch.bfloat16, device="cuda")
+    s, r = bufs(4, 32768), bufs(4, 32768)
+    assert tccl.tcclAllReduceRMSNorm(g.handle, s, r, 4, 32768, gam, 1e-6, 1, st) == \
+        tccl.tcclInvalidArgument  # hidden above the limit
+    s, r = bufs(4, 1003), bufs(4, 1003)
+    assert tccl.tcclAllReduceRMSNorm(g.handle, s, r, 4, 1003, gam, 1e-6, 1, st) == \
+        tccl.tcclInvalidArgument  # not a whole number of 16-byte vectors
+    s, r = bufs(4, 64, torch.int32), bufs(4, 64, torch.int32)
+    assert tccl.tcclAllReduceRMSNorm(g.handle, s, r, 4, 64, gam, 1e-6, 2, st) == \
+        tccl.tcclInvalidArgument  # int32
+    s, r = bufs(4, 64), bufs(4, 64)
+    assert tccl.tcclAllReduceRMSNorm(g.handle, s, r, 4, 64, gam.data_ptr() + 2, 1e-6, 1, st) == \
+        tccl.tcclInvalidArgument  # misaligned gamma
+    assert tccl.tcclAllReduceRMSNorm(g.handle, s, r, 4, 64, gam, -1.0, 1, st) == \
+        tccl.tcclInvalidArgument  # negative eps
+    assert tccl.tcclAllReduceRMSNorm(g.handle, s, r, 4, 64, gam, 1e-6, 1, st) == tccl.tcclSuccess
+    torch.cuda.synchronize()
