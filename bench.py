@@ -67,9 +67,11 @@ def measured_peak():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the bulk allreduce kernel is compiled from (its
+    template, its launch file and the shared argument structs)."""
     h = hashlib.sha256()
     csrc = ROOT / "collective_communication_planner_gb300" / "csrc"
-    for f in sorted(list(csrc.glob("*.cu")) + list(csrc.glob("*.cuh")) + [csrc / "internal.h"]):
+    for f in sorted(csrc / n for n in ("kernels_common.cuh", "dispatch.cuh", "kernels_bulk.cu", "internal.h")):
         h.update(f.name.encode())
         h.update(f.read_bytes())
     return h.hexdigest()[:16]
@@ -842,6 +844,9 @@ def rmsnorm_bench(args):
     torch.cuda.set_device(dev)
     p, hidden = 8, 8192
     g = tccl.Group(p)
+    os.environ["TCCL_RMSNORM_CLUSTER"] = "0"  # a second group with one CTA per row, for comparison
+    g_row = tccl.Group(p)
+    del os.environ["TCCL_RMSNORM_CLUSTER"]
     stream = torch.cuda.current_stream()
     peak, _ = measured_peak()
     gamma_h = datagen.rank_buffers("normal_bf16", 104, 1, hidden)[0]
@@ -877,23 +882,28 @@ def rmsnorm_bench(args):
         sends = [host_to_torch(x).to(dev).view(tokens, hidden) for x in xs]
         recvs = [torch.empty_like(t) for t in sends]
         fused = lambda: g.all_reduce_rmsnorm(sends, recvs, gamma)
+        fused_row = lambda: g_row.all_reduce_rmsnorm(sends, recvs, gamma)
         plain = lambda: g.all_reduce(sends, recvs)
         reps = 200 if tokens <= 64 else 30
         f_ms, p_ms = ev(fused, reps), ev(plain, reps)
         fused()
+        info = g.last_launch()
         torch.cuda.synchronize()
         got = recvs[5].view(torch.int16).cpu().numpy().ravel().view(np.uint16)
         d = np.abs(got.astype(np.int64) - exp.astype(np.int64))
         row = {"mode": "rmsnorm", "P": p, "tokens": tokens, "hidden": hidden,
                "fused_us": round(f_ms * 1e3, 2), "allreduce_us": round(p_ms * 1e3, 2),
                "fused_hbm_fraction": round((2 * p * n * 2 + hidden * 2) / (f_ms * 1e-3) / 1e9 / peak, 4),
-               "max_ulp": int(d.max()), "ulp_mismatches": int(np.count_nonzero(d))}
+               "max_ulp": int(d.max()), "ulp_mismatches": int(np.count_nonzero(d)),
+               "fused_ctas": info["ctas"]}
         if tokens <= 64:
             row["fused_graph_us"] = round(graph_us(fused), 2)
+            row["fused_one_cta_per_row_graph_us"] = round(graph_us(fused_row), 2)
             row["allreduce_graph_us"] = round(graph_us(plain), 2)
         print(json.dumps(row), flush=True)
-    assert g.query_error() == tccl.tcclSuccess
+    assert g.query_error() == tccl.tcclSuccess and g_row.query_error() == tccl.tcclSuccess
     g.close()
+    g_row.close()
 
 
 # ------------------------------------------------------------------ probe mode

@@ -292,6 +292,7 @@ struct tcclGroup {
   int* d_status = nullptr;     // [0] status code
   uint32_t* d_sm_mask = nullptr;  // 256-bit SM bitmap
   bool record_sms = false;
+  bool rms_cluster_enabled = true;  // TCCL_RMSNORM_CLUSTER=0 keeps one CTA per row
   uint64_t inject_ns = 0;
   std::map<PlanKey, std::unique_ptr<CachedPlan>> plans;
   std::map<std::string, std::unique_ptr<CachedReshard>> reshards;
@@ -503,6 +504,7 @@ tcclResult_t tcclGroupCreate(int nranks, tcclGroup_t* out) {
       cudaDeviceGetAttribute(&g->dev.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, g->device) != cudaSuccess)
     return tcclCudaError;
   g->cfg = config_from_env();
+  if (const char* e = std::getenv("TCCL_RMSNORM_CLUSTER")) g->rms_cluster_enabled = std::atoi(e) != 0;
   if (prepare_bulk_kernels((size_t)g->dev.smem_optin) != 0) return tcclCudaError;
   if (cudaMalloc(&g->d_status, 64) != cudaSuccess) return tcclCudaError;
   if (cudaMalloc(&g->d_sm_mask, 64) != cudaSuccess) {
@@ -728,15 +730,34 @@ tcclResult_t tcclAllReduceRMSNorm(tcclGroup_t g, const void* const sendbufs[],
   a.eps = eps;
   a.nranks = g->nranks;
   const size_t nvec = hidden / vec_elems;
-  const int vectors = nvec > (size_t)4 * kRmsMaxThreads ? 8 : 4;
-  int threads = (int)std::min<size_t>(kRmsMaxThreads, ((nvec + vectors - 1) / vectors + 31) / 32 * 32);
-  threads = std::max(threads, 32);
-  uint64_t grid = std::min<uint64_t>(rows, (uint64_t)g->dev.sm_count * 8);
-  if (cta_cap > 0) grid = std::min<uint64_t>(grid, (uint64_t)cta_cap);
-  const int err = launch_rmsnorm(datatype, a, (int)grid, threads, vectors, stream);
+  // Few rows: a cluster of C CTAs shares each row, so a decode-sized call
+  // uses more than one SM per row. C is the largest of 8, 4, 2 whose grid
+  // (rows x C CTAs, two resident per SM) fits in one wave; each CTA's slice
+  // must fit its 4 vectors per thread.
+  int C = kRmsCluster;
+  while (C > 2 && (rows * (size_t)C > (size_t)g->dev.sm_count * 2 || (cta_cap > 0 && cta_cap < C)))
+    C /= 2;
+  const bool cluster = g->rms_cluster_enabled && rows * (size_t)C <= (size_t)g->dev.sm_count * 2 &&
+                       (cta_cap <= 0 || cta_cap >= C) &&
+                       (nvec + C - 1) / C <= (size_t)4 * kRmsClusterThreads;
+  int err;
   std::memset(&g->last, 0, sizeof(g->last));
-  g->last.ctas = (int)grid;
-  g->last.threads = threads;
+  if (cluster) {
+    uint64_t clusters = std::min<uint64_t>(rows, (uint64_t)g->dev.sm_count * 8 / C);
+    if (cta_cap > 0) clusters = std::min<uint64_t>(clusters, (uint64_t)(cta_cap / C));
+    err = launch_rmsnorm_cluster(datatype, a, (int)clusters, C, stream);
+    g->last.ctas = (int)(clusters * C);
+    g->last.threads = kRmsClusterThreads;
+  } else {
+    const int vectors = nvec > (size_t)4 * kRmsMaxThreads ? 8 : 4;
+    int threads = (int)std::min<size_t>(kRmsMaxThreads, ((nvec + vectors - 1) / vectors + 31) / 32 * 32);
+    threads = std::max(threads, 32);
+    uint64_t grid = std::min<uint64_t>(rows, (uint64_t)g->dev.sm_count * 8);
+    if (cta_cap > 0) grid = std::min<uint64_t>(grid, (uint64_t)cta_cap);
+    err = launch_rmsnorm(datatype, a, (int)grid, threads, vectors, stream);
+    g->last.ctas = (int)grid;
+    g->last.threads = threads;
+  }
   if (cur != g->device) cudaSetDevice(cur);
   return err == 0 ? tcclSuccess : tcclCudaError;
 }

@@ -2,6 +2,8 @@
 // reduced row, before the row is stored to every rank (the Device API example
 // the "NCCL Roadmap" post describes: receive, sum, normalise, send out in one
 // kernel). The reduced row never leaves the chip unnormalised.
+#include <cooperative_groups.h>
+
 #include "kernels_common.cuh"
 #include "rmsnorm.h"
 
@@ -91,7 +93,118 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rmsnorm_kernel(const __grid_co
   }
 }
 
+// Few rows (decode-sized calls): a cluster of kRmsCluster CTAs shares each
+// row. CTA q of the cluster reduces and normalises a contiguous slice; the
+// slices' sums of squares meet through distributed shared memory, added in
+// cluster-rank order, so every CTA derives the same scale.
+template <int DT>
+__global__ void __launch_bounds__(kRmsClusterThreads)
+    rmsnorm_cluster_kernel(const __grid_constant__ RmsArgs a) {
+  namespace cg = cooperative_groups;
+  using dev::Fold;
+  constexpr int V = 4;
+  constexpr int RB = 4;
+  constexpr int kVecElems = DT == kBF16 ? 8 : 4;
+  __shared__ float partial[kRmsClusterThreads / 32];
+  __shared__ float slice_ss;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int q = static_cast<int>(cluster.block_rank());
+  const int C = static_cast<int>(cluster.num_blocks());
+  if (threadIdx.x == 0) dev::record_sm(a.sm_mask);
+  const int P = a.nranks;
+  const uint32_t nvec = a.hidden / kVecElems;
+  const uint32_t per = (nvec + C - 1) / C;
+  const uint32_t v0 = q * per;
+  const uint32_t v1 = min(nvec, v0 + per);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const uint64_t cid = blockIdx.x / C;
+  const uint64_t nclusters = gridDim.x / C;
+  for (uint64_t t = cid; t < a.rows; t += nclusters) {
+    const uint64_t row_off = t * static_cast<uint64_t>(a.hidden) * (DT == kBF16 ? 2 : 4);
+    Fold<DT, kSum> acc[V];
+    for (int r0 = 0; r0 < P; r0 += RB) {
+      uint4 x[V][RB];
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const uint32_t v = v0 + threadIdx.x + j * blockDim.x;
+#pragma unroll
+        for (int k = 0; k < RB; ++k)
+          if (v < v1 && r0 + k < P)
+            x[j][k] = dev::ld_global_v4(static_cast<const char*>(a.p.src[r0 + k]) + row_off + v * 16ull);
+      }
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const uint32_t v = v0 + threadIdx.x + j * blockDim.x;
+        if (v < v1) {
+#pragma unroll
+          for (int k = 0; k < RB; ++k) {
+            if (r0 + k >= P) break;
+            if (r0 + k == 0) acc[j].init(x[j][k]);
+            else acc[j].add(x[j][k]);
+          }
+        }
+      }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const uint32_t v = v0 + threadIdx.x + j * blockDim.x;
+      if (v < v1)
+#pragma unroll
+        for (int e = 0; e < kVecElems; ++e) ss = __fadd_rn(ss, __fmul_rn(acc[j].a[e], acc[j].a[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, o));
+    if (lane == 0) partial[warp] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float w = 0.f;
+      for (int i = 0; i < nwarps; ++i) w = __fadd_rn(w, partial[i]);
+      slice_ss = w;
+    }
+    cluster.sync();  // every slice's sum of squares is in its CTA's shared memory
+    float total = 0.f;
+    for (int i = 0; i < C; ++i) total = __fadd_rn(total, *cluster.map_shared_rank(&slice_ss, i));
+    const float scale = rsqrtf(__fadd_rn(__fdiv_rn(total, static_cast<float>(a.hidden)), a.eps));
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const uint32_t v = v0 + threadIdx.x + j * blockDim.x;
+      if (v < v1) {
+        Fold<DT, kSum> g;
+        g.init(dev::ld_global_v4(static_cast<const char*>(a.gamma) + v * 16ull));
+#pragma unroll
+        for (int e = 0; e < kVecElems; ++e)
+          acc[j].a[e] = __fmul_rn(__fmul_rn(acc[j].a[e], scale), g.a[e]);
+        const uint4 y = acc[j].out();
+        const uint64_t o = row_off + v * 16ull;
+        for (int d = 0; d < P; ++d) dev::st_global_v4(static_cast<char*>(a.p.dst[d]) + o, y);
+      }
+    }
+    cluster.sync();  // no CTA reuses slice_ss / partial[] before all have read them
+  }
+}
+
 }  // namespace
+
+int launch_rmsnorm_cluster(int dtype, const RmsArgs& a, int clusters, int cluster_size,
+                           void* stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * cluster_size));
+  cfg.blockDim = dim3(kRmsClusterThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_size);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = dtype == kBF16 ? cudaLaunchKernelEx(&cfg, rmsnorm_cluster_kernel<kBF16>, a)
+                                 : cudaLaunchKernelEx(&cfg, rmsnorm_cluster_kernel<kF32>, a);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  return static_cast<int>(cudaGetLastError());
+}
 
 int launch_rmsnorm(int dtype, const RmsArgs& a, int grid, int threads, int vectors, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);

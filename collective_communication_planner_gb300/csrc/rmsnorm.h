@@ -6,6 +6,8 @@
 namespace tccl {
 
 constexpr int kRmsMaxThreads = 256;
+constexpr int kRmsClusterThreads = 256;  // cluster path: threads per CTA (4 vectors each)
+constexpr int kRmsCluster = 8;           // cluster path: CTAs sharing a row
 constexpr int kRmsMaxVectors = 8;  // 16-byte vectors of a row per thread
 
 struct RmsArgs {
@@ -21,5 +23,8 @@ struct RmsArgs {
 // `vectors`: 16-byte vectors of a row per thread (4 or 8); gamma is staged in
 // hidden * element-size bytes of dynamic shared memory.
 int launch_rmsnorm(int dtype, const RmsArgs& a, int grid, int threads, int vectors, void* stream);
+// Few rows: `clusters` clusters of `cluster_size` CTAs, each cluster one row at a time.
+int launch_rmsnorm_cluster(int dtype, const RmsArgs& a, int clusters, int cluster_size,
+                           void* stream);
 
 }  // namespace tccl

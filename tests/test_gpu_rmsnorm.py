@@ -77,6 +77,34 @@ def test_in_place_caps_and_eps(groups):
     run(groups(4), "f32", 4, 64, 2048, eps=0.5)
 
 
+@pytest.mark.parametrize("dtype,hidden", [("bf16", 8192), ("bf16", 1000), ("bf16", 16384),
+                                          ("f32", 4), ("f32", 8192)])
+@pytest.mark.parametrize("rows", [1, 3, 19, 76])
+def test_cluster_split_matches_single_cta_rows(monkeypatch, dtype, hidden, rows):
+    """Few rows take the cluster path (a row split over C CTAs whose partial
+    sums of squares meet in distributed shared memory); the same call with the
+    cluster path switched off takes one CTA per row. Both meet the oracle's
+    tolerance, and the rank sums they normalise are the same."""
+    p = 4
+    g = tccl.Group(p)
+    try:
+        run(g, dtype, p, rows, hidden, seed=rows)
+        info = g.last_launch()
+        c = info["ctas"] // min(rows, info["ctas"])
+        assert info["threads"] == 256 and c in (2, 4, 8) and info["ctas"] == rows * c, info
+        run(g, dtype, p, rows, hidden, seed=rows, cap=5)
+        assert g.last_launch()["ctas"] == 4, g.last_launch()
+    finally:
+        g.close()
+    monkeypatch.setenv("TCCL_RMSNORM_CLUSTER", "0")
+    g = tccl.Group(p)
+    try:
+        run(g, dtype, p, rows, hidden, seed=rows)
+        assert g.last_launch()["ctas"] == rows
+    finally:
+        g.close()
+
+
 def test_rejects_unsupported_calls(groups):
     g = groups(2)
     st = torch.cuda.current_stream().cuda_stream
