@@ -546,6 +546,20 @@ def sweep(args):
     def emit(**kw):
         print(json.dumps(kw), flush=True)
 
+    def set_cfg(g, **kw):
+        c = tccl.tcclConfig_t()
+        for k, v in kw.items():
+            setattr(c, k, v)
+        assert tccl.tcclGroupSetConfig(g.handle, c) == 0
+
+    def copy_out_moved(row, p, nbytes):
+        """Copy-out allreduce rows: HBM bytes actually moved (the kernel reads
+        P x S and writes S; the copies read and write (P-1) x S) beside the
+        collective's own 2 x P x S."""
+        if row["engine"] == tccl.tcclEngineCopyOut:
+            moved = (p + 1) * nbytes + 2 * (p - 1) * nbytes
+            row["moved_hbm_fraction"] = round(moved / (row["us"] * 1e-6) / 1e9 / peak, 4)
+
     def to_dev(x):
         return host_to_torch(x).to(dev)
 
@@ -616,6 +630,9 @@ def sweep(args):
         emit(**row)
         emit(**run_point("C2", g, "RS", p, rc, "bf16", "sum", sends, parts))
         emit(**run_point("C2", g, "AG", p, rc, "bf16", "sum", parts, recvs))
+        set_cfg(g, engine=tccl.tcclEngineCopyOut)  # the all-gather as copies only
+        emit(**run_point("C2", g, "AG", p, rc, "bf16", "sum", parts, recvs, sms=True))
+        set_cfg(g)
         g.close()
         del sends, recvs, parts
     # C3
@@ -650,7 +667,15 @@ def sweep(args):
                 row["cpu_1core_s"] = cpu_time(lambda: oracle.allreduce(xs, "bf16", "sum", nthreads=1), 1.0)
                 row["cpu_all_s"] = cpu_time(lambda: oracle.allreduce(xs, "bf16", "sum", nthreads=0))
                 row["cpu_cores"] = ncores
+            copy_out_moved(row, p, n * 2)
             emit(**row)
+            if cap:
+                # the same cap on the SM-only path (Auto told never to pick copy-out)
+                set_cfg(g, ce_auto_max_cap=-1)
+                row = run_point("C4", g, "AR", p, n, "bf16", "sum", sends, recvs, cap=cap, sms=True)
+                row["variant"] = "sm_only"
+                emit(**row)
+                set_cfg(g)
         g.close()
         del sends, recvs
         torch.cuda.empty_cache()

@@ -23,6 +23,7 @@ tcclCudaError, tcclDeviceTimeout, tcclInternalError = 3, 4, 5
 tcclFloat32, tcclBfloat16, tcclInt32 = 0, 1, 2
 tcclSum, tcclMin, tcclMax = 0, 1, 2
 tcclEngineAuto, tcclEngineBulk, tcclEngineWarp, tcclEngineVec, tcclEngineTmaReduce = 0, 1, 2, 3, 4
+tcclEngineCopyOut = 5
 tcclStoreAuto, tcclStoreBulk, tcclStoreVec = 0, 1, 2
 tcclOrderAuto, tcclOrderBlocked, tcclOrderCyclic, tcclOrderDynamic = 0, 1, 2, 3
 tcclLayoutAuto, tcclLayoutShared, tcclLayoutPerRank = 0, 1, 2
@@ -42,7 +43,8 @@ class tcclConfig_t(ctypes.Structure):
                 ("ctas_per_sm", ctypes.c_int), ("wait_timeout_ms", ctypes.c_double),
                 ("chunk_order", ctypes.c_int), ("prefetch_chunks", ctypes.c_int),
                 ("load_policy", ctypes.c_int), ("max_chunk_bytes", ctypes.c_size_t),
-                ("stage_layout", ctypes.c_int)]
+                ("stage_layout", ctypes.c_int), ("ce_streams", ctypes.c_int),
+                ("ce_segment_bytes", ctypes.c_size_t), ("ce_auto_max_cap", ctypes.c_int)]
 
 
 class tcclLaunchInfo_t(ctypes.Structure):
@@ -51,7 +53,8 @@ class tcclLaunchInfo_t(ctypes.Structure):
                 ("chunk_bytes", ctypes.c_int), ("windows", ctypes.c_int),
                 ("tasks", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
                 ("chunk_order", ctypes.c_int), ("total_chunks", ctypes.c_uint64),
-                ("stage_layout", ctypes.c_int)]
+                ("stage_layout", ctypes.c_int), ("ce_segments", ctypes.c_int),
+                ("ce_copies", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

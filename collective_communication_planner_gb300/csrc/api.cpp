@@ -90,7 +90,9 @@ struct PlanKey {
   uint64_t count;
   int cap;
   std::string mod16;  // address mod 16 of every send then recv buffer
+  int anchor = -1;    // >= 0: every window stores to this rank only (copy-out shard-in)
   bool operator<(const PlanKey& o) const {
+    if (anchor != o.anchor) return anchor < o.anchor;
     if (coll != o.coll) return coll < o.coll;
     if (elem_size != o.elem_size) return elem_size < o.elem_size;
     if (count != o.count) return count < o.count;
@@ -160,7 +162,11 @@ Config config_from_env() {
     if (v == "bulk") c.engine = kEngineBulk;
     else if (v == "warp") c.engine = kEngineWarp;
     else if (v == "vec") c.engine = kEngineVec;
+    else if (v == "copy_out") c.engine = kEngineCopyOut;
   }
+  c.ce_streams = geti("TCCL_CE_STREAMS", 0);
+  if (const char* e = std::getenv("TCCL_CE_SEGMENT_BYTES")) c.ce_segment_bytes = std::strtoull(e, 0, 10);
+  c.ce_auto_max_cap = geti("TCCL_CE_AUTO_MAX_CAP", 0);
   if (const char* e = std::getenv("TCCL_SMALL_MAX_BYTES")) c.small_max_bytes = std::strtoull(e, 0, 10);
   if (const char* e = std::getenv("TCCL_VEC_MAX_BYTES")) c.vec_max_bytes = std::strtoull(e, 0, 10);
   c.stage_bytes = geti("TCCL_STAGE_BYTES", 0);
@@ -206,6 +212,9 @@ Config from_public(const tcclConfig_t& p) {
   c.prefetch_chunks = p.prefetch_chunks;
   c.load_policy = p.load_policy;
   c.max_chunk_bytes = p.max_chunk_bytes;
+  c.ce_streams = p.ce_streams;
+  c.ce_segment_bytes = p.ce_segment_bytes;
+  c.ce_auto_max_cap = p.ce_auto_max_cap;
   return resolve_config(c);
 }
 
@@ -226,11 +235,15 @@ tcclConfig_t to_public(const Config& c) {
   p.prefetch_chunks = c.prefetch_chunks;
   p.load_policy = c.load_policy;
   p.max_chunk_bytes = c.max_chunk_bytes;
+  p.ce_streams = c.ce_streams;
+  p.ce_segment_bytes = c.ce_segment_bytes;
+  p.ce_auto_max_cap = c.ce_auto_max_cap;
   return p;
 }
 
 bool config_ok(const tcclConfig_t& p) {
-  return p.engine >= 0 && p.engine <= 4 && p.store_mode >= 0 && p.store_mode <= 2 &&
+  return p.engine >= 0 && p.engine <= 5 && p.ce_streams >= 0 && p.ce_streams <= 8 &&
+         p.store_mode >= 0 && p.store_mode <= 2 &&
          p.stage_bytes >= 0 && p.stages >= 0 && p.consumer_warps >= 0 && p.ctas_per_sm >= 0 &&
          p.wait_timeout_ms >= 0 && p.chunk_order >= 0 && p.chunk_order <= 3 &&
          p.prefetch_chunks >= -1 && p.load_policy >= 0 && p.load_policy <= 2 &&
@@ -297,13 +310,19 @@ struct tcclGroup {
   std::map<PlanKey, std::unique_ptr<CachedPlan>> plans;
   std::map<std::string, std::unique_ptr<CachedReshard>> reshards;
   tcclLaunchInfo_t last;
+  // copy-out engine: the group's own copy streams and the events that order
+  // them after each segment's kernel and join them back to the caller
+  std::vector<cudaStream_t> ce_streams;
+  std::vector<cudaEvent_t> ce_seg_events;
+  std::vector<cudaEvent_t> ce_done_events;
+  cudaEvent_t ce_fork_event = nullptr;
 };
 
 namespace {
 
 tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* const* recv,
-                      size_t count, int es, int cap, CachedPlan** out) {
-  PlanKey key{coll, es, (uint64_t)count, cap > 0 ? cap : 0, std::string()};
+                      size_t count, int es, int cap, CachedPlan** out, int anchor = -1) {
+  PlanKey key{coll, es, (uint64_t)count, cap > 0 ? cap : 0, std::string(), anchor};
   key.mod16.resize(2 * g->nranks);
   for (int r = 0; r < g->nranks; ++r) {
     key.mod16[r] = (char)((uintptr_t)send[r] & 15);
@@ -322,10 +341,16 @@ tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* con
     sm[r] = (uint8_t)key.mod16[r];
     rm[r] = (uint8_t)key.mod16[g->nranks + r];
   }
-  if (!lower_plan(pl, sm.data(), rm.data(), g->cfg, g->dev, cap, &cp->low, &why)) {
+  Config cfg = g->cfg;
+  if (anchor >= 0) cfg.engine = kEngineBulk;
+  if (!lower_plan(pl, sm.data(), rm.data(), cfg, g->dev, cap, &cp->low, &why)) {
     if (log_level()) std::fprintf(stderr, "[tccl] cannot lower: %s\n", why.c_str());
     return tcclInvalidUsage;
   }
+  // copy-out shard-in: the reduced chunks go to the anchor rank alone; the
+  // copy engines carry them to the other ranks
+  if (anchor >= 0)
+    for (Window& w : cp->low.win) w.dst_sel = (int16_t)anchor;
   if (log_level()) dump_plan(pl, cp->low);
   const Lowered& low = cp->low;
   if (low.shape.engine == kEngineBulk || low.shape.engine == kEngineTmaReduce) {
@@ -351,6 +376,211 @@ tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* con
   return tcclSuccess;
 }
 
+// Launches one lowered plan on `stream` with these buffers; returns a CUDA
+// error code (0 on success).
+int launch_plan(tcclGroup* g, CachedPlan* cp, int coll, int dtype, int op,
+                const void* const* send, void* const* recv, int es, cudaStream_t stream) {
+  const Lowered& low = cp->low;
+  uint32_t* mask = g->record_sms ? g->d_sm_mask : nullptr;
+  if (low.shape.engine == kEngineBulk || low.shape.engine == kEngineTmaReduce) {
+    BulkArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int k = 0; k < g->nranks; ++k) {
+      a.p.src[k] = send[k];
+      a.p.dst[k] = recv[k];
+    }
+    a.win = cp->d_win;
+    a.chunk_prefix = cp->d_prefix;
+    a.cta_first = cp->d_cta_first;
+    a.total_chunks = low.total_chunks;
+    a.chunks_per_cta = low.chunks_per_cta;
+    a.nbody = low.nbody;
+    a.sched = cp->d_sched;
+    a.order = low.shape.order;
+    a.prefetch_chunks = low.shape.prefetch_chunks;
+    a.rank_streamed = low.shape.rank_streamed;
+    a.load_evict_first = low.shape.load_evict_first;
+    a.status = g->d_status;
+    a.sm_mask = mask;
+    a.timeout_ns = (uint64_t)(g->cfg.wait_timeout_ms * 1e6);
+    a.inject_timeout_ns = g->inject_ns;
+    a.nranks = g->nranks;
+    a.chunk_bytes = low.shape.chunk_bytes;
+    a.stages = low.shape.stages;
+    a.store_mode = low.shape.store_mode;
+    a.consumer_warps = low.shape.consumer_warps;
+    a.release_lag = low.shape.release_lag;
+    a.elem_size = es;
+    return low.shape.engine == kEngineBulk ? launch_bulk(coll, dtype, op, a, low.shape, stream)
+                                           : launch_reduce(coll, dtype, op, a, low.shape, stream);
+  }
+  std::vector<unsigned char>& buf = cp->small_args;  // pointers patched in place
+  if (low.size_class == 0)
+    fill_small_ptrs<kSmallRanks, kSmallWindows>(&buf, g->nranks, send, recv, mask);
+  else
+    fill_small_ptrs<kMaxRanks, kLargeWindows>(&buf, g->nranks, send, recv, mask);
+  if (coll == kAllReduce)
+    return launch_small_ar(dtype, op, low.shape.engine, low.size_class, buf.data(), low.shape, stream);
+  if (coll == kReduceScatter)
+    return launch_small_rs(dtype, op, low.shape.engine, low.size_class, buf.data(), low.shape, stream);
+  return launch_small_ag(dtype, op, low.shape.engine, low.size_class, buf.data(), low.shape, stream);
+}
+
+constexpr int kMaxCeSegments = 64;
+constexpr size_t kCeAutoMinBytes = (size_t)4 << 20;
+
+// Auto's choice of the copy-out engine: a capped allreduce or all-gather
+// whose per-rank buffer is large, with a cap small enough that the SMs, not
+// HBM, would bound the SM-only path.
+bool use_copy_out(const tcclGroup* g, int coll, size_t count, int es, int cap) {
+  if (coll == kReduceScatter || g->nranks < 2) return false;
+  if (g->cfg.engine == kEngineCopyOut) return true;
+  if (g->cfg.engine != kEngineAuto || cap <= 0 || g->cfg.ce_auto_max_cap < 0) return false;
+  const int max_cap = g->cfg.ce_auto_max_cap > 0 ? g->cfg.ce_auto_max_cap : g->dev.sm_count / 4;
+  const size_t per_rank = count * (size_t)es * (coll == kAllGather ? (size_t)g->nranks : 1);
+  return cap <= max_cap && per_rank >= kCeAutoMinBytes;
+}
+
+tcclResult_t ensure_ce_resources(tcclGroup* g, int segments) {
+  const int ns = g->cfg.ce_streams;
+  while ((int)g->ce_streams.size() < ns) {
+    cudaStream_t st;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return tcclCudaError;
+    g->ce_streams.push_back(st);
+  }
+  while ((int)g->ce_done_events.size() < ns) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return tcclCudaError;
+    g->ce_done_events.push_back(e);
+  }
+  while ((int)g->ce_seg_events.size() < segments) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return tcclCudaError;
+    g->ce_seg_events.push_back(e);
+  }
+  if (!g->ce_fork_event &&
+      cudaEventCreateWithFlags(&g->ce_fork_event, cudaEventDisableTiming) != cudaSuccess)
+    return tcclCudaError;
+  return tcclSuccess;
+}
+
+// Makes `stream` wait for everything queued on the first `used` copy streams.
+int join_ce_streams(tcclGroup* g, int used, cudaStream_t stream) {
+  int err = 0;
+  for (int j = 0; j < used; ++j) {
+    int e = cudaEventRecord(g->ce_done_events[j], g->ce_streams[j]);
+    if (!e) e = cudaStreamWaitEvent(stream, g->ce_done_events[j], 0);
+    if (e && !err) err = e;
+  }
+  return err;
+}
+
+// Allreduce on the copy-out engine. The message is cut into segments of
+// ce_segment_bytes per rank (offsets multiples of 256 bytes, so every full
+// segment shares one cached plan). Each segment's bulk-engine kernel folds
+// the P ranks in ascending order and stores the result to the anchor rank
+// (rank 0) alone; an event after it releases the device-to-device copies of
+// that segment from the anchor to ranks 1..P-1 on the group's copy streams,
+// so the copy engines fan segment s out while the SMs reduce segment s+1.
+// In place is safe: segment s of a rank is overwritten only after the
+// kernel that read it has finished.
+tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void* const* recv,
+                                    size_t count, int dtype, int op, int es, cudaStream_t stream,
+                                    int cap) {
+  const int P = g->nranks;
+  const int anchor = 0;
+  const size_t align = 256 / (size_t)es;
+  size_t seg = std::max<size_t>(align, (g->cfg.ce_segment_bytes / (size_t)es) / align * align);
+  if ((count + seg - 1) / seg > (size_t)kMaxCeSegments)
+    seg = ((count + kMaxCeSegments - 1) / kMaxCeSegments + align - 1) / align * align;
+  const int nseg = (int)((count + seg - 1) / seg);
+  tcclResult_t r = ensure_ce_resources(g, nseg);
+  if (r != tcclSuccess) return r;
+  // both plans (full segments, ragged tail) before any launch: a new plan's
+  // table upload is synchronous
+  std::vector<const void*> s_ptr(P);
+  std::vector<void*> r_ptr(P);
+  auto at = [&](size_t off) {
+    for (int k = 0; k < P; ++k) {
+      s_ptr[k] = static_cast<const char*>(send[k]) + off * es;
+      r_ptr[k] = static_cast<char*>(recv[k]) + off * es;
+    }
+  };
+  CachedPlan* full = nullptr;
+  CachedPlan* tail = nullptr;
+  const size_t tail_n = count - (size_t)(nseg - 1) * seg;
+  at(0);
+  r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), nseg > 1 ? seg : tail_n, es, cap, &full, anchor);
+  if (r == tcclSuccess && nseg > 1 && tail_n != seg) {
+    at((size_t)(nseg - 1) * seg);
+    r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), tail_n, es, cap, &tail, anchor);
+  }
+  if (r != tcclSuccess) return r;
+  const int used = std::min(g->cfg.ce_streams, P - 1);
+  int err = 0, copies = 0;
+  for (int sgi = 0; sgi < nseg && !err; ++sgi) {
+    const size_t off = (size_t)sgi * seg;
+    const size_t n = sgi == nseg - 1 ? tail_n : seg;
+    at(off);
+    CachedPlan* cp = (sgi == nseg - 1 && tail) ? tail : full;
+    err = launch_plan(g, cp, kAllReduce, dtype, op, s_ptr.data(), r_ptr.data(), es, stream);
+    if (err || used == 0) continue;
+    err = cudaEventRecord(g->ce_seg_events[sgi], stream);
+    for (int j = 0; j < used && !err; ++j) err = cudaStreamWaitEvent(g->ce_streams[j], g->ce_seg_events[sgi], 0);
+    int j = 0;
+    for (int k = 0; k < P && !err; ++k) {
+      if (k == anchor) continue;
+      err = cudaMemcpyAsync(r_ptr[k], r_ptr[anchor], n * es, cudaMemcpyDeviceToDevice, g->ce_streams[j]);
+      j = (j + 1) % used;
+      ++copies;
+    }
+  }
+  const int jerr = used ? join_ce_streams(g, used, stream) : 0;
+  if (!err) err = jerr;
+  fill_info(full->low, &g->last);
+  g->last.engine = kEngineCopyOut;
+  g->last.ce_segments = nseg;
+  g->last.ce_copies = copies;
+  if (err) {
+    if (log_level()) std::fprintf(stderr, "[tccl] copy-out allreduce failed: %s\n", cudaGetErrorString((cudaError_t)err));
+    return tcclCudaError;
+  }
+  return tcclSuccess;
+}
+
+// All-gather on the copy-out engine: P x P (P x (P-1) in place) device-to-
+// device copies spread over the group's copy streams. No kernel, no SM.
+tcclResult_t run_copy_out_allgather(tcclGroup* g, const void* const* send, void* const* recv,
+                                    size_t count, int es, cudaStream_t stream) {
+  const int P = g->nranks;
+  tcclResult_t r = ensure_ce_resources(g, 0);
+  if (r != tcclSuccess) return r;
+  const int used = std::min(g->cfg.ce_streams, P * P);
+  const size_t bytes = count * (size_t)es;
+  int err = cudaEventRecord(g->ce_fork_event, stream);
+  for (int j = 0; j < used && !err; ++j) err = cudaStreamWaitEvent(g->ce_streams[j], g->ce_fork_event, 0);
+  int j = 0, copies = 0;
+  for (int q = 0; q < P && !err; ++q) {
+    for (int k = 0; k < P && !err; ++k) {
+      char* dst = static_cast<char*>(recv[k]) + (size_t)q * bytes;
+      if (dst == static_cast<const char*>(send[q])) continue;  // in place: already there
+      err = cudaMemcpyAsync(dst, send[q], bytes, cudaMemcpyDeviceToDevice, g->ce_streams[j]);
+      j = (j + 1) % used;
+      ++copies;
+    }
+  }
+  const int jerr = join_ce_streams(g, used, stream);
+  if (!err) err = jerr;
+  std::memset(&g->last, 0, sizeof(g->last));
+  g->last.engine = kEngineCopyOut;
+  g->last.ce_copies = copies;
+  if (err) {
+    if (log_level()) std::fprintf(stderr, "[tccl] copy-out all-gather failed: %s\n", cudaGetErrorString((cudaError_t)err));
+    return tcclCudaError;
+  }
+  return tcclSuccess;
+}
+
 tcclResult_t run_collective(tcclGroup* g, int coll, const void* const* send, void* const* recv,
                             size_t count, int dtype, int op, cudaStream_t stream, int cap) {
   if (!g) return tcclInvalidArgument;
@@ -365,6 +595,13 @@ tcclResult_t run_collective(tcclGroup* g, int coll, const void* const* send, voi
   if (cudaGetDevice(&cur) != cudaSuccess) return tcclCudaError;
   if (cur != g->device && cudaSetDevice(g->device) != cudaSuccess) return tcclCudaError;
   const int es = elem_size_of(dtype);
+  if (use_copy_out(g, coll, count, es, cap)) {
+    tcclResult_t rc = coll == kAllReduce
+                          ? run_copy_out_allreduce(g, send, recv, count, dtype, op, es, stream, cap)
+                          : run_copy_out_allgather(g, send, recv, count, es, stream);
+    if (cur != g->device) cudaSetDevice(cur);
+    return rc;
+  }
   CachedPlan* cp = nullptr;
   tcclResult_t r = get_plan(g, coll, send, recv, count, es, cap, &cp);
   if (r == tcclSuccess && cp->low.shape.engine == kEngineTmaReduce &&
@@ -376,53 +613,8 @@ tcclResult_t run_collective(tcclGroup* g, int coll, const void* const* send, voi
   }
   int err = 0;
   if (r == tcclSuccess) {
-    const Lowered& low = cp->low;
-    uint32_t* mask = g->record_sms ? g->d_sm_mask : nullptr;
-    if (low.shape.engine == kEngineBulk || low.shape.engine == kEngineTmaReduce) {
-      BulkArgs a;
-      std::memset(&a, 0, sizeof(a));
-      for (int k = 0; k < g->nranks; ++k) {
-        a.p.src[k] = send[k];
-        a.p.dst[k] = recv[k];
-      }
-      a.win = cp->d_win;
-      a.chunk_prefix = cp->d_prefix;
-      a.cta_first = cp->d_cta_first;
-      a.total_chunks = low.total_chunks;
-      a.chunks_per_cta = low.chunks_per_cta;
-      a.nbody = low.nbody;
-      a.sched = cp->d_sched;
-      a.order = low.shape.order;
-      a.prefetch_chunks = low.shape.prefetch_chunks;
-      a.rank_streamed = low.shape.rank_streamed;
-      a.load_evict_first = low.shape.load_evict_first;
-      a.status = g->d_status;
-      a.sm_mask = mask;
-      a.timeout_ns = (uint64_t)(g->cfg.wait_timeout_ms * 1e6);
-      a.inject_timeout_ns = g->inject_ns;
-      a.nranks = g->nranks;
-      a.chunk_bytes = low.shape.chunk_bytes;
-      a.stages = low.shape.stages;
-      a.store_mode = low.shape.store_mode;
-      a.consumer_warps = low.shape.consumer_warps;
-      a.release_lag = low.shape.release_lag;
-      a.elem_size = es;
-      err = low.shape.engine == kEngineBulk ? launch_bulk(coll, dtype, op, a, low.shape, stream)
-                                            : launch_reduce(coll, dtype, op, a, low.shape, stream);
-    } else {
-      std::vector<unsigned char>& buf = cp->small_args;
-      if (low.size_class == 0)
-        fill_small_ptrs<kSmallRanks, kSmallWindows>(&buf, g->nranks, send, recv, mask);
-      else
-        fill_small_ptrs<kMaxRanks, kLargeWindows>(&buf, g->nranks, send, recv, mask);
-      if (coll == kAllReduce)
-        err = launch_small_ar(dtype, op, low.shape.engine, low.size_class, buf.data(), low.shape, stream);
-      else if (coll == kReduceScatter)
-        err = launch_small_rs(dtype, op, low.shape.engine, low.size_class, buf.data(), low.shape, stream);
-      else
-        err = launch_small_ag(dtype, op, low.shape.engine, low.size_class, buf.data(), low.shape, stream);
-    }
-    fill_info(low, &g->last);
+    err = launch_plan(g, cp, coll, dtype, op, send, recv, es, stream);
+    fill_info(cp->low, &g->last);
   }
   if (cur != g->device) cudaSetDevice(cur);
   if (r != tcclSuccess) return r;
@@ -526,6 +718,10 @@ tcclResult_t tcclGroupDestroy(tcclGroup_t g) {
   cudaDeviceSynchronize();
   g->plans.clear();
   g->reshards.clear();
+  for (cudaStream_t st : g->ce_streams) cudaStreamDestroy(st);
+  for (cudaEvent_t e : g->ce_seg_events) cudaEventDestroy(e);
+  for (cudaEvent_t e : g->ce_done_events) cudaEventDestroy(e);
+  if (g->ce_fork_event) cudaEventDestroy(g->ce_fork_event);
   cudaFree(g->d_status);
   cudaFree(g->d_sm_mask);
   delete g;

@@ -20,7 +20,8 @@ enum Engine : int {
   kEngineBulk = 1,
   kEngineWarp = 2,
   kEngineVec = 3,
-  kEngineTmaReduce = 4
+  kEngineTmaReduce = 4,
+  kEngineCopyOut = 5  // bulk-engine shard-in to one anchor rank + copy-engine shard-out
 };
 enum StoreMode : int { kStoreAuto = 0, kStoreBulk = 1, kStoreVec = 2 };
 enum ChunkOrder : int { kOrderAuto = 0, kOrderBlocked = 1, kOrderCyclic = 2, kOrderDynamic = 3 };

@@ -153,6 +153,10 @@ Config resolve_config(const Config& in) {
   if (c.load_policy < 0 || c.load_policy > 2) c.load_policy = 0;
   if (c.max_chunk_bytes == 0) c.max_chunk_bytes = 16384;
   c.max_chunk_bytes = std::min<size_t>(std::max<size_t>(c.max_chunk_bytes, 256), 65536) & ~(size_t)15;
+  if (c.ce_streams <= 0) c.ce_streams = 2;  // two streams fed the copy engines best (GB300 probe)
+  if (c.ce_streams > 8) c.ce_streams = 8;
+  if (c.ce_segment_bytes == 0) c.ce_segment_bytes = (size_t)8 << 20;
+  c.ce_segment_bytes = std::max<size_t>(c.ce_segment_bytes, 4096) & ~(size_t)255;
   return c;
 }
 
@@ -338,6 +342,9 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
     else if (mb <= cfg.vec_max_bytes && !capped) engine = kEngineVec;
     else engine = kEngineBulk;
   }
+  // the copy-out engine's kernels are bulk-engine kernels (its copies are
+  // issued by the host); a reduce-scatter has nothing to copy out
+  if (engine == kEngineCopyOut) engine = kEngineBulk;
   if (engine == kEngineWarp && p > 32) engine = kEngineVec;
   LaunchShape& sh = out->shape;
   sh.engine = engine;

@@ -77,6 +77,9 @@ struct Config {
   int prefetch_chunks = -1;   // -1: library default
   int load_policy = 0;        // 0 default (evict-normal), 1 evict-first, 2 evict-normal
   size_t max_chunk_bytes = 0;
+  int ce_streams = 0;
+  size_t ce_segment_bytes = 0;
+  int ce_auto_max_cap = 0;
 };
 
 // Fills zero fields with the library defaults.

@@ -69,10 +69,19 @@ typedef enum {
   tcclEngineBulk = 1, /* TMA cp.async.bulk pipeline: mbarrier stages, reduce, bulk stores */
   tcclEngineWarp = 2, /* small-message path: one lane per (vector, rank), shuffle fold */
   tcclEngineVec = 3,  /* plain 128-bit loads/stores, each lane folds all ranks */
-  tcclEngineTmaReduce = 4 /* the copy hardware reduces: rank 0 bulk-stored, ranks 1..P-1
-                             bulk-reduced in order, result loaded once and bulk-stored to all;
-                             fp32 sum, int32 sum/min/max, bf16 min/max only (other pairs:
-                             tcclInvalidUsage); never chosen by Auto */
+  tcclEngineTmaReduce = 4, /* the copy hardware reduces: rank 0 bulk-stored, ranks 1..P-1
+                              bulk-reduced in order, result loaded once and bulk-stored to all;
+                              fp32 sum, int32 sum/min/max, bf16 min/max only (other pairs:
+                              tcclInvalidUsage); never chosen by Auto */
+  tcclEngineCopyOut = 5    /* shard-in on SMs, shard-out on the GPU's copy engines. Allreduce:
+                              the message is cut into segments; each segment is reduced by the
+                              bulk engine (within the CTA cap) into one anchor rank's receive
+                              buffer only, then device-to-device copies on the group's own
+                              streams carry it to the other P-1 ranks. All-gather: copies only,
+                              no kernel, no SM. Reduce-scatter has no shard-out and runs on the
+                              bulk engine. Auto picks it for capped allreduce / all-gather calls
+                              of at least 4 MiB per rank when the cap is at most
+                              ce_auto_max_cap CTAs. */
 } tcclEngine_t;
 
 typedef enum {
@@ -102,7 +111,8 @@ typedef enum {
  * reads TCCL_ENGINE, TCCL_SMALL_MAX_BYTES, TCCL_VEC_MAX_BYTES, TCCL_STAGE_BYTES, TCCL_STAGES,
  * TCCL_STORE_MODE, TCCL_CONSUMER_WARPS, TCCL_CTAS_PER_SM,
  * TCCL_WAIT_TIMEOUT_MS, TCCL_CHUNK_ORDER, TCCL_PREFETCH_CHUNKS,
- * TCCL_LOAD_POLICY, TCCL_MAX_CHUNK_BYTES and TCCL_STAGE_LAYOUT once). Zero in a field means "library default".
+ * TCCL_LOAD_POLICY, TCCL_MAX_CHUNK_BYTES, TCCL_STAGE_LAYOUT, TCCL_CE_STREAMS,
+ * TCCL_CE_SEGMENT_BYTES and TCCL_CE_AUTO_MAX_CAP once). Zero in a field means "library default".
  */
 typedef struct {
   int engine;              /* tcclEngine_t */
@@ -120,6 +130,11 @@ typedef struct {
   int load_policy;         /* bulk engine: L2 policy of bulk loads: 0 default, 1 evict-first, 2 evict-normal */
   size_t max_chunk_bytes;  /* bulk engine: upper bound on bytes per source per chunk */
   int stage_layout;        /* bulk engine: tcclStageLayout_t */
+  int ce_streams;          /* copy-out engine: internal copy streams, 1..8 (default 2) */
+  size_t ce_segment_bytes; /* copy-out engine: bytes per rank in one segment (default 8 MiB;
+                              rounded down to a multiple of 256) */
+  int ce_auto_max_cap;     /* Auto picks the copy-out engine for caps up to this many CTAs
+                              (0: a quarter of the SMs; negative: never) */
 } tcclConfig_t;
 
 /* What the last launch on a group looked like. */
@@ -136,6 +151,8 @@ typedef struct {
   int chunk_order;     /* bulk engine: tcclChunkOrder_t used (0 otherwise) */
   uint64_t total_chunks; /* bulk engine: chunks per source in the call */
   int stage_layout;    /* bulk engine: tcclStageLayout_t used (0 otherwise) */
+  int ce_segments;     /* copy-out engine: kernel launches (segments) of the call (0 otherwise) */
+  int ce_copies;       /* copy-out engine: device-to-device copies enqueued (0 otherwise) */
 } tcclLaunchInfo_t;
 
 const char* tcclGetErrorString(tcclResult_t r);
@@ -169,6 +186,13 @@ tcclResult_t tcclGroupSetConfig(tcclGroup_t g, const tcclConfig_t* cfg);
  * tcclInvalidArgument; send buffers may overlap each other.
  * `cta_cap` > 0 bounds the number of CTAs (and so SMs) the call occupies;
  * <= 0 means uncapped. count == 0 returns tcclSuccess without a launch.
+ * With the copy-out engine (tcclEngineCopyOut; Auto picks it for large capped
+ * calls) the call also uses the group's internal copy streams. They join
+ * `stream` through events before the call returns, so work queued on
+ * `stream` afterwards sees every rank's result; the call stays capturable
+ * into a CUDA graph on `stream`. Calls on different user streams that share
+ * a group share those copy streams too (their order between such calls is
+ * the order of the calls).
  */
 tcclResult_t tcclAllReduce(tcclGroup_t g, const void* const sendbufs[], void* const recvbufs[],
                            size_t count, tcclDataType_t datatype, tcclRedOp_t op,

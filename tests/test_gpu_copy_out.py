@@ -1,0 +1,275 @@
+"""GPU parity for the copy-out engine (shard-in on SMs, shard-out on the
+copy engines) against the CPU oracle, bit for bit, through the C ABI.
+
+The allreduce is cut into segments; each segment's kernel stores the folded
+result to rank 0 only and device-to-device copies carry it to ranks 1..P-1.
+Small segment sizes make many segments (and a ragged last one) out of
+test-sized buffers. The all-gather is copies only. Cases cover every dtype
+and op, P = 2, 3 and 8, in-place and misaligned buffers, CTA caps and the SM
+footprint, Auto's choice, stream order on either side of the call, CUDA graph
+replay and the bounded-wait timeout path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import collective_communication_planner_gb300 as tccl
+import datagen
+import oracle
+from gpu_util import DT_CODE, Guarded, first_mismatch, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+KIND = {"f32": "uniform_f32", "bf16": "normal_bf16", "i32": "int32"}
+CE = tccl.tcclEngineCopyOut
+
+
+@pytest.fixture(scope="module")
+def groups():
+    made = {}
+
+    def get(p):
+        if p not in made:
+            made[p] = tccl.Group(p)
+        return made[p]
+
+    yield get
+    for g in made.values():
+        g.close()
+
+
+def reset_config(g, **kw):
+    c = tccl.tcclConfig_t()
+    for k, v in kw.items():
+        setattr(c, k, v)
+    assert tccl.tcclGroupSetConfig(g.handle, c) == tccl.tcclSuccess
+
+
+def check(got, exp, what):
+    for r in range(len(exp)):
+        mm = first_mismatch(got[r], exp[r])
+        assert mm is None, f"{what}: rank {r} first mismatch at {mm[0]} ({mm[1]} elements)"
+
+
+def allreduce(g, xs, dtype, op, cap=0, send_off=0, recv_off=0, in_place=False):
+    p, n = len(xs), xs[0].size
+    sends = [Guarded(n, dtype, send_off) for _ in range(p)]
+    for s, x in zip(sends, xs):
+        s.tensor.copy_(to_device(x))
+    recvs = sends if in_place else [Guarded(n, dtype, recv_off) for _ in range(p)]
+    r = tccl.tcclAllReduce(g.handle, [s.tensor for s in sends], [t.tensor for t in recvs], n,
+                           DT_CODE[dtype], tccl.OPS[op], torch.cuda.current_stream().cuda_stream, cap)
+    assert r == tccl.tcclSuccess, tccl.tcclGetErrorString(r)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    assert all(t.guards_intact() for t in recvs)
+    return [t.host() for t in recvs]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("op", ["sum", "min", "max"])
+@pytest.mark.parametrize("p", [2, 3, 8])
+def test_allreduce_segments_dtypes_ops(groups, dtype, op, p):
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=64 * 1024)
+    n = 300_007
+    xs = datagen.rank_buffers(KIND[dtype], 21, p, n)
+    got = allreduce(g, xs, dtype, op, cap=7)
+    info = g.last_launch()
+    es = 2 if dtype == "bf16" else 4
+    seg = 64 * 1024 // es
+    assert info["engine"] == CE and info["ctas"] <= 7
+    assert info["ce_segments"] == -(-n // seg) and info["ce_copies"] == info["ce_segments"] * (p - 1)
+    check(got, oracle.allreduce(xs, dtype, op, nthreads=0), f"copy-out {dtype} {op} P={p}")
+
+
+@pytest.mark.parametrize("offs", [(0, 0), (4, 4), (4, 8), (2, 6), (12, 0)])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_allreduce_misaligned_and_in_place(groups, offs, in_place):
+    p = 4
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=32 * 1024)
+    dtype = "bf16" if offs[0] % 4 else "f32"
+    xs = datagen.rank_buffers(KIND[dtype], 22, p, 123_457)
+    got = allreduce(g, xs, dtype, "sum", cap=16, send_off=offs[0], recv_off=offs[1], in_place=in_place)
+    check(got, oracle.allreduce(xs, dtype, "sum", nthreads=0), f"offs {offs} in_place {in_place}")
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 64, 4097, 65_536, 65_537])
+def test_allreduce_small_counts_and_exact_segments(groups, n):
+    p = 3
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=4096)
+    xs = datagen.rank_buffers("int32", 23, p, n)
+    got = allreduce(g, xs, "i32", "sum", cap=4)
+    assert g.last_launch()["ce_segments"] == min(64, -(-n // 1024)) or n > 64 * 1024
+    check(got, oracle.allreduce(xs, "i32", "sum", nthreads=0), f"n={n}")
+
+
+def test_segment_count_is_bounded(groups):
+    p = 2
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=4096)
+    xs = datagen.rank_buffers("uniform_f32", 24, p, 3_000_001)
+    got = allreduce(g, xs, "f32", "sum")
+    assert 1 <= g.last_launch()["ce_segments"] <= 64
+    check(got, oracle.allreduce(xs, "f32", "sum", nthreads=0), "64-segment bound")
+
+
+@pytest.mark.parametrize("cap", [1, 5, 16])
+def test_sm_footprint_stays_within_the_cap(groups, cap):
+    p = 8
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=1 << 20)
+    xs = datagen.rank_buffers("normal_bf16", 25, p, 2_000_001)
+    g.read_sm_record()
+    g.record_sms(True)
+    got = allreduce(g, xs, "bf16", "sum", cap=cap)
+    sms = g.read_sm_record()
+    g.record_sms(False)
+    assert g.last_launch()["ctas"] == cap and 1 <= sms <= cap
+    check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), f"cap {cap}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("p", [2, 4, 8])
+def test_allgather_copies_only(groups, dtype, p):
+    g = groups(p)
+    reset_config(g, engine=CE)
+    rc = 50_001
+    xs = datagen.rank_buffers(KIND[dtype], 26, p, rc)
+    exp = [np.concatenate(xs)] * p
+    sends = [to_device(x) for x in xs]
+    outs = [Guarded(p * rc, dtype) for _ in range(p)]
+    g.read_sm_record()
+    g.record_sms(True)
+    g.all_gather(sends, [t.tensor for t in outs])
+    torch.cuda.synchronize()
+    sms = g.read_sm_record()
+    g.record_sms(False)
+    info = g.last_launch()
+    assert info["engine"] == CE and info["ctas"] == 0 and info["ce_copies"] == p * p and sms == 0
+    assert all(t.guards_intact() for t in outs)
+    check([t.host() for t in outs], exp, f"AG {dtype} P={p}")
+    # in place: rank r's shard already sits in its own slot
+    bufs = [to_device(np.zeros(p * rc, dtype=xs[0].dtype)) for _ in range(p)]
+    es = bufs[0].element_size()
+    for r in range(p):
+        bufs[r][r * rc:(r + 1) * rc].copy_(sends[r])
+    r = tccl.tcclAllGather(g.handle, [b[i * rc:(i + 1) * rc] for i, b in enumerate(bufs)], bufs, rc,
+                           DT_CODE[dtype], torch.cuda.current_stream().cuda_stream, 0)
+    assert r == tccl.tcclSuccess and es in (2, 4)
+    torch.cuda.synchronize()
+    assert g.last_launch()["ce_copies"] == p * (p - 1)
+    check([to_host(b) for b in bufs], exp, f"AG in place {dtype} P={p}")
+
+
+def test_reduce_scatter_runs_on_the_bulk_engine(groups):
+    p, rc = 4, 77_777
+    g = groups(p)
+    reset_config(g, engine=CE)
+    xs = datagen.rank_buffers("normal_bf16", 27, p, p * rc)
+    sends = [to_device(x) for x in xs]
+    parts = [torch.empty(rc, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    g.reduce_scatter(sends, parts)
+    torch.cuda.synchronize()
+    assert g.last_launch()["engine"] == tccl.tcclEngineBulk
+    check([to_host(t) for t in parts], oracle.reduce_scatter(xs, "bf16", "sum", nthreads=0), "RS")
+
+
+def test_one_rank_falls_back_to_the_bulk_engine(groups):
+    g = groups(1)
+    reset_config(g, engine=CE)
+    xs = datagen.rank_buffers("uniform_f32", 28, 1, 10_000)
+    check(allreduce(g, xs, "f32", "sum"), xs, "P=1")
+    assert g.last_launch()["engine"] == tccl.tcclEngineBulk
+
+
+def test_auto_picks_copy_out_for_large_capped_calls(groups):
+    p = 4
+    g = groups(p)
+    reset_config(g)
+    n = 4 * 1024 * 1024  # 8 MiB of bf16 per rank
+    sends = [torch.ones(n, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    recvs = [torch.empty_like(s) for s in sends]
+    picks = {}
+    for cap in (0, 8, 16, 38, 39, 76):
+        g.all_reduce(sends, recvs, cta_cap=cap)
+        picks[cap] = g.last_launch()["engine"]
+    assert picks == {0: 1, 8: CE, 16: CE, 38: CE, 39: 1, 76: 1}, picks
+    small = [s[:1 << 20] for s in sends]  # 2 MiB per rank: below the threshold
+    g.all_reduce(small, [r[:1 << 20] for r in recvs], cta_cap=8)
+    assert g.last_launch()["engine"] == tccl.tcclEngineBulk
+    reset_config(g, ce_auto_max_cap=-1)
+    g.all_reduce(sends, recvs, cta_cap=8)
+    assert g.last_launch()["engine"] == tccl.tcclEngineBulk
+    reset_config(g, ce_auto_max_cap=100)
+    g.all_reduce(sends, recvs, cta_cap=76)
+    assert g.last_launch()["engine"] == CE
+    torch.cuda.synchronize()
+    assert all(bool((r == 4).all()) for r in recvs)
+    reset_config(g)
+
+
+def test_stream_order_on_both_sides(groups):
+    """Inputs written by a kernel queued just before the call, and results
+    read by a kernel queued just after it, on a side stream, with no host
+    synchronisation in between: the copy streams join in both directions."""
+    p, n = 8, 3_000_001
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=1 << 20)
+    xs = datagen.rank_buffers("uniform_f32", 29, p, n)
+    host = [to_device(x) for x in xs]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        sends = [torch.zeros_like(h) for h in host]
+        recvs = [torch.zeros_like(h) for h in host]
+        for _ in range(3):
+            for d, h in zip(sends, host):
+                d.copy_(h * 1.0)  # a kernel on s
+            g.all_reduce(sends, recvs, cta_cap=8, stream=s.cuda_stream)
+            outs = [r.clone() for r in recvs]  # kernels on s
+            for r in recvs:
+                r.fill_(0.0)
+    s.synchronize()
+    check([to_host(o) for o in outs], oracle.allreduce(xs, "f32", "sum", nthreads=0), "stream order")
+
+
+def test_graph_capture_replay(groups):
+    p, n = 4, 1_000_003
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=256 * 1024)
+    xs = datagen.rank_buffers("normal_bf16", 30, p, n)
+    sends = [to_device(x) for x in xs]
+    recvs = [torch.zeros_like(t) for t in sends]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g.all_reduce(sends, recvs, cta_cap=16, stream=s.cuda_stream)  # plans outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        g.all_reduce(sends, recvs, cta_cap=16, stream=s.cuda_stream)
+    for r in recvs:
+        r.zero_()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    check([to_host(r) for r in recvs], oracle.allreduce(xs, "bf16", "sum"), "graph replay")
+
+
+def test_timeout_is_reported_and_the_next_call_is_right(groups):
+    p, n = 4, 500_000
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=256 * 1024, wait_timeout_ms=1000.0)
+    xs = datagen.rank_buffers("uniform_f32", 31, p, n)
+    sends = [to_device(x) for x in xs]
+    recvs = [torch.zeros_like(t) for t in sends]
+    assert tccl.tcclGroupInjectWaitTimeout(g.handle, 1, 20.0) == tccl.tcclSuccess
+    g.all_reduce(sends, recvs, cta_cap=4)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclDeviceTimeout
+    assert tccl.tcclGroupInjectWaitTimeout(g.handle, 0, 0.0) == tccl.tcclSuccess
+    g.all_reduce(sends, recvs, cta_cap=4)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    check([to_host(r) for r in recvs], oracle.allreduce(xs, "f32", "sum", nthreads=0), "after timeout")
