@@ -133,7 +133,9 @@ def test_c4_p8_bf16_128mib_caps(groups, cap):
     assert g.query_error() == tccl.tcclSuccess
     info = g.last_launch()
     if cap:
-        assert info["ctas"] <= cap and sms <= cap
+        # per launch at most `cap` CTAs; the copy-out engine's segment kernels
+        # run one after the other, so the SM record (a union) may hold more
+        assert info["ctas"] <= cap and sms <= cap * max(1, info["ce_segments"])
     check_all(recvs, exp, f"C4 cap {cap}")
 
 
