@@ -225,10 +225,9 @@ __device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
 // Bounded wait on an mbarrier phase. Gives up when another thread of the CTA
 // has flagged an abort, or after `timeout_ns` of %globaltimer time, in which
 // case it flags the abort and records a timeout in the status word.
-static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag, uint64_t timeout_ns,
-                                          int* status, bool honour_abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool wait_bounded_slow(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort_flag, uint64_t timeout_ns,
+                                               int* status, bool honour_abort) {
   uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -239,6 +238,15 @@ static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
       return false;
     }
   }
+}
+
+// The common case (the phase has already completed) costs one try_wait and
+// no call; only a wait that has to spin takes the bounded slow path.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort_flag, uint64_t timeout_ns,
+                                             int* status, bool honour_abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bounded_slow(bar, parity, abort_flag, timeout_ns, status, honour_abort);
 }
 
 // ------------------------------------------------------------------ folds
@@ -332,6 +340,79 @@ struct Fold<kI32, OP> {
     return make_uint4(static_cast<uint32_t>(a[0]), static_cast<uint32_t>(a[1]),
                       static_cast<uint32_t>(a[2]), static_cast<uint32_t>(a[3]));
   }
+};
+
+// Sums on the packed fp32 pipe: add.rn.f32x2 rounds each half to nearest
+// exactly as two scalar adds do, so the fold (ascending rank, fp32, one final
+// rounding for bf16) is unchanged; each instruction adds two lanes.
+__device__ __forceinline__ uint64_t f32x2_pair(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, uint32_t& lo, uint32_t& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_add_rn(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+struct PackedSumF32 {
+  uint64_t a[2];
+  __device__ __forceinline__ void init(uint4 u) {
+    a[0] = f32x2_pair(u.x, u.y);
+    a[1] = f32x2_pair(u.z, u.w);
+  }
+  __device__ __forceinline__ void add(uint4 u) {
+    a[0] = f32x2_add_rn(a[0], f32x2_pair(u.x, u.y));
+    a[1] = f32x2_add_rn(a[1], f32x2_pair(u.z, u.w));
+  }
+  __device__ __forceinline__ uint4 out() const {
+    uint4 r;
+    f32x2_split(a[0], r.x, r.y);
+    f32x2_split(a[1], r.z, r.w);
+    return r;
+  }
+};
+
+struct PackedSumBF16 {
+  uint64_t a[4];  // fp32 pairs (element 2j, element 2j+1)
+  __device__ __forceinline__ static uint64_t widen(uint32_t w) {
+    return f32x2_pair(w << 16, w & 0xFFFF0000u);
+  }
+  __device__ __forceinline__ void init(uint4 u) {
+    a[0] = widen(u.x); a[1] = widen(u.y); a[2] = widen(u.z); a[3] = widen(u.w);
+  }
+  __device__ __forceinline__ void add(uint4 u) {
+    a[0] = f32x2_add_rn(a[0], widen(u.x));
+    a[1] = f32x2_add_rn(a[1], widen(u.y));
+    a[2] = f32x2_add_rn(a[2], widen(u.z));
+    a[3] = f32x2_add_rn(a[3], widen(u.w));
+  }
+  __device__ __forceinline__ static uint32_t narrow(uint64_t v) {
+    uint32_t lo, hi;
+    f32x2_split(v, lo, hi);
+    return pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
+  }
+  __device__ __forceinline__ uint4 out() const {
+    return make_uint4(narrow(a[0]), narrow(a[1]), narrow(a[2]), narrow(a[3]));
+  }
+};
+
+// The fold the streaming kernels use: packed sums where they exist.
+template <int DT, int OP>
+struct StreamFold {
+  using type = Fold<DT, OP>;
+};
+template <>
+struct StreamFold<kF32, kSum> {
+  using type = PackedSumF32;
+};
+template <>
+struct StreamFold<kBF16, kSum> {
+  using type = PackedSumBF16;
 };
 
 // One element of every selected source, folded, stored to every selected
@@ -466,7 +547,7 @@ __device__ __forceinline__ void per_rank_consumers(const BulkArgs& a, BulkSmemHe
   uint32_t it = 0, off = 0, n = 0;
   bool ok = true;
   for (;;) {
-    Fold<DT, OP> acc[V];
+    typename StreamFold<DT, OP>::type acc[V];
     bool stop = false;
     for (int r = 0; r < P; ++r) {
       const uint32_t k = it % S;
@@ -725,7 +806,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
         if (COLL == kAllGather) {
           res = reinterpret_cast<const uint4*>(st)[v];
         } else {
-          Fold<DT, OP> f;
+          typename StreamFold<DT, OP>::type f;
           f.init(reinterpret_cast<const uint4*>(st)[v]);
 #pragma unroll 4
           for (int r = 1; r < P; ++r)
@@ -746,7 +827,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
       loc.locate(a, c, off, n);
       const uint32_t nv = n >> 4;
       for (uint32_t v = ctid; v < nv; v += nct) {
-        Fold<DT, OP> f;
+        typename StreamFold<DT, OP>::type f;
         f.init(reinterpret_cast<const uint4*>(st)[v]);
 #pragma unroll 4
         for (int r = 1; r < P; ++r)
@@ -929,7 +1010,7 @@ __global__ void __launch_bounds__(256) small_kernel(const __grid_constant__ Smal
         res.z = __shfl_sync(0xFFFFFFFFu, x.z, base_lane);
         res.w = __shfl_sync(0xFFFFFFFFu, x.w, base_lane);
       } else {
-        Fold<DT, OP> f;
+        typename StreamFold<DT, OP>::type f;
         for (int rr = 0; rr < P; ++rr) {
           uint4 y;
           y.x = __shfl_sync(0xFFFFFFFFu, x.x, base_lane + rr);
@@ -959,7 +1040,7 @@ __global__ void __launch_bounds__(256) small_kernel(const __grid_constant__ Smal
       if (COLL == kAllGather) {
         res = ld_global_v4(static_cast<const char*>(a.p.src[w.src_sel < 0 ? 0 : w.src_sel]) + w.src_off + off);
       } else {
-        Fold<DT, OP> f;
+        typename StreamFold<DT, OP>::type f;
         f.init(ld_global_v4(static_cast<const char*>(a.p.src[0]) + w.src_off + off));
 #pragma unroll 8
         for (int r = 1; r < P; ++r)
