@@ -21,7 +21,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 HOST_SOURCES = ["api.cpp", "plan.cpp", "reshard.cpp"]
 CUDA_SOURCES = ["kernels_bulk.cu", "kernels_small_ar.cu", "kernels_small_rs.cu",
                 "kernels_small_ag.cu", "kernels_reshard.cu", "kernels_rmsnorm.cu",
-                "no_alloc.cu"]
+                "no_alloc.cu", "kernels_copy_out.cu"]
 
 
 def _cuda_home() -> Path:

@@ -14,6 +14,7 @@
 #include <string>
 #include <vector>
 
+#include "copy_out.h"
 #include "internal.h"
 #include "plan.h"
 #include "reshard.h"
@@ -476,14 +477,18 @@ int join_ce_streams(tcclGroup* g, int used, cudaStream_t stream) {
 }
 
 // Allreduce on the copy-out engine. The message is cut into segments of
-// ce_segment_bytes per rank (offsets multiples of 256 bytes, so every full
-// segment shares one cached plan). Each segment's bulk-engine kernel folds
-// the P ranks in ascending order and stores the result to the anchor rank
-// (rank 0) alone; an event after it releases the device-to-device copies of
-// that segment from the anchor to ranks 1..P-1 on the group's copy streams,
-// so the copy engines fan segment s out while the SMs reduce segment s+1.
-// In place is safe: segment s of a rank is overwritten only after the
-// kernel that read it has finished.
+// ce_segment_bytes per rank (offsets multiples of 256 bytes, so every
+// segment has the same alignment). Each segment's shard-in kernel folds the P
+// ranks in ascending order into the anchor rank's (rank 0's) receive buffer
+// alone; an event after it releases the device-to-device copies of that
+// segment from the anchor to ranks 1..P-1 on the group's copy streams, so the
+// copy engines fan segment s out while the SMs reduce segment s+1. In place
+// is safe: segment s of a rank is overwritten only after the kernel that read
+// it has finished.
+//
+// The shard-in kernel is the register-load anchor fold when every send buffer
+// and the anchor's receive buffer share their address mod 16, else the bulk
+// engine's TMA pipeline with every window pointed at the anchor.
 tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void* const* recv,
                                     size_t count, int dtype, int op, int es, cudaStream_t stream,
                                     int cap) {
@@ -496,8 +501,6 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
   const int nseg = (int)((count + seg - 1) / seg);
   tcclResult_t r = ensure_ce_resources(g, nseg);
   if (r != tcclSuccess) return r;
-  // both plans (full segments, ragged tail) before any launch: a new plan's
-  // table upload is synchronous
   std::vector<const void*> s_ptr(P);
   std::vector<void*> r_ptr(P);
   auto at = [&](size_t off) {
@@ -506,24 +509,52 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
       r_ptr[k] = static_cast<char*>(recv[k]) + off * es;
     }
   };
+  const uintptr_t mod = (uintptr_t)recv[anchor] & 15;
+  bool fast = seg * (size_t)es / 16 < kAnchorMaxVectors;
+  for (int k = 0; k < P; ++k) fast = fast && (((uintptr_t)send[k] & 15) == mod);
+  const size_t tail_n = count - (size_t)(nseg - 1) * seg;
+  // TMA fallback: both plans (full segments, ragged tail) before any launch,
+  // since a new plan's table upload is synchronous
   CachedPlan* full = nullptr;
   CachedPlan* tail = nullptr;
-  const size_t tail_n = count - (size_t)(nseg - 1) * seg;
-  at(0);
-  r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), nseg > 1 ? seg : tail_n, es, cap, &full, anchor);
-  if (r == tcclSuccess && nseg > 1 && tail_n != seg) {
-    at((size_t)(nseg - 1) * seg);
-    r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), tail_n, es, cap, &tail, anchor);
+  if (!fast) {
+    at(0);
+    r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), nseg > 1 ? seg : tail_n, es, cap, &full, anchor);
+    if (r == tcclSuccess && nseg > 1 && tail_n != seg) {
+      at((size_t)(nseg - 1) * seg);
+      r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), tail_n, es, cap, &tail, anchor);
+    }
+    if (r != tcclSuccess) return r;
   }
-  if (r != tcclSuccess) return r;
+  const int U = P <= 4 ? 2 : 1;
+  int fast_grid = 0;
+  AnchorArgs aa;
+  std::memset(&aa, 0, sizeof(aa));
+  aa.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
+  aa.nranks = P;
   const int used = std::min(g->cfg.ce_streams, P - 1);
   int err = 0, copies = 0;
   for (int sgi = 0; sgi < nseg && !err; ++sgi) {
     const size_t off = (size_t)sgi * seg;
     const size_t n = sgi == nseg - 1 ? tail_n : seg;
     at(off);
-    CachedPlan* cp = (sgi == nseg - 1 && tail) ? tail : full;
-    err = launch_plan(g, cp, kAllReduce, dtype, op, s_ptr.data(), r_ptr.data(), es, stream);
+    if (fast) {
+      const size_t bytes = n * es;
+      const size_t head = std::min(bytes, (size_t)((16 - mod) & 15));
+      aa.head_bytes = head;
+      aa.nvec = (bytes - head) / 16;
+      aa.tail_bytes = bytes - head - aa.nvec * 16;
+      for (int k = 0; k < P; ++k) aa.p.src[k] = s_ptr[k];
+      aa.p.dst[0] = r_ptr[anchor];
+      const uint64_t per_cta = (uint64_t)kAnchorThreads * U;
+      uint64_t grid = std::max<uint64_t>(1, (aa.nvec + per_cta - 1) / per_cta);
+      grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
+      fast_grid = std::max(fast_grid, (int)grid);
+      err = launch_anchor_reduce(dtype, op, aa, (int)grid, U, stream);
+    } else {
+      CachedPlan* cp = (sgi == nseg - 1 && tail) ? tail : full;
+      err = launch_plan(g, cp, kAllReduce, dtype, op, s_ptr.data(), r_ptr.data(), es, stream);
+    }
     if (err || used == 0) continue;
     err = cudaEventRecord(g->ce_seg_events[sgi], stream);
     for (int j = 0; j < used && !err; ++j) err = cudaStreamWaitEvent(g->ce_streams[j], g->ce_seg_events[sgi], 0);
@@ -537,7 +568,14 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
   }
   const int jerr = used ? join_ce_streams(g, used, stream) : 0;
   if (!err) err = jerr;
-  fill_info(full->low, &g->last);
+  if (fast) {
+    std::memset(&g->last, 0, sizeof(g->last));
+    g->last.store_mode = kStoreVec;
+    g->last.ctas = fast_grid;
+    g->last.threads = kAnchorThreads;
+  } else {
+    fill_info(full->low, &g->last);
+  }
   g->last.engine = kEngineCopyOut;
   g->last.ce_segments = nseg;
   g->last.ce_copies = copies;

@@ -1,0 +1,121 @@
+// Copy-out engine shard-in: the P-rank fold into one anchor buffer.
+//
+// Under a CTA cap the work of a few SMs decides the rate. Feeding a fold
+// through TMA copies and shared memory costs each byte a shared-memory write
+// and a read plus per-stage synchronisation, and a capped SM then reads about
+// 50 GB/s; 128-bit register loads with eight in flight per thread read about
+// 140 GB/s per SM on GB300. The result goes to one buffer only, so this
+// kernel is read-bound; the copy engines do the remaining P-1 stores.
+#include "copy_out.h"
+#include "dispatch.cuh"
+
+namespace tccl {
+namespace dev {
+namespace {
+
+// read-only path, no L1 allocation: each input byte is read exactly once
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// default write policy: the copy engines read the result back soon after,
+// so it should stay in L2 if it can
+__device__ __forceinline__ void st_keep_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Thread t of the grid folds vectors t, t + T, ... (T threads in all), U of
+// them at a time, the ranks in batches of 8 / U so that eight loads are in
+// flight; each batch is folded in ascending rank order into the same
+// accumulators, so the result is the plain left fold over all P ranks.
+template <int DT, int OP, int U>
+__global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const __grid_constant__ AnchorArgs a) {
+  constexpr int RB = 8 / U;
+  if (threadIdx.x == 0) record_sm(a.sm_mask);
+  const int P = a.nranks;
+  // a launch covers at most 2^28 vectors (the host splits larger segments),
+  // so vector indices and byte offsets within it fit 32 bits
+  const uint32_t nthr = gridDim.x * blockDim.x;
+  const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t nvec = static_cast<uint32_t>(a.nvec);
+  char* dst = static_cast<char*>(a.p.dst[0]) + a.head_bytes;
+  for (uint32_t base = gtid; base < nvec; base += nthr * U) {
+    typename StreamFold<DT, OP>::type acc[U];
+    for (int r0 = 0; r0 < P; r0 += RB) {
+      uint4 x[U][RB];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t v = base + u * nthr;
+#pragma unroll
+        for (int k = 0; k < RB; ++k)
+          if (v < nvec && r0 + k < P)
+            x[u][k] = ld_stream_v4(static_cast<const char*>(a.p.src[r0 + k]) + a.head_bytes +
+                                   static_cast<uint64_t>(v) * 16);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (base + u * nthr >= nvec) continue;
+#pragma unroll
+        for (int k = 0; k < RB; ++k) {
+          if (r0 + k >= P) break;
+          if (r0 + k == 0) acc[u].init(x[u][k]);
+          else acc[u].add(x[u][k]);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t v = base + u * nthr;
+      if (v < nvec) st_keep_v4(dst + static_cast<uint64_t>(v) * 16, acc[u].out());
+    }
+  }
+  // the unaligned head and tail, one element per thread
+  constexpr int es = DT == kBF16 ? 2 : 4;
+  const uint32_t nh = static_cast<uint32_t>(a.head_bytes / es);
+  const uint32_t nt = static_cast<uint32_t>(a.tail_bytes / es);
+  if (gtid < nh + nt) {
+    Window w;
+    w.src_sel = -1;
+    w.dst_sel = 0;
+    w.scalar = 1;
+    w.task = 0;
+    w.cta = -1;
+    uint64_t e = gtid;
+    if (gtid < nh) {
+      w.src_off = w.dst_off = 0;
+      w.bytes = static_cast<uint32_t>(a.head_bytes);
+    } else {
+      w.src_off = w.dst_off = a.head_bytes + static_cast<uint64_t>(nvec) * 16;
+      w.bytes = static_cast<uint32_t>(a.tail_bytes);
+      e -= nh;
+    }
+    scalar_element<kAllReduce, DT, OP, kMaxRanks>(a.p, P, w, e);
+  }
+}
+
+template <int C, int D, int O>
+int launch_anchor_t(const AnchorArgs& a, int grid, int u, cudaStream_t st) {
+  if (u == 2)
+    anchor_reduce_kernel<D, O, 2><<<grid, kAnchorThreads, 0, st>>>(a);
+  else
+    anchor_reduce_kernel<D, O, 1><<<grid, kAnchorThreads, 0, st>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+}  // namespace dev
+
+int launch_anchor_reduce(int dtype, int op, const AnchorArgs& a, int grid, int vectors_per_thread,
+                         void* stream) {
+  using namespace dev;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TCCL_REDUCE_SWITCH(kAllReduce, launch_anchor_t, a, grid, vectors_per_thread, st)
+}
+
+}  // namespace tccl

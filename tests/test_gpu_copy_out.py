@@ -262,18 +262,47 @@ def test_graph_capture_replay(groups):
 
 
 def test_timeout_is_reported_and_the_next_call_is_right(groups):
+    """Send and receive buffers that are not co-aligned take the TMA shard-in
+    (the register-load fold has no waits to run out); its injected wait runs
+    out, the status says so, and the next call is right."""
     p, n = 4, 500_000
     g = groups(p)
     reset_config(g, engine=CE, ce_segment_bytes=256 * 1024, wait_timeout_ms=1000.0)
     xs = datagen.rank_buffers("uniform_f32", 31, p, n)
-    sends = [to_device(x) for x in xs]
-    recvs = [torch.zeros_like(t) for t in sends]
+    sends = [Guarded(n, "f32", 4) for _ in range(p)]
+    for s_, x in zip(sends, xs):
+        s_.tensor.copy_(to_device(x))
+    recvs = [Guarded(n, "f32", 0) for _ in range(p)]
+    st = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        return tccl.tcclAllReduce(g.handle, [t.tensor for t in sends], [t.tensor for t in recvs], n,
+                                  DT_CODE["f32"], tccl.tcclSum, st, 4)
+
     assert tccl.tcclGroupInjectWaitTimeout(g.handle, 1, 20.0) == tccl.tcclSuccess
-    g.all_reduce(sends, recvs, cta_cap=4)
+    assert call() == tccl.tcclSuccess
     torch.cuda.synchronize()
     assert g.query_error() == tccl.tcclDeviceTimeout
+    assert g.last_launch()["threads"] == 544
     assert tccl.tcclGroupInjectWaitTimeout(g.handle, 0, 0.0) == tccl.tcclSuccess
-    g.all_reduce(sends, recvs, cta_cap=4)
+    assert call() == tccl.tcclSuccess
     torch.cuda.synchronize()
     assert g.query_error() == tccl.tcclSuccess
-    check([to_host(r) for r in recvs], oracle.allreduce(xs, "f32", "sum", nthreads=0), "after timeout")
+    assert all(t.guards_intact() for t in recvs)
+    check([t.host() for t in recvs], oracle.allreduce(xs, "f32", "sum", nthreads=0), "after timeout")
+
+
+@pytest.mark.parametrize("offs,fast", [((0, 0), True), ((4, 4), True), ((6, 6), True),
+                                       ((4, 0), False), ((0, 2), False)])
+@pytest.mark.parametrize("p", [2, 4, 8])
+def test_shard_in_kernel_choice(groups, offs, fast, p):
+    """Co-aligned buffers (same address mod 16, any offset) take the register
+    fold (1024 threads per CTA, unaligned edges element-wise); the rest take
+    the TMA pipeline (544 threads). Both are exact."""
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=64 * 1024)
+    xs = datagen.rank_buffers("normal_bf16", 32, p, 200_003)
+    got = allreduce(g, xs, "bf16", "sum", cap=6, send_off=offs[0], recv_off=offs[1])
+    info = g.last_launch()
+    assert info["threads"] == (1024 if fast else 544) and info["ctas"] <= 6, info
+    check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), f"offs {offs} P={p}")
