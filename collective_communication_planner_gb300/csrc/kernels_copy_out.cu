@@ -31,14 +31,15 @@ __device__ __forceinline__ void st_keep_v4(void* p, uint4 v) {
 }
 
 // Thread t of the grid folds vectors t, t + T, ... (T threads in all), U of
-// them at a time, the ranks in batches of 8 / U so that eight loads are in
-// flight; each batch is folded in ascending rank order into the same
-// accumulators, so the result is the plain left fold over all P ranks.
-template <int DT, int OP, int U>
+// them at a time. With the rank count fixed at compile time (NP = 2, 4, 8)
+// every load of a step is issued before the first add; otherwise the ranks
+// go in batches of 8 / U. Either way each accumulator receives the ranks in
+// ascending order: the plain left fold over all P ranks.
+template <int DT, int OP, int NP, int U>
 __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const __grid_constant__ AnchorArgs a) {
-  constexpr int RB = 8 / U;
+  constexpr int RB = NP > 0 ? NP : 8 / U;
   if (threadIdx.x == 0) record_sm(a.sm_mask);
-  const int P = a.nranks;
+  const int P = NP > 0 ? NP : a.nranks;
   // a launch covers at most 2^28 vectors (the host splits larger segments),
   // so vector indices and byte offsets within it fit 32 bits
   const uint32_t nthr = gridDim.x * blockDim.x;
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
         const uint32_t v = base + u * nthr;
 #pragma unroll
         for (int k = 0; k < RB; ++k)
-          if (v < nvec && r0 + k < P)
+          if (v < nvec && (NP > 0 || r0 + k < P))
             x[u][k] = ld_stream_v4(static_cast<const char*>(a.p.src[r0 + k]) + a.head_bytes +
                                    static_cast<uint64_t>(v) * 16);
       }
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
         if (base + u * nthr >= nvec) continue;
 #pragma unroll
         for (int k = 0; k < RB; ++k) {
-          if (r0 + k >= P) break;
+          if (NP == 0 && r0 + k >= P) break;
           if (r0 + k == 0) acc[u].init(x[u][k]);
           else acc[u].add(x[u][k]);
         }
@@ -101,10 +102,14 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
 
 template <int C, int D, int O>
 int launch_anchor_t(const AnchorArgs& a, int grid, int u, cudaStream_t st) {
-  if (u == 2)
-    anchor_reduce_kernel<D, O, 2><<<grid, kAnchorThreads, 0, st>>>(a);
-  else
-    anchor_reduce_kernel<D, O, 1><<<grid, kAnchorThreads, 0, st>>>(a);
+  switch (a.nranks) {
+    case 2: anchor_reduce_kernel<D, O, 2, 2><<<grid, kAnchorThreads, 0, st>>>(a); break;
+    case 4: anchor_reduce_kernel<D, O, 4, 2><<<grid, kAnchorThreads, 0, st>>>(a); break;
+    case 8: anchor_reduce_kernel<D, O, 8, 1><<<grid, kAnchorThreads, 0, st>>>(a); break;
+    default:
+      if (u == 2) anchor_reduce_kernel<D, O, 0, 2><<<grid, kAnchorThreads, 0, st>>>(a);
+      else anchor_reduce_kernel<D, O, 0, 1><<<grid, kAnchorThreads, 0, st>>>(a);
+  }
   return static_cast<int>(cudaGetLastError());
 }
 
