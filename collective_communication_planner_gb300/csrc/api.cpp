@@ -437,7 +437,8 @@ bool use_copy_out(const tcclGroup* g, int coll, size_t count, int es, int cap) {
   if (coll == kReduceScatter || g->nranks < 2) return false;
   if (g->cfg.engine == kEngineCopyOut) return true;
   if (g->cfg.engine != kEngineAuto || cap <= 0 || g->cfg.ce_auto_max_cap < 0) return false;
-  const int max_cap = g->cfg.ce_auto_max_cap > 0 ? g->cfg.ce_auto_max_cap : g->dev.sm_count / 4;
+  // GB300 sweep (P = 2, 4, 8): copy-out is ahead up to a cap of 48 of 152 SMs
+  const int max_cap = g->cfg.ce_auto_max_cap > 0 ? g->cfg.ce_auto_max_cap : g->dev.sm_count * 5 / 16;
   const size_t per_rank = count * (size_t)es * (coll == kAllGather ? (size_t)g->nranks : 1);
   return cap <= max_cap && per_rank >= kCeAutoMinBytes;
 }
@@ -494,8 +495,13 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
                                     int cap) {
   const int P = g->nranks;
   const int anchor = 0;
+  // at least four segments when that keeps them >= 4 MiB, none above
+  // ce_segment_bytes: the copies of the first segment and the kernel of the
+  // last one do not overlap anything, so they should be short
   const size_t align = 256 / (size_t)es;
-  size_t seg = std::max<size_t>(align, (g->cfg.ce_segment_bytes / (size_t)es) / align * align);
+  const size_t quarter = std::max<size_t>((size_t)4 << 20, (count * es + 3) / 4);
+  const size_t seg_bytes = std::min<size_t>(g->cfg.ce_segment_bytes, quarter);
+  size_t seg = std::max<size_t>(align, (seg_bytes / (size_t)es) / align * align);
   if ((count + seg - 1) / seg > (size_t)kMaxCeSegments)
     seg = ((count + kMaxCeSegments - 1) / kMaxCeSegments + align - 1) / align * align;
   const int nseg = (int)((count + seg - 1) / seg);

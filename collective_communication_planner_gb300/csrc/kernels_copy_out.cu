@@ -13,21 +13,45 @@ namespace tccl {
 namespace dev {
 namespace {
 
-// read-only path, no L1 allocation: each input byte is read exactly once
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+// L2 policies: the inputs are read exactly once (evict first); the result is
+// read back by the copy engines right after the kernel, up to P-1 times, and
+// should still be in L2 then (evict last)
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// read-only path, no L1 allocation; HINT: with the L2 policy
+template <bool HINT>
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p, uint64_t policy) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+  if (HINT)
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(policy));
+  else
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
   return r;
 }
 
-// default write policy: the copy engines read the result back soon after,
-// so it should stay in L2 if it can
-__device__ __forceinline__ void st_keep_v4(void* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
+template <bool HINT>
+__device__ __forceinline__ void st_keep_v4(void* p, uint4 v, uint64_t policy) {
+  if (HINT)
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
+  else
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
 }
 
 // Thread t of the grid folds vectors t, t + T, ... (T threads in all), U of
@@ -46,6 +70,11 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
   const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const uint32_t nvec = static_cast<uint32_t>(a.nvec);
   char* dst = static_cast<char*>(a.p.dst[0]) + a.head_bytes;
+  // the two policy registers fit beside one vector per thread (64 registers
+  // at 1024 threads), not beside two
+  constexpr bool kHint = U == 1;
+  const uint64_t load_policy = kHint ? l2_policy_evict_first() : 0;
+  const uint64_t store_policy = kHint ? l2_policy_evict_last() : 0;
   for (uint32_t base = gtid; base < nvec; base += nthr * U) {
     typename StreamFold<DT, OP>::type acc[U];
     for (int r0 = 0; r0 < P; r0 += RB) {
@@ -56,8 +85,8 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
 #pragma unroll
         for (int k = 0; k < RB; ++k)
           if (v < nvec && (NP > 0 || r0 + k < P))
-            x[u][k] = ld_stream_v4(static_cast<const char*>(a.p.src[r0 + k]) + a.head_bytes +
-                                   static_cast<uint64_t>(v) * 16);
+            x[u][k] = ld_stream_v4<kHint>(static_cast<const char*>(a.p.src[r0 + k]) + a.head_bytes +
+                                   static_cast<uint64_t>(v) * 16, load_policy);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -73,7 +102,7 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint32_t v = base + u * nthr;
-      if (v < nvec) st_keep_v4(dst + static_cast<uint64_t>(v) * 16, acc[u].out());
+      if (v < nvec) st_keep_v4<kHint>(dst + static_cast<uint64_t>(v) * 16, acc[u].out(), store_policy);
     }
   }
   // the unaligned head and tail, one element per thread

@@ -153,11 +153,12 @@ Config resolve_config(const Config& in) {
   if (c.load_policy < 0 || c.load_policy > 2) c.load_policy = 0;
   if (c.max_chunk_bytes == 0) c.max_chunk_bytes = 16384;
   c.max_chunk_bytes = std::min<size_t>(std::max<size_t>(c.max_chunk_bytes, 256), 65536) & ~(size_t)15;
-  // copy engines: four streams, 16 MiB pieces sustained ~4.8 TB/s of
-  // fan-out copies in a GB300 probe (one stream ~2.5, 2 MiB pieces ~1.1)
+  // copy engines: four streams and pieces of 16 MiB or more sustained
+  // ~4.8 TB/s of fan-out copies in a GB300 probe (one stream ~2.5, 2 MiB
+  // pieces ~1.1); segments up to 32 MiB per rank
   if (c.ce_streams <= 0) c.ce_streams = 4;
   if (c.ce_streams > 8) c.ce_streams = 8;
-  if (c.ce_segment_bytes == 0) c.ce_segment_bytes = (size_t)16 << 20;
+  if (c.ce_segment_bytes == 0) c.ce_segment_bytes = (size_t)32 << 20;
   c.ce_segment_bytes = std::min<size_t>(std::max<size_t>(c.ce_segment_bytes, 4096), (size_t)1 << 30) & ~(size_t)255;
   return c;
 }

@@ -81,7 +81,9 @@ typedef enum {
                               no kernel, no SM. Reduce-scatter has no shard-out and runs on the
                               bulk engine. Auto picks it for capped allreduce / all-gather calls
                               of at least 4 MiB per rank when the cap is at most
-                              ce_auto_max_cap CTAs. */
+                              ce_auto_max_cap CTAs. The segment kernel folds with 128-bit register
+                              loads when the send buffers and the anchor's receive buffer share
+                              their address mod 16, else with the bulk engine's TMA pipeline. */
 } tcclEngine_t;
 
 typedef enum {
@@ -131,10 +133,11 @@ typedef struct {
   size_t max_chunk_bytes;  /* bulk engine: upper bound on bytes per source per chunk */
   int stage_layout;        /* bulk engine: tcclStageLayout_t */
   int ce_streams;          /* copy-out engine: internal copy streams, 1..8 (default 2) */
-  size_t ce_segment_bytes; /* copy-out engine: bytes per rank in one segment (default 8 MiB;
-                              rounded down to a multiple of 256) */
+  size_t ce_segment_bytes; /* copy-out engine: most bytes per rank in one segment (default
+                              32 MiB; a call is cut into at least four segments of at least
+                              4 MiB where it can be; rounded down to a multiple of 256) */
   int ce_auto_max_cap;     /* Auto picks the copy-out engine for caps up to this many CTAs
-                              (0: a quarter of the SMs; negative: never) */
+                              (0: 5/16 of the SMs; negative: never) */
 } tcclConfig_t;
 
 /* What the last launch on a group looked like. */

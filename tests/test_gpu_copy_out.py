@@ -196,10 +196,11 @@ def test_auto_picks_copy_out_for_large_capped_calls(groups):
     sends = [torch.ones(n, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
     recvs = [torch.empty_like(s) for s in sends]
     picks = {}
-    for cap in (0, 8, 16, 38, 39, 76):
+    edge = torch.cuda.get_device_properties(0).multi_processor_count * 5 // 16
+    for cap in (0, 8, 16, edge, edge + 1, 2 * edge):
         g.all_reduce(sends, recvs, cta_cap=cap)
         picks[cap] = g.last_launch()["engine"]
-    assert picks == {0: 1, 8: CE, 16: CE, 38: CE, 39: 1, 76: 1}, picks
+    assert picks == {0: 1, 8: CE, 16: CE, edge: CE, edge + 1: 1, 2 * edge: 1}, picks
     small = [s[:1 << 20] for s in sends]  # 2 MiB per rank: below the threshold
     g.all_reduce(small, [r[:1 << 20] for r in recvs], cta_cap=8)
     assert g.last_launch()["engine"] == tccl.tcclEngineBulk
@@ -207,7 +208,7 @@ def test_auto_picks_copy_out_for_large_capped_calls(groups):
     g.all_reduce(sends, recvs, cta_cap=8)
     assert g.last_launch()["engine"] == tccl.tcclEngineBulk
     reset_config(g, ce_auto_max_cap=100)
-    g.all_reduce(sends, recvs, cta_cap=76)
+    g.all_reduce(sends, recvs, cta_cap=2 * edge)
     assert g.last_launch()["engine"] == CE
     torch.cuda.synchronize()
     assert all(bool((r == 4).all()) for r in recvs)
