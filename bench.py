@@ -553,12 +553,13 @@ def sweep(args):
         assert tccl.tcclGroupSetConfig(g.handle, c) == 0
 
     def copy_out_moved(row, p, nbytes):
-        """Copy-out allreduce rows: HBM bytes actually moved (the kernel reads
+        """Copy-out allreduce rows: every byte the call moves (the fold reads
         P x S and writes S; the copies read and write (P-1) x S) beside the
-        collective's own 2 x P x S."""
+        collective's own 2 x P x S. The copies' reads of the anchor can be
+        served from L2, so this can exceed the HBM peak."""
         if row["engine"] == tccl.tcclEngineCopyOut:
             moved = (p + 1) * nbytes + 2 * (p - 1) * nbytes
-            row["moved_hbm_fraction"] = round(moved / (row["us"] * 1e-6) / 1e9 / peak, 4)
+            row["moved_bytes_fraction"] = round(moved / (row["us"] * 1e-6) / 1e9 / peak, 4)
 
     def to_dev(x):
         return host_to_torch(x).to(dev)
@@ -933,20 +934,82 @@ def rmsnorm_bench(args):
 
 # ------------------------------------------------------------------ probe mode
 def probe():
-    """Builds and runs the per-SM bandwidth probe
-    (collective_communication_planner_gb300/probes/sm_bandwidth.cu): what one
-    SM can read, write and copy with each mechanism, which bounds what a CTA
-    cap can deliver. Prints the probe's JSON lines."""
-    src = ROOT / "collective_communication_planner_gb300" / "probes" / "sm_bandwidth.cu"
+    """Builds and runs the two hardware probes under
+    collective_communication_planner_gb300/probes/: what one SM can read,
+    write and copy with each mechanism (sm_bandwidth.cu, which bounds what a
+    CTA cap can deliver), and what the copy engines add beside a capped fold
+    (copy_engine.cu). Prints the probes' JSON lines."""
     out_dir = ROOT / "collective_communication_planner_gb300" / "_build"
     out_dir.mkdir(exist_ok=True)
-    exe = out_dir / "sm_bandwidth_probe"
-    subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
-                           "-std=c++17", "-lineinfo", "-o", str(exe), str(src)])
-    r = subprocess.run([str(exe)], capture_output=True, text=True)
-    sys.stdout.write(r.stdout)
-    if r.returncode != 0:
-        raise SystemExit(f"probe failed ({r.returncode}): {r.stderr.strip()}")
+    for name in ("sm_bandwidth", "copy_engine"):
+        src = ROOT / "collective_communication_planner_gb300" / "probes" / f"{name}.cu"
+        exe = out_dir / f"{name}_probe"
+        subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
+                               "-std=c++17", "-lineinfo", "-o", str(exe), str(src)])
+        r = subprocess.run([str(exe)], capture_output=True, text=True)
+        sys.stdout.write(r.stdout)
+        if r.returncode != 0:
+            raise SystemExit(f"{name} probe failed ({r.returncode}): {r.stderr.strip()}")
+
+
+# ------------------------------------------------------------------ copy-out mode
+def copy_out_bench(args):
+    """The C4 allreduce (P=8, bf16, 128 MiB per rank) at CTA caps 8, 16 and
+    32 with the default engine choice (the copy-out engine) and with the
+    SM-only bulk engine: device time per call, HBM fraction of the 2*P*S
+    bytes, segments and copies per call. Results checked against the oracle
+    on sampled elements. A small, fixed number of launches, so the command
+    also serves for an ncu launch list."""
+    import numpy as np
+    import torch
+    import collective_communication_planner_gb300 as tccl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS["c4"]
+    p, n = w["p"], w["count"]
+    xs = make_inputs(w)
+    sends = [host_to_torch(x).to(dev) for x in xs]
+    recvs = [torch.empty_like(t) for t in sends]
+    stream = torch.cuda.current_stream()
+    st = stream.cuda_stream
+    peak, _ = measured_peak()
+    g = tccl.Group(p)
+    alg = 2 * p * n * 2
+
+    def set_cfg(**kw):
+        c = tccl.tcclConfig_t()
+        for k, v in kw.items():
+            setattr(c, k, v)
+        assert tccl.tcclGroupSetConfig(g.handle, c) == 0
+
+    import oracle
+    idx = np.sort(np.random.default_rng(5).choice(n, size=4096, replace=False))
+    exp = oracle.allreduce([x[idx].copy() for x in xs], "bf16", "sum")[0]
+    for cap in (8, 16, 32):
+        for variant, kw in (("auto", {}), ("sm_only", {"ce_auto_max_cap": -1})):
+            set_cfg(**kw)
+            call = lambda: tccl.tcclAllReduce(g.handle, sends, recvs, n, tccl.DTYPES["bf16"],
+                                              tccl.tcclSum, st, cap)
+            for _ in range(3):
+                assert call() == 0
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(10):
+                assert call() == 0
+            e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1) / 10
+            info = g.last_launch()
+            got = recvs[p - 1].view(torch.int16).cpu().numpy().view(np.uint16)[idx]
+            print(json.dumps({"mode": "copy_out", "workload": w["name"], "cap": cap, "variant": variant,
+                              "engine": info["engine"], "ctas": info["ctas"], "threads": info["threads"],
+                              "segments": info["ce_segments"], "copies": info["ce_copies"],
+                              "us": round(ms * 1e3, 2), "hbm_fraction": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
+                              "sampled_exact": bool(np.array_equal(got, exp))}), flush=True)
+    assert g.query_error() == tccl.tcclSuccess
+    g.close()
 
 
 def main():
@@ -971,6 +1034,8 @@ def main():
                     help="M-to-N reshard throughput on an 8192 x 8192 bf16 weight")
     ap.add_argument("--rmsnorm", action="store_true",
                     help="allreduce fused with RMSNorm vs the plain allreduce (C5 shapes)")
+    ap.add_argument("--copy-out", action="store_true",
+                    help="C4 at CTA caps 8/16/32: copy-out engine vs SM-only bulk engine")
     ap.add_argument("--gemm-n", type=int, default=8192)
     ap.add_argument("--overlap-engine", type=int, default=0,
                     help="engine for the overlap study (0 auto, 1 bulk, 4 TMA-reduce)")
@@ -1014,6 +1079,9 @@ def main():
         return
     if args.rmsnorm:
         rmsnorm_bench(args)
+        return
+    if args.copy_out:
+        copy_out_bench(args)
         return
     if dist is not None:
         dist.barrier()
