@@ -434,12 +434,13 @@ constexpr size_t kCeAutoMinBytes = (size_t)4 << 20;
 // whose per-rank buffer is large, with a cap small enough that the SMs, not
 // HBM, would bound the SM-only path.
 bool use_copy_out(const tcclGroup* g, int coll, size_t count, int es, int cap) {
-  if (coll == kReduceScatter || g->nranks < 2) return false;
+  if (g->nranks < 2) return false;
   if (g->cfg.engine == kEngineCopyOut) return true;
   if (g->cfg.engine != kEngineAuto || cap <= 0 || g->cfg.ce_auto_max_cap < 0) return false;
   // GB300 sweep (P = 2, 4, 8): copy-out is ahead up to a cap of 48 of 152 SMs
   const int max_cap = g->cfg.ce_auto_max_cap > 0 ? g->cfg.ce_auto_max_cap : g->dev.sm_count * 5 / 16;
-  const size_t per_rank = count * (size_t)es * (coll == kAllGather ? (size_t)g->nranks : 1);
+  const size_t per_rank =
+      count * (size_t)es * (coll == kAllReduce ? 1 : (size_t)g->nranks);  // RS: send; AG: recv
   return cap <= max_cap && per_rank >= kCeAutoMinBytes;
 }
 
@@ -532,12 +533,13 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
     }
     if (r != tcclSuccess) return r;
   }
-  const int U = P <= 4 ? 2 : 1;
+  const int U = anchor_vectors_per_thread(P);
   int fast_grid = 0;
   AnchorArgs aa;
   std::memset(&aa, 0, sizeof(aa));
   aa.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
   aa.nranks = P;
+  aa.njobs = 1;
   const int used = std::min(g->cfg.ce_streams, P - 1);
   int err = 0, copies = 0;
   for (int sgi = 0; sgi < nseg && !err; ++sgi) {
@@ -556,7 +558,7 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
       uint64_t grid = std::max<uint64_t>(1, (aa.nvec + per_cta - 1) / per_cta);
       grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
       fast_grid = std::max(fast_grid, (int)grid);
-      err = launch_anchor_reduce(dtype, op, aa, (int)grid, U, stream);
+      err = launch_anchor_reduce(dtype, op, aa, (int)grid, stream);
     } else {
       CachedPlan* cp = (sgi == nseg - 1 && tail) ? tail : full;
       err = launch_plan(g, cp, kAllReduce, dtype, op, s_ptr.data(), r_ptr.data(), es, stream);
@@ -587,6 +589,52 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
   g->last.ce_copies = copies;
   if (err) {
     if (log_level()) std::fprintf(stderr, "[tccl] copy-out allreduce failed: %s\n", cudaGetErrorString((cudaError_t)err));
+    return tcclCudaError;
+  }
+  return tcclSuccess;
+}
+
+// Reduce-scatter on the copy-out engine: no copies, one launch of the
+// register-load fold with P jobs, shard j of every send buffer folded into
+// rank j's receive buffer. Needs every send and receive buffer to share its
+// address mod 16 and the shard size to be a multiple of 16 bytes (so every
+// shard starts at that same alignment); returns tcclInvalidUsage otherwise,
+// and the caller takes the bulk engine.
+tcclResult_t run_copy_out_reduce_scatter(tcclGroup* g, const void* const* send, void* const* recv,
+                                         size_t rc, int dtype, int op, int es, cudaStream_t stream,
+                                         int cap) {
+  const int P = g->nranks;
+  const size_t bytes = rc * (size_t)es;
+  const uintptr_t mod = (uintptr_t)recv[0] & 15;
+  bool ok = bytes % 16 == 0 && bytes / 16 < kAnchorMaxVectors;
+  for (int k = 0; k < P; ++k)
+    ok = ok && (((uintptr_t)send[k] & 15) == mod) && (((uintptr_t)recv[k] & 15) == mod);
+  if (!ok) return tcclInvalidUsage;
+  AnchorArgs aa;
+  std::memset(&aa, 0, sizeof(aa));
+  aa.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
+  aa.nranks = P;
+  aa.njobs = P;
+  aa.job_src_stride = bytes;
+  aa.head_bytes = std::min(bytes, (size_t)((16 - mod) & 15));
+  aa.nvec = (bytes - aa.head_bytes) / 16;
+  aa.tail_bytes = bytes - aa.head_bytes - aa.nvec * 16;
+  for (int k = 0; k < P; ++k) {
+    aa.p.src[k] = send[k];
+    aa.p.dst[k] = recv[k];
+  }
+  const uint64_t per_cta = (uint64_t)kAnchorThreads * anchor_vectors_per_thread(P);
+  uint64_t grid = std::max<uint64_t>(1, (aa.nvec * P + per_cta - 1) / per_cta);
+  grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
+  const int err = launch_anchor_reduce(dtype, op, aa, (int)grid, stream);
+  std::memset(&g->last, 0, sizeof(g->last));
+  g->last.engine = kEngineCopyOut;
+  g->last.store_mode = kStoreVec;
+  g->last.ctas = (int)grid;
+  g->last.threads = kAnchorThreads;
+  g->last.ce_segments = 1;
+  if (err) {
+    if (log_level()) std::fprintf(stderr, "[tccl] copy-out reduce-scatter failed: %s\n", cudaGetErrorString((cudaError_t)err));
     return tcclCudaError;
   }
   return tcclSuccess;
@@ -640,11 +688,19 @@ tcclResult_t run_collective(tcclGroup* g, int coll, const void* const* send, voi
   if (cur != g->device && cudaSetDevice(g->device) != cudaSuccess) return tcclCudaError;
   const int es = elem_size_of(dtype);
   if (use_copy_out(g, coll, count, es, cap)) {
-    tcclResult_t rc = coll == kAllReduce
-                          ? run_copy_out_allreduce(g, send, recv, count, dtype, op, es, stream, cap)
-                          : run_copy_out_allgather(g, send, recv, count, es, stream);
-    if (cur != g->device) cudaSetDevice(cur);
-    return rc;
+    tcclResult_t rc;
+    if (coll == kAllReduce)
+      rc = run_copy_out_allreduce(g, send, recv, count, dtype, op, es, stream, cap);
+    else if (coll == kAllGather)
+      rc = run_copy_out_allgather(g, send, recv, count, es, stream);
+    else
+      rc = run_copy_out_reduce_scatter(g, send, recv, count, dtype, op, es, stream, cap);
+    // a reduce-scatter whose buffers the register fold cannot take runs on
+    // the bulk engine below
+    if (!(coll == kReduceScatter && rc == tcclInvalidUsage)) {
+      if (cur != g->device) cudaSetDevice(cur);
+      return rc;
+    }
   }
   CachedPlan* cp = nullptr;
   tcclResult_t r = get_plan(g, coll, send, recv, count, es, cap, &cp);

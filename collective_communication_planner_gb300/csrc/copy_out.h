@@ -10,20 +10,26 @@ namespace tccl {
 constexpr int kAnchorThreads = 1024;
 constexpr uint64_t kAnchorMaxVectors = (uint64_t)1 << 28;  // per launch (4 GiB per rank)
 
-// One segment of a copy-out allreduce. All P sources and the destination
-// share their address mod 16: `head_bytes` element-wise bytes, then `nvec`
-// 16-byte vectors, then `tail_bytes` element-wise bytes.
+// One launch of the register-load fold: `njobs` independent folds of the P
+// sources. Job j reads every p.src[r] from byte offset j * job_src_stride and
+// writes p.dst[j]: one job (the copy-out allreduce segment, into the anchor's
+// receive buffer) or P jobs (a reduce-scatter, shard j into rank j's receive
+// buffer). Every source and destination of a job shares its address mod 16:
+// `head_bytes` element-wise bytes, then `nvec` 16-byte vectors, then
+// `tail_bytes` element-wise bytes, the same for every job.
 struct AnchorArgs {
-  BasePtrs<kMaxRanks> p;  // p.src[0..P-1] the sends, p.dst[0] the anchor's receive buffer
+  BasePtrs<kMaxRanks> p;
   uint32_t* sm_mask;      // SM recorder bitmap or null
   uint64_t head_bytes;
   uint64_t nvec;
   uint64_t tail_bytes;
+  uint64_t job_src_stride;
+  int njobs;
   int nranks;
 };
 
-// `vectors_per_thread` is 1 or 2 (loads in flight per thread: 8 either way).
-int launch_anchor_reduce(int dtype, int op, const AnchorArgs& a, int grid, int vectors_per_thread,
-                         void* stream);
+// Vectors each thread folds at a time: two for P = 2 and 4, one otherwise.
+int anchor_vectors_per_thread(int nranks);
+int launch_anchor_reduce(int dtype, int op, const AnchorArgs& a, int grid, void* stream);
 
 }  // namespace tccl

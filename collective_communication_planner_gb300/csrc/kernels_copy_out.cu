@@ -54,90 +54,96 @@ __device__ __forceinline__ void st_keep_v4(void* p, uint4 v, uint64_t policy) {
                  : "memory");
 }
 
-// Thread t of the grid folds vectors t, t + T, ... (T threads in all), U of
-// them at a time. With the rank count fixed at compile time (NP = 2, 4, 8)
+// For each job, thread t of the grid folds vectors t, t + T, ... (T threads
+// in all), U of them at a time. With the rank count fixed at compile time (NP = 2, 4, 8)
 // every load of a step is issued before the first add; otherwise the ranks
 // go in batches of 8 / U. Either way each accumulator receives the ranks in
 // ascending order: the plain left fold over all P ranks.
 template <int DT, int OP, int NP, int U>
 __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const __grid_constant__ AnchorArgs a) {
   constexpr int RB = NP > 0 ? NP : 8 / U;
+  constexpr int es = DT == kBF16 ? 2 : 4;
   if (threadIdx.x == 0) record_sm(a.sm_mask);
   const int P = NP > 0 ? NP : a.nranks;
-  // a launch covers at most 2^28 vectors (the host splits larger segments),
-  // so vector indices and byte offsets within it fit 32 bits
+  // a job covers at most 2^28 vectors (the host splits larger segments), so
+  // vector indices and byte offsets within it fit 32 bits
   const uint32_t nthr = gridDim.x * blockDim.x;
   const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const uint32_t nvec = static_cast<uint32_t>(a.nvec);
-  char* dst = static_cast<char*>(a.p.dst[0]) + a.head_bytes;
   // the two policy registers fit beside one vector per thread (64 registers
   // at 1024 threads), not beside two
   constexpr bool kHint = U == 1;
   const uint64_t load_policy = kHint ? l2_policy_evict_first() : 0;
   const uint64_t store_policy = kHint ? l2_policy_evict_last() : 0;
-  for (uint32_t base = gtid; base < nvec; base += nthr * U) {
-    typename StreamFold<DT, OP>::type acc[U];
-    for (int r0 = 0; r0 < P; r0 += RB) {
-      uint4 x[U][RB];
+  for (int job = 0; job < a.njobs; ++job) {
+    const uint64_t src_off = static_cast<uint64_t>(job) * a.job_src_stride + a.head_bytes;
+    char* dst = static_cast<char*>(a.p.dst[job]) + a.head_bytes;
+    for (uint32_t base = gtid; base < nvec; base += nthr * U) {
+      typename StreamFold<DT, OP>::type acc[U];
+      for (int r0 = 0; r0 < P; r0 += RB) {
+        uint4 x[U][RB];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const uint32_t v = base + u * nthr;
+#pragma unroll
+          for (int k = 0; k < RB; ++k)
+            if (v < nvec && (NP > 0 || r0 + k < P))
+              x[u][k] = ld_stream_v4<kHint>(static_cast<const char*>(a.p.src[r0 + k]) + src_off +
+                                            static_cast<uint64_t>(v) * 16, load_policy);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (base + u * nthr >= nvec) continue;
+#pragma unroll
+          for (int k = 0; k < RB; ++k) {
+            if (NP == 0 && r0 + k >= P) break;
+            if (r0 + k == 0) acc[u].init(x[u][k]);
+            else acc[u].add(x[u][k]);
+          }
+        }
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t v = base + u * nthr;
-#pragma unroll
-        for (int k = 0; k < RB; ++k)
-          if (v < nvec && (NP > 0 || r0 + k < P))
-            x[u][k] = ld_stream_v4<kHint>(static_cast<const char*>(a.p.src[r0 + k]) + a.head_bytes +
-                                   static_cast<uint64_t>(v) * 16, load_policy);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (base + u * nthr >= nvec) continue;
-#pragma unroll
-        for (int k = 0; k < RB; ++k) {
-          if (NP == 0 && r0 + k >= P) break;
-          if (r0 + k == 0) acc[u].init(x[u][k]);
-          else acc[u].add(x[u][k]);
-        }
+        if (v < nvec) st_keep_v4<kHint>(dst + static_cast<uint64_t>(v) * 16, acc[u].out(), store_policy);
       }
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint32_t v = base + u * nthr;
-      if (v < nvec) st_keep_v4<kHint>(dst + static_cast<uint64_t>(v) * 16, acc[u].out(), store_policy);
+    // the job's unaligned head and tail, one element per thread
+    const uint32_t nh = static_cast<uint32_t>(a.head_bytes / es);
+    const uint32_t nt = static_cast<uint32_t>(a.tail_bytes / es);
+    if (gtid < nh + nt) {
+      Window w;
+      w.src_sel = -1;
+      w.dst_sel = static_cast<int16_t>(job);
+      w.scalar = 1;
+      w.task = 0;
+      w.cta = -1;
+      uint64_t e = gtid;
+      const uint64_t job_off = static_cast<uint64_t>(job) * a.job_src_stride;
+      if (gtid < nh) {
+        w.src_off = job_off;
+        w.dst_off = 0;
+        w.bytes = static_cast<uint32_t>(a.head_bytes);
+      } else {
+        const uint64_t body_end = a.head_bytes + static_cast<uint64_t>(nvec) * 16;
+        w.src_off = job_off + body_end;
+        w.dst_off = body_end;
+        w.bytes = static_cast<uint32_t>(a.tail_bytes);
+        e -= nh;
+      }
+      scalar_element<kAllReduce, DT, OP, kMaxRanks>(a.p, P, w, e);
     }
-  }
-  // the unaligned head and tail, one element per thread
-  constexpr int es = DT == kBF16 ? 2 : 4;
-  const uint32_t nh = static_cast<uint32_t>(a.head_bytes / es);
-  const uint32_t nt = static_cast<uint32_t>(a.tail_bytes / es);
-  if (gtid < nh + nt) {
-    Window w;
-    w.src_sel = -1;
-    w.dst_sel = 0;
-    w.scalar = 1;
-    w.task = 0;
-    w.cta = -1;
-    uint64_t e = gtid;
-    if (gtid < nh) {
-      w.src_off = w.dst_off = 0;
-      w.bytes = static_cast<uint32_t>(a.head_bytes);
-    } else {
-      w.src_off = w.dst_off = a.head_bytes + static_cast<uint64_t>(nvec) * 16;
-      w.bytes = static_cast<uint32_t>(a.tail_bytes);
-      e -= nh;
-    }
-    scalar_element<kAllReduce, DT, OP, kMaxRanks>(a.p, P, w, e);
   }
 }
 
 template <int C, int D, int O>
-int launch_anchor_t(const AnchorArgs& a, int grid, int u, cudaStream_t st) {
+int launch_anchor_t(const AnchorArgs& a, int grid, cudaStream_t st) {
   switch (a.nranks) {
     case 2: anchor_reduce_kernel<D, O, 2, 2><<<grid, kAnchorThreads, 0, st>>>(a); break;
     case 4: anchor_reduce_kernel<D, O, 4, 2><<<grid, kAnchorThreads, 0, st>>>(a); break;
     case 8: anchor_reduce_kernel<D, O, 8, 1><<<grid, kAnchorThreads, 0, st>>>(a); break;
-    default:
-      if (u == 2) anchor_reduce_kernel<D, O, 0, 2><<<grid, kAnchorThreads, 0, st>>>(a);
-      else anchor_reduce_kernel<D, O, 0, 1><<<grid, kAnchorThreads, 0, st>>>(a);
+    default:  // other rank counts: one vector per thread (two would spill)
+      anchor_reduce_kernel<D, O, 0, 1><<<grid, kAnchorThreads, 0, st>>>(a);
   }
   return static_cast<int>(cudaGetLastError());
 }
@@ -145,11 +151,12 @@ int launch_anchor_t(const AnchorArgs& a, int grid, int u, cudaStream_t st) {
 }  // namespace
 }  // namespace dev
 
-int launch_anchor_reduce(int dtype, int op, const AnchorArgs& a, int grid, int vectors_per_thread,
-                         void* stream) {
+int anchor_vectors_per_thread(int nranks) { return (nranks == 2 || nranks == 4) ? 2 : 1; }
+
+int launch_anchor_reduce(int dtype, int op, const AnchorArgs& a, int grid, void* stream) {
   using namespace dev;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  TCCL_REDUCE_SWITCH(kAllReduce, launch_anchor_t, a, grid, vectors_per_thread, st)
+  TCCL_REDUCE_SWITCH(kAllReduce, launch_anchor_t, a, grid, st)
 }
 
 }  // namespace tccl

@@ -167,17 +167,76 @@ def test_allgather_copies_only(groups, dtype, p):
     check([to_host(b) for b in bufs], exp, f"AG in place {dtype} P={p}")
 
 
-def test_reduce_scatter_runs_on_the_bulk_engine(groups):
-    p, rc = 4, 77_777
+def reduce_scatter(g, xs, rc, dtype, op, cap=0, send_off=0, recv_off=0, in_place=False):
+    p = len(xs)
+    sends = [Guarded(p * rc, dtype, send_off) for _ in range(p)]
+    for s_, x in zip(sends, xs):
+        s_.tensor.copy_(to_device(x))
+    if in_place:
+        recv_t = [s_.tensor[r * rc:(r + 1) * rc] for r, s_ in enumerate(sends)]
+        recvs = None
+    else:
+        recvs = [Guarded(rc, dtype, recv_off) for _ in range(p)]
+        recv_t = [t.tensor for t in recvs]
+    r = tccl.tcclReduceScatter(g.handle, [s_.tensor for s_ in sends], recv_t, rc, DT_CODE[dtype],
+                               tccl.OPS[op], torch.cuda.current_stream().cuda_stream, cap)
+    assert r == tccl.tcclSuccess, tccl.tcclGetErrorString(r)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    if recvs is not None:
+        assert all(t.guards_intact() for t in recvs)
+    assert all(s_.guards_intact() for s_ in sends)
+    return [to_host(t) for t in recv_t]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("op", ["sum", "min", "max"])
+@pytest.mark.parametrize("p", [2, 3, 4, 8])
+def test_reduce_scatter_register_fold(groups, dtype, op, p):
+    """Reduce-scatter on the copy-out engine: one launch of the register-load
+    fold with one job per owner shard, no copies."""
     g = groups(p)
     reset_config(g, engine=CE)
-    xs = datagen.rank_buffers("normal_bf16", 27, p, p * rc)
-    sends = [to_device(x) for x in xs]
-    parts = [torch.empty(rc, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
-    g.reduce_scatter(sends, parts)
-    torch.cuda.synchronize()
+    rc = 40_000  # shard bytes a multiple of 16 for every dtype
+    xs = datagen.rank_buffers(KIND[dtype], 33, p, p * rc)
+    got = reduce_scatter(g, xs, rc, dtype, op, cap=5)
+    info = g.last_launch()
+    assert info["engine"] == CE and info["threads"] == 1024 and info["ctas"] <= 5, info
+    assert info["ce_copies"] == 0
+    check(got, oracle.reduce_scatter(xs, dtype, op, nthreads=0), f"RS {dtype} {op} P={p}")
+
+
+@pytest.mark.parametrize("case", ["in_place", "offset_co_aligned", "misaligned", "ragged_shard"])
+def test_reduce_scatter_layouts(groups, case):
+    """In place and co-aligned offsets (element-wise edges) take the register
+    fold; misaligned buffers and shards that are not a multiple of 16 bytes
+    take the bulk engine. All exact."""
+    p = 4
+    g = groups(p)
+    reset_config(g, engine=CE)
+    rc = 12_347 if case == "ragged_shard" else 12_352
+    xs = datagen.rank_buffers("normal_bf16", 34, p, p * rc)
+    kw = {"in_place": dict(in_place=True), "offset_co_aligned": dict(send_off=6, recv_off=6),
+          "misaligned": dict(send_off=2, recv_off=0), "ragged_shard": {}}[case]
+    got = reduce_scatter(g, xs, rc, "bf16", "sum", cap=8, **kw)
+    fold = case in ("in_place", "offset_co_aligned")
+    assert g.last_launch()["engine"] == (CE if fold else tccl.tcclEngineBulk), (case, g.last_launch())
+    check(got, oracle.reduce_scatter(xs, "bf16", "sum", nthreads=0), f"RS {case}")
+
+
+def test_reduce_scatter_auto_choice(groups):
+    p = 8
+    g = groups(p)
+    reset_config(g)
+    rc = 1 << 20  # 8 Mi bf16 per rank send buffer: 16 MiB
+    sends = [torch.ones(p * rc, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    recvs = [torch.empty(rc, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    g.reduce_scatter(sends, recvs, cta_cap=16)
+    assert g.last_launch()["engine"] == CE
+    g.reduce_scatter(sends, recvs)
     assert g.last_launch()["engine"] == tccl.tcclEngineBulk
-    check([to_host(t) for t in parts], oracle.reduce_scatter(xs, "bf16", "sum", nthreads=0), "RS")
+    torch.cuda.synchronize()
+    assert all(bool((r == p).all()) for r in recvs)
 
 
 def test_one_rank_falls_back_to_the_bulk_engine(groups):
