@@ -629,7 +629,15 @@ def sweep(args):
         row["cpu_all_s"] = cpu_time(lambda: oracle.allreduce(xs, "bf16", "sum", nthreads=0))
         row["cpu_cores"] = ncores
         emit(**row)
-        emit(**run_point("C2", g, "RS", p, rc, "bf16", "sum", sends, parts))
+        # reduce-scatter: Auto (the register fold) and the SM-only bulk engine,
+        # uncapped and under caps
+        for cap in (0, 8, 16, 32):
+            emit(**run_point("C2", g, "RS", p, rc, "bf16", "sum", sends, parts, cap=cap, sms=cap > 0))
+            set_cfg(g, ce_auto_max_cap=-1)
+            row = run_point("C2", g, "RS", p, rc, "bf16", "sum", sends, parts, cap=cap, sms=cap > 0)
+            row["variant"] = "sm_only"
+            emit(**row)
+            set_cfg(g)
         emit(**run_point("C2", g, "AG", p, rc, "bf16", "sum", parts, recvs))
         set_cfg(g, engine=tccl.tcclEngineCopyOut)  # the all-gather as copies only
         emit(**run_point("C2", g, "AG", p, rc, "bf16", "sum", parts, recvs, sms=True))

@@ -78,10 +78,13 @@ typedef enum {
                               bulk engine (within the CTA cap) into one anchor rank's receive
                               buffer only, then device-to-device copies on the group's own
                               streams carry it to the other P-1 ranks. All-gather: copies only,
-                              no kernel, no SM. Reduce-scatter has no shard-out and runs on the
-                              bulk engine. Auto picks it for capped allreduce / all-gather calls
-                              of at least 4 MiB per rank when the cap is at most
-                              ce_auto_max_cap CTAs. The segment kernel folds with 128-bit register
+                              no kernel, no SM. Reduce-scatter has no shard-out: one launch of
+                              the same register-load fold, shard j into rank j, when every
+                              buffer shares its address mod 16 and a shard is a multiple of 16
+                              bytes (else the bulk engine). Auto picks it, for calls of at least
+                              4 MiB per rank buffer, for allreduce / all-gather when the cap is
+                              at most ce_auto_max_cap CTAs, and for reduce-scatter under any cap
+                              or uncapped with P <= 4. The segment kernel folds with 128-bit register
                               loads when the send buffers and the anchor's receive buffer share
                               their address mod 16, else with the bulk engine's TMA pipeline. */
 } tcclEngine_t;

@@ -224,16 +224,21 @@ def test_reduce_scatter_layouts(groups, case):
     check(got, oracle.reduce_scatter(xs, "bf16", "sum", nthreads=0), f"RS {case}")
 
 
-def test_reduce_scatter_auto_choice(groups):
-    p = 8
+@pytest.mark.parametrize("p", [4, 8])
+def test_reduce_scatter_auto_choice(groups, p):
+    """Auto: the register fold under any cap, and uncapped for up to four
+    ranks; the bulk engine uncapped for more ranks and below 4 MiB."""
     g = groups(p)
     reset_config(g)
-    rc = 1 << 20  # 8 Mi bf16 per rank send buffer: 16 MiB
+    rc = (1 << 23) // p  # 8 Mi bf16 per rank send buffer: 16 MiB
     sends = [torch.ones(p * rc, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
     recvs = [torch.empty(rc, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
     g.reduce_scatter(sends, recvs, cta_cap=16)
     assert g.last_launch()["engine"] == CE
     g.reduce_scatter(sends, recvs)
+    assert g.last_launch()["engine"] == (CE if p <= 4 else tccl.tcclEngineBulk)
+    small = rc // 8  # 2 MiB per rank send buffer
+    g.reduce_scatter([s[:p * small] for s in sends], [r[:small] for r in recvs], cta_cap=16)
     assert g.last_launch()["engine"] == tccl.tcclEngineBulk
     torch.cuda.synchronize()
     assert all(bool((r == p).all()) for r in recvs)
