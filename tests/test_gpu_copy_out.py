@@ -244,6 +244,24 @@ def test_reduce_scatter_auto_choice(groups, p):
     assert all(bool((r == p).all()) for r in recvs)
 
 
+@pytest.mark.parametrize("p", [16, 33, 64])
+def test_many_ranks(groups, p):
+    """Rank counts with no compiled-in specialisation: the fold takes the
+    ranks in batches of 8 (allreduce and reduce-scatter), exact either way."""
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=16 * 1024)
+    xs = datagen.rank_buffers("normal_bf16", 35, p, 20_003)
+    got = allreduce(g, xs, "bf16", "sum", cap=6)
+    info = g.last_launch()
+    assert info["engine"] == CE and info["threads"] == 1024 and info["ce_copies"] == info["ce_segments"] * (p - 1)
+    check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), f"AR P={p}")
+    rc = 1024
+    ys = datagen.rank_buffers("int32", 36, p, p * rc)
+    got = reduce_scatter(g, ys, rc, "i32", "max", cap=3)
+    assert g.last_launch()["engine"] == CE
+    check(got, oracle.reduce_scatter(ys, "i32", "max", nthreads=0), f"RS P={p}")
+
+
 def test_one_rank_falls_back_to_the_bulk_engine(groups):
     g = groups(1)
     reset_config(g, engine=CE)
