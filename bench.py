@@ -490,7 +490,9 @@ def sweep(args):
     """One JSON line per configuration point of the five workloads (C1..C5):
     device time per op (CUDA events, back-to-back launches; graph-captured
     too for small messages), algbw, bus bandwidth, HBM fraction, SMs used, and
-    the CPU oracle on 1 core and on all cores for one point per workload."""
+    the CPU oracle on 1 core and on all cores for one point per workload.
+    Points whose traffic fits three times in L2 are also timed cold: L2
+    flushed before each of 20 single-launch timings (cold_l2_us)."""
     import numpy as np
     import torch
     import collective_communication_planner_gb300 as tccl
@@ -532,6 +534,23 @@ def sweep(args):
         t = ev_time(g.replay, 30.0) / reps
         del g
         return t
+
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20))
+    flush_buf = torch.empty(3 * l2_bytes // 4, dtype=torch.int32, device=dev)
+
+    def cold_time(fn, reps=20):
+        times = []
+        for _ in range(reps):
+            with torch.cuda.stream(stream):
+                flush_buf.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        times.sort()
+        return times[len(times) // 2]
 
     def cpu_time(fn, min_s=0.5):
         fn()
@@ -597,6 +616,12 @@ def sweep(args):
                    sms_used=used)
         if graph:
             row["graph_us"] = round(graph_time(fn) * 1e3, 3)
+        if hbm < 3 * l2_bytes:
+            # L2 honesty: the same call with L2 flushed (a write of 3 x L2)
+            # before each timed launch, median of 20 single-launch timings
+            cold = cold_time(fn)
+            row["cold_l2_us"] = round(cold * 1e3, 3)
+            row["cold_l2_hbm_fraction"] = round(hbm / (cold * 1e-3) / 1e9 / peak, 4)
         assert g.query_error() == 0
         return row
 
