@@ -9,8 +9,9 @@ Reported (one JSON line on rank 0):
   value      algbw = P * count * bytes / time (GB/s), device-resident inputs
   roofline   HBM bound: algorithmic bytes 2 * P * S per launch (read every
              rank's shard once, write every rank's result once) / mean
-             launch time from CUDA events on the launching stream, against
-             the measured copy bandwidth
+             launch time (the timed region between two CUDA events on the
+             launching stream, divided by its launches), against the
+             measured copy bandwidth
   e2e        same metric through the C ABI with the inputs copied from pinned
              host memory and every result copied back, inside the timed region
   cpu_baseline  the CPU oracle (threaded, same per-element order) on the
@@ -283,20 +284,24 @@ def run_ours(args, w, rank, world, dist):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    # the timed region: K back-to-back launches between two events on the
+    # launching stream. Only this kernel runs there, so the region divided by
+    # K is its average launch duration, inter-launch gaps included (an event
+    # pair around every launch would add gaps of its own).
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     t_start = time.time()
     with torch.cuda.stream(stream):
+        ev[0].record(stream)
         for i in range(args.steps):
-            ev[2 * i].record(stream)
             step()
-            ev[2 * i + 1].record(stream)
+        ev[1].record(stream)
     torch.cuda.synchronize()
     t_end = time.time()
     if dist is not None:
         dist.barrier()
     sampler.stop()
-    total_ms = ev[0].elapsed_time(ev[-1])
-    launch_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)) / args.steps
+    total_ms = ev[0].elapsed_time(ev[1])
+    launch_ms = total_ms / args.steps
     clocks = sampler.summary(t_soak, t_end)
 
     total_ms = replica_time(dist, total_ms)
