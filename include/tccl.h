@@ -199,6 +199,11 @@ tcclResult_t tcclGroupSetConfig(tcclGroup_t g, const tcclConfig_t* cfg);
  * into a CUDA graph on `stream`. Calls on different user streams that share
  * a group share those copy streams too (their order between such calls is
  * the order of the calls).
+ * The first call of a new shape (count, datatype, cap, the buffers' address
+ * mod 16) plans it and, for the bulk engine, uploads its tables with a
+ * synchronous copy; the first copy-out call creates the group's copy streams
+ * and events. Make those first calls before capturing a CUDA graph; later
+ * calls of the same shape allocate nothing and can be captured.
  */
 tcclResult_t tcclAllReduce(tcclGroup_t g, const void* const sendbufs[], void* const recvbufs[],
                            size_t count, tcclDataType_t datatype, tcclRedOp_t op,
