@@ -9,7 +9,25 @@ namespace dev {
 
 template <int C, int D, int O>
 int launch_bulk_t(const BulkArgs& a, const LaunchShape& s, cudaStream_t st) {
-  bulk_kernel<C, D, O><<<s.grid, s.threads, s.smem, st>>>(a);
+  if (!s.early_launch) {
+    bulk_kernel<C, D, O><<<s.grid, s.threads, s.smem, st>>>(a);
+    return static_cast<int>(cudaGetLastError());
+  }
+  // programmatic dependent launch: the CTAs may become resident while the
+  // stream's previous kernel drains; they wait (griddepcontrol.wait) for it
+  // to finish before touching global memory
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(s.threads));
+  cfg.dynamicSmemBytes = s.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, bulk_kernel<C, D, O>, a);
+  if (e != cudaSuccess) return static_cast<int>(e);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -119,6 +119,7 @@ struct LaunchShape {
   int rank_streamed = 0;
   int prefetch_chunks = 0;
   int load_evict_first = 0;
+  int early_launch = 0;  // bulk engine, uncapped: programmatic dependent launch
   size_t smem = 0;
 };
 

@@ -615,8 +615,15 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
     mbar_init(&h.never, 1);
     h.abort_flag = 0;
     fence_mbar_init();
-    record_sm(a.sm_mask);
   }
+  // An early (programmatic dependent) launch gets here while the stream's
+  // previous kernel may still run: every global access comes after this
+  // wait, which returns once that kernel has finished and its writes are
+  // visible (at once for an ordinary launch). The next launch may then be
+  // scheduled: its CTAs take this SM only after this CTA exits.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) record_sm(a.sm_mask);
   __syncthreads();
 
   // ---------------- producer: one thread chooses the chunks and issues every

@@ -456,6 +456,10 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
   sh.release_lag = std::max(1, std::min(7, stages / 2));
   sh.prefetch_chunks = cfg.prefetch_chunks;
   sh.load_evict_first = cfg.load_policy == 1 ? 1 : 0;
+  // an uncapped launch may start behind the previous kernel on the stream
+  // (its CTAs wait before touching global memory); a capped one never holds
+  // SMs beyond its cap
+  sh.early_launch = capped ? 0 : 1;
   sh.smem = 1024 + (size_t)stages * nsrc * chunk + (size_t)result_slots * chunk;
 
   build_chunk_tables(wins, chunk, 1, max_ctas_total, cta_cap, cfg, es, capped, out);
