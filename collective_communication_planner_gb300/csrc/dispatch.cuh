@@ -8,28 +8,7 @@ namespace tccl {
 namespace dev {
 
 template <int C, int D, int O>
-int launch_bulk_t(const BulkArgs& a, const LaunchShape& s, cudaStream_t st) {
-  if (!s.early_launch) {
-    bulk_kernel<C, D, O><<<s.grid, s.threads, s.smem, st>>>(a);
-    return static_cast<int>(cudaGetLastError());
-  }
-  // programmatic dependent launch: the CTAs may become resident while the
-  // stream's previous kernel drains; they wait (griddepcontrol.wait) for it
-  // to finish before touching global memory
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
-  cfg.blockDim = dim3(static_cast<unsigned>(s.threads));
-  cfg.dynamicSmemBytes = s.smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, bulk_kernel<C, D, O>, a);
-  if (e != cudaSuccess) return static_cast<int>(e);
-  return static_cast<int>(cudaGetLastError());
-}
+int launch_bulk_t(const BulkArgs& a, const LaunchShape& s, cudaStream_t st);
 
 template <int C, int D, int O>
 int launch_reduce_t(const BulkArgs& a, const LaunchShape& s, cudaStream_t st) {
@@ -67,14 +46,38 @@ int set_bulk_smem(size_t bytes) {
   return static_cast<int>(e);
 }
 
+// `kernel<<<…>>>(args)` or, with s.early_launch, the same launch with
+// programmatic stream serialisation (the kernel waits in
+// griddepcontrol.wait before touching global memory)
+template <typename Kernel, typename Args>
+int launch_maybe_early(Kernel kernel, const Args& a, const LaunchShape& s, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(s.threads));
+  cfg.dynamicSmemBytes = s.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = s.early_launch ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  return static_cast<int>(cudaGetLastError());
+}
+
+// bulk engine: an uncapped launch starts early (its CTAs take each SM as the
+// previous kernel's CTA there exits); a capped one is an ordinary launch
+template <int C, int D, int O>
+int launch_bulk_t(const BulkArgs& a, const LaunchShape& s, cudaStream_t st) {
+  return launch_maybe_early(bulk_kernel<C, D, O>, a, s, st);
+}
+
 template <int C, int D, int O, int MAXR, int MAXW>
 int launch_small_t(int engine, const void* args, const LaunchShape& s, cudaStream_t st) {
   const auto& a = *static_cast<const SmallArgs<MAXR, MAXW>*>(args);
-  if (engine == kEngineWarp)
-    small_kernel<C, D, O, MAXR, MAXW, true><<<s.grid, s.threads, 0, st>>>(a);
-  else
-    small_kernel<C, D, O, MAXR, MAXW, false><<<s.grid, s.threads, 0, st>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  if (engine == kEngineWarp) return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, true>, a, s, st);
+  return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, false>, a, s, st);
 }
 
 template <int C, int D, int O>

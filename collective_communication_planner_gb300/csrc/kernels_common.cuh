@@ -976,6 +976,10 @@ __device__ __forceinline__ int find_window(const uint64_t* prefix, int nwin, uin
 
 template <int COLL, int DT, int OP, int MAXR, int MAXW, bool SHFL>
 __global__ void __launch_bounds__(256) small_kernel(const __grid_constant__ SmallArgs<MAXR, MAXW> a) {
+  // an early (programmatic dependent) launch waits here for the stream's
+  // previous kernel before any global access (see bulk_kernel)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) record_sm(a.sm_mask);
   const int P = a.nranks;
   const uint64_t nvec = a.vec_prefix[a.nwin];

@@ -383,6 +383,7 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
     sh.grid = (int)std::max<uint64_t>(1, std::min(blocks, cap));
     sh.threads = threads;
     sh.smem = 0;
+    sh.early_launch = capped ? 0 : 1;
     return true;
   }
 
