@@ -564,7 +564,7 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
       uint64_t grid = std::max<uint64_t>(1, (aa.nvec + per_cta - 1) / per_cta);
       grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
       fast_grid = std::max(fast_grid, (int)grid);
-      err = launch_anchor_reduce(dtype, op, aa, (int)grid, stream);
+      err = launch_anchor_reduce(dtype, op, aa, (int)grid, cap <= 0, stream);
     } else {
       CachedPlan* cp = (sgi == nseg - 1 && tail) ? tail : full;
       err = launch_plan(g, cp, kAllReduce, dtype, op, s_ptr.data(), r_ptr.data(), es, stream);
@@ -632,7 +632,7 @@ tcclResult_t run_copy_out_reduce_scatter(tcclGroup* g, const void* const* send, 
   const uint64_t per_cta = (uint64_t)kAnchorThreads * anchor_vectors_per_thread(P);
   uint64_t grid = std::max<uint64_t>(1, (aa.nvec * P + per_cta - 1) / per_cta);
   grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
-  const int err = launch_anchor_reduce(dtype, op, aa, (int)grid, stream);
+  const int err = launch_anchor_reduce(dtype, op, aa, (int)grid, cap <= 0, stream);
   std::memset(&g->last, 0, sizeof(g->last));
   g->last.engine = kEngineCopyOut;
   g->last.store_mode = kStoreVec;

@@ -30,6 +30,9 @@ struct AnchorArgs {
 
 // Vectors each thread folds at a time: two for P = 2 and 4, one otherwise.
 int anchor_vectors_per_thread(int nranks);
-int launch_anchor_reduce(int dtype, int op, const AnchorArgs& a, int grid, void* stream);
+// early: programmatic dependent launch (uncapped calls only: a capped call
+// must not hold SMs beyond its cap while it waits)
+int launch_anchor_reduce(int dtype, int op, const AnchorArgs& a, int grid, bool early,
+                         void* stream);
 
 }  // namespace tccl

@@ -63,6 +63,10 @@ template <int DT, int OP, int NP, int U>
 __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const __grid_constant__ AnchorArgs a) {
   constexpr int RB = NP > 0 ? NP : 8 / U;
   constexpr int es = DT == kBF16 ? 2 : 4;
+  // an early (programmatic dependent) launch waits here for the stream's
+  // previous kernel before any global access
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) record_sm(a.sm_mask);
   const int P = NP > 0 ? NP : a.nranks;
   // a job covers at most 2^28 vectors (the host splits larger segments), so
@@ -137,15 +141,19 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
 }
 
 template <int C, int D, int O>
-int launch_anchor_t(const AnchorArgs& a, int grid, cudaStream_t st) {
+int launch_anchor_t(const AnchorArgs& a, int grid, bool early, cudaStream_t st) {
+  LaunchShape s;
+  s.grid = grid;
+  s.threads = kAnchorThreads;
+  s.smem = 0;
+  s.early_launch = early ? 1 : 0;
   switch (a.nranks) {
-    case 2: anchor_reduce_kernel<D, O, 2, 2><<<grid, kAnchorThreads, 0, st>>>(a); break;
-    case 4: anchor_reduce_kernel<D, O, 4, 2><<<grid, kAnchorThreads, 0, st>>>(a); break;
-    case 8: anchor_reduce_kernel<D, O, 8, 1><<<grid, kAnchorThreads, 0, st>>>(a); break;
+    case 2: return launch_maybe_early(anchor_reduce_kernel<D, O, 2, 2>, a, s, st);
+    case 4: return launch_maybe_early(anchor_reduce_kernel<D, O, 4, 2>, a, s, st);
+    case 8: return launch_maybe_early(anchor_reduce_kernel<D, O, 8, 1>, a, s, st);
     default:  // other rank counts: one vector per thread (two would spill)
-      anchor_reduce_kernel<D, O, 0, 1><<<grid, kAnchorThreads, 0, st>>>(a);
+      return launch_maybe_early(anchor_reduce_kernel<D, O, 0, 1>, a, s, st);
   }
-  return static_cast<int>(cudaGetLastError());
 }
 
 }  // namespace
@@ -153,10 +161,11 @@ int launch_anchor_t(const AnchorArgs& a, int grid, cudaStream_t st) {
 
 int anchor_vectors_per_thread(int nranks) { return (nranks == 2 || nranks == 4) ? 2 : 1; }
 
-int launch_anchor_reduce(int dtype, int op, const AnchorArgs& a, int grid, void* stream) {
+int launch_anchor_reduce(int dtype, int op, const AnchorArgs& a, int grid, bool early,
+                         void* stream) {
   using namespace dev;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  TCCL_REDUCE_SWITCH(kAllReduce, launch_anchor_t, a, grid, st)
+  TCCL_REDUCE_SWITCH(kAllReduce, launch_anchor_t, a, grid, early, st)
 }
 
 }  // namespace tccl
