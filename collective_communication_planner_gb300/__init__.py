@@ -106,6 +106,9 @@ def _open():
                                 ctypes.POINTER(ctypes.c_int64), i, ctypes.POINTER(i),
                                 ctypes.POINTER(i), ctypes.POINTER(tcclLaunchInfo_t)]),
         "tcclGroupInjectWaitTimeout": (i, [vp, i, ctypes.c_double]),
+        "tcclCopyOutInspect": (i, [i, i, pvp, pvp, sz, i, i, i, ctypes.POINTER(tcclConfig_t),
+                                   ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i),
+                                   ctypes.POINTER(sz)]),
         "tcclAllReduceNoAlloc": (i, [i, pvp, pvp, sz, i, i, vp, i]),
         "tcclAllReduceRMSNorm": (i, [vp, pvp, pvp, sz, sz, vp, ctypes.c_float, i, vp, i]),
         "tcclReshard": (i, [vp, pvp, ctypes.POINTER(tcclLayout_t), pvp,
@@ -128,7 +131,7 @@ _lib = _open()
 EXPORTED = ("tcclGetErrorString", "tcclGetVersion", "tcclGroupCreate", "tcclGroupDestroy",
             "tcclGroupGetConfig", "tcclGroupSetConfig", "tcclAllReduce", "tcclReduceScatter",
             "tcclAllGather", "tcclGroupQueryError", "tcclGetLastLaunchInfo",
-            "tcclGroupRecordSms", "tcclGroupReadSmRecord", "tcclPlanInspect",
+            "tcclGroupRecordSms", "tcclGroupReadSmRecord", "tcclPlanInspect", "tcclCopyOutInspect",
             "tcclGroupInjectWaitTimeout", "tcclAllReduceNoAlloc", "tcclReshard",
             "tcclReshardInspect", "tcclAllReduceRMSNorm")
 
@@ -300,6 +303,20 @@ def tcclPlanInspect(coll, nranks, sendbufs, recvbufs, count, datatype, cta_cap=0
     keys = ("cta", "src_sel", "src_off", "dst_sel", "dst_off", "bytes", "scalar", "task")
     wins = [dict(zip(keys, buf[8 * i:8 * i + 8])) for i in range(min(nw.value, max_windows))]
     return r, wins, nt.value, info
+
+
+def tcclCopyOutInspect(coll, nranks, sendbufs, recvbufs, count, datatype, cta_cap=0,
+                       sm_count=152, cfg=None):
+    """The copy-out engine's decisions on the host only. Returns (result,
+    copy_out, register_fold, segments, segment_elems)."""
+    sp, _k1 = _ptr_array(sendbufs)
+    rp, _k2 = _ptr_array(recvbufs)
+    co, rf, ns = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    se = ctypes.c_size_t()
+    r = _lib.tcclCopyOutInspect(coll, nranks, sp, rp, count, datatype, cta_cap, sm_count,
+                                ctypes.byref(cfg) if cfg is not None else None, ctypes.byref(co),
+                                ctypes.byref(rf), ctypes.byref(ns), ctypes.byref(se))
+    return r, co.value, rf.value, ns.value, se.value
 
 
 # ---------------------------------------------------------------- torch-facing wrapper

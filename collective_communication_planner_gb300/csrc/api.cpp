@@ -427,27 +427,14 @@ int launch_plan(tcclGroup* g, CachedPlan* cp, int coll, int dtype, int op,
   return launch_small_ag(dtype, op, low.shape.engine, low.size_class, buf.data(), low.shape, stream);
 }
 
-constexpr int kMaxCeSegments = 64;
-constexpr size_t kCeAutoMinBytes = (size_t)4 << 20;
-
-// Auto's choice of the copy-out engine: a capped allreduce or all-gather
-// whose per-rank buffer is large, with a cap small enough that the SMs, not
-// HBM, would bound the SM-only path.
 bool use_copy_out(const tcclGroup* g, int coll, size_t count, int es, int cap) {
-  if (g->nranks < 2) return false;
-  if (g->cfg.engine == kEngineCopyOut) return true;
-  if (g->cfg.engine != kEngineAuto || g->cfg.ce_auto_max_cap < 0) return false;
-  const size_t per_rank =
-      count * (size_t)es * (coll == kAllReduce ? 1 : (size_t)g->nranks);  // RS: send; AG: recv
-  if (per_rank < kCeAutoMinBytes) return false;
-  // GB300 sweeps: the reduce-scatter's register fold beats the TMA pipeline
-  // under every cap, and uncapped for up to four ranks (0.956 vs 0.912 of
-  // the HBM peak at P = 4, 64 MiB; 0.982 vs 1.045 at P = 8)
-  if (coll == kReduceScatter) return cap > 0 || g->nranks <= 4;
-  if (cap <= 0) return false;
-  // allreduce / all-gather (P = 2, 4, 8): copy-out is ahead up to a cap of 48 of 152 SMs
-  const int max_cap = g->cfg.ce_auto_max_cap > 0 ? g->cfg.ce_auto_max_cap : g->dev.sm_count * 5 / 16;
-  return cap <= max_cap;
+  return copy_out_chosen(g->cfg, g->dev.sm_count, g->nranks, coll, count, es, cap);
+}
+
+std::vector<uint8_t> mod16_of(int n, const void* const* p) {
+  std::vector<uint8_t> m(n);
+  for (int k = 0; k < n; ++k) m[k] = (uint8_t)((uintptr_t)p[k] & 15);
+  return m;
 }
 
 tcclResult_t ensure_ce_resources(tcclGroup* g, int segments) {
@@ -502,16 +489,9 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
                                     int cap) {
   const int P = g->nranks;
   const int anchor = 0;
-  // at least four segments when that keeps them >= 4 MiB, none above
-  // ce_segment_bytes: the copies of the first segment and the kernel of the
-  // last one do not overlap anything, so they should be short
-  const size_t align = 256 / (size_t)es;
-  const size_t quarter = std::max<size_t>((size_t)4 << 20, (count * es + 3) / 4);
-  const size_t seg_bytes = std::min<size_t>(g->cfg.ce_segment_bytes, quarter);
-  size_t seg = std::max<size_t>(align, (seg_bytes / (size_t)es) / align * align);
-  if ((count + seg - 1) / seg > (size_t)kMaxCeSegments)
-    seg = ((count + kMaxCeSegments - 1) / kMaxCeSegments + align - 1) / align * align;
-  const int nseg = (int)((count + seg - 1) / seg);
+  size_t seg = 0;
+  int nseg = 0;
+  copy_out_segments(g->cfg, count, es, &seg, &nseg);
   tcclResult_t r = ensure_ce_resources(g, nseg);
   if (r != tcclSuccess) return r;
   std::vector<const void*> s_ptr(P);
@@ -523,8 +503,8 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
     }
   };
   const uintptr_t mod = (uintptr_t)recv[anchor] & 15;
-  bool fast = seg * (size_t)es / 16 < kAnchorMaxVectors;
-  for (int k = 0; k < P; ++k) fast = fast && (((uintptr_t)send[k] & 15) == mod);
+  const bool fast = register_fold_ok(kAllReduce, P, mod16_of(P, send).data(),
+                                     mod16_of(P, (const void* const*)recv).data(), count, es, seg);
   const size_t tail_n = count - (size_t)(nseg - 1) * seg;
   // TMA fallback: both plans (full segments, ragged tail) before any launch,
   // since a new plan's table upload is synchronous
@@ -612,10 +592,9 @@ tcclResult_t run_copy_out_reduce_scatter(tcclGroup* g, const void* const* send, 
   const int P = g->nranks;
   const size_t bytes = rc * (size_t)es;
   const uintptr_t mod = (uintptr_t)recv[0] & 15;
-  bool ok = bytes % 16 == 0 && bytes / 16 < kAnchorMaxVectors;
-  for (int k = 0; k < P; ++k)
-    ok = ok && (((uintptr_t)send[k] & 15) == mod) && (((uintptr_t)recv[k] & 15) == mod);
-  if (!ok) return tcclInvalidUsage;
+  if (!register_fold_ok(kReduceScatter, P, mod16_of(P, send).data(),
+                        mod16_of(P, (const void* const*)recv).data(), rc, es, 0))
+    return tcclInvalidUsage;
   AnchorArgs aa;
   std::memset(&aa, 0, sizeof(aa));
   aa.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
@@ -1113,6 +1092,40 @@ tcclResult_t tcclReshardInspect(const tcclLayout_t* src, const tcclLayout_t* dst
 tcclResult_t tcclGroupInjectWaitTimeout(tcclGroup_t g, int enable, double timeout_ms) {
   if (!g || (enable && timeout_ms <= 0)) return tcclInvalidArgument;
   g->inject_ns = enable ? (uint64_t)(timeout_ms * 1e6) : 0;
+  return tcclSuccess;
+}
+
+tcclResult_t tcclCopyOutInspect(int coll, int nranks, const void* const sendbufs[],
+                                void* const recvbufs[], size_t count, tcclDataType_t datatype,
+                                int cta_cap, int sm_count, const tcclConfig_t* cfg, int* copy_out,
+                                int* register_fold, int* segments, size_t* segment_elems) {
+  if (!copy_out || !register_fold || !segments || !segment_elems || sm_count < 1)
+    return tcclInvalidArgument;
+  if (cfg && !config_ok(*cfg)) return tcclInvalidArgument;
+  tcclResult_t v = (tcclResult_t)validate_collective_args(coll, nranks, sendbufs, recvbufs, count, datatype, 0);
+  if (v != tcclSuccess) return v;
+  *copy_out = *register_fold = *segments = 0;
+  *segment_elems = 0;
+  if (count == 0 || is_noop(coll, nranks, sendbufs, recvbufs)) return tcclSuccess;
+  const int es = elem_size_of(datatype);
+  const Config c = cfg ? from_public(*cfg) : resolve_config(Config());
+  if (!copy_out_chosen(c, sm_count, nranks, coll, count, es, cta_cap)) return tcclSuccess;
+  *copy_out = 1;
+  const std::vector<uint8_t> sm = mod16_of(nranks, sendbufs);
+  const std::vector<uint8_t> rm = mod16_of(nranks, (const void* const*)recvbufs);
+  if (coll == kAllReduce) {
+    size_t seg = 0;
+    int nseg = 0;
+    copy_out_segments(c, count, es, &seg, &nseg);
+    *segments = nseg;
+    *segment_elems = seg;
+    *register_fold = register_fold_ok(coll, nranks, sm.data(), rm.data(), count, es, seg) ? 1 : 0;
+  } else if (coll == kReduceScatter) {
+    *register_fold = register_fold_ok(coll, nranks, sm.data(), rm.data(), count, es, 0) ? 1 : 0;
+    *copy_out = *register_fold;  // otherwise the bulk engine runs it
+    *segments = *register_fold;
+    *segment_elems = *register_fold ? count : 0;
+  }
   return tcclSuccess;
 }
 

@@ -8,7 +8,6 @@
 namespace tccl {
 
 constexpr int kAnchorThreads = 1024;
-constexpr uint64_t kAnchorMaxVectors = (uint64_t)1 << 28;  // per launch (4 GiB per rank)
 
 // One launch of the register-load fold: `njobs` independent folds of the P
 // sources. Job j reads every p.src[r] from byte offset j * job_src_stride and

@@ -163,6 +163,50 @@ Config resolve_config(const Config& in) {
   return c;
 }
 
+bool copy_out_chosen(const Config& c, int sm_count, int nranks, int coll, size_t count, int es,
+                     int cap) {
+  if (nranks < 2) return false;
+  if (c.engine == kEngineCopyOut) return true;
+  if (c.engine != kEngineAuto || c.ce_auto_max_cap < 0) return false;
+  const size_t per_rank = count * (size_t)es * (coll == kAllReduce ? 1 : (size_t)nranks);
+  if (per_rank < kCeAutoMinBytes) return false;
+  // GB300 sweeps: the reduce-scatter's register fold beats the TMA pipeline
+  // under every cap, and uncapped for up to four ranks (0.995 vs 0.959 of
+  // the HBM peak at P = 4, 64 MiB; 0.982 vs 1.045 at P = 8)
+  if (coll == kReduceScatter) return cap > 0 || nranks <= 4;
+  if (cap <= 0) return false;
+  // allreduce / all-gather (P = 2, 4, 8): copy-out is ahead up to a cap of 48 of 152 SMs
+  const int max_cap = c.ce_auto_max_cap > 0 ? c.ce_auto_max_cap : sm_count * 5 / 16;
+  return cap <= max_cap;
+}
+
+void copy_out_segments(const Config& c, size_t count, int es, size_t* seg_elems, int* nseg) {
+  // the copies of the first segment and the fold of the last one overlap
+  // nothing, so segments should be short; but each costs a launch
+  const size_t align = 256 / (size_t)es;
+  const size_t quarter = std::max<size_t>((size_t)4 << 20, (count * es + 3) / 4);
+  const size_t seg_bytes = std::min<size_t>(c.ce_segment_bytes, quarter);
+  size_t seg = std::max<size_t>(align, (seg_bytes / (size_t)es) / align * align);
+  if ((count + seg - 1) / seg > (size_t)kMaxCeSegments)
+    seg = ((count + kMaxCeSegments - 1) / kMaxCeSegments + align - 1) / align * align;
+  *seg_elems = seg;
+  *nseg = (int)((count + seg - 1) / seg);
+}
+
+bool register_fold_ok(int coll, int nranks, const uint8_t* send_mod16, const uint8_t* recv_mod16,
+                      size_t count, int es, size_t seg_elems) {
+  const uint8_t mod = recv_mod16[0];
+  for (int k = 0; k < nranks; ++k) {
+    if (send_mod16[k] != mod) return false;
+    if (coll == kReduceScatter && recv_mod16[k] != mod) return false;
+  }
+  if (coll == kReduceScatter) {
+    const size_t bytes = count * (size_t)es;
+    return bytes % 16 == 0 && bytes / 16 < kFoldMaxVectors;
+  }
+  return seg_elems * (size_t)es / 16 < kFoldMaxVectors;
+}
+
 // Body windows -> one chunk sequence (prefix table), element-wise windows cut
 // into pieces and bound to CTAs, and the grid size. Each CTA runs `lanes`
 // independent chunk streams (the TMA-reduce engine) or one (the bulk engine).

@@ -85,6 +85,36 @@ struct Config {
 // Fills zero fields with the library defaults.
 Config resolve_config(const Config& in);
 
+// ---- copy-out engine decisions (host only; the kernels and copies live in
+// api.cpp and kernels_copy_out.cu)
+constexpr int kMaxCeSegments = 64;
+constexpr size_t kCeAutoMinBytes = (size_t)4 << 20;
+constexpr uint64_t kFoldMaxVectors = (uint64_t)1 << 28;  // per launch job, 32-bit indices
+
+// Whether a call runs on the copy-out engine: always when the group's engine
+// is copy-out (P >= 2); under Auto, for calls of at least 4 MiB per rank
+// buffer (allreduce: the buffer; reduce-scatter: the send buffer; all-gather:
+// the receive buffer): allreduce / all-gather when 0 < cap <= ce_auto_max_cap
+// (default 5/16 of the SMs), reduce-scatter under any cap or uncapped with
+// P <= 4. ce_auto_max_cap < 0 turns Auto's choice off.
+bool copy_out_chosen(const Config& c, int sm_count, int nranks, int coll, size_t count, int es,
+                     int cap);
+
+// Segments of a copy-out allreduce of `count` elements: at most
+// ce_segment_bytes per rank, at least four where each stays >= 4 MiB, at most
+// kMaxCeSegments, offsets multiples of 256 bytes. *seg_elems is the length of
+// every segment but the last (which holds the rest).
+void copy_out_segments(const Config& c, size_t count, int es, size_t* seg_elems, int* nseg);
+
+// Whether the register-load fold takes a copy-out call (else the TMA
+// pipeline, or for reduce-scatter the bulk engine): every send buffer shares
+// its address mod 16 with the receive buffer(s) written (allreduce: rank 0's;
+// reduce-scatter: every rank's, and a shard must be a multiple of 16 bytes),
+// and a launch job stays below kFoldMaxVectors vectors. `seg_elems` is the
+// allreduce's segment length (ignored for reduce-scatter).
+bool register_fold_ok(int coll, int nranks, const uint8_t* send_mod16, const uint8_t* recv_mod16,
+                      size_t count, int es, size_t seg_elems);
+
 struct Lowered {
   LaunchShape shape;
   std::vector<Window> win;           // bulk: body windows, then scalar windows by CTA;

@@ -275,6 +275,27 @@ tcclResult_t tcclPlanInspect(int coll, int nranks, const void* const sendbufs[],
                              int* n_windows, int* n_tasks, tcclLaunchInfo_t* info);
 
 /*
+ * Host-only view of the copy-out engine's decisions (no GPU needed), for a
+ * call with these arguments on a device with `sm_count` SMs under `cfg`
+ * (null: the defaults). The buffer addresses are only used for their
+ * alignment and overlap. Outputs:
+ *   *copy_out       1 if the call would run on the copy-out engine;
+ *   *register_fold  1 if its shard-in would be the register-load fold
+ *                   (0: the TMA pipeline for an allreduce; a reduce-scatter
+ *                   the fold cannot take runs on the bulk engine, and then
+ *                   *copy_out is 0 too);
+ *   *segments, *segment_elems  an allreduce's segments and the length of all
+ *                   but the last; 1 and `count` for a reduce-scatter on the
+ *                   fold; 0 otherwise (an all-gather is copies only).
+ * count == 0 and no-op calls report 0 everywhere. Argument errors are
+ * reported exactly as the collective call would.
+ */
+tcclResult_t tcclCopyOutInspect(int coll, int nranks, const void* const sendbufs[],
+                                void* const recvbufs[], size_t count, tcclDataType_t datatype,
+                                int cta_cap, int sm_count, const tcclConfig_t* cfg, int* copy_out,
+                                int* register_fold, int* segments, size_t* segment_elems);
+
+/*
  * Test hook for the bounded-wait error path: while enabled, each bulk-engine
  * launch makes its first CTA wait on a barrier that nothing signals, with a
  * `timeout_ms` bound; the CTA then records tcclDeviceTimeout, skips its

@@ -1,0 +1,147 @@
+"""The copy-out engine's host decisions, checked through tcclCopyOutInspect
+(no GPU needed): when Auto picks the engine, how an allreduce is cut into
+segments, and when the register-load fold takes the shard-in."""
+import itertools
+
+import pytest
+
+import collective_communication_planner_gb300 as tccl
+
+AR, RS, AG = tccl.COLL_ALLREDUCE, tccl.COLL_REDUCE_SCATTER, tccl.COLL_ALLGATHER
+BF16, F32 = tccl.tcclBfloat16, tccl.tcclFloat32
+ES = {BF16: 2, F32: 4}
+MiB = 1 << 20
+BASE = 1 << 40
+SMS = 152
+
+
+def bufs(p, send_mis=0, recv_mis=0):
+    stride = 1 << 36
+    send = [BASE + 2 * r * stride + (send_mis[r] if isinstance(send_mis, list) else send_mis) for r in range(p)]
+    recv = [BASE + (2 * r + 1) * stride + (recv_mis[r] if isinstance(recv_mis, list) else recv_mis)
+            for r in range(p)]
+    return send, recv
+
+
+def inspect(coll, p, count, dt=BF16, cap=0, cfg=None, send_mis=0, recv_mis=0, sm_count=SMS):
+    send, recv = bufs(p, send_mis, recv_mis)
+    r, co, rf, ns, se = tccl.tcclCopyOutInspect(coll, p, send, recv, count, dt, cap, sm_count, cfg)
+    assert r == tccl.tcclSuccess, tccl.tcclGetErrorString(r)
+    return co, rf, ns, se
+
+
+def config(**kw):
+    c = tccl.tcclConfig_t()
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def per_rank_bytes(coll, p, count, es):
+    return count * es * (1 if coll == AR else p)
+
+
+@pytest.mark.parametrize("coll,p,mib,cap", list(itertools.product(
+    [AR, RS, AG], [1, 2, 4, 8], [2, 4, 64], [0, 8, 47, 48])))
+def test_auto_choice(coll, p, mib, cap):
+    """Auto's rule: P >= 2 and at least 4 MiB per rank buffer; allreduce and
+    all-gather under a cap of at most 5/16 of the SMs (47 of 152);
+    reduce-scatter under any cap, or uncapped for P <= 4."""
+    es = 2
+    count = mib * MiB // es // (1 if coll == AR else p)
+    co, rf, ns, se = inspect(coll, p, count, cap=cap)
+    big = per_rank_bytes(coll, p, count, es) >= 4 * MiB
+    if p < 2 or not big:
+        want = False
+    elif coll == RS:
+        want = cap > 0 or p <= 4
+    else:
+        want = 0 < cap <= SMS * 5 // 16
+    assert bool(co) == want, (coll, p, mib, cap, co)
+    if not co:
+        assert (rf, ns, se) == (0, 0, 0)
+
+
+def test_engine_setting_and_auto_limit():
+    p, count = 8, 64 * MiB // 2
+    # copy-out chosen explicitly: every allreduce / all-gather with P >= 2
+    assert inspect(AR, p, 1000, cfg=config(engine=tccl.tcclEngineCopyOut))[0] == 1
+    assert inspect(AG, p, 1000, cfg=config(engine=tccl.tcclEngineCopyOut))[0] == 1
+    assert inspect(AR, 1, count, cfg=config(engine=tccl.tcclEngineCopyOut))[0] == 0
+    # another explicit engine: never
+    assert inspect(AR, p, count, cap=16, cfg=config(engine=tccl.tcclEngineBulk))[0] == 0
+    # Auto switched off, or with a wider limit
+    assert inspect(AR, p, count, cap=16, cfg=config(ce_auto_max_cap=-1))[0] == 0
+    assert inspect(RS, p, count // p, cap=16, cfg=config(ce_auto_max_cap=-1))[0] == 0
+    assert inspect(AR, p, count, cap=100, cfg=config(ce_auto_max_cap=100))[0] == 1
+    assert inspect(AR, p, count, cap=101, cfg=config(ce_auto_max_cap=100))[0] == 0
+    # the limit scales with the device: 132 SMs -> 132 * 5 // 16 = 41
+    assert inspect(AR, p, count, cap=41, sm_count=132)[0] == 1
+    assert inspect(AR, p, count, cap=42, sm_count=132)[0] == 0
+
+
+@pytest.mark.parametrize("dt", [BF16, F32])
+@pytest.mark.parametrize("count_bytes", [4 * MiB + 16, 16 * MiB, 64 * MiB, 128 * MiB + 512,
+                                         1024 * MiB, 3 * 1024 * MiB + 256])
+@pytest.mark.parametrize("seg_cfg", [0, 8 * MiB, 4096])
+def test_segments(dt, count_bytes, seg_cfg):
+    """Segments cover the call, start at multiples of 256 bytes, are at most
+    ce_segment_bytes (32 MiB by default) unless that would need more than 64
+    of them, and number at least four while each stays >= 4 MiB."""
+    es = ES[dt]
+    count = count_bytes // es
+    cfg = config(engine=tccl.tcclEngineCopyOut, ce_segment_bytes=seg_cfg)
+    co, rf, ns, se = inspect(AR, 4, count, dt=dt, cfg=cfg)
+    assert co == 1 and rf == 1
+    assert (se * es) % 256 == 0 and se > 0
+    assert ns == -(-count // se) and 1 <= ns <= 64
+    cap_bytes = seg_cfg or 32 * MiB
+    if ns < 64:  # not grown to respect the 64-segment bound
+        assert se * es == 256 or se * es <= min(cap_bytes, max(4 * MiB, -(-count_bytes // 4)))
+    if cap_bytes >= 4 * MiB and count_bytes >= 16 * MiB:
+        assert ns >= 4 and se * es >= min(4 * MiB, cap_bytes)
+
+
+def test_segment_count_bound_grows_segments():
+    co, rf, ns, se = inspect(AR, 2, (1 << 30), dt=F32, cfg=config(engine=tccl.tcclEngineCopyOut,
+                                                                   ce_segment_bytes=4096))
+    assert ns == 64 and se * 4 >= (1 << 32) // 64
+
+
+@pytest.mark.parametrize("send_mis,recv_mis,fold", [
+    (0, 0, True), (4, 4, True), (6, 6, True), (4, 0, False), (0, 2, False),
+    ([0, 0, 0, 4], 0, False), (0, [0, 4, 4, 4], True)])
+def test_register_fold_for_allreduce(send_mis, recv_mis, fold):
+    """The allreduce's fold needs every send buffer co-aligned (mod 16) with
+    rank 0's receive buffer, the anchor; the other receive buffers are only
+    written by the copy engines, so their alignment does not matter."""
+    co, rf, ns, se = inspect(AR, 4, 8 * MiB, cap=16, send_mis=send_mis, recv_mis=recv_mis)
+    assert co == 1 and rf == int(fold)
+
+
+@pytest.mark.parametrize("rc_bytes,send_mis,recv_mis,fold", [
+    (1 * MiB, 0, 0, True), (1 * MiB, 6, 6, True), (1 * MiB + 2, 0, 0, False),
+    (1 * MiB, 4, 0, False), (1 * MiB, 0, [0, 0, 8, 0], False)])
+def test_register_fold_for_reduce_scatter(rc_bytes, send_mis, recv_mis, fold):
+    """Reduce-scatter's fold writes every rank, so every buffer must be
+    co-aligned and a shard a multiple of 16 bytes; otherwise the bulk engine
+    runs it and the inspect reports no copy-out at all."""
+    co, rf, ns, se = inspect(RS, 4, rc_bytes // 2, cap=8, send_mis=send_mis, recv_mis=recv_mis)
+    assert (co, rf) == ((1, 1) if fold else (0, 0))
+    assert (ns, se) == ((1, rc_bytes // 2) if fold else (0, 0))
+
+
+def test_all_gather_is_copies_only():
+    co, rf, ns, se = inspect(AG, 8, 1 * MiB, cap=8)
+    assert (co, rf, ns, se) == (1, 0, 0, 0)
+
+
+def test_errors_and_empty_calls():
+    send, recv = bufs(4)
+    r = tccl.tcclCopyOutInspect(AR, 4, send, recv, 0, BF16, 8, SMS)
+    assert r[0] == tccl.tcclSuccess and r[1:] == (0, 0, 0, 0)
+    # overlapping receive buffers are rejected exactly as the call would be
+    r = tccl.tcclCopyOutInspect(AR, 4, send, [recv[0]] * 4, 1 << 20, BF16, 8, SMS)
+    assert r[0] == tccl.tcclInvalidArgument
+    assert tccl.tcclCopyOutInspect(AR, 4, send, recv, 1 << 20, BF16, 8, 0)[0] == tccl.tcclInvalidArgument
+    assert tccl.tcclCopyOutInspect(AR, 4, send, recv, 1 << 20, 7, 8, SMS)[0] == tccl.tcclInvalidArgument
