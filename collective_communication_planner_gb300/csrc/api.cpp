@@ -1026,7 +1026,7 @@ tcclResult_t tcclAllReduceRMSNorm(tcclGroup_t g, const void* const sendbufs[],
   if (cluster) {
     uint64_t clusters = std::min<uint64_t>(rows, (uint64_t)g->dev.sm_count * 8 / C);
     if (cta_cap > 0) clusters = std::min<uint64_t>(clusters, (uint64_t)(cta_cap / C));
-    err = launch_rmsnorm_cluster(datatype, a, (int)clusters, C, stream);
+    err = launch_rmsnorm_cluster(datatype, a, (int)clusters, C, cta_cap <= 0, stream);
     g->last.ctas = (int)(clusters * C);
     g->last.threads = kRmsClusterThreads;
   } else {
@@ -1035,7 +1035,7 @@ tcclResult_t tcclAllReduceRMSNorm(tcclGroup_t g, const void* const sendbufs[],
     threads = std::max(threads, 32);
     uint64_t grid = std::min<uint64_t>(rows, (uint64_t)g->dev.sm_count * 8);
     if (cta_cap > 0) grid = std::min<uint64_t>(grid, (uint64_t)cta_cap);
-    err = launch_rmsnorm(datatype, a, (int)grid, threads, vectors, stream);
+    err = launch_rmsnorm(datatype, a, (int)grid, threads, vectors, cta_cap <= 0, stream);
     g->last.ctas = (int)grid;
     g->last.threads = threads;
   }

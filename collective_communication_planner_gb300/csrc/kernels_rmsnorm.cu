@@ -4,7 +4,7 @@
 // kernel). The reduced row never leaves the chip unnormalised.
 #include <cooperative_groups.h>
 
-#include "kernels_common.cuh"
+#include "dispatch.cuh"
 #include "rmsnorm.h"
 
 namespace tccl {
@@ -21,6 +21,10 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rmsnorm_kernel(const __grid_co
   extern __shared__ __align__(16) uint4 gamma_smem[];
   __shared__ float partial[kRmsMaxThreads / 32];
   __shared__ float row_scale;
+  // an early (programmatic dependent) launch waits here for the stream's
+  // previous kernel before any global access
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) dev::record_sm(a.sm_mask);
   const int P = a.nranks;
   const uint32_t nvec = a.hidden / kVecElems;
@@ -110,6 +114,8 @@ __global__ void __launch_bounds__(kRmsClusterThreads)
   cg::cluster_group cluster = cg::this_cluster();
   const int q = static_cast<int>(cluster.block_rank());
   const int C = static_cast<int>(cluster.num_blocks());
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // as in rmsnorm_kernel
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) dev::record_sm(a.sm_mask);
   const int P = a.nranks;
   const uint32_t nvec = a.hidden / kVecElems;
@@ -187,36 +193,40 @@ __global__ void __launch_bounds__(kRmsClusterThreads)
 }  // namespace
 
 int launch_rmsnorm_cluster(int dtype, const RmsArgs& a, int clusters, int cluster_size,
-                           void* stream) {
+                           bool early, void* stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * cluster_size));
   cfg.blockDim = dim3(kRmsClusterThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_size);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = early ? 2 : 1;
   cudaError_t e = dtype == kBF16 ? cudaLaunchKernelEx(&cfg, rmsnorm_cluster_kernel<kBF16>, a)
                                  : cudaLaunchKernelEx(&cfg, rmsnorm_cluster_kernel<kF32>, a);
   if (e != cudaSuccess) return static_cast<int>(e);
   return static_cast<int>(cudaGetLastError());
 }
 
-int launch_rmsnorm(int dtype, const RmsArgs& a, int grid, int threads, int vectors, void* stream) {
+int launch_rmsnorm(int dtype, const RmsArgs& a, int grid, int threads, int vectors, bool early,
+                   void* stream) {
+  LaunchShape s;
+  s.grid = grid;
+  s.threads = threads;
+  s.smem = static_cast<size_t>(a.hidden) * (dtype == kBF16 ? 2 : 4);
+  s.early_launch = early ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t smem = static_cast<size_t>(a.hidden) * (dtype == kBF16 ? 2 : 4);
-  if (dtype == kBF16) {
-    if (vectors <= 4) rmsnorm_kernel<kBF16, 4><<<grid, threads, smem, st>>>(a);
-    else rmsnorm_kernel<kBF16, 8><<<grid, threads, smem, st>>>(a);
-  } else {
-    if (vectors <= 4) rmsnorm_kernel<kF32, 4><<<grid, threads, smem, st>>>(a);
-    else rmsnorm_kernel<kF32, 8><<<grid, threads, smem, st>>>(a);
-  }
-  return static_cast<int>(cudaGetLastError());
+  if (dtype == kBF16)
+    return vectors <= 4 ? dev::launch_maybe_early(rmsnorm_kernel<kBF16, 4>, a, s, st)
+                        : dev::launch_maybe_early(rmsnorm_kernel<kBF16, 8>, a, s, st);
+  return vectors <= 4 ? dev::launch_maybe_early(rmsnorm_kernel<kF32, 4>, a, s, st)
+                      : dev::launch_maybe_early(rmsnorm_kernel<kF32, 8>, a, s, st);
 }
 
 }  // namespace tccl

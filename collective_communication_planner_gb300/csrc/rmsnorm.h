@@ -22,9 +22,11 @@ struct RmsArgs {
 
 // `vectors`: 16-byte vectors of a row per thread (4 or 8); gamma is staged in
 // hidden * element-size bytes of dynamic shared memory.
-int launch_rmsnorm(int dtype, const RmsArgs& a, int grid, int threads, int vectors, void* stream);
+// early: programmatic dependent launch (uncapped calls only)
+int launch_rmsnorm(int dtype, const RmsArgs& a, int grid, int threads, int vectors, bool early,
+                   void* stream);
 // Few rows: `clusters` clusters of `cluster_size` CTAs, each cluster one row at a time.
 int launch_rmsnorm_cluster(int dtype, const RmsArgs& a, int clusters, int cluster_size,
-                           void* stream);
+                           bool early, void* stream);
 
 }  // namespace tccl
