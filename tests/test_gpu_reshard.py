@@ -62,6 +62,15 @@ def test_article_example_a(group, golden_dir):
     run(group, glob, ((1, 4), (R, 0)), ((2, 2), (R, 0)), "bf16")
 
 
+@pytest.mark.parametrize("shape", [(4, 8), (4096, 1024)])
+def test_article_example_b(group, shape):
+    """Example B, both pipeline stages: trainer mesh [2] Shard(0) -> generator
+    mesh [1] Replicate(), the generator gathering each stage's whole weight."""
+    for stage in range(2):
+        glob = global_tensor("bf16", shape, seed=40 + stage)
+        run(group, glob, ((2,), (0,)), ((1,), (R,)), "bf16")
+
+
 LAYOUTS = [((4,), (0,)), ((4,), (R,)), ((2, 2), (R, 0)), ((2, 2), (0, R)), ((2, 2), (1, R)),
            ((1, 4), (R, 1)), ((2, 4), (R, 0)), ((8,), (1,)), ((2, 1, 2), (R, R, 1))]
 

@@ -59,6 +59,22 @@ def test_article_example_a_values(golden_dir):
         assert np.array_equal(out[grank - 4], exp)
 
 
+@pytest.mark.parametrize("shape", [(4, 8), (6, 3), (2, 5, 4)])
+def test_article_example_b_stage_gather(shape):
+    """The article's example B (TP2,PP2 -> TP1,PP1), one reshard per pipeline
+    stage: in a stage's communicator the trainer mesh [2] from c-rank 0 holds
+    Shard(0), the generator mesh [1] at c-rank 2 holds Replicate(). So the
+    generator ends with the whole stage weight, which in row-major order is
+    trainer c-rank 0's block followed by c-rank 1's."""
+    for stage in range(2):
+        src = [b + 100000 * stage for b in make_src(shape, (2,), (0,))]
+        out = rs.reshard(src, (2,), (0,), (1,), (R,), shape)
+        assert len(out) == 1
+        assert np.array_equal(out[0], np.concatenate(src))
+        half = shape[0] // 2
+        assert rs.local_box(shape, (2,), (0,), 1)[0] == (half, shape[0])
+
+
 def test_planted_column_major_coordinates_fail_the_golden(golden_dir, monkeypatch):
     def col_major(dims, m):
         out = []

@@ -47,6 +47,20 @@ def test_article_example_a_plan(golden_dir):
     assert br == 4 * 8 * 4 and bw == 2 * br
 
 
+def test_article_example_b_plan():
+    """Example B per pipeline stage: trainer mesh [2] Shard(0) from c-rank 0 to
+    generator mesh [1] Replicate() at c-rank 2. Two transfers, one per trainer
+    rank, each its half of the rows, both into the single generator block."""
+    shape = [6, 10]
+    r, tr, br, bw, nw = inspect(((2,), (0,), 0), ((1,), (R,), 2), shape)
+    assert r == 0 and len(tr) == 2
+    by_src = {t["src"]: t for t in tr}
+    assert by_src[0]["lo"] == [0, 0] and by_src[0]["hi"] == [3, 10]
+    assert by_src[1]["lo"] == [3, 0] and by_src[1]["hi"] == [6, 10]
+    assert all(t["dst_mask"] == 1 for t in tr)
+    assert br == 6 * 10 * 4 and bw == br
+
+
 LAYOUTS = [((4,), (0,)), ((4,), (R,)), ((2, 2), (R, 0)), ((2, 2), (0, R)), ((2, 2), (1, R)),
            ((1, 4), (R, 1)), ((2, 4), (R, 0)), ((8,), (1,)), ((2, 1, 2), (R, R, 1))]
 
