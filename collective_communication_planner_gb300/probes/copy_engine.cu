@@ -9,7 +9,10 @@
 //  D. the copy-out pipeline at a 16 or 32 CTA cap, P = 8, 128 MiB per rank:
 //     per segment a register-load fold of 8 ranks into rank 0 (1024 threads
 //     per CTA), then 7 copies of the segment from rank 0 to ranks 1..7 on 4
-//     streams; timed with the copies, without them, and copies alone.
+//     streams; timed with the copies, without them, and copies alone;
+//  E. the host link: pinned host memory to the device and back, 512 MiB each
+//     way, in 1, 2, 4 or 8 pieces on as many streams, one direction or both
+//     at once.
 //
 // Every buffer is 128 MiB or 1 GiB; each index is checked against its buffer
 // (segment offsets + segment sizes <= 128 MiB, fan-out destinations
@@ -20,6 +23,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 
 #define CK(x)                                                                  \
   do {                                                                         \
@@ -224,6 +228,47 @@ int main() {
                     cap, seg_mib, kMode[mode], best, 2.0 * kRanks * kRank / (best * 1e6) / 6800.0);
       }
     }
+  }
+  // E: host buffers of 512 MiB each way (pinned); device side = big_a / big_b
+  {
+    const size_t bytes = 4 * kRank;
+    char *h_in, *h_out;
+    CK(cudaMallocHost(&h_in, bytes));
+    CK(cudaMallocHost(&h_out, bytes));
+    std::memset(h_in, 1, bytes);
+    std::memset(h_out, 0, bytes);
+    for (int dir = 0; dir < 3; ++dir) {  // 0 host->device, 1 device->host, 2 both
+      for (int ns : {1, 2, 4, 8}) {
+        const size_t piece = bytes / ns;
+        best = 1e9f;
+        for (int rep = 0; rep < 3; ++rep) {
+          CK(cudaDeviceSynchronize());
+          CK(cudaEventRecord(e0, st[0]));
+          for (int j = 0; j < 8; ++j) CK(cudaStreamWaitEvent(st[j], e0, 0));
+          for (int k = 0; k < ns; ++k) {
+            if (dir != 1)
+              CK(cudaMemcpyAsync(big_a + k * piece, h_in + k * piece, piece, cudaMemcpyHostToDevice, st[k % 8]));
+            if (dir != 0)
+              CK(cudaMemcpyAsync(h_out + k * piece, big_b + k * piece, piece, cudaMemcpyDeviceToHost,
+                                 st[(k + (dir == 2 ? 4 : 0)) % 8]));
+          }
+          for (int j = 1; j < 8; ++j) {
+            CK(cudaEventRecord(ev[j], st[j]));
+            CK(cudaStreamWaitEvent(st[0], ev[j], 0));
+          }
+          CK(cudaEventRecord(e1, st[0]));
+          CK(cudaEventSynchronize(e1));
+          const float ms = elapsed(e0, e1);
+          if (ms < best) best = ms;
+        }
+        static const char* kDir[3] = {"host to device", "device to host", "both directions"};
+        std::printf("{\"probe\": \"E host link, pinned, 512 MiB each way\", \"direction\": \"%s\", "
+                    "\"pieces\": %d, \"ms\": %.4f, \"GBps_total\": %.1f}\n",
+                    kDir[dir], ns, best, (dir == 2 ? 2.0 : 1.0) * bytes / (best * 1e6));
+      }
+    }
+    CK(cudaFreeHost(h_in));
+    CK(cudaFreeHost(h_out));
   }
   CK(cudaDeviceSynchronize());
   std::printf("{\"probe\": \"done\"}\n");
