@@ -18,7 +18,7 @@ INCLUDE = ROOT / "include"
 LIB = PKG / "libtccl.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-HOST_SOURCES = ["api.cpp", "plan.cpp", "reshard.cpp"]
+HOST_SOURCES = ["api.cpp", "plan.cpp", "reshard.cpp", "copy_out_host.cpp"]
 CUDA_SOURCES = ["kernels_bulk.cu", "kernels_small_ar.cu", "kernels_small_rs.cu",
                 "kernels_small_ag.cu", "kernels_reshard.cu", "kernels_rmsnorm.cu",
                 "no_alloc.cu", "kernels_copy_out.cu"]

@@ -1,0 +1,250 @@
+// Host side of the copy-out engine: Auto's choice, the segment pipeline of
+// the allreduce (register-load fold or TMA shard-in into one anchor rank,
+// then device-to-device copies on the group's copy streams), the
+// reduce-scatter on the register fold, and the all-gather as copies only.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "copy_out.h"
+#include "group.h"
+#include "internal.h"
+#include "plan.h"
+
+namespace tccl {
+
+bool use_copy_out(const tcclGroup* g, int coll, size_t count, int es, int cap) {
+  return copy_out_chosen(g->cfg, g->dev.sm_count, g->nranks, coll, count, es, cap);
+}
+
+std::vector<uint8_t> mod16_of(int n, const void* const* p) {
+  std::vector<uint8_t> m(n);
+  for (int k = 0; k < n; ++k) m[k] = (uint8_t)((uintptr_t)p[k] & 15);
+  return m;
+}
+
+tcclResult_t ensure_ce_resources(tcclGroup* g, int segments) {
+  const int ns = g->cfg.ce_streams;
+  while ((int)g->ce_streams.size() < ns) {
+    cudaStream_t st;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return tcclCudaError;
+    g->ce_streams.push_back(st);
+  }
+  while ((int)g->ce_done_events.size() < ns) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return tcclCudaError;
+    g->ce_done_events.push_back(e);
+  }
+  while ((int)g->ce_seg_events.size() < segments) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return tcclCudaError;
+    g->ce_seg_events.push_back(e);
+  }
+  if (!g->ce_fork_event &&
+      cudaEventCreateWithFlags(&g->ce_fork_event, cudaEventDisableTiming) != cudaSuccess)
+    return tcclCudaError;
+  return tcclSuccess;
+}
+
+// Makes `stream` wait for everything queued on the first `used` copy streams.
+int join_ce_streams(tcclGroup* g, int used, cudaStream_t stream) {
+  int err = 0;
+  for (int j = 0; j < used; ++j) {
+    int e = cudaEventRecord(g->ce_done_events[j], g->ce_streams[j]);
+    if (!e) e = cudaStreamWaitEvent(stream, g->ce_done_events[j], 0);
+    if (e && !err) err = e;
+  }
+  return err;
+}
+
+// Allreduce on the copy-out engine. The message is cut into segments of
+// ce_segment_bytes per rank (offsets multiples of 256 bytes, so every
+// segment has the same alignment). Each segment's shard-in kernel folds the P
+// ranks in ascending order into the anchor rank's (rank 0's) receive buffer
+// alone; an event after it releases the device-to-device copies of that
+// segment from the anchor to ranks 1..P-1 on the group's copy streams, so the
+// copy engines fan segment s out while the SMs reduce segment s+1. In place
+// is safe: segment s of a rank is overwritten only after the kernel that read
+// it has finished.
+//
+// The shard-in kernel is the register-load anchor fold when every send buffer
+// and the anchor's receive buffer share their address mod 16, else the bulk
+// engine's TMA pipeline with every window pointed at the anchor.
+tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void* const* recv,
+                                    size_t count, int dtype, int op, int es, cudaStream_t stream,
+                                    int cap) {
+  const int P = g->nranks;
+  const int anchor = 0;
+  size_t seg = 0;
+  int nseg = 0;
+  copy_out_segments(g->cfg, count, es, &seg, &nseg);
+  tcclResult_t r = ensure_ce_resources(g, nseg);
+  if (r != tcclSuccess) return r;
+  std::vector<const void*> s_ptr(P);
+  std::vector<void*> r_ptr(P);
+  auto at = [&](size_t off) {
+    for (int k = 0; k < P; ++k) {
+      s_ptr[k] = static_cast<const char*>(send[k]) + off * es;
+      r_ptr[k] = static_cast<char*>(recv[k]) + off * es;
+    }
+  };
+  const uintptr_t mod = (uintptr_t)recv[anchor] & 15;
+  const bool fast = register_fold_ok(kAllReduce, P, mod16_of(P, send).data(),
+                                     mod16_of(P, (const void* const*)recv).data(), count, es, seg);
+  const size_t tail_n = count - (size_t)(nseg - 1) * seg;
+  // TMA fallback: both plans (full segments, ragged tail) before any launch,
+  // since a new plan's table upload is synchronous
+  CachedPlan* full = nullptr;
+  CachedPlan* tail = nullptr;
+  if (!fast) {
+    at(0);
+    r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), nseg > 1 ? seg : tail_n, es, cap, &full, anchor);
+    if (r == tcclSuccess && nseg > 1 && tail_n != seg) {
+      at((size_t)(nseg - 1) * seg);
+      r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), tail_n, es, cap, &tail, anchor);
+    }
+    if (r != tcclSuccess) return r;
+  }
+  const int U = anchor_vectors_per_thread(P);
+  int fast_grid = 0;
+  AnchorArgs aa;
+  std::memset(&aa, 0, sizeof(aa));
+  aa.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
+  aa.nranks = P;
+  aa.njobs = 1;
+  const int used = std::min(g->cfg.ce_streams, P - 1);
+  int err = 0, copies = 0;
+  for (int sgi = 0; sgi < nseg && !err; ++sgi) {
+    const size_t off = (size_t)sgi * seg;
+    const size_t n = sgi == nseg - 1 ? tail_n : seg;
+    at(off);
+    if (fast) {
+      const size_t bytes = n * es;
+      const size_t head = std::min(bytes, (size_t)((16 - mod) & 15));
+      aa.head_bytes = head;
+      aa.nvec = (bytes - head) / 16;
+      aa.tail_bytes = bytes - head - aa.nvec * 16;
+      for (int k = 0; k < P; ++k) aa.p.src[k] = s_ptr[k];
+      aa.p.dst[0] = r_ptr[anchor];
+      const uint64_t per_cta = (uint64_t)kAnchorThreads * U;
+      uint64_t grid = std::max<uint64_t>(1, (aa.nvec + per_cta - 1) / per_cta);
+      grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
+      fast_grid = std::max(fast_grid, (int)grid);
+      err = launch_anchor_reduce(dtype, op, aa, (int)grid, cap <= 0, stream);
+    } else {
+      CachedPlan* cp = (sgi == nseg - 1 && tail) ? tail : full;
+      err = launch_plan(g, cp, kAllReduce, dtype, op, s_ptr.data(), r_ptr.data(), es, stream);
+    }
+    if (err || used == 0) continue;
+    err = cudaEventRecord(g->ce_seg_events[sgi], stream);
+    for (int j = 0; j < used && !err; ++j) err = cudaStreamWaitEvent(g->ce_streams[j], g->ce_seg_events[sgi], 0);
+    int j = 0;
+    for (int k = 0; k < P && !err; ++k) {
+      if (k == anchor) continue;
+      err = cudaMemcpyAsync(r_ptr[k], r_ptr[anchor], n * es, cudaMemcpyDeviceToDevice, g->ce_streams[j]);
+      j = (j + 1) % used;
+      ++copies;
+    }
+  }
+  const int jerr = used ? join_ce_streams(g, used, stream) : 0;
+  if (!err) err = jerr;
+  if (fast) {
+    std::memset(&g->last, 0, sizeof(g->last));
+    g->last.store_mode = kStoreVec;
+    g->last.ctas = fast_grid;
+    g->last.threads = kAnchorThreads;
+  } else {
+    fill_info(full->low, &g->last);
+  }
+  g->last.engine = kEngineCopyOut;
+  g->last.ce_segments = nseg;
+  g->last.ce_copies = copies;
+  if (err) {
+    if (log_level()) std::fprintf(stderr, "[tccl] copy-out allreduce failed: %s\n", cudaGetErrorString((cudaError_t)err));
+    return tcclCudaError;
+  }
+  return tcclSuccess;
+}
+
+// Reduce-scatter on the copy-out engine: no copies, one launch of the
+// register-load fold with P jobs, shard j of every send buffer folded into
+// rank j's receive buffer. Needs every send and receive buffer to share its
+// address mod 16 and the shard size to be a multiple of 16 bytes (so every
+// shard starts at that same alignment); returns tcclInvalidUsage otherwise,
+// and the caller takes the bulk engine.
+tcclResult_t run_copy_out_reduce_scatter(tcclGroup* g, const void* const* send, void* const* recv,
+                                         size_t rc, int dtype, int op, int es, cudaStream_t stream,
+                                         int cap) {
+  const int P = g->nranks;
+  const size_t bytes = rc * (size_t)es;
+  const uintptr_t mod = (uintptr_t)recv[0] & 15;
+  if (!register_fold_ok(kReduceScatter, P, mod16_of(P, send).data(),
+                        mod16_of(P, (const void* const*)recv).data(), rc, es, 0))
+    return tcclInvalidUsage;
+  AnchorArgs aa;
+  std::memset(&aa, 0, sizeof(aa));
+  aa.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
+  aa.nranks = P;
+  aa.njobs = P;
+  aa.job_src_stride = bytes;
+  aa.head_bytes = std::min(bytes, (size_t)((16 - mod) & 15));
+  aa.nvec = (bytes - aa.head_bytes) / 16;
+  aa.tail_bytes = bytes - aa.head_bytes - aa.nvec * 16;
+  for (int k = 0; k < P; ++k) {
+    aa.p.src[k] = send[k];
+    aa.p.dst[k] = recv[k];
+  }
+  const uint64_t per_cta = (uint64_t)kAnchorThreads * anchor_vectors_per_thread(P);
+  uint64_t grid = std::max<uint64_t>(1, (aa.nvec * P + per_cta - 1) / per_cta);
+  grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
+  const int err = launch_anchor_reduce(dtype, op, aa, (int)grid, cap <= 0, stream);
+  std::memset(&g->last, 0, sizeof(g->last));
+  g->last.engine = kEngineCopyOut;
+  g->last.store_mode = kStoreVec;
+  g->last.ctas = (int)grid;
+  g->last.threads = kAnchorThreads;
+  g->last.ce_segments = 1;
+  if (err) {
+    if (log_level()) std::fprintf(stderr, "[tccl] copy-out reduce-scatter failed: %s\n", cudaGetErrorString((cudaError_t)err));
+    return tcclCudaError;
+  }
+  return tcclSuccess;
+}
+
+// All-gather on the copy-out engine: P x P (P x (P-1) in place) device-to-
+// device copies spread over the group's copy streams. No kernel, no SM.
+tcclResult_t run_copy_out_allgather(tcclGroup* g, const void* const* send, void* const* recv,
+                                    size_t count, int es, cudaStream_t stream) {
+  const int P = g->nranks;
+  tcclResult_t r = ensure_ce_resources(g, 0);
+  if (r != tcclSuccess) return r;
+  const int used = std::min(g->cfg.ce_streams, P * P);
+  const size_t bytes = count * (size_t)es;
+  int err = cudaEventRecord(g->ce_fork_event, stream);
+  for (int j = 0; j < used && !err; ++j) err = cudaStreamWaitEvent(g->ce_streams[j], g->ce_fork_event, 0);
+  int j = 0, copies = 0;
+  for (int q = 0; q < P && !err; ++q) {
+    for (int k = 0; k < P && !err; ++k) {
+      char* dst = static_cast<char*>(recv[k]) + (size_t)q * bytes;
+      if (dst == static_cast<const char*>(send[q])) continue;  // in place: already there
+      err = cudaMemcpyAsync(dst, send[q], bytes, cudaMemcpyDeviceToDevice, g->ce_streams[j]);
+      j = (j + 1) % used;
+      ++copies;
+    }
+  }
+  const int jerr = join_ce_streams(g, used, stream);
+  if (!err) err = jerr;
+  std::memset(&g->last, 0, sizeof(g->last));
+  g->last.engine = kEngineCopyOut;
+  g->last.ce_copies = copies;
+  if (err) {
+    if (log_level()) std::fprintf(stderr, "[tccl] copy-out all-gather failed: %s\n", cudaGetErrorString((cudaError_t)err));
+    return tcclCudaError;
+  }
+  return tcclSuccess;
+}
+
+}  // namespace tccl
