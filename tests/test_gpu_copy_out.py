@@ -344,6 +344,55 @@ def test_graph_capture_replay(groups):
     check([to_host(r) for r in recvs], oracle.allreduce(xs, "bf16", "sum"), "graph replay")
 
 
+@pytest.mark.parametrize("what", ["allreduce_uncapped", "reduce_scatter_capped",
+                                  "reduce_scatter_uncapped", "allgather"])
+def test_graph_capture_of_every_copy_out_path(groups, what):
+    """Each copy-out path captured into a CUDA graph and replayed: the
+    uncapped allreduce (early-launched segment kernels between events), the
+    register-fold reduce-scatter with and without a cap, and the copy-only
+    all-gather."""
+    p = 4
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=128 * 1024)
+    s = torch.cuda.Stream()
+    if what == "allreduce_uncapped":
+        n = 400_000
+        xs = datagen.rank_buffers("normal_bf16", 37, p, n)
+        ins = [to_device(x) for x in xs]
+        outs = [torch.zeros_like(t) for t in ins]
+        call = lambda: g.all_reduce(ins, outs, stream=s.cuda_stream)
+        exp = oracle.allreduce(xs, "bf16", "sum", nthreads=0)
+    elif what.startswith("reduce_scatter"):
+        rc = 100_000
+        xs = datagen.rank_buffers("uniform_f32", 38, p, p * rc)
+        ins = [to_device(x) for x in xs]
+        outs = [torch.zeros(rc, dtype=torch.float32, device="cuda") for _ in range(p)]
+        cap = 8 if what == "reduce_scatter_capped" else 0
+        call = lambda: g.reduce_scatter(ins, outs, cta_cap=cap, stream=s.cuda_stream)
+        exp = oracle.reduce_scatter(xs, "f32", "sum", nthreads=0)
+    else:
+        sc = 150_000
+        xs = datagen.rank_buffers("int32", 39, p, sc)
+        ins = [to_device(x) for x in xs]
+        outs = [torch.zeros(p * sc, dtype=torch.int32, device="cuda") for _ in range(p)]
+        call = lambda: g.all_gather(ins, outs, stream=s.cuda_stream)
+        exp = [np.concatenate(xs)] * p
+    with torch.cuda.stream(s):
+        call()  # first call outside the capture: plans, copy streams, events
+    torch.cuda.synchronize()
+    assert g.last_launch()["engine"] == CE, g.last_launch()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call()
+    for o in outs:
+        o.zero_()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    check([to_host(o) for o in outs], exp, f"graph {what}")
+
+
 def test_timeout_is_reported_and_the_next_call_is_right(groups):
     """Send and receive buffers that are not co-aligned take the TMA shard-in
     (the register-load fold has no waits to run out); its injected wait runs
