@@ -24,13 +24,25 @@ __global__ void __launch_bounds__(256) reshard_kernel(const __grid_constant__ Re
       const uint32_t end = min(begin + kReshardSegBytes, w.bytes);
       const char* s = src + row * w.src_pitch;
       const uint64_t doff = w.dst_off + row * w.dst_pitch;
-      for (uint32_t b = begin + lane * 16; b < end; b += 32 * 16) {
-        const uint4 v = dev::ld_global_v4(s + b);
-        uint64_t m = w.dst_mask;
-        while (m) {
-          const int d = __ffsll(static_cast<long long>(m)) - 1;
-          m &= m - 1;
-          dev::st_global_v4(static_cast<char*>(a.dst[d]) + doff + b, v);
+      // every load of the segment first (up to 8 per lane), then the stores:
+      // a row piece costs one load latency, not one per 512 bytes
+      constexpr int kPerLane = kReshardSegBytes / (32 * 16);
+      uint4 v[kPerLane];
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) {
+        const uint32_t b = begin + (lane + 32u * i) * 16u;
+        if (b < end) v[i] = dev::ld_global_v4(s + b);
+      }
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) {
+        const uint32_t b = begin + (lane + 32u * i) * 16u;
+        if (b < end) {
+          uint64_t m = w.dst_mask;
+          while (m) {
+            const int d = __ffsll(static_cast<long long>(m)) - 1;
+            m &= m - 1;
+            dev::st_global_v4(static_cast<char*>(a.dst[d]) + doff + b, v[i]);
+          }
         }
       }
     } else {
