@@ -26,6 +26,10 @@ std::vector<uint8_t> mod16_of(int n, const void* const* p) {
   return m;
 }
 
+namespace {
+
+// The group's copy streams, the per-segment events and the join events,
+// created on first use (so a group that never uses the engine holds none).
 tcclResult_t ensure_ce_resources(tcclGroup* g, int segments) {
   const int ns = g->cfg.ce_streams;
   while ((int)g->ce_streams.size() < ns) {
@@ -60,9 +64,12 @@ int join_ce_streams(tcclGroup* g, int used, cudaStream_t stream) {
   return err;
 }
 
-// Allreduce on the copy-out engine. The message is cut into segments of
-// ce_segment_bytes per rank (offsets multiples of 256 bytes, so every
-// segment has the same alignment). Each segment's shard-in kernel folds the P
+}  // namespace
+
+// Allreduce on the copy-out engine. The message is cut into segments
+// (copy_out_segments: at most ce_segment_bytes per rank, at least four of at
+// least 4 MiB where the message allows, offsets multiples of 256 bytes, so
+// every segment has the same alignment). Each segment's shard-in kernel folds the P
 // ranks in ascending order into the anchor rank's (rank 0's) receive buffer
 // alone; an event after it releases the device-to-device copies of that
 // segment from the anchor to ranks 1..P-1 on the group's copy streams, so the
