@@ -1,6 +1,7 @@
-// Copy-out engine: the shard-in kernel that folds P ranks into one anchor
-// rank's buffer with plain 128-bit register loads (no shared-memory staging),
-// before the GPU's copy engines fan the result out to the other ranks.
+// Copy-out engine: the kernel that folds P ranks with plain 128-bit register
+// loads (no shared-memory staging), into one anchor rank's buffer before the
+// GPU's copy engines fan the result out to the other ranks, or for a
+// reduce-scatter into each shard's owner.
 #pragma once
 
 #include "internal.h"

@@ -1,11 +1,13 @@
-// Copy-out engine shard-in: the P-rank fold into one anchor buffer.
+// The register-load fold of the copy-out engine: P ranks folded into one
+// anchor buffer (the allreduce's shard-in; the copy engines then do the
+// other P-1 stores) or each shard into its owner (a reduce-scatter).
 //
 // Under a CTA cap the work of a few SMs decides the rate. Feeding a fold
 // through TMA copies and shared memory costs each byte a shared-memory write
 // and a read plus per-stage synchronisation, and a capped SM then reads about
 // 50 GB/s; 128-bit register loads with eight in flight per thread read about
-// 140 GB/s per SM on GB300. The result goes to one buffer only, so this
-// kernel is read-bound; the copy engines do the remaining P-1 stores.
+// 140 GB/s per SM on GB300. Every result goes to one buffer, so the kernel is
+// read-bound.
 #include "copy_out.h"
 #include "dispatch.cuh"
 
@@ -55,9 +57,9 @@ __device__ __forceinline__ void st_keep_v4(void* p, uint4 v, uint64_t policy) {
 }
 
 // For each job, thread t of the grid folds vectors t, t + T, ... (T threads
-// in all), U of them at a time. With the rank count fixed at compile time (NP = 2, 4, 8)
-// every load of a step is issued before the first add; otherwise the ranks
-// go in batches of 8 / U. Either way each accumulator receives the ranks in
+// in all), U of them at a time. With the rank count fixed at compile time
+// (NP = 2, 4, 8) every load of a step is issued before the first add;
+// otherwise the ranks go in batches of 8 / U. Either way each accumulator receives the ranks in
 // ascending order: the plain left fold over all P ranks.
 template <int DT, int OP, int NP, int U>
 __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const __grid_constant__ AnchorArgs a) {
@@ -69,8 +71,8 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) record_sm(a.sm_mask);
   const int P = NP > 0 ? NP : a.nranks;
-  // a job covers at most 2^28 vectors (the host splits larger segments), so
-  // vector indices and byte offsets within it fit 32 bits
+  // a job covers fewer than 2^28 vectors (register_fold_ok keeps larger ones
+  // off this kernel), so vector indices and byte offsets within it fit 32 bits
   const uint32_t nthr = gridDim.x * blockDim.x;
   const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const uint32_t nvec = static_cast<uint32_t>(a.nvec);
