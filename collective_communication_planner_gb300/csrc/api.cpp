@@ -674,7 +674,7 @@ tcclResult_t tcclReshard(tcclGroup_t g, const void* const srcbufs[], const tcclL
     a.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
     a.nwin = (int)cr->plan.win.size();
     a.elem_size = es;
-    if (launch_reshard(a, cr->plan.grid, stream) != 0) result = tcclCudaError;
+    if (launch_reshard(a, cr->plan.grid, cta_cap <= 0, stream) != 0) result = tcclCudaError;
     std::memset(&g->last, 0, sizeof(g->last));
     g->last.ctas = cr->plan.grid;
     g->last.threads = 256;

@@ -1,12 +1,16 @@
 // M-to-N reshard kernel: strided row copies, each source piece read once and
 // written to every destination replica of its block (load once, store to all).
-#include "kernels_common.cuh"
+#include "dispatch.cuh"
 #include "reshard.h"
 
 namespace tccl {
 namespace {
 
 __global__ void __launch_bounds__(256) reshard_kernel(const __grid_constant__ ReshardArgs a) {
+  // an early (programmatic dependent) launch waits here for the stream's
+  // previous kernel before any global access
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) dev::record_sm(a.sm_mask);
   const int lane = threadIdx.x & 31;
   const uint64_t nunits = a.unit_prefix[a.nwin];
@@ -78,9 +82,13 @@ __global__ void __launch_bounds__(256) reshard_kernel(const __grid_constant__ Re
 
 }  // namespace
 
-int launch_reshard(const ReshardArgs& a, int grid, void* stream) {
-  reshard_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  return static_cast<int>(cudaGetLastError());
+int launch_reshard(const ReshardArgs& a, int grid, bool early, void* stream) {
+  LaunchShape s;
+  s.grid = grid;
+  s.threads = 256;
+  s.smem = 0;
+  s.early_launch = early ? 1 : 0;
+  return dev::launch_maybe_early(reshard_kernel, a, s, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace tccl

@@ -99,6 +99,7 @@ struct ReshardArgs {
   int elem_size;
 };
 
-int launch_reshard(const ReshardArgs& a, int grid, void* stream);
+// early: programmatic dependent launch (uncapped calls only)
+int launch_reshard(const ReshardArgs& a, int grid, bool early, void* stream);
 
 }  // namespace tccl
