@@ -101,3 +101,45 @@ def test_weight_sized_reshard(group):
     # an 8192 x 8192 bf16 weight: TP8 (row shards) -> TP2 x DP4 (column shards, replicated)
     glob = global_tensor("bf16", (8192, 8192), seed=9)
     run(group, glob, ((8,), (0,)), ((4, 2), (R, 1)), "bf16")
+
+
+def random_layout(rng, ndim):
+    naxes = int(rng.integers(1, 4))
+    dims = (64,)
+    while int(np.prod(dims)) > 32:  # both meshes fit the 64-rank group
+        dims = tuple(int(rng.integers(1, 5)) for _ in range(naxes))
+    place = [R] * naxes
+    if rng.random() < 0.8:
+        place[int(rng.integers(0, naxes))] = int(rng.integers(0, ndim))
+    return dims, tuple(place)
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_random_reshard(group, case):
+    """Seeded random layout pairs: meshes of one to three axes (each of size
+    one to four), Replicate or one Shard per layout, tensors of one to three
+    dimensions whose sharded extents the mesh axes divide, three dtypes,
+    misaligned buffers and caps."""
+    rng = np.random.default_rng(9000 + case)
+    ndim = int(rng.integers(1, 4))
+    src = random_layout(rng, ndim)
+    dst = random_layout(rng, ndim)
+    shape = [int(rng.integers(1, 40 if ndim > 1 else 400)) for _ in range(ndim)]
+    for dims, place in (src, dst):
+        for a, d in enumerate(place):
+            if d != R:
+                shape[d] = dims[a] * max(1, shape[d] // dims[a])
+    # both meshes' axes must divide the same extent: take a common multiple
+    for d in range(ndim):
+        m = 1
+        for dims, place in (src, dst):
+            for a, dd in enumerate(place):
+                if dd == d:
+                    m = int(np.lcm(m, dims[a]))
+        shape[d] = m * max(1, shape[d] // m)
+    dtype = str(rng.choice(["f32", "bf16", "i32"]))
+    es = 2 if dtype == "bf16" else 4
+    mis = int(rng.integers(0, 16 // es)) * es if rng.random() < 0.3 else 0
+    cap = int(rng.choice([0, 0, 1, 5, 40]))
+    glob = global_tensor(dtype, tuple(shape), seed=case)
+    run(group, glob, src, dst, dtype, cap=cap, mis=mis)

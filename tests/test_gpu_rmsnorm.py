@@ -129,3 +129,23 @@ def test_rejects_unsupported_calls(groups):
         tccl.tcclInvalidArgument  # negative eps
     assert tccl.tcclAllReduceRMSNorm(g.handle, s, r, 4, 64, gam, 1e-6, 1, st) == tccl.tcclSuccess
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("case", range(48))
+def test_random_call(groups, case):
+    """Seeded random fused calls: dtype, P from 1 to 12, rows from 1 to 700
+    (both sides of the cluster-split threshold), any hidden that is a whole
+    number of 16-byte vectors up to the limit (16384 bf16, 8192 fp32), caps,
+    eps and the in-place form; the oracle's work is kept to a few million
+    elements."""
+    rng = np.random.default_rng(7000 + case)
+    dtype = str(rng.choice(["bf16", "f32"]))
+    vec, limit = (8, 16384) if dtype == "bf16" else (4, 8192)
+    p = int(rng.integers(1, 13))
+    hidden = vec * int(rng.integers(1, limit // vec + 1))
+    max_rows = max(1, min(700, 4_000_000 // (hidden * p)))
+    rows = int(rng.integers(1, max_rows + 1))
+    cap = int(rng.choice([0, 0, 1, 3, 8, 40]))
+    eps = float(rng.choice([1e-6, 1e-5, 0.25]))
+    in_place = bool(rng.random() < 0.3)
+    run(groups(p), dtype, p, rows, hidden, eps=eps, cap=cap, in_place=in_place, seed=case)
