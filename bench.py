@@ -69,10 +69,12 @@ def measured_peak():
 
 def kernel_source_hash() -> str:
     """Hash of the sources the bulk allreduce kernel is compiled from (its
-    template, its launch file and the shared argument structs)."""
+    template, its launch file and the shared argument structs) and of the
+    planner that picks its launch shape."""
     h = hashlib.sha256()
     csrc = ROOT / "collective_communication_planner_gb300" / "csrc"
-    for f in sorted(csrc / n for n in ("kernels_common.cuh", "dispatch.cuh", "kernels_bulk.cu", "internal.h")):
+    for f in sorted(csrc / n for n in ("kernels_common.cuh", "dispatch.cuh", "kernels_bulk.cu", "internal.h",
+                                       "plan.h", "plan.cpp")):
         h.update(f.name.encode())
         h.update(f.read_bytes())
     return h.hexdigest()[:16]

@@ -264,9 +264,11 @@ tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* con
                       size_t count, int es, int cap, CachedPlan** out, int anchor) {
   PlanKey key{coll, es, (uint64_t)count, cap > 0 ? cap : 0, std::string(), anchor};
   key.mod16.resize(2 * g->nranks);
+  key.in_place = coll == kAllReduce;
   for (int r = 0; r < g->nranks; ++r) {
     key.mod16[r] = (char)((uintptr_t)send[r] & 15);
     key.mod16[g->nranks + r] = (char)((uintptr_t)recv[r] & 15);
+    key.in_place = key.in_place && send[r] == recv[r];
   }
   auto it = g->plans.find(key);
   if (it != g->plans.end()) {
@@ -274,6 +276,8 @@ tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* con
     return tcclSuccess;
   }
   Plan pl = plan_collective(coll, g->nranks, count, es, 0);
+  pl.in_place = key.in_place;
+  pl.anchor_only = anchor >= 0;
   auto cp = std::make_unique<CachedPlan>();
   std::string why;
   std::vector<uint8_t> sm(g->nranks), rm(g->nranks);
@@ -857,9 +861,11 @@ tcclResult_t tcclPlanInspect(int coll, int nranks, const void* const sendbufs[],
   const int es = elem_size_of(datatype);
   Plan pl = plan_collective(coll, nranks, count, es, 0);
   std::vector<uint8_t> sm(nranks), rm(nranks);
+  pl.in_place = coll == kAllReduce;
   for (int r = 0; r < nranks; ++r) {
     sm[r] = (uint8_t)((uintptr_t)sendbufs[r] & 15);
     rm[r] = (uint8_t)((uintptr_t)recvbufs[r] & 15);
+    pl.in_place = pl.in_place && sendbufs[r] == recvbufs[r];
   }
   DeviceDesc dev;
   dev.sm_count = sm_count;

@@ -23,8 +23,10 @@ struct PlanKey {
   int cap;
   std::string mod16;  // address mod 16 of every send then recv buffer
   int anchor = -1;    // >= 0: every window stores to this rank only (copy-out shard-in)
+  bool in_place = false;
   bool operator<(const PlanKey& o) const {
     if (anchor != o.anchor) return anchor < o.anchor;
+    if (in_place != o.in_place) return o.in_place;
     if (coll != o.coll) return coll < o.coll;
     if (elem_size != o.elem_size) return elem_size < o.elem_size;
     if (count != o.count) return count < o.count;

@@ -647,17 +647,29 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
       while (pf_pos < static_cast<uint32_t>(S) && pf.next(skip)) ++pf_pos;
     }
     const uint64_t policy = l2_evict_first_policy();
-    unsigned long long next_claim = dynamic ? atomicAdd(&a.sched[0], 1ull) : 0ull;
+    // dynamic order: a CTA's first chunks fill its ring and are fixed
+    // (blockIdx.x, + gridDim.x, ...), so the ring fills without waiting on
+    // the counter; the chunks after the first nfixed * gridDim.x are claimed
+    const uint32_t nfixed = (COLL != kAllGather && a.rank_streamed) ? max(1, S / P) : S;
+    const uint64_t claimed_base = static_cast<uint64_t>(nfixed) * gridDim.x;
+    uint32_t taken = 0;
+    unsigned long long next_claim =
+        dynamic ? claimed_base + atomicAdd(&a.sched[0], 1ull) : 0ull;
     uint32_t it = 0, off, n;
     bool ok = true;
     for (;;) {
       uint64_t c;
       bool more;
       if (dynamic) {
-        c = next_claim;
+        if (taken < nfixed) {
+          c = blockIdx.x + static_cast<uint64_t>(taken) * gridDim.x;
+          ++taken;
+        } else {
+          c = next_claim;
+          // claim the following chunk now; its latency hides behind this one
+          if (c < a.total_chunks) next_claim = claimed_base + atomicAdd(&a.sched[0], 1ull);
+        }
         more = c < a.total_chunks;
-        // claim the following chunk now; its latency hides behind this one
-        if (more) next_claim = atomicAdd(&a.sched[0], 1ull);
       } else {
         more = so.next(c);
       }
@@ -780,7 +792,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
           mbar_arrive(&h.empty[(it - a.release_lag) % S]);
         ++it;
       }
-      bulk_wait_all();
+      bulk_wait_read<0>();
     }
     if (!*abort_flag) bulk_scalar_windows<COLL, DT, OP>(a, ctid, nct);
     return;
@@ -788,7 +800,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
 
   if (COLL != kAllGather && a.rank_streamed) {
     per_rank_consumers<COLL, DT, OP>(a, h, stage_base, ctid, nct, lane);
-    if (ctid == 0) bulk_wait_all();
+    if (ctid == 0) bulk_wait_read<0>();
     if (!*abort_flag) bulk_scalar_windows<COLL, DT, OP>(a, ctid, nct);
     return;
   }
@@ -855,7 +867,11 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
     }
     ++it;
   }
-  if (ctid == 0) bulk_wait_all();
+  // the CTA may leave once its bulk stores have read shared memory: their
+  // writes are complete and visible when the grid is (to the next kernel on
+  // the stream, an event, the host); waiting for each write here only delays
+  // the grid's last CTA
+  if (ctid == 0) bulk_wait_read<0>();
   if (!*abort_flag) bulk_scalar_windows<COLL, DT, OP>(a, ctid, nct);
 }
 

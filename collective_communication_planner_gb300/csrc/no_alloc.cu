@@ -101,9 +101,11 @@ extern "C" tcclResult_t tcclAllReduceNoAlloc(int nranks, const void* const sendb
   const int es = datatype == tcclBfloat16 ? 2 : 4;
   Plan pl = plan_collective(kAllReduce, nranks, count, es, op);
   uint8_t sm[kMaxRanks], rm[kMaxRanks];
+  pl.in_place = true;
   for (int r = 0; r < nranks; ++r) {
     sm[r] = (uint8_t)((uintptr_t)sendbufs[r] & 15);
     rm[r] = (uint8_t)((uintptr_t)recvbufs[r] & 15);
+    pl.in_place = pl.in_place && sendbufs[r] == recvbufs[r];
   }
   Config cfg;
   cfg.engine = kEngineBulk;

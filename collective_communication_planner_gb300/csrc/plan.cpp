@@ -139,8 +139,8 @@ Config resolve_config(const Config& in) {
   // defaults chosen by launch-shape sweeps on GB300 (P = 4 and 8, bf16)
   if (c.small_max_bytes == 0) c.small_max_bytes = 128 * 1024;
   if (c.vec_max_bytes == 0) c.vec_max_bytes = 4 * 1024 * 1024;
-  if (c.stage_bytes <= 0) c.stage_bytes = 64 * 1024;
-  if (c.stages <= 0) c.stages = 8;
+  if (c.stage_bytes <= 0) c.stage_bytes = kDefaultStageBytes;
+  if (c.stages <= 0) c.stages = kDefaultStages;
   if (c.consumer_warps <= 0) c.consumer_warps = 16;
   if (c.consumer_warps > kMaxConsumerWarps) c.consumer_warps = kMaxConsumerWarps;
   if (c.stage_layout < kLayoutAuto || c.stage_layout > kLayoutPerRank) c.stage_layout = kLayoutAuto;
@@ -151,7 +151,7 @@ Config resolve_config(const Config& in) {
   if (c.prefetch_chunks < 0) c.prefetch_chunks = 0;
   if (c.prefetch_chunks > 64) c.prefetch_chunks = 64;
   if (c.load_policy < 0 || c.load_policy > 2) c.load_policy = 0;
-  if (c.max_chunk_bytes == 0) c.max_chunk_bytes = 16384;
+  if (c.max_chunk_bytes == 0) c.max_chunk_bytes = kDefaultMaxChunkBytes;
   c.max_chunk_bytes = std::min<size_t>(std::max<size_t>(c.max_chunk_bytes, 256), 65536) & ~(size_t)15;
   // copy engines: four streams and pieces of 16 MiB or more sustained
   // ~4.8 TB/s of fan-out copies in a GB300 probe (one stream ~2.5, 2 MiB
@@ -482,10 +482,28 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
     chunk = (uint64_t)16 * kPerRankVectors * 32 * cfg.consumer_warps;
   const int result_slots = (store == kStoreBulk && plan.coll != kAllGather) ? 2 : 0;
   const int budget = smem_budget;
+  int max_stages = cfg.stages;
+  const uint64_t traffic = 2ull * (uint64_t)p * plan.count * (uint64_t)es;
+  if (plan.coll == kAllReduce && !plan.in_place && !plan.anchor_only && !capped &&
+      !sh.rank_streamed && default_bulk_shape(cfg) && traffic >= kArInflightMinTraffic) {
+    // a large out-of-place allreduce streamed best with about 96 KiB of
+    // loads in flight per SM, not the most that fits: GB300 sweeps, P = 2 /
+    // 4 / 8 / 16 moving 512 MiB - 2 GiB, 0.5-1% faster than 192 KiB (its P
+    // stores per chunk keep the other half of the traffic moving). Calls
+    // that store once per P loads (a reduce-scatter lost 17% this way), in
+    // place (0.5% slower) or smaller (at 256 MiB the two were within 1.5%
+    // either way; at 64-128 MiB the full ring was 5-20% faster for P = 4
+    // and 8) keep the full ring. Chunks stay at 6 KiB or more: smaller ones
+    // cost more per byte than they save.
+    chunk = std::max<uint64_t>(kArMinChunkBytes,
+                               std::min<uint64_t>(cfg.max_chunk_bytes, kArInflightBytes / 3 / nsrc));
+    chunk &= ~(uint64_t)15;
+    max_stages = (int)std::max<uint64_t>(2, std::min<uint64_t>(cfg.stages, kArInflightBytes / (nsrc * chunk)));
+  }
   int stages = 0;
   for (;;) {
     int64_t room = (int64_t)budget - 1024 - (int64_t)result_slots * (int64_t)chunk;
-    stages = room > 0 ? (int)std::min<int64_t>(cfg.stages, room / (int64_t)(nsrc * chunk)) : 0;
+    stages = room > 0 ? (int)std::min<int64_t>(max_stages, room / (int64_t)(nsrc * chunk)) : 0;
     if (stages >= 2 || chunk <= 16 || sh.rank_streamed) break;
     chunk = std::max<uint64_t>(16, (chunk / 2) & ~(uint64_t)15);
   }

@@ -51,6 +51,9 @@ struct Plan {
   uint64_t count = 0;        // the call's count argument
   uint64_t shard_elems = 0;  // shard length q
   std::vector<LogicalTask> tasks;
+  // facts about the call that steer the lowering (not part of the tasks)
+  bool in_place = false;     // allreduce: every rank's receive buffer is its send buffer
+  bool anchor_only = false;  // every window will store to one rank only (copy-out shard-in)
 };
 
 // Splits the collective into logical tasks.
@@ -85,8 +88,26 @@ struct Config {
 // Fills zero fields with the library defaults.
 Config resolve_config(const Config& in);
 
-// ---- copy-out engine decisions (host only; the kernels and copies live in
-// api.cpp and kernels_copy_out.cu)
+// The bulk engine's default pipeline shape. With all three at these values
+// an uncapped, out-of-place allreduce that stores to every rank and moves at
+// least kArInflightMinTraffic bytes (2 * P * S) sizes its ring for
+// kArInflightBytes of loads in flight per CTA (chunks of at least
+// kArMinChunkBytes); other calls, and any shape set explicitly, use
+// stage_bytes / stages / max_chunk_bytes as given (stages reduced to what
+// shared memory holds).
+constexpr int kDefaultStageBytes = 64 * 1024;
+constexpr int kDefaultStages = 8;
+constexpr size_t kDefaultMaxChunkBytes = 16384;
+constexpr uint64_t kArInflightBytes = 96 * 1024;
+constexpr uint64_t kArMinChunkBytes = 6144;
+constexpr uint64_t kArInflightMinTraffic = (uint64_t)512 << 20;
+inline bool default_bulk_shape(const Config& c) {
+  return c.stage_bytes == kDefaultStageBytes && c.stages == kDefaultStages &&
+         c.max_chunk_bytes == kDefaultMaxChunkBytes;
+}
+
+// ---- copy-out engine decisions (host only; the launches and copies live in
+// copy_out_host.cpp, the fold kernel in kernels_copy_out.cu)
 constexpr int kMaxCeSegments = 64;
 constexpr size_t kCeAutoMinBytes = (size_t)4 << 20;
 constexpr uint64_t kFoldMaxVectors = (uint64_t)1 << 28;  // per launch job, 32-bit indices

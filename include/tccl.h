@@ -118,6 +118,15 @@ typedef enum {
  * TCCL_WAIT_TIMEOUT_MS, TCCL_CHUNK_ORDER, TCCL_PREFETCH_CHUNKS,
  * TCCL_LOAD_POLICY, TCCL_MAX_CHUNK_BYTES, TCCL_STAGE_LAYOUT, TCCL_CE_STREAMS,
  * TCCL_CE_SEGMENT_BYTES and TCCL_CE_AUTO_MAX_CAP once). Zero in a field means "library default".
+ *
+ * Bulk-engine shape: stage_bytes, stages and max_chunk_bytes default to 64 KiB,
+ * 8 and 16 KiB, and a call uses them as given (stages reduced to what shared
+ * memory holds), with one exception: while all three hold exactly those
+ * defaults, an uncapped, out-of-place allreduce on the bulk engine's shared
+ * stage layout that moves 2 * P * S >= 512 MiB keeps about 96 KiB of loads in
+ * flight per CTA instead: chunks of 32 KiB / P bytes (at least 6 KiB, at most
+ * max_chunk_bytes) and 96 KiB / (P * chunk) stages (at least 2), which
+ * streamed 0.5-1% faster on GB300 than a full ring.
  */
 typedef struct {
   int engine;              /* tcclEngine_t */
@@ -135,7 +144,7 @@ typedef struct {
   int load_policy;         /* bulk engine: L2 policy of bulk loads: 0 default, 1 evict-first, 2 evict-normal */
   size_t max_chunk_bytes;  /* bulk engine: upper bound on bytes per source per chunk */
   int stage_layout;        /* bulk engine: tcclStageLayout_t */
-  int ce_streams;          /* copy-out engine: internal copy streams, 1..8 (default 2) */
+  int ce_streams;          /* copy-out engine: internal copy streams, 1..8 (default 4) */
   size_t ce_segment_bytes; /* copy-out engine: most bytes per rank in one segment (default
                               32 MiB; a call is cut into at least four segments of at least
                               4 MiB where it can be; rounded down to a multiple of 256) */

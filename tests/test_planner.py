@@ -243,6 +243,49 @@ def test_pipeline_shape_follows_shared_memory():
     assert small.smem_bytes <= 48 * 1024 and small.stages >= 2
 
 
+@pytest.mark.parametrize("p,chunk,stages", [(1, 16384, 6), (2, 16384, 3), (3, 10912, 3), (4, 8192, 3),
+                                             (8, 6144, 2), (16, 6144, 2), (32, 3072, 2)])
+def test_uncapped_allreduce_default_shape(p, chunk, stages):
+    """With the default shape a large out-of-place allreduce (2 * P * S of
+    512 MiB or more) sizes its ring for about 96 KiB of loads per CTA, in
+    6 KiB chunks or more: stages * P * chunk stays within 96 KiB unless two
+    stages need more."""
+    send, recv = bufs(p, 0, 0)
+    count = -(-(512 << 20) // (2 * p * 2))  # bf16: exactly at the threshold
+    r, wins, _, info = inspect(AR, p, count, tccl.tcclBfloat16, send, recv, engine=tccl.tcclEngineBulk)
+    assert r == 0 and info.stage_layout == tccl.tcclLayoutShared
+    assert (info.chunk_bytes, info.stages) == (chunk, stages)
+    assert stages == 2 or stages * p * chunk <= 96 * 1024
+    check_cover(AR, p, count, 2, send, recv, wins, info)
+
+
+@pytest.mark.parametrize("p", [2, 4, 8])
+def test_other_calls_keep_the_full_ring(p):
+    """The 96 KiB rule is for large, uncapped, out-of-place allreduce only: a
+    reduce-scatter, a capped or in-place or smaller allreduce and an
+    explicitly set shape fill shared memory."""
+    send, recv = bufs(p, 0, 0)
+    big = (512 << 20) // (2 * p * 2)
+    full = lambda info: info.smem_bytes > 150 * 1024
+    ring = lambda info: info.chunk_bytes == min(16384, 65536 // p)
+    r, _, _, rs = inspect(RS, p, big, tccl.tcclBfloat16, send, recv, engine=tccl.tcclEngineBulk)
+    assert r == 0 and full(rs) and ring(rs)
+    r, _, _, capped = inspect(AR, p, big, tccl.tcclBfloat16, send, recv, cap=16,
+                              engine=tccl.tcclEngineBulk)
+    assert r == 0 and full(capped)
+    r, _, _, explicit = inspect(AR, p, big, tccl.tcclBfloat16, send, recv, engine=tccl.tcclEngineBulk,
+                                stage_bytes=65536, stages=7)
+    assert r == 0 and full(explicit) and ring(explicit)
+    r, _, _, small = inspect(AR, p, big - 8, tccl.tcclBfloat16, send, recv, engine=tccl.tcclEngineBulk)
+    assert r == 0 and full(small) and ring(small)
+    r, _, _, inpl = inspect(AR, p, big, tccl.tcclBfloat16, send, list(send), engine=tccl.tcclEngineBulk)
+    assert r == 0 and full(inpl) and ring(inpl)
+    mixed = list(send)
+    mixed[-1] = recv[-1]  # one rank out of place: the call is not in place
+    r, _, _, part = inspect(AR, p, big, tccl.tcclBfloat16, send, mixed, engine=tccl.tcclEngineBulk)
+    assert r == 0 and not full(part)
+
+
 @pytest.mark.parametrize("p", [2, 8, 64])
 @pytest.mark.parametrize("cw", [8, 16])
 def test_per_rank_stage_layout_shape(p, cw):
