@@ -870,25 +870,35 @@ def reshard_bench(args):
         dl = tccl.make_layout(dst[0], dst[1], rs.nranks(src[0]))
         r, tr, br, bw, nw = tccl.tcclReshardInspect(sl, dl, list(shape), tccl.tcclBfloat16,
                                                     sends, recvs)
-        fn = lambda: g.reshard(sends, sl, recvs, dl, shape)
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            fn()
-        e1.record(stream)
-        e1.synchronize()
-        ms = e0.elapsed_time(e1) / args.steps
-        ok = all(np.array_equal(t.view(torch.int16).cpu().numpy().view(np.uint16), e)
-                 for t, e in zip(recvs, exp))
-        print(json.dumps({"mode": "reshard", "case": name, "tensor": "bf16 8192x8192",
-                          "transfers": len(tr), "windows": nw, "bytes_read": br,
-                          "bytes_written": bw, "us": round(ms * 1e3, 2),
-                          "GBps": round((br + bw) / (ms * 1e-3) / 1e9, 1),
-                          "hbm_fraction": round((br + bw) / (ms * 1e-3) / 1e9 / peak, 4),
-                          "correct": ok}), flush=True)
+        # the default (the bulk ring for these co-aligned buffers), then the
+        # register-copy kernel the group uses when asked for the warp engine
+        for engine in (tccl.tcclEngineAuto, tccl.tcclEngineWarp):
+            c = tccl.tcclConfig_t()
+            c.engine = engine
+            assert tccl.tcclGroupSetConfig(g.handle, c) == tccl.tcclSuccess
+            for t in recvs:
+                t.zero_()
+            fn = lambda: g.reshard(sends, sl, recvs, dl, shape)
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            info = g.last_launch()
+            ok = all(np.array_equal(t.view(torch.int16).cpu().numpy().view(np.uint16), e)
+                     for t, e in zip(recvs, exp))
+            print(json.dumps({"mode": "reshard", "case": name, "tensor": "bf16 8192x8192",
+                              "engine": "bulk ring" if info["engine"] == tccl.tcclEngineBulk else "warp copies",
+                              "ctas": info["ctas"], "transfers": len(tr), "windows": nw, "bytes_read": br,
+                              "bytes_written": bw, "us": round(ms * 1e3, 2),
+                              "GBps": round((br + bw) / (ms * 1e-3) / 1e9, 1),
+                              "hbm_fraction": round((br + bw) / (ms * 1e-3) / 1e9 / peak, 4),
+                              "correct": ok}), flush=True)
         del sends, recvs
     assert g.query_error() == tccl.tcclSuccess
     g.close()

@@ -499,6 +499,7 @@ tcclResult_t tcclGroupCreate(int nranks, tcclGroup_t* out) {
   g->cfg = config_from_env();
   if (const char* e = std::getenv("TCCL_RMSNORM_CLUSTER")) g->rms_cluster_enabled = std::atoi(e) != 0;
   if (prepare_bulk_kernels((size_t)g->dev.smem_optin) != 0) return tcclCudaError;
+  if (prepare_reshard_kernels((size_t)g->dev.smem_optin) != 0) return tcclCudaError;
   if (cudaMalloc(&g->d_status, 64) != cudaSuccess) return tcclCudaError;
   if (cudaMalloc(&g->d_sm_mask, 64) != cudaSuccess) {
     cudaFree(g->d_status);
@@ -634,6 +635,8 @@ tcclResult_t tcclReshard(tcclGroup_t g, const void* const srcbufs[], const tcclL
   put(shape, sizeof(uint64_t) * tensor_ndims);
   put(&es, sizeof(int));
   put(&cta_cap, sizeof(int));
+  // the group's engine setting picks between the bulk ring and warp copies
+  put(&g->cfg.engine, sizeof(int));
   std::vector<uint8_t> sm(sl.size()), dm(dl.size());
   for (int m = 0; m < sl.size(); ++m) sm[m] = (uint8_t)((uintptr_t)srcbufs[m] & 15);
   for (int m = 0; m < dl.size(); ++m) dm[m] = (uint8_t)((uintptr_t)dstbufs[m] & 15);
@@ -650,13 +653,14 @@ tcclResult_t tcclReshard(tcclGroup_t g, const void* const srcbufs[], const tcclL
   } else {
     auto fresh = std::make_unique<CachedReshard>();
     if (!plan_reshard(sl, dl, tensor_ndims, shape, es, sm.data(), dm.data(), g->dev.sm_count,
-                      cta_cap, &fresh->plan, &why)) {
+                      cta_cap, g->cfg.engine, (size_t)g->dev.smem_optin, &fresh->plan, &why)) {
       if (log_level()) std::fprintf(stderr, "[tccl] reshard: %s\n", why.c_str());
       result = tcclInvalidArgument;
     } else {
+      // device table: windows, unit prefix, then two zeroed claim words
       const size_t wb = fresh->plan.win.size() * sizeof(ReshardWindow);
       const size_t pb = fresh->plan.unit_prefix.size() * sizeof(uint64_t);
-      std::vector<unsigned char> host(wb + pb);
+      std::vector<unsigned char> host(wb + pb + 16, 0);
       if (wb) std::memcpy(host.data(), fresh->plan.win.data(), wb);
       std::memcpy(host.data() + wb, fresh->plan.unit_prefix.data(), pb);
       if (cudaMalloc(&fresh->d_table, host.size()) != cudaSuccess ||
@@ -671,17 +675,32 @@ tcclResult_t tcclReshard(tcclGroup_t g, const void* const srcbufs[], const tcclL
   if (result == tcclSuccess && !cr->plan.win.empty()) {
     ReshardArgs a;
     std::memset(&a, 0, sizeof(a));
+    const size_t wb = cr->plan.win.size() * sizeof(ReshardWindow);
+    const size_t pb = cr->plan.unit_prefix.size() * sizeof(uint64_t);
     a.win = reinterpret_cast<const ReshardWindow*>(cr->d_table);
-    a.unit_prefix = reinterpret_cast<const uint64_t*>(cr->d_table + cr->plan.win.size() * sizeof(ReshardWindow));
+    a.unit_prefix = reinterpret_cast<const uint64_t*>(cr->d_table + wb);
+    a.sched = reinterpret_cast<unsigned long long*>(cr->d_table + wb + pb);
     for (int m = 0; m < sl.size(); ++m) a.src[m] = srcbufs[m];
     for (int m = 0; m < dl.size(); ++m) a.dst[m] = dstbufs[m];
     a.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
+    a.status = g->d_status;
+    a.timeout_ns = (uint64_t)(g->cfg.wait_timeout_ms * 1e6);
+    a.inject_timeout_ns = g->inject_ns;
     a.nwin = (int)cr->plan.win.size();
     a.elem_size = es;
-    if (launch_reshard(a, cr->plan.grid, cta_cap <= 0, stream) != 0) result = tcclCudaError;
+    const int rc = cr->plan.engine == kReshardBulk
+                       ? launch_reshard_bulk(a, cr->plan.grid, cr->plan.smem, cta_cap <= 0, stream)
+                       : launch_reshard(a, cr->plan.grid, cta_cap <= 0, stream);
+    if (rc != 0) result = tcclCudaError;
     std::memset(&g->last, 0, sizeof(g->last));
+    const bool bulk = cr->plan.engine == kReshardBulk;
+    g->last.engine = bulk ? kEngineBulk : kEngineWarp;
     g->last.ctas = cr->plan.grid;
-    g->last.threads = 256;
+    g->last.threads = cr->plan.threads;
+    g->last.stages = bulk ? kReshardBulkStages : 0;
+    g->last.chunk_bytes = bulk ? kReshardBulkSegBytes : kReshardSegBytes;
+    g->last.smem_bytes = cr->plan.smem;
+    g->last.total_chunks = cr->plan.unit_prefix.back();
     g->last.windows = (int)cr->plan.win.size();
     g->last.tasks = (int)cr->plan.transfers.size();
   }
@@ -784,7 +803,7 @@ tcclResult_t tcclReshardInspect(const tcclLayout_t* src, const tcclLayout_t* dst
   for (int m = 0; m < dl.size(); ++m) dm[m] = (uint8_t)((uintptr_t)dstbufs[m] & 15);
   ReshardPlan plan;
   if (!plan_reshard(sl, dl, tensor_ndims, shape, es, sm.data(), dm.data(), sm_count, cta_cap,
-                    &plan, &why))
+                    kEngineAuto, 232448, &plan, &why))
     return tcclInvalidArgument;
   *n_transfers = (int)plan.transfers.size();
   *bytes_read = (int64_t)plan.bytes_read;

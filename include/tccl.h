@@ -350,6 +350,16 @@ tcclResult_t tcclAllReduceRMSNorm(tcclGroup_t g, const void* const sendbufs[],
  * block needs is read once, from the least-loaded source replica, and written
  * to every destination replica of that block.
  *
+ * Engines (the group's tcclConfig_t.engine): with every piece 16-byte
+ * co-aligned in every buffer, a bulk ring (one CTA per SM, bulk loads into
+ * shared memory, bulk stores to every replica) runs the copies under
+ * tcclEngineBulk always, and under Auto when blocks have three or more
+ * replicas on average and every row piece is 4 KiB or more; otherwise, and
+ * always under tcclEngineWarp or tcclEngineVec, warps copy through
+ * registers. A ring wait that runs out is reported by tcclGroupQueryError as
+ * tcclDeviceTimeout. As for every call on a group, reshards on different
+ * streams need an ordering between them (a plan's ring keeps one work counter).
+ *
  * Errors: tcclInvalidArgument for a bad layout, shape, pointer or overlap
  * (destination buffers may not overlap each other or any source), or meshes
  * outside the group's ranks.

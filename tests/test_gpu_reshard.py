@@ -29,7 +29,26 @@ def src_blocks(glob, dims, place):
     return out
 
 
-def run(g, glob, src, dst, dtype, cap=0, mis=0):
+ENGINES = {"auto": tccl.tcclEngineAuto, "bulk": tccl.tcclEngineBulk, "warp": tccl.tcclEngineWarp}
+
+
+def edges_aligned(shape, layout, es):
+    """Every block of the layout starts and ends on a 16-byte boundary of its
+    rows (so every piece, offset and pitch of a reshard between two such
+    layouts is whole 16-byte vectors)."""
+    return all(lo * es % 16 == 0 and hi * es % 16 == 0
+               for m in range(rs.nranks(layout[0]))
+               for lo, hi in [rs.local_box(shape, layout[0], layout[1], m)[-1]])
+
+
+def set_engine(g, engine):
+    c = tccl.tcclConfig_t()
+    c.engine = ENGINES[engine]
+    assert tccl.tcclGroupSetConfig(g.handle, c) == tccl.tcclSuccess
+
+
+def run(g, glob, src, dst, dtype, cap=0, mis=0, engine="auto"):
+    set_engine(g, engine)
     shape = glob.shape
     sb = src_blocks(glob, *src)
     exp = rs.reshard(sb, src[0], src[1], dst[0], dst[1], shape)
@@ -44,10 +63,21 @@ def run(g, glob, src, dst, dtype, cap=0, mis=0):
               shape, cta_cap=cap)
     torch.cuda.synchronize()
     assert g.query_error() == tccl.tcclSuccess
+    # asked for, the bulk ring runs every 16-byte co-aligned plan; a plan
+    # with an element-wise piece, or a request for warps, runs on warps
+    es = np.dtype(exp[0].dtype).itemsize
+    aligned = mis % 16 == 0 and edges_aligned(shape, src, es) and edges_aligned(shape, dst, es)
+    misaligned = mis % 16 != 0 or any(e.size * es % 16 for e in exp)
+    info = g.last_launch()
+    if engine == "warp" or misaligned:
+        assert info["engine"] == tccl.tcclEngineWarp, info
+    if engine == "bulk" and aligned:
+        assert info["engine"] == tccl.tcclEngineBulk and info["threads"] == 64, info
     for m, (t, e) in enumerate(zip(recvs, exp)):
         assert t.guards_intact()
         mm = first_mismatch(t.host(), e)
-        assert mm is None, f"{src} -> {dst} {dtype}: rank {m} first mismatch {mm}"
+        assert mm is None, f"{src} -> {dst} {dtype} ({engine}): rank {m} first mismatch {mm}"
+    return info
 
 
 @pytest.fixture(scope="module")
@@ -75,20 +105,86 @@ LAYOUTS = [((4,), (0,)), ((4,), (R,)), ((2, 2), (R, 0)), ((2, 2), (0, R)), ((2, 
            ((1, 4), (R, 1)), ((2, 4), (R, 0)), ((8,), (1,)), ((2, 1, 2), (R, R, 1))]
 
 
+@pytest.mark.parametrize("engine", ["bulk", "warp"])
 @pytest.mark.parametrize("src", LAYOUTS)
 @pytest.mark.parametrize("dst", LAYOUTS[::2])
-def test_layout_pairs(group, src, dst):
+def test_layout_pairs(group, src, dst, engine):
     glob = global_tensor("f32", (64, 96))
-    run(group, glob, src, dst, "f32")
+    info = run(group, glob, src, dst, "f32", engine=engine)
+    if engine == "bulk":
+        assert info["engine"] == tccl.tcclEngineBulk, info
 
 
+@pytest.mark.parametrize("src,dst,bulk", [
+    (((2,), (0,)), ((8,), (R,)), True),            # 8 replicas, whole rows
+    (((8,), (0,)), ((4, 2), (R, 1)), True),        # 4 replicas, 8 KiB row pieces
+    (((1, 4), (R, 0)), ((2, 2), (R, 0)), False),   # 2 replicas
+    (((8,), (1,)), ((8,), (0,)), False),           # 1 replica, 2 KiB row pieces
+    (((8,), (1,)), ((4,), (R,)), False),           # 4 replicas, but 2 KiB row pieces
+    (((8,), (0,)), ((16,), (R,)), True)])          # 16 replicas, whole blocks
+def test_auto_engine_choice(group, src, dst, bulk):
+    """Auto takes the bulk ring for co-aligned plans that write every block
+    to three or more replicas on average in row pieces of 4 KiB or more, and
+    warp copies otherwise."""
+    glob = global_tensor("bf16", (512, 8192), seed=13)
+    info = run(group, glob, src, dst, "bf16", engine="auto")
+    assert (info["engine"] == tccl.tcclEngineBulk) == bulk, info
+
+
+@pytest.mark.parametrize("engine", ["bulk", "warp"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
 @pytest.mark.parametrize("mis", [0, 4])
 @pytest.mark.parametrize("cap", [0, 3])
-def test_dtypes_alignment_caps(group, dtype, mis, cap):
+def test_dtypes_alignment_caps(group, dtype, mis, cap, engine):
     glob = global_tensor(dtype, (256, 1000))
-    run(group, glob, ((8,), (1,)), ((2, 2), (R, 0)), dtype, cap=cap, mis=mis)
-    run(group, glob, ((4,), (0,)), ((2, 4), (R, 1)), dtype, cap=cap, mis=mis)
+    run(group, glob, ((8,), (1,)), ((2, 2), (R, 0)), dtype, cap=cap, mis=mis, engine=engine)
+    run(group, glob, ((4,), (0,)), ((2, 4), (R, 1)), dtype, cap=cap, mis=mis, engine=engine)
+    if cap:
+        assert group.last_launch()["ctas"] <= cap
+
+
+@pytest.mark.parametrize("shape", [(3, 40000), (40000, 24), (7, 8192 + 16), (1, 16384 * 3 + 16)])
+def test_bulk_unit_shapes(group, shape):
+    """The bulk ring's work units: rows longer than a stage cut into 16 KiB
+    segments with a ragged last one, rows shorter than a stage packed many
+    to a stage with a ragged last stage, and a single row."""
+    glob = global_tensor("bf16", shape, seed=11)
+    ran = 0
+    for src, dst in ((((1,), (R,)), ((2, 2), (R, 1))), (((2,), (0,)), ((4,), (R,))),
+                     (((1,), (R,)), ((3,), (R,)))):
+        if any(d != R and shape[d] % n for dims, place in (src, dst) for n, d in zip(dims, place)):
+            continue
+        info = run(group, glob, src, dst, "bf16", engine="bulk")
+        if edges_aligned(shape, src, 2) and edges_aligned(shape, dst, 2):
+            assert info["engine"] == tccl.tcclEngineBulk, info
+            ran += 1
+    assert ran >= 1
+
+
+def test_bulk_timeout_path(group):
+    """A bulk-ring wait that runs out (the test hook holds CTA 0's first stage
+    on a barrier nothing completes) is reported as a device timeout, and the
+    next reshard on the same group is exact."""
+    glob = global_tensor("bf16", (1024, 2048), seed=12)
+    set_engine(group, "bulk")  # a 2-replica plan: on the ring only when asked for
+    src, dst = ((4,), (0,)), ((2, 2), (R, 1))
+    sb = src_blocks(glob, *src)
+    exp = rs.reshard(sb, src[0], src[1], dst[0], dst[1], glob.shape)
+    sends = [to_device(b) for b in sb]
+    recvs = [torch.empty(e.size, dtype=torch.bfloat16, device="cuda") for e in exp]
+    args = (sends, tccl.make_layout(src[0], src[1], 0), recvs, tccl.make_layout(dst[0], dst[1], 4), glob.shape)
+    assert tccl.tcclGroupInjectWaitTimeout(group.handle, True, 50.0) == tccl.tcclSuccess
+    try:
+        group.reshard(*args)
+        assert group.query_error() == tccl.tcclDeviceTimeout
+    finally:
+        assert tccl.tcclGroupInjectWaitTimeout(group.handle, False, 0.0) == tccl.tcclSuccess
+    group.reshard(*args)
+    torch.cuda.synchronize()
+    assert group.query_error() == tccl.tcclSuccess
+    assert group.last_launch()["engine"] == tccl.tcclEngineBulk
+    for t, e in zip(recvs, exp):
+        assert first_mismatch(to_host(t), e) is None
 
 
 def test_three_dimensional(group):
@@ -114,8 +210,9 @@ def random_layout(rng, ndim):
     return dims, tuple(place)
 
 
+@pytest.mark.parametrize("engine", ["bulk", "warp"])
 @pytest.mark.parametrize("case", range(40))
-def test_random_reshard(group, case):
+def test_random_reshard(group, case, engine):
     """Seeded random layout pairs: meshes of one to three axes (each of size
     one to four), Replicate or one Shard per layout, tensors of one to three
     dimensions whose sharded extents the mesh axes divide, three dtypes,
@@ -142,4 +239,4 @@ def test_random_reshard(group, case):
     mis = int(rng.integers(0, 16 // es)) * es if rng.random() < 0.3 else 0
     cap = int(rng.choice([0, 0, 1, 5, 40]))
     glob = global_tensor(dtype, tuple(shape), seed=case)
-    run(group, glob, src, dst, dtype, cap=cap, mis=mis)
+    run(group, glob, src, dst, dtype, cap=cap, mis=mis, engine=engine)
