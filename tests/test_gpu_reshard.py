@@ -240,3 +240,36 @@ def test_random_reshard(group, case, engine):
     cap = int(rng.choice([0, 0, 1, 5, 40]))
     glob = global_tensor(dtype, tuple(shape), seed=case)
     run(group, glob, src, dst, dtype, cap=cap, mis=mis, engine=engine)
+
+
+@pytest.mark.parametrize("engine", ["bulk", "warp"])
+def test_graph_capture_replay(group, engine):
+    """Reshards captured into a CUDA graph (three back-to-back calls of one
+    plan, so the bulk ring's claim counter must reset between launches) and
+    replayed twice: every replay rebuilds the destination blocks exactly."""
+    set_engine(group, engine)
+    glob = global_tensor("bf16", (2048, 4096), seed=14)
+    src, dst = ((2,), (0,)), ((4, 2), (R, 1))
+    sb = src_blocks(glob, *src)
+    exp = rs.reshard(sb, src[0], src[1], dst[0], dst[1], glob.shape)
+    sends = [to_device(b) for b in sb]
+    recvs = [torch.zeros(e.size, dtype=torch.bfloat16, device="cuda") for e in exp]
+    sl, dl = tccl.make_layout(src[0], src[1], 0), tccl.make_layout(dst[0], dst[1], 2)
+    s = torch.cuda.Stream()
+    group.reshard(sends, sl, recvs, dl, glob.shape, stream=s.cuda_stream)  # plans outside the capture
+    torch.cuda.synchronize()
+    assert group.last_launch()["engine"] == ENGINES[engine]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for _ in range(3):
+            group.reshard(sends, sl, recvs, dl, glob.shape, stream=s.cuda_stream)
+    for _ in range(2):
+        for r in recvs:
+            r.zero_()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert group.query_error() == tccl.tcclSuccess
+        for m, (t, e) in enumerate(zip(recvs, exp)):
+            mm = first_mismatch(to_host(t), e)
+            assert mm is None, f"{engine} replay: rank {m} first mismatch {mm}"
