@@ -617,10 +617,32 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
     fence_mbar_init();
   }
   // An early (programmatic dependent) launch gets here while the stream's
-  // previous kernel may still run: every global access comes after this
-  // wait, which returns once that kernel has finished and its writes are
-  // visible (at once for an ordinary launch). The next launch may then be
-  // scheduled: its CTAs take this SM only after this CTA exits.
+  // previous kernel may still run. Before waiting for it, warm L2 with this
+  // CTA's first chunks (in the dynamic order they are fixed: blockIdx.x,
+  // + gridDim.x, ...). A prefetch writes nothing, and L2 is where every
+  // write lands, so a line the previous kernel still writes is never read
+  // stale; the chunk table is the host's upload, no kernel's output.
+  if (threadIdx.x == 0 && a.order == kOrderDynamic && !(COLL != kAllGather && a.rank_streamed)) {
+    ChunkLocator pl;
+    pl.init();
+    for (int j = 0; j < S; ++j) {
+      const uint64_t c = blockIdx.x + static_cast<uint64_t>(j) * gridDim.x;
+      if (c >= a.total_chunks) break;
+      uint32_t po, pn;
+      pl.locate(a, c, po, pn);
+      if (COLL == kAllGather) {
+        const char* src = static_cast<const char*>(a.p.src[pl.w.src_sel < 0 ? 0 : pl.w.src_sel]);
+        bulk_prefetch_l2(src + pl.w.src_off + po, pn);
+      } else {
+        for (int r = 0; r < P; ++r)
+          bulk_prefetch_l2(static_cast<const char*>(a.p.src[r]) + pl.w.src_off + po, pn);
+      }
+    }
+  }
+  // Every other global access comes after this wait, which returns once the
+  // previous kernel has finished and its writes are visible (at once for an
+  // ordinary launch). The next launch may then be scheduled: its CTAs take
+  // this SM only after this CTA exits.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) record_sm(a.sm_mask);

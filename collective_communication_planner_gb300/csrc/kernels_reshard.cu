@@ -7,15 +7,29 @@ namespace tccl {
 namespace {
 
 __global__ void __launch_bounds__(256) reshard_kernel(const __grid_constant__ ReshardArgs a) {
-  // an early (programmatic dependent) launch waits here for the stream's
-  // previous kernel before any global access
+  const int lane = threadIdx.x & 31;
+  const uint64_t nunits = a.unit_prefix[a.nwin];  // the host's upload, no kernel's output
+  const uint64_t warp = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const uint64_t nwarps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
+  // an early (programmatic dependent) launch gets here while the stream's
+  // previous kernel may still run: each warp first warms L2 with its first
+  // row segment (a prefetch writes nothing, and L2 is where every write
+  // lands), then waits before any access to the buffers
+  if (lane == 0 && warp < nunits) {
+    const int wi = dev::find_window<0>(a.unit_prefix, a.nwin, warp);
+    const ReshardWindow& w = a.win[wi];
+    if (!w.scalar) {
+      const uint64_t k = warp - a.unit_prefix[wi];
+      const uint64_t segs = (w.bytes + kReshardSegBytes - 1) / kReshardSegBytes;
+      const uint64_t row = k / segs;
+      const uint32_t begin = static_cast<uint32_t>(k - row * segs) * kReshardSegBytes;
+      dev::bulk_prefetch_l2(static_cast<const char*>(a.src[w.src]) + w.src_off + row * w.src_pitch + begin,
+                            min(kReshardSegBytes, w.bytes - begin));
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) dev::record_sm(a.sm_mask);
-  const int lane = threadIdx.x & 31;
-  const uint64_t nunits = a.unit_prefix[a.nwin];
-  const uint64_t warp = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const uint64_t nwarps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
   for (uint64_t u = warp; u < nunits; u += nwarps) {
     const int wi = dev::find_window<0>(a.unit_prefix, a.nwin, u);
     const ReshardWindow w = a.win[wi];
@@ -138,14 +152,30 @@ __global__ void __launch_bounds__(kReshardBulkThreads, 1)
     h.abort_flag = 0;
     fence_mbar_init();
   }
-  // an early (programmatic dependent) launch waits here for the stream's
-  // previous kernel before any global access
+  const uint64_t nunits = a.unit_prefix[a.nwin];  // the host's upload, no kernel's output
+  // an early (programmatic dependent) launch gets here while the stream's
+  // previous kernel may still run: thread 0 first warms L2 with this CTA's
+  // fixed first units (a prefetch writes nothing, and L2 is where every
+  // write lands, so nothing is read stale), then all wait before any access
+  // to the buffers
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < S; ++j) {
+      const uint64_t u = blockIdx.x + static_cast<uint64_t>(j) * gridDim.x;
+      if (u >= nunits) break;
+      const int wi = find_window<0>(a.unit_prefix, a.nwin, u);
+      const ReshardWindow& w = a.win[wi];
+      const BulkUnit bu = decode_bulk_unit(w, u - a.unit_prefix[wi]);
+      const char* src = static_cast<const char*>(a.src[w.src]) + w.src_off +
+                        static_cast<uint64_t>(bu.row) * w.src_pitch + bu.begin;
+      for (uint32_t r = 0; r < min(bu.rows, 8u); ++r)  // a few rows of a unit of short ones
+        bulk_prefetch_l2(src + static_cast<uint64_t>(r) * w.src_pitch, bu.n);
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) record_sm(a.sm_mask);
   __syncthreads();
   if ((threadIdx.x & 31) != 0) return;
-  const uint64_t nunits = a.unit_prefix[a.nwin];
 
   if (threadIdx.x == 0) {
     const uint64_t grid = gridDim.x;

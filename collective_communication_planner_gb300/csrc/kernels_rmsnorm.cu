@@ -21,8 +21,14 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rmsnorm_kernel(const __grid_co
   extern __shared__ __align__(16) uint4 gamma_smem[];
   __shared__ float partial[kRmsMaxThreads / 32];
   __shared__ float row_scale;
-  // an early (programmatic dependent) launch waits here for the stream's
-  // previous kernel before any global access
+  const uint32_t row_bytes = a.hidden * (DT == kBF16 ? 2u : 4u);
+  // an early (programmatic dependent) launch gets here while the stream's
+  // previous kernel may still run: it first warms L2 with this CTA's first
+  // row of every rank (a prefetch writes nothing and L2 is where every write
+  // lands, so nothing is read stale), then waits before any global access
+  if (threadIdx.x < a.nranks && blockIdx.x < a.rows)
+    dev::bulk_prefetch_l2(static_cast<const char*>(a.p.src[threadIdx.x]) + blockIdx.x * static_cast<uint64_t>(row_bytes),
+                          row_bytes);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) dev::record_sm(a.sm_mask);
@@ -114,9 +120,6 @@ __global__ void __launch_bounds__(kRmsClusterThreads)
   cg::cluster_group cluster = cg::this_cluster();
   const int q = static_cast<int>(cluster.block_rank());
   const int C = static_cast<int>(cluster.num_blocks());
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // as in rmsnorm_kernel
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) dev::record_sm(a.sm_mask);
   const int P = a.nranks;
   const uint32_t nvec = a.hidden / kVecElems;
   const uint32_t per = (nvec + C - 1) / C;
@@ -125,6 +128,15 @@ __global__ void __launch_bounds__(kRmsClusterThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const uint64_t cid = blockIdx.x / C;
   const uint64_t nclusters = gridDim.x / C;
+  // as in rmsnorm_kernel: warm L2 with this CTA's slice of its first row of
+  // every rank, then wait for the previous kernel before any global access
+  if (threadIdx.x < P && cid < a.rows && v1 > v0)
+    dev::bulk_prefetch_l2(static_cast<const char*>(a.p.src[threadIdx.x]) +
+                              cid * static_cast<uint64_t>(a.hidden) * (DT == kBF16 ? 2 : 4) + v0 * 16ull,
+                          (v1 - v0) * 16u);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) dev::record_sm(a.sm_mask);
   for (uint64_t t = cid; t < a.rows; t += nclusters) {
     const uint64_t row_off = t * static_cast<uint64_t>(a.hidden) * (DT == kBF16 ? 2 : 4);
     Fold<DT, kSum> acc[V];
