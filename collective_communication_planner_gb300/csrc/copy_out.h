@@ -26,6 +26,7 @@ struct AnchorArgs {
   uint64_t job_src_stride;
   int njobs;
   int nranks;
+  int prefetch_first;  // set by the launcher for early launches: warm L2 before the wait
 };
 
 // Vectors each thread folds at a time: two for P = 2 and 4, one otherwise.

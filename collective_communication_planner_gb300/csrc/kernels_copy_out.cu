@@ -65,17 +65,29 @@ template <int DT, int OP, int NP, int U>
 __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const __grid_constant__ AnchorArgs a) {
   constexpr int RB = NP > 0 ? NP : 8 / U;
   constexpr int es = DT == kBF16 ? 2 : 4;
-  // an early (programmatic dependent) launch waits here for the stream's
-  // previous kernel before any global access
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) record_sm(a.sm_mask);
   const int P = NP > 0 ? NP : a.nranks;
   // a job covers fewer than 2^28 vectors (register_fold_ok keeps larger ones
   // off this kernel), so vector indices and byte offsets within it fit 32 bits
   const uint32_t nthr = gridDim.x * blockDim.x;
   const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const uint32_t nvec = static_cast<uint32_t>(a.nvec);
+  // an early (programmatic dependent) launch gets here while the stream's
+  // previous kernel may still run: it first warms L2 with the block's first
+  // vectors of job 0 in every rank (a prefetch writes nothing, and L2 is
+  // where every write lands, so nothing is read stale), then waits before
+  // any global access
+  if (a.prefetch_first && threadIdx.x < static_cast<unsigned>(P)) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t vs = blockIdx.x * blockDim.x + u * nthr;
+      if (vs < nvec)
+        bulk_prefetch_l2(static_cast<const char*>(a.p.src[threadIdx.x]) + a.head_bytes + static_cast<uint64_t>(vs) * 16,
+                         min(blockDim.x, nvec - vs) * 16u);
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) record_sm(a.sm_mask);
   // the two policy registers fit beside one vector per thread (64 registers
   // at 1024 threads), not beside two
   constexpr bool kHint = U == 1;
@@ -143,7 +155,9 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
 }
 
 template <int C, int D, int O>
-int launch_anchor_t(const AnchorArgs& a, int grid, bool early, cudaStream_t st) {
+int launch_anchor_t(const AnchorArgs& args, int grid, bool early, cudaStream_t st) {
+  AnchorArgs a = args;
+  a.prefetch_first = early ? 1 : 0;  // an ordinary launch has nothing to overlap
   LaunchShape s;
   s.grid = grid;
   s.threads = kAnchorThreads;
