@@ -339,6 +339,9 @@ def run_ours(args, w, rank, world, dist):
     # pinned host memory, reduces, and copies every result back. Two device
     # buffer sets and three streams let step i+1's inputs travel while step
     # i's results come back (the host link carries both directions at once).
+    # Each step goes in `pieces` slices of the rank buffers (one allreduce
+    # call per slice), so a slice's results travel back while the next
+    # slice's inputs arrive: only a slice's reduction is not overlapped.
     h_in = [h.pin_memory() for h in host]
     h_out = [torch.empty_like(h).pin_memory() for h in host]
     e2e_steps = max(3, min(args.steps, 20))
@@ -346,7 +349,10 @@ def run_ours(args, w, rank, world, dist):
     sets = [(sends, recvs)]
     d2 = [torch.empty_like(t) for t in sends]
     sets.append((d2, d2 if w["in_place"] else [torch.empty_like(t) for t in sends]))
-    ev_in = [torch.cuda.Event() for _ in range(2)]
+    pieces = max(1, min(args.e2e_pieces, n // 4096))
+    cut = [n * k // pieces // 4096 * 4096 for k in range(pieces)] + [n]  # 16-byte aligned slices
+    ev_in = [[torch.cuda.Event() for _ in range(pieces)] for _ in range(2)]
+    ev_piece = [[torch.cuda.Event() for _ in range(pieces)] for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
@@ -355,22 +361,26 @@ def run_ours(args, w, rank, world, dist):
             b = i % 2
             snd, rcv = sets[b]
             if i >= 2:
-                s_in.wait_event(ev_done[b])   # the kernel of step i-2 has read this set
+                s_in.wait_event(ev_done[b])   # the kernels of step i-2 have read this set
                 s_in.wait_event(ev_out[b])    # and its results have left
-            with torch.cuda.stream(s_in):
-                for d, h in zip(snd, h_in):
-                    d.copy_(h, non_blocking=True)
-                ev_in[b].record(s_in)
-            stream.wait_event(ev_in[b])
-            r = tccl.tcclAllReduce(g.handle, snd, rcv, n, dt, op, st, cap)
-            if r != tccl.tcclSuccess:
-                raise tccl.TcclError(r, "tcclAllReduce")
+            for k in range(pieces):
+                lo, hi = cut[k], cut[k + 1]
+                with torch.cuda.stream(s_in):
+                    for d, h in zip(snd, h_in):
+                        d[lo:hi].copy_(h[lo:hi], non_blocking=True)
+                    ev_in[b][k].record(s_in)
+                stream.wait_event(ev_in[b][k])
+                r = tccl.tcclAllReduce(g.handle, [t[lo:hi] for t in snd], [t[lo:hi] for t in rcv], hi - lo,
+                                       dt, op, st, cap)
+                if r != tccl.tcclSuccess:
+                    raise tccl.TcclError(r, "tcclAllReduce")
+                ev_piece[b][k].record(stream)
+                s_out.wait_event(ev_piece[b][k])
+                with torch.cuda.stream(s_out):
+                    for h, d in zip(h_out, rcv):
+                        h[lo:hi].copy_(d[lo:hi], non_blocking=True)
             ev_done[b].record(stream)
-            s_out.wait_event(ev_done[b])
-            with torch.cuda.stream(s_out):
-                for h, d in zip(h_out, rcv):
-                    h.copy_(d, non_blocking=True)
-                ev_out[b].record(s_out)
+            ev_out[b].record(s_out)
 
     def e2e_serial_step():
         with torch.cuda.stream(stream):
@@ -443,8 +453,9 @@ def run_ours(args, w, rank, world, dist):
             "e2e": {"value": round(whole_job_rate(world, alg_bytes, e2e_ms), 2), "unit": "GB/s",
                     "h2d_bytes_per_step": p * S, "d2h_bytes_per_step": p * S,
                     "ms_per_step": round(e2e_ms, 4),
-                    "pipelining": "inputs of step i+1 copied in while step i's results copy out "
-                                  "(two device buffer sets, three streams)",
+                    "pipelining": f"each step in {pieces} slices (one allreduce call per slice); a slice's "
+                                  "results copy out while the next slice's, and the next step's, inputs copy "
+                                  "in (two device buffer sets, three streams)",
                     "serial_value": round(whole_job_rate(world, alg_bytes, e2e_serial_ms), 2),
                     "serial_ms_per_step": round(e2e_serial_ms, 4)},
             "cpu_baseline": cpu,
@@ -1080,6 +1091,8 @@ def main():
                     help="run the per-SM bandwidth probe (bounds for CTA-capped runs)")
     ap.add_argument("--overlap", action="store_true",
                     help="allreduce beside a concurrent cuBLAS GEMM, across CTA caps")
+    ap.add_argument("--e2e-pieces", type=int, default=2,
+                    help="slices per end-to-end step (host copies overlap the other slices' reductions)")
     ap.add_argument("--reshard", action="store_true",
                     help="M-to-N reshard throughput on an 8192 x 8192 bf16 weight")
     ap.add_argument("--rmsnorm", action="store_true",
