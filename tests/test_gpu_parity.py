@@ -471,3 +471,35 @@ def test_invalid_arguments_on_device(groups):
     # misaligned for the element size
     assert tccl.tcclAllReduce(g.handle, [a.data_ptr() + 2, b], [a, b], 8, 0, 0, st, 0) == \
         tccl.tcclInvalidArgument
+
+
+@pytest.mark.parametrize("p,n", [(4, 1 << 22), (8, 3 << 20), (2, (1 << 23) + 40)])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_back_to_back_chain_reads_the_previous_result(groups, p, n, in_place):
+    """Six uncapped allreduces on one stream, each reading what the one before
+    it wrote (ping-pong between two buffer sets, or in place). Every launch
+    starts early and prefetches its first chunks into L2 before it waits for
+    the previous one, so this checks that no call reads its input stale.
+    int32 sums wrap exactly: after k calls every rank holds P^(k-1) times the
+    first call's sum."""
+    g = groups(p)
+    reset_config(g)  # Auto: the bulk engine at these sizes, dynamic order, early launch
+    xs = inputs("i32", p, n, seed=21)
+    a = [to_device(x) for x in xs]
+    b = a if in_place else [torch.empty_like(t) for t in a]
+    sets = [a, b]
+    for k in range(6):
+        src, dst = sets[k % 2], sets[(k + 1) % 2]
+        assert tccl.tcclAllReduce(g.handle, src, dst, n, DT_CODE["i32"], tccl.tcclSum,
+                                  torch.cuda.current_stream().cuda_stream, 0) == tccl.tcclSuccess
+    assert g.last_launch()["engine"] == tccl.tcclEngineBulk
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    total = np.zeros(n, dtype=np.int64)
+    for x in xs:
+        total += x.astype(np.int64)
+    exp = ((total * p ** 5) % (1 << 32)).astype(np.uint64).astype(np.uint32).view(np.int32)
+    for r in range(p):
+        got = to_host(sets[6 % 2][r])
+        mm = first_mismatch(got, exp)
+        assert mm is None, f"P={p} in_place={in_place}: rank {r} first mismatch {mm}"
