@@ -26,6 +26,7 @@ tcclEngineAuto, tcclEngineBulk, tcclEngineWarp, tcclEngineVec, tcclEngineTmaRedu
 tcclEngineCopyOut = 5
 tcclStoreAuto, tcclStoreBulk, tcclStoreVec = 0, 1, 2
 tcclOrderAuto, tcclOrderBlocked, tcclOrderCyclic, tcclOrderDynamic = 0, 1, 2, 3
+tcclReduceAscending, tcclReduceArrival = 0, 1
 tcclLayoutAuto, tcclLayoutShared, tcclLayoutPerRank = 0, 1, 2
 TCCL_MAX_RANKS = 64
 
@@ -44,7 +45,8 @@ class tcclConfig_t(ctypes.Structure):
                 ("chunk_order", ctypes.c_int), ("prefetch_chunks", ctypes.c_int),
                 ("load_policy", ctypes.c_int), ("max_chunk_bytes", ctypes.c_size_t),
                 ("stage_layout", ctypes.c_int), ("ce_streams", ctypes.c_int),
-                ("ce_segment_bytes", ctypes.c_size_t), ("ce_auto_max_cap", ctypes.c_int)]
+                ("ce_segment_bytes", ctypes.c_size_t), ("ce_auto_max_cap", ctypes.c_int),
+                ("reduce_order", ctypes.c_int)]
 
 
 class tcclLaunchInfo_t(ctypes.Structure):

@@ -126,6 +126,7 @@ Config config_from_env() {
   c.ce_streams = geti("TCCL_CE_STREAMS", 0);
   if (const char* e = std::getenv("TCCL_CE_SEGMENT_BYTES")) c.ce_segment_bytes = std::strtoull(e, 0, 10);
   c.ce_auto_max_cap = geti("TCCL_CE_AUTO_MAX_CAP", 0);
+  if (const char* e = std::getenv("TCCL_REDUCE_ORDER")) c.reduce_order = std::string(e) == "arrival" ? 1 : 0;
   if (const char* e = std::getenv("TCCL_SMALL_MAX_BYTES")) c.small_max_bytes = std::strtoull(e, 0, 10);
   if (const char* e = std::getenv("TCCL_VEC_MAX_BYTES")) c.vec_max_bytes = std::strtoull(e, 0, 10);
   c.stage_bytes = geti("TCCL_STAGE_BYTES", 0);
@@ -174,6 +175,7 @@ Config from_public(const tcclConfig_t& p) {
   c.ce_streams = p.ce_streams;
   c.ce_segment_bytes = p.ce_segment_bytes;
   c.ce_auto_max_cap = p.ce_auto_max_cap;
+  c.reduce_order = p.reduce_order;
   return resolve_config(c);
 }
 
@@ -197,6 +199,7 @@ tcclConfig_t to_public(const Config& c) {
   p.ce_streams = c.ce_streams;
   p.ce_segment_bytes = c.ce_segment_bytes;
   p.ce_auto_max_cap = c.ce_auto_max_cap;
+  p.reduce_order = c.reduce_order;
   return p;
 }
 
@@ -206,7 +209,7 @@ bool config_ok(const tcclConfig_t& p) {
          p.stage_bytes >= 0 && p.stages >= 0 && p.consumer_warps >= 0 && p.ctas_per_sm >= 0 &&
          p.wait_timeout_ms >= 0 && p.chunk_order >= 0 && p.chunk_order <= 3 &&
          p.prefetch_chunks >= -1 && p.load_policy >= 0 && p.load_policy <= 2 &&
-         p.stage_layout >= 0 && p.stage_layout <= 2;
+         p.stage_layout >= 0 && p.stage_layout <= 2 && p.reduce_order >= 0 && p.reduce_order <= 1;
 }
 
 void dump_plan(const Plan& pl, const Lowered& low) {
@@ -344,6 +347,7 @@ int launch_plan(tcclGroup* g, CachedPlan* cp, int coll, int dtype, int op,
     a.prefetch_chunks = low.shape.prefetch_chunks;
     a.rank_streamed = low.shape.rank_streamed;
     a.load_evict_first = low.shape.load_evict_first;
+    a.arrival_order = low.shape.engine == kEngineTmaReduce && g->cfg.reduce_order == 1 ? 1 : 0;
     a.status = g->d_status;
     a.sm_mask = mask;
     a.timeout_ns = (uint64_t)(g->cfg.wait_timeout_ms * 1e6);

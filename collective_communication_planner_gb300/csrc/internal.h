@@ -90,6 +90,7 @@ struct BulkArgs {
   int rank_streamed;             // kLayoutPerRank (1) or kLayoutShared (0)
   int prefetch_chunks;           // L2 prefetch distance beyond the shared-memory ring (0: off)
   int load_evict_first;          // bulk loads carry an L2 evict-first policy
+  int arrival_order;             // TMA-reduce engine: ranks 1..P-1 reduced as they arrive
 };
 
 // Warp / vec (small-message) engines: the whole lowered plan rides in the

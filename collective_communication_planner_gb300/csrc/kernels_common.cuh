@@ -971,7 +971,11 @@ __global__ void __launch_bounds__(32 * kMaxConsumerWarps, 1)
           // test hook: a barrier nothing arrives on
           ok = wait_bounded(&bars[2 * lanes], 0, abort_flag, a.inject_timeout_ns, a.status, true);
         if (!ok) break;
-        bulk_wait_all();  // rank r-1's update of the owner chunk is complete
+        // rank r-1's update of the owner chunk is complete: the ascending
+        // order; in the arrival order only rank 0's store must land before
+        // the reductions, which then go out back to back (each element
+        // reduction is an atomic of its own, so none is lost)
+        if (r <= 1 || !a.arrival_order) bulk_wait_all();
         if (r == 0) bulk_store(owner, x(b), n);
         else bulk_reduce<DT, OP>(owner, x(b), n);
         bulk_commit();

@@ -160,6 +160,7 @@ Config resolve_config(const Config& in) {
   if (c.ce_streams > 8) c.ce_streams = 8;
   if (c.ce_segment_bytes == 0) c.ce_segment_bytes = (size_t)32 << 20;
   c.ce_segment_bytes = std::min<size_t>(std::max<size_t>(c.ce_segment_bytes, 4096), (size_t)1 << 30) & ~(size_t)255;
+  if (c.reduce_order != 1) c.reduce_order = 0;
   return c;
 }
 

@@ -83,6 +83,7 @@ struct Config {
   int ce_streams = 0;
   size_t ce_segment_bytes = 0;
   int ce_auto_max_cap = 0;
+  int reduce_order = 0;  // 0 ascending, 1 arrival (TMA-reduce engine only)
 };
 
 // Fills zero fields with the library defaults.

@@ -60,8 +60,20 @@ typedef enum {
 typedef enum { tcclFloat32 = 0, tcclBfloat16 = 1, tcclInt32 = 2 } tcclDataType_t;
 
 /* Element-wise reductions: the add / min / max the article's section 2.1
- * lists for bulk reductions. Reduction order is always ascending rank. */
+ * lists for bulk reductions. Reduction order is ascending rank (see
+ * tcclReduceOrder_t for the one exception). */
 typedef enum { tcclSum = 0, tcclMin = 1, tcclMax = 2 } tcclRedOp_t;
+
+/* The order in which ranks are combined (tcclConfig_t.reduce_order).
+ * Ascending: every engine folds rank 0, then 1, ..., P-1, so results are the
+ * same bits on every engine, launch shape and run. Arrival: on the
+ * TMA-reduce engine only (the other engines ignore it), ranks 1..P-1 are
+ * reduced into the owner chunk with bulk reductions issued back to back, as
+ * T-CCL's shard-in describes, and the memory system applies them in the order
+ * they arrive. int32 sum/min/max and bf16 min/max are unchanged by order
+ * (bit-exact); an fp32 sum may differ from the ascending fold by rounding,
+ * within 2 (P-1) 2^-24 sum_r |x_r| of it. */
+typedef enum { tcclReduceAscending = 0, tcclReduceArrival = 1 } tcclReduceOrder_t;
 
 /* Which kernel family runs a call (see tcclConfig_t). */
 typedef enum {
@@ -117,7 +129,8 @@ typedef enum {
  * TCCL_STORE_MODE, TCCL_CONSUMER_WARPS, TCCL_CTAS_PER_SM,
  * TCCL_WAIT_TIMEOUT_MS, TCCL_CHUNK_ORDER, TCCL_PREFETCH_CHUNKS,
  * TCCL_LOAD_POLICY, TCCL_MAX_CHUNK_BYTES, TCCL_STAGE_LAYOUT, TCCL_CE_STREAMS,
- * TCCL_CE_SEGMENT_BYTES and TCCL_CE_AUTO_MAX_CAP once). Zero in a field means "library default".
+ * TCCL_CE_SEGMENT_BYTES, TCCL_CE_AUTO_MAX_CAP and TCCL_REDUCE_ORDER once). Zero in a field
+ * means "library default".
  *
  * Bulk-engine shape: stage_bytes, stages and max_chunk_bytes default to 64 KiB,
  * 8 and 16 KiB, and a call uses them as given (stages reduced to what shared
@@ -150,6 +163,7 @@ typedef struct {
                               4 MiB where it can be; rounded down to a multiple of 256) */
   int ce_auto_max_cap;     /* Auto picks the copy-out engine for caps up to this many CTAs
                               (0: 5/16 of the SMs; negative: never) */
+  int reduce_order;        /* tcclReduceOrder_t (default ascending) */
 } tcclConfig_t;
 
 /* What the last launch on a group looked like. */

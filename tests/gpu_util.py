@@ -56,3 +56,19 @@ def first_mismatch(a: np.ndarray, b: np.ndarray):
     ub = b.view(np.uint8).reshape(b.size, -1)
     diff = np.nonzero(np.any(ua != ub, axis=1))[0]
     return None if diff.size == 0 else (int(diff[0]), int(diff.size))
+
+
+def within_summation_bound(got, exp, xs):
+    """Every element of an fp32 sum in another order within
+    2 (P-1) 2^-24 sum_r |x_r| of the ascending fold (each side is within
+    (P-1) 2^-24 sum_r |x_r| of the exact sum), or within 4 fp32 ulps of it.
+    Returns (ok, elements that needed the summation bound)."""
+    p = len(xs)
+    abs_sum = np.zeros(exp.shape, dtype=np.float64)
+    for x in xs:
+        abs_sum += np.abs(x.astype(np.float64))
+    d = np.abs(got.astype(np.float64) - exp.astype(np.float64))
+    ulp = np.spacing(np.abs(exp).astype(np.float32)).astype(np.float64)
+    by_ulp = d <= 4 * ulp
+    by_bound = d <= 2 * (p - 1) * 2.0 ** -24 * abs_sum
+    return bool(np.all(by_ulp | by_bound)), int(np.count_nonzero(~by_ulp & by_bound))

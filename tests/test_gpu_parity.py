@@ -13,7 +13,8 @@ import torch
 import collective_communication_planner_gb300 as tccl
 import datagen
 import oracle
-from gpu_util import DT_CODE, NP_OF, TORCH_OF, Guarded, first_mismatch, same_bits, to_device, to_host
+from gpu_util import (DT_CODE, NP_OF, TORCH_OF, Guarded, first_mismatch, same_bits, to_device, to_host,
+                      within_summation_bound)
 
 pytestmark = pytest.mark.gpu
 
@@ -238,6 +239,60 @@ def test_tma_reduce_engine(groups, dtype, op):
     assert g.query_error() == tccl.tcclSuccess
     assert_ranks_equal([to_host(t) for t in parts],
                        oracle.reduce_scatter(xs, dtype, op, nthreads=0), "TMA-reduce RS")
+
+
+@pytest.mark.parametrize("dtype,op", TMA_REDUCE_PAIRS)
+def test_tma_reduce_arrival_order(groups, dtype, op):
+    """tcclReduceArrival on the TMA-reduce engine: ranks 1..P-1 reduced back
+    to back in whatever order the memory system applies them. Order-free pairs
+    (int32 sum/min/max, bf16 min/max) stay bit-exact; an fp32 sum stays within
+    the summation bound of the ascending fold. Allreduce and reduce-scatter,
+    P = 2..8, a cap, misaligned buffers."""
+    for p, n, cap, offs in ((2, 1_000_003, 0, 0), (3, 77_777, 5, 4), (8, 500_001, 0, 0),
+                            (8, 300_000, 16, 8)):
+        g = groups(p)
+        reset_config(g, engine=tccl.tcclEngineTmaReduce, reduce_order=tccl.tcclReduceArrival)
+        xs = inputs(dtype, p, n)
+        got = run_allreduce(g, xs, dtype, op, cap=cap, send_off=offs, recv_off=offs)
+        assert g.last_launch()["engine"] == tccl.tcclEngineTmaReduce
+        exp = oracle.allreduce(xs, dtype, op, nthreads=0)
+        what = f"TMA-reduce arrival AR {dtype} {op} P={p} cap={cap} off={offs}"
+        if (dtype, op) == ("f32", "sum"):
+            for r in range(p):
+                ok, _ = within_summation_bound(got[r], exp[r], xs)
+                assert ok, f"{what}: rank {r} outside the summation bound"
+        else:
+            assert_ranks_equal(got, exp, what)
+    p, rc = 4, 123_457
+    g = groups(p)
+    reset_config(g, engine=tccl.tcclEngineTmaReduce, reduce_order=tccl.tcclReduceArrival)
+    xs = inputs(dtype, p, p * rc)
+    sends = [to_device(x) for x in xs]
+    parts = [torch.empty(rc, dtype=TORCH_OF[dtype], device="cuda") for _ in range(p)]
+    g.reduce_scatter(sends, parts, op=op)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    exp = oracle.reduce_scatter(xs, dtype, op, nthreads=0)
+    got = [to_host(t) for t in parts]
+    if (dtype, op) == ("f32", "sum"):
+        for r in range(p):
+            ok, _ = within_summation_bound(got[r], exp[r], [x[r * rc:(r + 1) * rc] for x in xs])
+            assert ok, f"TMA-reduce arrival RS: rank {r} outside the summation bound"
+    else:
+        assert_ranks_equal(got, exp, "TMA-reduce arrival RS")
+    reset_config(g)
+
+
+def test_arrival_order_leaves_other_engines_ascending(groups):
+    """The order setting only changes the TMA-reduce engine: the bulk engine's
+    fp32 sums stay bit-exact with it set."""
+    p, n = 4, 1_000_003
+    g = groups(p)
+    reset_config(g, engine=tccl.tcclEngineBulk, reduce_order=tccl.tcclReduceArrival)
+    xs = inputs("f32", p, n)
+    assert_ranks_equal(run_allreduce(g, xs, "f32", "sum"), oracle.allreduce(xs, "f32", "sum", nthreads=0),
+                       "bulk engine with the arrival order set")
+    reset_config(g)
 
 
 @pytest.mark.parametrize("dtype,op", [("bf16", "sum"), ("f32", "min"), ("f32", "max")])
@@ -503,3 +558,15 @@ def test_back_to_back_chain_reads_the_previous_result(groups, p, n, in_place):
         got = to_host(sets[6 % 2][r])
         mm = first_mismatch(got, exp)
         assert mm is None, f"P={p} in_place={in_place}: rank {r} first mismatch {mm}"
+
+
+def test_reduce_order_setting_round_trip(groups):
+    g = groups(2)
+    reset_config(g, reduce_order=tccl.tcclReduceArrival)
+    r, c = tccl.tcclGroupGetConfig(g.handle)
+    assert r == tccl.tcclSuccess and c.reduce_order == tccl.tcclReduceArrival
+    c.reduce_order = 2
+    assert tccl.tcclGroupSetConfig(g.handle, c) == tccl.tcclInvalidArgument
+    reset_config(g)
+    r, c = tccl.tcclGroupGetConfig(g.handle)
+    assert c.reduce_order == tccl.tcclReduceAscending
