@@ -962,7 +962,7 @@ def rmsnorm_bench(args):
                 fn()
         return ev(gr.replay, 20) / 20 * 1e3
 
-    for tokens in (1, 8, 64, 512, 4096):
+    for tokens in (int(t) for t in args.rmsnorm_tokens.split(",")):
         n = tokens * hidden
         xs = datagen.rank_buffers("normal_bf16", 4, p, n)
         exp, exp64 = rn.allreduce_rmsnorm(xs, gamma_h, tokens, hidden, 1e-6, "bf16")
@@ -1091,6 +1091,8 @@ def main():
                     help="run the per-SM bandwidth probe (bounds for CTA-capped runs)")
     ap.add_argument("--overlap", action="store_true",
                     help="allreduce beside a concurrent cuBLAS GEMM, across CTA caps")
+    ap.add_argument("--rmsnorm-tokens", default="1,8,64,512,4096",
+                    help="token counts (rows of 8192) for --rmsnorm, comma separated")
     ap.add_argument("--e2e-pieces", type=int, default=2,
                     help="slices per end-to-end step (host copies overlap the other slices' reductions)")
     ap.add_argument("--reshard", action="store_true",
