@@ -691,7 +691,10 @@ def sweep(args):
     if not only or "c3" in only:
         p = 8
         g = tccl.Group(p)
-        for nbytes in [4096 << k for k in range(17)]:
+        sizes = [4096 << k for k in range(17)]
+        if args.c3_bytes:
+            sizes = [int(b) for b in args.c3_bytes.split(",")]
+        for nbytes in sizes:
             n = nbytes // 4
             for dtype, op in (("f32", "sum"), ("f32", "min"), ("f32", "max"), ("i32", "sum")):
                 xs = (datagen.rank_buffers("uniform_f32", 2, p, n) if dtype == "f32" else
@@ -1087,6 +1090,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="measure every configuration point of C1..C5 (one JSON line each)")
     ap.add_argument("--sweep-configs", default="", help="comma list, e.g. c3,c5")
+    ap.add_argument("--c3-bytes", default="",
+                    help="C3 sizes per rank in bytes for --sweep, comma separated (default 4 KiB ... 256 MiB)")
     ap.add_argument("--probe", action="store_true",
                     help="run the per-SM bandwidth probe (bounds for CTA-capped runs)")
     ap.add_argument("--overlap", action="store_true",
