@@ -137,7 +137,7 @@ typedef enum {
  * memory holds), with one exception: while all three hold exactly those
  * defaults, an uncapped, out-of-place allreduce on the bulk engine's shared
  * stage layout that moves 2 * P * S >= 512 MiB keeps about 96 KiB of loads in
- * flight per CTA instead: chunks of 32 KiB / P bytes (at least 6 KiB, at most
+ * flight per CTA instead: chunks of 48 KiB / P bytes (at least 6 KiB, at most
  * max_chunk_bytes) and 96 KiB / (P * chunk) stages (at least 2), which
  * streamed 0.5-1% faster on GB300 than a full ring.
  */

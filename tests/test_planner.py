@@ -243,7 +243,7 @@ def test_pipeline_shape_follows_shared_memory():
     assert small.smem_bytes <= 48 * 1024 and small.stages >= 2
 
 
-@pytest.mark.parametrize("p,chunk,stages", [(1, 16384, 6), (2, 16384, 3), (3, 10912, 3), (4, 8192, 3),
+@pytest.mark.parametrize("p,chunk,stages", [(1, 16384, 6), (2, 16384, 3), (3, 16384, 2), (4, 12288, 2),
                                              (8, 6144, 2), (16, 6144, 2), (32, 3072, 2)])
 def test_uncapped_allreduce_default_shape(p, chunk, stages):
     """With the default shape a large out-of-place allreduce (2 * P * S of
