@@ -1,9 +1,9 @@
 """Benchmark: allreduce of P logical rank buffers on one GB300.
 
 Default workload (one step = one fused allreduce through the C ABI):
-  P = 4 ranks, bf16 sum, 32 Mi elements (64 MiB) per rank, out of place,
-  values N(0, 1) from seed 1. Footprint 512 MiB > 129 MB of L2, so timed
-  iterations stream from HBM without an explicit L2 flush.
+  C4: P = 8 ranks, bf16 sum, 64 Mi elements (128 MiB) per rank, out of
+  place, values N(0, 0.02) from seed 3, uncapped. Footprint 2 GiB > 129 MB of
+  L2, so timed iterations stream from HBM without an explicit L2 flush.
 
 Reported (one JSON line on rank 0):
   value      algbw = P * count * bytes / time (GB/s), device-resident inputs
@@ -12,6 +12,12 @@ Reported (one JSON line on rank 0):
              launch time (the timed region between two CUDA events on the
              launching stream, divided by its launches), against the
              measured copy bandwidth
+  caps, cap16  the same allreduce under CTA caps 8, 16 and 32 with the
+             default engine choice (the copy-out engine), timed the same way:
+             HBM fraction of 2 * P * S, the fraction of every byte the call
+             moves, engine, CTAs per launch, distinct SMs per launch and over
+             the call; cap 16 also with the SM-only bulk engine
+  c2         the P = 4, 64 MiB-per-rank allreduce, uncapped, for comparison
   e2e        same metric through the C ABI with the inputs copied from pinned
              host memory and every result copied back, inside the timed region
   cpu_baseline  the CPU oracle (threaded, same per-element order) on the
@@ -313,6 +319,106 @@ def run_ours(args, w, rank, world, dist):
     achieved = hbm_bytes / (launch_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
 
+    # the same allreduce under CTA caps, with the default engine choice (the
+    # copy-out engine: segment kernels within the cap fold into one anchor
+    # rank, the copy engines carry the result to the others) and, at cap 16,
+    # with the SM-only bulk engine; each point timed like the main line: K
+    # back-to-back calls between one event pair after three warm-up calls
+    def reset_config(**kw):
+        c = tccl.tcclConfig_t()
+        for key, val in kw.items():
+            setattr(c, key, val)
+        r = tccl.tcclGroupSetConfig(g.handle, c)
+        if r != tccl.tcclSuccess:
+            raise tccl.TcclError(r, "tcclGroupSetConfig")
+
+    def timed_calls(fn, k):
+        for _ in range(3):
+            fn()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k):
+            fn()
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / k
+
+    def sampled_exact():
+        got_s = recvs[p - 1].view(torch.int16 if w["dtype"] == "bf16" else recvs[0].dtype)
+        return bool(np.array_equal(got_s.cpu().numpy()[idx].view(np.uint8), exp.view(np.uint8)))
+
+    def cap_point(cap_k, sm_only):
+        reset_config(**({"ce_auto_max_cap": -1} if sm_only else {}))
+
+        def call():
+            r = tccl.tcclAllReduce(g.handle, sends, recvs, n, dt, op, st, cap_k)
+            if r != tccl.tcclSuccess:
+                raise tccl.TcclError(r, "tcclAllReduce")
+
+        for t in recvs:
+            t.fill_(0)
+        call()
+        stream.synchronize()
+        g.read_sm_record()
+        g.record_sms(True)
+        call()
+        per_launch, union = g.read_sm_record_launches()
+        g.record_sms(False)
+        pinfo = g.last_launch()
+        kc = max(10, min(args.steps, 50))
+        ms = timed_calls(call, kc)
+        copy_out = pinfo["engine"] == tccl.tcclEngineCopyOut
+        # the copy-out call moves more than the collective's 2 P S: the fold
+        # reads P S and writes S (the anchor), the copies read and write
+        # (P - 1) S (their reads of the anchor can come from L2)
+        moved = (3 * p - 1) * S if copy_out else hbm_bytes
+        row = {"cap": cap_k, "variant": "sm_only" if sm_only else "auto",
+               "engine": pinfo["engine"], "engine_name": "copy-out" if copy_out else "bulk",
+               "ctas_per_launch": pinfo["ctas"], "launches_per_call": len(per_launch),
+               "copies_per_call": pinfo["ce_copies"], "calls_timed": kc,
+               "ms_per_call": round(ms, 5),
+               "algbw": round(alg_bytes / (ms * 1e-3) / 1e9, 2),
+               "hbm_fraction": round(hbm_bytes / (ms * 1e-3) / 1e9 / peak, 4),
+               "moved_fraction": round(moved / (ms * 1e-3) / 1e9 / peak, 4),
+               "sms_per_launch_max": max(per_launch) if per_launch else 0,
+               "sms_per_launch": per_launch, "sms_union": union,
+               "sampled_exact": sampled_exact()}
+        if not row["sampled_exact"]:
+            raise SystemExit(f"bench: capped result (cap {cap_k}) differs from the oracle on sampled elements")
+        return row
+
+    cap_rows = []
+    c2_row = None
+    if not args.no_caps:
+        for cap_k in (8, 16, 32):
+            cap_rows.append(cap_point(cap_k, False))
+        cap_rows.append(cap_point(16, True))
+        reset_config()
+        if args.workload != "c2":
+            w2 = WORKLOADS["c2"]
+            p2, n2 = w2["p"], w2["count"]
+            xs2 = make_inputs(w2)
+            s2 = [host_to_torch(x).to(dev) for x in xs2]
+            r2 = [torch.empty_like(t) for t in s2]
+            with tccl.Group(p2) as g2:
+                def call2():
+                    r = tccl.tcclAllReduce(g2.handle, s2, r2, n2, tccl.DTYPES[w2["dtype"]],
+                                           tccl.OPS[w2["op"]], st, 0)
+                    if r != tccl.tcclSuccess:
+                        raise tccl.TcclError(r, "tcclAllReduce")
+                ms2 = timed_calls(call2, max(10, min(args.steps, 200)))
+                i2 = g2.last_launch()
+            got2 = r2[p2 - 1].view(torch.int16).cpu().numpy()[:4096].view(np.uint16)
+            exp2 = oracle.allreduce([x[:4096].copy() for x in xs2], w2["dtype"], w2["op"])[0]
+            S2 = n2 * 2
+            c2_row = {"workload": w2["name"], "ms_per_call": round(ms2, 5),
+                      "algbw": round(p2 * S2 / (ms2 * 1e-3) / 1e9, 2),
+                      "hbm_fraction": round(2 * p2 * S2 / (ms2 * 1e-3) / 1e9 / peak, 4),
+                      "engine": i2["engine"], "ctas": i2["ctas"],
+                      "sampled_exact": bool(np.array_equal(got2, exp2))}
+            del s2, r2, xs2
+
     # reduce-scatter then all-gather on the same workload (two launches)
     rc = n // p
     parts = [torch.empty(rc, dtype=sends[0].dtype, device=dev) for _ in range(p)]
@@ -447,6 +553,9 @@ def run_ours(args, w, rank, world, dist):
                          "traffic": traffic, "peak_source": peak_src,
                          "algorithmic_bytes_per_launch": hbm_bytes,
                          "mean_launch_ms": round(launch_ms, 5)},
+            "cap16": next((r for r in cap_rows if r["cap"] == 16 and r["variant"] == "auto"), None),
+            "caps": cap_rows,
+            "c2": c2_row,
             "rs_then_ag": {"ms_per_step": round(rs_ms, 5),
                            "algbw": round(alg_bytes / (rs_ms * 1e-3) / 1e9, 2),
                            "hbm_bytes_per_step": 2 * (p + 1) * S},
@@ -996,26 +1105,6 @@ def rmsnorm_bench(args):
     g_row.close()
 
 
-# ------------------------------------------------------------------ probe mode
-def probe():
-    """Builds and runs the two hardware probes under
-    collective_communication_planner_gb300/probes/: what one SM can read,
-    write and copy with each mechanism (sm_bandwidth.cu, which bounds what a
-    CTA cap can deliver), and what the copy engines add beside a capped fold
-    (copy_engine.cu). Prints the probes' JSON lines."""
-    out_dir = ROOT / "collective_communication_planner_gb300" / "_build"
-    out_dir.mkdir(exist_ok=True)
-    for name in ("sm_bandwidth", "copy_engine"):
-        src = ROOT / "collective_communication_planner_gb300" / "probes" / f"{name}.cu"
-        exe = out_dir / f"{name}_probe"
-        subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
-                               "-std=c++17", "-lineinfo", "-o", str(exe), str(src)])
-        r = subprocess.run([str(exe)], capture_output=True, text=True)
-        sys.stdout.write(r.stdout)
-        if r.returncode != 0:
-            raise SystemExit(f"{name} probe failed ({r.returncode}): {r.stderr.strip()}")
-
-
 # ------------------------------------------------------------------ copy-out mode
 def copy_out_bench(args):
     """The C4 allreduce (P=8, bf16, 128 MiB per rank) at CTA caps 8, 16 and
@@ -1082,7 +1171,9 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c4")
+    ap.add_argument("--no-caps", action="store_true",
+                    help="skip the capped points (CTA caps 8/16/32) and the C2 comparison")
     ap.add_argument("--cap", type=int, default=None, help="CTA cap (default: the workload's)")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load first")
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
@@ -1092,8 +1183,6 @@ def main():
     ap.add_argument("--sweep-configs", default="", help="comma list, e.g. c3,c5")
     ap.add_argument("--c3-bytes", default="",
                     help="C3 sizes per rank in bytes for --sweep, comma separated (default 4 KiB ... 256 MiB)")
-    ap.add_argument("--probe", action="store_true",
-                    help="run the per-SM bandwidth probe (bounds for CTA-capped runs)")
     ap.add_argument("--overlap", action="store_true",
                     help="allreduce beside a concurrent cuBLAS GEMM, across CTA caps")
     ap.add_argument("--rmsnorm-tokens", default="1,8,64,512,4096",
@@ -1113,9 +1202,6 @@ def main():
     ap.add_argument("--overlap-caps", type=lambda v: [int(x) for x in v.split(",")],
                     default=[8, 16, 32, 64, 0])
     args = ap.parse_args()
-    if args.probe:
-        probe()
-        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = WORKLOADS[args.workload]

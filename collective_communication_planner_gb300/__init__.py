@@ -104,6 +104,8 @@ def _open():
         "tcclGetLastLaunchInfo": (i, [vp, ctypes.POINTER(tcclLaunchInfo_t)]),
         "tcclGroupRecordSms": (i, [vp, i]),
         "tcclGroupReadSmRecord": (i, [vp, ctypes.POINTER(i)]),
+        "tcclGroupReadSmRecordLaunches": (i, [vp, ctypes.POINTER(i), i, ctypes.POINTER(i),
+                                              ctypes.POINTER(i)]),
         "tcclPlanInspect": (i, [i, i, pvp, pvp, sz, i, i, i, i, ctypes.POINTER(tcclConfig_t),
                                 ctypes.POINTER(ctypes.c_int64), i, ctypes.POINTER(i),
                                 ctypes.POINTER(i), ctypes.POINTER(tcclLaunchInfo_t)]),
@@ -133,7 +135,8 @@ _lib = _open()
 EXPORTED = ("tcclGetErrorString", "tcclGetVersion", "tcclGroupCreate", "tcclGroupDestroy",
             "tcclGroupGetConfig", "tcclGroupSetConfig", "tcclAllReduce", "tcclReduceScatter",
             "tcclAllGather", "tcclGroupQueryError", "tcclGetLastLaunchInfo",
-            "tcclGroupRecordSms", "tcclGroupReadSmRecord", "tcclPlanInspect", "tcclCopyOutInspect",
+            "tcclGroupRecordSms", "tcclGroupReadSmRecord", "tcclGroupReadSmRecordLaunches",
+            "tcclPlanInspect", "tcclCopyOutInspect",
             "tcclGroupInjectWaitTimeout", "tcclAllReduceNoAlloc", "tcclReshard",
             "tcclReshardInspect", "tcclAllReduceRMSNorm")
 
@@ -282,6 +285,15 @@ def tcclGroupReadSmRecord(group):
     n = ctypes.c_int()
     r = _lib.tcclGroupReadSmRecord(group, ctypes.byref(n))
     return r, n.value
+
+
+def tcclGroupReadSmRecordLaunches(group, max_launches: int = 64):
+    """(result, distinct SMs per recorded launch, distinct SMs of all of them)."""
+    buf = (ctypes.c_int * max(1, max_launches))()
+    n, total = ctypes.c_int(), ctypes.c_int()
+    r = _lib.tcclGroupReadSmRecordLaunches(group, buf, max_launches, ctypes.byref(n),
+                                           ctypes.byref(total))
+    return r, list(buf[:min(n.value, max_launches)]), total.value
 
 
 def tcclGroupInjectWaitTimeout(group, enable: bool, timeout_ms: float = 0.0) -> int:
@@ -452,3 +464,9 @@ class Group:
         r, n = tcclGroupReadSmRecord(self.handle)
         _check(r, "tcclGroupReadSmRecord")
         return n
+
+    def read_sm_record_launches(self):
+        """(distinct SMs of each recorded launch, distinct SMs of all of them)."""
+        r, per, total = tcclGroupReadSmRecordLaunches(self.handle)
+        _check(r, "tcclGroupReadSmRecordLaunches")
+        return per, total

@@ -328,7 +328,7 @@ tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* con
 int launch_plan(tcclGroup* g, CachedPlan* cp, int coll, int dtype, int op,
                 const void* const* send, void* const* recv, int es, cudaStream_t stream) {
   const Lowered& low = cp->low;
-  uint32_t* mask = g->record_sms ? g->d_sm_mask : nullptr;
+  uint32_t* mask = sm_record_slot(g);
   if (low.shape.engine == kEngineBulk || low.shape.engine == kEngineTmaReduce) {
     BulkArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -505,11 +505,12 @@ tcclResult_t tcclGroupCreate(int nranks, tcclGroup_t* out) {
   if (prepare_bulk_kernels((size_t)g->dev.smem_optin) != 0) return tcclCudaError;
   if (prepare_reshard_kernels((size_t)g->dev.smem_optin) != 0) return tcclCudaError;
   if (cudaMalloc(&g->d_status, 64) != cudaSuccess) return tcclCudaError;
-  if (cudaMalloc(&g->d_sm_mask, 64) != cudaSuccess) {
+  const size_t sm_bytes = sizeof(uint32_t) * kSmSlots * kSmSlotWords;
+  if (cudaMalloc(&g->d_sm_mask, sm_bytes) != cudaSuccess) {
     cudaFree(g->d_status);
     return tcclCudaError;
   }
-  if (cudaMemset(g->d_status, 0, 64) != cudaSuccess || cudaMemset(g->d_sm_mask, 0, 64) != cudaSuccess) {
+  if (cudaMemset(g->d_status, 0, 64) != cudaSuccess || cudaMemset(g->d_sm_mask, 0, sm_bytes) != cudaSuccess) {
     cudaFree(g->d_status);
     cudaFree(g->d_sm_mask);
     return tcclCudaError;
@@ -597,17 +598,53 @@ tcclResult_t tcclGroupRecordSms(tcclGroup_t g, int enable) {
   return tcclSuccess;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Reads and clears the SM record: the distinct SMs of each recorded launch
+// (up to max_launches of them) and of all launches together.
+tcclResult_t read_sm_record(tcclGroup_t g, int* per_launch, int max_launches, int* n_launches,
+                            int* distinct_sms) {
+  std::vector<uint32_t> m((size_t)kSmSlots * kSmSlotWords);
+  const size_t bytes = m.size() * sizeof(uint32_t);
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(m.data(), g->d_sm_mask, bytes, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(g->d_sm_mask, 0, bytes) != cudaSuccess)
+    return tcclCudaError;
+  const int launches = g->sm_launches;
+  g->sm_launches = 0;
+  uint32_t all[kSmSlotWords] = {0};
+  for (int s = 0; s < kSmSlots; ++s) {
+    int n = 0;
+    for (int w = 0; w < kSmSlotWords; ++w) {
+      const uint32_t v = m[(size_t)s * kSmSlotWords + w];
+      all[w] |= v;
+      n += __builtin_popcount(v);
+    }
+    if (per_launch && s < max_launches && s < launches) per_launch[s] = n;
+  }
+  int n = 0;
+  for (uint32_t w : all) n += __builtin_popcount(w);
+  if (distinct_sms) *distinct_sms = n;
+  if (n_launches) *n_launches = launches;
+  return tcclSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
 tcclResult_t tcclGroupReadSmRecord(tcclGroup_t g, int* distinct_sms) {
   if (!g || !distinct_sms) return tcclInvalidArgument;
-  uint32_t m[8];
-  if (cudaDeviceSynchronize() != cudaSuccess ||
-      cudaMemcpy(m, g->d_sm_mask, sizeof(m), cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemset(g->d_sm_mask, 0, sizeof(m)) != cudaSuccess)
-    return tcclCudaError;
-  int n = 0;
-  for (uint32_t w : m) n += __builtin_popcount(w);
-  *distinct_sms = n;
-  return tcclSuccess;
+  return read_sm_record(g, nullptr, 0, nullptr, distinct_sms);
+}
+
+tcclResult_t tcclGroupReadSmRecordLaunches(tcclGroup_t g, int* per_launch, int max_launches,
+                                           int* n_launches, int* distinct_sms) {
+  if (!g || !n_launches || !distinct_sms || max_launches < 0 || (max_launches > 0 && !per_launch))
+    return tcclInvalidArgument;
+  return read_sm_record(g, per_launch, max_launches, n_launches, distinct_sms);
 }
 
 tcclResult_t tcclReshard(tcclGroup_t g, const void* const srcbufs[], const tcclLayout_t* src,
@@ -686,7 +723,7 @@ tcclResult_t tcclReshard(tcclGroup_t g, const void* const srcbufs[], const tcclL
     a.sched = reinterpret_cast<unsigned long long*>(cr->d_table + wb + pb);
     for (int m = 0; m < sl.size(); ++m) a.src[m] = srcbufs[m];
     for (int m = 0; m < dl.size(); ++m) a.dst[m] = dstbufs[m];
-    a.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
+    a.sm_mask = sm_record_slot(g);
     a.status = g->d_status;
     a.timeout_ns = (uint64_t)(g->cfg.wait_timeout_ms * 1e6);
     a.inject_timeout_ns = g->inject_ns;
@@ -744,7 +781,7 @@ tcclResult_t tcclAllReduceRMSNorm(tcclGroup_t g, const void* const sendbufs[],
     a.p.dst[r] = recvbufs[r];
   }
   a.gamma = gamma;
-  a.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
+  a.sm_mask = sm_record_slot(g);
   a.rows = rows;
   a.hidden = (uint32_t)hidden;
   a.eps = eps;

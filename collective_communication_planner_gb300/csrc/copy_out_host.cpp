@@ -119,7 +119,6 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
   int fast_grid = 0;
   AnchorArgs aa;
   std::memset(&aa, 0, sizeof(aa));
-  aa.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
   aa.nranks = P;
   aa.njobs = 1;
   const int used = std::min(g->cfg.ce_streams, P - 1);
@@ -140,6 +139,7 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
       uint64_t grid = std::max<uint64_t>(1, (aa.nvec + per_cta - 1) / per_cta);
       grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
       fast_grid = std::max(fast_grid, (int)grid);
+      aa.sm_mask = sm_record_slot(g);
       err = launch_anchor_reduce(dtype, op, aa, (int)grid, cap <= 0, stream);
     } else {
       CachedPlan* cp = (sgi == nseg - 1 && tail) ? tail : full;
@@ -193,7 +193,7 @@ tcclResult_t run_copy_out_reduce_scatter(tcclGroup* g, const void* const* send, 
     return tcclInvalidUsage;
   AnchorArgs aa;
   std::memset(&aa, 0, sizeof(aa));
-  aa.sm_mask = g->record_sms ? g->d_sm_mask : nullptr;
+  aa.sm_mask = sm_record_slot(g);
   aa.nranks = P;
   aa.njobs = P;
   aa.job_src_stride = bytes;

@@ -59,6 +59,9 @@ struct CachedReshard {
   }
 };
 
+constexpr int kSmSlots = 64;
+constexpr int kSmSlotWords = 8;  // 256 bits: one per SM
+
 int log_level();  // TCCL_LOG: > 0 prints plans and launch errors to stderr
 int elem_size_of(int dtype);
 void fill_info(const Lowered& low, tcclLaunchInfo_t* info);
@@ -71,8 +74,11 @@ struct tcclGroup {
   tccl::DeviceDesc dev;
   tccl::Config cfg;
   int* d_status = nullptr;     // [0] status code
-  uint32_t* d_sm_mask = nullptr;  // 256-bit SM bitmap
+  // SM recorder: one 256-bit bitmap per kernel launch while recording
+  // (tccl::kSmSlots of them; launches past the last slot share it)
+  uint32_t* d_sm_mask = nullptr;
   bool record_sms = false;
+  int sm_launches = 0;         // launches recorded since the last read
   bool rms_cluster_enabled = true;  // TCCL_RMSNORM_CLUSTER=0 keeps one CTA per row
   uint64_t inject_ns = 0;
   std::map<tccl::PlanKey, std::unique_ptr<tccl::CachedPlan>> plans;
@@ -87,6 +93,15 @@ struct tcclGroup {
 };
 
 namespace tccl {
+
+// The SM bitmap the next kernel launch records into, or null when the group
+// is not recording. Call once per launch.
+inline uint32_t* sm_record_slot(tcclGroup* g) {
+  if (!g->record_sms) return nullptr;
+  const int slot = g->sm_launches < kSmSlots ? g->sm_launches : kSmSlots - 1;
+  ++g->sm_launches;
+  return g->d_sm_mask + (size_t)slot * kSmSlotWords;
+}
 
 // The plan (cached) of one call: its lowering and, for the bulk engines, its
 // device tables. anchor >= 0: every window stores to that rank only (the

@@ -275,6 +275,20 @@ tcclResult_t tcclGroupRecordSms(tcclGroup_t g, int enable);
 tcclResult_t tcclGroupReadSmRecord(tcclGroup_t g, int* distinct_sms);
 
 /*
+ * The same record, launch by launch: each kernel launch made while recording
+ * sets bits in a bitmap of its own (up to 64 launches; later ones share the
+ * last bitmap). Synchronises the device, writes the distinct SMs of each of
+ * the first `max_launches` recorded launches to per_launch[0 ..], the number
+ * of launches recorded to *n_launches and the distinct SMs of all of them
+ * together to *distinct_sms, then clears the record. A copy-out call (several
+ * segment kernels, each within the cap) shows here as several launches.
+ * per_launch may be null when max_launches is 0. Errors: tcclInvalidArgument
+ * for a null group or output, tcclCudaError if the device cannot be read.
+ */
+tcclResult_t tcclGroupReadSmRecordLaunches(tcclGroup_t g, int* per_launch, int max_launches,
+                                           int* n_launches, int* distinct_sms);
+
+/*
  * Host-only view of the planner and lowering (no GPU needed). Plans and
  * lowers one collective for a device with `sm_count` SMs and
  * `smem_per_block` bytes of opt-in shared memory, as a call with these

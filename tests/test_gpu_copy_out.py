@@ -124,13 +124,17 @@ def test_sm_footprint_stays_within_the_cap(groups, cap):
     g.read_sm_record()
     g.record_sms(True)
     got = allreduce(g, xs, "bf16", "sum", cap=cap)
-    sms = g.read_sm_record()
+    per_launch, sms = g.read_sm_record_launches()
     g.record_sms(False)
     # every segment's kernel has `cap` CTAs and the segments run one after the
-    # other on the stream, so at most `cap` SMs are busy at any time; the
-    # record is the union over the call's launches
+    # other on the stream, so at most `cap` SMs are busy at any time: each
+    # launch's own record holds at most `cap` SMs, and the union over the
+    # call's launches at most cap x segments
     info = g.last_launch()
     assert info["ctas"] == cap and 1 <= sms <= cap * info["ce_segments"]
+    assert len(per_launch) == info["ce_segments"]
+    assert all(1 <= n <= cap for n in per_launch), per_launch
+    assert max(per_launch) <= sms
     check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), f"cap {cap}")
 
 
