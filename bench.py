@@ -1139,11 +1139,25 @@ def copy_out_bench(args):
     import oracle
     idx = np.sort(np.random.default_rng(5).choice(n, size=4096, replace=False))
     exp = oracle.allreduce([x[idx].copy() for x in xs], "bf16", "sum")[0]
-    for cap in (8, 16, 32):
-        for variant, kw in (("auto", {}), ("sm_only", {"ce_auto_max_cap": -1})):
+    variants = {
+        "auto": {},
+        "sm_only": {"ce_auto_max_cap": -1},
+        # the copy-out engine with its segments folded by the bulk engine's
+        # TMA pipeline instead of register loads
+        "tma_shared": {"ce_fold": 2},
+        "tma_per_rank": {"ce_fold": 2, "stage_layout": 2},
+        "tma_per_rank_8w": {"ce_fold": 2, "stage_layout": 2, "consumer_warps": 8},
+    }
+    chosen = args.copy_out_variants.split(",") if args.copy_out_variants else ["auto", "sm_only"]
+    caps = [int(c) for c in args.copy_out_caps.split(",")]
+    for cap in caps:
+        for variant in chosen:
+            kw = variants[variant]
             set_cfg(**kw)
             call = lambda: tccl.tcclAllReduce(g.handle, sends, recvs, n, tccl.DTYPES["bf16"],
                                               tccl.tcclSum, st, cap)
+            for t in recvs:
+                t.fill_(0)
             for _ in range(3):
                 assert call() == 0
             stream.synchronize()
@@ -1158,6 +1172,8 @@ def copy_out_bench(args):
             got = recvs[p - 1].view(torch.int16).cpu().numpy().view(np.uint16)[idx]
             print(json.dumps({"mode": "copy_out", "workload": w["name"], "cap": cap, "variant": variant,
                               "engine": info["engine"], "ctas": info["ctas"], "threads": info["threads"],
+                              "stages": info["stages"], "chunk_bytes": info["chunk_bytes"],
+                              "stage_layout": info["stage_layout"],
                               "segments": info["ce_segments"], "copies": info["ce_copies"],
                               "us": round(ms * 1e3, 2), "hbm_fraction": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
                               "sampled_exact": bool(np.array_equal(got, exp))}), flush=True)
@@ -1195,6 +1211,10 @@ def main():
                     help="allreduce fused with RMSNorm vs the plain allreduce (C5 shapes)")
     ap.add_argument("--copy-out", action="store_true",
                     help="C4 at CTA caps 8/16/32: copy-out engine vs SM-only bulk engine")
+    ap.add_argument("--copy-out-variants", default="",
+                    help="for --copy-out: comma list of auto, sm_only, tma_shared, tma_per_rank, "
+                         "tma_per_rank_8w (default auto,sm_only)")
+    ap.add_argument("--copy-out-caps", default="8,16,32", help="for --copy-out: CTA caps")
     ap.add_argument("--gemm-n", type=int, default=8192)
     ap.add_argument("--overlap-engine", type=int, default=0,
                     help="engine for the overlap study (0 auto, 1 bulk, 4 TMA-reduce)")

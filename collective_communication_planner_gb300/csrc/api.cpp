@@ -127,6 +127,11 @@ Config config_from_env() {
   if (const char* e = std::getenv("TCCL_CE_SEGMENT_BYTES")) c.ce_segment_bytes = std::strtoull(e, 0, 10);
   c.ce_auto_max_cap = geti("TCCL_CE_AUTO_MAX_CAP", 0);
   if (const char* e = std::getenv("TCCL_REDUCE_ORDER")) c.reduce_order = std::string(e) == "arrival" ? 1 : 0;
+  if (const char* e = std::getenv("TCCL_CE_FOLD")) {
+    std::string v(e);
+    if (v == "register") c.ce_fold = kFoldRegister;
+    else if (v == "tma") c.ce_fold = kFoldTma;
+  }
   if (const char* e = std::getenv("TCCL_SMALL_MAX_BYTES")) c.small_max_bytes = std::strtoull(e, 0, 10);
   if (const char* e = std::getenv("TCCL_VEC_MAX_BYTES")) c.vec_max_bytes = std::strtoull(e, 0, 10);
   c.stage_bytes = geti("TCCL_STAGE_BYTES", 0);
@@ -176,6 +181,7 @@ Config from_public(const tcclConfig_t& p) {
   c.ce_segment_bytes = p.ce_segment_bytes;
   c.ce_auto_max_cap = p.ce_auto_max_cap;
   c.reduce_order = p.reduce_order;
+  c.ce_fold = p.ce_fold;
   return resolve_config(c);
 }
 
@@ -200,6 +206,7 @@ tcclConfig_t to_public(const Config& c) {
   p.ce_segment_bytes = c.ce_segment_bytes;
   p.ce_auto_max_cap = c.ce_auto_max_cap;
   p.reduce_order = c.reduce_order;
+  p.ce_fold = c.ce_fold;
   return p;
 }
 
@@ -209,7 +216,8 @@ bool config_ok(const tcclConfig_t& p) {
          p.stage_bytes >= 0 && p.stages >= 0 && p.consumer_warps >= 0 && p.ctas_per_sm >= 0 &&
          p.wait_timeout_ms >= 0 && p.chunk_order >= 0 && p.chunk_order <= 3 &&
          p.prefetch_chunks >= -1 && p.load_policy >= 0 && p.load_policy <= 2 &&
-         p.stage_layout >= 0 && p.stage_layout <= 2 && p.reduce_order >= 0 && p.reduce_order <= 1;
+         p.stage_layout >= 0 && p.stage_layout <= 2 && p.reduce_order >= 0 && p.reduce_order <= 1 &&
+         p.ce_fold >= 0 && p.ce_fold <= 2;
 }
 
 void dump_plan(const Plan& pl, const Lowered& low) {
@@ -895,7 +903,7 @@ tcclResult_t tcclCopyOutInspect(int coll, int nranks, const void* const sendbufs
     copy_out_segments(c, count, es, &seg, &nseg);
     *segments = nseg;
     *segment_elems = seg;
-    *register_fold = register_fold_ok(coll, nranks, sm.data(), rm.data(), count, es, seg) ? 1 : 0;
+    *register_fold = allreduce_register_fold(c, nranks, sm.data(), rm.data(), count, es, seg) ? 1 : 0;
   } else if (coll == kReduceScatter) {
     *register_fold = register_fold_ok(coll, nranks, sm.data(), rm.data(), count, es, 0) ? 1 : 0;
     *copy_out = *register_fold;  // otherwise the bulk engine runs it

@@ -99,8 +99,9 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
     }
   };
   const uintptr_t mod = (uintptr_t)recv[anchor] & 15;
-  const bool fast = register_fold_ok(kAllReduce, P, mod16_of(P, send).data(),
-                                     mod16_of(P, (const void* const*)recv).data(), count, es, seg);
+  const bool fast = allreduce_register_fold(g->cfg, P, mod16_of(P, send).data(),
+                                            mod16_of(P, (const void* const*)recv).data(), count,
+                                            es, seg);
   const size_t tail_n = count - (size_t)(nseg - 1) * seg;
   // TMA fallback: both plans (full segments, ragged tail) before any launch,
   // since a new plan's table upload is synchronous

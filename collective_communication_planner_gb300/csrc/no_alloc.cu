@@ -10,6 +10,13 @@
 // per-CTA offsets and the window table) lives in one file-scope __device__
 // array below, which every GPU that loads this library holds until the
 // process exits. The caller passes only inputs and outputs.
+//
+// A kernel that gives up on a bounded wait records tcclDeviceTimeout in the
+// array's status word, which stays set until a later call reads it: each
+// call first asks, without waiting, whether the kernel of the previous call
+// on the device has finished (an event recorded after it) and, if so, reads
+// the word on a private stream. A recorded timeout makes that call return
+// tcclDeviceTimeout without launching anything, and clears the word.
 #include "tccl.h"
 
 #include <cuda_runtime.h>
@@ -28,7 +35,7 @@ namespace {
 
 constexpr size_t kScratchBytes = TCCL_NO_ALLOC_SCRATCH_BYTES;
 // Layout of the scratch array (byte offsets).
-constexpr size_t kStatusOff = 0;                 // int status word (cleared every call)
+constexpr size_t kStatusOff = 0;                 // int status word (cleared once read)
 constexpr size_t kSchedOff = 64;                 // two 8-byte scheduler words (cleared every call)
 constexpr size_t kCtaOff = 256;                  // uint32_t per-CTA scalar-window offsets
 constexpr size_t kPrefixOff = kCtaOff + 4 * (TCCL_NO_ALLOC_MAX_CTAS + 1 + 63);
@@ -47,6 +54,9 @@ struct DeviceSetup {
   bool ready = false;
   unsigned char* scratch = nullptr;  // device address of g_no_alloc_scratch
   DeviceDesc dev;
+  cudaEvent_t done = nullptr;        // recorded after every launch
+  cudaStream_t side = nullptr;       // reads and clears the status word
+  bool unread = false;               // a launch whose status word was not read yet
 };
 
 constexpr int kMaxDevices = 64;
@@ -68,6 +78,10 @@ int setup_device(int device, DeviceSetup** out) {
         cudaDeviceGetAttribute(&s.dev.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess)
       return tcclCudaError;
     if (prepare_bulk_kernels((size_t)s.dev.smem_optin) != 0) return tcclCudaError;
+    if (!s.done && cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess)
+      return tcclCudaError;
+    if (!s.side && cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking) != cudaSuccess)
+      return tcclCudaError;
     s.scratch = static_cast<unsigned char*>(ptr);
     s.ready = true;
   }
@@ -78,6 +92,35 @@ int setup_device(int device, DeviceSetup** out) {
 bool log_on() {
   const char* e = std::getenv("TCCL_LOG");
   return e && std::atoi(e) > 0;
+}
+
+// Test hook for the timeout path: TCCL_NO_ALLOC_INJECT_TIMEOUT_MS > 0 makes
+// the first CTA of each launch wait that long on a barrier nothing signals.
+uint64_t injected_wait_ns() {
+  const char* e = std::getenv("TCCL_NO_ALLOC_INJECT_TIMEOUT_MS");
+  const double ms = e ? std::atof(e) : 0.0;
+  return ms > 0 ? (uint64_t)(ms * 1e6) : 0;
+}
+
+// The status of earlier launches, if the last one has finished: tcclSuccess
+// (also while it is still running: it is read by a later call), or
+// tcclDeviceTimeout, which is cleared here.
+int read_status(DeviceSetup* ds) {
+  if (!ds->unread) return tcclSuccess;
+  const cudaError_t q = cudaEventQuery(ds->done);
+  if (q == cudaErrorNotReady) return tcclSuccess;
+  if (q != cudaSuccess) return tcclCudaError;
+  int st = 0;
+  if (cudaMemcpyFromSymbolAsync(&st, g_no_alloc_scratch, sizeof(int), kStatusOff,
+                                cudaMemcpyDeviceToHost, ds->side) != cudaSuccess ||
+      cudaStreamSynchronize(ds->side) != cudaSuccess)
+    return tcclCudaError;
+  ds->unread = false;
+  if (st == 0) return tcclSuccess;
+  if (cudaMemsetAsync(ds->scratch + kStatusOff, 0, sizeof(int), ds->side) != cudaSuccess ||
+      cudaStreamSynchronize(ds->side) != cudaSuccess)
+    return tcclCudaError;
+  return tcclDeviceTimeout;
 }
 
 }  // namespace
@@ -92,10 +135,17 @@ extern "C" tcclResult_t tcclAllReduceNoAlloc(int nranks, const void* const sendb
   int v = validate_collective_args(kAllReduce, nranks, sendbufs, recvbufs, count, datatype, op);
   if (v != tcclSuccess) return (tcclResult_t)v;
   if (count == 0 || (nranks == 1 && sendbufs[0] == recvbufs[0])) return tcclSuccess;
+  // each call stages its plan from host memory with an ordinary copy, which
+  // a stream capture cannot hold: refuse a capturing stream up front
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return tcclCudaError;
+  if (cs != cudaStreamCaptureStatusNone) return tcclInvalidUsage;
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess) return tcclCudaError;
   DeviceSetup* ds = nullptr;
   int st = setup_device(device, &ds);
+  if (st != tcclSuccess) return (tcclResult_t)st;
+  st = read_status(ds);
   if (st != tcclSuccess) return (tcclResult_t)st;
 
   const int es = datatype == tcclBfloat16 ? 2 : 4;
@@ -124,13 +174,13 @@ extern "C" tcclResult_t tcclAllReduceNoAlloc(int nranks, const void* const sendb
   }
 
   // Stage this call's plan into the shared scratch, in stream order, and
-  // clear the status word the kernel reports timeouts in and the chunk
-  // scheduler's counters.
+  // clear the chunk scheduler's counters (the status word keeps whatever an
+  // earlier launch recorded until a call reads it).
   unsigned char* base = ds->scratch;
   const size_t wbytes = low.win.size() * sizeof(Window);
   const size_t pbytes = low.chunk_prefix.size() * sizeof(uint64_t);
   const size_t cbytes = low.cta_first.size() * sizeof(uint32_t);
-  if (cudaMemsetAsync(base + kStatusOff, 0, kCtaOff, stream) != cudaSuccess ||
+  if (cudaMemsetAsync(base + kSchedOff, 0, kCtaOff - kSchedOff, stream) != cudaSuccess ||
       cudaMemcpyAsync(base + kCtaOff, low.cta_first.data(), cbytes, cudaMemcpyHostToDevice,
                       stream) != cudaSuccess ||
       cudaMemcpyAsync(base + kPrefixOff, low.chunk_prefix.data(), pbytes,
@@ -159,7 +209,7 @@ extern "C" tcclResult_t tcclAllReduceNoAlloc(int nranks, const void* const sendb
   a.status = reinterpret_cast<int*>(base + kStatusOff);
   a.sm_mask = nullptr;
   a.timeout_ns = (uint64_t)(resolve_config(cfg).wait_timeout_ms * 1e6);
-  a.inject_timeout_ns = 0;
+  a.inject_timeout_ns = injected_wait_ns();
   a.nranks = nranks;
   a.chunk_bytes = low.shape.chunk_bytes;
   a.stages = low.shape.stages;
@@ -168,5 +218,8 @@ extern "C" tcclResult_t tcclAllReduceNoAlloc(int nranks, const void* const sendb
   a.release_lag = low.shape.release_lag;
   a.elem_size = es;
   int err = launch_bulk(kAllReduce, datatype, op, a, low.shape, stream);
-  return err == 0 ? tcclSuccess : tcclCudaError;
+  if (err == 0) err = cudaEventRecord(ds->done, stream);
+  if (err != 0) return tcclCudaError;
+  ds->unread = true;
+  return tcclSuccess;
 }

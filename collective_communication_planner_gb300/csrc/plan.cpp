@@ -161,6 +161,7 @@ Config resolve_config(const Config& in) {
   if (c.ce_segment_bytes == 0) c.ce_segment_bytes = (size_t)32 << 20;
   c.ce_segment_bytes = std::min<size_t>(std::max<size_t>(c.ce_segment_bytes, 4096), (size_t)1 << 30) & ~(size_t)255;
   if (c.reduce_order != 1) c.reduce_order = 0;
+  if (c.ce_fold < kFoldAuto || c.ce_fold > kFoldTma) c.ce_fold = kFoldAuto;
   return c;
 }
 
@@ -206,6 +207,12 @@ bool register_fold_ok(int coll, int nranks, const uint8_t* send_mod16, const uin
     return bytes % 16 == 0 && bytes / 16 < kFoldMaxVectors;
   }
   return seg_elems * (size_t)es / 16 < kFoldMaxVectors;
+}
+
+bool allreduce_register_fold(const Config& c, int nranks, const uint8_t* send_mod16,
+                             const uint8_t* recv_mod16, size_t count, int es, size_t seg_elems) {
+  if (c.ce_fold == kFoldTma) return false;
+  return register_fold_ok(kAllReduce, nranks, send_mod16, recv_mod16, count, es, seg_elems);
 }
 
 // Body windows -> one chunk sequence (prefix table), element-wise windows cut

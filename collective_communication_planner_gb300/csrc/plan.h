@@ -84,7 +84,13 @@ struct Config {
   size_t ce_segment_bytes = 0;
   int ce_auto_max_cap = 0;
   int reduce_order = 0;  // 0 ascending, 1 arrival (TMA-reduce engine only)
+  int ce_fold = 0;       // copy-out allreduce shard-in: kFoldAuto / kFoldRegister / kFoldTma
 };
+
+// The copy-out allreduce's shard-in kernel. Auto and Register: the
+// register-load fold wherever the buffers allow it (register_fold_ok), else
+// the bulk engine's TMA pipeline; Tma: always the TMA pipeline.
+enum CeFold : int { kFoldAuto = 0, kFoldRegister = 1, kFoldTma = 2 };
 
 // Fills zero fields with the library defaults.
 Config resolve_config(const Config& in);
@@ -136,6 +142,12 @@ void copy_out_segments(const Config& c, size_t count, int es, size_t* seg_elems,
 // allreduce's segment length (ignored for reduce-scatter).
 bool register_fold_ok(int coll, int nranks, const uint8_t* send_mod16, const uint8_t* recv_mod16,
                       size_t count, int es, size_t seg_elems);
+
+// Whether a copy-out allreduce's segments fold with the register-load kernel
+// (else the TMA pipeline): register_fold_ok, unless the config asks for the
+// TMA pipeline (ce_fold = kFoldTma).
+bool allreduce_register_fold(const Config& c, int nranks, const uint8_t* send_mod16,
+                             const uint8_t* recv_mod16, size_t count, int es, size_t seg_elems);
 
 struct Lowered {
   LaunchShape shape;

@@ -129,7 +129,7 @@ typedef enum {
  * TCCL_STORE_MODE, TCCL_CONSUMER_WARPS, TCCL_CTAS_PER_SM,
  * TCCL_WAIT_TIMEOUT_MS, TCCL_CHUNK_ORDER, TCCL_PREFETCH_CHUNKS,
  * TCCL_LOAD_POLICY, TCCL_MAX_CHUNK_BYTES, TCCL_STAGE_LAYOUT, TCCL_CE_STREAMS,
- * TCCL_CE_SEGMENT_BYTES, TCCL_CE_AUTO_MAX_CAP and TCCL_REDUCE_ORDER once). Zero in a field
+ * TCCL_CE_SEGMENT_BYTES, TCCL_CE_AUTO_MAX_CAP, TCCL_REDUCE_ORDER and TCCL_CE_FOLD once). Zero in a field
  * means "library default".
  *
  * Bulk-engine shape: stage_bytes, stages and max_chunk_bytes default to 64 KiB,
@@ -164,6 +164,11 @@ typedef struct {
   int ce_auto_max_cap;     /* Auto picks the copy-out engine for caps up to this many CTAs
                               (0: 5/16 of the SMs; negative: never) */
   int reduce_order;        /* tcclReduceOrder_t (default ascending) */
+  int ce_fold;             /* copy-out allreduce, the kernel that folds each segment into the anchor:
+                              0 or 1: the 128-bit register-load fold where every send buffer
+                              shares its address mod 16 with the anchor's receive buffer, else the
+                              bulk engine's TMA pipeline; 2: always the TMA pipeline (with the
+                              group's stage layout and shape) */
 } tcclConfig_t;
 
 /* What the last launch on a group looked like. */
@@ -439,16 +444,31 @@ tcclResult_t tcclReshardInspect(const tcclLayout_t* src, const tcclLayout_t* dst
  * holds until the process exits; host-side planning uses ordinary C++ heap
  * memory.
  *  - The first call on a device (with that device current) resolves the
- *    array's device address with cudaGetSymbolAddress; make that first call
- *    before any stream capture.
- *  - Every call shares the one array and overwrites it, in stream order, with
- *    its own plan, so calls whose work overlaps on the GPU (different streams,
- *    or other threads) race and give undefined results. Serialise them.
+ *    array's device address with cudaGetSymbolAddress and creates one event
+ *    and one stream for reading the status word; make that first call before
+ *    any stream capture.
+ *  - Each call copies its plan from host memory into the array, in stream
+ *    order. A call on a stream that is being captured returns
+ *    tcclInvalidUsage and enqueues nothing.
+ *  - Every call shares the one array and overwrites it with its own plan, so
+ *    calls whose work overlaps on the GPU (different streams, or other
+ *    threads) race and give undefined results. Serialise them; the function
+ *    is not thread safe.
  *  - Plans needing more than TCCL_NO_ALLOC_MAX_CTAS CTAs, or more windows
  *    than the array holds, are rejected with tcclInvalidUsage (TCCL_LOG=1
  *    prints the sizes); every other argument rule is tcclAllReduce's.
- *  - A device-side wait that gives up is not reported: the kernel records it
- *    in the array's status word, which this call clears and nothing reads.
+ *  - Device-side timeouts: a kernel that gives up on a bounded wait skips
+ *    the rest of its work (its outputs are undefined) and records
+ *    tcclDeviceTimeout in the array's status word. A later call on the same
+ *    device reports it: each call first checks, without waiting, whether the
+ *    previous call's kernel has finished and, if so, reads the word. When it
+ *    finds a timeout recorded, the call returns tcclDeviceTimeout, launches
+ *    nothing and clears the record; call again to run it. A timeout of the
+ *    last call is therefore seen by the next call made after that call's
+ *    work has finished (for instance after a stream synchronisation).
+ *  - Test hook: the environment variable TCCL_NO_ALLOC_INJECT_TIMEOUT_MS > 0
+ *    makes the first CTA of each launch wait that many milliseconds on a
+ *    barrier nothing signals, so the timeout path can be exercised.
  */
 #define TCCL_NO_ALLOC_SCRATCH_BYTES (256 * 1024)
 #define TCCL_NO_ALLOC_MAX_CTAS 1024

@@ -442,3 +442,20 @@ def test_shard_in_kernel_choice(groups, offs, fast, p):
     info = g.last_launch()
     assert info["threads"] == (1024 if fast else 544) and info["ctas"] <= 6, info
     check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), f"offs {offs} P={p}")
+
+
+@pytest.mark.parametrize("layout,warps", [(0, 0), (2, 0), (2, 8)])
+@pytest.mark.parametrize("dtype,op,p", [("bf16", "sum", 8), ("f32", "max", 3), ("i32", "sum", 4)])
+def test_tma_fold_when_asked(groups, layout, warps, dtype, op, p):
+    """ce_fold = 2 puts the segments of co-aligned buffers on the TMA pipeline
+    (shared or per-rank stage layout) instead of the register fold; the
+    result is the same bits."""
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=256 * 1024, ce_fold=2, stage_layout=layout,
+                 consumer_warps=warps)
+    xs = datagen.rank_buffers(KIND[dtype], 33, p, 500_009)
+    got = allreduce(g, xs, dtype, op, cap=5)
+    info = g.last_launch()
+    assert info["engine"] == CE and info["threads"] != 1024 and info["ctas"] <= 5, info
+    assert info["stage_layout"] == (2 if layout == 2 else 1), info
+    check(got, oracle.allreduce(xs, dtype, op, nthreads=0), f"TMA fold layout {layout} P={p}")
