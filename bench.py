@@ -1105,6 +1105,92 @@ def rmsnorm_bench(args):
     g_row.close()
 
 
+# ------------------------------------------------------------------ host-cost mode
+def build_host_cost() -> Path:
+    """Compiles tests/host_cost.cu (a C++ driver of the C ABI) against the
+    in-tree libtccl.so; returns the executable's path."""
+    pkg = ROOT / "collective_communication_planner_gb300"
+    out = pkg / "_build" / "host_cost"
+    out.parent.mkdir(exist_ok=True)
+    subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-std=c++17",
+                           f"-I{ROOT / 'include'}", str(ROOT / "tests" / "host_cost.cu"), "-o", str(out),
+                           f"-L{pkg}", "-ltccl", "-Xlinker", "-rpath", "-Xlinker", str(pkg)])
+    return out
+
+
+def host_cost(args):
+    """Per-call host cost of tcclAllReduce from C++ (no ctypes): enqueue time,
+    device time and graph-replay time for decode-sized messages, beside the
+    empty-kernel launch floor. One JSON line per case."""
+    exe = build_host_cost()
+    r = subprocess.run([str(exe), str(args.host_cost_batches)], capture_output=True, text=True)
+    sys.stdout.write(r.stdout)
+    if r.returncode != 0:
+        raise SystemExit(f"host-cost driver failed ({r.returncode}): {r.stderr.strip()}")
+
+
+# ------------------------------------------------------------------ TMA-reduce mode
+def tma_reduce_bench(args):
+    """The TMA-reduce engine (the copy hardware applies the reduction) beside
+    the bulk engine's register fold: fp32 sum allreduce of 64 MiB per rank,
+    out of place, P = 4 and 8, uncapped and under caps, ascending and arrival
+    order. Device time per call (CUDA events over back-to-back calls), HBM
+    fraction of 2 * P * S, sampled parity against the oracle. A fixed number
+    of launches per line, so the command also serves ncu."""
+    import numpy as np
+    import torch
+    import collective_communication_planner_gb300 as tccl
+    import datagen
+    import oracle
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    st = stream.cuda_stream
+    peak, _ = measured_peak()
+    n = (64 << 20) // 4
+    for p in [int(x) for x in args.tma_reduce_ranks.split(",")]:
+        xs = datagen.rank_buffers("uniform_f32", 2, p, n)
+        sends = [torch.from_numpy(x).to(dev) for x in xs]
+        recvs = [torch.empty_like(t) for t in sends]
+        idx = np.sort(np.random.default_rng(9).choice(n, size=4096, replace=False))
+        exp = oracle.allreduce([x[idx].copy() for x in xs], "f32", "sum")[0]
+        g = tccl.Group(p)
+        for cap in [int(c) for c in args.tma_reduce_caps.split(",")]:
+            for engine, order in ((tccl.tcclEngineBulk, 0), (tccl.tcclEngineTmaReduce, 0),
+                                  (tccl.tcclEngineTmaReduce, 1)):
+                c = tccl.tcclConfig_t()
+                c.engine, c.reduce_order = engine, order
+                assert tccl.tcclGroupSetConfig(g.handle, c) == 0
+                for t in recvs:
+                    t.fill_(0)
+                call = lambda: tccl.tcclAllReduce(g.handle, sends, recvs, n, tccl.tcclFloat32,
+                                                  tccl.tcclSum, st, cap)
+                for _ in range(3):
+                    assert call() == 0
+                stream.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(10):
+                    assert call() == 0
+                e1.record(stream)
+                e1.synchronize()
+                ms = e0.elapsed_time(e1) / 10
+                info = g.last_launch()
+                got = recvs[p - 1].cpu().numpy()[idx]
+                exact = bool(np.array_equal(got.view(np.uint32), exp.view(np.uint32)))
+                print(json.dumps({"mode": "tma_reduce", "P": p, "bytes_per_rank": n * 4, "cap": cap,
+                                  "engine": "tma_reduce" if engine == tccl.tcclEngineTmaReduce else "bulk",
+                                  "order": "arrival" if order else "ascending", "ctas": info["ctas"],
+                                  "threads": info["threads"], "chunk_bytes": info["chunk_bytes"],
+                                  "stages": info["stages"], "us": round(ms * 1e3, 2),
+                                  "hbm_fraction": round(2 * p * n * 4 / (ms * 1e-3) / 1e9 / peak, 4),
+                                  "sampled_exact": exact}), flush=True)
+        assert g.query_error() == tccl.tcclSuccess
+        g.close()
+        del sends, recvs
+
+
 # ------------------------------------------------------------------ copy-out mode
 def copy_out_bench(args):
     """The C4 allreduce (P=8, bf16, 128 MiB per rank) at CTA caps 8, 16 and
@@ -1215,6 +1301,13 @@ def main():
                     help="for --copy-out: comma list of auto, sm_only, tma_shared, tma_per_rank, "
                          "tma_per_rank_8w (default auto,sm_only)")
     ap.add_argument("--copy-out-caps", default="8,16,32", help="for --copy-out: CTA caps")
+    ap.add_argument("--host-cost", action="store_true",
+                    help="per-call host cost of tcclAllReduce from a C++ driver (decode-sized messages)")
+    ap.add_argument("--host-cost-batches", type=int, default=50)
+    ap.add_argument("--tma-reduce", action="store_true",
+                    help="TMA-reduce engine vs the bulk engine, fp32 sum, 64 MiB per rank")
+    ap.add_argument("--tma-reduce-ranks", default="4,8")
+    ap.add_argument("--tma-reduce-caps", default="0,32,16")
     ap.add_argument("--gemm-n", type=int, default=8192)
     ap.add_argument("--overlap-engine", type=int, default=0,
                     help="engine for the overlap study (0 auto, 1 bulk, 4 TMA-reduce)")
@@ -1258,6 +1351,12 @@ def main():
         return
     if args.copy_out:
         copy_out_bench(args)
+        return
+    if args.host_cost:
+        host_cost(args)
+        return
+    if args.tma_reduce:
+        tma_reduce_bench(args)
         return
     if dist is not None:
         dist.barrier()
