@@ -1233,6 +1233,15 @@ def copy_out_bench(args):
         "tma_shared": {"ce_fold": 2},
         "tma_per_rank": {"ce_fold": 2, "stage_layout": 2},
         "tma_per_rank_8w": {"ce_fold": 2, "stage_layout": 2, "consumer_warps": 8},
+        # the segment schedule: a shorter last segment (its copies overlap no
+        # fold), more segments, fewer copy streams
+        "tail30": {"ce_tail_percent": 30},
+        "tail45": {"ce_tail_percent": 45},
+        "tail60": {"ce_tail_percent": 60},
+        "seg16": {"ce_segment_bytes": 16 << 20},
+        "seg16_tail45": {"ce_segment_bytes": 16 << 20, "ce_tail_percent": 45},
+        "streams1": {"ce_streams": 1},
+        "streams2": {"ce_streams": 2},
     }
     chosen = args.copy_out_variants.split(",") if args.copy_out_variants else ["auto", "sm_only"]
     caps = [int(c) for c in args.copy_out_caps.split(",")]
@@ -1299,7 +1308,8 @@ def main():
                     help="C4 at CTA caps 8/16/32: copy-out engine vs SM-only bulk engine")
     ap.add_argument("--copy-out-variants", default="",
                     help="for --copy-out: comma list of auto, sm_only, tma_shared, tma_per_rank, "
-                         "tma_per_rank_8w (default auto,sm_only)")
+                         "tma_per_rank_8w, tail30, tail45, tail60, seg16, seg16_tail45, streams1, "
+                         "streams2 (default auto,sm_only)")
     ap.add_argument("--copy-out-caps", default="8,16,32", help="for --copy-out: CTA caps")
     ap.add_argument("--host-cost", action="store_true",
                     help="per-call host cost of tcclAllReduce from a C++ driver (decode-sized messages)")

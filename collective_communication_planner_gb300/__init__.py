@@ -46,7 +46,8 @@ class tcclConfig_t(ctypes.Structure):
                 ("load_policy", ctypes.c_int), ("max_chunk_bytes", ctypes.c_size_t),
                 ("stage_layout", ctypes.c_int), ("ce_streams", ctypes.c_int),
                 ("ce_segment_bytes", ctypes.c_size_t), ("ce_auto_max_cap", ctypes.c_int),
-                ("reduce_order", ctypes.c_int), ("ce_fold", ctypes.c_int)]
+                ("reduce_order", ctypes.c_int), ("ce_fold", ctypes.c_int),
+                ("ce_tail_percent", ctypes.c_int)]
 
 
 class tcclLaunchInfo_t(ctypes.Structure):

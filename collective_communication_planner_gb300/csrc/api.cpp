@@ -127,6 +127,7 @@ Config config_from_env() {
   if (const char* e = std::getenv("TCCL_CE_SEGMENT_BYTES")) c.ce_segment_bytes = std::strtoull(e, 0, 10);
   c.ce_auto_max_cap = geti("TCCL_CE_AUTO_MAX_CAP", 0);
   if (const char* e = std::getenv("TCCL_REDUCE_ORDER")) c.reduce_order = std::string(e) == "arrival" ? 1 : 0;
+  c.ce_tail_percent = geti("TCCL_CE_TAIL_PERCENT", 0);
   if (const char* e = std::getenv("TCCL_CE_FOLD")) {
     std::string v(e);
     if (v == "register") c.ce_fold = kFoldRegister;
@@ -182,6 +183,7 @@ Config from_public(const tcclConfig_t& p) {
   c.ce_auto_max_cap = p.ce_auto_max_cap;
   c.reduce_order = p.reduce_order;
   c.ce_fold = p.ce_fold;
+  c.ce_tail_percent = p.ce_tail_percent;
   return resolve_config(c);
 }
 
@@ -207,6 +209,7 @@ tcclConfig_t to_public(const Config& c) {
   p.ce_auto_max_cap = c.ce_auto_max_cap;
   p.reduce_order = c.reduce_order;
   p.ce_fold = c.ce_fold;
+  p.ce_tail_percent = c.ce_tail_percent;
   return p;
 }
 
@@ -217,7 +220,7 @@ bool config_ok(const tcclConfig_t& p) {
          p.wait_timeout_ms >= 0 && p.chunk_order >= 0 && p.chunk_order <= 3 &&
          p.prefetch_chunks >= -1 && p.load_policy >= 0 && p.load_policy <= 2 &&
          p.stage_layout >= 0 && p.stage_layout <= 2 && p.reduce_order >= 0 && p.reduce_order <= 1 &&
-         p.ce_fold >= 0 && p.ce_fold <= 2;
+         p.ce_fold >= 0 && p.ce_fold <= 2 && p.ce_tail_percent >= 0 && p.ce_tail_percent <= 100;
 }
 
 void dump_plan(const Plan& pl, const Lowered& low) {

@@ -162,6 +162,7 @@ Config resolve_config(const Config& in) {
   c.ce_segment_bytes = std::min<size_t>(std::max<size_t>(c.ce_segment_bytes, 4096), (size_t)1 << 30) & ~(size_t)255;
   if (c.reduce_order != 1) c.reduce_order = 0;
   if (c.ce_fold < kFoldAuto || c.ce_fold > kFoldTma) c.ce_fold = kFoldAuto;
+  if (c.ce_tail_percent <= 0 || c.ce_tail_percent > 100) c.ce_tail_percent = 100;
   return c;
 }
 
@@ -191,6 +192,14 @@ void copy_out_segments(const Config& c, size_t count, int es, size_t* seg_elems,
   size_t seg = std::max<size_t>(align, (seg_bytes / (size_t)es) / align * align);
   if ((count + seg - 1) / seg > (size_t)kMaxCeSegments)
     seg = ((count + kMaxCeSegments - 1) / kMaxCeSegments + align - 1) / align * align;
+  const size_t n = (count + seg - 1) / seg;
+  if (n >= 2 && c.ce_tail_percent > 0 && c.ce_tail_percent < 100) {
+    // n - 1 full segments of s and a last one of about f s: s = count / (n - 1 + f)
+    const double f = c.ce_tail_percent / 100.0;
+    size_t s = (size_t)((double)count / ((double)(n - 1) + f));
+    s = (s + align - 1) / align * align;
+    if (s >= seg && (n - 1) * s < count) seg = s;
+  }
   *seg_elems = seg;
   *nseg = (int)((count + seg - 1) / seg);
 }

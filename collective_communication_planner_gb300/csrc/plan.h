@@ -85,6 +85,7 @@ struct Config {
   int ce_auto_max_cap = 0;
   int reduce_order = 0;  // 0 ascending, 1 arrival (TMA-reduce engine only)
   int ce_fold = 0;       // copy-out allreduce shard-in: kFoldAuto / kFoldRegister / kFoldTma
+  int ce_tail_percent = 0;  // copy-out allreduce: last segment's length, % of the others (0: 100)
 };
 
 // The copy-out allreduce's shard-in kernel. Auto and Register: the
@@ -131,7 +132,11 @@ bool copy_out_chosen(const Config& c, int sm_count, int nranks, int coll, size_t
 // Segments of a copy-out allreduce of `count` elements: at most
 // ce_segment_bytes per rank, at least four where each stays >= 4 MiB, at most
 // kMaxCeSegments, offsets multiples of 256 bytes. *seg_elems is the length of
-// every segment but the last (which holds the rest).
+// every segment but the last (which holds the rest). With ce_tail_percent
+// below 100, the same number of segments is kept and the last one is cut to
+// about that share of the others, which grow (past ce_segment_bytes if need
+// be) to cover the rest: the last segment's copies overlap no fold, so a
+// shorter last segment shortens the call's exposed tail.
 void copy_out_segments(const Config& c, size_t count, int es, size_t* seg_elems, int* nseg);
 
 // Whether the register-load fold takes a copy-out call (else the TMA

@@ -129,7 +129,8 @@ typedef enum {
  * TCCL_STORE_MODE, TCCL_CONSUMER_WARPS, TCCL_CTAS_PER_SM,
  * TCCL_WAIT_TIMEOUT_MS, TCCL_CHUNK_ORDER, TCCL_PREFETCH_CHUNKS,
  * TCCL_LOAD_POLICY, TCCL_MAX_CHUNK_BYTES, TCCL_STAGE_LAYOUT, TCCL_CE_STREAMS,
- * TCCL_CE_SEGMENT_BYTES, TCCL_CE_AUTO_MAX_CAP, TCCL_REDUCE_ORDER and TCCL_CE_FOLD once). Zero in a field
+ * TCCL_CE_SEGMENT_BYTES, TCCL_CE_AUTO_MAX_CAP, TCCL_REDUCE_ORDER, TCCL_CE_FOLD and
+ * TCCL_CE_TAIL_PERCENT once). Zero in a field
  * means "library default".
  *
  * Bulk-engine shape: stage_bytes, stages and max_chunk_bytes default to 64 KiB,
@@ -169,6 +170,11 @@ typedef struct {
                               shares its address mod 16 with the anchor's receive buffer, else the
                               bulk engine's TMA pipeline; 2: always the TMA pipeline (with the
                               group's stage layout and shape) */
+  int ce_tail_percent;     /* copy-out allreduce: the last segment's length as a percentage of
+                              the others (1..100; 0: default 100, equal segments). The number
+                              of segments stays the same and the others grow to cover the rest
+                              (past ce_segment_bytes if need be): the last segment's copies
+                              overlap no fold, so a shorter last segment shortens the tail */
 } tcclConfig_t;
 
 /* What the last launch on a group looked like. */

@@ -155,3 +155,25 @@ def test_errors_and_empty_calls():
     assert r[0] == tccl.tcclInvalidArgument
     assert tccl.tcclCopyOutInspect(AR, 4, send, recv, 1 << 20, BF16, 8, 0)[0] == tccl.tcclInvalidArgument
     assert tccl.tcclCopyOutInspect(AR, 4, send, recv, 1 << 20, 7, 8, SMS)[0] == tccl.tcclInvalidArgument
+
+
+@pytest.mark.parametrize("pct", [30, 45, 60, 100])
+@pytest.mark.parametrize("mib", [16, 128, 1000])
+def test_short_last_segment(pct, mib):
+    """ce_tail_percent keeps the number of segments and cuts the last one to
+    about that share of the others (which grow to cover the rest)."""
+    es = 2
+    count = mib * MiB // es
+    _, _, ns0, se0 = inspect(AR, 8, count, cap=16)
+    co, rf, ns, se = inspect(AR, 8, count, cap=16, cfg=config(ce_tail_percent=pct))
+    assert co == 1 and ns == ns0
+    last = count - (ns - 1) * se
+    assert se * es % 256 == 0 and 0 < last <= se
+    last0 = count - (ns0 - 1) * se0
+    if pct == 100 or last0 <= pct / 100 * se0:
+        # equal segments, or the equal split's ragged last one is short enough already
+        assert se == se0
+    else:
+        assert se >= se0
+        # the last segment is pct % of the others, to within the 256-byte rounding of each
+        assert abs(last - pct / 100 * se) <= ns * 256 // es, (last, se)
