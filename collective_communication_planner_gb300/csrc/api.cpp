@@ -128,6 +128,7 @@ Config config_from_env() {
   c.ce_auto_max_cap = geti("TCCL_CE_AUTO_MAX_CAP", 0);
   if (const char* e = std::getenv("TCCL_REDUCE_ORDER")) c.reduce_order = std::string(e) == "arrival" ? 1 : 0;
   c.ce_tail_percent = geti("TCCL_CE_TAIL_PERCENT", 0);
+  c.reduce_slots = geti("TCCL_REDUCE_SLOTS", 0);
   if (const char* e = std::getenv("TCCL_CE_FOLD")) {
     std::string v(e);
     if (v == "register") c.ce_fold = kFoldRegister;
@@ -184,6 +185,7 @@ Config from_public(const tcclConfig_t& p) {
   c.reduce_order = p.reduce_order;
   c.ce_fold = p.ce_fold;
   c.ce_tail_percent = p.ce_tail_percent;
+  c.reduce_slots = p.reduce_slots;
   return resolve_config(c);
 }
 
@@ -210,6 +212,7 @@ tcclConfig_t to_public(const Config& c) {
   p.reduce_order = c.reduce_order;
   p.ce_fold = c.ce_fold;
   p.ce_tail_percent = c.ce_tail_percent;
+  p.reduce_slots = c.reduce_slots;
   return p;
 }
 
@@ -220,7 +223,8 @@ bool config_ok(const tcclConfig_t& p) {
          p.wait_timeout_ms >= 0 && p.chunk_order >= 0 && p.chunk_order <= 3 &&
          p.prefetch_chunks >= -1 && p.load_policy >= 0 && p.load_policy <= 2 &&
          p.stage_layout >= 0 && p.stage_layout <= 2 && p.reduce_order >= 0 && p.reduce_order <= 1 &&
-         p.ce_fold >= 0 && p.ce_fold <= 2 && p.ce_tail_percent >= 0 && p.ce_tail_percent <= 100;
+         p.ce_fold >= 0 && p.ce_fold <= 2 && p.ce_tail_percent >= 0 && p.ce_tail_percent <= 100 &&
+         p.reduce_slots >= 0 && p.reduce_slots <= 8;
 }
 
 void dump_plan(const Plan& pl, const Lowered& low) {
@@ -359,6 +363,8 @@ int launch_plan(tcclGroup* g, CachedPlan* cp, int coll, int dtype, int op,
     a.rank_streamed = low.shape.rank_streamed;
     a.load_evict_first = low.shape.load_evict_first;
     a.arrival_order = low.shape.engine == kEngineTmaReduce && g->cfg.reduce_order == 1 ? 1 : 0;
+    a.reduce_slots = low.shape.reduce_slots;
+    a.reduce_bufs = low.shape.reduce_bufs;
     a.status = g->d_status;
     a.sm_mask = mask;
     a.timeout_ns = (uint64_t)(g->cfg.wait_timeout_ms * 1e6);

@@ -31,6 +31,10 @@ enum ChunkOrder : int { kOrderAuto = 0, kOrderBlocked = 1, kOrderCyclic = 2, kOr
 enum StageLayout : int { kLayoutAuto = 0, kLayoutShared = 1, kLayoutPerRank = 2 };
 
 constexpr int kMaxConsumerWarps = 16;  // bulk kernel: 1 + 16 warps = 544 threads
+constexpr int kMaxReduceSlots = 8;     // TMA-reduce engine: chunk slots per issuing thread
+// TMA-reduce engine: mbarriers (lanes x slots x buffers) its 1 KiB
+// shared-memory head holds, beside a test barrier and the abort flag
+constexpr int kReduceMaxBarriers = 120;
 constexpr int kPerRankVectors = 4;     // per-rank layout: 16-byte vectors per consumer thread
 
 // Status codes a kernel may leave in the group's status word (same values
@@ -91,6 +95,8 @@ struct BulkArgs {
   int prefetch_chunks;           // L2 prefetch distance beyond the shared-memory ring (0: off)
   int load_evict_first;          // bulk loads carry an L2 evict-first policy
   int arrival_order;             // TMA-reduce engine: ranks 1..P-1 reduced as they arrive
+  int reduce_slots;              // TMA-reduce engine: chunks each issuing thread keeps in flight
+  int reduce_bufs;               // TMA-reduce engine: buffers per slot (2, or 3 for reduce-scatter)
 };
 
 // Warp / vec (small-message) engines: the whole lowered plan rides in the
@@ -121,6 +127,8 @@ struct LaunchShape {
   int prefetch_chunks = 0;
   int load_evict_first = 0;
   int early_launch = 0;  // bulk engine, uncapped: programmatic dependent launch
+  int reduce_slots = 0;  // TMA-reduce engine: chunk slots per issuing thread
+  int reduce_bufs = 0;   // TMA-reduce engine: buffers per slot
   size_t smem = 0;
 };
 

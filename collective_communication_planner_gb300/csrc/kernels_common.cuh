@@ -901,104 +901,166 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
 // The reduction itself offloaded to the copy hardware, as the shard-in of the
 // T-CCL description does: for each chunk, rank 0's data is bulk-stored into
 // the owner's buffer, then ranks 1 .. P-1 are bulk-reduced into it in
-// ascending order (each reduction complete before the next is issued, so the
-// order is fixed). For allreduce the final chunk is then loaded once and
-// bulk-stored to every other rank. No thread touches the data. Lane 0 of
-// every warp runs its own stream of chunks (every (grid x warps)-th chunk)
-// with two shared-memory buffers, so the load of rank r+1 overlaps the
-// reduction of rank r. Types the hardware reduces exactly in this order:
-// fp32 add (round to nearest), int32 add/min/max, bf16 min/max.
+// ascending order. For allreduce the final chunk is then loaded once and
+// bulk-stored to every other rank. No thread touches the data. Types the
+// hardware reduces exactly in this order: fp32 add (round to nearest), int32
+// add/min/max, bf16 min/max.
+//
+// Lane 0 of every warp issues the copies for K chunk slots at once (chunks
+// c, c + G, ..., c + (K-1) G of its stream, G = grid x warps), in lock step
+// over the ranks: slot 0's operation for rank r, slot 1's, ..., then rank
+// r + 1. Each operation is its own bulk async-group, so the group committed
+// K groups earlier is the same slot's previous rank: waiting until at most
+// K - 1 groups are pending orders the reductions into one owner chunk
+// (ascending) while the other K - 1 slots' reductions stay in flight. Each
+// slot double-buffers its rank loads; a reduce-scatter gets a third buffer:
+// in place, the owner's receive chunk is its own input chunk, which is
+// loaded first and kept there, since rank 0's store overwrites it.
+
+__device__ __forceinline__ void bulk_wait_all_dyn(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.bulk.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.bulk.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.bulk.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.bulk.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.bulk.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.bulk.wait_group 7;" ::: "memory"); break;
+  }
+}
+
 template <int COLL, int DT, int OP>
 __global__ void __launch_bounds__(32 * kMaxConsumerWarps, 1)
     reduce_kernel(const __grid_constant__ BulkArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // 2 per warp, then the test barrier
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 512);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* never = bars + kReduceMaxBarriers;  // test hook: a barrier nothing arrives on
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 8 * (kReduceMaxBarriers + 1));
   unsigned char* buf_base = smem + 1024;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int lanes = blockDim.x >> 5;
+  const int K = a.reduce_slots;
+  const int NB = a.reduce_bufs;
   const int P = a.nranks;
   const uint32_t chunk = static_cast<uint32_t>(a.chunk_bytes);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2 * lanes + 1; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < lanes * K * NB; ++i) mbar_init(&bars[i], 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_mbar_init();
     record_sm(a.sm_mask);
   }
   __syncthreads();
   if (lane == 0) {
-    uint64_t* bar = bars + 2 * warp;
-    unsigned char* xbase = buf_base + static_cast<size_t>(2 * warp) * chunk;
-    auto x = [&](int b) { return xbase + static_cast<size_t>(b) * chunk; };
-    uint32_t phase = 0;    // bit b: parity to wait for on bar[b]
-    uint32_t pending = 0;  // bit b: a load into buffer b not yet waited for
-    ChunkLocator loc;
-    loc.init();
-    bool ok = true;
-    const uint64_t first = static_cast<uint64_t>(blockIdx.x) * lanes + warp;
-    const uint64_t step = static_cast<uint64_t>(gridDim.x) * lanes;
-    auto issue = [&](int b, const char* src, uint32_t n) {
-      mbar_arrive_expect_tx(&bar[b], n);
-      bulk_load(x(b), src, n, &bar[b]);
-      pending |= 1u << b;
+    const int first_bar = warp * K * NB;
+    auto bar = [&](int j, int b) { return &bars[first_bar + j * NB + b]; };
+    auto buf = [&](int j, int b) {
+      return buf_base + static_cast<size_t>(first_bar + j * NB + b) * chunk;
     };
-    auto wait_buf = [&](int b) {
-      const bool done = wait_bounded(&bar[b], (phase >> b) & 1, abort_flag, a.timeout_ns,
+    uint32_t phase = 0;    // bit j * NB + b: parity to wait for on bar(j, b)
+    uint32_t pending = 0;  // bit j * NB + b: a load not yet waited for
+    auto issue = [&](int j, int b, const char* src, uint32_t n) {
+      mbar_arrive_expect_tx(bar(j, b), n);
+      bulk_load(buf(j, b), src, n, bar(j, b));
+      pending |= 1u << (j * NB + b);
+    };
+    auto wait_buf = [&](int j, int b) {
+      const int bit = j * NB + b;
+      const bool done = wait_bounded(bar(j, b), (phase >> bit) & 1, abort_flag, a.timeout_ns,
                                      a.status, true);
       if (done) {
-        phase ^= 1u << b;
-        pending &= ~(1u << b);
+        phase ^= 1u << bit;
+        pending &= ~(1u << bit);
       }
       return done;
     };
-    for (uint64_t c = first; c < a.total_chunks && ok; c += step) {
-      uint32_t off, n;
-      loc.locate(a, c, off, n);
-      const Window& w = loc.w;
-      const int owner_rank = w.dst_sel < 0 ? 0 : w.dst_sel;
-      char* owner = static_cast<char*>(a.p.dst[owner_rank]) + w.dst_off + off;
-      bulk_wait_read<0>();  // both buffers free: earlier stores have read them
-      issue(0, static_cast<const char*>(a.p.src[0]) + w.src_off + off, n);
-      int b = 0;
-      for (int r = 0; r < P; ++r) {
-        if (r + 1 < P) {
-          bulk_wait_read<0>();  // rank r-1's reduction has read the other buffer
-          issue(b ^ 1, static_cast<const char*>(a.p.src[r + 1]) + w.src_off + off, n);
+    // per-slot state of the current K chunks
+    uint64_t src_off[kMaxReduceSlots], dst_off[kMaxReduceSlots];
+    uint32_t nbytes[kMaxReduceSlots];
+    int owner_rank[kMaxReduceSlots], alias[kMaxReduceSlots];
+    ChunkLocator loc;
+    loc.init();
+    bool ok = true, injected = false;
+    const uint64_t step = static_cast<uint64_t>(gridDim.x) * lanes;
+    for (uint64_t base = static_cast<uint64_t>(blockIdx.x) * lanes + warp;
+         base < a.total_chunks && ok; base += step * K) {
+      int nvalid = 0;
+      for (int j = 0; j < K; ++j) {
+        const uint64_t c = base + j * step;
+        if (c >= a.total_chunks) break;
+        uint32_t off;
+        loc.locate(a, c, off, nbytes[j]);
+        src_off[j] = loc.w.src_off + off;
+        dst_off[j] = loc.w.dst_off + off;
+        owner_rank[j] = loc.w.dst_sel < 0 ? 0 : loc.w.dst_sel;
+        const char* own = static_cast<const char*>(a.p.dst[owner_rank[j]]) + dst_off[j];
+        alias[j] = (NB > 2 && owner_rank[j] > 0 &&
+                    own == static_cast<const char*>(a.p.src[owner_rank[j]]) + src_off[j])
+                       ? owner_rank[j] : -1;
+        ++nvalid;
+      }
+      bulk_wait_read<0>();  // earlier stores and reductions have read every buffer
+      for (int j = 0; j < nvalid; ++j) {
+        if (alias[j] > 0)
+          issue(j, 2, static_cast<const char*>(a.p.src[alias[j]]) + src_off[j], nbytes[j]);
+        issue(j, 0, static_cast<const char*>(a.p.src[0]) + src_off[j], nbytes[j]);
+      }
+      for (int r = 0; r < P && ok; ++r) {
+        for (int j = 0; j < K; ++j) {
+          if (j >= nvalid) {
+            bulk_commit();  // an empty group keeps every slot K groups apart
+            continue;
+          }
+          // slot j's operation for rank r - 1 is complete (the ascending
+          // order; in the arrival order only rank 0's store must land before
+          // the reductions, the rest need their buffers read)
+          if (r >= 1) {
+            if (r == 1 || !a.arrival_order) bulk_wait_all_dyn(K - 1);
+            else bulk_wait_read_dyn(K - 1);
+          }
+          if (r + 1 < P && r + 1 != alias[j])
+            issue(j, (r + 1) & 1, static_cast<const char*>(a.p.src[r + 1]) + src_off[j], nbytes[j]);
+          if (r == 0 && alias[j] > 0) ok = wait_buf(j, 2);  // the owner's own chunk is safe
+          const int b = r == alias[j] ? 2 : (r & 1);
+          if (ok && b != 2) ok = wait_buf(j, b);
+          if (ok && a.inject_timeout_ns && blockIdx.x == 0 && warp == 0 && !injected) {
+            injected = true;
+            ok = wait_bounded(never, 0, abort_flag, a.inject_timeout_ns, a.status, true);
+          }
+          if (!ok) break;
+          char* owner = static_cast<char*>(a.p.dst[owner_rank[j]]) + dst_off[j];
+          if (r == 0) bulk_store(owner, buf(j, b), nbytes[j]);
+          else bulk_reduce<DT, OP>(owner, buf(j, b), nbytes[j]);
+          bulk_commit();
         }
-        ok = wait_buf(b);
-        if (ok && a.inject_timeout_ns && blockIdx.x == 0 && warp == 0 && c == first && r == 0)
-          // test hook: a barrier nothing arrives on
-          ok = wait_bounded(&bars[2 * lanes], 0, abort_flag, a.inject_timeout_ns, a.status, true);
-        if (!ok) break;
-        // rank r-1's update of the owner chunk is complete: the ascending
-        // order; in the arrival order only rank 0's store must land before
-        // the reductions, which then go out back to back (each element
-        // reduction is an atomic of its own, so none is lost)
-        if (r <= 1 || !a.arrival_order) bulk_wait_all();
-        if (r == 0) bulk_store(owner, x(b), n);
-        else bulk_reduce<DT, OP>(owner, x(b), n);
-        bulk_commit();
-        b ^= 1;
       }
       if (!ok) break;
-      bulk_wait_all();  // the owner chunk holds the final result
       if (COLL == kAllReduce && P > 1) {
-        // shard-out: the final chunk is loaded once and stored to every rank
-        issue(0, owner, n);
-        ok = wait_buf(0);
-        if (!ok) break;
-        for (int d = 0; d < P; ++d)
-          if (d != owner_rank)
-            bulk_store(static_cast<char*>(a.p.dst[d]) + w.dst_off + off, x(0), n);
-        bulk_commit();
+        // shard-out: each slot's final chunk is loaded once and stored to
+        // every other rank; no group is committed in the first loop, so slot
+        // j's last reduction has the K - 1 - j later slots' groups after it
+        for (int j = 0; j < nvalid; ++j) {
+          bulk_wait_all_dyn(K - 1 - j);
+          issue(j, 0, static_cast<const char*>(a.p.dst[owner_rank[j]]) + dst_off[j], nbytes[j]);
+        }
+        for (int j = 0; j < nvalid && ok; ++j) {
+          ok = wait_buf(j, 0);
+          if (!ok) break;
+          for (int d = 0; d < P; ++d)
+            if (d != owner_rank[j])
+              bulk_store(static_cast<char*>(a.p.dst[d]) + dst_off[j], buf(j, 0), nbytes[j]);
+          bulk_commit();
+        }
       }
     }
     bulk_wait_all();
     // after an abort, let any load still in flight land before the CTA exits
-    for (int b = 0; b < 2; ++b)
-      if (pending & (1u << b))
-        wait_bounded(&bar[b], (phase >> b) & 1, abort_flag, a.timeout_ns, a.status, false);
+    for (int bit = 0; bit < K * NB; ++bit)
+      if (pending & (1u << bit))
+        wait_bounded(&bars[first_bar + bit], (phase >> bit) & 1, abort_flag, a.timeout_ns,
+                     a.status, false);
   }
   __syncthreads();
   if (!*abort_flag) bulk_scalar_windows<COLL, DT, OP>(a, threadIdx.x, blockDim.x);

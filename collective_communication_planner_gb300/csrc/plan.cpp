@@ -163,6 +163,7 @@ Config resolve_config(const Config& in) {
   if (c.reduce_order != 1) c.reduce_order = 0;
   if (c.ce_fold < kFoldAuto || c.ce_fold > kFoldTma) c.ce_fold = kFoldAuto;
   if (c.ce_tail_percent <= 0 || c.ce_tail_percent > 100) c.ce_tail_percent = 100;
+  if (c.reduce_slots < 0 || c.reduce_slots > kMaxReduceSlots) c.reduce_slots = 0;
   return c;
 }
 
@@ -458,19 +459,36 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
       *why = "an all-gather has nothing for the TMA-reduce engine to reduce";
       return false;
     }
-    const uint64_t chunk = 8192;
-    const int lanes = std::min<int>(cfg.consumer_warps, (smem_budget - 1024) / (int)(2 * chunk));
+    // each issuing thread (lane 0 of a warp) keeps `slots` chunks in flight,
+    // each double-buffered over the ranks; a reduce-scatter's slots get a
+    // third buffer for an in-place owner's own chunk
+    const int bufs = plan.coll == kReduceScatter ? 3 : 2;
+    int slots = cfg.reduce_slots > 0 ? cfg.reduce_slots : kDefaultReduceSlots;
+    uint64_t chunk = cfg.max_chunk_bytes == kDefaultMaxChunkBytes ? kDefaultReduceChunkBytes
+                                                                   : (uint64_t)cfg.max_chunk_bytes;
+    int lanes = 0;
+    for (;;) {
+      const int64_t room = (int64_t)smem_budget - 1024;
+      lanes = (int)std::min<int64_t>(cfg.consumer_warps, room / (int64_t)(slots * bufs * chunk));
+      lanes = std::min(lanes, kReduceMaxBarriers / (slots * bufs));
+      if (lanes >= 1) break;
+      if (slots > 1) slots /= 2;
+      else if (chunk > 1024) chunk = (chunk / 2) & ~(uint64_t)15;
+      else break;
+    }
     if (lanes < 1) {
       *why = "shared memory too small for the TMA-reduce engine";
       return false;
     }
     sh.chunk_bytes = (int)chunk;
-    sh.stages = 2;
+    sh.stages = slots;
+    sh.reduce_slots = slots;
+    sh.reduce_bufs = bufs;
     sh.consumer_warps = lanes;
     sh.threads = 32 * lanes;
     sh.store_mode = kStoreBulk;
-    sh.smem = 1024 + (size_t)lanes * 2 * chunk;
-    build_chunk_tables(wins, chunk, lanes, max_ctas_total, cta_cap, cfg, es, capped, out);
+    sh.smem = 1024 + (size_t)lanes * slots * bufs * chunk;
+    build_chunk_tables(wins, chunk, lanes * slots, max_ctas_total, cta_cap, cfg, es, capped, out);
     sh.order = kOrderCyclic;  // every (grid x lanes)-th chunk per lane
     return true;
   }

@@ -86,6 +86,7 @@ struct Config {
   int reduce_order = 0;  // 0 ascending, 1 arrival (TMA-reduce engine only)
   int ce_fold = 0;       // copy-out allreduce shard-in: kFoldAuto / kFoldRegister / kFoldTma
   int ce_tail_percent = 0;  // copy-out allreduce: last segment's length, % of the others (0: 100)
+  int reduce_slots = 0;     // TMA-reduce engine: chunks each issuing thread keeps in flight (0: default)
 };
 
 // The copy-out allreduce's shard-in kernel. Auto and Register: the
@@ -109,6 +110,10 @@ constexpr size_t kDefaultMaxChunkBytes = 16384;
 constexpr uint64_t kArInflightBytes = 96 * 1024;
 constexpr uint64_t kArMinChunkBytes = 6144;
 constexpr uint64_t kArInflightMinTraffic = (uint64_t)512 << 20;
+// TMA-reduce engine defaults (max_chunk_bytes left at its default selects
+// kDefaultReduceChunkBytes)
+constexpr int kDefaultReduceSlots = 4;
+constexpr uint64_t kDefaultReduceChunkBytes = 4096;
 inline bool default_bulk_shape(const Config& c) {
   return c.stage_bytes == kDefaultStageBytes && c.stages == kDefaultStages &&
          c.max_chunk_bytes == kDefaultMaxChunkBytes;

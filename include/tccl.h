@@ -129,8 +129,8 @@ typedef enum {
  * TCCL_STORE_MODE, TCCL_CONSUMER_WARPS, TCCL_CTAS_PER_SM,
  * TCCL_WAIT_TIMEOUT_MS, TCCL_CHUNK_ORDER, TCCL_PREFETCH_CHUNKS,
  * TCCL_LOAD_POLICY, TCCL_MAX_CHUNK_BYTES, TCCL_STAGE_LAYOUT, TCCL_CE_STREAMS,
- * TCCL_CE_SEGMENT_BYTES, TCCL_CE_AUTO_MAX_CAP, TCCL_REDUCE_ORDER, TCCL_CE_FOLD and
- * TCCL_CE_TAIL_PERCENT once). Zero in a field
+ * TCCL_CE_SEGMENT_BYTES, TCCL_CE_AUTO_MAX_CAP, TCCL_REDUCE_ORDER, TCCL_CE_FOLD,
+ * TCCL_CE_TAIL_PERCENT and TCCL_REDUCE_SLOTS once). Zero in a field
  * means "library default".
  *
  * Bulk-engine shape: stage_bytes, stages and max_chunk_bytes default to 64 KiB,
@@ -175,6 +175,9 @@ typedef struct {
                               of segments stays the same and the others grow to cover the rest
                               (past ce_segment_bytes if need be): the last segment's copies
                               overlap no fold, so a shorter last segment shortens the tail */
+  int reduce_slots;        /* TMA-reduce engine: chunks each issuing thread keeps in flight,
+                              1..8 (0: default 4); its chunk size is max_chunk_bytes when that
+                              is set, else 4 KiB */
 } tcclConfig_t;
 
 /* What the last launch on a group looked like. */

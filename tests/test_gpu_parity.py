@@ -283,6 +283,56 @@ def test_tma_reduce_arrival_order(groups, dtype, op):
     reset_config(g)
 
 
+@pytest.mark.parametrize("dtype,op", TMA_REDUCE_PAIRS)
+@pytest.mark.parametrize("p", [2, 3, 8])
+def test_tma_reduce_in_place_reduce_scatter(groups, dtype, op, p):
+    """In place, shard s's owner chunk is rank s's own input chunk, which rank
+    0's first store would overwrite: the engine loads it first and keeps it."""
+    g = groups(p)
+    for slots, cap in ((0, 0), (1, 5), (8, 0)):
+        reset_config(g, engine=tccl.tcclEngineTmaReduce, reduce_slots=slots)
+        rc = 50_021
+        xs = inputs(dtype, p, p * rc)
+        bufs = [to_device(x) for x in xs]
+        parts = [b[r * rc:(r + 1) * rc] for r, b in enumerate(bufs)]
+        g.reduce_scatter(bufs, parts, op=op, cta_cap=cap)
+        torch.cuda.synchronize()
+        assert g.query_error() == tccl.tcclSuccess
+        assert g.last_launch()["engine"] == tccl.tcclEngineTmaReduce
+        assert_ranks_equal([to_host(t) for t in parts], oracle.reduce_scatter(xs, dtype, op, nthreads=0),
+                           f"TMA-reduce in-place RS {dtype} {op} P={p} slots={slots} cap={cap}")
+    reset_config(g)
+
+
+@pytest.mark.parametrize("slots,chunk", [(1, 8192), (2, 4096), (4, 0), (8, 2048), (3, 32768)])
+@pytest.mark.parametrize("order", [tccl.tcclReduceAscending, tccl.tcclReduceArrival])
+def test_tma_reduce_slot_shapes(groups, slots, chunk, order):
+    """Every (slots, chunk) shape of the TMA-reduce engine, allreduce and
+    reduce-scatter, P = 8, with ragged chunk counts per lane, bit-exact in the
+    ascending order (int32 sums in the arrival order too)."""
+    p, n = 8, 700_003
+    g = groups(p)
+    reset_config(g, engine=tccl.tcclEngineTmaReduce, reduce_slots=slots, max_chunk_bytes=chunk,
+                 reduce_order=order)
+    dtype = "f32" if order == tccl.tcclReduceAscending else "i32"
+    xs = inputs(dtype, p, n)
+    got = run_allreduce(g, xs, dtype, "sum", cap=11)
+    info = g.last_launch()
+    assert info["engine"] == tccl.tcclEngineTmaReduce and (slots == 0 or info["stages"] == slots)
+    assert_ranks_equal(got, oracle.allreduce(xs, dtype, "sum", nthreads=0),
+                       f"TMA-reduce AR slots={slots} chunk={chunk} order={order}")
+    rc = 90_001
+    xs = inputs(dtype, p, p * rc)
+    sends = [to_device(x) for x in xs]
+    parts = [torch.empty(rc, dtype=TORCH_OF[dtype], device="cuda") for _ in range(p)]
+    g.reduce_scatter(sends, parts)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    assert_ranks_equal([to_host(t) for t in parts], oracle.reduce_scatter(xs, dtype, "sum", nthreads=0),
+                       f"TMA-reduce RS slots={slots} chunk={chunk} order={order}")
+    reset_config(g)
+
+
 def test_arrival_order_leaves_other_engines_ascending(groups):
     """The order setting only changes the TMA-reduce engine: the bulk engine's
     fp32 sums stay bit-exact with it set."""

@@ -325,10 +325,56 @@ def test_tma_reduce_engine_shape(coll, p):
                                engine=tccl.tcclEngineTmaReduce)
     assert r == 0 and info.engine == tccl.tcclEngineTmaReduce
     lanes = info.threads // 32
-    assert info.chunk_bytes == 8192 and info.stages == 2
-    assert info.smem_bytes == 1024 + lanes * 2 * 8192 <= 232448
-    assert info.ctas <= -(-info.total_chunks // lanes)
+    # default shape: 4 KiB chunks, 4 slots per issuing thread, two buffers per
+    # slot (three for a reduce-scatter), within the shared memory and the
+    # head's 120 barriers
+    bufs_per_slot = 3 if coll == RS else 2
+    assert info.chunk_bytes == 4096 and info.stages == 4
+    assert info.smem_bytes == 1024 + lanes * 4 * bufs_per_slot * 4096 <= 232448
+    assert lanes * 4 * bufs_per_slot <= 120
+    assert info.ctas <= -(-info.total_chunks // (lanes * 4))
     check_cover(coll, p, 1_000_003, 4, send, recv, wins, info)
+
+
+@pytest.mark.parametrize("slots,chunk", [(1, 8192), (2, 8192), (8, 2048), (4, 12288)])
+def test_tma_reduce_engine_shape_knobs(slots, chunk):
+    """reduce_slots and max_chunk_bytes set the TMA-reduce shape; the lanes
+    fill what the shared memory and the barrier head allow."""
+    p = 8
+    send, recv = bufs(p, 0, 0)
+    c = cfg(tccl.tcclEngineTmaReduce)
+    c.reduce_slots = slots
+    c.max_chunk_bytes = chunk
+    r, wins, _, info = tccl.tcclPlanInspect(AR, p, send, recv, 3_000_001, tccl.tcclFloat32, 0, 152,
+                                            232448, c)
+    assert r == 0 and info.stages == slots and info.chunk_bytes == chunk
+    lanes = info.threads // 32
+    assert 1 <= lanes <= 16 and lanes * slots * 2 <= 120
+    assert info.smem_bytes == 1024 + lanes * slots * 2 * chunk <= 232448
+
+
+@pytest.mark.parametrize("slots", [1, 2, 4, 8])
+def test_tma_reduce_slot_walk_covers_every_chunk(slots):
+    """The TMA-reduce kernel's chunk walk: lane w of CTA b starts at
+    b * lanes + w, takes `slots` chunks `step = grid * lanes` apart, then
+    moves on by step * slots. Every chunk is taken exactly once."""
+    for total in (1, 5, 100, 1000, 4097):
+        for grid in (1, 3, 152):
+            for lanes in (1, 7, 16):
+                seen = set()
+                step = grid * lanes
+                for b in range(grid):
+                    for w in range(lanes):
+                        base = b * lanes + w
+                        while base < total:
+                            for j in range(slots):
+                                c = base + j * step
+                                if c >= total:
+                                    break
+                                assert c not in seen
+                                seen.add(c)
+                            base += step * slots
+                assert seen == set(range(total)), (total, grid, lanes, slots)
 
 
 def test_tma_reduce_engine_rejects_allgather():
