@@ -1156,11 +1156,16 @@ def tma_reduce_bench(args):
         idx = np.sort(np.random.default_rng(9).choice(n, size=4096, replace=False))
         exp = oracle.allreduce([x[idx].copy() for x in xs], "f32", "sum")[0]
         g = tccl.Group(p)
+        shapes = [tuple(int(v) for v in sh.split(":")) for sh in args.tma_reduce_shapes.split(",")] \
+            if args.tma_reduce_shapes else [(0, 0)]
+        runs = [(tccl.tcclEngineBulk, 0, 0, 0)]
+        for slots, chunk in shapes:
+            runs += [(tccl.tcclEngineTmaReduce, 0, slots, chunk), (tccl.tcclEngineTmaReduce, 1, slots, chunk)]
         for cap in [int(c) for c in args.tma_reduce_caps.split(",")]:
-            for engine, order in ((tccl.tcclEngineBulk, 0), (tccl.tcclEngineTmaReduce, 0),
-                                  (tccl.tcclEngineTmaReduce, 1)):
+            for engine, order, slots, chunk in runs:
                 c = tccl.tcclConfig_t()
                 c.engine, c.reduce_order = engine, order
+                c.reduce_slots, c.max_chunk_bytes = slots, chunk
                 assert tccl.tcclGroupSetConfig(g.handle, c) == 0
                 for t in recvs:
                     t.fill_(0)
@@ -1318,6 +1323,8 @@ def main():
                     help="TMA-reduce engine vs the bulk engine, fp32 sum, 64 MiB per rank")
     ap.add_argument("--tma-reduce-ranks", default="4,8")
     ap.add_argument("--tma-reduce-caps", default="0,32,16")
+    ap.add_argument("--tma-reduce-shapes", default="",
+                    help="TMA-reduce shapes slots:chunk_bytes, comma separated (default: the library's)")
     ap.add_argument("--gemm-n", type=int, default=8192)
     ap.add_argument("--overlap-engine", type=int, default=0,
                     help="engine for the overlap study (0 auto, 1 bulk, 4 TMA-reduce)")
