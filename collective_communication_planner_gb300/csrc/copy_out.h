@@ -27,6 +27,7 @@ struct AnchorArgs {
   int njobs;
   int nranks;
   int prefetch_first;  // set by the launcher for early launches: warm L2 before the wait
+  int mixed_bf16;      // bf16 sums: fold with the mixed-precision add (same bits, fewer instructions)
 };
 
 // Vectors each thread folds at a time: two for P = 2 and 4, one otherwise.

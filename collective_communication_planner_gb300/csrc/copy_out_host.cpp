@@ -6,7 +6,9 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <string>
 #include <vector>
 
 #include "copy_out.h"
@@ -27,6 +29,16 @@ std::vector<uint8_t> mod16_of(int n, const void* const* p) {
 }
 
 namespace {
+
+// bf16 sums in the register-load fold: the mixed-precision add unless
+// TCCL_BF16_FOLD=packed asks for the packed fp32 adds (the same bits).
+int mixed_bf16_fold() {
+  static const int v = [] {
+    const char* e = std::getenv("TCCL_BF16_FOLD");
+    return (e && std::string(e) == "packed") ? 0 : 1;
+  }();
+  return v;
+}
 
 // The group's copy streams, the per-segment events and the join events,
 // created on first use (so a group that never uses the engine holds none).
@@ -122,6 +134,7 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
   std::memset(&aa, 0, sizeof(aa));
   aa.nranks = P;
   aa.njobs = 1;
+  aa.mixed_bf16 = mixed_bf16_fold();
   const int used = std::min(g->cfg.ce_streams, P - 1);
   int err = 0, copies = 0;
   for (int sgi = 0; sgi < nseg && !err; ++sgi) {
@@ -197,6 +210,7 @@ tcclResult_t run_copy_out_reduce_scatter(tcclGroup* g, const void* const* send, 
   aa.sm_mask = sm_record_slot(g);
   aa.nranks = P;
   aa.njobs = P;
+  aa.mixed_bf16 = mixed_bf16_fold();
   aa.job_src_stride = bytes;
   aa.head_bytes = std::min(bytes, (size_t)((16 - mod) & 15));
   aa.nvec = (bytes - aa.head_bytes) / 16;

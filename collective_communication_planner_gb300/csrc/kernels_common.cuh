@@ -401,6 +401,45 @@ struct PackedSumBF16 {
   }
 };
 
+// bf16 sums with the mixed-precision add of sm_100 and later: add.rn.f32.bf16
+// widens one bf16 half of a register (exactly) and adds it to an fp32
+// accumulator with one round to nearest, the same bits as widening first and
+// then adding; one instruction per element instead of a widening step per
+// element plus half a packed add. The first rank is widened exactly (an add
+// to zero would turn -0 into +0).
+__device__ __forceinline__ float add_bf16_lo(uint32_t w, float c) {
+  float d;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, l, %2;\n\t}"
+      : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float add_bf16_hi(uint32_t w, float c) {
+  float d;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, h, %2;\n\t}"
+      : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
+
+struct MixedSumBF16 {
+  float a[8];
+  __device__ __forceinline__ void init(uint4 u) {
+    a[0] = bf16_lo(u.x); a[1] = bf16_hi(u.x);
+    a[2] = bf16_lo(u.y); a[3] = bf16_hi(u.y);
+    a[4] = bf16_lo(u.z); a[5] = bf16_hi(u.z);
+    a[6] = bf16_lo(u.w); a[7] = bf16_hi(u.w);
+  }
+  __device__ __forceinline__ void add(uint4 u) {
+    a[0] = add_bf16_lo(u.x, a[0]); a[1] = add_bf16_hi(u.x, a[1]);
+    a[2] = add_bf16_lo(u.y, a[2]); a[3] = add_bf16_hi(u.y, a[3]);
+    a[4] = add_bf16_lo(u.z, a[4]); a[5] = add_bf16_hi(u.z, a[5]);
+    a[6] = add_bf16_lo(u.w, a[6]); a[7] = add_bf16_hi(u.w, a[7]);
+  }
+  __device__ __forceinline__ uint4 out() const {
+    return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                      pack_bf16x2(a[6], a[7]));
+  }
+};
+
 // The fold the streaming kernels use: packed sums where they exist.
 template <int DT, int OP>
 struct StreamFold {

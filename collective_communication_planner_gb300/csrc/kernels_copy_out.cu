@@ -61,7 +61,18 @@ __device__ __forceinline__ void st_keep_v4(void* p, uint4 v, uint64_t policy) {
 // (NP = 2, 4, 8) every load of a step is issued before the first add;
 // otherwise the ranks go in batches of 8 / U. Either way each accumulator receives the ranks in
 // ascending order: the plain left fold over all P ranks.
-template <int DT, int OP, int NP, int U>
+// The fold of one vector: the streaming fold, or for bf16 sums with MIXED
+// the mixed-precision adds (the same bits, fewer instructions).
+template <int DT, int OP, bool MIXED>
+struct AnchorFold {
+  using type = typename StreamFold<DT, OP>::type;
+};
+template <>
+struct AnchorFold<kBF16, kSum, true> {
+  using type = MixedSumBF16;
+};
+
+template <int DT, int OP, int NP, int U, bool MIXED>
 __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const __grid_constant__ AnchorArgs a) {
   constexpr int RB = NP > 0 ? NP : 8 / U;
   constexpr int es = DT == kBF16 ? 2 : 4;
@@ -97,7 +108,7 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
     const uint64_t src_off = static_cast<uint64_t>(job) * a.job_src_stride + a.head_bytes;
     char* dst = static_cast<char*>(a.p.dst[job]) + a.head_bytes;
     for (uint32_t base = gtid; base < nvec; base += nthr * U) {
-      typename StreamFold<DT, OP>::type acc[U];
+      typename AnchorFold<DT, OP, MIXED>::type acc[U];
       for (int r0 = 0; r0 < P; r0 += RB) {
         uint4 x[U][RB];
 #pragma unroll
@@ -163,12 +174,21 @@ int launch_anchor_t(const AnchorArgs& args, int grid, bool early, cudaStream_t s
   s.threads = kAnchorThreads;
   s.smem = 0;
   s.early_launch = early ? 1 : 0;
+  constexpr bool kCanMix = D == kBF16 && O == kSum;
+  if (kCanMix && a.mixed_bf16) {
+    switch (a.nranks) {
+      case 2: return launch_maybe_early(anchor_reduce_kernel<D, O, 2, 2, kCanMix>, a, s, st);
+      case 4: return launch_maybe_early(anchor_reduce_kernel<D, O, 4, 2, kCanMix>, a, s, st);
+      case 8: return launch_maybe_early(anchor_reduce_kernel<D, O, 8, 1, kCanMix>, a, s, st);
+      default: return launch_maybe_early(anchor_reduce_kernel<D, O, 0, 1, kCanMix>, a, s, st);
+    }
+  }
   switch (a.nranks) {
-    case 2: return launch_maybe_early(anchor_reduce_kernel<D, O, 2, 2>, a, s, st);
-    case 4: return launch_maybe_early(anchor_reduce_kernel<D, O, 4, 2>, a, s, st);
-    case 8: return launch_maybe_early(anchor_reduce_kernel<D, O, 8, 1>, a, s, st);
+    case 2: return launch_maybe_early(anchor_reduce_kernel<D, O, 2, 2, false>, a, s, st);
+    case 4: return launch_maybe_early(anchor_reduce_kernel<D, O, 4, 2, false>, a, s, st);
+    case 8: return launch_maybe_early(anchor_reduce_kernel<D, O, 8, 1, false>, a, s, st);
     default:  // other rank counts: one vector per thread (two would spill)
-      return launch_maybe_early(anchor_reduce_kernel<D, O, 0, 1>, a, s, st);
+      return launch_maybe_early(anchor_reduce_kernel<D, O, 0, 1, false>, a, s, st);
   }
 }
 

@@ -113,7 +113,7 @@ constexpr uint64_t kArInflightMinTraffic = (uint64_t)512 << 20;
 // TMA-reduce engine defaults (max_chunk_bytes left at its default selects
 // kDefaultReduceChunkBytes)
 constexpr int kDefaultReduceSlots = 4;
-constexpr uint64_t kDefaultReduceChunkBytes = 4096;
+constexpr uint64_t kDefaultReduceChunkBytes = 8192;
 inline bool default_bulk_shape(const Config& c) {
   return c.stage_bytes == kDefaultStageBytes && c.stages == kDefaultStages &&
          c.max_chunk_bytes == kDefaultMaxChunkBytes;

@@ -177,7 +177,7 @@ typedef struct {
                               overlap no fold, so a shorter last segment shortens the tail */
   int reduce_slots;        /* TMA-reduce engine: chunks each issuing thread keeps in flight,
                               1..8 (0: default 4); its chunk size is max_chunk_bytes when that
-                              is set, else 4 KiB */
+                              is set, else 8 KiB */
 } tcclConfig_t;
 
 /* What the last launch on a group looked like. */

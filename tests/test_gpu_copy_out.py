@@ -459,3 +459,27 @@ def test_tma_fold_when_asked(groups, layout, warps, dtype, op, p):
     assert info["engine"] == CE and info["threads"] != 1024 and info["ctas"] <= 5, info
     assert info["stage_layout"] == (2 if layout == 2 else 1), info
     check(got, oracle.allreduce(xs, dtype, op, nthreads=0), f"TMA fold layout {layout} P={p}")
+
+
+SPECIAL_BF16 = np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x807F, 0x0080, 0x8080,
+                         0x0040, 0x8040, 0x3F80, 0xBF80, 0x3F81, 0x4000, 0xC000, 0x0100],
+                        dtype=np.uint16)
+
+
+@pytest.mark.parametrize("p", [2, 3, 4, 8])
+def test_register_fold_bf16_special_values(groups, p):
+    """bf16 sums on the register fold with subnormals, signed zeros and
+    values that cancel exactly planted among normal data: every output element
+    equals the oracle's (fp32 accumulation without flushing, one rounding)."""
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=256 * 1024)
+    n = 300_007
+    xs = datagen.rank_buffers("normal_bf16", 34, p, n)
+    rng = np.random.default_rng(34)
+    for r in range(p):
+        pick = rng.random(n) < 0.5
+        xs[r] = xs[r].copy()
+        xs[r][pick] = SPECIAL_BF16[rng.integers(0, SPECIAL_BF16.size, int(pick.sum()))]
+    got = allreduce(g, xs, "bf16", "sum", cap=9)
+    assert g.last_launch()["threads"] == 1024  # the register fold
+    check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), f"special bf16 P={p}")

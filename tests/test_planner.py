@@ -325,12 +325,12 @@ def test_tma_reduce_engine_shape(coll, p):
                                engine=tccl.tcclEngineTmaReduce)
     assert r == 0 and info.engine == tccl.tcclEngineTmaReduce
     lanes = info.threads // 32
-    # default shape: 4 KiB chunks, 4 slots per issuing thread, two buffers per
+    # default shape: 8 KiB chunks, 4 slots per issuing thread, two buffers per
     # slot (three for a reduce-scatter), within the shared memory and the
     # head's 120 barriers
     bufs_per_slot = 3 if coll == RS else 2
-    assert info.chunk_bytes == 4096 and info.stages == 4
-    assert info.smem_bytes == 1024 + lanes * 4 * bufs_per_slot * 4096 <= 232448
+    assert info.chunk_bytes == 8192 and info.stages == 4
+    assert info.smem_bytes == 1024 + lanes * 4 * bufs_per_slot * 8192 <= 232448
     assert lanes * 4 * bufs_per_slot <= 120
     assert info.ctas <= -(-info.total_chunks // (lanes * 4))
     check_cover(coll, p, 1_000_003, 4, send, recv, wins, info)
