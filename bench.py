@@ -1247,6 +1247,13 @@ def copy_out_bench(args):
         "seg16_tail45": {"ce_segment_bytes": 16 << 20, "ce_tail_percent": 45},
         "streams1": {"ce_streams": 1},
         "streams2": {"ce_streams": 2},
+        # allreduce copy streams: (each segment but the last, the last)
+        "ar1_tail4": {"ce_ar_streams": 1, "ce_tail_streams": 4},
+        "ar2_tail2": {"ce_ar_streams": 2, "ce_tail_streams": 2},
+        "ar2_tail4": {"ce_ar_streams": 2, "ce_tail_streams": 4},
+        "ar3_tail3": {"ce_ar_streams": 3, "ce_tail_streams": 3},
+        "ar3_tail4": {"ce_ar_streams": 3, "ce_tail_streams": 4},
+        "ar2_tail6": {"ce_streams": 6, "ce_ar_streams": 2, "ce_tail_streams": 6},
     }
     chosen = args.copy_out_variants.split(",") if args.copy_out_variants else ["auto", "sm_only"]
     caps = [int(c) for c in args.copy_out_caps.split(",")]

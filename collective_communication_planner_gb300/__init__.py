@@ -47,7 +47,8 @@ class tcclConfig_t(ctypes.Structure):
                 ("stage_layout", ctypes.c_int), ("ce_streams", ctypes.c_int),
                 ("ce_segment_bytes", ctypes.c_size_t), ("ce_auto_max_cap", ctypes.c_int),
                 ("reduce_order", ctypes.c_int), ("ce_fold", ctypes.c_int),
-                ("ce_tail_percent", ctypes.c_int), ("reduce_slots", ctypes.c_int)]
+                ("ce_tail_percent", ctypes.c_int), ("reduce_slots", ctypes.c_int),
+                ("ce_ar_streams", ctypes.c_int), ("ce_tail_streams", ctypes.c_int)]
 
 
 class tcclLaunchInfo_t(ctypes.Structure):

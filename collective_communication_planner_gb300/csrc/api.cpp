@@ -129,6 +129,8 @@ Config config_from_env() {
   if (const char* e = std::getenv("TCCL_REDUCE_ORDER")) c.reduce_order = std::string(e) == "arrival" ? 1 : 0;
   c.ce_tail_percent = geti("TCCL_CE_TAIL_PERCENT", 0);
   c.reduce_slots = geti("TCCL_REDUCE_SLOTS", 0);
+  c.ce_ar_streams = geti("TCCL_CE_AR_STREAMS", 0);
+  c.ce_tail_streams = geti("TCCL_CE_TAIL_STREAMS", 0);
   if (const char* e = std::getenv("TCCL_CE_FOLD")) {
     std::string v(e);
     if (v == "register") c.ce_fold = kFoldRegister;
@@ -186,6 +188,8 @@ Config from_public(const tcclConfig_t& p) {
   c.ce_fold = p.ce_fold;
   c.ce_tail_percent = p.ce_tail_percent;
   c.reduce_slots = p.reduce_slots;
+  c.ce_ar_streams = p.ce_ar_streams;
+  c.ce_tail_streams = p.ce_tail_streams;
   return resolve_config(c);
 }
 
@@ -213,6 +217,8 @@ tcclConfig_t to_public(const Config& c) {
   p.ce_fold = c.ce_fold;
   p.ce_tail_percent = c.ce_tail_percent;
   p.reduce_slots = c.reduce_slots;
+  p.ce_ar_streams = c.ce_ar_streams;
+  p.ce_tail_streams = c.ce_tail_streams;
   return p;
 }
 
@@ -224,7 +230,8 @@ bool config_ok(const tcclConfig_t& p) {
          p.prefetch_chunks >= -1 && p.load_policy >= 0 && p.load_policy <= 2 &&
          p.stage_layout >= 0 && p.stage_layout <= 2 && p.reduce_order >= 0 && p.reduce_order <= 1 &&
          p.ce_fold >= 0 && p.ce_fold <= 2 && p.ce_tail_percent >= 0 && p.ce_tail_percent <= 100 &&
-         p.reduce_slots >= 0 && p.reduce_slots <= 8;
+         p.reduce_slots >= 0 && p.reduce_slots <= 8 && p.ce_ar_streams >= 0 && p.ce_ar_streams <= 8 &&
+         p.ce_tail_streams >= 0 && p.ce_tail_streams <= 8;
 }
 
 void dump_plan(const Plan& pl, const Lowered& low) {

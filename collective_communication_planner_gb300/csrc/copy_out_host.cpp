@@ -135,7 +135,11 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
   aa.nranks = P;
   aa.njobs = 1;
   aa.mixed_bf16 = mixed_bf16_fold();
-  const int used = std::min(g->cfg.ce_streams, P - 1);
+  // the copies of every segment but the last run beside the next segment's
+  // fold, the last segment's beside nothing: each has its own stream count
+  const int mid_streams = std::min(g->cfg.ce_ar_streams, P - 1);
+  const int tail_streams = std::min(g->cfg.ce_tail_streams, P - 1);
+  const int used = std::max(mid_streams, tail_streams);
   int err = 0, copies = 0;
   for (int sgi = 0; sgi < nseg && !err; ++sgi) {
     const size_t off = (size_t)sgi * seg;
@@ -160,13 +164,14 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
       err = launch_plan(g, cp, kAllReduce, dtype, op, s_ptr.data(), r_ptr.data(), es, stream);
     }
     if (err || used == 0) continue;
+    const int seg_streams = sgi == nseg - 1 ? tail_streams : mid_streams;
     err = cudaEventRecord(g->ce_seg_events[sgi], stream);
-    for (int j = 0; j < used && !err; ++j) err = cudaStreamWaitEvent(g->ce_streams[j], g->ce_seg_events[sgi], 0);
+    for (int j = 0; j < seg_streams && !err; ++j) err = cudaStreamWaitEvent(g->ce_streams[j], g->ce_seg_events[sgi], 0);
     int j = 0;
     for (int k = 0; k < P && !err; ++k) {
       if (k == anchor) continue;
       err = cudaMemcpyAsync(r_ptr[k], r_ptr[anchor], n * es, cudaMemcpyDeviceToDevice, g->ce_streams[j]);
-      j = (j + 1) % used;
+      j = (j + 1) % seg_streams;
       ++copies;
     }
   }

@@ -164,6 +164,10 @@ Config resolve_config(const Config& in) {
   if (c.ce_fold < kFoldAuto || c.ce_fold > kFoldTma) c.ce_fold = kFoldAuto;
   if (c.ce_tail_percent <= 0 || c.ce_tail_percent > 100) c.ce_tail_percent = 100;
   if (c.reduce_slots < 0 || c.reduce_slots > kMaxReduceSlots) c.reduce_slots = 0;
+  if (c.ce_ar_streams <= 0) c.ce_ar_streams = c.ce_streams;
+  if (c.ce_tail_streams <= 0) c.ce_tail_streams = c.ce_streams;
+  c.ce_ar_streams = std::min(c.ce_ar_streams, c.ce_streams);
+  c.ce_tail_streams = std::min(c.ce_tail_streams, c.ce_streams);
   return c;
 }
 

@@ -87,6 +87,8 @@ struct Config {
   int ce_fold = 0;       // copy-out allreduce shard-in: kFoldAuto / kFoldRegister / kFoldTma
   int ce_tail_percent = 0;  // copy-out allreduce: last segment's length, % of the others (0: 100)
   int reduce_slots = 0;     // TMA-reduce engine: chunks each issuing thread keeps in flight (0: default)
+  int ce_ar_streams = 0;    // copy-out allreduce: copy streams of each segment but the last
+  int ce_tail_streams = 0;  // copy-out allreduce: copy streams of the last segment
 };
 
 // The copy-out allreduce's shard-in kernel. Auto and Register: the

@@ -130,7 +130,7 @@ typedef enum {
  * TCCL_WAIT_TIMEOUT_MS, TCCL_CHUNK_ORDER, TCCL_PREFETCH_CHUNKS,
  * TCCL_LOAD_POLICY, TCCL_MAX_CHUNK_BYTES, TCCL_STAGE_LAYOUT, TCCL_CE_STREAMS,
  * TCCL_CE_SEGMENT_BYTES, TCCL_CE_AUTO_MAX_CAP, TCCL_REDUCE_ORDER, TCCL_CE_FOLD,
- * TCCL_CE_TAIL_PERCENT and TCCL_REDUCE_SLOTS once). Zero in a field
+ * TCCL_CE_TAIL_PERCENT, TCCL_REDUCE_SLOTS, TCCL_CE_AR_STREAMS and TCCL_CE_TAIL_STREAMS once). Zero in a field
  * means "library default".
  *
  * Bulk-engine shape: stage_bytes, stages and max_chunk_bytes default to 64 KiB,
@@ -178,6 +178,11 @@ typedef struct {
   int reduce_slots;        /* TMA-reduce engine: chunks each issuing thread keeps in flight,
                               1..8 (0: default 4); its chunk size is max_chunk_bytes when that
                               is set, else 8 KiB */
+  int ce_ar_streams;       /* copy-out allreduce: copy streams that carry each segment but the
+                              last (those copies run beside the next segment's fold); 0: ce_streams;
+                              at most ce_streams */
+  int ce_tail_streams;     /* copy-out allreduce: copy streams that carry the last segment (its
+                              copies run beside nothing); 0: ce_streams; at most ce_streams */
 } tcclConfig_t;
 
 /* What the last launch on a group looked like. */
