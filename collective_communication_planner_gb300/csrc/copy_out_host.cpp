@@ -137,9 +137,9 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
   aa.mixed_bf16 = mixed_bf16_fold();
   // the copies of every segment but the last run beside the next segment's
   // fold, the last segment's beside nothing: each has its own stream count
-  const int mid_streams = std::min(g->cfg.ce_ar_streams, P - 1);
-  const int tail_streams = std::min(g->cfg.ce_tail_streams, P - 1);
-  const int used = std::max(mid_streams, tail_streams);
+  int mid_streams = 0, tail_streams = 0;
+  copy_out_streams(g->cfg, P, cap, &mid_streams, &tail_streams);
+  const int used = P > 1 ? std::max(mid_streams, tail_streams) : 0;
   int err = 0, copies = 0;
   for (int sgi = 0; sgi < nseg && !err; ++sgi) {
     const size_t off = (size_t)sgi * seg;

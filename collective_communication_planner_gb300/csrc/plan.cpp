@@ -164,7 +164,7 @@ Config resolve_config(const Config& in) {
   if (c.ce_fold < kFoldAuto || c.ce_fold > kFoldTma) c.ce_fold = kFoldAuto;
   if (c.ce_tail_percent <= 0 || c.ce_tail_percent > 100) c.ce_tail_percent = 100;
   if (c.reduce_slots < 0 || c.reduce_slots > kMaxReduceSlots) c.reduce_slots = 0;
-  if (c.ce_ar_streams <= 0) c.ce_ar_streams = c.ce_streams;
+  if (c.ce_ar_streams < 0) c.ce_ar_streams = 0;  // 0: by the cap (copy_out_streams)
   if (c.ce_tail_streams <= 0) c.ce_tail_streams = c.ce_streams;
   c.ce_ar_streams = std::min(c.ce_ar_streams, c.ce_streams);
   c.ce_tail_streams = std::min(c.ce_tail_streams, c.ce_streams);
@@ -221,6 +221,21 @@ bool register_fold_ok(int coll, int nranks, const uint8_t* send_mod16, const uin
     return bytes % 16 == 0 && bytes / 16 < kFoldMaxVectors;
   }
   return seg_elems * (size_t)es / 16 < kFoldMaxVectors;
+}
+
+void copy_out_streams(const Config& c, int nranks, int cap, int* mid, int* tail) {
+  // the copies of a segment run beside the next segment's fold, whose length
+  // goes as 1 / cap: more copies at once slow that fold down (they share the
+  // memory system) more than they gain once the copies keep up with it.
+  // GB300, C4 (P = 8, bf16, 128 MiB per rank), share of the HBM peak, one
+  // stream for the overlapped segments against two / three / four: cap 8
+  // 0.306 / 0.303 / 0.303 / 0.298, cap 16 0.512 / 0.508 / 0.508 / 0.497;
+  // cap 32 two or three (0.729-0.733) against one (0.720) and four (0.722).
+  int m = c.ce_ar_streams;
+  if (m <= 0) m = cap > 0 ? std::max(1, (cap + 8) / 16) : c.ce_streams;
+  m = std::min(m, c.ce_streams);
+  *mid = std::max(1, std::min(m, nranks - 1));
+  *tail = std::max(1, std::min(c.ce_tail_streams, nranks - 1));
 }
 
 bool allreduce_register_fold(const Config& c, int nranks, const uint8_t* send_mod16,

@@ -87,7 +87,7 @@ struct Config {
   int ce_fold = 0;       // copy-out allreduce shard-in: kFoldAuto / kFoldRegister / kFoldTma
   int ce_tail_percent = 0;  // copy-out allreduce: last segment's length, % of the others (0: 100)
   int reduce_slots = 0;     // TMA-reduce engine: chunks each issuing thread keeps in flight (0: default)
-  int ce_ar_streams = 0;    // copy-out allreduce: copy streams of each segment but the last
+  int ce_ar_streams = 0;    // copy-out allreduce: copy streams of each segment but the last (0: by cap)
   int ce_tail_streams = 0;  // copy-out allreduce: copy streams of the last segment
 };
 
@@ -154,6 +154,12 @@ void copy_out_segments(const Config& c, size_t count, int es, size_t* seg_elems,
 // allreduce's segment length (ignored for reduce-scatter).
 bool register_fold_ok(int coll, int nranks, const uint8_t* send_mod16, const uint8_t* recv_mod16,
                       size_t count, int es, size_t seg_elems);
+
+// Copy streams of a copy-out allreduce: *mid for the segments whose copies
+// run beside the next segment's fold (ce_ar_streams, or by default about one
+// per 16 CTAs of the cap, at least 1), *tail for the last segment
+// (ce_tail_streams); both within ce_streams and P - 1.
+void copy_out_streams(const Config& c, int nranks, int cap, int* mid, int* tail);
 
 // Whether a copy-out allreduce's segments fold with the register-load kernel
 // (else the TMA pipeline): register_fold_ok, unless the config asks for the

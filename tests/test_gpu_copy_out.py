@@ -483,3 +483,18 @@ def test_register_fold_bf16_special_values(groups, p):
     got = allreduce(g, xs, "bf16", "sum", cap=9)
     assert g.last_launch()["threads"] == 1024  # the register fold
     check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), f"special bf16 P={p}")
+
+
+@pytest.mark.parametrize("mid,tail", [(0, 0), (1, 4), (2, 2), (3, 1), (4, 4)])
+@pytest.mark.parametrize("cap", [5, 16, 40])
+def test_copy_stream_splits(groups, mid, tail, cap):
+    """Any split of the copy streams between the overlapped segments and the
+    last one (0 = the default: by the cap, and ce_streams) gives the same bits."""
+    p = 8
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=128 * 1024, ce_ar_streams=mid, ce_tail_streams=tail)
+    xs = datagen.rank_buffers("normal_bf16", 35, p, 400_009)
+    got = allreduce(g, xs, "bf16", "sum", cap=cap)
+    info = g.last_launch()
+    assert info["engine"] == CE and info["ce_segments"] >= 4 and info["ce_copies"] == 7 * info["ce_segments"]
+    check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), f"streams {mid}/{tail} cap {cap}")
