@@ -1198,20 +1198,22 @@ def tma_reduce_bench(args):
 
 # ------------------------------------------------------------------ copy-out mode
 def copy_out_bench(args):
-    """The C4 allreduce (P=8, bf16, 128 MiB per rank) at CTA caps 8, 16 and
-    32 with the default engine choice (the copy-out engine) and with the
-    SM-only bulk engine: device time per call, HBM fraction of the 2*P*S
-    bytes, segments and copies per call. Results checked against the oracle
-    on sampled elements. A small, fixed number of launches, so the command
-    also serves for an ncu launch list."""
+    """An allreduce workload (default C4: P=8, bf16, 128 MiB per rank) at CTA
+    caps (default 8, 16 and 32) with the default engine choice (the copy-out
+    engine) and other variants (the SM-only bulk engine, the TMA-fed fold,
+    segment and copy-stream schedules): device time per call, HBM fraction of
+    the 2*P*S bytes, segments and copies per call. Results checked against the
+    oracle on sampled elements. A small, fixed number of launches, so the
+    command also serves for an ncu launch list."""
     import numpy as np
     import torch
     import collective_communication_planner_gb300 as tccl
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    w = WORKLOADS["c4"]
+    w = WORKLOADS[args.copy_out_workload]
     p, n = w["p"], w["count"]
+    es = 2 if w["dtype"] == "bf16" else 4
     xs = make_inputs(w)
     sends = [host_to_torch(x).to(dev) for x in xs]
     recvs = [torch.empty_like(t) for t in sends]
@@ -1219,7 +1221,7 @@ def copy_out_bench(args):
     st = stream.cuda_stream
     peak, _ = measured_peak()
     g = tccl.Group(p)
-    alg = 2 * p * n * 2
+    alg = 2 * p * n * es
 
     def set_cfg(**kw):
         c = tccl.tcclConfig_t()
@@ -1229,7 +1231,7 @@ def copy_out_bench(args):
 
     import oracle
     idx = np.sort(np.random.default_rng(5).choice(n, size=4096, replace=False))
-    exp = oracle.allreduce([x[idx].copy() for x in xs], "bf16", "sum")[0]
+    exp = oracle.allreduce([x[idx].copy() for x in xs], w["dtype"], w["op"])[0]
     variants = {
         "auto": {},
         "sm_only": {"ce_auto_max_cap": -1},
@@ -1254,6 +1256,8 @@ def copy_out_bench(args):
         "ar3_tail3": {"ce_ar_streams": 3, "ce_tail_streams": 3},
         "ar3_tail4": {"ce_ar_streams": 3, "ce_tail_streams": 4},
         "ar2_tail6": {"ce_streams": 6, "ce_ar_streams": 2, "ce_tail_streams": 6},
+        # the copy-out engine whatever the cap (Auto stops at ce_auto_max_cap)
+        "copy_out": {"engine": 5},
     }
     chosen = args.copy_out_variants.split(",") if args.copy_out_variants else ["auto", "sm_only"]
     caps = [int(c) for c in args.copy_out_caps.split(",")]
@@ -1261,8 +1265,8 @@ def copy_out_bench(args):
         for variant in chosen:
             kw = variants[variant]
             set_cfg(**kw)
-            call = lambda: tccl.tcclAllReduce(g.handle, sends, recvs, n, tccl.DTYPES["bf16"],
-                                              tccl.tcclSum, st, cap)
+            call = lambda: tccl.tcclAllReduce(g.handle, sends, recvs, n, tccl.DTYPES[w["dtype"]],
+                                              tccl.OPS[w["op"]], st, cap)
             for t in recvs:
                 t.fill_(0)
             for _ in range(3):
@@ -1276,7 +1280,7 @@ def copy_out_bench(args):
             e1.synchronize()
             ms = e0.elapsed_time(e1) / 10
             info = g.last_launch()
-            got = recvs[p - 1].view(torch.int16).cpu().numpy().view(np.uint16)[idx]
+            got = recvs[p - 1].view(torch.int16 if es == 2 else recvs[0].dtype).cpu().numpy()[idx].view(exp.dtype)
             print(json.dumps({"mode": "copy_out", "workload": w["name"], "cap": cap, "variant": variant,
                               "engine": info["engine"], "ctas": info["ctas"], "threads": info["threads"],
                               "stages": info["stages"], "chunk_bytes": info["chunk_bytes"],
@@ -1323,6 +1327,8 @@ def main():
                          "tma_per_rank_8w, tail30, tail45, tail60, seg16, seg16_tail45, streams1, "
                          "streams2 (default auto,sm_only)")
     ap.add_argument("--copy-out-caps", default="8,16,32", help="for --copy-out: CTA caps")
+    ap.add_argument("--copy-out-workload", choices=sorted(WORKLOADS), default="c4",
+                    help="for --copy-out: the allreduce workload")
     ap.add_argument("--host-cost", action="store_true",
                     help="per-call host cost of tcclAllReduce from a C++ driver (decode-sized messages)")
     ap.add_argument("--host-cost-batches", type=int, default=50)
