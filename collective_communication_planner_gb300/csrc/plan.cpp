@@ -171,6 +171,19 @@ Config resolve_config(const Config& in) {
   return c;
 }
 
+int copy_out_auto_max_cap(const Config& c, int sm_count, int nranks) {
+  if (c.ce_auto_max_cap > 0) return c.ce_auto_max_cap;
+  // allreduce / all-gather: where the copy-out engine stays ahead of the
+  // SM-only bulk engine grows with P (the copy engines take P - 1 of the P
+  // stores). GB300 allreduce, share of the HBM peak, copy-out / SM only:
+  // P = 8, 128 MiB per rank: cap 48 0.787 / 0.662, 56 0.821 / 0.756,
+  // 64 0.820 / 0.836; P = 4, 64 MiB: cap 48 0.669 / 0.639, 56 0.696 / 0.726.
+  // P = 2: ahead up to 48 (the engine's first sweep).
+  if (nranks <= 2) return sm_count * 5 / 16;
+  if (nranks <= 4) return sm_count / 3;
+  return sm_count * 3 / 8;
+}
+
 bool copy_out_chosen(const Config& c, int sm_count, int nranks, int coll, size_t count, int es,
                      int cap) {
   if (nranks < 2) return false;
@@ -183,9 +196,7 @@ bool copy_out_chosen(const Config& c, int sm_count, int nranks, int coll, size_t
   // the HBM peak at P = 4, 64 MiB; 0.982 vs 1.045 at P = 8)
   if (coll == kReduceScatter) return cap > 0 || nranks <= 4;
   if (cap <= 0) return false;
-  // allreduce / all-gather (P = 2, 4, 8): copy-out is ahead up to a cap of 48 of 152 SMs
-  const int max_cap = c.ce_auto_max_cap > 0 ? c.ce_auto_max_cap : sm_count * 5 / 16;
-  return cap <= max_cap;
+  return cap <= copy_out_auto_max_cap(c, sm_count, nranks);
 }
 
 void copy_out_segments(const Config& c, size_t count, int es, size_t* seg_elems, int* nseg) {

@@ -131,10 +131,15 @@ constexpr uint64_t kFoldMaxVectors = (uint64_t)1 << 28;  // per launch job, 32-b
 // is copy-out (P >= 2); under Auto, for calls of at least 4 MiB per rank
 // buffer (allreduce: the buffer; reduce-scatter: the send buffer; all-gather:
 // the receive buffer): allreduce / all-gather when 0 < cap <= ce_auto_max_cap
-// (default 5/16 of the SMs), reduce-scatter under any cap or uncapped with
+// (default by P, copy_out_auto_max_cap), reduce-scatter under any cap or uncapped with
 // P <= 4. ce_auto_max_cap < 0 turns Auto's choice off.
 bool copy_out_chosen(const Config& c, int sm_count, int nranks, int coll, size_t count, int es,
                      int cap);
+
+// The largest cap for which Auto picks the copy-out engine for an allreduce
+// or all-gather: ce_auto_max_cap when set, else 5/16 of the SMs for P <= 2,
+// 1/3 for P = 3 and 4, 3/8 for P >= 5 (47, 50 and 57 on 152 SMs).
+int copy_out_auto_max_cap(const Config& c, int sm_count, int nranks);
 
 // Segments of a copy-out allreduce of `count` elements: at most
 // ce_segment_bytes per rank, at least four where each stays >= 4 MiB, at most
