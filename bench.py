@@ -724,12 +724,13 @@ def sweep(args):
             S, hbm = p * n * es, (p + 1) * p * n * es   # S = per-rank recv bytes
         assert fn() == 0
         info = g.last_launch()
-        used = None
+        used = per_launch = None
         if sms:
             g.read_sm_record()
             g.record_sms(True)
             fn()
-            used = g.read_sm_record()
+            per, used = g.read_sm_record_launches()
+            per_launch = max(per) if per else 0
             g.record_sms(False)
         ms = ev_time(fn)
         row = dict(config=cfg, coll=coll, P=p, dtype=dtype, op=op, count=n,
@@ -740,7 +741,7 @@ def sweep(args):
                    hbm_GBps=round(hbm / (ms * 1e-3) / 1e9, 1),
                    hbm_fraction=round(hbm / (ms * 1e-3) / 1e9 / peak, 4),
                    l2_resident=hbm < 129e6, engine=info["engine"], ctas=info["ctas"],
-                   sms_used=used)
+                   sms_used=used, sms_per_launch_max=per_launch)
         if graph:
             row["graph_us"] = round(graph_time(fn) * 1e3, 3)
         if hbm < 3 * l2_bytes:
