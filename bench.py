@@ -1257,6 +1257,9 @@ def copy_out_bench(args):
         "ar3_tail3": {"ce_ar_streams": 3, "ce_tail_streams": 3},
         "ar3_tail4": {"ce_ar_streams": 3, "ce_tail_streams": 4},
         "ar2_tail6": {"ce_streams": 6, "ce_ar_streams": 2, "ce_tail_streams": 6},
+        "seg20": {"ce_segment_bytes": 20 << 20},
+        "seg24": {"ce_segment_bytes": 24 << 20},
+        "seg28": {"ce_segment_bytes": 28 << 20},
         # the copy-out engine whatever the cap (Auto stops at ce_auto_max_cap)
         "copy_out": {"engine": 5},
     }
