@@ -1260,6 +1260,8 @@ def copy_out_bench(args):
         "seg20": {"ce_segment_bytes": 20 << 20},
         "seg24": {"ce_segment_bytes": 24 << 20},
         "seg28": {"ce_segment_bytes": 28 << 20},
+        "seg26": {"ce_segment_bytes": 26 << 20},
+        "seg30": {"ce_segment_bytes": 30 << 20},
         # the copy-out engine whatever the cap (Auto stops at ce_auto_max_cap)
         "copy_out": {"engine": 5},
     }
