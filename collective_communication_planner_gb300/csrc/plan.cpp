@@ -155,10 +155,14 @@ Config resolve_config(const Config& in) {
   c.max_chunk_bytes = std::min<size_t>(std::max<size_t>(c.max_chunk_bytes, 256), 65536) & ~(size_t)15;
   // copy engines: four streams and pieces of 16 MiB or more sustained
   // ~4.8 TB/s of fan-out copies in a GB300 probe (one stream ~2.5, 2 MiB
-  // pieces ~1.1); segments up to 32 MiB per rank
+  // pieces ~1.1); segments up to 28 MiB per rank: a 128 MiB-per-rank
+  // allreduce (P = 8, bf16) then runs in five segments, the last of 16 MiB,
+  // whose copies (which overlap no fold) end sooner: 0.312 / 0.528 / 0.744 /
+  // 0.812 of the HBM peak at caps 8 / 16 / 32 / 47 against 0.310 / 0.519 /
+  // 0.736 / 0.789 in four of 32 MiB (26 and 30 MiB: at or below 28)
   if (c.ce_streams <= 0) c.ce_streams = 4;
   if (c.ce_streams > 8) c.ce_streams = 8;
-  if (c.ce_segment_bytes == 0) c.ce_segment_bytes = (size_t)32 << 20;
+  if (c.ce_segment_bytes == 0) c.ce_segment_bytes = (size_t)28 << 20;
   c.ce_segment_bytes = std::min<size_t>(std::max<size_t>(c.ce_segment_bytes, 4096), (size_t)1 << 30) & ~(size_t)255;
   if (c.reduce_order != 1) c.reduce_order = 0;
   if (c.ce_fold < kFoldAuto || c.ce_fold > kFoldTma) c.ce_fold = kFoldAuto;

@@ -160,7 +160,7 @@ typedef struct {
   int stage_layout;        /* bulk engine: tcclStageLayout_t */
   int ce_streams;          /* copy-out engine: internal copy streams, 1..8 (default 4) */
   size_t ce_segment_bytes; /* copy-out engine: most bytes per rank in one segment (default
-                              32 MiB; a call is cut into at least four segments of at least
+                              28 MiB; a call is cut into at least four segments of at least
                               4 MiB where it can be; rounded down to a multiple of 256) */
   int ce_auto_max_cap;     /* Auto picks the copy-out engine for caps up to this many CTAs
                               (0: by the rank count, 5/16 of the SMs for P <= 2, 1/3 for P = 3

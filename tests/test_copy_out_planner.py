@@ -92,7 +92,7 @@ def test_engine_setting_and_auto_limit():
 @pytest.mark.parametrize("seg_cfg", [0, 8 * MiB, 4096])
 def test_segments(dt, count_bytes, seg_cfg):
     """Segments cover the call, start at multiples of 256 bytes, are at most
-    ce_segment_bytes (32 MiB by default) unless that would need more than 64
+    ce_segment_bytes (28 MiB by default) unless that would need more than 64
     of them, and number at least four while each stays >= 4 MiB."""
     es = ES[dt]
     count = count_bytes // es
@@ -101,7 +101,7 @@ def test_segments(dt, count_bytes, seg_cfg):
     assert co == 1 and rf == 1
     assert (se * es) % 256 == 0 and se > 0
     assert ns == -(-count // se) and 1 <= ns <= 64
-    cap_bytes = seg_cfg or 32 * MiB
+    cap_bytes = seg_cfg or 28 * MiB
     if ns < 64:  # not grown to respect the 64-segment bound
         assert se * es == 256 or se * es <= min(cap_bytes, max(4 * MiB, -(-count_bytes // 4)))
     if cap_bytes >= 4 * MiB and count_bytes >= 16 * MiB:
