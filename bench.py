@@ -740,7 +740,8 @@ def sweep(args):
                    busbw=round(S / (ms * 1e-3) * (2 if coll == "AR" else 1) * (p - 1) / p / 1e9, 2),
                    hbm_GBps=round(hbm / (ms * 1e-3) / 1e9, 1),
                    hbm_fraction=round(hbm / (ms * 1e-3) / 1e9 / peak, 4),
-                   l2_resident=hbm < 129e6, engine=info["engine"], ctas=info["ctas"],
+                   # near or below L2: back-to-back calls hit L2 and read above the HBM peak
+                   l2_resident=hbm < 1.5 * l2_bytes, engine=info["engine"], ctas=info["ctas"],
                    sms_used=used, sms_per_launch_max=per_launch)
         if graph:
             row["graph_us"] = round(graph_time(fn) * 1e3, 3)
