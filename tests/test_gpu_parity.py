@@ -393,6 +393,33 @@ def test_cta_cap_results_and_sm_footprint(groups, cap):
     assert_ranks_equal(got, exp, f"cap {cap}")
 
 
+def test_sm_record_launch_by_launch(groups):
+    """The SM record keeps one bitmap per launch: 70 capped launches (caps 1
+    to 7 in turn) give 70 recorded launches, the first 64 reported one by
+    one, each within its own cap; later launches share the last bitmap; the
+    union covers them all. Reading clears the record."""
+    p, n = 4, 200_000
+    g = groups(p)
+    configure(g, "bulk")
+    xs = inputs("f32", p, n)
+    sends = [to_device(x) for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    g.read_sm_record()
+    g.record_sms(True)
+    caps = [1 + i % 7 for i in range(70)]
+    for cap in caps:
+        g.all_reduce(sends, recvs, cta_cap=cap)
+    per_launch, union = g.read_sm_record_launches()
+    g.record_sms(False)
+    assert len(per_launch) == 64
+    assert all(1 <= m <= cap for m, cap in zip(per_launch[:63], caps[:63])), per_launch
+    assert 1 <= per_launch[63] <= sum(caps[63:]) and max(per_launch) <= union <= sum(caps)
+    assert g.read_sm_record_launches() == ([], 0)
+    torch.cuda.synchronize()
+    assert_ranks_equal([to_host(t) for t in recvs], oracle.allreduce(xs, "f32", "sum", nthreads=0),
+                       "after 70 recorded launches")
+
+
 def test_one_rank_copy_and_count_zero(groups):
     g = groups(1)
     configure(g, tccl.tcclEngineAuto)
