@@ -53,6 +53,9 @@ WORKLOADS = {
     "c2": dict(name="C2: P=4 bf16 sum allreduce, out of place, 32 Mi elems (64 MiB)/rank, "
                     "N(0,1) seed 1", p=4, count=32 * 1024 * 1024, dtype="bf16", op="sum",
                kind="normal_bf16", seed=1, kw=dict(mu=0.0, sigma=1.0), in_place=False, cap=0),
+    "c3": dict(name="C3 at 64 MiB/rank: P=8 fp32 sum allreduce, in place, 16 Mi elems/rank, "
+                    "uniform[-1,1) seed 2", p=8, count=16 * 1024 * 1024, dtype="f32", op="sum",
+               kind="uniform_f32", seed=2, kw={}, in_place=True, cap=0),
     "c4": dict(name="C4: P=8 bf16 sum allreduce, 64 Mi elems (128 MiB)/rank, N(0,0.02) seed 3",
                p=8, count=64 * 1024 * 1024, dtype="bf16", op="sum", kind="normal_bf16", seed=3,
                kw=dict(mu=0.0, sigma=0.02), in_place=False, cap=0),
@@ -1265,6 +1268,11 @@ def copy_out_bench(args):
         "seg30": {"ce_segment_bytes": 30 << 20},
         # the copy-out engine whatever the cap (Auto stops at ce_auto_max_cap)
         "copy_out": {"engine": 5},
+        # segments bulk-reduced into the anchor by the TMA-reduce engine (the
+        # pairs it supports), Auto's cap rule / whatever the cap
+        "tma_reduce_fold": {"ce_fold": 3},
+        "copy_out_tma_reduce": {"engine": 5, "ce_fold": 3},
+        "tma_reduce": {"engine": 4},
     }
     chosen = args.copy_out_variants.split(",") if args.copy_out_variants else ["auto", "sm_only"]
     caps = [int(c) for c in args.copy_out_caps.split(",")]

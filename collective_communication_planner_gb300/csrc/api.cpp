@@ -229,7 +229,7 @@ bool config_ok(const tcclConfig_t& p) {
          p.wait_timeout_ms >= 0 && p.chunk_order >= 0 && p.chunk_order <= 3 &&
          p.prefetch_chunks >= -1 && p.load_policy >= 0 && p.load_policy <= 2 &&
          p.stage_layout >= 0 && p.stage_layout <= 2 && p.reduce_order >= 0 && p.reduce_order <= 1 &&
-         p.ce_fold >= 0 && p.ce_fold <= 2 && p.ce_tail_percent >= 0 && p.ce_tail_percent <= 100 &&
+         p.ce_fold >= 0 && p.ce_fold <= 3 && p.ce_tail_percent >= 0 && p.ce_tail_percent <= 100 &&
          p.reduce_slots >= 0 && p.reduce_slots <= 8 && p.ce_ar_streams >= 0 && p.ce_ar_streams <= 8 &&
          p.ce_tail_streams >= 0 && p.ce_tail_streams <= 8;
 }
@@ -286,8 +286,10 @@ void fill_info(const Lowered& low, tcclLaunchInfo_t* info) {
 }
 
 tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* const* recv,
-                      size_t count, int es, int cap, CachedPlan** out, int anchor) {
+                      size_t count, int es, int cap, CachedPlan** out, int anchor,
+                      int anchor_engine) {
   PlanKey key{coll, es, (uint64_t)count, cap > 0 ? cap : 0, std::string(), anchor};
+  key.anchor_engine = anchor >= 0 ? anchor_engine : 0;
   key.mod16.resize(2 * g->nranks);
   key.in_place = coll == kAllReduce;
   for (int r = 0; r < g->nranks; ++r) {
@@ -311,7 +313,7 @@ tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* con
     rm[r] = (uint8_t)key.mod16[g->nranks + r];
   }
   Config cfg = g->cfg;
-  if (anchor >= 0) cfg.engine = kEngineBulk;
+  if (anchor >= 0) cfg.engine = anchor_engine;
   if (!lower_plan(pl, sm.data(), rm.data(), cfg, g->dev, cap, &cp->low, &why)) {
     if (log_level()) std::fprintf(stderr, "[tccl] cannot lower: %s\n", why.c_str());
     return tcclInvalidUsage;
@@ -340,6 +342,7 @@ tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* con
   } else {
     build_small_args<kMaxRanks, kLargeWindows>(low, g->nranks, es, &cp->small_args);
   }
+  cp->anchor_only = anchor >= 0;
   *out = cp.get();
   g->plans.emplace(key, std::move(cp));
   return tcclSuccess;
@@ -371,6 +374,7 @@ int launch_plan(tcclGroup* g, CachedPlan* cp, int coll, int dtype, int op,
     a.load_evict_first = low.shape.load_evict_first;
     a.arrival_order = low.shape.engine == kEngineTmaReduce && g->cfg.reduce_order == 1 ? 1 : 0;
     a.reduce_slots = low.shape.reduce_slots;
+    a.anchor_only = cp->anchor_only ? 1 : 0;
     a.reduce_bufs = low.shape.reduce_bufs;
     a.status = g->d_status;
     a.sm_mask = mask;

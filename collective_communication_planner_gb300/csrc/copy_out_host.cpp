@@ -111,9 +111,16 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
     }
   };
   const uintptr_t mod = (uintptr_t)recv[anchor] & 15;
-  const bool fast = allreduce_register_fold(g->cfg, P, mod16_of(P, send).data(),
+  // ce_fold = 3: bulk reductions into the anchor, for the pairs the copy
+  // hardware reduces exactly; any other pair folds as under Auto
+  const bool tma_reduce = g->cfg.ce_fold == kFoldTmaReduce && tma_reduce_supported(dtype, op);
+  Config fold_cfg = g->cfg;
+  if (fold_cfg.ce_fold == kFoldTmaReduce && !tma_reduce) fold_cfg.ce_fold = kFoldAuto;
+  const bool fast = !tma_reduce &&
+                    allreduce_register_fold(fold_cfg, P, mod16_of(P, send).data(),
                                             mod16_of(P, (const void* const*)recv).data(), count,
                                             es, seg);
+  const int anchor_engine = tma_reduce ? kEngineTmaReduce : kEngineBulk;
   const size_t tail_n = count - (size_t)(nseg - 1) * seg;
   // TMA fallback: both plans (full segments, ragged tail) before any launch,
   // since a new plan's table upload is synchronous
@@ -121,10 +128,12 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
   CachedPlan* tail = nullptr;
   if (!fast) {
     at(0);
-    r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), nseg > 1 ? seg : tail_n, es, cap, &full, anchor);
+    r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), nseg > 1 ? seg : tail_n, es, cap, &full, anchor,
+                 anchor_engine);
     if (r == tcclSuccess && nseg > 1 && tail_n != seg) {
       at((size_t)(nseg - 1) * seg);
-      r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), tail_n, es, cap, &tail, anchor);
+      r = get_plan(g, kAllReduce, s_ptr.data(), r_ptr.data(), tail_n, es, cap, &tail, anchor,
+                   anchor_engine);
     }
     if (r != tcclSuccess) return r;
   }

@@ -23,9 +23,11 @@ struct PlanKey {
   int cap;
   std::string mod16;  // address mod 16 of every send then recv buffer
   int anchor = -1;    // >= 0: every window stores to this rank only (copy-out shard-in)
+  int anchor_engine = 0;  // the engine of such a plan (bulk or TMA-reduce)
   bool in_place = false;
   bool operator<(const PlanKey& o) const {
     if (anchor != o.anchor) return anchor < o.anchor;
+    if (anchor_engine != o.anchor_engine) return anchor_engine < o.anchor_engine;
     if (in_place != o.in_place) return o.in_place;
     if (coll != o.coll) return coll < o.coll;
     if (elem_size != o.elem_size) return elem_size < o.elem_size;
@@ -46,6 +48,7 @@ struct CachedPlan {
   unsigned long long* d_sched = nullptr;
   // small engines: the launch argument block without its pointers
   std::vector<unsigned char> small_args;
+  bool anchor_only = false;  // copy-out shard-in: the result goes to the anchor rank alone
   ~CachedPlan() {
     if (d_table) cudaFree(d_table);
   }
@@ -105,9 +108,12 @@ inline uint32_t* sm_record_slot(tcclGroup* g) {
 
 // The plan (cached) of one call: its lowering and, for the bulk engines, its
 // device tables. anchor >= 0: every window stores to that rank only (the
-// copy-out engine's TMA shard-in). A new plan's table upload is synchronous.
+// copy-out engine's shard-in, on the bulk engine's TMA pipeline or, with
+// anchor_engine = kEngineTmaReduce, on the TMA-reduce engine). A new plan's
+// table upload is synchronous.
 tcclResult_t get_plan(tcclGroup* g, int coll, const void* const* send, void* const* recv,
-                      size_t count, int es, int cap, CachedPlan** out, int anchor = -1);
+                      size_t count, int es, int cap, CachedPlan** out, int anchor = -1,
+                      int anchor_engine = kEngineBulk);
 // Launches one lowered plan on `stream`; returns a CUDA error code (0 on success).
 int launch_plan(tcclGroup* g, CachedPlan* cp, int coll, int dtype, int op,
                 const void* const* send, void* const* recv, int es, cudaStream_t stream);

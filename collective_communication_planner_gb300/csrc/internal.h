@@ -97,6 +97,7 @@ struct BulkArgs {
   int arrival_order;             // TMA-reduce engine: ranks 1..P-1 reduced as they arrive
   int reduce_slots;              // TMA-reduce engine: chunks each issuing thread keeps in flight
   int reduce_bufs;               // TMA-reduce engine: buffers per slot (2, or 3 for reduce-scatter)
+  int anchor_only;               // TMA-reduce engine: allreduce into the anchor only (no shard-out)
 };
 
 // Warp / vec (small-message) engines: the whole lowered plan rides in the

@@ -1076,7 +1076,7 @@ __global__ void __launch_bounds__(32 * kMaxConsumerWarps, 1)
         }
       }
       if (!ok) break;
-      if (COLL == kAllReduce && P > 1) {
+      if (COLL == kAllReduce && P > 1 && !a.anchor_only) {
         // shard-out: each slot's final chunk is loaded once and stored to
         // every other rank; no group is committed in the first loop, so slot
         // j's last reduction has the K - 1 - j later slots' groups after it

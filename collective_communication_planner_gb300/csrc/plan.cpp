@@ -165,7 +165,7 @@ Config resolve_config(const Config& in) {
   if (c.ce_segment_bytes == 0) c.ce_segment_bytes = (size_t)28 << 20;
   c.ce_segment_bytes = std::min<size_t>(std::max<size_t>(c.ce_segment_bytes, 4096), (size_t)1 << 30) & ~(size_t)255;
   if (c.reduce_order != 1) c.reduce_order = 0;
-  if (c.ce_fold < kFoldAuto || c.ce_fold > kFoldTma) c.ce_fold = kFoldAuto;
+  if (c.ce_fold < kFoldAuto || c.ce_fold > kFoldTmaReduce) c.ce_fold = kFoldAuto;
   if (c.ce_tail_percent <= 0 || c.ce_tail_percent > 100) c.ce_tail_percent = 100;
   if (c.reduce_slots < 0 || c.reduce_slots > kMaxReduceSlots) c.reduce_slots = 0;
   if (c.ce_ar_streams < 0) c.ce_ar_streams = 0;  // 0: by the cap (copy_out_streams)
@@ -255,7 +255,7 @@ void copy_out_streams(const Config& c, int nranks, int cap, int* mid, int* tail)
 
 bool allreduce_register_fold(const Config& c, int nranks, const uint8_t* send_mod16,
                              const uint8_t* recv_mod16, size_t count, int es, size_t seg_elems) {
-  if (c.ce_fold == kFoldTma) return false;
+  if (c.ce_fold == kFoldTma || c.ce_fold == kFoldTmaReduce) return false;
   return register_fold_ok(kAllReduce, nranks, send_mod16, recv_mod16, count, es, seg_elems);
 }
 

@@ -93,8 +93,10 @@ struct Config {
 
 // The copy-out allreduce's shard-in kernel. Auto and Register: the
 // register-load fold wherever the buffers allow it (register_fold_ok), else
-// the bulk engine's TMA pipeline; Tma: always the TMA pipeline.
-enum CeFold : int { kFoldAuto = 0, kFoldRegister = 1, kFoldTma = 2 };
+// the bulk engine's TMA pipeline; Tma: always the TMA pipeline; TmaReduce:
+// the TMA-reduce engine into the anchor (the copy hardware reduces, no thread
+// touches the data), for the (dtype, op) pairs it reduces exactly, else Auto.
+enum CeFold : int { kFoldAuto = 0, kFoldRegister = 1, kFoldTma = 2, kFoldTmaReduce = 3 };
 
 // Fills zero fields with the library defaults.
 Config resolve_config(const Config& in);

@@ -170,7 +170,11 @@ typedef struct {
                               0 or 1: the 128-bit register-load fold where every send buffer
                               shares its address mod 16 with the anchor's receive buffer, else the
                               bulk engine's TMA pipeline; 2: always the TMA pipeline (with the
-                              group's stage layout and shape) */
+                              group's stage layout and shape); 3: the TMA-reduce engine, rank 0
+                              bulk-stored and ranks 1..P-1 bulk-reduced into the anchor in order
+                              (no thread touches the data; with the copy engines' shard-out, no
+                              thread touches it anywhere), for the pairs that engine supports
+                              (fp32 sum, int32 sum/min/max, bf16 min/max), else as 0 */
   int ce_tail_percent;     /* copy-out allreduce: the last segment's length as a percentage of
                               the others (1..100; 0: default 100, equal segments). The number
                               of segments stays the same and the others grow to cover the rest

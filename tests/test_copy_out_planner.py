@@ -125,14 +125,15 @@ def test_register_fold_for_allreduce(send_mis, recv_mis, fold):
     assert co == 1 and rf == int(fold)
 
 
-@pytest.mark.parametrize("ce_fold,fold", [(0, True), (1, True), (2, False)])
+@pytest.mark.parametrize("ce_fold,fold", [(0, True), (1, True), (2, False), (3, False)])
 def test_fold_choice_follows_the_config(ce_fold, fold):
-    """ce_fold = 2 asks for the TMA pipeline even where the register fold
-    could run; 0 and 1 keep the register fold for co-aligned buffers."""
+    """ce_fold = 2 asks for the TMA pipeline and 3 for the TMA-reduce engine
+    even where the register fold could run; 0 and 1 keep the register fold
+    for co-aligned buffers."""
     co, rf, ns, se = inspect(AR, 8, 64 * MiB, cap=16, cfg=config(ce_fold=ce_fold))
     assert co == 1 and rf == int(fold)
     assert tccl.tcclCopyOutInspect(AR, 8, *bufs(8), 1 << 20, BF16, 16, SMS,
-                                   config(ce_fold=3))[0] == tccl.tcclInvalidArgument
+                                   config(ce_fold=4))[0] == tccl.tcclInvalidArgument
 
 
 @pytest.mark.parametrize("rc_bytes,send_mis,recv_mis,fold", [

@@ -498,3 +498,35 @@ def test_copy_stream_splits(groups, mid, tail, cap):
     info = g.last_launch()
     assert info["engine"] == CE and info["ce_segments"] >= 4 and info["ce_copies"] == 7 * info["ce_segments"]
     check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), f"streams {mid}/{tail} cap {cap}")
+
+
+TMA_REDUCE_PAIRS = [("f32", "sum"), ("i32", "sum"), ("i32", "min"), ("i32", "max"),
+                    ("bf16", "min"), ("bf16", "max")]
+
+
+@pytest.mark.parametrize("dtype,op", TMA_REDUCE_PAIRS)
+@pytest.mark.parametrize("p,cap,offs,in_place", [(2, 0, 0, False), (3, 7, 4, False), (8, 16, 0, False),
+                                                 (8, 0, 0, True), (8, 5, 8, False)])
+def test_tma_reduce_fold(groups, dtype, op, p, cap, offs, in_place):
+    """ce_fold = 3: each segment is bulk-reduced into the anchor by the
+    TMA-reduce engine (rank 0 stored, ranks 1..P-1 reduced in order) and the
+    copy engines carry it to the other ranks; the same bits as the oracle,
+    capped or not, misaligned or in place."""
+    g = groups(p)
+    reset_config(g, engine=CE, ce_segment_bytes=256 * 1024, ce_fold=3)
+    xs = datagen.rank_buffers(KIND[dtype], 36, p, 300_007)
+    got = allreduce(g, xs, dtype, op, cap=cap, send_off=offs, recv_off=offs, in_place=in_place)
+    info = g.last_launch()
+    assert info["engine"] == CE and info["threads"] != 1024 and info["ce_segments"] > 1, info
+    check(got, oracle.allreduce(xs, dtype, op, nthreads=0), f"TMA-reduce fold {dtype} {op} P={p}")
+
+
+def test_tma_reduce_fold_falls_back_for_other_pairs(groups):
+    """A pair the copy hardware cannot reduce exactly (bf16 sum) takes the
+    register fold under ce_fold = 3, with the same bits."""
+    g = groups(8)
+    reset_config(g, engine=CE, ce_segment_bytes=256 * 1024, ce_fold=3)
+    xs = datagen.rank_buffers("normal_bf16", 37, 8, 300_007)
+    got = allreduce(g, xs, "bf16", "sum", cap=16)
+    assert g.last_launch()["threads"] == 1024
+    check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), "bf16 sum under ce_fold 3")
