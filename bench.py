@@ -1265,6 +1265,9 @@ def copy_out_bench(args):
         "seg24": {"ce_segment_bytes": 24 << 20},
         "seg28": {"ce_segment_bytes": 28 << 20},
         "seg26": {"ce_segment_bytes": 26 << 20},
+        "seg8": {"ce_segment_bytes": 8 << 20},
+        "seg12": {"ce_segment_bytes": 12 << 20},
+        "seg14": {"ce_segment_bytes": 14 << 20},
         "seg30": {"ce_segment_bytes": 30 << 20},
         # the copy-out engine whatever the cap (Auto stops at ce_auto_max_cap)
         "copy_out": {"engine": 5},
