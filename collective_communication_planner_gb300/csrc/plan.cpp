@@ -246,8 +246,11 @@ void copy_out_streams(const Config& c, int nranks, int cap, int* mid, int* tail)
   // stream for the overlapped segments against two / three / four: cap 8
   // 0.306 / 0.303 / 0.303 / 0.298, cap 16 0.512 / 0.508 / 0.508 / 0.497;
   // cap 32 two or three (0.729-0.733) against one (0.720) and four (0.722).
+  // A segment's copies are P - 1 of its size, so the count scales with P - 1
+  // as well: one stream per 112 / (P - 1) CTAs, rounded (P = 8: one per 16);
+  // P = 4, 64 MiB per rank, cap 32: one stream 0.605, two 0.583.
   int m = c.ce_ar_streams;
-  if (m <= 0) m = cap > 0 ? std::max(1, (cap + 8) / 16) : c.ce_streams;
+  if (m <= 0) m = cap > 0 ? std::max(1, (cap * (nranks - 1) + 56) / 112) : c.ce_streams;
   m = std::min(m, c.ce_streams);
   *mid = std::max(1, std::min(m, nranks - 1));
   *tail = std::max(1, std::min(c.ce_tail_streams, nranks - 1));

@@ -163,8 +163,9 @@ bool register_fold_ok(int coll, int nranks, const uint8_t* send_mod16, const uin
                       size_t count, int es, size_t seg_elems);
 
 // Copy streams of a copy-out allreduce: *mid for the segments whose copies
-// run beside the next segment's fold (ce_ar_streams, or by default about one
-// per 16 CTAs of the cap, at least 1), *tail for the last segment
+// run beside the next segment's fold (ce_ar_streams, or by default one per
+// 112 / (P - 1) CTAs of the cap, rounded, at least 1: one per 16 CTAs for
+// P = 8), *tail for the last segment
 // (ce_tail_streams); both within ce_streams and P - 1.
 void copy_out_streams(const Config& c, int nranks, int cap, int* mid, int* tail);
 

@@ -185,8 +185,9 @@ typedef struct {
                               is set, else 8 KiB */
   int ce_ar_streams;       /* copy-out allreduce: copy streams that carry each segment but the
                               last (those copies run beside the next segment's fold, which they
-                              slow down); 0: one per 16 CTAs of the cap, rounded, at least one
-                              (ce_streams uncapped); at most ce_streams */
+                              slow down); 0: one per 112 / (P - 1) CTAs of the cap (one per 16
+                              for P = 8), rounded, at least one (ce_streams uncapped); at most
+                              ce_streams */
   int ce_tail_streams;     /* copy-out allreduce: copy streams that carry the last segment (its
                               copies run beside nothing); 0: ce_streams; at most ce_streams */
 } tcclConfig_t;
