@@ -1112,7 +1112,7 @@ def rmsnorm_bench(args):
 
 # ------------------------------------------------------------------ host-cost mode
 def build_host_cost() -> Path:
-    """Compiles tests/host_cost.cu (a C++ driver of the C ABI) against the
+    """Compiles tests/host_cost.cu (a C++ program that calls the C ABI) against the
     in-tree libtccl.so; returns the executable's path."""
     pkg = ROOT / "collective_communication_planner_gb300"
     out = pkg / "_build" / "host_cost"
@@ -1131,7 +1131,7 @@ def host_cost(args):
     r = subprocess.run([str(exe), str(args.host_cost_batches)], capture_output=True, text=True)
     sys.stdout.write(r.stdout)
     if r.returncode != 0:
-        raise SystemExit(f"host-cost driver failed ({r.returncode}): {r.stderr.strip()}")
+        raise SystemExit(f"host-cost program failed ({r.returncode}): {r.stderr.strip()}")
 
 
 # ------------------------------------------------------------------ TMA-reduce mode
@@ -1348,7 +1348,7 @@ def main():
     ap.add_argument("--copy-out-workload", choices=sorted(WORKLOADS), default="c4",
                     help="for --copy-out: the allreduce workload")
     ap.add_argument("--host-cost", action="store_true",
-                    help="per-call host cost of tcclAllReduce from a C++ driver (decode-sized messages)")
+                    help="per-call host cost of tcclAllReduce from a C++ program (decode-sized messages)")
     ap.add_argument("--host-cost-batches", type=int, default=50)
     ap.add_argument("--tma-reduce", action="store_true",
                     help="TMA-reduce engine vs the bulk engine, fp32 sum, 64 MiB per rank")

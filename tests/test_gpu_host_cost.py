@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 ROOT = Path(__file__).resolve().parents[1]
 
 
-def test_c_driver_results_and_host_cost():
+def test_cpp_caller_results_and_host_cost():
     sys.path.insert(0, str(ROOT))
     import bench
 
