@@ -618,11 +618,13 @@ def run_reference(args, w):
 # ------------------------------------------------------------------ sweep mode
 def sweep(args):
     """One JSON line per configuration point of the five workloads (C1..C5):
-    device time per op (CUDA events, back-to-back launches; graph-captured
+    device time per op (CUDA events around batches of back-to-back launches:
+    `us` is the median of five batches, `us_min` the fastest; graph-captured
     too for small messages), algbw, bus bandwidth, HBM fraction, SMs used, and
     the CPU oracle on 1 core and on all cores for one point per workload.
-    Points whose traffic fits three times in L2 are also timed cold: L2
-    flushed before each of 20 single-launch timings (cold_l2_us)."""
+    Points whose traffic fits three times in L2 are also timed cold: before
+    each of 20 single-launch timings, a 3 x L2 write and then a 2 x L2 read
+    leave L2 holding clean lines of other data (cold_l2_us, the median)."""
     import numpy as np
     import torch
     import collective_communication_planner_gb300 as tccl
@@ -636,22 +638,34 @@ def sweep(args):
     peak, _ = measured_peak()
     ncores = os.cpu_count() or 1
 
-    def ev_time(fn, min_ms=60.0):
+    def ev_stats(fn, min_ms=60.0, batches=5):
+        """Per-call ms of back-to-back calls: `batches` batches, each between
+        one event pair and at least min_ms / batches long (and at least 200
+        calls when a call is short); returns (median, min) over the batches."""
         for _ in range(3):
             fn()
         stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        it = 1
-        while True:
+
+        def batch(it):
             e0.record(stream)
             for _ in range(it):
                 fn()
             e1.record(stream)
             e1.synchronize()
-            ms = e0.elapsed_time(e1)
-            if ms >= min_ms or it >= 20000:
-                return ms / it
-            it = min(20000, max(it * 2, int(it * min_ms / max(ms, 1e-3)) + 1))
+            return e0.elapsed_time(e1)
+
+        want = min_ms / batches
+        it = 1
+        while True:
+            ms = batch(it)
+            if ms >= want or it >= 20000:
+                break
+            it = min(20000, max(it * 2, int(it * want / max(ms, 1e-3)) + 1))
+        if ms / it < 1e-2:
+            it = max(it, 200)
+        per = sorted(batch(it) / it for _ in range(batches))
+        return per[len(per) // 2], per[0]
 
     def graph_time(fn, reps=20):
         with torch.cuda.stream(stream):
@@ -661,18 +675,23 @@ def sweep(args):
         with torch.cuda.graph(g, stream=stream):
             for _ in range(reps):
                 fn()
-        t = ev_time(g.replay, 30.0) / reps
+        t = ev_stats(g.replay, 30.0)[0] / reps
         del g
         return t
 
     l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20))
     flush_buf = torch.empty(3 * l2_bytes // 4, dtype=torch.int32, device=dev)
 
+    # read after the flush write, so that the flush's dirty lines are written
+    # back before the timed launch rather than inside it
+    clean_buf = torch.zeros(2 * l2_bytes // 4, dtype=torch.int32, device=dev)
+
     def cold_time(fn, reps=20):
         times = []
         for _ in range(reps):
             with torch.cuda.stream(stream):
                 flush_buf.fill_(1)
+                clean_buf.max()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fn()
@@ -735,10 +754,10 @@ def sweep(args):
             per, used = g.read_sm_record_launches()
             per_launch = max(per) if per else 0
             g.record_sms(False)
-        ms = ev_time(fn)
+        ms, ms_min = ev_stats(fn)
         row = dict(config=cfg, coll=coll, P=p, dtype=dtype, op=op, count=n,
                    bytes_per_rank=(n * es if coll == "AR" else S), cap=cap,
-                   us=round(ms * 1e3, 3),
+                   us=round(ms * 1e3, 3), us_min=round(ms_min * 1e3, 3),
                    algbw=round(p * (n * es if coll == "AR" else S) / (ms * 1e-3) / 1e9, 2),
                    busbw=round(S / (ms * 1e-3) * (2 if coll == "AR" else 1) * (p - 1) / p / 1e9, 2),
                    hbm_GBps=round(hbm / (ms * 1e-3) / 1e9, 1),
