@@ -58,7 +58,8 @@ class tcclLaunchInfo_t(ctypes.Structure):
                 ("tasks", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
                 ("chunk_order", ctypes.c_int), ("total_chunks", ctypes.c_uint64),
                 ("stage_layout", ctypes.c_int), ("ce_segments", ctypes.c_int),
-                ("ce_copies", ctypes.c_int)]
+                ("ce_copies", ctypes.c_int),
+                ("ce_wide_folds", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -149,7 +149,7 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
   int mid_streams = 0, tail_streams = 0;
   copy_out_streams(g->cfg, P, cap, &mid_streams, &tail_streams);
   const int used = P > 1 ? std::max(mid_streams, tail_streams) : 0;
-  int err = 0, copies = 0;
+  int err = 0, copies = 0, wide_folds = 0;
   for (int sgi = 0; sgi < nseg && !err; ++sgi) {
     const size_t off = (size_t)sgi * seg;
     const size_t n = sgi == nseg - 1 ? tail_n : seg;
@@ -162,7 +162,9 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
       aa.tail_bytes = bytes - head - aa.nvec * 16;
       for (int k = 0; k < P; ++k) aa.p.src[k] = s_ptr[k];
       aa.p.dst[0] = r_ptr[anchor];
-      const uint64_t per_cta = (uint64_t)kAnchorThreads * U;
+      aa.wide = anchor_wide_ok(aa) ? 1 : 0;
+      wide_folds += aa.wide;
+      const uint64_t per_cta = (uint64_t)kAnchorThreads * (aa.wide ? anchor_vectors_per_thread(P, true) : U);
       uint64_t grid = std::max<uint64_t>(1, (aa.nvec + per_cta - 1) / per_cta);
       grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
       fast_grid = std::max(fast_grid, (int)grid);
@@ -197,6 +199,7 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
   g->last.engine = kEngineCopyOut;
   g->last.ce_segments = nseg;
   g->last.ce_copies = copies;
+  g->last.ce_wide_folds = wide_folds;
   if (err) {
     if (log_level()) std::fprintf(stderr, "[tccl] copy-out allreduce failed: %s\n", cudaGetErrorString((cudaError_t)err));
     return tcclCudaError;
@@ -233,7 +236,8 @@ tcclResult_t run_copy_out_reduce_scatter(tcclGroup* g, const void* const* send, 
     aa.p.src[k] = send[k];
     aa.p.dst[k] = recv[k];
   }
-  const uint64_t per_cta = (uint64_t)kAnchorThreads * anchor_vectors_per_thread(P);
+  aa.wide = anchor_wide_ok(aa) ? 1 : 0;
+  const uint64_t per_cta = (uint64_t)kAnchorThreads * anchor_vectors_per_thread(P, aa.wide != 0);
   uint64_t grid = std::max<uint64_t>(1, (aa.nvec * P + per_cta - 1) / per_cta);
   grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
   const int err = launch_anchor_reduce(dtype, op, aa, (int)grid, cap <= 0, stream);
@@ -243,6 +247,7 @@ tcclResult_t run_copy_out_reduce_scatter(tcclGroup* g, const void* const* send, 
   g->last.ctas = (int)grid;
   g->last.threads = kAnchorThreads;
   g->last.ce_segments = 1;
+  g->last.ce_wide_folds = aa.wide;
   if (err) {
     if (log_level()) std::fprintf(stderr, "[tccl] copy-out reduce-scatter failed: %s\n", cudaGetErrorString((cudaError_t)err));
     return tcclCudaError;

@@ -6,8 +6,12 @@
 // through TMA copies and shared memory costs each byte a shared-memory write
 // and a read plus per-stage synchronisation, and a capped SM then reads about
 // 50 GB/s; 128-bit register loads with eight in flight per thread read about
-// 140 GB/s per SM on GB300. Every result goes to one buffer, so the kernel is
-// read-bound.
+// 140 GB/s per SM on GB300, and 256-bit loads of the same bytes in flight
+// (buffers 32-byte aligned) about 6% more. Every result goes to one buffer,
+// so the kernel is read-bound.
+#include <cstdlib>
+#include <string>
+
 #include "copy_out.h"
 #include "dispatch.cuh"
 
@@ -56,6 +60,21 @@ __device__ __forceinline__ void st_keep_v4(void* p, uint4 v, uint64_t policy) {
                  : "memory");
 }
 
+// 256-bit forms (sm_100 and later): one 32-byte vector as two 16-byte halves
+__device__ __forceinline__ void ld_stream_v8(const void* p, uint64_t policy, uint4& lo, uint4& hi) {
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
+      : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+      : "l"(p), "l"(policy));
+}
+
+__device__ __forceinline__ void st_keep_v8(void* p, uint4 lo, uint4 hi, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p),
+               "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w),
+               "l"(policy)
+               : "memory");
+}
+
 // For each job, thread t of the grid folds vectors t, t + T, ... (T threads
 // in all), U of them at a time. With the rank count fixed at compile time
 // (NP = 2, 4, 8) every load of a step is issued before the first add;
@@ -72,10 +91,39 @@ struct AnchorFold<kBF16, kSum, true> {
   using type = MixedSumBF16;
 };
 
+// The job's unaligned head and tail (the bytes before and after its 16-byte
+// vectors), one element per thread of the grid.
+template <int DT, int OP>
+__device__ __forceinline__ void anchor_edges(const AnchorArgs& a, int job, int P, uint32_t gtid) {
+  constexpr int es = DT == kBF16 ? 2 : 4;
+  const uint32_t nh = static_cast<uint32_t>(a.head_bytes / es);
+  const uint32_t nt = static_cast<uint32_t>(a.tail_bytes / es);
+  if (gtid >= nh + nt) return;
+  Window w;
+  w.src_sel = -1;
+  w.dst_sel = static_cast<int16_t>(job);
+  w.scalar = 1;
+  w.task = 0;
+  w.cta = -1;
+  uint64_t e = gtid;
+  const uint64_t job_off = static_cast<uint64_t>(job) * a.job_src_stride;
+  if (gtid < nh) {
+    w.src_off = job_off;
+    w.dst_off = 0;
+    w.bytes = static_cast<uint32_t>(a.head_bytes);
+  } else {
+    const uint64_t body_end = a.head_bytes + a.nvec * 16;
+    w.src_off = job_off + body_end;
+    w.dst_off = body_end;
+    w.bytes = static_cast<uint32_t>(a.tail_bytes);
+    e -= nh;
+  }
+  scalar_element<kAllReduce, DT, OP, kMaxRanks>(a.p, P, w, e);
+}
+
 template <int DT, int OP, int NP, int U, bool MIXED>
 __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const __grid_constant__ AnchorArgs a) {
   constexpr int RB = NP > 0 ? NP : 8 / U;
-  constexpr int es = DT == kBF16 ? 2 : 4;
   const int P = NP > 0 ? NP : a.nranks;
   // a job covers fewer than 2^28 vectors (register_fold_ok keeps larger ones
   // off this kernel), so vector indices and byte offsets within it fit 32 bits
@@ -137,31 +185,74 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
         if (v < nvec) st_keep_v4<kHint>(dst + static_cast<uint64_t>(v) * 16, acc[u].out(), store_policy);
       }
     }
-    // the job's unaligned head and tail, one element per thread
-    const uint32_t nh = static_cast<uint32_t>(a.head_bytes / es);
-    const uint32_t nt = static_cast<uint32_t>(a.tail_bytes / es);
-    if (gtid < nh + nt) {
-      Window w;
-      w.src_sel = -1;
-      w.dst_sel = static_cast<int16_t>(job);
-      w.scalar = 1;
-      w.task = 0;
-      w.cta = -1;
-      uint64_t e = gtid;
-      const uint64_t job_off = static_cast<uint64_t>(job) * a.job_src_stride;
-      if (gtid < nh) {
-        w.src_off = job_off;
-        w.dst_off = 0;
-        w.bytes = static_cast<uint32_t>(a.head_bytes);
-      } else {
-        const uint64_t body_end = a.head_bytes + static_cast<uint64_t>(nvec) * 16;
-        w.src_off = job_off + body_end;
-        w.dst_off = body_end;
-        w.bytes = static_cast<uint32_t>(a.tail_bytes);
-        e -= nh;
+    anchor_edges<DT, OP>(a, job, P, gtid);
+  }
+}
+
+// The same fold with 256-bit loads: each thread folds one 32-byte vector of
+// every rank at a time, the ranks in batches of four (NP = 4 or 8), so each
+// thread keeps as many bytes in flight as eight 128-bit loads with half the
+// load instructions. The two 16-byte halves of a vector have one accumulator
+// each and receive the ranks in ascending order, as above. Needs every source
+// and the destination 32-byte aligned after the head (the launcher checks);
+// an odd last 16-byte vector is folded by the grid's last thread.
+template <int DT, int OP, int NP, bool MIXED>
+__global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_wide_kernel(const __grid_constant__ AnchorArgs a) {
+  static_assert(NP == 4 || NP == 8, "ranks go in batches of four");
+  constexpr int RB = 4;
+  const uint32_t nthr = gridDim.x * blockDim.x;
+  const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t nvec = static_cast<uint32_t>(a.nvec);
+  const uint32_t nwide = nvec / 2;
+  if (a.prefetch_first && threadIdx.x < static_cast<unsigned>(NP)) {
+    const uint32_t vs = blockIdx.x * blockDim.x;
+    if (vs < nwide)
+      bulk_prefetch_l2(static_cast<const char*>(a.p.src[threadIdx.x]) + a.head_bytes + static_cast<uint64_t>(vs) * 32,
+                       min(blockDim.x, nwide - vs) * 32u);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) record_sm(a.sm_mask);
+  const uint64_t load_policy = l2_policy_evict_first();
+  const uint64_t store_policy = l2_policy_evict_last();
+  using Acc = typename AnchorFold<DT, OP, MIXED>::type;
+  for (int job = 0; job < a.njobs; ++job) {
+    const uint64_t src_off = static_cast<uint64_t>(job) * a.job_src_stride + a.head_bytes;
+    char* dst = static_cast<char*>(a.p.dst[job]) + a.head_bytes;
+    for (uint32_t v = gtid; v < nwide; v += nthr) {
+      Acc lo, hi;
+#pragma unroll
+      for (int r0 = 0; r0 < NP; r0 += RB) {
+        uint4 xl[RB], xh[RB];
+#pragma unroll
+        for (int k = 0; k < RB; ++k)
+          ld_stream_v8(static_cast<const char*>(a.p.src[r0 + k]) + src_off + static_cast<uint64_t>(v) * 32,
+                       load_policy, xl[k], xh[k]);
+#pragma unroll
+        for (int k = 0; k < RB; ++k) {
+          if (r0 + k == 0) {
+            lo.init(xl[k]);
+            hi.init(xh[k]);
+          } else {
+            lo.add(xl[k]);
+            hi.add(xh[k]);
+          }
+        }
       }
-      scalar_element<kAllReduce, DT, OP, kMaxRanks>(a.p, P, w, e);
+      st_keep_v8(dst + static_cast<uint64_t>(v) * 32, lo.out(), hi.out(), store_policy);
     }
+    if ((nvec & 1) && gtid == nthr - 1) {
+      const uint64_t last = static_cast<uint64_t>(nvec - 1) * 16;
+      Acc acc;
+#pragma unroll
+      for (int k = 0; k < NP; ++k) {
+        const uint4 x = ld_stream_v4<true>(static_cast<const char*>(a.p.src[k]) + src_off + last, load_policy);
+        if (k == 0) acc.init(x);
+        else acc.add(x);
+      }
+      st_keep_v4<true>(dst + last, acc.out(), store_policy);
+    }
+    anchor_edges<DT, OP>(a, job, NP, gtid);
   }
 }
 
@@ -175,6 +266,13 @@ int launch_anchor_t(const AnchorArgs& args, int grid, bool early, cudaStream_t s
   s.smem = 0;
   s.early_launch = early ? 1 : 0;
   constexpr bool kCanMix = D == kBF16 && O == kSum;
+  if (a.wide && (a.nranks == 4 || a.nranks == 8)) {
+    if (kCanMix && a.mixed_bf16)
+      return a.nranks == 8 ? launch_maybe_early(anchor_reduce_wide_kernel<D, O, 8, kCanMix>, a, s, st)
+                           : launch_maybe_early(anchor_reduce_wide_kernel<D, O, 4, kCanMix>, a, s, st);
+    return a.nranks == 8 ? launch_maybe_early(anchor_reduce_wide_kernel<D, O, 8, false>, a, s, st)
+                         : launch_maybe_early(anchor_reduce_wide_kernel<D, O, 4, false>, a, s, st);
+  }
   if (kCanMix && a.mixed_bf16) {
     switch (a.nranks) {
       case 2: return launch_maybe_early(anchor_reduce_kernel<D, O, 2, 2, kCanMix>, a, s, st);
@@ -195,7 +293,24 @@ int launch_anchor_t(const AnchorArgs& args, int grid, bool early, cudaStream_t s
 }  // namespace
 }  // namespace dev
 
-int anchor_vectors_per_thread(int nranks) { return (nranks == 2 || nranks == 4) ? 2 : 1; }
+int anchor_vectors_per_thread(int nranks, bool wide) {
+  return (wide || nranks == 2 || nranks == 4) ? 2 : 1;
+}
+
+bool anchor_wide_ok(const AnchorArgs& a) {
+  static const bool enabled = [] {
+    const char* e = std::getenv("TCCL_ANCHOR_WIDE");
+    return !(e && std::string(e) == "0");
+  }();
+  if (!enabled || (a.nranks != 4 && a.nranks != 8)) return false;
+  for (int j = 0; j < a.njobs; ++j) {
+    const uint64_t off = static_cast<uint64_t>(j) * a.job_src_stride + a.head_bytes;
+    for (int k = 0; k < a.nranks; ++k)
+      if ((reinterpret_cast<uintptr_t>(a.p.src[k]) + off) % 32) return false;
+    if ((reinterpret_cast<uintptr_t>(a.p.dst[j]) + a.head_bytes) % 32) return false;
+  }
+  return true;
+}
 
 int launch_anchor_reduce(int dtype, int op, const AnchorArgs& a, int grid, bool early,
                          void* stream) {

@@ -208,6 +208,10 @@ typedef struct {
   int stage_layout;    /* bulk engine: tcclStageLayout_t used (0 otherwise) */
   int ce_segments;     /* copy-out engine: kernel launches (segments) of the call (0 otherwise) */
   int ce_copies;       /* copy-out engine: device-to-device copies enqueued (0 otherwise) */
+  int ce_wide_folds;   /* copy-out engine: register-fold launches that read with 256-bit loads
+                          (P = 4 or 8 with every buffer 32-byte aligned past the head; the same
+                          bits as the 128-bit loads, which TCCL_ANCHOR_WIDE=0 in the process's
+                          environment keeps); 0 otherwise */
 } tcclLaunchInfo_t;
 
 const char* tcclGetErrorString(tcclResult_t r);

@@ -530,3 +530,46 @@ def test_tma_reduce_fold_falls_back_for_other_pairs(groups):
     got = allreduce(g, xs, "bf16", "sum", cap=16)
     assert g.last_launch()["threads"] == 1024
     check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), "bf16 sum under ce_fold 3")
+
+
+@pytest.mark.parametrize("p", [4, 8])
+@pytest.mark.parametrize("dtype,op", [("bf16", "sum"), ("f32", "sum"), ("i32", "max"), ("bf16", "min")])
+@pytest.mark.parametrize("case", ["aligned", "odd_vectors", "head_32", "head_16"])
+def test_wide_fold_layouts(groups, p, dtype, op, case):
+    """The register fold's 256-bit loads (P = 4 or 8, every buffer 32-byte
+    aligned past the head): an even and an odd count of 16-byte vectors (the
+    odd last one folded on its own), and a head that leaves the body 32-byte
+    aligned; a head that leaves it only 16-byte aligned takes the 128-bit
+    loads. Both bit-exact against the oracle."""
+    g = groups(p)
+    es = 2 if dtype == "bf16" else 4
+    reset_config(g, engine=CE, ce_segment_bytes=256 * 1024)
+    n = {"aligned": 200_000 * 16 // es, "odd_vectors": (100_001 * 16 + 6) // es}.get(case, 150_001)
+    # head_32: start 18 bytes past a 32-byte boundary (bf16) or 20 (4-byte
+    # types), so the 14- / 12-byte head ends on one; head_16: 2 or 4 bytes
+    # past it, so the head ends 16 bytes short of one
+    off = {"head_32": 18 if es == 2 else 20, "head_16": 2 if es == 2 else 4}.get(case, 0)
+    xs = datagen.rank_buffers(KIND[dtype], 41, p, n)
+    got = allreduce(g, xs, dtype, op, cap=16, send_off=off, recv_off=off)
+    info = g.last_launch()
+    assert info["engine"] == CE and info["ctas"] <= 16, info
+    want_wide = info["ce_segments"] if case != "head_16" else 0
+    assert info["ce_wide_folds"] == want_wide, (case, info)
+    check(got, oracle.allreduce(xs, dtype, op, nthreads=0), f"wide fold {case} {dtype} {op} P={p}")
+
+
+@pytest.mark.parametrize("p", [4, 8])
+@pytest.mark.parametrize("rc", [40_000, 40_008])
+def test_wide_fold_reduce_scatter(groups, p, rc):
+    """Reduce-scatter on the register fold: shards of a multiple of 32 bytes
+    keep every job 32-byte aligned and take the 256-bit loads; shards of an
+    odd multiple of 16 bytes leave every other job 16 bytes off and take the
+    128-bit loads. Both exact."""
+    g = groups(p)
+    reset_config(g, engine=CE)
+    xs = datagen.rank_buffers("normal_bf16", 42, p, p * rc)
+    got = reduce_scatter(g, xs, rc, "bf16", "sum", cap=8)
+    info = g.last_launch()
+    assert info["engine"] == CE and info["ce_copies"] == 0, info
+    assert info["ce_wide_folds"] == (1 if rc * 2 % 32 == 0 else 0), info
+    check(got, oracle.reduce_scatter(xs, "bf16", "sum", nthreads=0), f"RS wide rc={rc} P={p}")
