@@ -1288,6 +1288,8 @@ def copy_out_bench(args):
         "seg12": {"ce_segment_bytes": 12 << 20},
         "seg14": {"ce_segment_bytes": 14 << 20},
         "seg30": {"ce_segment_bytes": 30 << 20},
+        "seg32": {"ce_segment_bytes": 32 << 20},
+        "seg36": {"ce_segment_bytes": 36 << 20},
         # the copy-out engine whatever the cap (Auto stops at ce_auto_max_cap)
         "copy_out": {"engine": 5},
         # segments bulk-reduced into the anchor by the TMA-reduce engine (the
