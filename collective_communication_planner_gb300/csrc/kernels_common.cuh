@@ -609,6 +609,10 @@ __device__ __forceinline__ void per_rank_consumers(const BulkArgs& a, BulkSmemHe
           else acc[j].add(st[v]);
         }
       }
+      // the stage's reads (generic proxy) before the producer's next bulk
+      // copy into it (async proxy): without the proxy fence the release can
+      // overtake reads whose values are still in flight
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&h.empty[k]);
       ++it;
@@ -896,6 +900,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
         const uint64_t o = loc.w.dst_off + off + static_cast<uint64_t>(v) * 16;
         for (int d = d0; d < d1; ++d) st_global_v4(static_cast<char*>(a.p.dst[d]) + o, res);
       }
+      fence_proxy_async_smem();  // the stage's reads before its next bulk copy
       __syncwarp();
       if (lane == 0) mbar_arrive(&h.empty[k]);
     } else {
@@ -914,9 +919,11 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps), 1)
           f.add(reinterpret_cast<const uint4*>(st + static_cast<size_t>(r) * chunk)[v]);
         reinterpret_cast<uint4*>(res_slot)[v] = f.out();
       }
+      // the stage's reads before its next bulk copy, and the result slot's
+      // writes before the bulk stores read it
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&h.empty[k]);
-      fence_proxy_async_smem();
       named_bar_sync(1, nct);
       if (ctid == 0 && !*abort_flag) {
         const int d0 = loc.w.dst_sel < 0 ? 0 : loc.w.dst_sel;
