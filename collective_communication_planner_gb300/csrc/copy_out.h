@@ -1,5 +1,6 @@
-// Copy-out engine: the kernel that folds P ranks with plain 128-bit register
-// loads (no shared-memory staging), into one anchor rank's buffer before the
+// Copy-out engine: the kernel that folds P ranks with plain register loads
+// (128-bit, or 256-bit where every buffer is 32-byte aligned past the head;
+// no shared-memory staging), into one anchor rank's buffer before the
 // GPU's copy engines fan the result out to the other ranks, or for a
 // reduce-scatter into each shard's owner.
 #pragma once

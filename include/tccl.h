@@ -96,9 +96,11 @@ typedef enum {
                               bytes (else the bulk engine). Auto picks it, for calls of at least
                               4 MiB per rank buffer, for allreduce / all-gather when the cap is
                               at most ce_auto_max_cap CTAs, and for reduce-scatter under any cap
-                              or uncapped with P <= 4. The segment kernel folds with 128-bit register
-                              loads when the send buffers and the anchor's receive buffer share
-                              their address mod 16, else with the bulk engine's TMA pipeline. */
+                              or uncapped with P <= 4. The segment kernel folds with register
+                              loads (128-bit, or 256-bit for P = 4 or 8 with every buffer 32-byte
+                              aligned past the head) when the send buffers and the anchor's
+                              receive buffer share their address mod 16, else with the bulk
+                              engine's TMA pipeline. */
 } tcclEngine_t;
 
 typedef enum {
@@ -167,7 +169,7 @@ typedef struct {
                               and 4, 3/8 for P >= 5; negative: never) */
   int reduce_order;        /* tcclReduceOrder_t (default ascending) */
   int ce_fold;             /* copy-out allreduce, the kernel that folds each segment into the anchor:
-                              0 or 1: the 128-bit register-load fold where every send buffer
+                              0 or 1: the register-load fold where every send buffer
                               shares its address mod 16 with the anchor's receive buffer, else the
                               bulk engine's TMA pipeline; 2: always the TMA pipeline (with the
                               group's stage layout and shape); 3: the TMA-reduce engine, rank 0
