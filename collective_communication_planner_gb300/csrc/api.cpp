@@ -837,8 +837,18 @@ tcclResult_t tcclAllReduceRMSNorm(tcclGroup_t g, const void* const sendbufs[],
     const int vectors = nvec > (size_t)4 * kRmsMaxThreads ? 8 : 4;
     int threads = (int)std::min<size_t>(kRmsMaxThreads, ((nvec + vectors - 1) / vectors + 31) / 32 * 32);
     threads = std::max(threads, 32);
+    // up to 8 rows per SM: one CTA per row; up to 16: 8 CTAs per SM taking
+    // every gridDim-th row (the block scheduler spreads the CTAs). More rows
+    // than that, or than a cap allows: a grid of the CTAs that fit on the SMs
+    // at once, which claim rows from a counter in the group's status block
+    // (bytes 32..47), so the SMs finish together
     uint64_t grid = std::min<uint64_t>(rows, (uint64_t)g->dev.sm_count * 8);
     if (cta_cap > 0) grid = std::min<uint64_t>(grid, (uint64_t)cta_cap);
+    if (rows > grid && (cta_cap > 0 || rows > (uint64_t)g->dev.sm_count * 16)) {
+      const int per_sm = rmsnorm_ctas_per_sm(datatype, threads, vectors, hidden * es);
+      if (per_sm > 0) grid = std::min<uint64_t>(grid, (uint64_t)g->dev.sm_count * per_sm);
+      a.claim = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(g->d_status) + 32);
+    }
     err = launch_rmsnorm(datatype, a, (int)grid, threads, vectors, cta_cap <= 0, stream);
     g->last.ctas = (int)grid;
     g->last.threads = threads;

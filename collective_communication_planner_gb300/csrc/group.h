@@ -76,7 +76,8 @@ struct tcclGroup {
   int device = 0;
   tccl::DeviceDesc dev;
   tccl::Config cfg;
-  int* d_status = nullptr;     // [0] status code
+  int* d_status = nullptr;     // 64 bytes: [0] status code; bytes 32..47 the fused
+                               // RMSNorm's row counter and finished-CTA count
   // SM recorder: one 256-bit bitmap per kernel launch while recording
   // (tccl::kSmSlots of them; launches past the last slot share it)
   uint32_t* d_sm_mask = nullptr;

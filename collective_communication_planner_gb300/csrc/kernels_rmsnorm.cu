@@ -12,15 +12,21 @@ namespace {
 
 // V: 16-byte vectors of a row per thread. Loads of RB ranks are issued
 // together before they are folded (ascending rank order is kept), so a row
-// costs a few memory round trips, not P of them.
+// costs a few memory round trips, not P of them. CTA b reduces row b first;
+// with a.claim set (more rows than CTAs) it then claims rows from a device
+// counter, so SMs that stream faster take more rows and the grid ends within
+// about one row's time of itself; without it, rows b + G, b + 2G, ... One
+// block barrier per row: the sums of squares of the warps are exchanged
+// through a double-buffered slot, and every warp adds them up in the same
+// order, so every warp derives the same scale.
 template <int DT, int V>
 __global__ void __launch_bounds__(kRmsMaxThreads) rmsnorm_kernel(const __grid_constant__ RmsArgs a) {
   using dev::Fold;
   constexpr int kVecElems = DT == kBF16 ? 8 : 4;
   constexpr int RB = 16 / V;  // ranks per load batch: V * RB 16-byte registers in flight
   extern __shared__ __align__(16) uint4 gamma_smem[];
-  __shared__ float partial[kRmsMaxThreads / 32];
-  __shared__ float row_scale;
+  __shared__ float partial[2][kRmsMaxThreads / 32];
+  __shared__ unsigned long long next_row[2];
   const uint32_t row_bytes = a.hidden * (DT == kBF16 ? 2u : 4u);
   // an early (programmatic dependent) launch gets here while the stream's
   // previous kernel may still run: when every CTA has one row and all of
@@ -42,7 +48,13 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rmsnorm_kernel(const __grid_co
   for (uint32_t v = threadIdx.x; v < nvec; v += blockDim.x)
     gamma_smem[v] = dev::ld_global_v4(static_cast<const char*>(a.gamma) + v * 16ull);
   __syncthreads();
-  for (uint64_t t = blockIdx.x; t < a.rows; t += gridDim.x) {
+  int buf = 0;
+  for (uint64_t t = blockIdx.x; t < a.rows; buf ^= 1) {
+    // the row after this one: claimed now, its value needed (and published
+    // through shared memory) only at this row's barrier, so the claim's round
+    // trip overlaps the row's loads
+    unsigned long long nxt = 0;
+    if (threadIdx.x == 0) nxt = a.claim ? gridDim.x + atomicAdd(a.claim, 1ull) : t + gridDim.x;
     const uint64_t row_off = t * static_cast<uint64_t>(a.hidden) * (DT == kBF16 ? 2 : 4);
     Fold<DT, kSum> acc[V];
     for (int r0 = 0; r0 < P; r0 += RB) {
@@ -79,16 +91,16 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rmsnorm_kernel(const __grid_co
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, o));
-    if (lane == 0) partial[warp] = ss;
+    if (lane == 0) partial[buf][warp] = ss;
+    if (threadIdx.x == 0) next_row[buf] = nxt;
+    // the one barrier of the row; a slot is written again two rows later,
+    // after the next row's barrier, which every thread reaches only once it
+    // has read this row's slot
     __syncthreads();
-    if (warp == 0) {
-      float w = lane < nwarps ? partial[lane] : 0.f;
+    float w = lane < nwarps ? partial[buf][lane] : 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) w = __fadd_rn(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
-      if (lane == 0) row_scale = rsqrtf(__fadd_rn(__fdiv_rn(w, static_cast<float>(a.hidden)), a.eps));
-    }
-    __syncthreads();
-    const float scale = row_scale;
+    for (int o = 16; o > 0; o >>= 1) w = __fadd_rn(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
+    const float scale = rsqrtf(__fadd_rn(__fdiv_rn(w, static_cast<float>(a.hidden)), a.eps));
 #pragma unroll
     for (int j = 0; j < V; ++j) {
       const uint32_t v = threadIdx.x + j * blockDim.x;
@@ -103,7 +115,16 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rmsnorm_kernel(const __grid_co
         for (int d = 0; d < P; ++d) dev::st_global_v4(static_cast<char*>(a.p.dst[d]) + o, y);
       }
     }
-    __syncthreads();  // partial[] and row_scale are reused by the next row
+    t = next_row[buf];
+  }
+  // the last CTA to finish resets the counter for the next launch (every
+  // CTA made its last claim before it counts itself finished)
+  if (a.claim && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.claim + 1, 1ull) == gridDim.x - 1) {
+      atomicExch(a.claim, 0ull);
+      atomicExch(a.claim + 1, 0ull);
+    }
   }
 }
 
@@ -243,6 +264,18 @@ int launch_rmsnorm(int dtype, const RmsArgs& a, int grid, int threads, int vecto
                         : dev::launch_maybe_early(rmsnorm_kernel<kBF16, 8>, a, s, st);
   return vectors <= 4 ? dev::launch_maybe_early(rmsnorm_kernel<kF32, 4>, a, s, st)
                       : dev::launch_maybe_early(rmsnorm_kernel<kF32, 8>, a, s, st);
+}
+
+int rmsnorm_ctas_per_sm(int dtype, int threads, int vectors, size_t smem) {
+  int n = 0;
+  cudaError_t e;
+  if (dtype == kBF16)
+    e = vectors <= 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rmsnorm_kernel<kBF16, 4>, threads, smem)
+                     : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rmsnorm_kernel<kBF16, 8>, threads, smem);
+  else
+    e = vectors <= 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rmsnorm_kernel<kF32, 4>, threads, smem)
+                     : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rmsnorm_kernel<kF32, 8>, threads, smem);
+  return e == cudaSuccess ? n : 0;
 }
 
 }  // namespace tccl

@@ -149,3 +149,30 @@ def test_random_call(groups, case):
     eps = float(rng.choice([1e-6, 1e-5, 0.25]))
     in_place = bool(rng.random() < 0.3)
     run(groups(p), dtype, p, rows, hidden, eps=eps, cap=cap, in_place=in_place, seed=case)
+
+
+@pytest.mark.parametrize("cap,rows", [(4, 4), (4, 5), (4, 9), (1, 7), (3, 300), (0, 700), (0, 4096)])
+def test_row_claiming_back_to_back(groups, cap, rows):
+    """With more rows than CTAs the fused kernel's CTAs claim rows from a
+    counter that the last CTA resets for the next launch: three calls on
+    different data, enqueued back to back with no synchronisation between
+    them, each equal to the oracle (rows = CTAs takes no counter)."""
+    p, hidden = 8, 1024
+    g = groups(p)
+    cases = []
+    for k in range(3):
+        xs = datagen.rank_buffers("normal_bf16", 60 + k, p, rows * hidden)
+        gamma = datagen.rank_buffers("normal_bf16", 70 + k, 1, hidden)[0]
+        sends = [to_device(x).view(rows, hidden) for x in xs]
+        recvs = [torch.empty_like(s) for s in sends]
+        cases.append((xs, gamma, sends, recvs, to_device(gamma)))
+    for xs, gamma, sends, recvs, gamma_d in cases:
+        g.all_reduce_rmsnorm(sends, recvs, gamma_d, eps=1e-6, cta_cap=cap)
+    torch.cuda.synchronize()
+    assert g.query_error() == tccl.tcclSuccess
+    if cap:
+        assert g.last_launch()["ctas"] <= cap
+    for k, (xs, gamma, sends, recvs, _) in enumerate(cases):
+        exp, exp64 = rn.allreduce_rmsnorm(xs, gamma, rows, hidden, 1e-6, "bf16")
+        for r in range(p):
+            check(to_host(recvs[r]).ravel(), exp, exp64, "bf16", f"call {k} cap {cap} rows {rows} rank {r}")
