@@ -164,7 +164,7 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
       aa.p.dst[0] = r_ptr[anchor];
       aa.wide = anchor_wide_ok(aa) ? 1 : 0;
       wide_folds += aa.wide;
-      const uint64_t per_cta = (uint64_t)kAnchorThreads * (aa.wide ? anchor_vectors_per_thread(P, true) : U);
+      const uint64_t per_cta = (uint64_t)kAnchorThreads * (aa.wide ? anchor_vectors_per_thread(P, true, dtype) : U);
       uint64_t grid = std::max<uint64_t>(1, (aa.nvec + per_cta - 1) / per_cta);
       grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
       fast_grid = std::max(fast_grid, (int)grid);
@@ -237,7 +237,7 @@ tcclResult_t run_copy_out_reduce_scatter(tcclGroup* g, const void* const* send, 
     aa.p.dst[k] = recv[k];
   }
   aa.wide = anchor_wide_ok(aa) ? 1 : 0;
-  const uint64_t per_cta = (uint64_t)kAnchorThreads * anchor_vectors_per_thread(P, aa.wide != 0);
+  const uint64_t per_cta = (uint64_t)kAnchorThreads * anchor_vectors_per_thread(P, aa.wide != 0, dtype);
   uint64_t grid = std::max<uint64_t>(1, (aa.nvec * P + per_cta - 1) / per_cta);
   grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);
   const int err = launch_anchor_reduce(dtype, op, aa, (int)grid, cap <= 0, stream);

@@ -189,26 +189,31 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
   }
 }
 
-// The same fold with 256-bit loads: each thread folds one 32-byte vector of
-// every rank at a time, the ranks in batches of four (NP = 4 or 8), so each
-// thread keeps as many bytes in flight as eight 128-bit loads with half the
-// load instructions. The two 16-byte halves of a vector have one accumulator
+// The same fold with 256-bit loads (P = 2, 4 or 8): each thread folds U
+// 32-byte vectors of every rank at a time, the ranks in batches of four (P =
+// 2: both at once), so each thread keeps as many bytes in flight as the
+// 128-bit form with half the load instructions (P = 2 with 4-byte types: U =
+// 2, twice as many). The two 16-byte halves of a vector have one accumulator
 // each and receive the ranks in ascending order, as above. Needs every source
 // and the destination 32-byte aligned after the head (the launcher checks);
 // an odd last 16-byte vector is folded by the grid's last thread.
-template <int DT, int OP, int NP, bool MIXED>
+template <int DT, int OP, int NP, int U, bool MIXED>
 __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_wide_kernel(const __grid_constant__ AnchorArgs a) {
-  static_assert(NP == 4 || NP == 8, "ranks go in batches of four");
-  constexpr int RB = 4;
+  static_assert(NP == 2 || NP == 4 || NP == 8, "a fixed rank count");
+  constexpr int RB = NP == 2 ? 2 : 4;
+  constexpr int P = NP;
   const uint32_t nthr = gridDim.x * blockDim.x;
   const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const uint32_t nvec = static_cast<uint32_t>(a.nvec);
   const uint32_t nwide = nvec / 2;
-  if (a.prefetch_first && threadIdx.x < static_cast<unsigned>(NP)) {
-    const uint32_t vs = blockIdx.x * blockDim.x;
-    if (vs < nwide)
-      bulk_prefetch_l2(static_cast<const char*>(a.p.src[threadIdx.x]) + a.head_bytes + static_cast<uint64_t>(vs) * 32,
-                       min(blockDim.x, nwide - vs) * 32u);
+  if (a.prefetch_first && threadIdx.x < static_cast<unsigned>(P)) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t vs = blockIdx.x * blockDim.x + u * nthr;
+      if (vs < nwide)
+        bulk_prefetch_l2(static_cast<const char*>(a.p.src[threadIdx.x]) + a.head_bytes + static_cast<uint64_t>(vs) * 32,
+                         min(blockDim.x, nwide - vs) * 32u);
+    }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -219,40 +224,52 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_wide_kernel(c
   for (int job = 0; job < a.njobs; ++job) {
     const uint64_t src_off = static_cast<uint64_t>(job) * a.job_src_stride + a.head_bytes;
     char* dst = static_cast<char*>(a.p.dst[job]) + a.head_bytes;
-    for (uint32_t v = gtid; v < nwide; v += nthr) {
-      Acc lo, hi;
+    for (uint32_t base = gtid; base < nwide; base += nthr * U) {
+      Acc lo[U], hi[U];
 #pragma unroll
-      for (int r0 = 0; r0 < NP; r0 += RB) {
-        uint4 xl[RB], xh[RB];
+      for (int r0 = 0; r0 < P; r0 += RB) {
+        uint4 xl[U][RB], xh[U][RB];
 #pragma unroll
-        for (int k = 0; k < RB; ++k)
-          ld_stream_v8(static_cast<const char*>(a.p.src[r0 + k]) + src_off + static_cast<uint64_t>(v) * 32,
-                       load_policy, xl[k], xh[k]);
+        for (int u = 0; u < U; ++u) {
+          const uint32_t v = base + u * nthr;
 #pragma unroll
-        for (int k = 0; k < RB; ++k) {
-          if (r0 + k == 0) {
-            lo.init(xl[k]);
-            hi.init(xh[k]);
-          } else {
-            lo.add(xl[k]);
-            hi.add(xh[k]);
+          for (int k = 0; k < RB; ++k)
+            if (v < nwide)
+              ld_stream_v8(static_cast<const char*>(a.p.src[r0 + k]) + src_off + static_cast<uint64_t>(v) * 32,
+                           load_policy, xl[u][k], xh[u][k]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (base + u * nthr >= nwide) continue;
+#pragma unroll
+          for (int k = 0; k < RB; ++k) {
+            if (r0 + k == 0) {
+              lo[u].init(xl[u][k]);
+              hi[u].init(xh[u][k]);
+            } else {
+              lo[u].add(xl[u][k]);
+              hi[u].add(xh[u][k]);
+            }
           }
         }
       }
-      st_keep_v8(dst + static_cast<uint64_t>(v) * 32, lo.out(), hi.out(), store_policy);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t v = base + u * nthr;
+        if (v < nwide) st_keep_v8(dst + static_cast<uint64_t>(v) * 32, lo[u].out(), hi[u].out(), store_policy);
+      }
     }
     if ((nvec & 1) && gtid == nthr - 1) {
       const uint64_t last = static_cast<uint64_t>(nvec - 1) * 16;
       Acc acc;
-#pragma unroll
-      for (int k = 0; k < NP; ++k) {
+      for (int k = 0; k < P; ++k) {
         const uint4 x = ld_stream_v4<true>(static_cast<const char*>(a.p.src[k]) + src_off + last, load_policy);
         if (k == 0) acc.init(x);
         else acc.add(x);
       }
       st_keep_v4<true>(dst + last, acc.out(), store_policy);
     }
-    anchor_edges<DT, OP>(a, job, NP, gtid);
+    anchor_edges<DT, OP>(a, job, P, gtid);
   }
 }
 
@@ -266,12 +283,22 @@ int launch_anchor_t(const AnchorArgs& args, int grid, bool early, cudaStream_t s
   s.smem = 0;
   s.early_launch = early ? 1 : 0;
   constexpr bool kCanMix = D == kBF16 && O == kSum;
-  if (a.wide && (a.nranks == 4 || a.nranks == 8)) {
-    if (kCanMix && a.mixed_bf16)
-      return a.nranks == 8 ? launch_maybe_early(anchor_reduce_wide_kernel<D, O, 8, kCanMix>, a, s, st)
-                           : launch_maybe_early(anchor_reduce_wide_kernel<D, O, 4, kCanMix>, a, s, st);
-    return a.nranks == 8 ? launch_maybe_early(anchor_reduce_wide_kernel<D, O, 8, false>, a, s, st)
-                         : launch_maybe_early(anchor_reduce_wide_kernel<D, O, 4, false>, a, s, st);
+  if (a.wide) {
+    // P = 2: two vectors per thread where the accumulators allow (bf16 sums
+    // hold 16 fp32 accumulators per vector: one)
+    constexpr int U2 = anchor_wide_vectors(2, D);
+    if (kCanMix && a.mixed_bf16) {
+      switch (a.nranks) {
+        case 2: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 2, U2, kCanMix>, a, s, st);
+        case 4: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 4, 1, kCanMix>, a, s, st);
+        default: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 8, 1, kCanMix>, a, s, st);
+      }
+    }
+    switch (a.nranks) {
+      case 2: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 2, U2, false>, a, s, st);
+      case 4: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 4, 1, false>, a, s, st);
+      default: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 8, 1, false>, a, s, st);
+    }
   }
   if (kCanMix && a.mixed_bf16) {
     switch (a.nranks) {
@@ -293,8 +320,9 @@ int launch_anchor_t(const AnchorArgs& args, int grid, bool early, cudaStream_t s
 }  // namespace
 }  // namespace dev
 
-int anchor_vectors_per_thread(int nranks, bool wide) {
-  return (wide || nranks == 2 || nranks == 4) ? 2 : 1;
+int anchor_vectors_per_thread(int nranks, bool wide, int dtype) {
+  if (wide) return 2 * anchor_wide_vectors(nranks, dtype);
+  return (nranks == 2 || nranks == 4) ? 2 : 1;
 }
 
 bool anchor_wide_ok(const AnchorArgs& a) {
@@ -302,7 +330,7 @@ bool anchor_wide_ok(const AnchorArgs& a) {
     const char* e = std::getenv("TCCL_ANCHOR_WIDE");
     return !(e && std::string(e) == "0");
   }();
-  if (!enabled || (a.nranks != 4 && a.nranks != 8)) return false;
+  if (!enabled || (a.nranks != 2 && a.nranks != 4 && a.nranks != 8)) return false;
   for (int j = 0; j < a.njobs; ++j) {
     const uint64_t off = static_cast<uint64_t>(j) * a.job_src_stride + a.head_bytes;
     for (int k = 0; k < a.nranks; ++k)
