@@ -884,6 +884,21 @@ def sweep(args):
                 row["cpu_cores"] = ncores
             emit(**row)
         g.close()
+    # the rank count at a fixed size: bf16 sum, 32 Mi elements (64 MiB) per
+    # rank, uncapped and at a 16-CTA cap (Auto's engine). Timing only: the
+    # inputs are torch's N(0, 1) draws, and parity at these rank counts is
+    # the GPU tests' job
+    if only and "vs_p" in only:
+        n = 32 << 20
+        for p in (2, 3, 4, 8, 16, 32, 64):
+            g = tccl.Group(p)
+            sends = [torch.randn(n, device=dev).to(torch.bfloat16) for _ in range(p)]
+            recvs = [torch.empty_like(t) for t in sends]
+            for cap in (0, 16):
+                emit(**run_point("vs_P", g, "AR", p, n, "bf16", "sum", sends, recvs, cap=cap, sms=cap > 0))
+            g.close()
+            del sends, recvs
+            torch.cuda.empty_cache()
 
 
 # ------------------------------------------------------------------ overlap mode
@@ -1346,7 +1361,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="measure every configuration point of C1..C5 (one JSON line each)")
-    ap.add_argument("--sweep-configs", default="", help="comma list, e.g. c3,c5")
+    ap.add_argument("--sweep-configs", default="",
+                    help="comma list, e.g. c3,c5 (default c1..c5); vs_p: allreduce over P = 2..64 at "
+                         "64 MiB per rank, uncapped and at cap 16")
     ap.add_argument("--c3-bytes", default="",
                     help="C3 sizes per rank in bytes for --sweep, comma separated (default 4 KiB ... 256 MiB)")
     ap.add_argument("--overlap", action="store_true",
