@@ -675,7 +675,11 @@ def sweep(args):
         with torch.cuda.graph(g, stream=stream):
             for _ in range(reps):
                 fn()
-        t = ev_stats(g.replay, 30.0)[0] / reps
+        def replay():
+            with torch.cuda.stream(stream):  # the timed stream (replay uses the current one)
+                g.replay()
+
+        t = ev_stats(replay, 30.0)[0] / reps
         del g
         return t
 
