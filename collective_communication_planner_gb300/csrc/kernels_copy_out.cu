@@ -189,19 +189,20 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
   }
 }
 
-// The same fold with 256-bit loads (P = 2 or a multiple of 4; NP = 0: the
-// rank count at run time): each thread folds U 32-byte vectors of every rank
-// at a time, the ranks in batches of four (P = 2: both at once), so each
-// thread keeps as many bytes in flight as the 128-bit form with half the load
-// instructions (P = 2 with 4-byte types: U = 2, twice as many). The two
+// The same fold with 256-bit loads (P = 2, 3, 6 or a multiple of 4; NP = 0:
+// a multiple of 4 read at run time): each thread folds U 32-byte vectors of
+// every rank at a time, the ranks in batches of four (P = 2 and 3: all at
+// once; P = 6: two batches of three), so each thread keeps as many bytes in
+// flight as the 128-bit form with half the load instructions (P = 2 with
+// 4-byte types: U = 2, twice as many; P = 3 and 6: 96 bytes). The two
 // 16-byte halves of a vector have one accumulator each and receive the ranks
 // in ascending order, as above. Needs every source and the destination
 // 32-byte aligned after the head (the launcher checks); an odd last 16-byte
 // vector is folded by the grid's last thread.
 template <int DT, int OP, int NP, int U, bool MIXED>
 __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_wide_kernel(const __grid_constant__ AnchorArgs a) {
-  static_assert(NP == 0 || NP == 2 || NP % 4 == 0, "P = 2 or whole batches of four");
-  constexpr int RB = NP == 2 ? 2 : 4;
+  static_assert(NP == 0 || NP == 2 || NP == 3 || NP == 6 || NP % 4 == 0, "whole batches");
+  constexpr int RB = NP == 2 ? 2 : (NP == 3 || NP == 6) ? 3 : 4;
   const int P = NP > 0 ? NP : a.nranks;
   const uint32_t nthr = gridDim.x * blockDim.x;
   const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
@@ -291,7 +292,9 @@ int launch_anchor_t(const AnchorArgs& args, int grid, bool early, cudaStream_t s
     if (kCanMix && a.mixed_bf16) {
       switch (a.nranks) {
         case 2: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 2, U2, kCanMix>, a, s, st);
+        case 3: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 3, 1, kCanMix>, a, s, st);
         case 4: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 4, 1, kCanMix>, a, s, st);
+        case 6: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 6, 1, kCanMix>, a, s, st);
         case 8: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 8, 1, kCanMix>, a, s, st);
         case 16: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 16, 1, kCanMix>, a, s, st);
         default: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 0, 1, kCanMix>, a, s, st);
@@ -299,7 +302,9 @@ int launch_anchor_t(const AnchorArgs& args, int grid, bool early, cudaStream_t s
     }
     switch (a.nranks) {
       case 2: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 2, U2, false>, a, s, st);
+      case 3: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 3, 1, false>, a, s, st);
       case 4: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 4, 1, false>, a, s, st);
+      case 6: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 6, 1, false>, a, s, st);
       case 8: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 8, 1, false>, a, s, st);
       case 16: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 16, 1, false>, a, s, st);
       default: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 0, 1, false>, a, s, st);
@@ -335,7 +340,8 @@ bool anchor_wide_ok(const AnchorArgs& a) {
     const char* e = std::getenv("TCCL_ANCHOR_WIDE");
     return !(e && std::string(e) == "0");
   }();
-  if (!enabled || (a.nranks != 2 && (a.nranks < 4 || a.nranks % 4))) return false;
+  const int P = a.nranks;
+  if (!enabled || !(P == 2 || P == 3 || P == 6 || (P >= 4 && P % 4 == 0))) return false;
   for (int j = 0; j < a.njobs; ++j) {
     const uint64_t off = static_cast<uint64_t>(j) * a.job_src_stride + a.head_bytes;
     for (int k = 0; k < a.nranks; ++k)
