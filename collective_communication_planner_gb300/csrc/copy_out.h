@@ -29,7 +29,7 @@ struct AnchorArgs {
   int nranks;
   int prefetch_first;  // set by the launcher for early launches: warm L2 before the wait
   int mixed_bf16;      // bf16 sums: fold with the mixed-precision add (same bits, fewer instructions)
-  int wide;            // 256-bit loads (P = 2, 3, 6 or a multiple of 4; see anchor_wide_ok)
+  int wide;            // 256-bit loads (P = 2 to 8 or a multiple of 4; see anchor_wide_ok)
 };
 
 // 32-byte vectors each thread folds at a time with 256-bit loads: two for
@@ -40,7 +40,7 @@ constexpr int anchor_wide_vectors(int nranks, int dtype) {
 // 16-byte vectors each thread folds at a time: two for P = 2 and 4, one
 // otherwise; with 256-bit loads, twice anchor_wide_vectors.
 int anchor_vectors_per_thread(int nranks, bool wide = false, int dtype = kBF16);
-// Whether a fold can take 256-bit loads: P = 2, 3, 6 or a multiple of 4, and every source and
+// Whether a fold can take 256-bit loads: P = 2 to 8 or a multiple of 4, and every source and
 // destination of every job 32-byte aligned once the head is skipped.
 // TCCL_ANCHOR_WIDE=0 turns them off (the same bits either way).
 bool anchor_wide_ok(const AnchorArgs& a);

@@ -189,19 +189,19 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_kernel(const 
   }
 }
 
-// The same fold with 256-bit loads (P = 2, 3, 6 or a multiple of 4; NP = 0:
-// a multiple of 4 read at run time): each thread folds U 32-byte vectors of
-// every rank at a time, the ranks in batches of four (P = 2 and 3: all at
-// once; P = 6: two batches of three), so each thread keeps as many bytes in
-// flight as the 128-bit form with half the load instructions (P = 2 with
-// 4-byte types: U = 2, twice as many; P = 3 and 6: 96 bytes). The two
+// The same fold with 256-bit loads (P = 2 to 8, 16, or a multiple of 4 read
+// at run time, NP = 0): each thread folds U 32-byte vectors of every rank at
+// a time, the ranks in batches of four (P = 2 and 3: all at once; P = 6: two
+// batches of three; P = 5 and 7: four, then the rest), so each thread keeps
+// as many bytes in flight as the 128-bit form with half the load
+// instructions (P = 2 with 4-byte types: U = 2, twice as many). The two
 // 16-byte halves of a vector have one accumulator each and receive the ranks
 // in ascending order, as above. Needs every source and the destination
 // 32-byte aligned after the head (the launcher checks); an odd last 16-byte
 // vector is folded by the grid's last thread.
 template <int DT, int OP, int NP, int U, bool MIXED>
 __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_wide_kernel(const __grid_constant__ AnchorArgs a) {
-  static_assert(NP == 0 || NP == 2 || NP == 3 || NP == 6 || NP % 4 == 0, "whole batches");
+  static_assert(NP == 0 || (NP >= 2 && NP <= 8) || NP == 16, "a batched rank count");
   constexpr int RB = NP == 2 ? 2 : (NP == 3 || NP == 6) ? 3 : 4;
   const int P = NP > 0 ? NP : a.nranks;
   const uint32_t nthr = gridDim.x * blockDim.x;
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_wide_kernel(c
     char* dst = static_cast<char*>(a.p.dst[job]) + a.head_bytes;
     for (uint32_t base = gtid; base < nwide; base += nthr * U) {
       Acc lo[U], hi[U];
-#pragma unroll (NP > 0 ? NP / RB : 1)
+#pragma unroll (NP > 0 ? (NP + RB - 1) / RB : 1)
       for (int r0 = 0; r0 < P; r0 += RB) {
         uint4 xl[U][RB], xh[U][RB];
 #pragma unroll
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_wide_kernel(c
           const uint32_t v = base + u * nthr;
 #pragma unroll
           for (int k = 0; k < RB; ++k)
-            if (v < nwide)
+            if (v < nwide && (NP == 0 || r0 + k < NP))
               ld_stream_v8(static_cast<const char*>(a.p.src[r0 + k]) + src_off + static_cast<uint64_t>(v) * 32,
                            load_policy, xl[u][k], xh[u][k]);
         }
@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(kAnchorThreads, 1) anchor_reduce_wide_kernel(c
           if (base + u * nthr >= nwide) continue;
 #pragma unroll
           for (int k = 0; k < RB; ++k) {
+            if (NP > 0 && r0 + k >= NP) break;
             if (r0 + k == 0) {
               lo[u].init(xl[u][k]);
               hi[u].init(xh[u][k]);
@@ -294,7 +295,9 @@ int launch_anchor_t(const AnchorArgs& args, int grid, bool early, cudaStream_t s
         case 2: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 2, U2, kCanMix>, a, s, st);
         case 3: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 3, 1, kCanMix>, a, s, st);
         case 4: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 4, 1, kCanMix>, a, s, st);
+        case 5: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 5, 1, kCanMix>, a, s, st);
         case 6: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 6, 1, kCanMix>, a, s, st);
+        case 7: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 7, 1, kCanMix>, a, s, st);
         case 8: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 8, 1, kCanMix>, a, s, st);
         case 16: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 16, 1, kCanMix>, a, s, st);
         default: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 0, 1, kCanMix>, a, s, st);
@@ -304,7 +307,9 @@ int launch_anchor_t(const AnchorArgs& args, int grid, bool early, cudaStream_t s
       case 2: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 2, U2, false>, a, s, st);
       case 3: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 3, 1, false>, a, s, st);
       case 4: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 4, 1, false>, a, s, st);
+      case 5: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 5, 1, false>, a, s, st);
       case 6: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 6, 1, false>, a, s, st);
+      case 7: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 7, 1, false>, a, s, st);
       case 8: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 8, 1, false>, a, s, st);
       case 16: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 16, 1, false>, a, s, st);
       default: return launch_maybe_early(anchor_reduce_wide_kernel<D, O, 0, 1, false>, a, s, st);
@@ -341,7 +346,7 @@ bool anchor_wide_ok(const AnchorArgs& a) {
     return !(e && std::string(e) == "0");
   }();
   const int P = a.nranks;
-  if (!enabled || !(P == 2 || P == 3 || P == 6 || (P >= 4 && P % 4 == 0))) return false;
+  if (!enabled || !((P >= 2 && P <= 8) || (P > 8 && P % 4 == 0))) return false;
   for (int j = 0; j < a.njobs; ++j) {
     const uint64_t off = static_cast<uint64_t>(j) * a.job_src_stride + a.head_bytes;
     for (int k = 0; k < a.nranks; ++k)

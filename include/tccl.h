@@ -97,7 +97,7 @@ typedef enum {
                               4 MiB per rank buffer, for allreduce / all-gather when the cap is
                               at most ce_auto_max_cap CTAs, and for reduce-scatter under any cap
                               or uncapped with P <= 4. The segment kernel folds with register
-                              loads (128-bit, or 256-bit for P = 2, 3, 6 or a multiple of 4
+                              loads (128-bit, or 256-bit for P = 2 to 8 or a multiple of 4
                               with every buffer 32-byte aligned past the head) when the send
                               buffers and the anchor's receive buffer share their address mod
                               16, else with the bulk engine's TMA pipeline. */
@@ -211,7 +211,7 @@ typedef struct {
   int ce_segments;     /* copy-out engine: kernel launches (segments) of the call (0 otherwise) */
   int ce_copies;       /* copy-out engine: device-to-device copies enqueued (0 otherwise) */
   int ce_wide_folds;   /* copy-out engine: register-fold launches that read with 256-bit loads
-                          (P = 2, 3, 6 or a multiple of 4, every buffer 32-byte aligned past the head; the same
+                          (P = 2 to 8 or a multiple of 4, every buffer 32-byte aligned past the head; the same
                           bits as the 128-bit loads, which TCCL_ANCHOR_WIDE=0 in the process's
                           environment keeps); 0 otherwise */
 } tcclLaunchInfo_t;

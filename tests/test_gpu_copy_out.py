@@ -532,12 +532,12 @@ def test_tma_reduce_fold_falls_back_for_other_pairs(groups):
     check(got, oracle.allreduce(xs, "bf16", "sum", nthreads=0), "bf16 sum under ce_fold 3")
 
 
-@pytest.mark.parametrize("p", [2, 3, 4, 6, 8, 12, 16])
+@pytest.mark.parametrize("p", [2, 3, 4, 5, 6, 7, 8, 12, 16])
 @pytest.mark.parametrize("dtype,op", [("bf16", "sum"), ("f32", "sum"), ("i32", "max"), ("bf16", "min")])
 @pytest.mark.parametrize("case", ["aligned", "odd_vectors", "head_32", "head_16"])
 def test_wide_fold_layouts(groups, p, dtype, op, case):
-    """The register fold's 256-bit loads (P = 2, 3, 6 or a multiple of 4,
-    here 12 with the rank count read at run time; every buffer 32-byte
+    """The register fold's 256-bit loads (P = 2 to 8, 16, or a multiple of 4
+    read at run time, here 12; every buffer 32-byte
     aligned past the head): an even and an odd count of 16-byte vectors (the
     odd last one folded on its own), and a head that leaves the body 32-byte
     aligned; a head that leaves it only 16-byte aligned takes the 128-bit
@@ -559,18 +559,18 @@ def test_wide_fold_layouts(groups, p, dtype, op, case):
     check(got, oracle.allreduce(xs, dtype, op, nthreads=0), f"wide fold {case} {dtype} {op} P={p}")
 
 
-@pytest.mark.parametrize("p", [2, 3, 4, 5, 8, 12, 16])
+@pytest.mark.parametrize("p", [2, 3, 4, 5, 8, 9, 12, 16])
 @pytest.mark.parametrize("rc", [40_000, 40_008])
 def test_wide_fold_reduce_scatter(groups, p, rc):
     """Reduce-scatter on the register fold: shards of a multiple of 32 bytes
     keep every job 32-byte aligned and take the 256-bit loads; shards of an
     odd multiple of 16 bytes leave every other job 16 bytes off and take the
-    128-bit loads, as P = 5 does always. All exact."""
+    128-bit loads, as P = 9 does always. All exact."""
     g = groups(p)
     reset_config(g, engine=CE)
     xs = datagen.rank_buffers("normal_bf16", 42, p, p * rc)
     got = reduce_scatter(g, xs, rc, "bf16", "sum", cap=8)
     info = g.last_launch()
     assert info["engine"] == CE and info["ce_copies"] == 0, info
-    assert info["ce_wide_folds"] == (1 if rc * 2 % 32 == 0 and p != 5 else 0), info
+    assert info["ce_wide_folds"] == (1 if rc * 2 % 32 == 0 and p != 9 else 0), info
     check(got, oracle.reduce_scatter(xs, "bf16", "sum", nthreads=0), f"RS wide rc={rc} P={p}")
