@@ -177,15 +177,17 @@ Config resolve_config(const Config& in) {
 
 int copy_out_auto_max_cap(const Config& c, int sm_count, int nranks) {
   if (c.ce_auto_max_cap > 0) return c.ce_auto_max_cap;
-  // allreduce / all-gather: where the copy-out engine stays ahead of the
-  // SM-only bulk engine grows with P (the copy engines take P - 1 of the P
-  // stores). GB300 allreduce, share of the HBM peak, copy-out / SM only:
-  // P = 8, 128 MiB per rank: cap 48 0.787 / 0.662, 56 0.821 / 0.756,
-  // 64 0.820 / 0.836; P = 4, 64 MiB: cap 48 0.669 / 0.639, 56 0.696 / 0.726.
-  // P = 2: ahead up to 48 (the engine's first sweep).
-  if (nranks <= 2) return sm_count * 5 / 16;
-  if (nranks <= 4) return sm_count / 3;
-  return sm_count * 3 / 8;
+  // allreduce / all-gather: the cap up to which the copy-out engine (its
+  // fold with 256-bit loads) stays ahead of the SM-only bulk engine. GB300
+  // allreduce, bf16, 128 MiB per rank, share of the HBM peak, copy-out / SM
+  // only: P = 2 cap 80 0.705 / 0.664, 96 0.718 / 0.786; P = 3 cap 60
+  // 0.729 / 0.690, 64 0.731 / 0.732; P = 4 cap 60 0.800 / 0.780, 64
+  // 0.806 / 0.820; P = 5 cap 68 0.816 / 0.809, 72 0.758 / 0.842; P = 8 cap
+  // 66 0.859 / 0.846, 68 0.855 / 0.865. (A copy-out all-gather uses no SM
+  // and stays ahead further.)
+  if (nranks <= 2) return sm_count * 4 / 7;
+  if (nranks <= 4) return sm_count * 5 / 12;
+  return sm_count * 7 / 16;
 }
 
 bool copy_out_chosen(const Config& c, int sm_count, int nranks, int coll, size_t count, int es,

@@ -139,8 +139,8 @@ bool copy_out_chosen(const Config& c, int sm_count, int nranks, int coll, size_t
                      int cap);
 
 // The largest cap for which Auto picks the copy-out engine for an allreduce
-// or all-gather: ce_auto_max_cap when set, else 5/16 of the SMs for P <= 2,
-// 1/3 for P = 3 and 4, 3/8 for P >= 5 (47, 50 and 57 on 152 SMs).
+// or all-gather: ce_auto_max_cap when set, else 4/7 of the SMs for P <= 2,
+// 5/12 for P = 3 and 4, 7/16 for P >= 5 (86, 63 and 66 on 152 SMs).
 int copy_out_auto_max_cap(const Config& c, int sm_count, int nranks);
 
 // Segments of a copy-out allreduce of `count` elements: at most

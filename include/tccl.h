@@ -165,8 +165,8 @@ typedef struct {
                               28 MiB; a call is cut into at least four segments of at least
                               4 MiB where it can be; rounded down to a multiple of 256) */
   int ce_auto_max_cap;     /* Auto picks the copy-out engine for caps up to this many CTAs
-                              (0: by the rank count, 5/16 of the SMs for P <= 2, 1/3 for P = 3
-                              and 4, 3/8 for P >= 5; negative: never) */
+                              (0: by the rank count, 4/7 of the SMs for P <= 2, 5/12 for P = 3
+                              and 4, 7/16 for P >= 5; negative: never) */
   int reduce_order;        /* tcclReduceOrder_t (default ascending) */
   int ce_fold;             /* copy-out allreduce, the kernel that folds each segment into the anchor:
                               0 or 1: the register-load fold where every send buffer

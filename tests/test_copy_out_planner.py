@@ -42,15 +42,15 @@ def per_rank_bytes(coll, p, count, es):
 
 
 def auto_max_cap(p):
-    return SMS * 5 // 16 if p <= 2 else (SMS // 3 if p <= 4 else SMS * 3 // 8)
+    return SMS * 4 // 7 if p <= 2 else (SMS * 5 // 12 if p <= 4 else SMS * 7 // 16)
 
 
 @pytest.mark.parametrize("coll,p,mib,cap", list(itertools.product(
-    [AR, RS, AG], [1, 2, 3, 4, 5, 8], [2, 4, 64], [0, 8, 47, 48, 50, 51, 57, 58])))
+    [AR, RS, AG], [1, 2, 3, 4, 5, 8], [2, 4, 64], [0, 8, 47, 63, 64, 66, 67, 86, 87])))
 def test_auto_choice(coll, p, mib, cap):
     """Auto's rule: P >= 2 and at least 4 MiB per rank buffer; allreduce and
-    all-gather under a cap of at most 5/16 of the SMs for P <= 2 (47 of 152),
-    1/3 for P = 3 and 4 (50), 3/8 for P >= 5 (57); reduce-scatter under any
+    all-gather under a cap of at most 4/7 of the SMs for P <= 2 (86 of 152),
+    5/12 for P = 3 and 4 (63), 7/16 for P >= 5 (66); reduce-scatter under any
     cap, or uncapped for P <= 4."""
     es = 2
     count = mib * MiB // es // (1 if coll == AR else p)
@@ -81,9 +81,9 @@ def test_engine_setting_and_auto_limit():
     assert inspect(RS, p, count // p, cap=16, cfg=config(ce_auto_max_cap=-1))[0] == 0
     assert inspect(AR, p, count, cap=100, cfg=config(ce_auto_max_cap=100))[0] == 1
     assert inspect(AR, p, count, cap=101, cfg=config(ce_auto_max_cap=100))[0] == 0
-    # the limit scales with the device: 132 SMs -> 132 * 3 // 8 = 49 for P = 8
-    assert inspect(AR, p, count, cap=49, sm_count=132)[0] == 1
-    assert inspect(AR, p, count, cap=50, sm_count=132)[0] == 0
+    # the limit scales with the device: 132 SMs -> 132 * 7 // 16 = 57 for P = 8
+    assert inspect(AR, p, count, cap=57, sm_count=132)[0] == 1
+    assert inspect(AR, p, count, cap=58, sm_count=132)[0] == 0
 
 
 @pytest.mark.parametrize("dt", [BF16, F32])

@@ -282,7 +282,7 @@ def test_auto_picks_copy_out_for_large_capped_calls(groups):
     sends = [torch.ones(n, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
     recvs = [torch.empty_like(s) for s in sends]
     picks = {}
-    edge = torch.cuda.get_device_properties(0).multi_processor_count // 3  # P = 4
+    edge = torch.cuda.get_device_properties(0).multi_processor_count * 5 // 12  # P = 4
     for cap in (0, 8, 16, edge, edge + 1, 2 * edge):
         g.all_reduce(sends, recvs, cta_cap=cap)
         picks[cap] = g.last_launch()["engine"]
