@@ -293,7 +293,7 @@ def test_auto_picks_copy_out_for_large_capped_calls(groups):
     reset_config(g, ce_auto_max_cap=-1)
     g.all_reduce(sends, recvs, cta_cap=8)
     assert g.last_launch()["engine"] == tccl.tcclEngineBulk
-    reset_config(g, ce_auto_max_cap=100)
+    reset_config(g, ce_auto_max_cap=2 * edge)
     g.all_reduce(sends, recvs, cta_cap=2 * edge)
     assert g.last_launch()["engine"] == CE
     torch.cuda.synchronize()
