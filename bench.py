@@ -977,6 +977,8 @@ def overlap(args):
     otype = "f32" if xs[0].dtype == np.float32 else "bf16"
     exp = oracle.allreduce([x[idx].copy() for x in xs], otype, "sum")[0]
     for cap in args.overlap_caps:
+        for _ in range(3):  # warm: a new cap's first call may create copy streams and events
+            ar(cap)
         _, ar_alone = timed(None, lambda: ar(cap))
         for t in recvs:
             t.zero_()
