@@ -115,7 +115,7 @@ def _open():
         "tcclGroupInjectWaitTimeout": (i, [vp, i, ctypes.c_double]),
         "tcclCopyOutInspect": (i, [i, i, pvp, pvp, sz, i, i, i, ctypes.POINTER(tcclConfig_t),
                                    ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i),
-                                   ctypes.POINTER(sz)]),
+                                   ctypes.POINTER(sz), ctypes.POINTER(i)]),
         "tcclAllReduceNoAlloc": (i, [i, pvp, pvp, sz, i, i, vp, i]),
         "tcclAllReduceRMSNorm": (i, [vp, pvp, pvp, sz, sz, vp, ctypes.c_float, i, vp, i]),
         "tcclReshard": (i, [vp, pvp, ctypes.POINTER(tcclLayout_t), pvp,
@@ -325,15 +325,16 @@ def tcclPlanInspect(coll, nranks, sendbufs, recvbufs, count, datatype, cta_cap=0
 def tcclCopyOutInspect(coll, nranks, sendbufs, recvbufs, count, datatype, cta_cap=0,
                        sm_count=152, cfg=None):
     """The copy-out engine's decisions on the host only. Returns (result,
-    copy_out, register_fold, segments, segment_elems)."""
+    copy_out, register_fold, segments, segment_elems, wide_folds)."""
     sp, _k1 = _ptr_array(sendbufs)
     rp, _k2 = _ptr_array(recvbufs)
-    co, rf, ns = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    co, rf, ns, wf = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     se = ctypes.c_size_t()
     r = _lib.tcclCopyOutInspect(coll, nranks, sp, rp, count, datatype, cta_cap, sm_count,
                                 ctypes.byref(cfg) if cfg is not None else None, ctypes.byref(co),
-                                ctypes.byref(rf), ctypes.byref(ns), ctypes.byref(se))
-    return r, co.value, rf.value, ns.value, se.value
+                                ctypes.byref(rf), ctypes.byref(ns), ctypes.byref(se),
+                                ctypes.byref(wf))
+    return r, co.value, rf.value, ns.value, se.value, wf.value
 
 
 # ---------------------------------------------------------------- torch-facing wrapper

@@ -912,13 +912,14 @@ tcclResult_t tcclGroupInjectWaitTimeout(tcclGroup_t g, int enable, double timeou
 tcclResult_t tcclCopyOutInspect(int coll, int nranks, const void* const sendbufs[],
                                 void* const recvbufs[], size_t count, tcclDataType_t datatype,
                                 int cta_cap, int sm_count, const tcclConfig_t* cfg, int* copy_out,
-                                int* register_fold, int* segments, size_t* segment_elems) {
-  if (!copy_out || !register_fold || !segments || !segment_elems || sm_count < 1)
+                                int* register_fold, int* segments, size_t* segment_elems,
+                                int* wide_folds) {
+  if (!copy_out || !register_fold || !segments || !segment_elems || !wide_folds || sm_count < 1)
     return tcclInvalidArgument;
   if (cfg && !config_ok(*cfg)) return tcclInvalidArgument;
   tcclResult_t v = (tcclResult_t)validate_collective_args(coll, nranks, sendbufs, recvbufs, count, datatype, 0);
   if (v != tcclSuccess) return v;
-  *copy_out = *register_fold = *segments = 0;
+  *copy_out = *register_fold = *segments = *wide_folds = 0;
   *segment_elems = 0;
   if (count == 0 || is_noop(coll, nranks, sendbufs, recvbufs)) return tcclSuccess;
   const int es = elem_size_of(datatype);
@@ -934,11 +935,23 @@ tcclResult_t tcclCopyOutInspect(int coll, int nranks, const void* const sendbufs
     *segments = nseg;
     *segment_elems = seg;
     *register_fold = allreduce_register_fold(c, nranks, sm.data(), rm.data(), count, es, seg) ? 1 : 0;
+    // the fold's arguments segment by segment, as the call would make them
+    for (int k = 0; k < nseg && *register_fold; ++k) {
+      AnchorArgs a;
+      allreduce_segment_args(&a, nranks, sendbufs, recvbufs[0], (size_t)k * seg,
+                             k == nseg - 1 ? count - (size_t)k * seg : seg, es);
+      *wide_folds += a.wide;
+    }
   } else if (coll == kReduceScatter) {
     *register_fold = register_fold_ok(coll, nranks, sm.data(), rm.data(), count, es, 0) ? 1 : 0;
     *copy_out = *register_fold;  // otherwise the bulk engine runs it
     *segments = *register_fold;
     *segment_elems = *register_fold ? count : 0;
+    if (*register_fold) {
+      AnchorArgs a;
+      reduce_scatter_args(&a, nranks, sendbufs, recvbufs, count, es);
+      *wide_folds = a.wide;
+    }
   }
   return tcclSuccess;
 }

@@ -44,6 +44,16 @@ int anchor_vectors_per_thread(int nranks, bool wide = false, int dtype = kBF16);
 // destination of every job 32-byte aligned once the head is skipped.
 // TCCL_ANCHOR_WIDE=0 turns them off (the same bits either way).
 bool anchor_wide_ok(const AnchorArgs& a);
+// The register fold's arguments (rank count, jobs, pointers, head / vectors /
+// tail split and the 256-bit choice; not sm_mask or mixed_bf16) for one
+// allreduce segment, elements [off, off + n) of every send buffer into the
+// anchor's receive buffer, all sharing the anchor's address mod 16 ...
+void allreduce_segment_args(AnchorArgs* a, int nranks, const void* const* send,
+                            void* anchor_recv, size_t off, size_t n, int es);
+// ... and for a reduce-scatter, shard j of every send buffer into recv[j]
+// (rc elements each, every buffer sharing recv[0]'s address mod 16).
+void reduce_scatter_args(AnchorArgs* a, int nranks, const void* const* send,
+                         void* const* recv, size_t rc, int es);
 // early: programmatic dependent launch (uncapped calls only: a capped call
 // must not hold SMs beyond its cap while it waits)
 int launch_anchor_reduce(int dtype, int op, const AnchorArgs& a, int grid, bool early,

@@ -92,6 +92,39 @@ int join_ce_streams(tcclGroup* g, int used, cudaStream_t stream) {
 // The shard-in kernel is the register-load anchor fold when every send buffer
 // and the anchor's receive buffer share their address mod 16, else the bulk
 // engine's TMA pipeline with every window pointed at the anchor.
+void allreduce_segment_args(AnchorArgs* a, int nranks, const void* const* send,
+                            void* anchor_recv, size_t off, size_t n, int es) {
+  std::memset(a, 0, sizeof(*a));
+  a->nranks = nranks;
+  a->njobs = 1;
+  const uintptr_t mod = (uintptr_t)anchor_recv & 15;
+  const size_t bytes = n * es;
+  a->head_bytes = std::min(bytes, (size_t)((16 - mod) & 15));
+  a->nvec = (bytes - a->head_bytes) / 16;
+  a->tail_bytes = bytes - a->head_bytes - a->nvec * 16;
+  for (int k = 0; k < nranks; ++k) a->p.src[k] = static_cast<const char*>(send[k]) + off * es;
+  a->p.dst[0] = static_cast<char*>(anchor_recv) + off * es;
+  a->wide = anchor_wide_ok(*a) ? 1 : 0;
+}
+
+void reduce_scatter_args(AnchorArgs* a, int nranks, const void* const* send,
+                         void* const* recv, size_t rc, int es) {
+  std::memset(a, 0, sizeof(*a));
+  a->nranks = nranks;
+  a->njobs = nranks;
+  const uintptr_t mod = (uintptr_t)recv[0] & 15;
+  const size_t bytes = rc * (size_t)es;
+  a->job_src_stride = bytes;
+  a->head_bytes = std::min(bytes, (size_t)((16 - mod) & 15));
+  a->nvec = (bytes - a->head_bytes) / 16;
+  a->tail_bytes = bytes - a->head_bytes - a->nvec * 16;
+  for (int k = 0; k < nranks; ++k) {
+    a->p.src[k] = send[k];
+    a->p.dst[k] = recv[k];
+  }
+  a->wide = anchor_wide_ok(*a) ? 1 : 0;
+}
+
 tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void* const* recv,
                                     size_t count, int dtype, int op, int es, cudaStream_t stream,
                                     int cap) {
@@ -110,7 +143,6 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
       r_ptr[k] = static_cast<char*>(recv[k]) + off * es;
     }
   };
-  const uintptr_t mod = (uintptr_t)recv[anchor] & 15;
   // ce_fold = 3: bulk reductions into the anchor, for the pairs the copy
   // hardware reduces exactly; any other pair folds as under Auto
   const bool tma_reduce = g->cfg.ce_fold == kFoldTmaReduce && tma_reduce_supported(dtype, op);
@@ -140,10 +172,6 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
   const int U = anchor_vectors_per_thread(P);
   int fast_grid = 0;
   AnchorArgs aa;
-  std::memset(&aa, 0, sizeof(aa));
-  aa.nranks = P;
-  aa.njobs = 1;
-  aa.mixed_bf16 = mixed_bf16_fold();
   // the copies of every segment but the last run beside the next segment's
   // fold, the last segment's beside nothing: each has its own stream count
   int mid_streams = 0, tail_streams = 0;
@@ -155,14 +183,8 @@ tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void*
     const size_t n = sgi == nseg - 1 ? tail_n : seg;
     at(off);
     if (fast) {
-      const size_t bytes = n * es;
-      const size_t head = std::min(bytes, (size_t)((16 - mod) & 15));
-      aa.head_bytes = head;
-      aa.nvec = (bytes - head) / 16;
-      aa.tail_bytes = bytes - head - aa.nvec * 16;
-      for (int k = 0; k < P; ++k) aa.p.src[k] = s_ptr[k];
-      aa.p.dst[0] = r_ptr[anchor];
-      aa.wide = anchor_wide_ok(aa) ? 1 : 0;
+      allreduce_segment_args(&aa, P, send, recv[anchor], off, n, es);
+      aa.mixed_bf16 = mixed_bf16_fold();
       wide_folds += aa.wide;
       const uint64_t per_cta = (uint64_t)kAnchorThreads * (aa.wide ? anchor_vectors_per_thread(P, true, dtype) : U);
       uint64_t grid = std::max<uint64_t>(1, (aa.nvec + per_cta - 1) / per_cta);
@@ -217,26 +239,13 @@ tcclResult_t run_copy_out_reduce_scatter(tcclGroup* g, const void* const* send, 
                                          size_t rc, int dtype, int op, int es, cudaStream_t stream,
                                          int cap) {
   const int P = g->nranks;
-  const size_t bytes = rc * (size_t)es;
-  const uintptr_t mod = (uintptr_t)recv[0] & 15;
   if (!register_fold_ok(kReduceScatter, P, mod16_of(P, send).data(),
                         mod16_of(P, (const void* const*)recv).data(), rc, es, 0))
     return tcclInvalidUsage;
   AnchorArgs aa;
-  std::memset(&aa, 0, sizeof(aa));
+  reduce_scatter_args(&aa, P, send, recv, rc, es);
   aa.sm_mask = sm_record_slot(g);
-  aa.nranks = P;
-  aa.njobs = P;
   aa.mixed_bf16 = mixed_bf16_fold();
-  aa.job_src_stride = bytes;
-  aa.head_bytes = std::min(bytes, (size_t)((16 - mod) & 15));
-  aa.nvec = (bytes - aa.head_bytes) / 16;
-  aa.tail_bytes = bytes - aa.head_bytes - aa.nvec * 16;
-  for (int k = 0; k < P; ++k) {
-    aa.p.src[k] = send[k];
-    aa.p.dst[k] = recv[k];
-  }
-  aa.wide = anchor_wide_ok(aa) ? 1 : 0;
   const uint64_t per_cta = (uint64_t)kAnchorThreads * anchor_vectors_per_thread(P, aa.wide != 0, dtype);
   uint64_t grid = std::max<uint64_t>(1, (aa.nvec * P + per_cta - 1) / per_cta);
   grid = std::min<uint64_t>(grid, cap > 0 ? (uint64_t)cap : (uint64_t)g->dev.sm_count);

@@ -355,14 +355,18 @@ tcclResult_t tcclPlanInspect(int coll, int nranks, const void* const sendbufs[],
  *                   *copy_out is 0 too);
  *   *segments, *segment_elems  an allreduce's segments and the length of all
  *                   but the last; 1 and `count` for a reduce-scatter on the
- *                   fold; 0 otherwise (an all-gather is copies only).
+ *                   fold; 0 otherwise (an all-gather is copies only);
+ *   *wide_folds     how many of those fold launches would read with 256-bit
+ *                   loads (the launch info's ce_wide_folds), in this
+ *                   process's environment (TCCL_ANCHOR_WIDE).
  * count == 0 and no-op calls report 0 everywhere. Argument errors are
  * reported exactly as the collective call would.
  */
 tcclResult_t tcclCopyOutInspect(int coll, int nranks, const void* const sendbufs[],
                                 void* const recvbufs[], size_t count, tcclDataType_t datatype,
                                 int cta_cap, int sm_count, const tcclConfig_t* cfg, int* copy_out,
-                                int* register_fold, int* segments, size_t* segment_elems);
+                                int* register_fold, int* segments, size_t* segment_elems,
+                                int* wide_folds);
 
 /*
  * Test hook for the bounded-wait error path: while enabled, each bulk-engine

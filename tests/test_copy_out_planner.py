@@ -24,10 +24,14 @@ def bufs(p, send_mis=0, recv_mis=0):
 
 
 def inspect(coll, p, count, dt=BF16, cap=0, cfg=None, send_mis=0, recv_mis=0, sm_count=SMS):
+    return inspect_wide(coll, p, count, dt, cap, cfg, send_mis, recv_mis, sm_count)[:4]
+
+
+def inspect_wide(coll, p, count, dt=BF16, cap=0, cfg=None, send_mis=0, recv_mis=0, sm_count=SMS):
     send, recv = bufs(p, send_mis, recv_mis)
-    r, co, rf, ns, se = tccl.tcclCopyOutInspect(coll, p, send, recv, count, dt, cap, sm_count, cfg)
+    r, co, rf, ns, se, wf = tccl.tcclCopyOutInspect(coll, p, send, recv, count, dt, cap, sm_count, cfg)
     assert r == tccl.tcclSuccess, tccl.tcclGetErrorString(r)
-    return co, rf, ns, se
+    return co, rf, ns, se, wf
 
 
 def config(**kw):
@@ -156,7 +160,7 @@ def test_all_gather_is_copies_only():
 def test_errors_and_empty_calls():
     send, recv = bufs(4)
     r = tccl.tcclCopyOutInspect(AR, 4, send, recv, 0, BF16, 8, SMS)
-    assert r[0] == tccl.tcclSuccess and r[1:] == (0, 0, 0, 0)
+    assert r[0] == tccl.tcclSuccess and r[1:] == (0, 0, 0, 0, 0)
     # overlapping receive buffers are rejected exactly as the call would be
     r = tccl.tcclCopyOutInspect(AR, 4, send, [recv[0]] * 4, 1 << 20, BF16, 8, SMS)
     assert r[0] == tccl.tcclInvalidArgument
@@ -184,3 +188,39 @@ def test_short_last_segment(pct, mib):
         assert se >= se0
         # the last segment is pct % of the others, to within the 256-byte rounding of each
         assert abs(last - pct / 100 * se) <= ns * 256 // es, (last, se)
+
+
+@pytest.mark.parametrize("p", [2, 3, 5, 8, 9, 12, 16, 17])
+@pytest.mark.parametrize("mis", [0, 2, 18])
+def test_wide_folds_allreduce(p, mis):
+    """The fold reads with 256-bit loads for P = 2 to 8 and multiples of 4,
+    when every source and the anchor's destination is 32-byte aligned past
+    the head. bf16 buffers 2 bytes past a 32-byte boundary have a 14-byte
+    head that ends 16 bytes short of one (128-bit loads); 18 bytes past it,
+    the head ends on one. Segments of 28 MiB keep that for every segment."""
+    co, rf, ns, se, wf = inspect_wide(AR, p, 64 * MiB, cap=16, send_mis=mis, recv_mis=mis)
+    assert co == 1 and rf == 1 and ns >= 4
+    rank_ok = 2 <= p <= 8 or p % 4 == 0
+    assert wf == (ns if rank_ok and mis in (0, 18) else 0), (p, mis, ns, wf)
+
+
+def test_wide_folds_follow_each_segment():
+    """Segments are whole multiples of 256 bytes (a requested 4 MiB + 16 is
+    rounded down), so every segment starts as aligned as the buffers and
+    all of them take the 256-bit loads."""
+    seg_bytes = 4 * MiB + 16
+    co, rf, ns, se, wf = inspect_wide(AR, 8, 8 * seg_bytes // 2, cap=8,
+                                      cfg=config(ce_segment_bytes=seg_bytes))
+    assert co == 1 and rf == 1 and se * 2 == 4 * MiB and ns == 9
+    assert wf == ns
+
+
+@pytest.mark.parametrize("p,rc_bytes,wide", [(4, 1 * MiB, 1), (4, 1 * MiB + 16, 0), (9, 1 * MiB, 0),
+                                             (16, 64 * 1024, 1), (3, 32, 1)])
+def test_wide_folds_reduce_scatter(p, rc_bytes, wide):
+    """Reduce-scatter: every job (shard j of each send buffer) must stay
+    32-byte aligned, so the shard size must be a multiple of 32 bytes."""
+    co, rf, ns, se, wf = inspect_wide(RS, p, rc_bytes // 2, cap=8,
+                                      cfg=config(engine=tccl.tcclEngineCopyOut))
+    assert co == 1 and rf == 1 and wf == wide
+
