@@ -822,6 +822,14 @@ def sweep(args):
         set_cfg(g, engine=tccl.tcclEngineCopyOut)  # the all-gather as copies only
         emit(**run_point("C2", g, "AG", p, rc, "bf16", "sum", parts, recvs, sms=True))
         set_cfg(g)
+        # all-gather under caps: Auto (copies only) and the SM-only bulk engine
+        for cap in (8, 16, 32):
+            emit(**run_point("C2", g, "AG", p, rc, "bf16", "sum", parts, recvs, cap=cap, sms=True))
+            set_cfg(g, ce_auto_max_cap=-1)
+            row = run_point("C2", g, "AG", p, rc, "bf16", "sum", parts, recvs, cap=cap, sms=True)
+            row["variant"] = "sm_only"
+            emit(**row)
+            set_cfg(g)
         g.close()
         del sends, recvs, parts
     # C3
