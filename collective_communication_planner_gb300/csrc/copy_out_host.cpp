@@ -78,20 +78,8 @@ int join_ce_streams(tcclGroup* g, int used, cudaStream_t stream) {
 
 }  // namespace
 
-// Allreduce on the copy-out engine. The message is cut into segments
-// (copy_out_segments: at most ce_segment_bytes per rank, at least four of at
-// least 4 MiB where the message allows, offsets multiples of 256 bytes, so
-// every segment has the same alignment). Each segment's shard-in kernel folds the P
-// ranks in ascending order into the anchor rank's (rank 0's) receive buffer
-// alone; an event after it releases the device-to-device copies of that
-// segment from the anchor to ranks 1..P-1 on the group's copy streams, so the
-// copy engines fan segment s out while the SMs reduce segment s+1. In place
-// is safe: segment s of a rank is overwritten only after the kernel that read
-// it has finished.
-//
-// The shard-in kernel is the register-load anchor fold when every send buffer
-// and the anchor's receive buffer share their address mod 16, else the bulk
-// engine's TMA pipeline with every window pointed at the anchor.
+// The register fold's arguments for one allreduce segment or one
+// reduce-scatter (both declared in copy_out.h).
 void allreduce_segment_args(AnchorArgs* a, int nranks, const void* const* send,
                             void* anchor_recv, size_t off, size_t n, int es) {
   std::memset(a, 0, sizeof(*a));
@@ -125,6 +113,20 @@ void reduce_scatter_args(AnchorArgs* a, int nranks, const void* const* send,
   a->wide = anchor_wide_ok(*a) ? 1 : 0;
 }
 
+// Allreduce on the copy-out engine. The message is cut into segments
+// (copy_out_segments: at most ce_segment_bytes per rank, at least four of at
+// least 4 MiB where the message allows, offsets multiples of 256 bytes, so
+// every segment has the same alignment). Each segment's shard-in kernel folds the P
+// ranks in ascending order into the anchor rank's (rank 0's) receive buffer
+// alone; an event after it releases the device-to-device copies of that
+// segment from the anchor to ranks 1..P-1 on the group's copy streams, so the
+// copy engines fan segment s out while the SMs reduce segment s+1. In place
+// is safe: segment s of a rank is overwritten only after the kernel that read
+// it has finished.
+//
+// The shard-in kernel is the register-load anchor fold when every send buffer
+// and the anchor's receive buffer share their address mod 16, else the bulk
+// engine's TMA pipeline with every window pointed at the anchor.
 tcclResult_t run_copy_out_allreduce(tcclGroup* g, const void* const* send, void* const* recv,
                                     size_t count, int dtype, int op, int es, cudaStream_t stream,
                                     int cap) {
