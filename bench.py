@@ -740,7 +740,10 @@ def sweep(args):
         es = 2 if dtype == "bf16" else 4
         dt, o = tccl.DTYPES[dtype], tccl.OPS[op]
         if coll == "AR":
-            fn = lambda: tccl.tcclAllReduce(g.handle, sends, recvs, n, dt, o, st, cap)
+            # arguments marshalled once, so small calls measure the library,
+            # not Python's per-call packing of pointer arrays
+            prepared = g.prepare_all_reduce(sends, recvs, op=op, cta_cap=cap, stream=st)
+            fn = lambda: prepared() or 0
             S, hbm = n * es, 2 * p * n * es
         elif coll == "RS":
             fn = lambda: tccl.tcclReduceScatter(g.handle, sends, recvs, n, dt, o, st, cap)

@@ -409,6 +409,26 @@ class Group:
             setattr(c, k, v)
         _check(tcclGroupSetConfig(self.handle, c), "tcclGroupSetConfig")
 
+    def prepare_all_reduce(self, sends, recvs=None, op="sum", cta_cap=0, stream=None):
+        """A callable that issues this allreduce each time it is called, with
+        its arguments marshalled once (pointer arrays, datatype, stream). For
+        small messages the per-call marshalling is most of the host time. The
+        tensors must stay alive, at the same addresses, while it is in use."""
+        recvs = sends if recvs is None else recvs
+        sp, keep_s = _ptr_array(sends)
+        rp, keep_r = _ptr_array(recvs)
+        args = (self.handle, sp, rp, sends[0].numel(), _dtype_code(sends[0]), OPS[op],
+                _stream(stream) if stream is not None else _current_stream(), cta_cap)
+        fn = _lib.tcclAllReduce
+
+        def call():
+            r = fn(*args)
+            if r != tcclSuccess:
+                raise TcclError(r, "tcclAllReduce")
+
+        call.keep = (keep_s, keep_r, sends, recvs)
+        return call
+
     def all_reduce(self, sends, recvs=None, op="sum", cta_cap=0, stream=None):
         """recvs[r] = fold over ranks of sends (ascending rank order). With
         recvs=None the reduction is in place."""

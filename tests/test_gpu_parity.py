@@ -647,3 +647,29 @@ def test_reduce_order_setting_round_trip(groups):
     reset_config(g)
     r, c = tccl.tcclGroupGetConfig(g.handle)
     assert c.reduce_order == tccl.tcclReduceAscending
+
+
+@pytest.mark.parametrize("tokens,cap", [(1, 0), (64, 0), (512, 16)])
+def test_prepared_allreduce_call(tokens, cap):
+    """Group.prepare_all_reduce marshals the arguments once; each call then
+    issues the same allreduce, on the given stream, and a call on fresh
+    inputs in the same buffers gives the oracle's result for them."""
+    p, hidden = 8, 8192
+    n = tokens * hidden
+    with tccl.Group(p) as g:
+        s = torch.cuda.Stream()
+        sends = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+        recvs = [torch.empty_like(t) for t in sends]
+        call = g.prepare_all_reduce(sends, recvs, cta_cap=cap, stream=s)
+        for seed in (5, 6):
+            xs = datagen.rank_buffers("normal_bf16", seed, p, n)
+            for t, x in zip(sends, xs):
+                t.copy_(to_device(x))
+            torch.cuda.synchronize()
+            for _ in range(3):
+                call()
+            s.synchronize()
+            assert g.query_error() == tccl.tcclSuccess
+            exp = oracle.allreduce(xs, "bf16", "sum", nthreads=0)
+            for r in range(p):
+                assert same_bits(to_host(recvs[r]), exp[r]), (tokens, cap, seed, r)
