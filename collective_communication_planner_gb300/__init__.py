@@ -409,6 +409,18 @@ class Group:
             setattr(c, k, v)
         _check(tcclGroupSetConfig(self.handle, c), "tcclGroupSetConfig")
 
+    @staticmethod
+    def _prepared(fn, args, name, keep):
+        """A callable that makes the C call `fn(*args)` each time, with the
+        arguments already marshalled; `keep` holds what they point into."""
+        def call():
+            r = fn(*args)
+            if r != tcclSuccess:
+                raise TcclError(r, name)
+
+        call.keep = keep
+        return call
+
     def prepare_all_reduce(self, sends, recvs=None, op="sum", cta_cap=0, stream=None):
         """A callable that issues this allreduce each time it is called, with
         its arguments marshalled once (pointer arrays, datatype, stream). For
@@ -419,15 +431,34 @@ class Group:
         rp, keep_r = _ptr_array(recvs)
         args = (self.handle, sp, rp, sends[0].numel(), _dtype_code(sends[0]), OPS[op],
                 _stream(stream) if stream is not None else _current_stream(), cta_cap)
-        fn = _lib.tcclAllReduce
+        return self._prepared(_lib.tcclAllReduce, args, "tcclAllReduce", (keep_s, keep_r, sends, recvs))
 
-        def call():
-            r = fn(*args)
-            if r != tcclSuccess:
-                raise TcclError(r, "tcclAllReduce")
+    def prepare_reduce_scatter(self, sends, recvs, op="sum", cta_cap=0, stream=None):
+        """prepare_all_reduce for reduce_scatter."""
+        sp, keep_s = _ptr_array(sends)
+        rp, keep_r = _ptr_array(recvs)
+        args = (self.handle, sp, rp, recvs[0].numel(), _dtype_code(sends[0]), OPS[op],
+                _stream(stream) if stream is not None else _current_stream(), cta_cap)
+        return self._prepared(_lib.tcclReduceScatter, args, "tcclReduceScatter",
+                              (keep_s, keep_r, sends, recvs))
 
-        call.keep = (keep_s, keep_r, sends, recvs)
-        return call
+    def prepare_all_gather(self, sends, recvs, cta_cap=0, stream=None):
+        """prepare_all_reduce for all_gather."""
+        sp, keep_s = _ptr_array(sends)
+        rp, keep_r = _ptr_array(recvs)
+        args = (self.handle, sp, rp, sends[0].numel(), _dtype_code(sends[0]),
+                _stream(stream) if stream is not None else _current_stream(), cta_cap)
+        return self._prepared(_lib.tcclAllGather, args, "tcclAllGather", (keep_s, keep_r, sends, recvs))
+
+    def prepare_all_reduce_rmsnorm(self, sends, recvs, gamma, eps=1e-6, cta_cap=0, stream=None):
+        """prepare_all_reduce for all_reduce_rmsnorm."""
+        rows, hidden = sends[0].shape
+        sp, keep_s = _ptr_array(sends)
+        rp, keep_r = _ptr_array(recvs)
+        args = (self.handle, sp, rp, rows, hidden, _ptr(gamma), eps, _dtype_code(sends[0]),
+                _stream(stream) if stream is not None else _current_stream(), cta_cap)
+        return self._prepared(_lib.tcclAllReduceRMSNorm, args, "tcclAllReduceRMSNorm",
+                              (keep_s, keep_r, sends, recvs, gamma))
 
     def all_reduce(self, sends, recvs=None, op="sum", cta_cap=0, stream=None):
         """recvs[r] = fold over ranks of sends (ascending rank order). With

@@ -673,3 +673,26 @@ def test_prepared_allreduce_call(tokens, cap):
             exp = oracle.allreduce(xs, "bf16", "sum", nthreads=0)
             for r in range(p):
                 assert same_bits(to_host(recvs[r]), exp[r]), (tokens, cap, seed, r)
+
+
+def test_prepared_reduce_scatter_and_all_gather_calls():
+    """The prepared reduce-scatter and all-gather match the oracle, and
+    chained (RS then AG) they equal the allreduce."""
+    p, rc = 4, 123_456
+    with tccl.Group(p) as g:
+        xs = datagen.rank_buffers("normal_bf16", 7, p, p * rc)
+        sends = [to_device(x) for x in xs]
+        parts = [torch.empty(rc, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+        outs = [torch.empty(p * rc, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+        rs = g.prepare_reduce_scatter(sends, parts, cta_cap=8)
+        ag = g.prepare_all_gather(parts, outs)
+        for _ in range(2):
+            rs()
+            ag()
+        torch.cuda.synchronize()
+        assert g.query_error() == tccl.tcclSuccess
+        exp_rs = oracle.reduce_scatter(xs, "bf16", "sum", nthreads=0)
+        exp_ar = oracle.allreduce(xs, "bf16", "sum", nthreads=0)
+        for r in range(p):
+            assert same_bits(to_host(parts[r]), exp_rs[r])
+            assert same_bits(to_host(outs[r]), exp_ar[r])

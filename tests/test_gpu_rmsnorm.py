@@ -176,3 +176,26 @@ def test_row_claiming_back_to_back(groups, cap, rows):
         exp, exp64 = rn.allreduce_rmsnorm(xs, gamma, rows, hidden, 1e-6, "bf16")
         for r in range(p):
             check(to_host(recvs[r]).ravel(), exp, exp64, "bf16", f"call {k} cap {cap} rows {rows} rank {r}")
+
+
+def test_prepared_fused_call(groups):
+    """prepare_all_reduce_rmsnorm issues the same fused call as
+    all_reduce_rmsnorm; repeated on new data in the same buffers it follows
+    the data."""
+    p, rows, hidden = 8, 4, 8192
+    g = groups(p)
+    gamma = datagen.rank_buffers("normal_bf16", 81, 1, hidden)[0]
+    gamma_d = to_device(gamma)
+    sends = [torch.empty(rows, hidden, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    recvs = [torch.empty_like(s) for s in sends]
+    call = g.prepare_all_reduce_rmsnorm(sends, recvs, gamma_d, eps=1e-6)
+    for seed in (82, 83):
+        xs = datagen.rank_buffers("normal_bf16", seed, p, rows * hidden)
+        for t, x in zip(sends, xs):
+            t.copy_(to_device(x).view(rows, hidden))
+        call()
+        torch.cuda.synchronize()
+        assert g.query_error() == tccl.tcclSuccess
+        exp, exp64 = rn.allreduce_rmsnorm(xs, gamma, rows, hidden, 1e-6, "bf16")
+        for r in range(p):
+            check(to_host(recvs[r]).ravel(), exp, exp64, "bf16", f"prepared seed {seed} rank {r}")
