@@ -1124,14 +1124,16 @@ __device__ __forceinline__ int find_window(const uint64_t* prefix, int nwin, uin
   return lo;
 }
 
-template <int COLL, int DT, int OP, int MAXR, int MAXW, bool SHFL>
+// NP: the rank count fixed at compile time (0: a.nranks), so the warp
+// engine's lane groups and its shuffle fold need no run-time division or loop.
+template <int COLL, int DT, int OP, int MAXR, int MAXW, bool SHFL, int NP>
 __global__ void __launch_bounds__(256) small_kernel(const __grid_constant__ SmallArgs<MAXR, MAXW> a) {
   // an early (programmatic dependent) launch waits here for the stream's
   // previous kernel before any global access (see bulk_kernel)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) record_sm(a.sm_mask);
-  const int P = a.nranks;
+  const int P = NP > 0 ? NP : a.nranks;
   const uint64_t nvec = a.vec_prefix[a.nwin];
   const uint64_t nelem = a.elem_prefix[a.nwin];
   const uint64_t gtid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -1154,7 +1156,7 @@ __global__ void __launch_bounds__(256) small_kernel(const __grid_constant__ Smal
       int wi = 0;
       uint64_t off = 0;
       if (valid) {
-        wi = find_window<MAXW>(a.vec_prefix, a.nwin, u);
+        wi = a.nwin == 1 ? 0 : find_window<MAXW>(a.vec_prefix, a.nwin, u);
         off = (u - a.vec_prefix[wi]) * 16;
         const Window& w = a.win[wi];
         if (COLL == kAllGather) {
@@ -1172,6 +1174,7 @@ __global__ void __launch_bounds__(256) small_kernel(const __grid_constant__ Smal
         res.w = __shfl_sync(0xFFFFFFFFu, x.w, base_lane);
       } else {
         typename StreamFold<DT, OP>::type f;
+#pragma unroll (NP > 0 ? NP : 1)
         for (int rr = 0; rr < P; ++rr) {
           uint4 y;
           y.x = __shfl_sync(0xFFFFFFFFu, x.x, base_lane + rr);
