@@ -73,22 +73,25 @@ int launch_bulk_t(const BulkArgs& a, const LaunchShape& s, cudaStream_t st) {
   return launch_maybe_early(bulk_kernel<C, D, O>, a, s, st);
 }
 
+template <int C, int D, int O, int MAXR, int MAXW, bool SHFL>
+int launch_small_np(const SmallArgs<MAXR, MAXW>& a, const LaunchShape& s, cudaStream_t st) {
+  // the common rank counts compiled in (small tables only)
+  if constexpr (MAXR == kSmallRanks) {
+    switch (a.nranks) {
+      case 2: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 2>, a, s, st);
+      case 4: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 4>, a, s, st);
+      case 8: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 8>, a, s, st);
+      default: break;
+    }
+  }
+  return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 0>, a, s, st);
+}
+
 template <int C, int D, int O, int MAXR, int MAXW>
 int launch_small_t(int engine, const void* args, const LaunchShape& s, cudaStream_t st) {
   const auto& a = *static_cast<const SmallArgs<MAXR, MAXW>*>(args);
-  if (engine == kEngineWarp) {
-    // decode-sized calls: the common rank counts compiled in
-    if constexpr (MAXR == kSmallRanks) {
-      switch (a.nranks) {
-        case 2: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, true, 2>, a, s, st);
-        case 4: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, true, 4>, a, s, st);
-        case 8: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, true, 8>, a, s, st);
-        default: break;
-      }
-    }
-    return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, true, 0>, a, s, st);
-  }
-  return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, false, 0>, a, s, st);
+  if (engine == kEngineWarp) return launch_small_np<C, D, O, MAXR, MAXW, true>(a, s, st);
+  return launch_small_np<C, D, O, MAXR, MAXW, false>(a, s, st);
 }
 
 template <int C, int D, int O>

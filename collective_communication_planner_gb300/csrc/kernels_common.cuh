@@ -1124,8 +1124,9 @@ __device__ __forceinline__ int find_window(const uint64_t* prefix, int nwin, uin
   return lo;
 }
 
-// NP: the rank count fixed at compile time (0: a.nranks), so the warp
-// engine's lane groups and its shuffle fold need no run-time division or loop.
+// NP: the rank count fixed at compile time (0: a.nranks). The warp engine's
+// lane groups then need no run-time division, and both engines' folds (and the
+// vec engine's P stores) are unrolled.
 template <int COLL, int DT, int OP, int MAXR, int MAXW, bool SHFL, int NP>
 __global__ void __launch_bounds__(256) small_kernel(const __grid_constant__ SmallArgs<MAXR, MAXW> a) {
   // an early (programmatic dependent) launch waits here for the stream's
@@ -1197,7 +1198,7 @@ __global__ void __launch_bounds__(256) small_kernel(const __grid_constant__ Smal
     }
   } else {
     for (uint64_t u = gtid; u < nvec; u += nthr) {
-      const int wi = find_window<MAXW>(a.vec_prefix, a.nwin, u);
+      const int wi = a.nwin == 1 ? 0 : find_window<MAXW>(a.vec_prefix, a.nwin, u);
       const Window& w = a.win[wi];
       const uint64_t off = (u - a.vec_prefix[wi]) * 16;
       uint4 res;
@@ -1206,7 +1207,7 @@ __global__ void __launch_bounds__(256) small_kernel(const __grid_constant__ Smal
       } else {
         typename StreamFold<DT, OP>::type f;
         f.init(ld_global_v4(static_cast<const char*>(a.p.src[0]) + w.src_off + off));
-#pragma unroll 8
+#pragma unroll (NP > 0 ? NP : 8)
         for (int r = 1; r < P; ++r)
           f.add(ld_global_v4(static_cast<const char*>(a.p.src[r]) + w.src_off + off));
         res = f.out();

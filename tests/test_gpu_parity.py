@@ -81,7 +81,7 @@ def assert_ranks_equal(got, exp, what):
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
 @pytest.mark.parametrize("op", ["sum", "min", "max"])
 def test_allreduce_engines_dtypes_ops(groups, engine, dtype, op):
-    for p, n in ((2, 70_001), (3, 1000), (8, 300_007), (5, 17)):
+    for p, n in ((2, 70_001), (3, 1000), (8, 300_007), (5, 17), (4, 33_337)):
         g = groups(p)
         configure(g, engine)
         xs = inputs(dtype, p, n)
@@ -114,7 +114,7 @@ def test_allreduce_misaligned_buffers(groups, engine, offs):
     assert_ranks_equal(got, exp, f"misaligned {offs}")
 
 
-@pytest.mark.parametrize("engine", ["bulk", "warp"])
+@pytest.mark.parametrize("engine", ["bulk", "warp", "vec"])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
 def test_allreduce_in_place(groups, engine, dtype):
     p, n = 8, 123_457
