@@ -134,10 +134,18 @@ Plan plan_collective(int coll, int nranks, uint64_t count, int elem_size, int op
   return pl;
 }
 
+uint64_t small_max_bytes(const Config& c, int nranks) {
+  // 0: by rank count. Graph-captured on GB300 (the warp engine against the vec
+  // engine with 128-lane CTAs): at P = 8 the vec engine is as fast at 64 KiB per
+  // rank and faster above (128 KiB: 1.8 against 2.2 us); at P = 4 and 6 the warp
+  // engine keeps up to 128 KiB; at P = 16 it is faster up to 96 KiB only.
+  if (c.small_max_bytes) return c.small_max_bytes;
+  return nranks >= 8 ? 64 * 1024 : 128 * 1024;
+}
+
 Config resolve_config(const Config& in) {
   Config c = in;
   // defaults chosen by launch-shape sweeps on GB300 (P = 4 and 8, bf16)
-  if (c.small_max_bytes == 0) c.small_max_bytes = 128 * 1024;
   if (c.vec_max_bytes == 0) c.vec_max_bytes = 4 * 1024 * 1024;
   if (c.stage_bytes <= 0) c.stage_bytes = kDefaultStageBytes;
   if (c.stages <= 0) c.stages = kDefaultStages;
@@ -442,7 +450,7 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
   int engine = cfg.engine;
   if (engine == kEngineAuto) {
     const uint64_t mb = message_bytes(plan.coll, p, plan.count, es);
-    if (mb <= cfg.small_max_bytes) engine = kEngineWarp;
+    if (mb <= small_max_bytes(cfg, p)) engine = kEngineWarp;
     else if (mb <= cfg.vec_max_bytes && !capped) engine = kEngineVec;
     else engine = kEngineBulk;
   }
@@ -469,7 +477,6 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
     }
     uint64_t nvec = out->vec_prefix.back();
     uint64_t nelem = out->elem_prefix.back();
-    const int threads = 256;
     uint64_t lanes;
     if (engine == kEngineWarp) {
       int vpw = 32 / p;  // vectors per warp: one group of P lanes per vector
@@ -478,6 +485,13 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
       lanes = nvec;
     }
     lanes = std::max<uint64_t>(lanes, nelem);
+    // the vec engine up to 256 KiB of vectors: CTAs of 128 lanes, twice as
+    // many as of 256, spread over the SMs more evenly. Graph-captured on GB300,
+    // P = 4 to 16, 64 to 256 KiB per rank: as fast or faster at every size
+    // (P = 8, 256 KiB: 1.88 against 2.17 us). From 512 KiB they gain nothing
+    // (P = 16, 1 MiB: 0.4 us slower), and from 2 MiB the grid reaches its cap
+    // of 8 CTAs per SM, where smaller CTAs lose.
+    const int threads = (engine == kEngineVec && lanes <= kVecNarrowLanes) ? 128 : 256;
     uint64_t blocks = std::max<uint64_t>(1, ceil_div(lanes, threads));
     uint64_t cap = (uint64_t)dev.sm_count * 8;
     if (cta_cap > 0) cap = std::min<uint64_t>(cap, (uint64_t)cta_cap);

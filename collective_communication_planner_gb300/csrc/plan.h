@@ -98,8 +98,18 @@ struct Config {
 // touches the data), for the (dtype, op) pairs it reduces exactly, else Auto.
 enum CeFold : int { kFoldAuto = 0, kFoldRegister = 1, kFoldTma = 2, kFoldTmaReduce = 3 };
 
-// Fills zero fields with the library defaults.
+// Fills zero fields with the library defaults (small_max_bytes stays 0: it
+// depends on the rank count, see small_max_bytes()).
 Config resolve_config(const Config& in);
+
+// The largest message per rank buffer Auto gives the warp engine: the
+// config's small_max_bytes, or when that is 0, 64 KiB for P >= 8 and 128 KiB
+// below.
+uint64_t small_max_bytes(const Config& c, int nranks);
+
+// The vec engine runs CTAs of 128 lanes up to this many lanes (256 KiB of
+// 16-byte vectors), else 256.
+constexpr uint64_t kVecNarrowLanes = (uint64_t)1 << 14;
 
 // The bulk engine's default pipeline shape. With all three at these values
 // an uncapped, out-of-place allreduce that stores to every rank and moves at

@@ -40,12 +40,13 @@ def bufs(p, nbytes_send, nbytes_recv, send_mis=0, recv_mis=0, in_place=None, col
     return send, recv
 
 
-def cfg(engine=0, store=0, stage_bytes=0, stages=0):
+def cfg(engine=0, store=0, stage_bytes=0, stages=0, small_max_bytes=0):
     c = tccl.tcclConfig_t()
     c.engine = engine
     c.store_mode = store
     c.stage_bytes = stage_bytes
     c.stages = stages
+    c.small_max_bytes = small_max_bytes
     return c
 
 
@@ -230,6 +231,32 @@ def test_auto_engine_choice():
     r, _, _, info = inspect(AR, 40, 1024, tccl.tcclFloat32, *bufs(40, 0, 0),
                             engine=tccl.tcclEngineWarp)
     assert info.engine == tccl.tcclEngineVec  # more ranks than lanes
+
+
+def test_small_engine_switch_by_rank_count():
+    # the warp engine up to 64 KiB per rank at P >= 8 and up to 128 KiB below;
+    # the vec engine above, in CTAs of 128 lanes up to 256 KiB of vectors
+    for p, kib, exp in ((8, 64, tccl.tcclEngineWarp), (8, 96, tccl.tcclEngineVec),
+                        (8, 128, tccl.tcclEngineVec), (16, 128, tccl.tcclEngineVec),
+                        (4, 128, tccl.tcclEngineWarp), (6, 128, tccl.tcclEngineWarp),
+                        (4, 192, tccl.tcclEngineVec)):
+        send, recv = bufs(p, 0, 0)
+        r, _, _, info = inspect(AR, p, kib * 512, tccl.tcclBfloat16, send, recv)
+        assert r == 0 and info.engine == exp, (p, kib, info.engine)
+        if exp == tccl.tcclEngineVec:
+            assert info.threads == 128 and info.ctas == kib * 1024 // 16 // 128, (p, kib, info.ctas)
+        else:
+            assert info.threads == 256
+    send, recv = bufs(8, 0, 0)
+    r, _, _, info = inspect(AR, 8, 1 << 17, tccl.tcclBfloat16, send, recv)  # 256 KiB: 16384 lanes
+    assert info.engine == tccl.tcclEngineVec and info.threads == 128 and info.ctas == 128
+    r, _, _, info = inspect(AR, 8, 1 << 18, tccl.tcclBfloat16, send, recv)  # 512 KiB
+    assert info.engine == tccl.tcclEngineVec and info.threads == 256 and info.ctas == 128
+    r, _, _, info = inspect(AR, 8, 1 << 20, tccl.tcclBfloat16, send, recv)  # 2 MiB
+    assert info.engine == tccl.tcclEngineVec and info.threads == 256 and info.ctas == 512
+    # an explicit threshold wins over the rank-count default
+    r, _, _, info = inspect(AR, 8, 1 << 16, tccl.tcclBfloat16, send, recv, small_max_bytes=128 << 10)
+    assert info.engine == tccl.tcclEngineWarp
 
 
 def test_pipeline_shape_follows_shared_memory():
