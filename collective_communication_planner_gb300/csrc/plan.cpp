@@ -485,13 +485,17 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
       lanes = nvec;
     }
     lanes = std::max<uint64_t>(lanes, nelem);
-    // the vec engine up to 256 KiB of vectors: CTAs of 128 lanes, twice as
-    // many as of 256, spread over the SMs more evenly. Graph-captured on GB300,
-    // P = 4 to 16, 64 to 256 KiB per rank: as fast or faster at every size
-    // (P = 8, 256 KiB: 1.88 against 2.17 us). From 512 KiB they gain nothing
-    // (P = 16, 1 MiB: 0.4 us slower), and from 2 MiB the grid reaches its cap
-    // of 8 CTAs per SM, where smaller CTAs lose.
-    const int threads = (engine == kEngineVec && lanes <= kVecNarrowLanes) ? 128 : 256;
+    // the vec engine with few lanes: one CTA per SM, each of the lanes / SMs
+    // rounded up to a warp, so that every SM gets the same few lanes. Graph-
+    // captured on GB300 (P = 2, 4, 8, f32 and bf16, 16 KiB to 1 MiB per rank,
+    // in place and out of place), against fixed CTAs of 128 lanes: 1.75 against
+    // 2.1 us at P = 8, 128 KiB in place (64 CTAs on 152 SMs), and no slower
+    // beyond noise anywhere up to 192 lanes per SM (P = 8: 384 KiB). From
+    // 512 KiB on, CTAs of 256.
+    int threads = 256;
+    const uint64_t sms = (uint64_t)std::max(1, dev.sm_count);
+    if (engine == kEngineVec && lanes <= sms * kVecSpreadLanesPerSm)
+      threads = (int)std::max<uint64_t>(32, ceil_div(ceil_div(lanes, sms), (uint64_t)32) * 32);
     uint64_t blocks = std::max<uint64_t>(1, ceil_div(lanes, threads));
     uint64_t cap = (uint64_t)dev.sm_count * 8;
     if (cta_cap > 0) cap = std::min<uint64_t>(cap, (uint64_t)cta_cap);

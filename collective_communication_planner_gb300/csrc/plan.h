@@ -107,9 +107,9 @@ Config resolve_config(const Config& in);
 // below.
 uint64_t small_max_bytes(const Config& c, int nranks);
 
-// The vec engine runs CTAs of 128 lanes up to this many lanes (256 KiB of
-// 16-byte vectors), else 256.
-constexpr uint64_t kVecNarrowLanes = (uint64_t)1 << 14;
+// Up to this many lanes per SM the vec engine spreads its lanes over one CTA
+// per SM (CTAs of the lanes / SMs, rounded up to a warp); above, CTAs of 256.
+constexpr uint64_t kVecSpreadLanesPerSm = 192;
 
 // The bulk engine's default pipeline shape. With all three at these values
 // an uncapped, out-of-place allreduce that stores to every rank and moves at

@@ -235,21 +235,30 @@ def test_auto_engine_choice():
 
 def test_small_engine_switch_by_rank_count():
     # the warp engine up to 64 KiB per rank at P >= 8 and up to 128 KiB below;
-    # the vec engine above, in CTAs of 128 lanes up to 256 KiB of vectors
+    # the vec engine above, up to 192 lanes per SM in one CTA per SM of the
+    # lanes / SMs rounded up to a warp, else in CTAs of 256
+    sms = 152
     for p, kib, exp in ((8, 64, tccl.tcclEngineWarp), (8, 96, tccl.tcclEngineVec),
                         (8, 128, tccl.tcclEngineVec), (16, 128, tccl.tcclEngineVec),
                         (4, 128, tccl.tcclEngineWarp), (6, 128, tccl.tcclEngineWarp),
-                        (4, 192, tccl.tcclEngineVec)):
+                        (4, 192, tccl.tcclEngineVec), (8, 256, tccl.tcclEngineVec),
+                        (8, 384, tccl.tcclEngineVec), (8, 512, tccl.tcclEngineVec),
+                        (8, 2048, tccl.tcclEngineVec)):
         send, recv = bufs(p, 0, 0)
-        r, _, _, info = inspect(AR, p, kib * 512, tccl.tcclBfloat16, send, recv)
+        r, _, _, info = inspect(AR, p, kib * 512, tccl.tcclBfloat16, send, recv, sm=sms)
         assert r == 0 and info.engine == exp, (p, kib, info.engine)
-        if exp == tccl.tcclEngineVec:
-            assert info.threads == 128 and info.ctas == kib * 1024 // 16 // 128, (p, kib, info.ctas)
+        lanes = kib * 1024 // 16
+        if exp == tccl.tcclEngineVec and lanes <= sms * 192:
+            per_sm = -(-lanes // sms)
+            threads = max(32, -(-per_sm // 32) * 32)
+            assert info.threads == threads and info.ctas == -(-lanes // threads) <= sms, (p, kib, info.threads)
+        elif exp == tccl.tcclEngineVec:
+            assert info.threads == 256 and info.ctas == min(-(-lanes // 256), 8 * sms), (p, kib, info.ctas)
         else:
             assert info.threads == 256
     send, recv = bufs(8, 0, 0)
-    r, _, _, info = inspect(AR, 8, 1 << 17, tccl.tcclBfloat16, send, recv)  # 256 KiB: 16384 lanes
-    assert info.engine == tccl.tcclEngineVec and info.threads == 128 and info.ctas == 128
+    r, _, _, info = inspect(AR, 8, 1 << 16, tccl.tcclBfloat16, send, recv)  # 128 KiB: 8192 lanes
+    assert info.engine == tccl.tcclEngineVec and info.threads == 64 and info.ctas == 128
     r, _, _, info = inspect(AR, 8, 1 << 18, tccl.tcclBfloat16, send, recv)  # 512 KiB
     assert info.engine == tccl.tcclEngineVec and info.threads == 256 and info.ctas == 128
     r, _, _, info = inspect(AR, 8, 1 << 20, tccl.tcclBfloat16, send, recv)  # 2 MiB
