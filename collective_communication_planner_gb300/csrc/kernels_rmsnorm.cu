@@ -129,19 +129,29 @@ __global__ void __launch_bounds__(kRmsMaxThreads) rmsnorm_kernel(const __grid_co
 }
 
 // Few rows (decode-sized calls): a cluster of kRmsCluster CTAs shares each
-// row. CTA q of the cluster reduces and normalises a contiguous slice; the
-// slices' sums of squares meet through distributed shared memory, added in
-// cluster-rank order, so every CTA derives the same scale.
-template <int DT>
+// row. CTA q of the cluster reduces and normalises a contiguous slice. Thread
+// 0 of every CTA writes its slice's sum of squares into slot q of every CTA's
+// shared memory (distributed shared memory), and after one cluster barrier
+// each CTA adds its own slots in cluster-rank order, so every CTA derives the
+// same scale. No CTA reads another's shared memory, so none waits for the
+// others before it moves on or exits; the slots alternate between two sets
+// from row to row, since a CTA may write the next row's sum while another
+// still adds up this row's.
+//
+// V vectors per thread, RB ranks per load batch: a slice of at most one
+// vector per thread takes V = 1 and RB = 8, so up to eight ranks cost one
+// memory round trip, and loads its gamma vector once, before the first row,
+// so the scale step waits on no load (with V = 4 the gamma vectors would cost
+// the registers of a second resident CTA per SM; they are loaded after the
+// scale).
+template <int DT, int V, int RB>
 __global__ void __launch_bounds__(kRmsClusterThreads)
     rmsnorm_cluster_kernel(const __grid_constant__ RmsArgs a) {
   namespace cg = cooperative_groups;
   using dev::Fold;
-  constexpr int V = 4;
-  constexpr int RB = 4;
   constexpr int kVecElems = DT == kBF16 ? 8 : 4;
   __shared__ float partial[kRmsClusterThreads / 32];
-  __shared__ float slice_ss;
+  __shared__ float slots[2][kRmsCluster];
   cg::cluster_group cluster = cg::this_cluster();
   const int q = static_cast<int>(cluster.block_rank());
   const int C = static_cast<int>(cluster.num_blocks());
@@ -162,7 +172,17 @@ __global__ void __launch_bounds__(kRmsClusterThreads)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) dev::record_sm(a.sm_mask);
-  for (uint64_t t = cid; t < a.rows; t += nclusters) {
+  constexpr bool kGammaFirst = V == 1;
+  Fold<DT, kSum> gam[V];
+  if (kGammaFirst) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const uint32_t v = v0 + threadIdx.x + j * blockDim.x;
+      if (v < v1) gam[j].init(dev::ld_global_v4(static_cast<const char*>(a.gamma) + v * 16ull));
+    }
+  }
+  int buf = 0;
+  for (uint64_t t = cid; t < a.rows; t += nclusters, buf ^= 1) {
     const uint64_t row_off = t * static_cast<uint64_t>(a.hidden) * (DT == kBF16 ? 2 : 4);
     Fold<DT, kSum> acc[V];
     for (int r0 = 0; r0 < P; r0 += RB) {
@@ -203,27 +223,25 @@ __global__ void __launch_bounds__(kRmsClusterThreads)
     if (threadIdx.x == 0) {
       float w = 0.f;
       for (int i = 0; i < nwarps; ++i) w = __fadd_rn(w, partial[i]);
-      slice_ss = w;
+      for (int i = 0; i < C; ++i) *cluster.map_shared_rank(&slots[buf][q], i) = w;
     }
-    cluster.sync();  // every slice's sum of squares is in its CTA's shared memory
+    cluster.sync();  // every slice's sum of squares is in every CTA's slots
     float total = 0.f;
-    for (int i = 0; i < C; ++i) total = __fadd_rn(total, *cluster.map_shared_rank(&slice_ss, i));
+    for (int i = 0; i < C; ++i) total = __fadd_rn(total, slots[buf][i]);
     const float scale = rsqrtf(__fadd_rn(__fdiv_rn(total, static_cast<float>(a.hidden)), a.eps));
 #pragma unroll
     for (int j = 0; j < V; ++j) {
       const uint32_t v = v0 + threadIdx.x + j * blockDim.x;
       if (v < v1) {
-        Fold<DT, kSum> g;
-        g.init(dev::ld_global_v4(static_cast<const char*>(a.gamma) + v * 16ull));
+        if (!kGammaFirst) gam[j].init(dev::ld_global_v4(static_cast<const char*>(a.gamma) + v * 16ull));
 #pragma unroll
         for (int e = 0; e < kVecElems; ++e)
-          acc[j].a[e] = __fmul_rn(__fmul_rn(acc[j].a[e], scale), g.a[e]);
+          acc[j].a[e] = __fmul_rn(__fmul_rn(acc[j].a[e], scale), gam[j].a[e]);
         const uint4 y = acc[j].out();
         const uint64_t o = row_off + v * 16ull;
         for (int d = 0; d < P; ++d) dev::st_global_v4(static_cast<char*>(a.p.dst[d]) + o, y);
       }
     }
-    cluster.sync();  // no CTA reuses slice_ss / partial[] before all have read them
   }
 }
 
@@ -245,8 +263,16 @@ int launch_rmsnorm_cluster(int dtype, const RmsArgs& a, int clusters, int cluste
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = early ? 2 : 1;
-  cudaError_t e = dtype == kBF16 ? cudaLaunchKernelEx(&cfg, rmsnorm_cluster_kernel<kBF16>, a)
-                                 : cudaLaunchKernelEx(&cfg, rmsnorm_cluster_kernel<kF32>, a);
+  // a slice of at most one vector per thread: one batch of up to 8 ranks
+  const uint32_t nvec = a.hidden / (dtype == kBF16 ? 8u : 4u);
+  const bool one = (nvec + cluster_size - 1) / cluster_size <= static_cast<uint32_t>(kRmsClusterThreads);
+  cudaError_t e;
+  if (dtype == kBF16)
+    e = one ? cudaLaunchKernelEx(&cfg, rmsnorm_cluster_kernel<kBF16, 1, 8>, a)
+            : cudaLaunchKernelEx(&cfg, rmsnorm_cluster_kernel<kBF16, 4, 4>, a);
+  else
+    e = one ? cudaLaunchKernelEx(&cfg, rmsnorm_cluster_kernel<kF32, 1, 8>, a)
+            : cudaLaunchKernelEx(&cfg, rmsnorm_cluster_kernel<kF32, 4, 4>, a);
   if (e != cudaSuccess) return static_cast<int>(e);
   return static_cast<int>(cudaGetLastError());
 }
