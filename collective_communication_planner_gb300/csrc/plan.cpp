@@ -136,9 +136,10 @@ Plan plan_collective(int coll, int nranks, uint64_t count, int elem_size, int op
 
 uint64_t small_max_bytes(const Config& c, int nranks) {
   // 0: by rank count. Graph-captured on GB300 (the warp engine against the vec
-  // engine with 128-lane CTAs): at P = 8 the vec engine is as fast at 64 KiB per
-  // rank and faster above (128 KiB: 1.8 against 2.2 us); at P = 4 and 6 the warp
-  // engine keeps up to 128 KiB; at P = 16 it is faster up to 96 KiB only.
+  // engine with its small CTAs spread over the SMs): at P = 8 the vec engine is
+  // as fast at 64 KiB per rank and faster above (128 KiB: 1.6-1.8 against
+  // 2.2 us); at P = 4 and 6 the warp engine keeps up to 128 KiB; at P = 16 it is
+  // faster up to 96 KiB only.
   if (c.small_max_bytes) return c.small_max_bytes;
   return nranks >= 8 ? 64 * 1024 : 128 * 1024;
 }
