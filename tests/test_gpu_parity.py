@@ -114,6 +114,31 @@ def test_allreduce_misaligned_buffers(groups, engine, offs):
     assert_ranks_equal(got, exp, f"misaligned {offs}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("lanes_per_sm", [1, 27, 191, 192, 193, 300])
+def test_vec_engine_grid_shapes(groups, dtype, lanes_per_sm):
+    """The vec engine's grid: one CTA per SM of the lanes / SMs rounded up to a
+    warp up to 192 lanes per SM, CTAs of 256 above. Counts on both sides of
+    that bound, with a ragged tail of scalar elements, in place and out of
+    place, the vec engine forced."""
+    p = 8
+    g = groups(p)
+    configure(g, "vec")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    epv = 4 if dtype == "f32" else 8  # elements per 16-byte vector
+    n = lanes_per_sm * sms * epv + 3
+    xs = inputs(dtype, p, n, seed=lanes_per_sm)
+    exp = oracle.allreduce(xs, dtype, "sum", nthreads=0)
+    assert_ranks_equal(run_allreduce(g, xs, dtype, "sum"), exp, f"vec {dtype} {lanes_per_sm}/SM")
+    info = g.last_launch()
+    assert info["engine"] == tccl.tcclEngineVec
+    if lanes_per_sm <= 192:
+        assert info["ctas"] <= sms and info["threads"] % 32 == 0 and info["threads"] <= 256, info
+    else:
+        assert info["threads"] == 256, info
+    assert_ranks_equal(run_allreduce(g, xs, dtype, "sum", in_place=True), exp, f"vec in place {dtype}")
+
+
 @pytest.mark.parametrize("engine", ["bulk", "warp", "vec"])
 @pytest.mark.parametrize("dtype", ["f32", "i32"])
 def test_allreduce_in_place(groups, engine, dtype):
