@@ -268,6 +268,33 @@ def test_small_engine_switch_by_rank_count():
     assert info.engine == tccl.tcclEngineWarp
 
 
+def test_small_engine_switch_edges():
+    # the default switch-over follows the rank count: P = 7 keeps 128 KiB, P = 9 takes 64 KiB
+    for p, kib, exp in ((7, 128, tccl.tcclEngineWarp), (7, 129, tccl.tcclEngineVec),
+                        (9, 64, tccl.tcclEngineWarp), (9, 65, tccl.tcclEngineVec)):
+        send, recv = bufs(p, 0, 0)
+        r, _, _, info = inspect(AR, p, kib * 256, tccl.tcclFloat32, send, recv)
+        assert r == 0 and info.engine == exp, (p, kib, info.engine)
+    # a capped call of any size keeps off the vec engine
+    send, recv = bufs(8, 0, 0)
+    r, _, _, info = inspect(AR, 8, 1 << 16, tccl.tcclBfloat16, send, recv, cap=16)
+    assert info.engine == tccl.tcclEngineBulk
+
+
+@pytest.mark.parametrize("sms", [132, 152, 160])
+def test_vec_grid_follows_sm_count(sms):
+    # one CTA per SM up to 192 lanes per SM of this device, CTAs of 256 above
+    send, recv = bufs(8, 0, 0)
+    for lanes in (sms * 192, sms * 192 + 32):
+        r, _, _, info = inspect(AR, 8, lanes * 4, tccl.tcclFloat32, send, recv, sm=sms,
+                                engine=tccl.tcclEngineVec)
+        assert r == 0 and info.engine == tccl.tcclEngineVec
+        if lanes <= sms * 192:
+            assert info.threads == 192 and info.ctas == sms, (sms, lanes, info.threads, info.ctas)
+        else:
+            assert info.threads == 256 and info.ctas == -(-lanes // 256), (sms, lanes, info.threads)
+
+
 def test_pipeline_shape_follows_shared_memory():
     send, recv = bufs(8, 0, 0)
     r, _, _, info = inspect(AR, 8, 1 << 24, tccl.tcclBfloat16, send, recv,
