@@ -75,11 +75,15 @@ int launch_bulk_t(const BulkArgs& a, const LaunchShape& s, cudaStream_t st) {
 
 template <int C, int D, int O, int MAXR, int MAXW, bool SHFL>
 int launch_small_np(const SmallArgs<MAXR, MAXW>& a, const LaunchShape& s, cudaStream_t st) {
-  // the common rank counts compiled in (small tables only)
+  // rank counts up to 8 compiled in (small tables only)
   if constexpr (MAXR == kSmallRanks) {
     switch (a.nranks) {
       case 2: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 2>, a, s, st);
+      case 3: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 3>, a, s, st);
       case 4: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 4>, a, s, st);
+      case 5: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 5>, a, s, st);
+      case 6: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 6>, a, s, st);
+      case 7: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 7>, a, s, st);
       case 8: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 8>, a, s, st);
       default: break;
     }

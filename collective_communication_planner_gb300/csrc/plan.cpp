@@ -136,12 +136,13 @@ Plan plan_collective(int coll, int nranks, uint64_t count, int elem_size, int op
 
 uint64_t small_max_bytes(const Config& c, int nranks) {
   // 0: by rank count. Graph-captured on GB300 (the warp engine against the vec
-  // engine with its small CTAs spread over the SMs): at P = 8 the vec engine is
-  // as fast at 64 KiB per rank and faster above (128 KiB: 1.6-1.8 against
-  // 2.2 us); at P = 4 and 6 the warp engine keeps up to 128 KiB; at P = 16 it is
-  // faster up to 96 KiB only.
+  // engine with its small CTAs spread over the SMs, both with the rank count
+  // compiled in): from P = 5 to 8 the vec engine is about as fast at 64 KiB per
+  // rank and faster above (P = 8, 128 KiB: 1.6-1.8 against 2.2 us; P = 6:
+  // 1.65 against 1.97); at P = 3 and 4 the two tie up to 128 KiB; at P = 16
+  // the warp engine is faster up to 96 KiB only.
   if (c.small_max_bytes) return c.small_max_bytes;
-  return nranks >= 8 ? 64 * 1024 : 128 * 1024;
+  return nranks >= 5 ? 64 * 1024 : 128 * 1024;
 }
 
 Config resolve_config(const Config& in) {

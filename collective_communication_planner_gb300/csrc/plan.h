@@ -103,7 +103,7 @@ enum CeFold : int { kFoldAuto = 0, kFoldRegister = 1, kFoldTma = 2, kFoldTmaRedu
 Config resolve_config(const Config& in);
 
 // The largest message per rank buffer Auto gives the warp engine: the
-// config's small_max_bytes, or when that is 0, 64 KiB for P >= 8 and 128 KiB
+// config's small_max_bytes, or when that is 0, 64 KiB for P >= 5 and 128 KiB
 // below.
 uint64_t small_max_bytes(const Config& c, int nranks);
 

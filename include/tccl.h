@@ -147,7 +147,7 @@ typedef enum {
 typedef struct {
   int engine;              /* tcclEngine_t */
   size_t small_max_bytes;  /* Auto picks the warp engine at or below this many bytes per rank buffer
-                              (0: 64 KiB for P >= 8, 128 KiB for fewer ranks) */
+                              (0: 64 KiB for P >= 5, 128 KiB for fewer ranks) */
   size_t vec_max_bytes;    /* ... and the vec engine up to this many (uncapped calls only) */
   int stage_bytes;         /* bulk engine: shared-memory bytes of one pipeline stage (all sources of one chunk) */
   int stages;              /* bulk engine: pipeline depth (reduced to what shared memory holds) */

@@ -234,13 +234,14 @@ def test_auto_engine_choice():
 
 
 def test_small_engine_switch_by_rank_count():
-    # the warp engine up to 64 KiB per rank at P >= 8 and up to 128 KiB below;
+    # the warp engine up to 64 KiB per rank at P >= 5 and up to 128 KiB below;
     # the vec engine above, up to 192 lanes per SM in one CTA per SM of the
     # lanes / SMs rounded up to a warp, else in CTAs of 256
     sms = 152
     for p, kib, exp in ((8, 64, tccl.tcclEngineWarp), (8, 96, tccl.tcclEngineVec),
                         (8, 128, tccl.tcclEngineVec), (16, 128, tccl.tcclEngineVec),
-                        (4, 128, tccl.tcclEngineWarp), (6, 128, tccl.tcclEngineWarp),
+                        (4, 128, tccl.tcclEngineWarp), (6, 128, tccl.tcclEngineVec),
+                        (6, 64, tccl.tcclEngineWarp), (3, 128, tccl.tcclEngineWarp),
                         (4, 192, tccl.tcclEngineVec), (8, 256, tccl.tcclEngineVec),
                         (8, 384, tccl.tcclEngineVec), (8, 512, tccl.tcclEngineVec),
                         (8, 2048, tccl.tcclEngineVec)):
@@ -269,8 +270,9 @@ def test_small_engine_switch_by_rank_count():
 
 
 def test_small_engine_switch_edges():
-    # the default switch-over follows the rank count: P = 7 keeps 128 KiB, P = 9 takes 64 KiB
-    for p, kib, exp in ((7, 128, tccl.tcclEngineWarp), (7, 129, tccl.tcclEngineVec),
+    # the default switch-over follows the rank count: P = 4 keeps 128 KiB, P = 5 and 9 take 64 KiB
+    for p, kib, exp in ((4, 128, tccl.tcclEngineWarp), (4, 129, tccl.tcclEngineVec),
+                        (5, 64, tccl.tcclEngineWarp), (5, 65, tccl.tcclEngineVec),
                         (9, 64, tccl.tcclEngineWarp), (9, 65, tccl.tcclEngineVec)):
         send, recv = bufs(p, 0, 0)
         r, _, _, info = inspect(AR, p, kib * 256, tccl.tcclFloat32, send, recv)
