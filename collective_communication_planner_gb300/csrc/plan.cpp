@@ -452,7 +452,13 @@ bool lower_plan(const Plan& plan, const uint8_t* send_mod16, const uint8_t* recv
   int engine = cfg.engine;
   if (engine == kEngineAuto) {
     const uint64_t mb = message_bytes(plan.coll, p, plan.count, es);
-    if (mb <= small_max_bytes(cfg, p)) engine = kEngineWarp;
+    // an out-of-place allreduce over 8 ranks goes to the vec engine at every
+    // small size: graph-captured on GB300, 4-64 KiB per rank, 1.56-1.76 against
+    // 1.67-1.86 us on the warp engine (bf16, 16 KiB: 1.66 against 1.80). In
+    // place the warp engine stays ahead below 64 KiB (16 KiB: 1.85 against
+    // 1.95), and at other rank counts the two were within noise or mixed.
+    const bool vec_first = cfg.small_max_bytes == 0 && plan.coll == kAllReduce && !plan.in_place && p == 8;
+    if (mb <= small_max_bytes(cfg, p) && !vec_first) engine = kEngineWarp;
     else if (mb <= cfg.vec_max_bytes && !capped) engine = kEngineVec;
     else engine = kEngineBulk;
   }

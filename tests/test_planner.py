@@ -217,7 +217,7 @@ def test_task_structure():
 def test_auto_engine_choice():
     p = 8
     send, recv = bufs(p, 0, 0)
-    r, _, _, info = inspect(AR, p, 8192, tccl.tcclBfloat16, send, recv)  # 16 KiB per rank
+    r, _, _, info = inspect(AR, p, 8192, tccl.tcclBfloat16, send, send)  # 16 KiB per rank, in place
     assert info.engine == tccl.tcclEngineWarp
     r, _, _, info = inspect(AR, p, 1 << 20, tccl.tcclBfloat16, send, recv)  # 2 MiB per rank
     assert info.engine == tccl.tcclEngineVec
@@ -238,7 +238,7 @@ def test_small_engine_switch_by_rank_count():
     # the vec engine above, up to 192 lanes per SM in one CTA per SM of the
     # lanes / SMs rounded up to a warp, else in CTAs of 256
     sms = 152
-    for p, kib, exp in ((8, 64, tccl.tcclEngineWarp), (8, 96, tccl.tcclEngineVec),
+    for p, kib, exp in ((9, 64, tccl.tcclEngineWarp), (8, 96, tccl.tcclEngineVec),
                         (8, 128, tccl.tcclEngineVec), (16, 128, tccl.tcclEngineVec),
                         (4, 128, tccl.tcclEngineWarp), (6, 128, tccl.tcclEngineVec),
                         (6, 64, tccl.tcclEngineWarp), (3, 128, tccl.tcclEngineWarp),
@@ -266,6 +266,22 @@ def test_small_engine_switch_by_rank_count():
     assert info.engine == tccl.tcclEngineVec and info.threads == 256 and info.ctas == 512
     # an explicit threshold wins over the rank-count default
     r, _, _, info = inspect(AR, 8, 1 << 16, tccl.tcclBfloat16, send, recv, small_max_bytes=128 << 10)
+    assert info.engine == tccl.tcclEngineWarp
+
+
+def test_out_of_place_allreduce_over_8_ranks_takes_the_vec_engine():
+    # at P = 8 an out-of-place allreduce goes to the vec engine at every small size;
+    # in place, other collectives, other rank counts and an explicit threshold keep the warp engine
+    for kib in (1, 4, 16, 64):
+        r, _, _, info = inspect(AR, 8, kib * 512, tccl.tcclBfloat16, *bufs(8, 0, 0))
+        assert r == 0 and info.engine == tccl.tcclEngineVec, kib
+        r, _, _, info = inspect(AR, 8, kib * 512, tccl.tcclBfloat16, *bufs(8, 0, 0, in_place=True))
+        assert r == 0 and info.engine == tccl.tcclEngineWarp, kib
+    r, _, _, info = inspect(AR, 7, 8192, tccl.tcclBfloat16, *bufs(7, 0, 0))
+    assert info.engine == tccl.tcclEngineWarp
+    r, _, _, info = inspect(RS, 8, 1024, tccl.tcclBfloat16, *bufs(8, 0, 0))
+    assert info.engine == tccl.tcclEngineWarp
+    r, _, _, info = inspect(AR, 8, 8192, tccl.tcclBfloat16, *bufs(8, 0, 0), small_max_bytes=64 << 10)
     assert info.engine == tccl.tcclEngineWarp
 
 
