@@ -114,6 +114,23 @@ def test_allreduce_misaligned_buffers(groups, engine, offs):
     assert_ranks_equal(got, exp, f"misaligned {offs}")
 
 
+@pytest.mark.parametrize("p", [4, 8])
+@pytest.mark.parametrize("kib", [1, 16, 64])
+def test_auto_small_engine_by_placement(groups, p, kib):
+    """Under Auto a small out-of-place allreduce over 8 ranks runs on the vec
+    engine and an in-place one on the warp engine; over 4 ranks both take the
+    warp engine. Every result matches the oracle."""
+    g = groups(p)
+    reset_config(g)
+    n = kib * 512  # bf16 elements
+    xs = inputs("bf16", p, n, seed=kib + p)
+    exp = oracle.allreduce(xs, "bf16", "sum")
+    assert_ranks_equal(run_allreduce(g, xs, "bf16", "sum"), exp, f"out of place P={p} {kib} KiB")
+    assert g.last_launch()["engine"] == (tccl.tcclEngineVec if p == 8 else tccl.tcclEngineWarp)
+    assert_ranks_equal(run_allreduce(g, xs, "bf16", "sum", in_place=True), exp, f"in place P={p} {kib} KiB")
+    assert g.last_launch()["engine"] == tccl.tcclEngineWarp
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("lanes_per_sm", [1, 27, 191, 192, 193, 300])
 def test_vec_engine_grid_shapes(groups, dtype, lanes_per_sm):
