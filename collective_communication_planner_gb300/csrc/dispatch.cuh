@@ -75,7 +75,10 @@ int launch_bulk_t(const BulkArgs& a, const LaunchShape& s, cudaStream_t st) {
 
 template <int C, int D, int O, int MAXR, int MAXW, bool SHFL>
 int launch_small_np(const SmallArgs<MAXR, MAXW>& a, const LaunchShape& s, cudaStream_t st) {
-  // rank counts up to 8 compiled in (small tables only)
+  // rank counts up to 8 compiled in (small tables), and 16 (large tables:
+  // graph-captured on GB300, P = 16 at 16-512 KiB per rank, the vec engine
+  // went from 4.2-5.1 to 2.2-3.3 us and the warp engine from 2.7-12 to
+  // 2.2-10 us)
   if constexpr (MAXR == kSmallRanks) {
     switch (a.nranks) {
       case 2: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 2>, a, s, st);
@@ -87,6 +90,9 @@ int launch_small_np(const SmallArgs<MAXR, MAXW>& a, const LaunchShape& s, cudaSt
       case 8: return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 8>, a, s, st);
       default: break;
     }
+  }
+  if constexpr (MAXR != kSmallRanks) {
+    if (a.nranks == 16) return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 16>, a, s, st);
   }
   return launch_maybe_early(small_kernel<C, D, O, MAXR, MAXW, SHFL, 0>, a, s, st);
 }

@@ -1124,7 +1124,7 @@ __device__ __forceinline__ int find_window(const uint64_t* prefix, int nwin, uin
   return lo;
 }
 
-// NP: the rank count fixed at compile time (2 to 8; 0: a.nranks). The warp engine's
+// NP: the rank count fixed at compile time (2 to 8 or 16; 0: a.nranks). The warp engine's
 // lane groups then need no run-time division, and both engines' folds (and the
 // vec engine's P stores) are unrolled.
 template <int COLL, int DT, int OP, int MAXR, int MAXW, bool SHFL, int NP>

@@ -93,7 +93,7 @@ def test_allreduce_engines_dtypes_ops(groups, engine, dtype, op):
 @pytest.mark.parametrize("engine", ["bulk", "warp", "vec"])
 @pytest.mark.parametrize("n", [1, 2, 3, 7, 8, 9, 15, 16, 17, 63, 64, 65, 4095, 4096, 4097])
 def test_allreduce_small_and_ragged_counts(groups, engine, n):
-    for p in (1, 2, 8):
+    for p in (1, 2, 8, 16):
         g = groups(p)
         configure(g, engine)
         xs = inputs("bf16", p, n, seed=n)
