@@ -140,7 +140,8 @@ uint64_t small_max_bytes(const Config& c, int nranks) {
   // compiled in): from P = 5 to 8 the vec engine is about as fast at 64 KiB per
   // rank and faster above (P = 8, 128 KiB: 1.6-1.8 against 2.2 us; P = 6:
   // 1.65 against 1.97); at P = 3 and 4 the two tie up to 128 KiB; at P = 16
-  // the warp engine is faster up to 96 KiB only.
+  // they tie at 16 KiB and the vec engine is faster from 64 KiB (2.4 against
+  // 2.7 us).
   if (c.small_max_bytes) return c.small_max_bytes;
   return nranks >= 5 ? 64 * 1024 : 128 * 1024;
 }
